@@ -1,0 +1,166 @@
+"""CPU oracle for the DeepSeek V4.1 Indexer -> top-k -> sparse sink attention path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference legs of ``bench.py`` may import this package; the product package never does.
+
+The arithmetic lives in ``oracle.c`` (plain C, double accumulation); this module only
+builds it with gcc, loads it with ctypes and marshals numpy arrays.  bf16 tensors are
+numpy ``uint16`` arrays holding the bf16 bit patterns.
+
+Every function is pinned by the CPU tests in ``tests/test_oracle_*.py``:
+  window_topk_idxs   worked rows of get_window_topk_idxs (tests/golden/window_idx.txt)
+  visible / compress_len   closed forms and the worked Indexer rows (golden)
+  index_score        one-hot closed forms, rank-one identity, head additivity, relu cut-off
+  topk               numpy lexsort reference, subset brute force, vis <= k layout
+  sparse_attn        textbook softmax (sink -> -inf), single-row closed form, empty rows,
+                     duplicate-row sink shift, permutation invariance, mass + sink = 1
+  dense_attn         independent of index lists; equal to sparse_attn when k >= visible
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (portable flags, no -march)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_window_topk_idxs.argtypes = [I, I, I, I, P]
+        lib.oracle_window_topk_idxs.restype = I
+        lib.oracle_compress_len.argtypes = [I, I, I]
+        lib.oracle_compress_len.restype = I
+        lib.oracle_visible.argtypes = [I, I, I]
+        lib.oracle_visible.restype = I
+        lib.oracle_index_score.argtypes = [P, P, I64, P, D, P, I, I, I, I, I, I, P, I]
+        lib.oracle_index_score.restype = None
+        lib.oracle_topk.argtypes = [P, P, I, I, I, I, I, ctypes.c_int32, P, I]
+        lib.oracle_topk.restype = None
+        lib.oracle_sparse_attn.argtypes = [P, P, I64, P, I64, I, I, P, P, D, I, I, I, I, I, P, P, I]
+        lib.oracle_sparse_attn.restype = None
+        lib.oracle_dense_attn.argtypes = [P, P, I64, P, I64, P, P, D, I, I, I, I, I, I, P, I]
+        lib.oracle_dense_attn.restype = None
+        _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def window_topk_idxs(window_size: int, bsz: int, seqlen: int, start_pos: int) -> np.ndarray:
+    """get_window_topk_idxs: [bsz, seqlen, min(seqlen, W)] in prefill, [bsz, 1, W] in decode."""
+    lib = _load()
+    if start_pos == 0:
+        rows, width = seqlen, min(seqlen, window_size)
+    else:
+        rows, width = 1, window_size
+    out = np.empty((bsz, rows, width), dtype=np.int32)
+    got = lib.oracle_window_topk_idxs(window_size, bsz, seqlen, start_pos, _ptr(out))
+    assert got == width
+    return out
+
+
+def compress_len(start_pos: int, seqlen: int, ratio: int) -> int:
+    return int(_load().oracle_compress_len(start_pos, seqlen, ratio))
+
+
+def visible(start_pos: int, t: int, ratio: int) -> int:
+    return int(_load().oracle_visible(start_pos, t, ratio))
+
+
+def index_score(iq, ik, w, c: float, start_pos, n_cols: int, ratio: int, threads: int | None = None) -> np.ndarray:
+    """Scores [b, s, n_cols] (float64, -inf where not visible).
+
+    iq: [b, s, H, D] bf16 bits; ik: [b, >= n_cols, D] bf16 bits; w: [b, s, H] bf16 bits."""
+    iq = _c(iq, np.uint16)
+    ik = _c(ik, np.uint16)
+    w = _c(w, np.uint16)
+    sp = _c(start_pos, np.int32)
+    b, s, H, D = iq.shape
+    assert ik.shape[0] == b and ik.shape[2] == D and ik.shape[1] >= n_cols
+    assert w.shape == (b, s, H) and sp.shape == (b,)
+    out = np.empty((b, s, n_cols), dtype=np.float64)
+    _load().oracle_index_score(
+        _ptr(iq), _ptr(ik), ik.shape[1] * D, _ptr(w), float(c), _ptr(sp), b, s, H, D, n_cols, ratio, _ptr(out),
+        threads or default_threads(),
+    )
+    return out
+
+
+def topk(score, start_pos, ratio: int, k: int, offset: int, threads: int | None = None) -> np.ndarray:
+    """Top-k positions per row: [b, s, k] int32, ascending, +offset, -1 padded."""
+    score = _c(score, np.float64)
+    sp = _c(start_pos, np.int32)
+    b, s, n_cols = score.shape
+    out = np.empty((b, s, k), dtype=np.int32)
+    _load().oracle_topk(_ptr(score), _ptr(sp), b, s, n_cols, ratio, k, offset, _ptr(out), threads or default_threads())
+    return out
+
+
+def sparse_attn(q, kv1, sink, idx, scale: float, kv2=None, threads: int | None = None):
+    """Sparse attention with sink; returns (out [b,s,h,d] float64, lse [b,s,h] float64).
+
+    q: [b, s, h, d] bf16 bits; kv1: [b, n1, d]; kv2: optional [b, n2, d] (row r >= n1 of the
+    concatenated KV is kv2[r - n1]); sink: [h] float32; idx: [b, s, k] int32."""
+    q = _c(q, np.uint16)
+    kv1 = _c(kv1, np.uint16)
+    kv2 = None if kv2 is None else _c(kv2, np.uint16)
+    sink = _c(sink, np.float32)
+    idx = _c(idx, np.int32)
+    b, s, h, d = q.shape
+    k = idx.shape[2]
+    n1 = kv1.shape[1]
+    n2 = 0 if kv2 is None else kv2.shape[1]
+    out = np.empty((b, s, h, d), dtype=np.float64)
+    lse = np.empty((b, s, h), dtype=np.float64)
+    _load().oracle_sparse_attn(
+        _ptr(q), _ptr(kv1), n1 * d, _ptr(kv2), n2 * d, n1, n2, _ptr(sink), _ptr(idx), float(scale), b, s, h, d, k,
+        _ptr(out), _ptr(lse), threads or default_threads(),
+    )
+    return out, lse
+
+
+def dense_attn(q, win, comp, start_pos, sink, scale: float, window_size: int, ratio: int, threads: int | None = None):
+    """Dense causal window + visible compressed attention with sink (no index lists)."""
+    q = _c(q, np.uint16)
+    win = _c(win, np.uint16)
+    comp = _c(comp, np.uint16)
+    sp = _c(start_pos, np.int32)
+    sink = _c(sink, np.float32)
+    b, s, h, d = q.shape
+    out = np.empty((b, s, h, d), dtype=np.float64)
+    _load().oracle_dense_attn(
+        _ptr(q), _ptr(win), win.shape[1] * d, _ptr(comp), comp.shape[1] * d, _ptr(sp), _ptr(sink), float(scale),
+        b, s, h, d, window_size, ratio, _ptr(out), threads or default_threads(),
+    )
+    return out

@@ -1,0 +1,383 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Each test checks an oracle function against something other than itself: hand-worked rows
+of the page's definitions (tests/golden), closed forms, a textbook/library computation, or
+brute force, chosen so a dropped term, a wrong sign or index, or a transposed operand fails.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+from workloads import bf16_bits_to_f32, index_lists, rng_for, to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(spec):
+    return [[int(v) for v in r.split()] for r in spec.split(";")]
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ----------------------------------------------------------------- window indices
+
+
+def test_window_idx_golden(orc):
+    for ln in _golden_lines("window_idx.txt"):
+        head, rows = ln.split("|")
+        W, s, sp = (int(v) for v in head.split())
+        want = np.array(_rows(rows), dtype=np.int32)
+        got = orc.window_topk_idxs(W, 2, s, sp)
+        assert got.shape == (2,) + want.shape
+        np.testing.assert_array_equal(got[0], want)
+        np.testing.assert_array_equal(got[1], want)
+
+
+@pytest.mark.parametrize("W,s", [(1, 1), (4, 9), (16, 256), (128, 300), (7, 7)])
+def test_window_idx_prefill_positions(orc, W, s):
+    got = orc.window_topk_idxs(W, 1, s, 0)[0]
+    assert got.shape == (s, min(s, W))
+    for t in range(s):
+        valid = sorted(int(v) for v in got[t] if v >= 0)
+        assert valid == list(range(max(0, t - W + 1), t + 1))
+
+
+@pytest.mark.parametrize("W", [1, 4, 16, 128])
+def test_window_idx_decode_ring(orc, W):
+    for sp in list(range(1, 3 * W)) + [65535, 131071]:
+        got = orc.window_topk_idxs(W, 1, 1, sp)[0, 0]
+        assert got.shape == (W,)
+        valid = [int(v) for v in got if v >= 0]
+        positions = list(range(max(0, sp - W + 1), sp + 1))
+        # slots listed oldest first: slot of each held position, in increasing position order
+        assert valid == [p % W for p in positions]
+
+
+# ----------------------------------------------------------------- lengths
+
+
+def test_compress_len_and_visible_closed_forms(orc):
+    for sp in [0, 1, 3, 4, 5, 127, 65535]:
+        for s in [1, 2, 7, 64]:
+            for r in [1, 2, 4]:
+                assert orc.compress_len(sp, s, r) == (sp + s) // r
+                for t in range(s):
+                    # group j sits at position j*r and becomes visible once (j+1)*r <= p+1
+                    brute = sum(1 for j in range(0, (sp + s) // r + 2) if (j + 1) * r <= sp + t + 1)
+                    assert orc.visible(sp, t, r) == brute
+    # the last query of a chunk sees exactly compress_len groups
+    for sp, s, r in [(0, 8, 4), (9, 1, 4), (65535, 1, 4), (100, 13, 2)]:
+        assert orc.visible(sp, s - 1, r) == orc.compress_len(sp, s, r)
+
+
+# ----------------------------------------------------------------- top-k
+
+
+def test_indexer_rows_golden(orc):
+    for ln in _golden_lines("indexer_rows.txt"):
+        head, scores, rows = ln.split("|")
+        s, sp, r, k, off = (int(v) for v in head.split())
+        vals = np.array([float(v) for v in scores.split()], dtype=np.float64)
+        n_cols = (sp + s) // r
+        assert vals.size == n_cols
+        score = np.tile(vals, (1, s, 1))
+        want = np.array(_rows(rows), dtype=np.int32).reshape(1, s, k)
+        got = orc.topk(score, np.array([sp], np.int32), r, k, off)
+        np.testing.assert_array_equal(got, want)
+
+
+def _topk_numpy(row, vis, k, offset):
+    """Independent restatement: lexsort by (-score, position), keep min(k, vis), ascending."""
+    pos = np.arange(vis)
+    order = np.lexsort((pos, -row[:vis]))
+    m = min(k, vis)
+    sel = np.sort(pos[order[:m]])
+    return np.concatenate([sel + offset, np.full(k - m, -1)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("n_cols,k,sp,s", [(300, 16, 0, 1300), (2048, 512, 65535 - 2047 * 4, 1), (97, 100, 600, 1)])
+def test_topk_matches_lexsort(orc, n_cols, k, sp, s):
+    rng = rng_for(7, n_cols)
+    s_eff = min(s, 40)
+    score = rng.standard_normal((2, s_eff, n_cols))
+    spv = np.array([sp, sp + 4], np.int32)
+    got = orc.topk(score, spv, 4, k, 128)
+    for bi in range(2):
+        for t in range(s_eff):
+            vis = min((int(spv[bi]) + t + 1) // 4, n_cols)
+            np.testing.assert_array_equal(got[bi, t], _topk_numpy(score[bi, t], vis, k, 128))
+
+
+def test_topk_brute_force_subsets(orc):
+    rng = rng_for(11, 0)
+    for trial in range(30):
+        n = int(rng.integers(1, 9))
+        k = int(rng.integers(1, 6))
+        row = rng.standard_normal(n)
+        got = orc.topk(row.reshape(1, 1, n), np.array([n * 2 - 1], np.int32), 2, k, 0)[0, 0]
+        m = min(k, n)
+        best = max(itertools.combinations(range(n), m), key=lambda c: sum(row[list(c)]))
+        assert list(got[:m]) == sorted(best)
+        assert all(v == -1 for v in got[m:])
+
+
+def test_topk_ties_prefer_lower_position(orc):
+    row = np.array([1.0, 3.0, 2.0, 3.0, 2.0, 2.0])
+    got = orc.topk(row.reshape(1, 1, 6), np.array([23], np.int32), 4, 3, 0)[0, 0]
+    np.testing.assert_array_equal(got, [1, 2, 3])
+
+
+def test_topk_all_visible_when_k_exceeds(orc):
+    rng = rng_for(12, 0)
+    score = rng.standard_normal((1, 1, 50))
+    got = orc.topk(score, np.array([4 * 30 - 1], np.int32), 4, 40, 7)[0, 0]
+    np.testing.assert_array_equal(got, np.concatenate([np.arange(30) + 7, np.full(10, -1)]))
+
+
+# ----------------------------------------------------------------- index scores
+
+
+def _f(bits):
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def test_index_score_hand_values(orc):
+    q = to_bf16_bits(np.array([[[[1, 2], [-1, 1]]]], np.float32))          # [1,1,2,2]
+    k = to_bf16_bits(np.array([[[1, 0], [0, 1], [1, 1], [-2, 1]]], np.float32))
+    w = to_bf16_bits(np.array([[[0.5, 2.0]]], np.float32))
+    for ln in _golden_lines("index_score_hand.txt"):
+        head, vals = ln.split("|")
+        sp, r = (int(v) for v in head.split())
+        want = np.array([-np.inf if v == "-inf" else float(v) for v in vals.split()])
+        got = orc.index_score(q, k, w, 1.0, np.array([sp], np.int32), 4, r)[0, 0]
+        np.testing.assert_array_equal(got, want)
+
+
+def _rand_index_inputs(seed, b=2, s=3, H=4, D=32, n=70):
+    rng = rng_for(seed, 0)
+    iq = to_bf16_bits(rng.standard_normal((b, s, H, D)))
+    ik = to_bf16_bits(rng.standard_normal((b, n, D)))
+    w = to_bf16_bits(rng.standard_normal((b, s, H)))
+    return iq, ik, w
+
+
+def test_index_score_relu_identity(orc):
+    """relu(x) - relu(-x) = x, so S(q) - S(-q) = c * sum_h w_h q_h . k (a plain matmul)."""
+    iq, ik, w = _rand_index_inputs(21)
+    neg = iq ^ np.uint16(0x8000)
+    sp = np.array([400, 400], np.int32)
+    c = 0.37
+    a = orc.index_score(iq, ik, w, c, sp, 70, 4)
+    bneg = orc.index_score(neg, ik, w, c, sp, 70, 4)
+    lin = c * np.einsum("bsh,bshd,bnd->bsn", _f(w), _f(iq), _f(ik))
+    np.testing.assert_allclose(a - bneg, lin, rtol=1e-12, atol=1e-12)
+    # and relu really cuts: the two are not equal to +-lin individually
+    assert np.abs(a - lin).max() > 1e-3
+
+
+def test_index_score_rank_one_when_all_positive(orc):
+    """All dots positive -> S = c * (sum_h w_h q_h) . k_j."""
+    rng = rng_for(22, 0)
+    iq = to_bf16_bits(np.abs(rng.standard_normal((1, 2, 3, 16))))
+    ik = to_bf16_bits(np.abs(rng.standard_normal((1, 40, 16))))
+    w = to_bf16_bits(rng.standard_normal((1, 2, 3)))
+    got = orc.index_score(iq, ik, w, 0.5, np.array([1000], np.int32), 40, 4)
+    u = (_f(w)[..., None] * _f(iq)).sum(2)                    # [1,2,16]
+    want = 0.5 * u @ _f(ik)[0].T
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_index_score_head_additivity(orc):
+    """Splitting heads into two groups (zeroed weights) sums back to the full score:
+    the partial-head sums a head-sharded run would all-reduce."""
+    iq, ik, w = _rand_index_inputs(23)
+    sp = np.array([299, 311], np.int32)
+    wf = _f(w)
+    mask = np.zeros(4)
+    mask[[0, 2]] = 1
+    wa = to_bf16_bits(wf * mask)
+    wb = to_bf16_bits(wf * (1 - mask))
+    full = orc.index_score(iq, ik, w, 0.1, sp, 70, 4)
+    part = orc.index_score(iq, ik, wa, 0.1, sp, 70, 4) + orc.index_score(iq, ik, wb, 0.1, sp, 70, 4)
+    np.testing.assert_allclose(full, part, rtol=1e-12, atol=1e-12)
+
+
+def test_index_score_batches_and_mask(orc):
+    iq, ik, w = _rand_index_inputs(24)
+    sp = np.array([7, 150], np.int32)         # batch 0 sees (7+t+1)//4 = 2..2 columns, batch 1 37..38
+    a = orc.index_score(iq, ik, w, 1.0, sp, 70, 4)
+    for bi in range(2):
+        for t in range(3):
+            vis = (int(sp[bi]) + t + 1) // 4
+            assert np.all(np.isfinite(a[bi, t, :vis]))
+            assert np.all(a[bi, t, vis:] == -np.inf)
+    ik2 = ik.copy()
+    ik2[1] = to_bf16_bits(rng_for(25, 0).standard_normal(ik[1].shape))
+    b2 = orc.index_score(iq, ik2, w, 1.0, sp, 70, 4)
+    np.testing.assert_array_equal(a[0], b2[0])
+    assert not np.array_equal(a[1], b2[1])
+    # scale c multiplies every visible entry
+    c2 = orc.index_score(iq, ik, w, 2.0, sp, 70, 4)
+    fin = np.isfinite(a)
+    np.testing.assert_allclose(c2[fin], 2 * a[fin], rtol=1e-15)
+
+
+# ----------------------------------------------------------------- sparse attention
+
+
+def _attn_inputs(seed, b=2, s=2, h=3, d=16, n1=12, n2=20):
+    rng = rng_for(seed, 0)
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    return q, kv1, kv2, sink
+
+
+def _softmax_attn_numpy(qf, rows, scale):
+    """Textbook softmax attention of one query head over the given rows."""
+    from scipy.special import softmax
+
+    p = softmax(scale * rows @ qf)
+    return p @ rows
+
+
+def test_attn_textbook_when_sink_vanishes(orc):
+    q, kv1, kv2, _ = _attn_inputs(31)
+    sink = np.full(3, -1e30, np.float32)
+    idx = index_lists(rng_for(31, 1), 2, 2, 9, 32, masked_frac=0.2)
+    out, _ = orc.sparse_attn(q, kv1, sink, idx, 0.25, kv2=kv2)
+    allkv = np.concatenate([_f(kv1), _f(kv2)], axis=1)
+    for bi in range(2):
+        for t in range(2):
+            rows = allkv[bi, [i for i in idx[bi, t] if i >= 0]]
+            for hh in range(3):
+                want = _softmax_attn_numpy(_f(q)[bi, t, hh], rows, 0.25)
+                np.testing.assert_allclose(out[bi, t, hh], want, rtol=1e-12, atol=1e-12)
+
+
+def test_attn_single_row_closed_form(orc):
+    q, kv1, _, sink = _attn_inputs(32, b=1, s=1)
+    idx = np.full((1, 1, 5), -1, np.int32)
+    idx[0, 0, 3] = 7
+    out, lse = orc.sparse_attn(q, kv1, sink, idx, 0.3)
+    v = _f(kv1)[0, 7]
+    for hh in range(3):
+        sc = 0.3 * float(_f(q)[0, 0, hh] @ v)
+        want = v / (1.0 + math.exp(float(sink[hh]) - sc))
+        np.testing.assert_allclose(out[0, 0, hh], want, rtol=1e-13, atol=1e-13)
+        assert lse[0, 0, hh] == pytest.approx(math.log(math.exp(sc) + math.exp(float(sink[hh]))), rel=1e-13)
+
+
+def test_attn_empty_rows_are_zero(orc):
+    q, kv1, kv2, sink = _attn_inputs(33)
+    idx = np.full((2, 2, 6), -1, np.int32)
+    idx[1, 1, 0] = 3
+    out, lse = orc.sparse_attn(q, kv1, sink, idx, 0.25, kv2=kv2)
+    assert np.all(out[0] == 0) and np.all(out[1, 0] == 0)
+    assert np.all(lse[0] == -np.inf)
+    assert np.any(out[1, 1] != 0)
+
+
+def test_attn_mass_plus_sink_is_one(orc):
+    q, kv1, kv2, sink = _attn_inputs(34)
+    idx = index_lists(rng_for(34, 1), 2, 2, 11, 32, masked_frac=0.3)
+    _, lse = orc.sparse_attn(q, kv1, sink, idx, 0.25, kv2=kv2)
+    allkv = np.concatenate([_f(kv1), _f(kv2)], axis=1)
+    for bi in range(2):
+        for t in range(2):
+            rows = allkv[bi, [i for i in idx[bi, t] if i >= 0]]
+            for hh in range(3):
+                s_i = 0.25 * rows @ _f(q)[bi, t, hh]
+                total = np.exp(s_i - lse[bi, t, hh]).sum() + math.exp(float(sink[hh]) - lse[bi, t, hh])
+                assert total == pytest.approx(1.0, abs=1e-12)
+
+
+def test_attn_slot_order_masked_and_duplicates(orc):
+    q, kv1, kv2, sink = _attn_inputs(35)
+    idx = index_lists(rng_for(35, 1), 2, 2, 8, 32, masked_frac=0.25)
+    base, _ = orc.sparse_attn(q, kv1, sink, idx, 0.25, kv2=kv2)
+    perm = idx[..., rng_for(35, 2).permutation(8)]
+    out_p, _ = orc.sparse_attn(q, kv1, sink, perm, 0.25, kv2=kv2)
+    np.testing.assert_allclose(out_p, base, rtol=1e-13, atol=1e-13)
+    padded = np.concatenate([idx, np.full((2, 2, 5), -1, np.int32)], axis=-1)
+    out_m, _ = orc.sparse_attn(q, kv1, sink, padded, 0.25, kv2=kv2)
+    np.testing.assert_allclose(out_m, base, rtol=1e-13, atol=1e-13)
+    # a slot listed twice counts twice: same as listing it once with the sink lowered by ln 2
+    one = np.array([[[5, -1]]], np.int32)
+    two = np.array([[[5, 5]]], np.int32)
+    o1, _ = orc.sparse_attn(q[:1, :1], kv1[:1], (sink - np.float32(math.log(2))).astype(np.float32), one, 0.25)
+    o2, _ = orc.sparse_attn(q[:1, :1], kv1[:1], sink, two, 0.25)
+    np.testing.assert_allclose(o2, o1, rtol=1e-6, atol=1e-7)   # float32 sink shift
+
+
+def test_attn_two_sources_equal_concatenation(orc):
+    q, kv1, kv2, sink = _attn_inputs(36)
+    idx = index_lists(rng_for(36, 1), 2, 2, 10, 32, masked_frac=0.1)
+    a, la = orc.sparse_attn(q, kv1, sink, idx, 0.25, kv2=kv2)
+    cat = np.concatenate([kv1, kv2], axis=1)
+    b, lb = orc.sparse_attn(q, cat, sink, idx, 0.25)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
+    # indices past the end of both sources hold nothing (treated as masked)
+    bad = idx.copy()
+    bad[0, 0, 0] = 32 + 5
+    c, _ = orc.sparse_attn(q, kv1, sink, bad, 0.25, kv2=kv2)
+    ref = idx.copy()
+    ref[0, 0, 0] = -1
+    d, _ = orc.sparse_attn(q, kv1, sink, ref, 0.25, kv2=kv2)
+    np.testing.assert_array_equal(c, d)
+
+
+# ----------------------------------------------------------------- dense reference
+
+
+def test_dense_is_textbook_causal_window(orc):
+    """Prefill with ratio > s: no compressed group visible -> causal sliding-window softmax + sink."""
+    rng = rng_for(41, 0)
+    s, h, d, W = 9, 2, 8, 4
+    q = to_bf16_bits(rng.standard_normal((1, s, h, d)))
+    win = to_bf16_bits(rng.standard_normal((1, s, d)))
+    comp = to_bf16_bits(rng.standard_normal((1, 1, d)))
+    sink = np.full(h, -1e30, np.float32)
+    out = orc.dense_attn(q, win, comp, np.zeros(1, np.int32), sink, 0.5, W, 100)
+    for t in range(s):
+        rows = _f(win)[0, max(0, t - W + 1): t + 1]
+        for hh in range(h):
+            np.testing.assert_allclose(out[0, t, hh], _softmax_attn_numpy(_f(q)[0, t, hh], rows, 0.5), rtol=1e-12)
+
+
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_sparse_equals_dense_when_topk_covers(orc, mode):
+    """index_topk >= visible count: window indices + Indexer rows select everything the
+    position-defined dense attention sees, so the two must agree."""
+    rng = rng_for(42, 0 if mode == "prefill" else 1)
+    h, d, W, r, Hi, Di = 3, 16, 8, 4, 2, 8
+    if mode == "prefill":
+        b, s, sp = 1, 37, np.zeros(1, np.int32)
+        n_win_rows = s
+    else:
+        b, s, sp = 3, 1, np.array([5, 8, 61], np.int32)
+        n_win_rows = W
+    n_cols = int((sp.max() + s) // r)
+    K = n_cols + 3
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    win = to_bf16_bits(rng.standard_normal((b, n_win_rows, d)))
+    comp = to_bf16_bits(rng.standard_normal((b, n_cols, d)))
+    iq = to_bf16_bits(rng.standard_normal((b, s, Hi, Di)))
+    ik = to_bf16_bits(rng.standard_normal((b, n_cols, Di)))
+    w = to_bf16_bits(rng.standard_normal((b, s, Hi)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    score = orc.index_score(iq, ik, w, 1.0, sp, n_cols, r)
+    comp_idx = orc.topk(score, sp, r, K, n_win_rows)
+    win_idx = np.concatenate([orc.window_topk_idxs(W, 1, s, int(sp[bi])) for bi in range(b)], axis=0)
+    idx = np.concatenate([win_idx, comp_idx], axis=-1)
+    sparse, _ = orc.sparse_attn(q, win, sink, idx, d ** -0.5, kv2=comp)
+    dense = orc.dense_attn(q, win, comp, sp, sink, d ** -0.5, W, r)
+    np.testing.assert_allclose(sparse, dense, rtol=1e-12, atol=1e-12)
