@@ -1,0 +1,202 @@
+/*
+ * sti.h -- C ABI of the GB300 (sm_103a) library for the DeepSeek V4.1 attention hot path:
+ * the Indexer's scores, their top-k, the sliding-window indices, and sparse attention with
+ * an attention sink over the selected rows of one shared latent KV.
+ *
+ * Sources: the "DeepSeek V4.1" model pages -- attention "attend/selected" (prefill) and
+ * "attend/allowed" (decode): get_window_topk_idxs, Indexer.forward, sparse_attn_kernel,
+ * sparse_attn, Attention.forward; "reindex-layer/read-weights" (decode):
+ * Attention._compress_kv and Attention._compress_topk_idxs.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates or frees device memory, never synchronises (except sti_read_device_status),
+ *    and enqueues its kernels on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - bf16 tensors are passed as uint16_t bit patterns (IEEE bfloat16); float is fp32.
+ *  - Layouts are row-major and contiguous unless a stride argument says otherwise; strides
+ *    are in ELEMENTS.
+ *  - Arguments the host can check (null pointers, shapes, supported sizes, alignment,
+ *    workspace size) are checked before anything is enqueued; a failed check returns
+ *    STI_ERR_INVALID_ARG or STI_ERR_UNSUPPORTED and enqueues nothing.
+ *  - Conditions only the device sees (an index out of range, a bounded wait that timed out,
+ *    start_pos != 0 with seqlen > 1) set bits in the workspace's status word; the call still
+ *    completes (bad indices are treated as masked).  sti_read_device_status reports them.
+ *  - `ws` is a caller-owned device workspace of at least the size the matching
+ *    sti_*_workspace_size() returns, aligned to 256 bytes.  Its first 4 bytes (the status
+ *    word) must be zero before the first call; sti_read_device_status clears them again.
+ *    Calls that share one workspace must not overlap on the device.
+ *  - Returns STI_ERR_CUDA if a launch fails (the CUDA error is in sti_last_cuda_error()).
+ */
+#ifndef STI_H_
+#define STI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sti_status {
+    STI_OK = 0,
+    STI_ERR_INVALID_ARG = 1,       /* null pointer, bad shape or stride, workspace too small */
+    STI_ERR_UNSUPPORTED = 2,       /* a size this build does not handle (see each call) */
+    STI_ERR_CUDA = 3,              /* a CUDA runtime/driver call failed */
+    STI_ERR_INDEX_RANGE = 4,       /* device: an index was < -1 or >= the number of KV rows */
+    STI_ERR_DEVICE_TIMEOUT = 5,    /* device: a bounded wait inside a kernel gave up */
+    STI_ERR_DEVICE_UNSUPPORTED = 6 /* device: start_pos != 0 with seqlen > 1 (chunked prefill) */
+} sti_status;
+
+/* Bits of the device status word (first 4 bytes of every workspace). */
+#define STI_FLAG_INDEX_RANGE 1u
+#define STI_FLAG_TIMEOUT 2u
+#define STI_FLAG_CHUNKED 4u
+
+typedef void *sti_stream; /* cudaStream_t */
+
+/* Human-readable name of a status code (static storage). */
+const char *sti_status_string(sti_status s);
+
+/* Text of this thread's last CUDA failure seen by the library (thread-local storage). */
+const char *sti_last_cuda_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int sti_version(void);
+
+/*
+ * Synchronises `stream`, reads the device status word of `ws` (STI_FLAG_* bits) into
+ * *flags (may be NULL), clears it, and returns STI_OK when no bit was set, else the
+ * status of the most severe bit (TIMEOUT > INDEX_RANGE > DEVICE_UNSUPPORTED).
+ */
+sti_status sti_read_device_status(void *ws, uint32_t *flags, sti_stream stream);
+
+/* ------------------------------------------------------------------ window indices */
+/*
+ * get_window_topk_idxs (attend/selected page): which window-KV rows each query sees.
+ *   seqlen > 1 (prefill, start_pos[b] must be 0): row t holds max(0,t-W+1)+i for
+ *       i < width = min(seqlen, W); entries > t are -1.  The window KV source is then the
+ *       seqlen raw KV rows of the chunk.  (start_pos != 0 raises STI_FLAG_CHUNKED when ws
+ *       is given and writes -1 rows.)
+ *   seqlen == 1 (decode): width = W; the ring slots oldest first,
+ *       (start_pos%W)+1 .. W-1, 0 .. start_pos%W; a slot > start_pos is -1.  Position p
+ *       lives in ring slot p % W.  (For start_pos == 0 this lists the same single slot as
+ *       the page's prefill branch, at another place in the row; slot order does not matter.)
+ * start_pos: int32 [b] device.  idxs: int32, row (b,t) at idxs + (b*seqlen+t)*row_stride,
+ * `width` entries written (row_stride >= width).  The width goes to *width_out (host
+ * pointer, may be NULL).  ws: optional workspace (NULL: no status reporting).
+ */
+sti_status sti_window_idxs(const int32_t *start_pos, int b, int seqlen, int window_size, int32_t *idxs,
+                           int64_t row_stride, int *width_out, void *ws, sti_stream stream);
+
+/* ------------------------------------------------------------------ index scores */
+/*
+ * Indexer.forward (attend/selected page), the score block:
+ *   scores[b,t,j] = c * sum_h w[b,t,h] * relu( sum_e iq[b,t,h,e] * ik[b,j,e] )   j < vis(b,t)
+ *                 = -inf                                                         otherwise
+ *   vis(b,t) = min(n_cols, (start_pos[b] + t + 1) // ratio)   (group j is visible once the
+ *   query passed its last token; prefill compress_lens[t] = (t+1)//ratio, decode
+ *   end_pos//ratio).  c = index_head_dim^-0.5 * index_n_heads^-0.5 (passed in).
+ * Tensor-core (tcgen05) GEMM over bf16 inputs with fp32 accumulation; scores are fp32.
+ *   iq: bf16 [b, seqlen, Hi, Di];  w: bf16 [b, seqlen, Hi]
+ *   ik: bf16 [b, *, Di], batch b at ik + b*ik_bstride (ik_bstride >= n_cols*Di, a multiple
+ *       of 8; rows >= n_cols are never read)
+ *   scores: fp32 [b, seqlen, n_cols]
+ * Supported: Di in {32, 64, 128}; Hi in {4, 8, 16, 32, 64}; ratio >= 1; iq and ik 16-byte
+ * aligned.  ws: sti_idx_scores_workspace_size() bytes.
+ */
+size_t sti_idx_scores_workspace_size(void);
+sti_status sti_idx_scores(const uint16_t *iq, const uint16_t *ik, int64_t ik_bstride, const uint16_t *w, float c,
+                          const int32_t *start_pos, int b, int seqlen, int Hi, int Di, int n_cols, int ratio,
+                          float *scores, void *ws, size_t ws_bytes, sti_stream stream);
+
+/* ------------------------------------------------------------------ top-k */
+/*
+ * Indexer.forward (attend/selected page), the selection block:
+ *   topk = min(k, vis(b,t)); the topk largest scores[b,t,j] over j < vis(b,t) (equal scores:
+ *   the lower position first), listed in ascending position order, each plus `offset`;
+ *   the row is padded to width k with -1.  (The page's row width is min(index_topk,
+ *   end_pos//ratio); the extra -1 slots select nothing.)
+ * Radix select on order-preserving keys of the fp32 scores (no sort of the row).
+ *   scores: fp32 [b, seqlen, n_cols];  idxs: int32, row (b,t) at idxs + (b*seqlen+t)*row_stride,
+ *   k entries written (row_stride >= k; pass idxs+width to write after the window indices).
+ * Supported: 1 <= k <= 4096, n_cols >= 0.  ws: sti_idx_topk_workspace_size() bytes.
+ */
+size_t sti_idx_topk_workspace_size(void);
+sti_status sti_idx_topk(const float *scores, const int32_t *start_pos, int b, int seqlen, int n_cols, int ratio,
+                        int k, int32_t offset, int32_t *idxs, int64_t row_stride, void *ws, size_t ws_bytes,
+                        sti_stream stream);
+
+/* ------------------------------------------------------------------ sparse attention */
+/*
+ * sparse_attn / sparse_attn_kernel (attend/selected page) with the two KV sources of
+ * Attention.forward addressed in place (no concatenation copy): KV row r is
+ *   kv[b, r]        for 0 <= r < n1     (window source: the chunk's raw rows, or the ring)
+ *   kv2[b, r - n1]  for n1 <= r < n1+n2 (shared compressed KV; kv2 may be NULL when n2 == 0)
+ * For every query (b,t) and head h, over the slots i with idx[b,t,i] != -1:
+ *   s_i = softmax_scale * q[b,t,h,:] . row_i
+ *   out[b,t,h,:] = sum_i e^{s_i} row_i / (sum_i e^{s_i} + e^{attn_sink[h]})
+ * the same row serving as key and value; a query with no valid slot gets 0.
+ * bf16 inputs, tcgen05 tensor-core MMAs with fp32 accumulation, P rounded to bf16 for the
+ * PV product, fp32 online softmax, bf16 output.
+ *   q: bf16 [b, seqlen, h, d];  out: bf16 [b, seqlen, h, d]
+ *   kv: bf16 batch b at kv + b*kv_bstride, row stride d;  kv2 likewise with kv2_bstride
+ *   attn_sink: fp32 [h];  idxs: int32 [b, seqlen, k] with row stride idx_row_stride (>= k)
+ *   lse: optional fp32 [b, seqlen, h] = ln(sum_i e^{s_i} + e^{sink}); -inf for a query with
+ *        no valid slot; may be NULL.
+ * Indices < -1 or >= n1+n2 are treated as masked and raise STI_FLAG_INDEX_RANGE.
+ * Supported: 1 <= h <= 64, d a multiple of 64 up to 512, k >= 1, kv_bstride/kv2_bstride
+ * multiples of 8.  ws: sti_sparse_attn_workspace_size(b, seqlen, h, d, k) bytes (it holds
+ * split-KV partials when there are few queries; the size depends on the current device's
+ * SM count).
+ */
+size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k);
+sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,
+                                int64_t kv2_bstride, int n1, int n2, const float *attn_sink, const int32_t *idxs,
+                                int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
+                                uint16_t *out, float *lse, void *ws, size_t ws_bytes, sti_stream stream);
+
+/* ------------------------------------------------------------------ fused decode layer */
+/*
+ * One decode step (seqlen == 1) of an index-source attention layer, as
+ * Attention.forward -> _window_kv / _compress_kv -> _compress_topk_idxs -> Indexer ->
+ * sparse_attn composes it, enqueued back to back on one stream:
+ *   1. window indices of the W-slot ring (sti_window_idxs, decode branch) -> topk_idxs[:, :W]
+ *   2. index scores over the n_cols compressed positions (sti_idx_scores) -> workspace
+ *   3. top-k of the visible positions, + offset W (sti_idx_topk) -> topk_idxs[:, W:W+k]
+ *   4. sparse sink attention over [ring ; compressed KV] (sti_sparse_attn_sink)
+ * Ragged batches: start_pos is per sequence, compress_len = (start_pos+1)//ratio.
+ * topk_idxs ([b, W+k] int32) is an output the caller owns, so reuse layers can consume it
+ * through sti_sparse_attn_sink without running the Indexer (_compress_topk_idxs).
+ */
+typedef struct sti_decode_args {
+    /* attention */
+    const uint16_t *q;          /* bf16 [b, h, d] */
+    const uint16_t *window_kv;  /* bf16 ring, batch b at + b*window_bstride, [W, d] */
+    int64_t window_bstride;
+    const uint16_t *comp_kv;    /* bf16 compressed KV, batch b at + b*comp_bstride, [n_cols, d] */
+    int64_t comp_bstride;
+    const float *attn_sink;     /* fp32 [h] */
+    float softmax_scale;
+    int h, d, window_size;
+    /* indexer */
+    const uint16_t *iq;         /* bf16 [b, Hi, Di] */
+    const uint16_t *ik;         /* bf16 index keys, batch b at + b*ik_bstride, [n_cols, Di] */
+    int64_t ik_bstride;
+    const uint16_t *w;          /* bf16 [b, Hi] */
+    float index_scale;          /* c = Di^-0.5 * Hi^-0.5 */
+    int Hi, Di, index_topk, ratio, n_cols;
+    /* batch */
+    const int32_t *start_pos;   /* int32 [b] */
+    int b;
+    /* outputs */
+    uint16_t *out;              /* bf16 [b, h, d] */
+    int32_t *topk_idxs;         /* int32 [b, W + index_topk] */
+} sti_decode_args;
+
+size_t sti_decode_workspace_size(const sti_decode_args *a);
+sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* STI_H_ */

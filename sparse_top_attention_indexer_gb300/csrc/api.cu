@@ -1,0 +1,344 @@
+// api.cu -- the C ABI declared in include/sti.h: argument checks, TMA tensor-map encoding,
+// workspace carving, launch sequencing and device-status reporting.  No allocation, no
+// synchronisation (except sti_read_device_status), no torch types.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "sti.h"
+#include "sti_internal.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+sti_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+    return STI_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map: dims {inner, rows, batch}, strides in bytes for rows and batch.
+sti_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t batch,
+                       uint64_t row_stride_bytes, uint64_t batch_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                       CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled unavailable");
+        return STI_ERR_CUDA;
+    }
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {row_stride_bytes, batch_stride_bytes};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return STI_ERR_CUDA;
+    }
+    return STI_OK;
+}
+
+uint32_t* status_word(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
+
+bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
+    return ws != nullptr && aligned(ws, sti::kWsAlign) && ws_bytes >= need;
+}
+
+}  // namespace
+
+namespace sti {
+int device_num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+}  // namespace sti
+
+// ---------------------------------------------------------------------- shared implementations
+
+static sti_status window_impl(const int32_t* start_pos, int b, int seqlen, int window_size, int32_t* idxs,
+                              int64_t row_stride, int* width_out, uint32_t* status, cudaStream_t st) {
+    if (b < 0 || seqlen < 1 || window_size < 1) return STI_ERR_INVALID_ARG;
+    const int width = seqlen > 1 ? (seqlen < window_size ? seqlen : window_size) : window_size;
+    if (width_out) *width_out = width;
+    if (b == 0) return STI_OK;
+    if (!start_pos || !idxs || row_stride < width) return STI_ERR_INVALID_ARG;
+    cudaError_t e = sti::launch_window_idxs(start_pos, b, seqlen, window_size, width, idxs, row_stride, status, st);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_window_idxs");
+}
+
+static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_t ik_bstride, const uint16_t* w,
+                                  float c, const int32_t* start_pos, int b, int seqlen, int Hi, int Di, int n_cols,
+                                  int ratio, float* scores, uint32_t* status, cudaStream_t st) {
+    if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1) return STI_ERR_INVALID_ARG;
+    if (!(Di == 32 || Di == 64 || Di == 128)) return STI_ERR_UNSUPPORTED;
+    if (!(Hi == 4 || Hi == 8 || Hi == 16 || Hi == 32 || Hi == 64)) return STI_ERR_UNSUPPORTED;
+    if (b == 0 || n_cols == 0) return STI_OK;
+    if (!iq || !ik || !w || !start_pos || !scores) return STI_ERR_INVALID_ARG;
+    if (ik_bstride < (int64_t)n_cols * Di || (ik_bstride % 8) != 0) return STI_ERR_INVALID_ARG;
+    if (!aligned(iq, 16) || !aligned(ik, 16)) return STI_ERR_INVALID_ARG;
+    if ((int64_t)seqlen * Hi > 0x7FFFFFFF || (int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
+
+    sti::IdxScoresParams p{};
+    p.w = w;
+    p.start_pos = start_pos;
+    p.scores = scores;
+    p.status = status;
+    p.c = c;
+    p.B = b;
+    p.s = seqlen;
+    p.Hi = Hi;
+    p.Di = Di;
+    p.n_cols = n_cols;
+    p.ratio = ratio;
+    p.nq = sti::idx_scores_pick_nq(Hi, seqlen);
+    p.QT = (seqlen + p.nq - 1) / p.nq;
+    p.n_pad = ((p.nq * Hi + 15) / 16) * 16;
+    p.n_alloc = ((p.n_pad + 31) / 32) * 32;
+    int cols = 32;
+    while (cols < 2 * p.n_alloc) cols *= 2;
+    p.tmem_cols = cols;
+    p.total_units = b * p.QT;
+    const size_t a_bytes = (size_t)128 * Di * 2, b_bytes = (size_t)p.n_pad * Di * 2;
+    const size_t budget = 200 * 1024;
+    int stages = (int)((budget - b_bytes) / a_bytes);
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    p.stages = stages;
+
+    const uint32_t box_inner = Di >= 64 ? 64u : (uint32_t)Di;
+    const CUtensorMapSwizzle swz = Di >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tm_a, tm_b;
+    sti_status s = make_map_3d(&tm_a, ik, (uint64_t)Di, (uint64_t)n_cols, (uint64_t)b, (uint64_t)Di * 2,
+                               (uint64_t)ik_bstride * 2, box_inner, 128, swz);
+    if (s != STI_OK) return s;
+    s = make_map_3d(&tm_b, iq, (uint64_t)Di, (uint64_t)seqlen * Hi, (uint64_t)b, (uint64_t)Di * 2,
+                    (uint64_t)seqlen * Hi * Di * 2, box_inner, (uint32_t)p.n_pad, swz);
+    if (s != STI_OK) return s;
+    cudaError_t e = sti::launch_idx_scores(tm_a, tm_b, p, sti::device_num_sms(), st);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_idx_scores");
+}
+
+static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b, int seqlen, int n_cols, int ratio,
+                            int k, int32_t offset, int32_t* idxs, int64_t row_stride, uint32_t* status,
+                            cudaStream_t st) {
+    if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1 || k < 1 || row_stride < k) return STI_ERR_INVALID_ARG;
+    if (k > 4096) return STI_ERR_UNSUPPORTED;
+    if ((int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
+    if (b == 0) return STI_OK;
+    if (!start_pos || !idxs || (n_cols > 0 && !scores)) return STI_ERR_INVALID_ARG;
+    cudaError_t e = sti::launch_topk(scores, start_pos, b, seqlen, n_cols, ratio, k, offset, idxs, row_stride,
+                                     status, st);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_idx_topk");
+}
+
+static int attn_splits_for(int n_queries, int k) {
+    const int n_tiles = (k + 127) / 128;
+    const int splits = sti::attn_pick_splits(n_queries, n_tiles, sti::device_num_sms());
+    const int tps = (n_tiles + splits - 1) / splits;
+    return (n_tiles + tps - 1) / tps;   // no empty split
+}
+
+static size_t attn_ws_bytes(int n_queries, int splits, int d) {
+    return sti::kWsStatusBytes + sti::align_up(sti::attn_partials_bytes(n_queries, splits, d), sti::kWsAlign);
+}
+
+static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
+                            int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
+                            int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
+                            uint16_t* out, float* lse, uint8_t* ws, size_t ws_bytes, cudaStream_t st) {
+    if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
+    if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
+    if (b == 0) return STI_OK;
+    if (!q || !attn_sink || !idxs || !out || (n1 > 0 && !kv) || (n2 > 0 && !kv2)) return STI_ERR_INVALID_ARG;
+    if (idx_row_stride < k) return STI_ERR_INVALID_ARG;
+    if ((n1 > 0 && (kv_bstride < (int64_t)n1 * d || kv_bstride % 8)) ||
+        (n2 > 0 && (kv2_bstride < (int64_t)n2 * d || kv2_bstride % 8)))
+        return STI_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || (kv && !aligned(kv, 16)) || (kv2 && !aligned(kv2, 16))) return STI_ERR_INVALID_ARG;
+    if ((int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
+    const int nq = b * seqlen;
+    const int splits = attn_splits_for(nq, k);
+    if (ws_bytes < attn_ws_bytes(nq, splits, d)) return STI_ERR_INVALID_ARG;
+
+    sti::AttnParams p{};
+    p.q = q;
+    p.kv = kv;
+    p.kv2 = kv2;
+    p.sink = attn_sink;
+    p.idx = idxs;
+    p.out = out;
+    p.lse = lse;
+    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.kv_bstride = kv_bstride;
+    p.kv2_bstride = kv2_bstride;
+    p.idx_stride = idx_row_stride;
+    p.scale_log2 = (float)((double)softmax_scale * 1.4426950408889634);
+    p.n1 = n1;
+    p.n2 = n2;
+    p.B = b;
+    p.s = seqlen;
+    p.h = h;
+    p.d = d;
+    p.k = k;
+    p.d_pad = ((d + 127) / 128) * 128;
+    p.n_tiles = (k + 127) / 128;
+    p.splits = splits;
+    p.tiles_per_split = (p.n_tiles + splits - 1) / splits;
+    if (splits > 1) {
+        float* part = reinterpret_cast<float*>(ws + sti::kWsStatusBytes);
+        p.part_ml = part;
+        p.part_o = part + (size_t)nq * splits * 2 * 64;
+    }
+    cudaError_t e = sti::launch_sparse_attn(p, st);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
+}
+
+extern "C" {
+
+const char* sti_status_string(sti_status s) {
+    switch (s) {
+        case STI_OK: return "STI_OK";
+        case STI_ERR_INVALID_ARG: return "STI_ERR_INVALID_ARG";
+        case STI_ERR_UNSUPPORTED: return "STI_ERR_UNSUPPORTED";
+        case STI_ERR_CUDA: return "STI_ERR_CUDA";
+        case STI_ERR_INDEX_RANGE: return "STI_ERR_INDEX_RANGE";
+        case STI_ERR_DEVICE_TIMEOUT: return "STI_ERR_DEVICE_TIMEOUT";
+        case STI_ERR_DEVICE_UNSUPPORTED: return "STI_ERR_DEVICE_UNSUPPORTED";
+    }
+    return "STI_UNKNOWN";
+}
+
+const char* sti_last_cuda_error(void) { return g_last_cuda_error; }
+
+int sti_version(void) { return 100; }
+
+sti_status sti_read_device_status(void* ws, uint32_t* flags, sti_stream stream) {
+    if (!ws) return STI_ERR_INVALID_ARG;
+    uint32_t host = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&host, ws, sizeof host, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof host, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "sti_read_device_status");
+    if (flags) *flags = host;
+    if (host & STI_FLAG_TIMEOUT) return STI_ERR_DEVICE_TIMEOUT;
+    if (host & STI_FLAG_INDEX_RANGE) return STI_ERR_INDEX_RANGE;
+    if (host & STI_FLAG_CHUNKED) return STI_ERR_DEVICE_UNSUPPORTED;
+    return STI_OK;
+}
+
+sti_status sti_window_idxs(const int32_t* start_pos, int b, int seqlen, int window_size, int32_t* idxs,
+                           int64_t row_stride, int* width_out, void* ws, sti_stream stream) {
+    if (ws && !aligned(ws, sti::kWsAlign)) return STI_ERR_INVALID_ARG;
+    return window_impl(start_pos, b, seqlen, window_size, idxs, row_stride, width_out,
+                       ws ? status_word(ws) : nullptr, static_cast<cudaStream_t>(stream));
+}
+
+size_t sti_idx_scores_workspace_size(void) { return sti::kWsStatusBytes; }
+
+sti_status sti_idx_scores(const uint16_t* iq, const uint16_t* ik, int64_t ik_bstride, const uint16_t* w, float c,
+                          const int32_t* start_pos, int b, int seqlen, int Hi, int Di, int n_cols, int ratio,
+                          float* scores, void* ws, size_t ws_bytes, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti_idx_scores_workspace_size())) return STI_ERR_INVALID_ARG;
+    return idx_scores_impl(iq, ik, ik_bstride, w, c, start_pos, b, seqlen, Hi, Di, n_cols, ratio, scores,
+                           status_word(ws), static_cast<cudaStream_t>(stream));
+}
+
+size_t sti_idx_topk_workspace_size(void) { return sti::kWsStatusBytes; }
+
+sti_status sti_idx_topk(const float* scores, const int32_t* start_pos, int b, int seqlen, int n_cols, int ratio,
+                        int k, int32_t offset, int32_t* idxs, int64_t row_stride, void* ws, size_t ws_bytes,
+                        sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti_idx_topk_workspace_size())) return STI_ERR_INVALID_ARG;
+    return topk_impl(scores, start_pos, b, seqlen, n_cols, ratio, k, offset, idxs, row_stride, status_word(ws),
+                     static_cast<cudaStream_t>(stream));
+}
+
+size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k) {
+    (void)h;
+    if (b <= 0 || seqlen <= 0 || d <= 0 || k <= 0) return sti::kWsStatusBytes;
+    const int nq = b * seqlen;
+    return attn_ws_bytes(nq, attn_splits_for(nq, k), d);
+}
+
+sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
+                                int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
+                                int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
+                                uint16_t* out, float* lse, void* ws, size_t ws_bytes, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
+    return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
+                     seqlen, h, d, k, out, lse, static_cast<uint8_t*>(ws), ws_bytes,
+                     static_cast<cudaStream_t>(stream));
+}
+
+static size_t decode_scores_bytes(const sti_decode_args* a) {
+    return sti::align_up((size_t)a->b * (size_t)(a->n_cols > 0 ? a->n_cols : 1) * sizeof(float), sti::kWsAlign);
+}
+
+size_t sti_decode_workspace_size(const sti_decode_args* a) {
+    if (!a || a->b <= 0) return sti::kWsStatusBytes;
+    const int k_total = a->window_size + a->index_topk;
+    // [status | attention partials | scores]
+    return sti_sparse_attn_workspace_size(a->b, 1, a->h, a->d, k_total) + decode_scores_bytes(a);
+}
+
+sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream) {
+    if (!a) return STI_ERR_INVALID_ARG;
+    if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
+    if (a->b == 0) return STI_OK;
+    if (!ws_ok(ws, ws_bytes, sti_decode_workspace_size(a))) return STI_ERR_INVALID_ARG;
+    if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    uint32_t* status = status_word(ws);
+    const int W = a->window_size, K = a->index_topk, k_total = W + K;
+    const size_t attn_ws = sti_sparse_attn_workspace_size(a->b, 1, a->h, a->d, k_total);
+    float* scores = reinterpret_cast<float*>(wsb + attn_ws);
+
+    sti_status s = window_impl(a->start_pos, a->b, 1, W, a->topk_idxs, k_total, nullptr, status, st);
+    if (s != STI_OK) return s;
+    if (a->n_cols > 0) {
+        s = idx_scores_impl(a->iq, a->ik, a->ik_bstride, a->w, a->index_scale, a->start_pos, a->b, 1, a->Hi, a->Di,
+                            a->n_cols, a->ratio, scores, status, st);
+        if (s != STI_OK) return s;
+    }
+    s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st);
+    if (s != STI_OK) return s;
+    return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
+                     a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, wsb,
+                     attn_ws, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,395 @@
+// idx_scores.cu -- Indexer scores on the tcgen05 tensor cores.
+//
+// DeepSeek V4.1, attention "attend/selected" page, Indexer.forward (score block):
+//   index_score[b,t,j] = sum_h relu(q[b,t,h,:] . k[b,j,:]) * weights[b,t,h]*c,  -inf where j >= vis(b,t)
+//
+// Shape of the GEMM: keys go in the MMA M dimension (128 keys per tile) and (queries x index
+// heads) in N, K = index_head_dim.  One TMEM lane then holds every head of one key for the
+// unit's queries, so the head-weighted ReLU reduction is an in-thread FMA chain in the
+// epilogue, with no cross-lane traffic.  Keys stream from HBM by TMA (128-byte swizzle) through
+// a multi-stage shared-memory ring; the index queries of a unit (<= 256 rows) stay resident.
+//
+// Persistent kernel, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer (index-key tiles, and the unit's query tile)
+//   warp 1      TMEM allocator + single-thread MMA issuer
+//   warps 2..5  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced)
+// Work = the flattened list of (unit, key tile) pairs over all units (unit = one sequence and
+// nq consecutive queries), cut into equal contiguous ranges, one per CTA.  Key tiles past the
+// last visible position of a unit are not computed; the epilogue writes -inf there.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "sti_internal.h"
+#include "sti_ptx.cuh"
+
+namespace sti {
+namespace {
+
+constexpr int kTileKeys = 128;
+constexpr int kThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+struct __align__(8) Barriers {
+    uint64_t full_a[kMaxStages];
+    uint64_t empty_a[kMaxStages];
+    uint64_t full_b, empty_b;
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+
+__device__ __forceinline__ int unit_tiles(const IdxScoresParams& p, int u) {
+    const int b = u / p.QT, qt = u - b * p.QT;
+    const int t_last = min(p.s, (qt + 1) * p.nq) - 1;
+    int vis = (__ldg(p.start_pos + b) + t_last + 1) / p.ratio;
+    vis = max(0, min(vis, p.n_cols));
+    return (vis + kTileKeys - 1) / kTileKeys;
+}
+
+// Warp-cooperative: total number of compute tiles over all units.
+__device__ int total_tiles(const IdxScoresParams& p) {
+    const int lane = threadIdx.x & 31;
+    int sum = 0;
+    for (int u0 = 0; u0 < p.total_units; u0 += 32) {
+        const int u = u0 + lane;
+        sum += (u < p.total_units) ? unit_tiles(p, u) : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    return sum;
+}
+
+// Warp-cooperative: (unit, tile) of flattened tile index g (unit == total_units past the end).
+__device__ void locate(const IdxScoresParams& p, int g, int& u_out, int& tile_out) {
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    for (int u0 = 0; u0 < p.total_units; u0 += 32) {
+        const int u = u0 + lane;
+        const int n = (u < p.total_units) ? unit_tiles(p, u) : 0;
+        int inc = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int chunk_total = __shfl_sync(kFull, inc, 31);
+        if (g < base + chunk_total) {
+            const unsigned m = __ballot_sync(kFull, base + inc > g);
+            const int l = __ffs(m) - 1;
+            const int excl = __shfl_sync(kFull, inc - n, l);
+            u_out = u0 + l;
+            tile_out = g - base - excl;
+            return;
+        }
+        base += chunk_total;
+    }
+    u_out = p.total_units;
+    tile_out = 0;
+}
+
+__device__ __forceinline__ void advance(const IdxScoresParams& p, int& u, int& tile) {
+    ++tile;
+    while (u < p.total_units && tile >= unit_tiles(p, u)) {
+        ++u;
+        tile = 0;
+    }
+}
+
+// K-major operand descriptor of K-step kk (16 bf16) for a tile of `rows` rows stored as column
+// blocks of rows x 128 bytes (128-byte swizzle, Di >= 64) or one block of 64-byte rows (Di == 32).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int Di, int rows) {
+    if (Di >= 64) {
+        const uint32_t addr = base + (uint32_t)(kk >> 2) * (uint32_t)rows * 128u + (uint32_t)(kk & 3) * 32u;
+        return sdesc(addr, 16, 1024, kLayoutSW128);
+    }
+    const uint32_t addr = base + (uint32_t)kk * 32u;
+    return sdesc(addr, 16, 512, kLayoutSW64);
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const IdxScoresParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int a_bytes = kTileKeys * p.Di * 2;
+    const int b_bytes = p.n_pad * p.Di * 2;
+    uint8_t* a_ring = smem;
+    uint8_t* b_buf = smem + (size_t)p.stages * a_bytes;
+    Barriers* bars = reinterpret_cast<Barriers*>(b_buf + b_bytes);
+    float* w_s = reinterpret_cast<float*>(bars + 1);   // [nq * HI], pre-multiplied by c
+    int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(&bars->full_a[i], 1);
+            mbar_init(&bars->empty_a[i], 1);
+        }
+        mbar_init(&bars->full_b, 1);
+        mbar_init(&bars->empty_b, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->acc_full[i], 1);
+            mbar_init(&bars->acc_empty[i], 4);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    // this CTA's contiguous range of the flattened (unit, tile) list
+    const int T = total_tiles(p);
+    const int g0 = (int)(((int64_t)T * blockIdx.x) / gridDim.x);
+    const int g1 = (int)(((int64_t)T * (blockIdx.x + 1)) / gridDim.x);
+    int u, tile;
+    locate(p, g0, u, tile);
+    const int ncb = p.Di >= 64 ? p.Di / 64 : 1;  // column blocks per row
+    const int box_inner = p.Di >= 64 ? 64 : p.Di;
+
+    auto aborted = [&]() { return *(volatile uint32_t*)&bars->abort != 0u; };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        // Every iteration runs even after an abort (with the waits skipped), so all roles stay
+        // in step; at the end the producer waits for the last load of each stage so no TMA
+        // write is in flight when the CTA exits.
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a);
+            tma_prefetch_desc(&tm_b);
+        }
+        int stage = 0;
+        uint32_t phase = 0, b_phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;  // per stage: armed at least once, parity of last arm
+        bool b_issued = false;
+        int cur_unit = -1;
+        for (int g = g0; g < g1; ++g) {
+            const int b = u / p.QT, qt = u - (u / p.QT) * p.QT;
+            if (lane == 0 && !aborted()) {
+                bool ok = true;
+                if (u != cur_unit) {
+                    ok = mbar_wait(&bars->empty_b, b_phase ^ 1u, p.status);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bars->full_b, (uint32_t)b_bytes);
+                        for (int cb = 0; cb < ncb; ++cb)
+                            tma_load_3d(b_buf + (size_t)cb * p.n_pad * box_inner * 2, &tm_b, &bars->full_b,
+                                        cb * box_inner, qt * p.nq * HI, b);
+                        b_issued = true;
+                    }
+                }
+                ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
+                if (ok) {
+                    uint8_t* dst = a_ring + (size_t)stage * a_bytes;
+                    mbar_arrive_expect_tx(&bars->full_a[stage], (uint32_t)a_bytes);
+                    for (int cb = 0; cb < ncb; ++cb)
+                        tma_load_3d(dst + (size_t)cb * kTileKeys * box_inner * 2, &tm_a, &bars->full_a[stage],
+                                    cb * box_inner, tile * kTileKeys, b);
+                    issued_mask |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                } else {
+                    atomicExch(&bars->abort, 1u);
+                }
+            }
+            if (u != cur_unit) b_phase ^= 1u;
+            cur_unit = u;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            advance(p, u, tile);
+        }
+        if (lane == 0) {
+            for (int st = 0; st < p.stages; ++st)
+                if (issued_mask & (1u << st)) mbar_wait(&bars->full_a[st], (issued_parity >> st) & 1u, p.status);
+            if (b_issued) mbar_wait(&bars->full_b, b_phase ^ 1u, p.status);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        const uint32_t idesc = idesc_bf16_f32(128, p.n_pad, false, false);
+        const int ksteps = p.Di / 16;
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0, b_phase = 0;
+        int cur_unit = -1;
+        for (int g = g0; g < g1; ++g) {
+            if (lane == 0 && !aborted()) {
+                bool ok = true;
+                if (u != cur_unit) {
+                    if (cur_unit >= 0) umma_commit(&bars->empty_b);
+                    ok = mbar_wait(&bars->full_b, b_phase, p.status);
+                }
+                ok = ok && mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, p.status);
+                ok = ok && mbar_wait(&bars->full_a[stage], phase, p.status);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t a_base = smem_u32(a_ring + (size_t)stage * a_bytes);
+                    const uint32_t b_base = smem_u32(b_buf);
+                    const uint32_t d_tmem = tmem + (uint32_t)(acc * p.n_alloc);
+                    for (int kk = 0; kk < ksteps; ++kk)
+                        umma_bf16(d_tmem, kmajor_desc(a_base, kk, p.Di, kTileKeys),
+                                  kmajor_desc(b_base, kk, p.Di, p.n_pad), idesc, kk > 0 ? 1u : 0u);
+                    umma_commit(&bars->empty_a[stage]);
+                    umma_commit(&bars->acc_full[acc]);
+                } else {
+                    atomicExch(&bars->abort, 1u);
+                }
+            }
+            if (u != cur_unit) b_phase ^= 1u;
+            cur_unit = u;
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            advance(p, u, tile);
+        }
+        if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
+            umma_commit(&bars->mma_done);
+            mbar_wait(&bars->mma_done, 0, p.status);
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int ep_tid = threadIdx.x - 64;           // 0..127
+        const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        constexpr int QPC = HI >= 32 ? 1 : 32 / HI;    // queries per 32-column load
+        constexpr int CPQ = HI >= 32 ? HI / 32 : 1;    // 32-column loads per query
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int cur_unit = -1;
+        for (int g = g0; g < g1; ++g) {
+            const int b = u / p.QT, qt = u - (u / p.QT) * p.QT;
+            const int t0 = qt * p.nq;
+            const int nq_here = min(p.nq, p.s - t0);
+            if (u != cur_unit) {
+                named_bar_sync(1, 128);
+                for (int i = ep_tid; i < nq_here * HI; i += 128) {
+                    const uint16_t wb = p.w[((size_t)b * p.s + t0) * HI + i];
+                    w_s[i] = __uint_as_float((uint32_t)wb << 16) * p.c;
+                }
+                for (int i = ep_tid; i < nq_here; i += 128)
+                    vis_s[i] = max(0, min(p.n_cols, (__ldg(p.start_pos + b) + t0 + i + 1) / p.ratio));
+                named_bar_sync(1, 128);
+                cur_unit = u;
+            }
+            const bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
+            if (!ok) atomicExch(&bars->abort, 1u);
+            tc_fence_after();
+            const int key = tile * kTileKeys + quarter * 32 + lane;
+            const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * p.n_alloc);
+            if (ok) {
+                for (int q0 = 0; q0 < nq_here; q0 += QPC) {
+                    float sacc[QPC];
+#pragma unroll
+                    for (int i = 0; i < QPC; ++i) sacc[i] = 0.f;
+#pragma unroll
+                    for (int cq = 0; cq < CPQ; ++cq) {
+                        uint32_t r[32];
+                        tmem_ld32(col_base + (uint32_t)(q0 * HI + cq * 32), r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int qq = HI >= 32 ? 0 : i / HI;
+                            const int hh = HI >= 32 ? cq * 32 + i : i % HI;
+                            const float v = fmaxf(__uint_as_float(r[i]), 0.f);
+                            sacc[qq] = fmaf(w_s[(q0 + qq) * HI + hh], v, sacc[qq]);
+                        }
+                    }
+                    if (key < p.n_cols) {
+#pragma unroll
+                        for (int qq = 0; qq < QPC; ++qq) {
+                            const int q = q0 + qq;
+                            if (q < nq_here) {
+                                float* dst = p.scores + ((size_t)b * p.s + t0 + q) * p.n_cols + key;
+                                *dst = key < vis_s[q] ? sacc[qq] : -INFINITY;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            advance(p, u, tile);
+        }
+        // -inf for key tiles no query of a unit can see (units strided over CTAs)
+        for (int uu = blockIdx.x; uu < p.total_units; uu += gridDim.x) {
+            const int b = uu / p.QT, qt = uu - (uu / p.QT) * p.QT;
+            const int t0 = qt * p.nq;
+            const int nq_here = min(p.nq, p.s - t0);
+            const int first = unit_tiles(p, uu) * kTileKeys;
+            for (int q = 0; q < nq_here; ++q) {
+                float* row = p.scores + ((size_t)b * p.s + t0 + q) * p.n_cols;
+                for (int j = first + ep_tid; j < p.n_cols; j += 128) row[j] = -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+    }
+}
+
+}  // namespace
+
+int idx_scores_pick_nq(int Hi, int s) {
+    // N = nq * Hi <= 256 (one MMA), never more queries than the sequence has
+    int nq = 256 / Hi;
+    if (nq > s) nq = s;
+    if (nq < 1) nq = 1;
+    return nq;
+}
+
+size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
+    const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
+    const size_t b_bytes = (size_t)p.n_pad * p.Di * 2;
+    return 1024 + p.stages * a_bytes + b_bytes + sizeof(Barriers) + 256 * 4 + 256 * 4;
+}
+
+cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const IdxScoresParams& p,
+                              int num_sms, cudaStream_t stream) {
+    size_t smem = idx_scores_smem_bytes(p);
+    // keep one CTA per SM: the kernel's TMEM demand assumes it owns the SM's TMEM
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    const int grid = num_sms;
+    cudaError_t err = cudaSuccess;
+#define STI_LAUNCH_HI(HV)                                                                              \
+    case HV: {                                                                                         \
+        auto kern = idx_scores_kernel<HV>;                                                             \
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
+        if (err != cudaSuccess) return err;                                                            \
+        kern<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, p);                                         \
+        return cudaGetLastError();                                                                     \
+    }
+    switch (p.Hi) {
+        STI_LAUNCH_HI(4)
+        STI_LAUNCH_HI(8)
+        STI_LAUNCH_HI(16)
+        STI_LAUNCH_HI(32)
+        STI_LAUNCH_HI(64)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef STI_LAUNCH_HI
+}
+
+}  // namespace sti

@@ -1,0 +1,424 @@
+// sparse_attn.cu -- sparse multi-head attention with an attention sink over gathered rows of one
+// shared latent KV.
+//
+// DeepSeek V4.1, attention "attend/selected" page, sparse_attn_kernel / sparse_attn:
+//   for every query and head, over the slots i whose index is not -1:
+//     s_i = softmax_scale * q . kv[idx_i];  o = sum_i e^{s_i} kv[idx_i] / (sum_i e^{s_i} + e^{sink_h})
+//   the same row serving as key and value; a query with no valid slot gets 0.
+//
+// GB300 design (not the page's kernel, which puts the heads in the MMA M dimension):
+//   * One CTA handles one query and a range of 128-row KV tiles.  The rows of a tile are gathered
+//     with 16-byte cp.async straight into the 128-byte-swizzled UMMA layout (column blocks of
+//     128 rows x 128 bytes); masked slots are zero-filled and get score -inf.
+//   * S^T = KV_tile . Q^T runs as tcgen05 M=128 (rows) x N=64 (heads, zero-padded) x K=d, so the
+//     MMA uses the full 128-lane datapath even though a query has only 64 heads.  The tile is the
+//     K-major A operand; Q (resident, zero-padded to 64 heads) the K-major B operand.
+//   * Online softmax in fp32 on the TMEM tile: thread r owns row r; per-head maxima and sums across
+//     the 128 rows are warp reduce-scatters plus a 4-warp combine in shared memory.  P^T is
+//     written as bf16 (the page also rounds P to bf16 before the PV product).
+//   * O^T += V^T . P^T runs as tcgen05 M=128 (d block) x N=64 x K=128 rows, reading the SAME
+//     shared-memory tile as an MN-major A operand -- K and V are one row, fetched once.
+//     O^T lives in TMEM (d/128 blocks of 128 lanes x 64 columns); rescaling when a head's
+//     running max grows is a TMEM load-scale-store by the owning thread.
+//   * Few queries (decode) split a query's tiles over several CTAs, each writing its
+//     unnormalised partial (O, running max, running sum) to the workspace; a combine kernel merges
+//     the partials with the sink (flash-decoding style).  Many queries write the output directly.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "sti_internal.h"
+#include "sti_ptx.cuh"
+
+namespace sti {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kRows = 128;        // KV rows per tile (MMA M)
+constexpr int kHp = 64;           // heads padded (MMA N)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+struct __align__(8) AttnSmemTail {
+    uint64_t mma_bar;
+    uint32_t tmem_base;
+    uint32_t pad;
+    float m_run[kHp];     // running max, log2 domain
+    float l_run[kHp];     // running sum of 2^(x - m)
+    float alpha[kHp];     // rescale factor of this tile
+    float red[4][kHp];    // per-warp partial reductions
+    const uint16_t* row_src[kRows];
+    int row_valid[kRows];
+};
+
+// Swizzled byte offset of 16-byte chunk `ch` (of 8 bf16) of row `r` in a tile of `rows` rows
+// stored as column blocks of rows x 128 bytes (128-byte swizzle: chunk ^= row % 8).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
+    return (uint32_t)(ch >> 3) * (uint32_t)rows * 128u + (uint32_t)r * 128u + (uint32_t)(((ch & 7) ^ (r & 7)) << 4);
+}
+
+// Reduce-scatter of 64 per-lane values over the 32 lanes of a warp: afterwards lane l holds the
+// reduction (over the warp's 32 rows) of heads 2l and 2l+1 in v[0], v[1].
+template <bool IS_MAX>
+__device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int half = 32 >> step;          // values still held: 2*half
+        const int off = 16 >> step;           // partner lane distance
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float lo = v[i], hi = v[i + half];
+            const float send = upper ? lo : hi;
+            const float keep = upper ? hi : lo;
+            const float recv = __shfl_xor_sync(kFull, send, off);
+            v[i] = IS_MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_s = smem;                                 // [64 heads] x d_pad, K-major SW128
+    uint8_t* kv_s = q_s + (size_t)kHp * p.d_pad * 2;     // [128 rows] x d_pad, SW128
+    uint8_t* p_s = kv_s + (size_t)kRows * p.d_pad * 2;   // [128 rows] x 64 heads bf16, SW128
+    AttnSmemTail* tl = reinterpret_cast<AttnSmemTail*>(p_s + kRows * 128);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int query = blockIdx.x, split = blockIdx.y;
+    const int b = query / p.s;
+    const int tile_begin = split * p.tiles_per_split;
+    const int tile_end = min(p.n_tiles, tile_begin + p.tiles_per_split);
+
+    if (warp == 0) {
+        tmem_alloc(&tl->tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&tl->mma_bar, 1);
+        fence_mbar_init();
+    }
+    if (tid < kHp) {
+        tl->m_run[tid] = -INFINITY;
+        tl->l_run[tid] = 0.f;
+    }
+    // Q -> shared memory (heads >= h and columns >= d are zero)
+    {
+        const uint16_t* qrow = p.q + (size_t)query * p.h * p.d;
+        const int chunks_per_row = p.d_pad / 8;
+        for (int c = tid; c < kHp * chunks_per_row; c += kThreads) {
+            const int hr = c / chunks_per_row, ch = c - hr * chunks_per_row;
+            const bool ok = hr < p.h && ch * 8 < p.d;
+            const uint16_t* src = ok ? qrow + (size_t)hr * p.d + ch * 8 : p.q;
+            cp_async_16(smem_u32(q_s) + sw128_offset(hr, ch, kHp), src, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tl->tmem_base;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tm_s = tmem;              // S^T: columns [0, 64)
+    const uint32_t tm_o = tmem + 64;         // O^T block m: columns [64 + 64m, 128 + 64m)
+    const int nmb = p.d_pad / 128;           // d blocks of 128
+    uint32_t mma_phase = 0;
+    bool dead = false;
+
+    const uint32_t idesc_qk = idesc_bf16_f32(128, kHp, false, false);
+    const uint32_t idesc_pv = idesc_bf16_f32(128, kHp, true, true);
+    const int32_t* idx_row = p.idx + (size_t)query * p.idx_stride;
+    const int n_rows = p.n1 + p.n2;
+
+    for (int tile = tile_begin; tile < tile_end; ++tile) {
+        // ---- gather: thread r resolves slot r of the tile
+        {
+            const int slot = tile * kRows + tid;
+            int idx = slot < p.k ? __ldg(idx_row + slot) : -1;
+            if (idx < -1 || idx >= n_rows) {
+                atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
+                idx = -1;
+            }
+            const uint16_t* src = nullptr;
+            if (idx >= 0)
+                src = idx < p.n1 ? p.kv + (size_t)b * p.kv_bstride + (size_t)idx * p.d
+                                 : p.kv2 + (size_t)b * p.kv2_bstride + (size_t)(idx - p.n1) * p.d;
+            tl->row_src[tid] = src;
+            tl->row_valid[tid] = idx >= 0;
+        }
+        __syncthreads();
+        {
+            const int chunks_per_row = p.d_pad / 8;
+            const uint32_t kv_base = smem_u32(kv_s);
+            for (int c = tid; c < kRows * chunks_per_row; c += kThreads) {
+                const int r = c / chunks_per_row, ch = c - r * chunks_per_row;
+                const uint16_t* rs = tl->row_src[r];
+                const bool ok = rs != nullptr && ch * 8 < p.d;
+                cp_async_16(kv_base + sw128_offset(r, ch, kRows), ok ? rs + ch * 8 : p.q, ok ? 16u : 0u);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---- S^T = KV . Q^T
+        if (tid == 0 && !dead) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(kv_s), b0 = smem_u32(q_s);
+            for (int kk = 0; kk < p.d_pad / 16; ++kk) {
+                const uint32_t cb = (uint32_t)(kk >> 2), ko = (uint32_t)(kk & 3) * 32u;
+                umma_bf16(tm_s, sdesc(a0 + cb * kRows * 128u + ko, 16, 1024, kLayoutSW128),
+                          sdesc(b0 + cb * kHp * 128u + ko, 16, 1024, kLayoutSW128), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&tl->mma_bar);
+        }
+        if (!dead) dead = !mbar_wait(&tl->mma_bar, mma_phase, p.status);
+        mma_phase ^= 1u;
+        tc_fence_after();
+
+        // ---- online softmax (thread = row, 64 heads in registers)
+        float x[kHp];
+        {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tm_s + lane_base, r0);
+            tmem_ld32(tm_s + lane_base + 32, r1);
+            tmem_ld_wait();
+            const bool valid = tl->row_valid[tid] != 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                x[i] = valid ? __uint_as_float(r0[i]) * p.scale_log2 : -INFINITY;
+                x[i + 32] = valid ? __uint_as_float(r1[i]) * p.scale_log2 : -INFINITY;
+            }
+        }
+        {
+            float v[kHp];
+#pragma unroll
+            for (int i = 0; i < kHp; ++i) v[i] = x[i];
+            warp_reduce_scatter64<true>(v);
+            tl->red[warp][2 * lane] = v[0];
+            tl->red[warp][2 * lane + 1] = v[1];
+        }
+        __syncthreads();
+        if (tid < kHp) {
+            const float mt = fmaxf(fmaxf(tl->red[0][tid], tl->red[1][tid]), fmaxf(tl->red[2][tid], tl->red[3][tid]));
+            const float m_old = tl->m_run[tid];
+            const float m_new = fmaxf(m_old, mt);
+            tl->alpha[tid] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+            tl->m_run[tid] = m_new;
+        }
+        __syncthreads();
+        {
+            float v[kHp];
+#pragma unroll
+            for (int i = 0; i < kHp; ++i) {
+                const float m = tl->m_run[i];
+                x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
+                v[i] = x[i];
+            }
+            // P^T row (this thread's row): 64 heads as bf16, 8 chunks of 16 bytes, swizzled
+            uint8_t* prow = p_s + tid * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 pk;
+                pk.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
+                pk.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+                pk.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+                pk.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = pk;
+            }
+            warp_reduce_scatter64<false>(v);
+            tl->red[warp][2 * lane] = v[0];   // every read of the maxima happened before the last barrier
+            tl->red[warp][2 * lane + 1] = v[1];
+        }
+        __syncthreads();
+        if (tid < kHp)
+            tl->l_run[tid] = tl->l_run[tid] * tl->alpha[tid] + (tl->red[0][tid] + tl->red[1][tid]) +
+                             (tl->red[2][tid] + tl->red[3][tid]);
+        // rescale the running O^T (lane = d within a block, column = head)
+        if (tile > tile_begin && !dead) {
+            for (int m = 0; m < nmb; ++m) {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    const uint32_t ta = tm_o + lane_base + (uint32_t)(64 * m + 32 * half);
+                    tmem_ld32(ta, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[32 * half + i]);
+                    tmem_st32(ta, r);
+                }
+            }
+            tmem_st_wait();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- O^T += V^T . P^T  (A = the same KV tile, MN-major; B = P^T, MN-major)
+        if (tid == 0 && !dead) {
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(kv_s), b0 = smem_u32(p_s);
+            const uint32_t lbo_a = kRows * 128u;      // next 64-column block of the tile
+            for (int m = 0; m < nmb; ++m)
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                    umma_bf16(tm_o + (uint32_t)(64 * m),
+                              sdesc(a0 + (uint32_t)(2 * m) * lbo_a + (uint32_t)kk * 2048u, lbo_a, 1024, kLayoutSW128),
+                              sdesc(b0 + (uint32_t)kk * 2048u, kRows * 128u, 1024, kLayoutSW128), idesc_pv,
+                              (tile > tile_begin || kk > 0) ? 1u : 0u);
+            umma_commit(&tl->mma_bar);
+        }
+        if (!dead) dead = !mbar_wait(&tl->mma_bar, mma_phase, p.status);
+        mma_phase ^= 1u;
+        tc_fence_after();
+    }
+
+    // ---- epilogue: O^T (lane = d, column = head) -> output or split partial
+    cp_async_wait<0>();   // Q's copy when this CTA had no tile
+    __syncthreads();
+    const bool has_tiles = tile_begin < tile_end && !dead;
+    if (p.splits == 1) {
+        // final: o = O / (l + 2^(sink*log2e - m)); empty rows (m = -inf) give 0
+        if (tid < kHp) {
+            const float m = tl->m_run[tid];
+            float inv = 0.f, lse = -INFINITY;
+            if (m != -INFINITY && tid < p.h) {
+                const float den = tl->l_run[tid] + exp2f(__ldg(p.sink + tid) * kLog2e - m);
+                inv = 1.f / den;
+                lse = (m + log2f(den)) * kLn2;
+            }
+            tl->alpha[tid] = inv;
+            if (p.lse && tid < p.h) p.lse[(size_t)query * p.h + tid] = lse;
+        }
+        __syncthreads();
+        uint16_t* orow = p.out + (size_t)query * p.h * p.d;
+        for (int m = 0; m < nmb; ++m) {
+            const int dd = 128 * m + tid;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                if (has_tiles) {
+                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (dd < p.d) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int hh = 32 * half + i;
+                        if (hh < p.h) {
+                            const float v = __uint_as_float(r[i]) * tl->alpha[hh];
+                            orow[(size_t)hh * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        const size_t part = (size_t)query * p.splits + split;
+        if (tid < kHp) {
+            p.part_ml[part * 2 * kHp + tid] = has_tiles ? tl->m_run[tid] : -INFINITY;
+            p.part_ml[part * 2 * kHp + kHp + tid] = has_tiles ? tl->l_run[tid] : 0.f;
+        }
+        float* po = p.part_o + part * (size_t)p.h * p.d;
+        for (int m = 0; m < nmb; ++m) {
+            const int dd = 128 * m + tid;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                if (has_tiles) {
+                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), r);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                }
+                if (dd < p.d) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int hh = 32 * half + i;
+                        if (hh < p.h) po[(size_t)hh * p.d + dd] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Merge the split partials of one (query, head):
+//   o = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(sink*log2e - M)),  M = max_s m_s.
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
+    const int query = blockIdx.x, hh = blockIdx.y;
+    const float* ml = p.part_ml + (size_t)query * p.splits * 2 * kHp;
+    float M = -INFINITY;
+    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, ml[sp * 2 * kHp + hh]);
+    float den = 0.f;
+    if (M != -INFINITY) {
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float m = ml[sp * 2 * kHp + hh];
+            if (m != -INFINITY) den += ml[sp * 2 * kHp + kHp + hh] * exp2f(m - M);
+        }
+        den += exp2f(__ldg(p.sink + hh) * kLog2e - M);
+    }
+    const float inv = (M == -INFINITY) ? 0.f : 1.f / den;
+    if (p.lse && threadIdx.x == 0)
+        p.lse[(size_t)query * p.h + hh] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * kLn2;
+    uint16_t* orow = p.out + ((size_t)query * p.h + hh) * p.d;
+    for (int dd = threadIdx.x; dd < p.d; dd += blockDim.x) {
+        float acc = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+            const float m = ml[sp * 2 * kHp + hh];
+            if (m != -INFINITY)
+                acc += p.part_o[(((size_t)query * p.splits + sp) * p.h + hh) * p.d + dd] * exp2f(m - M);
+        }
+        orow[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
+    }
+}
+
+size_t attn_smem_bytes(int d_pad) {
+    return 1024 + (size_t)kHp * d_pad * 2 + (size_t)kRows * d_pad * 2 + kRows * 128 + sizeof(AttnSmemTail);
+}
+
+}  // namespace
+
+int attn_pick_splits(int n_queries, int n_tiles, int num_sms) {
+    if (n_tiles <= 1) return 1;
+    if (n_queries >= num_sms) return 1;
+    int splits = (num_sms + n_queries - 1) / n_queries;
+    if (splits > n_tiles) splits = n_tiles;
+    return splits;
+}
+
+size_t attn_partials_bytes(int n_queries, int splits, int d) {
+    if (splits <= 1) return 0;
+    return (size_t)n_queries * splits * (size_t)(kHp * d + 2 * kHp) * sizeof(float);
+}
+
+cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
+    const int n_queries = p.B * p.s;
+    if (n_queries == 0) return cudaSuccess;
+    const size_t smem = attn_smem_bytes(p.d_pad);
+    cudaError_t err =
+        cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(n_queries, p.splits);
+    sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || p.splits == 1) return err;
+    attn_combine_kernel<<<dim3(n_queries, p.h), 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sti

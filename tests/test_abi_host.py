@@ -1,0 +1,102 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libsti():
+    from sparse_top_attention_indexer_gb300 import _build
+
+    _build.build()
+    import sparse_top_attention_indexer_gb300 as m
+
+    return m.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "sti.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(sti_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(libsti):
+    names = _declared()
+    assert "sti_idx_scores" in names and "sti_sparse_attn_sink" in names and "sti_decode_fused" in names
+    for n in names:
+        assert hasattr(libsti, n), f"{n} declared in sti.h but not exported"
+
+
+def test_binding_lists_every_export():
+    import sparse_top_attention_indexer_gb300 as m
+
+    assert sorted(m.EXPORTS) == _declared()
+
+
+def test_status_strings_and_version(libsti):
+    assert libsti.sti_status_string(0) == b"STI_OK"
+    assert libsti.sti_status_string(4) == b"STI_ERR_INDEX_RANGE"
+    assert libsti.sti_version() >= 100
+
+
+def test_host_argument_checks(libsti):
+    """Invalid arguments return before any CUDA call (no GPU needed)."""
+    fake = 1 << 20     # aligned non-null pointer value; never dereferenced on the host
+    P = ctypes.c_void_p
+    # workspace missing / misaligned
+    assert libsti.sti_idx_scores(P(fake), P(fake), 128 * 100, P(fake), 1.0, P(fake), 1, 1, 32, 128, 100, 4, P(fake),
+                                 None, 256, None) == 1
+    assert libsti.sti_idx_scores(P(fake), P(fake), 128 * 100, P(fake), 1.0, P(fake), 1, 1, 32, 128, 100, 4, P(fake),
+                                 P(fake + 8), 256, None) == 1
+    # unsupported index head dim / head count
+    assert libsti.sti_idx_scores(P(fake), P(fake), 100 * 96, P(fake), 1.0, P(fake), 1, 1, 32, 96, 100, 4, P(fake),
+                                 P(fake), 256, None) == 2
+    assert libsti.sti_idx_scores(P(fake), P(fake), 100 * 128, P(fake), 1.0, P(fake), 1, 1, 12, 128, 100, 4, P(fake),
+                                 P(fake), 256, None) == 2
+    # key batch stride too small / not a multiple of 8
+    assert libsti.sti_idx_scores(P(fake), P(fake), 128 * 99, P(fake), 1.0, P(fake), 1, 1, 32, 128, 100, 4, P(fake),
+                                 P(fake), 256, None) == 1
+    assert libsti.sti_idx_scores(P(fake), P(fake), 128 * 100 + 4, P(fake), 1.0, P(fake), 1, 1, 32, 128, 100, 4,
+                                 P(fake), P(fake), 256, None) == 1
+    # top-k: k too large, row stride smaller than k
+    assert libsti.sti_idx_topk(P(fake), P(fake), 1, 1, 100, 4, 5000, 0, P(fake), 5000, P(fake), 256, None) == 2
+    assert libsti.sti_idx_topk(P(fake), P(fake), 1, 1, 100, 4, 64, 0, P(fake), 32, P(fake), 256, None) == 1
+    # attention: too many heads, head dim not a multiple of 64, index row stride < k, small workspace
+    assert libsti.sti_sparse_attn_sink(P(fake), P(fake), 100 * 512, None, 0, 100, 0, P(fake), P(fake), 640, 0.1, 1,
+                                       1, 65, 512, 640, P(fake), None, P(fake), 1 << 30, None) == 2
+    assert libsti.sti_sparse_attn_sink(P(fake), P(fake), 100 * 96, None, 0, 100, 0, P(fake), P(fake), 640, 0.1, 1, 1,
+                                       64, 96, 640, P(fake), None, P(fake), 1 << 30, None) == 2
+    assert libsti.sti_sparse_attn_sink(P(fake), P(fake), 100 * 512, None, 0, 100, 0, P(fake), P(fake), 100, 0.1, 1,
+                                       1, 64, 512, 640, P(fake), None, P(fake), 1 << 30, None) == 1
+    assert libsti.sti_sparse_attn_sink(P(fake), P(fake), 100 * 512, None, 0, 100, 0, P(fake), P(fake), 640, 0.1, 2,
+                                       1, 64, 512, 640, P(fake), None, P(fake), 256, None) == 1
+    # second source missing while n2 > 0
+    assert libsti.sti_sparse_attn_sink(P(fake), P(fake), 100 * 512, None, 0, 100, 10, P(fake), P(fake), 640, 0.1,
+                                       4096, 1, 64, 512, 640, P(fake), None, P(fake), 1 << 30, None) == 1
+    # window: row stride shorter than the width; empty batch is a no-op
+    assert libsti.sti_window_idxs(P(fake), 1, 1, 128, P(fake), 64, None, None, None) == 1
+    assert libsti.sti_window_idxs(None, 0, 1, 128, None, 128, None, None, None) == 0
+
+
+def test_window_width_reported(libsti):
+    w = ctypes.c_int(0)
+    assert libsti.sti_window_idxs(None, 0, 300, 128, None, 128, ctypes.byref(w), None, None) == 0
+    assert w.value == 128
+    assert libsti.sti_window_idxs(None, 0, 37, 128, None, 128, ctypes.byref(w), None, None) == 0
+    assert w.value == 37
+    assert libsti.sti_window_idxs(None, 0, 1, 128, None, 128, ctypes.byref(w), None, None) == 0
+    assert w.value == 128
+
+
+def test_workspace_sizes(libsti):
+    assert libsti.sti_idx_scores_workspace_size() >= 4
+    assert libsti.sti_idx_topk_workspace_size() >= 4
+    # split partials only when queries are few
+    small = libsti.sti_sparse_attn_workspace_size(2, 1, 64, 512, 640)
+    big = libsti.sti_sparse_attn_workspace_size(4096, 1, 64, 512, 640)
+    assert small > 256 and big == 256
