@@ -1,0 +1,479 @@
+"""Benchmark of the Indexer -> top-k -> sparse sink attention path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2|3|4|5] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
+window indices, Indexer scores, top-k, sparse sink attention (and the split-KV combine),
+launched through the C ABI on one stream.  Default workload: single-layer decode, b=32,
+context 65536 (16384 compressed rows), 64 heads x 512, index heads 32 x 128, top-512.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream with an event between every kernel; a 256 MiB buffer is written before
+every step (outside the events) so no step finds the previous step's data in L2.
+`value` is tokens/s (decode) or queries/s (prefill) over the timed region; `e2e` is the same
+metric through the fused public entry point with the step's inputs copied from pinned host
+memory and the output copied back every step (wall clock).  `roofline` reports the kernel
+with the largest share of the step against the measured HBM or bf16 tensor peak.
+`cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (weak scaling; the
+path needs no data exchange); rank 0 prints the line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decode tokens/s and prefill queries/s (indexer+topk+sparse_attn); % HBM/TC roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the sources of the kernels whose ncu counters profiles/ records."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_top_attention_indexer_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for ln in f:
+            m = re.match(r"\s*(\S+)\s+(\S+)\s+bytes_per_launch=(\d+)\s+sources=(\w+)", ln)
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == want:
+                return int(m.group(3))
+    return None
+
+
+# ---------------------------------------------------------------------------------- GPU steps
+
+
+class GpuPath:
+    """Device-resident inputs of one workload and the step that runs the path on them."""
+
+    def __init__(self, shape: workloads.Shape, data: dict, device):
+        import torch
+
+        import sparse_top_attention_indexer_gb300 as sti
+        from tests._util import to_dev, to_dev_any
+
+        self.sti, self.torch, self.shape = sti, torch, shape
+        self.dev = device
+        self.b, self.s = shape.b, shape.s
+        self.prefill = shape.prefill
+        self.W = shape.window
+        self.width = shape.win_width
+        self.k_total = self.width + shape.topk
+        self.L = shape.n_layers
+        self.q = [to_dev(data["q"][i], device) for i in range(self.L)]
+        self.win = [to_dev(data["win"][i], device) for i in range(self.L)]
+        self.sink = [to_dev_any(data["sink"][i], device) for i in range(self.L)]
+        self.comp = to_dev(data["comp"], device)
+        self.iq = to_dev(data["iq"], device)
+        self.ik = to_dev(data["ik"], device)
+        self.w = to_dev(data["w"], device)
+        self.sp = to_dev_any(data["start_pos"], device)
+        self.scores = torch.empty(self.b, self.s, shape.n_cols, dtype=torch.float32, device=device)
+        self.idx = torch.empty(self.b, self.s, self.k_total, dtype=torch.int32, device=device)
+        self.out = [torch.empty_like(self.q[i]) for i in range(self.L)]
+        ws_attn = sti.sparse_attn_workspace_size(self.b, self.s, shape.h, shape.d, self.k_total)
+        self.ws = sti.workspace(max(ws_attn, 256), device)
+        self.splits = ws_attn > 256
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.names = ["window_idx", "idx_scores", "idx_topk"] + [f"sparse_attn[{i}]" for i in range(self.L)]
+
+    def launches_per_step(self) -> int:
+        return 3 + self.L * (2 if self.splits else 1)
+
+    def step(self, events=None):
+        """One pass of the path; events (len = len(names)+1) are recorded around every call."""
+        sti, shp = self.sti, self.shape
+        rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        rec(0)
+        sti.window_idxs(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
+        rec(1)
+        sti.idx_scores(self.iq, self.ik, self.w, shp.index_scale, self.sp, shp.n_cols, shp.ratio, out=self.scores,
+                       ws=self.ws)
+        rec(2)
+        sti.idx_topk(self.scores, self.sp, shp.ratio, shp.topk, self.width, out=self.idx[..., self.width:],
+                     ws=self.ws)
+        rec(3)
+        for i in range(self.L):
+            sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale, kv2=self.comp,
+                                 out=self.out[i], ws=self.ws)
+            rec(4 + i)
+
+    def flush_l2(self):
+        self.flush.fill_(1)
+
+
+# ---------------------------------------------------------------------------------- work accounting
+
+
+def work(shape: workloads.Shape, data: dict) -> dict:
+    """Algorithmic bytes and FLOPs per kernel launch (what the method must move / compute)."""
+    sp = data["start_pos"].astype(np.int64)
+    b, s, Hi, Di, h, d = shape.b, shape.s, shape.Hi, shape.Di, shape.h, shape.d
+    t = np.arange(s, dtype=np.int64)
+    vis = np.minimum((sp[:, None] + t[None, :] + 1) // shape.ratio, shape.n_cols)   # [b, s]
+    n_keys = np.minimum((sp + s) // shape.ratio, shape.n_cols)                       # unique keys per sequence
+    sel = np.minimum(vis, shape.topk)
+    if shape.prefill:
+        win_valid = np.minimum(t + 1, shape.window)[None, :].repeat(b, 0)
+    else:
+        win_valid = np.minimum(sp + 1, shape.window)[:, None]
+    rows = (sel + win_valid).sum()                                                  # valid gathered rows
+    w = {}
+    w["idx_scores"] = {
+        "bytes": float(n_keys.sum() * Di * 2 + b * s * Hi * Di * 2 + b * s * Hi * 2 + b * s * shape.n_cols * 4),
+        "flops": float(2 * Hi * Di * vis.sum()),
+    }
+    w["idx_topk"] = {"bytes": float(vis.sum() * 4 + b * s * shape.topk * 4), "flops": 0.0}
+    w["window_idx"] = {"bytes": float(b * s * shape.win_width * 4), "flops": 0.0}
+    if shape.prefill:
+        kv_bytes = (shape.win_rows + n_keys.sum()) * d * 2                          # unique rows (L2 serves reuse)
+    else:
+        kv_bytes = rows * d * 2                                                     # every gathered row from HBM
+    attn = {"bytes": float(kv_bytes + 2 * b * s * h * d * 2 + b * s * shape.k_total * 4),
+            "flops": float(4 * h * d * rows)}
+    for i in range(shape.n_layers):
+        w[f"sparse_attn[{i}]"] = dict(attn)
+    return w
+
+
+def roofline_of(kernel: str, wk: dict, avg_s: float, pk: dict, workload: str) -> dict:
+    t_mem = wk["bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = wk["flops"] / (pk["bf16_tflops"] * 1e12)
+    if t_tc > t_mem:
+        achieved = wk["flops"] / avg_s / 1e12
+        out = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = wk["bytes"] / avg_s / 1e9
+        out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    out["frac"] = round(achieved / out["peak"], 4)
+    out["kernel"] = kernel
+    out["peak_source"] = pk["source"]
+    out["traffic"] = recorded_traffic(kernel.split("[")[0], workload)
+    out["algorithmic_bytes"] = int(wk["bytes"])
+    out["algorithmic_flops"] = int(wk["flops"])
+    return out
+
+
+# ---------------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = None):
+    """The path on the CPU oracle (test infrastructure), for a subset of query rows of batch
+    element 0 in prefill (rows given) or for the whole decode batch."""
+    import oracle
+
+    W = shape.window
+    if shape.prefill:
+        t = rows
+        sp = t.astype(np.int32)                 # query t of a start_pos=0 chunk sees (t+1)//ratio groups
+        iq = data["iq"][0][t][:, None]
+        w = data["w"][0][t][:, None]
+        ik = np.broadcast_to(data["ik"][0], (len(t),) + data["ik"].shape[1:])
+        score = oracle.index_score(iq, ik, w, shape.index_scale, sp, shape.n_cols, shape.ratio)
+        cidx = oracle.topk(score, sp, shape.ratio, shape.topk, shape.win_rows)
+        widx = oracle.window_topk_idxs(W, 1, shape.s, 0)[0][t][:, None]
+        idx = np.concatenate([widx, cidx], axis=-1).reshape(1, len(t), -1)
+        q = data["q"][0][0][t][None]
+        out, _ = oracle.sparse_attn(q, data["win"][0], data["sink"][0], idx, shape.softmax_scale,
+                                    kv2=data["comp"])
+        return len(t)
+    sp = data["start_pos"]
+    score = oracle.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
+    cidx = oracle.topk(score, sp, shape.ratio, shape.topk, W)
+    widx = np.concatenate([oracle.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0)
+    idx = np.concatenate([widx, cidx], axis=-1)
+    for i in range(shape.n_layers):
+        oracle.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], idx, shape.softmax_scale,
+                           kv2=data["comp"])
+    return shape.b * shape.s
+
+
+def cpu_baseline(shape: workloads.Shape, data: dict, budget_s: float = 12.0) -> dict:
+    """Oracle throughput on a bounded sample: decode runs whole batches, prefill a spread of
+    query rows; repeated until about budget_s of CPU time."""
+    import oracle
+
+    oracle.build()
+    if shape.prefill:
+        rows = np.linspace(0, shape.s - 1, 16).astype(np.int64)
+        sample = f"16 query rows spread over the {shape.s}-query prefill, repeated"
+    else:
+        rows = None
+        sample = f"the whole b={shape.b} decode batch (all {shape.n_layers} attention layer(s)), repeated"
+    done, t0 = 0, time.perf_counter()
+    reps = 0
+    while True:
+        done += oracle_step(shape, data, rows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": round(done / el, 3), "unit": "queries/s" if shape.prefill else "tokens/s",
+            "cores": oracle.default_threads(), "kind": "oracle", "sample": f"{sample} x{reps} ({el:.1f} s)"}
+
+
+# ---------------------------------------------------------------------------------- main
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi sampling (profiler runs)")
+    return ap.parse_args()
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = workloads.config(args.workload)
+    unit = "queries/s" if shape.prefill else "tokens/s"
+    cfg = {"workload": shape.name, "b": shape.b, "seqlen": shape.s, "context": int(shape.start_pos.max()) + shape.s,
+           "heads": shape.h, "head_dim": shape.d, "window": shape.window, "ratio": shape.ratio,
+           "compressed_rows": shape.n_cols, "index_heads": shape.Hi, "index_head_dim": shape.Di,
+           "index_topk": shape.topk, "attention_layers": shape.n_layers, "l2": "256 MiB written before every step"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        data = workloads.make(shape)
+        cb = cpu_baseline(shape, data)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": cb["unit"], "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    data = workloads.make(shape)
+    path = GpuPath(shape, data, device)
+    stream = torch.cuda.current_stream()
+
+    sampler = None if args.no_clocks else ClockSampler(device.index)
+    for _ in range(args.warmup):
+        path.flush_l2()
+        path.step()
+    torch.cuda.synchronize()
+    n_ev = len(path.names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        path.flush_l2()
+        path.step(evs[k])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = None
+    if sampler:
+        # keep the GPU loaded until the clock sampler has seen the load
+        t_end = time.perf_counter() + 0.6
+        while time.perf_counter() < t_end:
+            path.flush_l2()
+            path.step()
+        torch.cuda.synchronize()
+        clocks = sampler.stop()
+
+    per_kernel = {n: [] for n in path.names}
+    step_ms = []
+    for ev in evs:
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+        for i, n in enumerate(path.names):
+            per_kernel[n].append(ev[i].elapsed_time(ev[i + 1]))
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    units = shape.b * shape.s
+    value = units * args.steps * world / (total_ms / 1e3)
+    avg_us = {n: round(1e3 * statistics.mean(v), 2) for n, v in per_kernel.items()}
+
+    wk = work(shape, data)
+    pk = peaks()
+    dominant = max(avg_us, key=lambda n: avg_us[n])
+    roof = roofline_of(dominant, wk[dominant], avg_us[dominant] / 1e6, pk, shape.name)
+    others = {n: roofline_of(n, wk[n], avg_us[n] / 1e6, pk, shape.name)["frac"] for n in path.names}
+
+    # e2e: fused public entry, inputs copied from pinned host memory, output read back, every step
+    e2e = None
+    if not args.no_e2e and shape.n_layers == 1 and not shape.prefill:
+        e2e = measure_e2e(path, data, args.steps, args.warmup)
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
+            "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks}
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, data)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
+    """Decode steps through sti_decode_fused: q, index q, weights and start_pos copied in from
+    pinned host memory, the attention output copied out, synchronised every step."""
+    import torch
+
+    sti = path.sti
+    h_q = torch.from_numpy(data["q"][0].view(np.int16)).view(torch.bfloat16).reshape(path.b, -1).pin_memory()
+    h_iq = torch.from_numpy(data["iq"].view(np.int16)).view(torch.bfloat16).reshape(path.b, -1).pin_memory()
+    h_w = torch.from_numpy(data["w"].view(np.int16)).view(torch.bfloat16).reshape(path.b, -1).pin_memory()
+    h_sp = torch.from_numpy(data["start_pos"].copy()).pin_memory()
+    h_out = torch.empty(path.out[0].numel(), dtype=torch.bfloat16).pin_memory()
+    d_q = torch.empty_like(path.q[0]).reshape(path.b, -1)
+    d_iq = torch.empty_like(path.iq).reshape(path.b, -1)
+    d_w = torch.empty_like(path.w).reshape(path.b, -1)
+    d_sp = torch.empty_like(path.sp)
+    shp = path.shape
+    a, out, tk = sti.decode_args(d_q.view_as(path.q[0]), path.win[0], path.comp, path.sink[0], shp.softmax_scale,
+                                 d_iq.view_as(path.iq), path.ik, d_w.view_as(path.w), shp.index_scale, d_sp,
+                                 shp.ratio, shp.n_cols, shp.topk)
+    ws = sti.workspace(sti.decode_workspace_size(a), path.dev)
+    bi = h_q.numel() * 2 + h_iq.numel() * 2 + h_w.numel() * 2 + h_sp.numel() * 4
+    bo = h_out.numel() * 2
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        d_iq.copy_(h_iq, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        d_sp.copy_(h_sp, non_blocking=True)
+        sti.decode_fused(a, ws)
+        h_out.copy_(out.reshape(-1), non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        path.flush_l2()
+        one()
+    el = 0.0
+    for _ in range(steps):
+        path.flush_l2()
+        torch.cuda.current_stream().synchronize()
+        t0 = time.perf_counter()
+        one()
+        el += time.perf_counter() - t0
+    return {"value": round(path.b * steps / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo), "how": "sti_decode_fused, wall clock, synchronised every step"}
+
+
+if __name__ == "__main__":
+    main()
