@@ -111,22 +111,55 @@ class GpuPath:
         self.ws = sti.workspace(max(ws_attn, 256), device)
         self.splits = ws_attn > 256
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-        self.names = ["window_idx", "idx_scores", "idx_topk"] + [f"sparse_attn[{i}]" for i in range(self.L)]
+        if self.prefill:
+            self.names = ["window_idx", "idx_scores", "idx_topk"] + [f"sparse_attn[{i}]" for i in range(self.L)]
+        else:
+            # decode: the fused entry point (scores, top-k + window indices, attention), then the
+            # reuse layers' attention on the published indices
+            self.names = ["idx_scores", "idx_topk", "sparse_attn[0]"] + [f"sparse_attn[{i}]" for i in
+                                                                          range(1, self.L)]
+            self.args, _, _ = sti.decode_args(self.q[0], self.win[0], self.comp, self.sink[0], shape.softmax_scale,
+                                              self.iq, self.ik, self.w, shape.index_scale, self.sp, shape.ratio,
+                                              shape.n_cols, shape.topk,
+                                              out=self.out[0].view(self.b, shape.h, shape.d),
+                                              topk_idxs=self.idx.view(self.b, self.k_total))
+            self.dws = sti.workspace(sti.decode_workspace_size(self.args), device)
+
+    def scores_view(self):
+        """The index scores of the last step ([b, s, n_cols] fp32)."""
+        if self.prefill:
+            return self.scores
+        n = self.b * self.s * self.shape.n_cols
+        return self.dws[256:256 + 4 * n].view(self.torch.float32).view(self.b, self.s, self.shape.n_cols)
+
+    def read_status(self) -> int:
+        flags = self.sti.read_device_status(self.ws)
+        if not self.prefill:
+            flags |= self.sti.read_device_status(self.dws)
+        return flags
 
     def launches_per_step(self) -> int:
-        return 3 + self.L * (2 if self.splits else 1)
+        return 3 + self.L if self.prefill else 2 + self.L
 
     def step(self, events=None):
-        """One pass of the path; events (len = len(names)+1) are recorded around every call."""
+        """One pass of the path; events (len = len(names)+1) are recorded around every kernel."""
         sti, shp = self.sti, self.shape
         rec = (lambda i: events[i].record()) if events is not None else (lambda i: None)
+        if not self.prefill:
+            sti.decode_fused(self.args, self.dws, events=None if events is None else events[:4])
+            for i in range(1, self.L):
+                sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale,
+                                     kv2=self.comp, out=self.out[i], ws=self.ws)
+                rec(3 + i)
+            return
         rec(0)
         sti.window_idxs(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
         rec(1)
         sti.idx_scores(self.iq, self.ik, self.w, shp.index_scale, self.sp, shp.n_cols, shp.ratio, out=self.scores,
                        ws=self.ws)
         rec(2)
-        sti.idx_topk(self.scores, self.sp, shp.ratio, shp.topk, self.width, out=self.idx[..., self.width:],
+        # compressed rows follow the window source's rows: offset = s raw rows (prefill) or W slots (decode)
+        sti.idx_topk(self.scores, self.sp, shp.ratio, shp.topk, shp.win_rows, out=self.idx[..., self.width:],
                      ws=self.ws)
         rec(3)
         for i in range(self.L):
@@ -161,6 +194,8 @@ def work(shape: workloads.Shape, data: dict) -> dict:
     }
     w["idx_topk"] = {"bytes": float(vis.sum() * 4 + b * s * shape.topk * 4), "flops": 0.0}
     w["window_idx"] = {"bytes": float(b * s * shape.win_width * 4), "flops": 0.0}
+    if not shape.prefill:   # the decode top-k kernel also writes the window indices
+        w["idx_topk"]["bytes"] += w.pop("window_idx")["bytes"]
     if shape.prefill:
         kv_bytes = (shape.win_rows + n_keys.sum()) * d * 2                          # unique rows (L2 serves reuse)
     else:

@@ -22,9 +22,10 @@
  *    start_pos != 0 with seqlen > 1) set bits in the workspace's status word; the call still
  *    completes (bad indices are treated as masked).  sti_read_device_status reports them.
  *  - `ws` is a caller-owned device workspace of at least the size the matching
- *    sti_*_workspace_size() returns, aligned to 256 bytes.  Its first 4 bytes (the status
- *    word) must be zero before the first call; sti_read_device_status clears them again.
- *    Calls that share one workspace must not overlap on the device.
+ *    sti_*_workspace_size() returns, aligned to 256 bytes.  It must be zero-filled once
+ *    after allocation; the library leaves the parts that must start at zero at zero
+ *    (sti_read_device_status clears the status word).  Calls that share one workspace must
+ *    not overlap on the device.
  *  - Returns STI_ERR_CUDA if a launch fails (the CUDA error is in sti_last_cuda_error()).
  */
 #ifndef STI_H_
@@ -144,10 +145,11 @@ sti_status sti_idx_topk(const float *scores, const int32_t *start_pos, int b, in
  *   lse: optional fp32 [b, seqlen, h] = ln(sum_i e^{s_i} + e^{sink}); -inf for a query with
  *        no valid slot; may be NULL.
  * Indices < -1 or >= n1+n2 are treated as masked and raise STI_FLAG_INDEX_RANGE.
+ * With few queries (decode) a query's slots are split over a thread-block cluster of up to 8
+ * CTAs whose partial results are merged in distributed shared memory; nothing but the status
+ * word is kept in the workspace.
  * Supported: 1 <= h <= 64, d a multiple of 64 up to 512, k >= 1, kv_bstride/kv2_bstride
- * multiples of 8.  ws: sti_sparse_attn_workspace_size(b, seqlen, h, d, k) bytes (it holds
- * split-KV partials when there are few queries; the size depends on the current device's
- * SM count).
+ * multiples of 8.  ws: sti_sparse_attn_workspace_size(b, seqlen, h, d, k) bytes.
  */
 size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k);
 sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,
@@ -159,11 +161,12 @@ sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t k
 /*
  * One decode step (seqlen == 1) of an index-source attention layer, as
  * Attention.forward -> _window_kv / _compress_kv -> _compress_topk_idxs -> Indexer ->
- * sparse_attn composes it, enqueued back to back on one stream:
- *   1. window indices of the W-slot ring (sti_window_idxs, decode branch) -> topk_idxs[:, :W]
- *   2. index scores over the n_cols compressed positions (sti_idx_scores) -> workspace
- *   3. top-k of the visible positions, + offset W (sti_idx_topk) -> topk_idxs[:, W:W+k]
- *   4. sparse sink attention over [ring ; compressed KV] (sti_sparse_attn_sink)
+ * sparse_attn composes it, three kernels enqueued back to back on one stream:
+ *   1. index scores over the n_cols compressed positions (as sti_idx_scores) -> workspace; the
+ *      kernel also counts the scores' top 11 key bits, the first radix pass of the top-k
+ *   2. top-k of the visible positions, + offset W (as sti_idx_topk) -> topk_idxs[:, W:W+k],
+ *      and the W-slot ring's window indices (as sti_window_idxs) -> topk_idxs[:, :W]
+ *   3. sparse sink attention over [ring ; compressed KV] (as sti_sparse_attn_sink)
  * Ragged batches: start_pos is per sequence, compress_len = (start_pos+1)//ratio.
  * topk_idxs ([b, W+k] int32) is an output the caller owns, so reuse layers can consume it
  * through sti_sparse_attn_sink without running the Indexer (_compress_topk_idxs).
@@ -193,8 +196,11 @@ typedef struct sti_decode_args {
     int32_t *topk_idxs;         /* int32 [b, W + index_topk] */
 } sti_decode_args;
 
+/* events: NULL, or 4 cudaEvent_t handles recorded on `stream` before step 1 and after steps
+ * 1, 2 and 3 (per-kernel timing). */
 size_t sti_decode_workspace_size(const sti_decode_args *a);
-sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream);
+sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream,
+                            void *const *events);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libsti.so")
+# STI_LIB selects another build of the same library (for example one compiled with other
+# tuning macros); by default the in-tree libsti.so
+LIB_PATH = os.environ.get("STI_LIB") or os.path.join(_HERE, "libsti.so")
 
 STATUS_NAMES = {0: "STI_OK", 1: "STI_ERR_INVALID_ARG", 2: "STI_ERR_UNSUPPORTED", 3: "STI_ERR_CUDA",
                 4: "STI_ERR_INDEX_RANGE", 5: "STI_ERR_DEVICE_TIMEOUT", 6: "STI_ERR_DEVICE_UNSUPPORTED"}
@@ -78,7 +80,7 @@ def lib() -> ctypes.CDLL:
         L.sti_sparse_attn_sink.restype = I
         L.sti_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.sti_decode_workspace_size.restype = SZ
-        L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P]
+        L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
         L.sti_decode_fused.restype = I
         _lib = L
     return _lib
@@ -240,6 +242,14 @@ def decode_workspace_size(a: DecodeArgs) -> int:
     return int(lib().sti_decode_workspace_size(ctypes.byref(a)))
 
 
-def decode_fused(a: DecodeArgs, ws: torch.Tensor, stream=None):
-    """One decode step of an index-source layer: window indices, scores, top-k, sparse attention."""
-    _check(lib().sti_decode_fused(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "sti_decode_fused")
+def decode_fused(a: DecodeArgs, ws: torch.Tensor, stream=None, events=None):
+    """One decode step of an index-source layer: scores, top-k with window indices, sparse
+    attention.  `events`: optional 4 torch.cuda.Event(enable_timing=True), recorded before
+    the first kernel and after each of the three."""
+    ev = None
+    if events is not None:
+        for e in events:
+            if e.cuda_event == 0:   # torch creates the event on first record
+                e.record()
+        ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    _check(lib().sti_decode_fused(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream), ev), "sti_decode_fused")

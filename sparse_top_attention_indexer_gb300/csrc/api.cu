@@ -99,7 +99,8 @@ static sti_status window_impl(const int32_t* start_pos, int b, int seqlen, int w
 
 static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_t ik_bstride, const uint16_t* w,
                                   float c, const int32_t* start_pos, int b, int seqlen, int Hi, int Di, int n_cols,
-                                  int ratio, float* scores, uint32_t* status, cudaStream_t st) {
+                                  int ratio, float* scores, uint32_t* status, cudaStream_t st,
+                                  uint32_t* hist = nullptr) {
     if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1) return STI_ERR_INVALID_ARG;
     if (!(Di == 32 || Di == 64 || Di == 128)) return STI_ERR_UNSUPPORTED;
     if (!(Hi == 4 || Hi == 8 || Hi == 16 || Hi == 32 || Hi == 64)) return STI_ERR_UNSUPPORTED;
@@ -113,6 +114,7 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     p.w = w;
     p.start_pos = start_pos;
     p.scores = scores;
+    p.hist = hist;
     p.status = status;
     p.c = c;
     p.B = b;
@@ -130,7 +132,10 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     p.tmem_cols = cols;
     p.total_units = b * p.QT;
     const size_t a_bytes = (size_t)128 * Di * 2, b_bytes = (size_t)p.n_pad * Di * 2;
-    const size_t budget = 200 * 1024;
+    // Two CTAs per SM stream faster than one with the same total stage count (two independent
+    // TMA producers); possible when both CTAs' accumulators fit the SM's 512 TMEM columns.
+    p.ctas_per_sm = p.tmem_cols <= 256 ? 2 : 1;
+    const size_t budget = p.ctas_per_sm == 2 ? 104 * 1024 : 200 * 1024;
     int stages = (int)((budget - b_bytes) / a_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
@@ -151,32 +156,37 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
 
 static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b, int seqlen, int n_cols, int ratio,
                             int k, int32_t offset, int32_t* idxs, int64_t row_stride, uint32_t* status,
-                            cudaStream_t st) {
+                            cudaStream_t st, uint32_t* hist = nullptr, int32_t* win_out = nullptr, int win_W = 0,
+                            int win_width = 0) {
     if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1 || k < 1 || row_stride < k) return STI_ERR_INVALID_ARG;
     if (k > 4096) return STI_ERR_UNSUPPORTED;
     if ((int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
     if (!start_pos || !idxs || (n_cols > 0 && !scores)) return STI_ERR_INVALID_ARG;
-    cudaError_t e = sti::launch_topk(scores, start_pos, b, seqlen, n_cols, ratio, k, offset, idxs, row_stride,
-                                     status, st);
+    sti::TopkParams p{};
+    p.scores = scores;
+    p.start_pos = start_pos;
+    p.idxs = idxs;
+    p.row_stride = row_stride;
+    p.hist = hist;
+    p.win_out = win_out;
+    p.status = status;
+    p.B = b;
+    p.s = seqlen;
+    p.n_cols = n_cols;
+    p.ratio = ratio;
+    p.k = k;
+    p.offset = offset;
+    p.win_W = win_W;
+    p.win_width = win_width;
+    cudaError_t e = sti::launch_topk(p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_idx_topk");
-}
-
-static int attn_splits_for(int n_queries, int k) {
-    const int n_tiles = (k + 127) / 128;
-    const int splits = sti::attn_pick_splits(n_queries, n_tiles, sti::device_num_sms());
-    const int tps = (n_tiles + splits - 1) / splits;
-    return (n_tiles + tps - 1) / tps;   // no empty split
-}
-
-static size_t attn_ws_bytes(int n_queries, int splits, int d) {
-    return sti::kWsStatusBytes + sti::align_up(sti::attn_partials_bytes(n_queries, splits, d), sti::kWsAlign);
 }
 
 static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
                             int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
-                            uint16_t* out, float* lse, uint8_t* ws, size_t ws_bytes, cudaStream_t st) {
+                            uint16_t* out, float* lse, uint32_t* status, cudaStream_t st) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
@@ -186,10 +196,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
         (n2 > 0 && (kv2_bstride < (int64_t)n2 * d || kv2_bstride % 8)))
         return STI_ERR_INVALID_ARG;
     if (!aligned(q, 16) || (kv && !aligned(kv, 16)) || (kv2 && !aligned(kv2, 16))) return STI_ERR_INVALID_ARG;
-    if ((int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
+    if ((int64_t)b * seqlen * 8 > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
     const int nq = b * seqlen;
-    const int splits = attn_splits_for(nq, k);
-    if (ws_bytes < attn_ws_bytes(nq, splits, d)) return STI_ERR_INVALID_ARG;
 
     sti::AttnParams p{};
     p.q = q;
@@ -199,7 +207,7 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.idx = idxs;
     p.out = out;
     p.lse = lse;
-    p.status = reinterpret_cast<uint32_t*>(ws);
+    p.status = status;
     p.kv_bstride = kv_bstride;
     p.kv2_bstride = kv2_bstride;
     p.idx_stride = idx_row_stride;
@@ -212,14 +220,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.d = d;
     p.k = k;
     p.d_pad = ((d + 127) / 128) * 128;
-    p.n_tiles = (k + 127) / 128;
-    p.splits = splits;
-    p.tiles_per_split = (p.n_tiles + splits - 1) / splits;
-    if (splits > 1) {
-        float* part = reinterpret_cast<float*>(ws + sti::kWsStatusBytes);
-        p.part_ml = part;
-        p.part_o = part + (size_t)nq * splits * 2 * 64;
-    }
+    p.cluster = sti::attn_pick_cluster(nq, k);
+    p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     cudaError_t e = sti::launch_sparse_attn(p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
@@ -287,10 +289,12 @@ sti_status sti_idx_topk(const float* scores, const int32_t* start_pos, int b, in
 }
 
 size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k) {
+    (void)b;
+    (void)seqlen;
     (void)h;
-    if (b <= 0 || seqlen <= 0 || d <= 0 || k <= 0) return sti::kWsStatusBytes;
-    const int nq = b * seqlen;
-    return attn_ws_bytes(nq, attn_splits_for(nq, k), d);
+    (void)d;
+    (void)k;
+    return sti::kWsStatusBytes;
 }
 
 sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
@@ -299,22 +303,22 @@ sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t k
                                 uint16_t* out, float* lse, void* ws, size_t ws_bytes, sti_stream stream) {
     if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
     return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
-                     seqlen, h, d, k, out, lse, static_cast<uint8_t*>(ws), ws_bytes,
-                     static_cast<cudaStream_t>(stream));
+                     seqlen, h, d, k, out, lse, status_word(ws), static_cast<cudaStream_t>(stream));
 }
 
+// fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048]]
 static size_t decode_scores_bytes(const sti_decode_args* a) {
     return sti::align_up((size_t)a->b * (size_t)(a->n_cols > 0 ? a->n_cols : 1) * sizeof(float), sti::kWsAlign);
 }
+static size_t decode_hist_bytes(const sti_decode_args* a) { return (size_t)a->b * 2048 * sizeof(uint32_t); }
 
 size_t sti_decode_workspace_size(const sti_decode_args* a) {
     if (!a || a->b <= 0) return sti::kWsStatusBytes;
-    const int k_total = a->window_size + a->index_topk;
-    // [status | attention partials | scores]
-    return sti_sparse_attn_workspace_size(a->b, 1, a->h, a->d, k_total) + decode_scores_bytes(a);
+    return sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a);
 }
 
-sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream) {
+sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream,
+                            void* const* events) {
     if (!a) return STI_ERR_INVALID_ARG;
     if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
     if (a->b == 0) return STI_OK;
@@ -324,21 +328,30 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     uint32_t* status = status_word(ws);
     const int W = a->window_size, K = a->index_topk, k_total = W + K;
-    const size_t attn_ws = sti_sparse_attn_workspace_size(a->b, 1, a->h, a->d, k_total);
-    float* scores = reinterpret_cast<float*>(wsb + attn_ws);
-
-    sti_status s = window_impl(a->start_pos, a->b, 1, W, a->topk_idxs, k_total, nullptr, status, st);
-    if (s != STI_OK) return s;
+    float* scores = reinterpret_cast<float*>(wsb + sti::kWsStatusBytes);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + sti::kWsStatusBytes + decode_scores_bytes(a));
+    auto mark = [&](int i) -> cudaError_t {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+    };
+    cudaError_t e = mark(0);
+    if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    sti_status s = STI_OK;
     if (a->n_cols > 0) {
         s = idx_scores_impl(a->iq, a->ik, a->ik_bstride, a->w, a->index_scale, a->start_pos, a->b, 1, a->Hi, a->Di,
-                            a->n_cols, a->ratio, scores, status, st);
+                            a->n_cols, a->ratio, scores, status, st, hist);
         if (s != STI_OK) return s;
     }
-    s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st);
+    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    // top-k of the compressed positions (+W) and the ring's window indices, one kernel
+    s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
+                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W);
     if (s != STI_OK) return s;
-    return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
-                     a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, wsb,
-                     attn_ws, st);
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
+                  a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, st);
+    if (s != STI_OK) return s;
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    return STI_OK;
 }
 
 }  // extern "C"

@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_bar_sync(1, 128);
                 cur_unit = u;
             }
-            const bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
+            bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
+            ok = __all_sync(kFull, ok);   // warp-uniform: the loop below holds warp collectives
             if (!ok) atomicExch(&bars->abort, 1u);
             tc_fence_after();
             const int key = tile * kTileKeys + quarter * 32 + lane;
@@ -307,14 +308,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sacc[qq] = fmaf(w_s[(q0 + qq) * HI + hh], v, sacc[qq]);
                         }
                     }
-                    if (key < p.n_cols) {
 #pragma unroll
-                        for (int qq = 0; qq < QPC; ++qq) {
-                            const int q = q0 + qq;
-                            if (q < nq_here) {
-                                float* dst = p.scores + ((size_t)b * p.s + t0 + q) * p.n_cols + key;
-                                *dst = key < vis_s[q] ? sacc[qq] : -INFINITY;
-                            }
+                    for (int qq = 0; qq < QPC; ++qq) {
+                        const int q = q0 + qq;
+                        const bool in_row = q < nq_here && key < p.n_cols;
+                        const bool visible = in_row && key < vis_s[q];
+                        if (in_row) p.scores[((size_t)b * p.s + t0 + q) * p.n_cols + key] = visible ? sacc[qq] : -INFINITY;
+                        if (p.hist != nullptr) {
+                            // first radix pass of the top-k: top 11 bits of the order-preserving key,
+                            // one aggregated shared-L2 atomic per distinct bin in the warp
+                            const uint32_t dig = visible ? (float_key(sacc[qq]) >> 21) : 0xFFFFFFFFu;
+                            const unsigned peers = __match_any_sync(kFull, dig);
+                            if (visible && lane == __ffs(peers) - 1)
+                                atomicAdd(p.hist + ((size_t)b * p.s + t0 + q) * 2048 + dig, (uint32_t)__popc(peers));
                         }
                     }
                 }
@@ -368,9 +374,11 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
 cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const IdxScoresParams& p,
                               int num_sms, cudaStream_t stream) {
     size_t smem = idx_scores_smem_bytes(p);
-    // keep one CTA per SM: the kernel's TMEM demand assumes it owns the SM's TMEM
-    if (smem < 120 * 1024) smem = 120 * 1024;
-    const int grid = num_sms;
+    // p.ctas_per_sm CTAs share an SM (together they fit the SM's 512 TMEM columns); pad shared
+    // memory so no more than that many become resident
+    const size_t floor_smem = (size_t)(228 * 1024 / (p.ctas_per_sm + 1)) + 1024;
+    if (smem < floor_smem) smem = floor_smem;
+    const int grid = num_sms * p.ctas_per_sm;
     cudaError_t err = cudaSuccess;
 #define STI_LAUNCH_HI(HV)                                                                              \
     case HV: {                                                                                         \

@@ -22,6 +22,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kWarps = kTopkThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kSmemKeyCap = 32768;   // rows up to this many visible positions are staged in shared memory
+constexpr int kCandCap = 4096;       // threshold-bin members kept for passes 2 and 3
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __global__ void window_idx_kernel(const int32_t* __restrict__ start_pos, int B, int s, int W, int width,
@@ -76,51 +77,36 @@ __device__ __forceinline__ int block_excl_scan(int v, int* warp_tot, int& total)
     return wpre + inc - v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_kernel(const float* __restrict__ scores, const int32_t* __restrict__ start_pos, int s, int n_cols,
-                int ratio, int k, int32_t offset, int32_t* __restrict__ idxs, int64_t row_stride, int use_smem) {
-    extern __shared__ uint32_t sm[];
-    uint32_t* hist = sm;                                      // [kBins]
-    int* warp_tot = reinterpret_cast<int*>(sm + kBins);       // [kWarps]
-    int* misc = warp_tot + kWarps;                            // [8]
-    uint32_t* keys = sm + kBins + kWarps + 8;                 // [vis] when staged
-
-    const int row = blockIdx.x;
-    const int b = row / s, t = row - b * s;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int vis = (__ldg(start_pos + b) + t + 1) / ratio;
-    vis = max(0, min(vis, n_cols));
-    int32_t* out = idxs + (int64_t)row * row_stride;
-
-    if (vis <= k) {  // every visible position is selected
-        for (int i = tid; i < k; i += kTopkThreads) out[i] = i < vis ? i + offset : -1;
-        return;
+// Value of window slot i for query (b, t) (get_window_topk_idxs): prefill band when s > 1,
+// decode ring otherwise; -1 for slots that hold nothing.
+__device__ __forceinline__ int window_slot(int s, int t, int sp, int W, int i) {
+    if (s > 1) {
+        const int idx = max(0, t - W + 1) + i;
+        return (sp != 0 || idx > t) ? -1 : idx;
     }
+    const int oldest = sp % W + 1;
+    const int idx = i < W - oldest ? oldest + i : i - (W - oldest);
+    return idx > sp ? -1 : idx;
+}
 
-    const float* src = scores + (int64_t)row * n_cols;
-    if (use_smem) {
-        for (int j = tid; j < vis; j += kTopkThreads) keys[j] = float_key(__ldg(src + j));
-        __syncthreads();
-    }
-    auto key_at = [&](int j) -> uint32_t { return use_smem ? keys[j] : float_key(__ldg(src + j)); };
-
-    uint32_t prefix = 0;
-    int remaining = k;   // how many still to take at or below the current prefix
-    int shift = 32;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int bits = pass < 2 ? 11 : 10;
-        const int hi_shift = shift;   // bits above the digit are already fixed in `prefix`
-        shift -= bits;
-        const uint32_t mask = (1u << bits) - 1u;
+// Histogram of digit (key >> shift) & mask over the n keys from `src` whose bits above
+// hi_shift equal `prefix`, then the bin d* where the count from the top first reaches
+// `remaining`: returns d* and the number of matching keys in higher bins (via *above).
+template <typename Src>
+__device__ __forceinline__ int radix_pass(Src src, int n, int hi_shift, int shift, int bits, uint32_t prefix,
+                                          int remaining, uint32_t* hist, int* warp_tot, int* misc, int* above_out,
+                                          bool hist_ready) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t mask = (1u << bits) - 1u;
+    if (!hist_ready) {
         for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0;
         __syncthreads();
-        for (int base = 0; base < vis; base += kTopkThreads) {
+        for (int base = 0; base < n; base += kTopkThreads) {
             const int j = base + tid;
             bool m = false;
             uint32_t dig = 0xFFFFFFFFu;
-            if (j < vis) {
-                const uint32_t key = key_at(j);
+            if (j < n) {
+                const uint32_t key = src(j);
                 m = hi_shift >= 32 ? true : ((key >> hi_shift) == prefix);
                 if (m) dig = (key >> shift) & mask;
             }
@@ -128,28 +114,112 @@ __global__ void __launch_bounds__(kTopkThreads)
             if (m && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
         }
         __syncthreads();
-        // bins owned by this thread: 4*tid .. 4*tid+3; entries above them = total - inclusive
-        int local = 0;
+    }
+    int local = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) local += (int)hist[4 * tid + i];
-        int total;
-        const int excl = block_excl_scan(local, warp_tot, total);
-        int above = total - excl - local;
+    for (int i = 0; i < 4; ++i) local += (int)hist[4 * tid + i];
+    int total;
+    const int excl = block_excl_scan(local, warp_tot, total);
+    int above = total - excl - local;   // matching keys in bins above this thread's 4 bins
 #pragma unroll
-        for (int i = 3; i >= 0; --i) {
-            const int bin = 4 * tid + i;
-            const int c = (int)hist[bin];
-            if (above < remaining && above + c >= remaining) {
-                misc[0] = bin;
-                misc[1] = above;
-            }
-            above += c;
+    for (int i = 3; i >= 0; --i) {
+        const int bin = 4 * tid + i;
+        const int c = (int)hist[bin];
+        if (above < remaining && above + c >= remaining) {
+            misc[0] = bin;
+            misc[1] = above;
+        }
+        above += c;
+    }
+    __syncthreads();
+    const int d = misc[0];
+    *above_out = misc[1];
+    __syncthreads();
+    return d;
+}
+
+template <bool HAS_HIST>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, int use_smem) {
+    extern __shared__ uint32_t sm[];
+    uint32_t* hist = sm;                                      // [kBins]
+    int* warp_tot = reinterpret_cast<int*>(sm + kBins);       // [kWarps]
+    int* misc = warp_tot + kWarps;                            // [8]
+    uint32_t* cand = sm + kBins + kWarps + 8;                 // [kCandCap] keys of the threshold bin
+    uint32_t* keys = cand + kCandCap;                         // [vis] when staged
+
+    const int row = blockIdx.x;
+    const int b = row / p.s, t = row - b * p.s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sp = __ldg(p.start_pos + b);
+    if (p.win_out != nullptr) {
+        int32_t* wrow = p.win_out + (int64_t)row * p.row_stride;
+        for (int i = tid; i < p.win_width; i += kTopkThreads) wrow[i] = window_slot(p.s, t, sp, p.win_W, i);
+        if (tid == 0 && p.s > 1 && sp != 0 && p.status) atomicOr(p.status, 4u /* STI_FLAG_CHUNKED */);
+    }
+    int vis = (sp + t + 1) / p.ratio;
+    vis = max(0, min(vis, p.n_cols));
+    int32_t* out = p.idxs + (int64_t)row * p.row_stride;
+    uint32_t* ghist = HAS_HIST ? p.hist + (size_t)row * kBins : nullptr;
+
+    if (vis <= p.k) {  // every visible position is selected
+        for (int i = tid; i < p.k; i += kTopkThreads) out[i] = i < vis ? i + p.offset : -1;
+        if (HAS_HIST)
+            for (int i = tid; i < kBins; i += kTopkThreads) ghist[i] = 0;
+        return;
+    }
+
+    const float* src = p.scores + (int64_t)row * p.n_cols;
+    if (use_smem) {
+        for (int j = tid; j < vis; j += kTopkThreads) keys[j] = float_key(__ldg(src + j));
+    }
+    if (HAS_HIST) {
+        for (int i = tid; i < kBins; i += kTopkThreads) {
+            hist[i] = ghist[i];
+            ghist[i] = 0;   // ready for the next call
+        }
+    }
+    __syncthreads();
+    auto key_at = [&](int j) -> uint32_t { return use_smem ? keys[j] : float_key(__ldg(src + j)); };
+
+    // pass 1: top 11 bits over the whole row (histogram precomputed by the scores kernel, or here)
+    int above;
+    const int d1 = radix_pass(key_at, vis, 32, 21, 11, 0u, p.k, hist, warp_tot, misc, &above, HAS_HIST);
+    int remaining = p.k - above;
+    uint32_t prefix = (uint32_t)d1;
+    const int c1 = (int)hist[d1];
+    __syncthreads();
+    if (c1 <= kCandCap) {
+        // passes 2 and 3 only look at the keys of bin d1: gather them first
+        if (tid == 0) misc[2] = 0;
+        __syncthreads();
+        for (int base = 0; base < vis; base += kTopkThreads) {
+            const int j = base + tid;
+            const uint32_t key = j < vis ? key_at(j) : 0u;
+            const bool m = j < vis && (key >> 21) == (uint32_t)d1;
+            const unsigned bal = __ballot_sync(kFull, m);
+            int wbase = 0;
+            if (lane == 0 && bal) wbase = atomicAdd(&misc[2], __popc(bal));
+            wbase = __shfl_sync(kFull, wbase, 0);
+            const int at = wbase + __popc(bal & ((1u << lane) - 1u));
+            if (m && at < kCandCap) cand[at] = key;
         }
         __syncthreads();
-        const int dstar = misc[0];
-        remaining -= misc[1];
-        prefix = (prefix << bits) | (uint32_t)dstar;
-        __syncthreads();
+    }
+    if (c1 <= kCandCap && misc[2] == c1) {
+        auto cand_at = [&](int j) -> uint32_t { return cand[j]; };
+        const int d2 = radix_pass(cand_at, c1, 21, 10, 11, prefix, remaining, hist, warp_tot, misc, &above, false);
+        remaining -= above;
+        prefix = (prefix << 11) | (uint32_t)d2;
+        const int d3 = radix_pass(cand_at, c1, 10, 0, 10, prefix, remaining, hist, warp_tot, misc, &above, false);
+        remaining -= above;
+        prefix = (prefix << 10) | (uint32_t)d3;
+    } else {
+        const int d2 = radix_pass(key_at, vis, 21, 10, 11, prefix, remaining, hist, warp_tot, misc, &above, false);
+        remaining -= above;
+        prefix = (prefix << 11) | (uint32_t)d2;
+        const int d3 = radix_pass(key_at, vis, 10, 0, 10, prefix, remaining, hist, warp_tot, misc, &above, false);
+        remaining -= above;
+        prefix = (prefix << 10) | (uint32_t)d3;
     }
     const uint32_t tau = prefix;
     const int need_eq = remaining;   // >= 1 keys equal to tau are taken, lowest positions first
@@ -184,7 +254,8 @@ __global__ void __launch_bounds__(kTopkThreads)
         const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
         const bool take = gt || (eq && eq_rank < eq_take);
         const unsigned take_mask = __ballot_sync(kFull, take);
-        if (take) out[pos + __popc(take_mask & ((1u << lane) - 1u))] = j + offset;
+        const int at = pos + __popc(take_mask & ((1u << lane) - 1u));
+        if (take && at < p.k) out[at] = j + p.offset;
         pos += __popc(take_mask);
         eq_seen += __popc(eq_mask);
     }
@@ -203,17 +274,15 @@ cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, in
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* scores, const int32_t* start_pos, int B, int s, int n_cols, int ratio, int k,
-                        int32_t offset, int32_t* idxs, int64_t row_stride, uint32_t* /*status*/,
-                        cudaStream_t stream) {
-    const int rows = B * s;
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
+    const int rows = p.B * p.s;
     if (rows == 0) return cudaSuccess;
-    const int use_smem = n_cols <= kSmemKeyCap ? 1 : 0;
-    const size_t smem = (size_t)(kBins + kWarps + 8 + (use_smem ? n_cols : 0)) * 4;
-    cudaError_t err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int use_smem = p.n_cols <= kSmemKeyCap ? 1 : 0;
+    const size_t smem = (size_t)(kBins + kWarps + 8 + kCandCap + (use_smem ? p.n_cols : 0)) * 4;
+    auto kern = p.hist != nullptr ? topk_kernel<true> : topk_kernel<false>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    topk_kernel<<<rows, kTopkThreads, smem, stream>>>(scores, start_pos, s, n_cols, ratio, k, offset, idxs,
-                                                       row_stride, use_smem);
+    kern<<<rows, kTopkThreads, smem, stream>>>(p, use_smem);
     return cudaGetLastError();
 }
 

@@ -20,11 +20,17 @@
 //     shared-memory tile as an MN-major A operand -- K and V are one row, fetched once.
 //     O^T lives in TMEM (d/128 blocks of 128 lanes x 64 columns); rescaling when a head's
 //     running max grows is a TMEM load-scale-store by the owning thread.
-//   * Few queries (decode) split a query's tiles over several CTAs, each writing its
-//     unnormalised partial (O, running max, running sum) to the workspace; a combine kernel merges
-//     the partials with the sink (flash-decoding style).  Many queries write the output directly.
+//   * Few queries (decode) split a query's index slots over a thread-block cluster of up to 8
+//     CTAs (one wave on the GPU).  Each CTA runs the online softmax over its slots; the cluster
+//     then exchanges running maxima and sums through distributed shared memory, every CTA scales
+//     its O^T by 2^(m_cta - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)) into its own shared
+//     memory, and each CTA sums a slice of d across the cluster and writes it -- no partials in
+//     global memory and no second kernel.  Many queries use one CTA per query.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <mutex>
+#include <vector>
 
 #include "sti_internal.h"
 #include "sti_ptx.cuh"
@@ -87,10 +93,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     AttnSmemTail* tl = reinterpret_cast<AttnSmemTail*>(p_s + kRows * 128);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int query = blockIdx.x, split = blockIdx.y;
+    const int C = p.cluster;
+    const int query = blockIdx.x / C, rank = blockIdx.x - (blockIdx.x / C) * C;   // rank in the cluster
     const int b = query / p.s;
-    const int tile_begin = split * p.tiles_per_split;
-    const int tile_end = min(p.n_tiles, tile_begin + p.tiles_per_split);
+    const int slot_begin = min(p.k, rank * p.rows_per_cta);
+    const int slot_end = min(p.k, slot_begin + p.rows_per_cta);
+    const int tile_begin = 0;
+    const int tile_end = (slot_end - slot_begin + kRows - 1) / kRows;
 
     if (warp == 0) {
         tmem_alloc(&tl->tmem_base, 512);
@@ -135,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     for (int tile = tile_begin; tile < tile_end; ++tile) {
         // ---- gather: thread r resolves slot r of the tile
         {
-            const int slot = tile * kRows + tid;
-            int idx = slot < p.k ? __ldg(idx_row + slot) : -1;
+            const int slot = slot_begin + tile * kRows + tid;
+            int idx = slot < slot_end ? __ldg(idx_row + slot) : -1;
             if (idx < -1 || idx >= n_rows) {
                 atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
                 idx = -1;
@@ -280,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     cp_async_wait<0>();   // Q's copy when this CTA had no tile
     __syncthreads();
     const bool has_tiles = tile_begin < tile_end && !dead;
-    if (p.splits == 1) {
+    if (C == 1) {
         // final: o = O / (l + 2^(sink*log2e - m)); empty rows (m = -inf) give 0
         if (tid < kHp) {
             const float m = tl->m_run[tid];
@@ -320,12 +329,29 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
             }
         }
     } else {
-        const size_t part = (size_t)query * p.splits + split;
+        // ---- cluster reduction through distributed shared memory
+        if (!has_tiles && tid < kHp) tl->m_run[tid] = -INFINITY;   // nothing valid here
+        cluster_sync();                                            // every CTA's m, l are final
         if (tid < kHp) {
-            p.part_ml[part * 2 * kHp + tid] = has_tiles ? tl->m_run[tid] : -INFINITY;
-            p.part_ml[part * 2 * kHp + kHp + tid] = has_tiles ? tl->l_run[tid] : 0.f;
+            float M = -INFINITY;
+            for (int r = 0; r < C; ++r) M = fmaxf(M, ld_dsmem_f32(dsmem_addr(&tl->m_run[tid], (uint32_t)r)));
+            float L = 0.f;
+            if (M != -INFINITY) {
+                for (int r = 0; r < C; ++r) {
+                    const float mr = ld_dsmem_f32(dsmem_addr(&tl->m_run[tid], (uint32_t)r));
+                    if (mr != -INFINITY) L += ld_dsmem_f32(dsmem_addr(&tl->l_run[tid], (uint32_t)r)) * exp2f(mr - M);
+                }
+                if (tid < p.h) L += exp2f(__ldg(p.sink + tid) * kLog2e - M);
+            }
+            const float mo = tl->m_run[tid];
+            tl->alpha[tid] = (M == -INFINITY || mo == -INFINITY || L == 0.f) ? 0.f : exp2f(mo - M) / L;
+            if (rank == 0 && p.lse && tid < p.h)
+                p.lse[(size_t)query * p.h + tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
         }
-        float* po = p.part_o + part * (size_t)p.h * p.d;
+        __syncthreads();
+        // this CTA's normalised share of O^T -> own shared memory (the KV tile is free now):
+        // row dd holds 64 heads as 16 chunks of 4 floats, chunk c stored at c ^ (dd & 15)
+        float* dump = reinterpret_cast<float*>(kv_s);
         for (int m = 0; m < nmb; ++m) {
             const int dd = 128 * m + tid;
 #pragma unroll
@@ -338,15 +364,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = 0u;
                 }
-                if (dd < p.d) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int hh = 32 * half + i;
-                        if (hh < p.h) po[(size_t)hh * p.d + dd] = __uint_as_float(r[i]);
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    const int hc = 8 * half + c;
+                    float4 v;
+                    v.x = __uint_as_float(r[4 * c + 0]) * tl->alpha[4 * hc + 0];
+                    v.y = __uint_as_float(r[4 * c + 1]) * tl->alpha[4 * hc + 1];
+                    v.z = __uint_as_float(r[4 * c + 2]) * tl->alpha[4 * hc + 2];
+                    v.w = __uint_as_float(r[4 * c + 3]) * tl->alpha[4 * hc + 3];
+                    *reinterpret_cast<float4*>(dump + (size_t)dd * kHp + ((hc ^ (dd & 15)) << 2)) = v;
                 }
             }
         }
+        cluster_sync();   // every CTA's share is in its shared memory
+        // CTA `rank` sums d in [rank*dper, (rank+1)*dper) over the cluster and writes the output
+        const int dper = (p.d + C - 1) / C;
+        const int d_lo = rank * dper, d_hi = min(p.d, d_lo + dper);
+        uint16_t* orow = p.out + (size_t)query * p.h * p.d;
+        const int n_hc = (p.h + 3) / 4;
+        for (int dd = d_lo + tid; dd < d_hi; dd += kThreads) {
+            for (int hc = 0; hc < n_hc; ++hc) {
+                const float* loc = dump + (size_t)dd * kHp + ((hc ^ (dd & 15)) << 2);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int r = 0; r < C; ++r) {
+                    const float4 v = ld_dsmem_f4(dsmem_addr(loc, (uint32_t)r));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int hh = 4 * hc + j;
+                    if (hh < p.h) orow[(size_t)hh * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(a4[j]));
+                }
+            }
+        }
+        cluster_sync();   // partners finished reading this CTA's shared memory
     }
 
     tc_fence_before();
@@ -357,53 +412,61 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     }
 }
 
-// Merge the split partials of one (query, head):
-//   o = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(sink*log2e - M)),  M = max_s m_s.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnParams p) {
-    const int query = blockIdx.x, hh = blockIdx.y;
-    const float* ml = p.part_ml + (size_t)query * p.splits * 2 * kHp;
-    float M = -INFINITY;
-    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, ml[sp * 2 * kHp + hh]);
-    float den = 0.f;
-    if (M != -INFINITY) {
-        for (int sp = 0; sp < p.splits; ++sp) {
-            const float m = ml[sp * 2 * kHp + hh];
-            if (m != -INFINITY) den += ml[sp * 2 * kHp + kHp + hh] * exp2f(m - M);
-        }
-        den += exp2f(__ldg(p.sink + hh) * kLog2e - M);
-    }
-    const float inv = (M == -INFINITY) ? 0.f : 1.f / den;
-    if (p.lse && threadIdx.x == 0)
-        p.lse[(size_t)query * p.h + hh] = (M == -INFINITY) ? -INFINITY : (M + log2f(den)) * kLn2;
-    uint16_t* orow = p.out + ((size_t)query * p.h + hh) * p.d;
-    for (int dd = threadIdx.x; dd < p.d; dd += blockDim.x) {
-        float acc = 0.f;
-        for (int sp = 0; sp < p.splits; ++sp) {
-            const float m = ml[sp * 2 * kHp + hh];
-            if (m != -INFINITY)
-                acc += p.part_o[(((size_t)query * p.splits + sp) * p.h + hh) * p.d + dd] * exp2f(m - M);
-        }
-        orow[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * inv));
-    }
-}
-
 size_t attn_smem_bytes(int d_pad) {
     return 1024 + (size_t)kHp * d_pad * 2 + (size_t)kRows * d_pad * 2 + kRows * 128 + sizeof(AttnSmemTail);
 }
 
 }  // namespace
 
-int attn_pick_splits(int n_queries, int n_tiles, int num_sms) {
-    if (n_tiles <= 1) return 1;
-    if (n_queries >= num_sms) return 1;
-    int splits = (num_sms + n_queries - 1) / n_queries;
-    if (splits > n_tiles) splits = n_tiles;
-    return splits;
+static int attn_pick_cluster_uncached(int n_queries, int k) {
+    const int num_sms = device_num_sms();
+    const int max_c = (k + 63) / 64;          // at least 64 slots per CTA
+    int c = n_queries > 0 ? num_sms / n_queries : 1;
+    if (c > 8) c = 8;
+    if (c > max_c) c = max_c;
+    if (c <= 1) return 1;
+    // shrink the cluster until all queries' clusters are resident at once
+    const size_t smem = attn_smem_bytes(512);
+    cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    for (; c > 1; --c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(n_queries * c));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, sparse_attn_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (active >= n_queries) return c;
+    }
+    return 1;
 }
 
-size_t attn_partials_bytes(int n_queries, int splits, int d) {
-    if (splits <= 1) return 0;
-    return (size_t)n_queries * splits * (size_t)(kHp * d + 2 * kHp) * sizeof(float);
+int attn_pick_cluster(int n_queries, int k) {
+    struct Entry {
+        int dev, n_queries, k, c;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (const Entry& e : cache)
+            if (e.dev == dev && e.n_queries == n_queries && e.k == k) return e.c;
+    }
+    const int c = attn_pick_cluster_uncached(n_queries, k);
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() < 4096) cache.push_back({dev, n_queries, k, c});
+    return c;
 }
 
 cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
@@ -413,12 +476,24 @@ cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
     cudaError_t err =
         cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(n_queries, p.splits);
-    sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(p);
-    err = cudaGetLastError();
-    if (err != cudaSuccess || p.splits == 1) return err;
-    attn_combine_kernel<<<dim3(n_queries, p.h), 128, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.cluster <= 1) {
+        sparse_attn_kernel<<<n_queries, kThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_queries * p.cluster));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, p);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace sti

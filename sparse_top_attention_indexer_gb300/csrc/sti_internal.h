@@ -18,6 +18,7 @@ struct IdxScoresParams {
     const uint16_t* w;      // bf16 [B, s, Hi]
     const int32_t* start_pos;
     float* scores;          // fp32 [B, s, n_cols]
+    uint32_t* hist;         // optional [B*s, 2048] counts of the visible scores' top 11 key bits
     uint32_t* status;
     float c;
     int B, s, Hi, Di, n_cols, ratio;
@@ -27,6 +28,7 @@ struct IdxScoresParams {
     int n_alloc;            // TMEM columns per accumulator buffer (multiple of 32)
     int tmem_cols;          // power of two >= 2 * n_alloc
     int stages;             // A pipeline depth
+    int ctas_per_sm;        // 2 when two CTAs' TMEM fits one SM (decode), else 1
     int total_units;        // B * QT
 };
 // tm_a: index keys, tm_b: index queries.
@@ -38,8 +40,19 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p);
 // ------------------------------------------------------------------ window indices, top-k
 cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, int width, int32_t* idxs,
                                int64_t row_stride, uint32_t* status, cudaStream_t stream);
-cudaError_t launch_topk(const float* scores, const int32_t* start_pos, int B, int s, int n_cols, int ratio, int k,
-                        int32_t offset, int32_t* idxs, int64_t row_stride, uint32_t* status, cudaStream_t stream);
+struct TopkParams {
+    const float* scores;      // fp32 [B, s, n_cols]
+    const int32_t* start_pos;
+    int32_t* idxs;            // row (b,t) at idxs + (b*s+t)*row_stride, k entries
+    int64_t row_stride;
+    uint32_t* hist;           // optional [B*s, 2048] first-pass histogram (from the scores kernel); re-zeroed
+    int32_t* win_out;         // optional: window indices of the row written here too (win_width entries)
+    uint32_t* status;
+    int B, s, n_cols, ratio, k;
+    int32_t offset;
+    int win_W, win_width;
+};
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ sparse attention
 struct AttnParams {
@@ -50,19 +63,17 @@ struct AttnParams {
     const int32_t* idx;      // [B, s, k] row stride idx_stride
     uint16_t* out;           // bf16 [B, s, h, d]
     float* lse;              // [B, s, h] or null
-    float* part_o;           // split partials [B*s, splits, h, d] fp32 (splits > 1)
-    float* part_ml;          // [B*s, splits, 2, 64] fp32
     uint32_t* status;
     int64_t kv_bstride, kv2_bstride, idx_stride;
     float scale_log2;        // softmax_scale * log2(e)
     int n1, n2;
     int B, s, h, d, k;
     int d_pad;               // round_up(d, 128)
-    int n_tiles;             // ceil(k / 128)
-    int splits, tiles_per_split;
+    int cluster;             // CTAs per query (a thread-block cluster when > 1)
+    int rows_per_cta;        // index slots each CTA of a cluster handles
 };
-int attn_pick_splits(int n_queries, int n_tiles, int num_sms);
-size_t attn_partials_bytes(int n_queries, int splits, int d);
+// CTAs per query for n_queries queries of k slots (1 = no cluster); cached per device.
+int attn_pick_cluster(int n_queries, int k);
 cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ device properties

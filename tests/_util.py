@@ -80,6 +80,7 @@ def check_topk_rows(gpu_rows: np.ndarray, ref_rows: np.ndarray, ref_scores: np.n
         srow = sc[i]
         vis = np.isfinite(srow)
         order = np.sort(srow[vis])[::-1]
+        assert len(order) > k, f"row {i}: every visible position should be selected, sets differ"
         tau = order[k - 1]
         amb = set((np.nonzero(np.abs(srow - tau) <= band * abs(tau))[0] + offset).tolist())
         gs, rs = set(gv.tolist()) - amb, set(rv.tolist()) - amb

@@ -34,7 +34,7 @@ def _run(shape, data, device):
     path = bench.GpuPath(shape, data, device)
     path.step()
     torch.cuda.synchronize()
-    assert path.sti.read_device_status(path.ws) == 0
+    assert path.read_status() == 0
     return path
 
 
@@ -47,7 +47,7 @@ def test_workload_full(gpu, orc, n):
     W, width = shape.window, shape.win_width
     # scores, every row and column
     ref_s = orc.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
-    got_s = path.scores.cpu().numpy()
+    got_s = path.scores_view().cpu().numpy()
     worst = check_scores(got_s, ref_s)
     # indices: window part exact, compressed part the same set outside the boundary band
     ref_c = orc.topk(ref_s, sp, shape.ratio, shape.topk, shape.win_rows)
@@ -73,7 +73,7 @@ def test_workload_prefill_sampled(gpu, orc):
     data = workloads.make(shape)
     path = _run(shape, data, gpu)
     s, W, K, r = shape.s, shape.window, shape.topk, shape.ratio
-    got_s = path.scores[0].cpu().numpy()
+    got_s = path.scores_view()[0].cpu().numpy()
     got_i = path.idx[0].cpu().numpy()
     # properties of every row at full size
     t = np.arange(s)
