@@ -63,6 +63,28 @@ sti_status make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_
     return STI_OK;
 }
 
+// 2-D bf16 tensor map: dims {inner, rows}, row stride in bytes, 128-byte swizzle.
+sti_status make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled unavailable");
+        return STI_ERR_CUDA;
+    }
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return STI_ERR_CUDA;
+    }
+    return STI_OK;
+}
+
 uint32_t* status_word(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
@@ -222,7 +244,25 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.d_pad = ((d + 127) / 128) * 128;
     p.cluster = sti::attn_pick_cluster(nq, k);
     p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
-    cudaError_t e = sti::launch_sparse_attn(p, st);
+    // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
+    p.rows1 = n1 > 0 ? kv_bstride / d : 0;
+    p.rows2 = n2 > 0 ? kv2_bstride / d : 0;
+    p.default_src = n1 > 0 ? 0 : 1;
+    p.use_tma = (n1 + n2 > 0) && (n1 == 0 || kv_bstride % d == 0) && (n2 == 0 || kv2_bstride % d == 0) &&
+                (int64_t)b * (p.rows1 > p.rows2 ? p.rows1 : p.rows2) < 0x7FFFFFFF;
+    CUtensorMap tm_q, tm_kv1, tm_kv2;
+    memset(&tm_q, 0, sizeof tm_q);
+    memset(&tm_kv1, 0, sizeof tm_kv1);
+    memset(&tm_kv2, 0, sizeof tm_kv2);
+    if (p.use_tma) {
+        sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, (uint32_t)h);
+        if (s == STI_OK && n1 > 0) s = make_map_2d(&tm_kv1, kv, (uint64_t)d, (uint64_t)b * p.rows1, (uint64_t)d * 2, 64, 1);
+        if (s == STI_OK && n2 > 0) s = make_map_2d(&tm_kv2, kv2, (uint64_t)d, (uint64_t)b * p.rows2, (uint64_t)d * 2, 64, 1);
+        if (s != STI_OK) return s;
+        if (n1 == 0) tm_kv1 = tm_kv2;
+        if (n2 == 0) tm_kv2 = tm_kv1;
+    }
+    cudaError_t e = sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
 

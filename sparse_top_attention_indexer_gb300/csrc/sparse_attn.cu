@@ -47,6 +47,8 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 struct __align__(8) AttnSmemTail {
     uint64_t mma_bar;
+    uint64_t q_bar;        // Q tile landed (TMA)
+    uint64_t gather_bar;   // this tile's rows landed (TMA)
     uint32_t tmem_base;
     uint32_t pad;
     float m_run[kHp];     // running max, log2 domain
@@ -55,6 +57,8 @@ struct __align__(8) AttnSmemTail {
     float red[4][kHp];    // per-warp partial reductions
     const uint16_t* row_src[kRows];
     int row_valid[kRows];
+    int row_coord[kRows];  // row in its source viewed as [B*rows, d]
+    int row_srcid[kRows];  // 0: kv, 1: kv2, -1: masked
 };
 
 // Swizzled byte offset of 16-byte chunk `ch` (of 8 bf16) of row `r` in a tile of `rows` rows
@@ -84,7 +88,21 @@ __device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64]) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnParams p) {
+#ifdef STI_ATTN_TIMING
+__device__ unsigned long long g_attn_t[2048][16];
+#define STI_TSTAMP(i)                                                                                  \
+    do {                                                                                               \
+        if (threadIdx.x == 0 && blockIdx.x < 2048) g_attn_t[blockIdx.x][i] = clock64();               \
+    } while (0)
+#else
+#define STI_TSTAMP(i) \
+    do {              \
+    } while (0)
+#endif
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
+                       const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* q_s = smem;                                 // [64 heads] x d_pad, K-major SW128
@@ -100,21 +118,45 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     const int slot_end = min(p.k, slot_begin + p.rows_per_cta);
     const int tile_begin = 0;
     const int tile_end = (slot_end - slot_begin + kRows - 1) / kRows;
+    STI_TSTAMP(0);
 
     if (warp == 0) {
         tmem_alloc(&tl->tmem_base, 512);
         tmem_relinquish();
     }
+    const int ncb_real = p.d / 64;        // column blocks holding data; the rest stay zero
+    const int ncb = p.d_pad / 64;
     if (tid == 0) {
         mbar_init(&tl->mma_bar, 1);
+        mbar_init(&tl->q_bar, 1);
+        mbar_init(&tl->gather_bar, 1);
         fence_mbar_init();
     }
     if (tid < kHp) {
         tl->m_run[tid] = -INFINITY;
         tl->l_run[tid] = 0.f;
     }
-    // Q -> shared memory (heads >= h and columns >= d are zero)
-    {
+    if (p.use_tma) {
+        // zero what no copy writes: Q rows >= h, and every padded column block of Q and the tile
+        for (int cb = 0; cb < ncb; ++cb) {
+            const int r0 = cb < ncb_real ? p.h : 0;
+            uint4* q_blk = reinterpret_cast<uint4*>(q_s + (size_t)cb * kHp * 128);
+            for (int i = r0 * 8 + tid; i < kHp * 8; i += kThreads) q_blk[i] = make_uint4(0, 0, 0, 0);
+            if (cb >= ncb_real) {
+                uint4* kv_blk = reinterpret_cast<uint4*>(kv_s + (size_t)cb * kRows * 128);
+                for (int i = tid; i < kRows * 8; i += kThreads) kv_blk[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        __syncthreads();   // barrier initialisation visible before the copies use it
+        if (tid == 0) {
+            tma_prefetch_desc(&tm_kv1);
+            tma_prefetch_desc(&tm_kv2);
+            mbar_arrive_expect_tx(&tl->q_bar, (uint32_t)(ncb_real * p.h * 128));
+            for (int cb = 0; cb < ncb_real; ++cb)
+                tma_load_2d(q_s + (size_t)cb * kHp * 128, &tm_q, &tl->q_bar, cb * 64, query * p.h);
+        }
+    } else {
+        // Q -> shared memory (heads >= h and columns >= d are zero)
         const uint16_t* qrow = p.q + (size_t)query * p.h * p.d;
         const int chunks_per_row = p.d_pad / 8;
         for (int c = tid; c < kHp * chunks_per_row; c += kThreads) {
@@ -129,11 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tl->tmem_base;
+    STI_TSTAMP(1);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tm_s = tmem;              // S^T: columns [0, 64)
     const uint32_t tm_o = tmem + 64;         // O^T block m: columns [64 + 64m, 128 + 64m)
     const int nmb = p.d_pad / 128;           // d blocks of 128
-    uint32_t mma_phase = 0;
+    uint32_t mma_phase = 0, gather_phase = 0;
     bool dead = false;
 
     const uint32_t idesc_qk = idesc_bf16_f32(128, kHp, false, false);
@@ -150,17 +193,73 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
                 atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
                 idx = -1;
             }
-            const uint16_t* src = nullptr;
-            if (idx >= 0)
-                src = idx < p.n1 ? p.kv + (size_t)b * p.kv_bstride + (size_t)idx * p.d
-                                 : p.kv2 + (size_t)b * p.kv2_bstride + (size_t)(idx - p.n1) * p.d;
+            const int srcid = idx < 0 ? -1 : (idx < p.n1 ? 0 : 1);
+            const int64_t coord = srcid < 0 ? 0 : (srcid == 0 ? b * p.rows1 + idx : b * p.rows2 + (idx - p.n1));
+            const uint16_t* src = srcid < 0 ? nullptr : (srcid == 0 ? p.kv : p.kv2) + coord * p.d;
             tl->row_src[tid] = src;
             tl->row_valid[tid] = idx >= 0;
+            tl->row_coord[tid] = (int)coord;
+            tl->row_srcid[tid] = srcid;
         }
         __syncthreads();
-        {
-            const int chunks_per_row = p.d_pad / 8;
-            const uint32_t kv_base = smem_u32(kv_s);
+        const uint32_t kv_base = smem_u32(kv_s);
+        const int chunks_per_row = p.d_pad / 8;
+        if (p.use_tma) {
+            // warp 0: lane g gathers rows 4g..4g+3, one 4-row TMA per 128-byte column block.  Masked
+            // slots load a real row of the same source (their score is -inf, so P = 0); a group whose
+            // rows come from both sources is copied with cp.async instead.
+            if (warp == 0) {
+                const int g = lane;
+                int sid[4], crd[4];
+                int S = -1, fc = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sid[i] = tl->row_srcid[4 * g + i];
+                    crd[i] = tl->row_coord[4 * g + i];
+                    if (sid[i] >= 0 && S < 0) {
+                        S = sid[i];
+                        fc = crd[i];
+                    }
+                }
+                bool mixed = false;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) mixed = mixed || (sid[i] >= 0 && sid[i] != S);
+                if (S < 0) {
+                    S = p.default_src;
+                    fc = (int)(b * (S == 0 ? p.rows1 : p.rows2));
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (sid[i] != S) crd[i] = fc;
+                const unsigned tma_groups = __ballot_sync(kFull, !mixed);
+                if (lane == 0 && !dead)
+                    mbar_arrive_expect_tx(&tl->gather_bar, (uint32_t)(__popc(tma_groups) * ncb_real * 512));
+                __syncwarp();
+                if (!dead) {
+                    if (!mixed) {
+                        const void* map = S == 0 ? (const void*)&tm_kv1 : (const void*)&tm_kv2;
+                        for (int cb = 0; cb < ncb_real; ++cb)
+                            tma_gather4(kv_s + (size_t)cb * kRows * 128 + (size_t)g * 512, map, &tl->gather_bar,
+                                        cb * 64, crd[0], crd[1], crd[2], crd[3]);
+                    } else {
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = 4 * g + i;
+                            const uint16_t* rs = tl->row_src[r];
+                            for (int ch = 0; ch < chunks_per_row; ++ch) {
+                                const bool ok = rs != nullptr && ch * 8 < p.d;
+                                cp_async_16(kv_base + sw128_offset(r, ch, kRows), ok ? rs + ch * 8 : p.q,
+                                            ok ? 16u : 0u);
+                            }
+                        }
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait<0>();
+            }
+            if (tile == tile_begin && !dead) dead = !mbar_wait(&tl->q_bar, 0, p.status);
+            if (!dead) dead = !mbar_wait(&tl->gather_bar, gather_phase, p.status);
+            gather_phase ^= 1u;
+        } else {
             for (int c = tid; c < kRows * chunks_per_row; c += kThreads) {
                 const int r = c / chunks_per_row, ch = c - r * chunks_per_row;
                 const uint16_t* rs = tl->row_src[r];
@@ -174,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         __syncthreads();
 
         // ---- S^T = KV . Q^T
+        if (tile < 2) STI_TSTAMP(2 + 4 * tile);
         if (tid == 0 && !dead) {
             tc_fence_after();
             const uint32_t a0 = smem_u32(kv_s), b0 = smem_u32(q_s);
@@ -189,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         tc_fence_after();
 
         // ---- online softmax (thread = row, 64 heads in registers)
+        if (tile < 2) STI_TSTAMP(3 + 4 * tile);
         float x[kHp];
         {
             uint32_t r0[32], r1[32];
@@ -268,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         __syncthreads();
 
         // ---- O^T += V^T . P^T  (A = the same KV tile, MN-major; B = P^T, MN-major)
+        if (tile < 2) STI_TSTAMP(4 + 4 * tile);
         if (tid == 0 && !dead) {
             tc_fence_after();
             const uint32_t a0 = smem_u32(kv_s), b0 = smem_u32(p_s);
@@ -283,10 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         if (!dead) dead = !mbar_wait(&tl->mma_bar, mma_phase, p.status);
         mma_phase ^= 1u;
         tc_fence_after();
+        if (tile < 2) STI_TSTAMP(5 + 4 * tile);
     }
 
+    STI_TSTAMP(10);
     // ---- epilogue: O^T (lane = d, column = head) -> output or split partial
     cp_async_wait<0>();   // Q's copy when this CTA had no tile
+    if (p.use_tma && tile_begin == tile_end) mbar_wait(&tl->q_bar, 0, p.status);
     __syncthreads();
     const bool has_tiles = tile_begin < tile_end && !dead;
     if (C == 1) {
@@ -332,15 +437,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         // ---- cluster reduction through distributed shared memory
         if (!has_tiles && tid < kHp) tl->m_run[tid] = -INFINITY;   // nothing valid here
         cluster_sync();                                            // every CTA's m, l are final
+        STI_TSTAMP(11);
         if (tid < kHp) {
+            // every partner's (m, l) in flight at once, then combined
+            float mr[8], lr[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < C) {
+                    mr[r] = ld_dsmem_f32(dsmem_addr(&tl->m_run[tid], (uint32_t)r));
+                    lr[r] = ld_dsmem_f32(dsmem_addr(&tl->l_run[tid], (uint32_t)r));
+                }
             float M = -INFINITY;
-            for (int r = 0; r < C; ++r) M = fmaxf(M, ld_dsmem_f32(dsmem_addr(&tl->m_run[tid], (uint32_t)r)));
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                if (r < C) M = fmaxf(M, mr[r]);
             float L = 0.f;
             if (M != -INFINITY) {
-                for (int r = 0; r < C; ++r) {
-                    const float mr = ld_dsmem_f32(dsmem_addr(&tl->m_run[tid], (uint32_t)r));
-                    if (mr != -INFINITY) L += ld_dsmem_f32(dsmem_addr(&tl->l_run[tid], (uint32_t)r)) * exp2f(mr - M);
-                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < C && mr[r] != -INFINITY) L += lr[r] * exp2f(mr[r] - M);
                 if (tid < p.h) L += exp2f(__ldg(p.sink + tid) * kLog2e - M);
             }
             const float mo = tl->m_run[tid];
@@ -377,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
             }
         }
         cluster_sync();   // every CTA's share is in its shared memory
+        STI_TSTAMP(12);
         // CTA `rank` sums d in [rank*dper, (rank+1)*dper) over the cluster and writes the output
         const int dper = (p.d + C - 1) / C;
         const int d_lo = rank * dper, d_hi = min(p.d, d_lo + dper);
@@ -385,14 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         for (int dd = d_lo + tid; dd < d_hi; dd += kThreads) {
             for (int hc = 0; hc < n_hc; ++hc) {
                 const float* loc = dump + (size_t)dd * kHp + ((hc ^ (dd & 15)) << 2);
+                float4 v[8];   // all partners' shares in flight before any is added
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < C) v[r] = ld_dsmem_f4(dsmem_addr(loc, (uint32_t)r));
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int r = 0; r < C; ++r) {
-                    const float4 v = ld_dsmem_f4(dsmem_addr(loc, (uint32_t)r));
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r < C) {
+                        acc.x += v[r].x;
+                        acc.y += v[r].y;
+                        acc.z += v[r].z;
+                        acc.w += v[r].w;
+                    }
                 const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -401,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
                 }
             }
         }
+        STI_TSTAMP(13);
         cluster_sync();   // partners finished reading this CTA's shared memory
     }
 
@@ -410,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnPara
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    STI_TSTAMP(14);
 }
 
 size_t attn_smem_bytes(int d_pad) {
@@ -469,7 +592,8 @@ int attn_pick_cluster(int n_queries, int k) {
     return c;
 }
 
-cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
+cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                               const AttnParams& p, cudaStream_t stream) {
     const int n_queries = p.B * p.s;
     if (n_queries == 0) return cudaSuccess;
     const size_t smem = attn_smem_bytes(p.d_pad);
@@ -477,7 +601,7 @@ cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
         cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     if (p.cluster <= 1) {
-        sparse_attn_kernel<<<n_queries, kThreads, smem, stream>>>(p);
+        sparse_attn_kernel<<<n_queries, kThreads, smem, stream>>>(tm_q, tm_kv1, tm_kv2, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -492,8 +616,15 @@ cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, p);
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, tm_kv1, tm_kv2, p);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace sti
+
+#ifdef STI_ATTN_TIMING
+// profiling builds only: per-CTA clock64 stamps of the attention phases
+extern "C" int sti_dbg_attn_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_attn_t, sizeof(unsigned long long) * 16 * (size_t)n_blocks);
+}
+#endif

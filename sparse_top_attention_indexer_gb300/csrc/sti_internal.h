@@ -71,10 +71,16 @@ struct AttnParams {
     int d_pad;               // round_up(d, 128)
     int cluster;             // CTAs per query (a thread-block cluster when > 1)
     int rows_per_cta;        // index slots each CTA of a cluster handles
+    int use_tma;             // gather rows with TMA (tensor maps valid); else 16-byte cp.async
+    int64_t rows1, rows2;    // rows per batch element of kv / kv2 (batch stride / d)
+    int default_src;         // source whose row 0 stands in for masked slots (0: kv, 1: kv2)
 };
 // CTAs per query for n_queries queries of k slots (1 = no cluster); cached per device.
 int attn_pick_cluster(int n_queries, int k);
-cudaError_t launch_sparse_attn(const AttnParams& p, cudaStream_t stream);
+// tm_q: q as [B*s*h, d] (box 64 x h); tm_kv1 / tm_kv2: the sources as [B*rows, d] (box 64 x 1,
+// for 4-row gathers).  Ignored unless p.use_tma.
+cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                               const AttnParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ device properties
 int device_num_sms();

@@ -92,6 +92,25 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// Four rows y0..y3 of a 2-D tensor (box: one row high), columns [x, x + box width), written as
+// four consecutive box rows at dst.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* map, uint64_t* bar, int x, int y0, int y1, int y2,
+                                            int y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+        : "memory");
+}
+
 // ------------------------------------------------------------------ LSU async copies
 
 // 16-byte global->shared copy; src_bytes == 0 zero-fills the destination.
