@@ -45,7 +45,8 @@ typedef enum sti_status {
     STI_ERR_CUDA = 3,              /* a CUDA runtime/driver call failed */
     STI_ERR_INDEX_RANGE = 4,       /* device: an index was < -1 or >= the number of KV rows */
     STI_ERR_DEVICE_TIMEOUT = 5,    /* device: a bounded wait inside a kernel gave up */
-    STI_ERR_DEVICE_UNSUPPORTED = 6 /* device: start_pos != 0 with seqlen > 1 (chunked prefill) */
+    STI_ERR_DEVICE_UNSUPPORTED = 6, /* device: start_pos != 0 with seqlen > 1 (chunked prefill) */
+    STI_ERR_TOO_LARGE = 7           /* the sizes exceed the fixed scratch of sti_decode_fused_noalloc */
 } sti_status;
 
 /* Bits of the device status word (first 4 bytes of every workspace). */
@@ -201,6 +202,30 @@ typedef struct sti_decode_args {
 size_t sti_decode_workspace_size(const sti_decode_args *a);
 sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream,
                             void *const *events);
+
+/* ------------------------------------------------------------------ fused decode, no allocation */
+/*
+ * Not an operation of the paper (it has no counterpart there): the same decode step as
+ * sti_decode_fused, for callers that cannot hand the library a device workspace -- for example
+ * a plugin inside a host runtime that owns every device allocation and offers no workspace
+ * hook, or a serving loop that must never enter the CUDA allocator once it is running.  The
+ * step's scratch (status word, scores, first-pass histograms) lives in one fixed array inside
+ * this library instead: about 10 MiB of device memory that every GPU on which the library is
+ * used holds until the process exits.  The call allocates and frees nothing.
+ *  - Limits: b <= STI_NOALLOC_MAX_BATCH and b * n_cols <= STI_NOALLOC_MAX_SCORES; larger calls
+ *    return STI_ERR_TOO_LARGE before anything is enqueued.  Other checks as sti_decode_fused.
+ *  - The first call on a device looks up the array's device address (once per device, with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call uses the same array and it keeps the previous call's contents: the call clears
+ *    the parts that must start at zero, and calls that overlap on the GPU (other streams, other
+ *    threads) race on it -- serialise them.  Device-side status bits are cleared by the next
+ *    call; read them with sti_decode_noalloc_status.
+ */
+#define STI_NOALLOC_MAX_BATCH 256
+#define STI_NOALLOC_MAX_SCORES (1 << 21)
+sti_status sti_decode_fused_noalloc(const sti_decode_args *a, sti_stream stream);
+/* Synchronises `stream` and returns the STI_FLAG_* bits the last no-allocation call left. */
+sti_status sti_decode_noalloc_status(uint32_t *flags, sti_stream stream);
 
 #ifdef __cplusplus
 }

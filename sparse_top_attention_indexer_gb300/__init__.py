@@ -23,13 +23,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("STI_LIB") or os.path.join(_HERE, "libsti.so")
 
 STATUS_NAMES = {0: "STI_OK", 1: "STI_ERR_INVALID_ARG", 2: "STI_ERR_UNSUPPORTED", 3: "STI_ERR_CUDA",
-                4: "STI_ERR_INDEX_RANGE", 5: "STI_ERR_DEVICE_TIMEOUT", 6: "STI_ERR_DEVICE_UNSUPPORTED"}
+                4: "STI_ERR_INDEX_RANGE", 5: "STI_ERR_DEVICE_TIMEOUT", 6: "STI_ERR_DEVICE_UNSUPPORTED",
+                7: "STI_ERR_TOO_LARGE"}
 FLAG_INDEX_RANGE, FLAG_TIMEOUT, FLAG_CHUNKED = 1, 2, 4
 
 EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_device_status", "sti_window_idxs",
            "sti_idx_scores_workspace_size", "sti_idx_scores", "sti_idx_topk_workspace_size", "sti_idx_topk",
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_decode_workspace_size",
-           "sti_decode_fused"]
+           "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status"]
 
 
 class StiError(RuntimeError):
@@ -82,6 +83,10 @@ def lib() -> ctypes.CDLL:
         L.sti_decode_workspace_size.restype = SZ
         L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
         L.sti_decode_fused.restype = I
+        L.sti_decode_fused_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), P]
+        L.sti_decode_fused_noalloc.restype = I
+        L.sti_decode_noalloc_status.argtypes = [P, P]
+        L.sti_decode_noalloc_status.restype = I
         _lib = L
     return _lib
 
@@ -253,3 +258,17 @@ def decode_fused(a: DecodeArgs, ws: torch.Tensor, stream=None, events=None):
                 e.record()
         ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
     _check(lib().sti_decode_fused(ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream), ev), "sti_decode_fused")
+
+
+def decode_fused_noalloc(a: DecodeArgs, stream=None):
+    """The decode step of decode_fused without a workspace: its scratch is a fixed array inside
+    the library (for callers that cannot allocate device memory).  Calls that overlap on the GPU
+    race on that array; the first call on a device should come before any stream capture."""
+    _check(lib().sti_decode_fused_noalloc(ctypes.byref(a), _stream(stream)), "sti_decode_fused_noalloc")
+
+
+def decode_noalloc_status(stream=None) -> int:
+    """Synchronise and return the STI_FLAG_* bits the last no-allocation call left."""
+    flags = ctypes.c_uint32(0)
+    lib().sti_decode_noalloc_status(ctypes.byref(flags), _stream(stream))
+    return int(flags.value)

@@ -277,6 +277,7 @@ const char* sti_status_string(sti_status s) {
         case STI_ERR_INDEX_RANGE: return "STI_ERR_INDEX_RANGE";
         case STI_ERR_DEVICE_TIMEOUT: return "STI_ERR_DEVICE_TIMEOUT";
         case STI_ERR_DEVICE_UNSUPPORTED: return "STI_ERR_DEVICE_UNSUPPORTED";
+        case STI_ERR_TOO_LARGE: return "STI_ERR_TOO_LARGE";
     }
     return "STI_UNKNOWN";
 }
@@ -391,6 +392,89 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
                   a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, st);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    return STI_OK;
+}
+
+// ---------------------------------------------------------------------- fused decode, no allocation
+//
+// Scratch of sti_decode_fused_noalloc: [status word | scores fp32 (up to STI_NOALLOC_MAX_SCORES) |
+// first-pass histograms u32 (up to STI_NOALLOC_MAX_BATCH rows of 2048 bins)].  A file-scope device
+// array: in host code its name is only a stand-in, so the device address is looked up once per
+// device with cudaGetSymbolAddress and that pointer is what the kernels get.
+
+static constexpr size_t kNoallocScoresOff = sti::kWsStatusBytes;
+static constexpr size_t kNoallocHistOff = kNoallocScoresOff + (size_t)STI_NOALLOC_MAX_SCORES * sizeof(float);
+static constexpr size_t kNoallocBytes = kNoallocHistOff + (size_t)STI_NOALLOC_MAX_BATCH * 2048 * sizeof(uint32_t);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[64];
+
+// Device address of the scratch array on the current device (looked up on first use).
+static sti_status noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= 64) return STI_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                             "sti_decode_fused_noalloc: cudaGetSymbolAddress");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = static_cast<uint8_t*>(g_noalloc_addr[dev]);
+    return STI_OK;
+}
+
+sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream) {
+    if (!a) return STI_ERR_INVALID_ARG;
+    if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
+    if (a->b == 0) return STI_OK;
+    if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
+    if (a->b > STI_NOALLOC_MAX_BATCH || (int64_t)a->b * (a->n_cols > 0 ? a->n_cols : 1) > STI_NOALLOC_MAX_SCORES)
+        return STI_ERR_TOO_LARGE;
+    uint8_t* scratch = nullptr;
+    sti_status s = noalloc_scratch(&scratch);
+    if (s != STI_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
+    float* scores = reinterpret_cast<float*>(scratch + kNoallocScoresOff);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(scratch + kNoallocHistOff);
+    // the array still holds the previous call's data: zero the status word and the histograms
+    cudaError_t e = cudaMemsetAsync(status, 0, sti::kWsStatusBytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(hist, 0, (size_t)a->b * 2048 * sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused_noalloc: cudaMemsetAsync");
+    const int W = a->window_size, K = a->index_topk, k_total = W + K;
+    if (a->n_cols > 0) {
+        s = idx_scores_impl(a->iq, a->ik, a->ik_bstride, a->w, a->index_scale, a->start_pos, a->b, 1, a->Hi, a->Di,
+                            a->n_cols, a->ratio, scores, status, st, hist);
+        if (s != STI_OK) return s;
+    }
+    s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
+                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W);
+    if (s != STI_OK) return s;
+    return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
+                     a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
+                     st);
+}
+
+sti_status sti_decode_noalloc_status(uint32_t* flags, sti_stream stream) {
+    uint8_t* scratch = nullptr;
+    sti_status s = noalloc_scratch(&scratch);
+    if (s != STI_OK) return s;
+    uint32_t host = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&host, scratch, sizeof host, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "sti_decode_noalloc_status");
+    if (flags) *flags = host;
+    if (host & STI_FLAG_TIMEOUT) return STI_ERR_DEVICE_TIMEOUT;
+    if (host & STI_FLAG_INDEX_RANGE) return STI_ERR_INDEX_RANGE;
+    if (host & STI_FLAG_CHUNKED) return STI_ERR_DEVICE_UNSUPPORTED;
     return STI_OK;
 }
 
