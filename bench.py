@@ -8,8 +8,9 @@ launched through the C ABI on one stream.  Default workload: single-layer decode
 context 65536 (16384 compressed rows), 64 heads x 512, index heads 32 x 128, top-512.
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream with an event between every kernel; a 256 MiB buffer is written before
-every step (outside the events) so no step finds the previous step's data in L2.
+launching stream with an event between every kernel; a 256 MiB buffer is written and then
+read before every step (outside the events), so no step finds the previous step's data in L2
+and no step pays for write-backs of the flush itself.
 `value` is tokens/s (decode) or queries/s (prefill) over the timed region; `e2e` is the same
 metric through the fused public entry point with the step's inputs copied from pinned host
 memory and the output copied back every step (wall clock).  `roofline` reports the kernel
@@ -125,6 +126,34 @@ class GpuPath:
                                               topk_idxs=self.idx.view(self.b, self.k_total))
             self.dws = sti.workspace(sti.decode_workspace_size(self.args), device)
 
+    def capture(self):
+        """Capture one decode step (the fused entry point, with its 4 timing events) in a CUDA
+        graph; replaying it costs one launch instead of the entry point's host work."""
+        torch = self.torch
+        assert not self.prefill and self.L == 1
+        self.gevents = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in self.gevents:
+            e.record()
+        self.sti.decode_fused(self.args, self.dws, events=self.gevents)   # warm caches before capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.sti.decode_fused(self.args, self.dws, events=self.gevents)
+        torch.cuda.synchronize()
+        # the same step without the events between its kernels
+        self.pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.pgraph):
+            self.sti.decode_fused(self.args, self.dws)
+        torch.cuda.synchronize()
+
+    def graph_step(self):
+        self.graph.replay()
+
+    def graph_times_ms(self):
+        """Per-kernel and whole-step milliseconds of the last replay (after a synchronize)."""
+        ev = self.gevents
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(3)], ev[0].elapsed_time(ev[3])
+
     def scores_view(self):
         """The index scores of the last step ([b, s, n_cols] fp32)."""
         if self.prefill:
@@ -168,7 +197,10 @@ class GpuPath:
             rec(4 + i)
 
     def flush_l2(self):
+        # write, then read: no data of the step stays in L2 and none of L2 is left dirty, so the
+        # step neither hits on its own inputs nor pays for the flush's write-backs
         self.flush.fill_(1)
+        self._flush_sink = self.flush.view(self.torch.int64).sum()
 
 
 # ---------------------------------------------------------------------------------- work accounting
@@ -358,7 +390,7 @@ def main():
     cfg = {"workload": shape.name, "b": shape.b, "seqlen": shape.s, "context": int(shape.start_pos.max()) + shape.s,
            "heads": shape.h, "head_dim": shape.d, "window": shape.window, "ratio": shape.ratio,
            "compressed_rows": shape.n_cols, "index_heads": shape.Hi, "index_head_dim": shape.Di,
-           "index_topk": shape.topk, "attention_layers": shape.n_layers, "l2": "256 MiB written before every step"}
+           "index_topk": shape.topk, "attention_layers": shape.n_layers, "l2": "256 MiB written then read before every step (outside the timed region)"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -394,12 +426,16 @@ def main():
     stream = torch.cuda.current_stream()
 
     sampler = None if args.no_clocks else ClockSampler(device.index)
+    use_graph = not shape.prefill and shape.n_layers == 1
+    if use_graph:
+        path.capture()
     for _ in range(args.warmup):
         path.flush_l2()
-        path.step()
+        path.graph_step() if use_graph else path.step()
     torch.cuda.synchronize()
     n_ev = len(path.names) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    graph_times = []
     if sampler:
         sampler.start()
         time.sleep(0.3)
@@ -408,7 +444,13 @@ def main():
     torch.cuda.synchronize()
     for k in range(args.steps):
         path.flush_l2()
-        path.step(evs[k])
+        if use_graph:
+            # the graph's own events time each replay; read them before the next replay
+            path.graph_step()
+            torch.cuda.synchronize()
+            graph_times.append(path.graph_times_ms())
+        else:
+            path.step(evs[k])
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -418,16 +460,36 @@ def main():
         t_end = time.perf_counter() + 0.6
         while time.perf_counter() < t_end:
             path.flush_l2()
-            path.step()
+            path.graph_step() if use_graph else path.step()
         torch.cuda.synchronize()
         clocks = sampler.stop()
 
+    plain_ms = None
+    if use_graph:
+        # diagnostic: the same step replayed without events between its kernels
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        pl = []
+        for _ in range(min(args.steps, 50)):
+            path.flush_l2()
+            pe[0].record()
+            path.pgraph.replay()
+            pe[1].record()
+            torch.cuda.synchronize()
+            pl.append(pe[0].elapsed_time(pe[1]))
+        plain_ms = round(statistics.median(pl), 5)
+
     per_kernel = {n: [] for n in path.names}
     step_ms = []
-    for ev in evs:
-        step_ms.append(ev[0].elapsed_time(ev[-1]))
-        for i, n in enumerate(path.names):
-            per_kernel[n].append(ev[i].elapsed_time(ev[i + 1]))
+    if use_graph:
+        for ks, st in graph_times:
+            step_ms.append(st)
+            for n, t in zip(path.names, ks):
+                per_kernel[n].append(t)
+    else:
+        for ev in evs:
+            step_ms.append(ev[0].elapsed_time(ev[-1]))
+            for i, n in enumerate(path.names):
+                per_kernel[n].append(ev[i].elapsed_time(ev[i + 1]))
     total_ms = float(sum(step_ms))
     if dist:
         t = torch.tensor([total_ms], device=device)
@@ -452,7 +514,10 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
             "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
-            "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks}
+            "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks,
+            "launch": "CUDA graph of sti_decode_fused, replayed per step" if use_graph else "direct C-ABI calls"}
+    if plain_ms is not None:
+        line["ms_per_step_without_kernel_events"] = plain_ms
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:

@@ -146,11 +146,12 @@ sti_status sti_idx_topk(const float *scores, const int32_t *start_pos, int b, in
  *   lse: optional fp32 [b, seqlen, h] = ln(sum_i e^{s_i} + e^{sink}); -inf for a query with
  *        no valid slot; may be NULL.
  * Indices < -1 or >= n1+n2 are treated as masked and raise STI_FLAG_INDEX_RANGE.
- * With few queries (decode) a query's slots are split over a thread-block cluster of up to 8
- * CTAs whose partial results are merged in distributed shared memory; nothing but the status
- * word is kept in the workspace.
+ * With few queries (decode) a query's slots are split over a thread-block cluster of 2 or 4
+ * CTAs; their partial outputs meet in distributed shared memory and each CTA of the cluster
+ * finishes a slice of the head dimension.  The workspace holds only the status word.
  * Supported: 1 <= h <= 64, d a multiple of 64 up to 512, k >= 1, kv_bstride/kv2_bstride
- * multiples of 8.  ws: sti_sparse_attn_workspace_size(b, seqlen, h, d, k) bytes.
+ * multiples of 8, q/kv/kv2/out 16-byte aligned.  ws: sti_sparse_attn_workspace_size(b, seqlen,
+ * h, d, k) bytes.
  */
 size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k);
 sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,

@@ -179,7 +179,7 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
 static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b, int seqlen, int n_cols, int ratio,
                             int k, int32_t offset, int32_t* idxs, int64_t row_stride, uint32_t* status,
                             cudaStream_t st, uint32_t* hist = nullptr, int32_t* win_out = nullptr, int win_W = 0,
-                            int win_width = 0) {
+                            int win_width = 0, bool pdl = false) {
     if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1 || k < 1 || row_stride < k) return STI_ERR_INVALID_ARG;
     if (k > 4096) return STI_ERR_UNSUPPORTED;
     if ((int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
@@ -201,6 +201,7 @@ static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b
     p.offset = offset;
     p.win_W = win_W;
     p.win_width = win_width;
+    p.pdl = pdl ? 1 : 0;
     cudaError_t e = sti::launch_topk(p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_idx_topk");
 }
@@ -208,7 +209,7 @@ static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b
 static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
                             int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
-                            uint16_t* out, float* lse, uint32_t* status, cudaStream_t st) {
+                            uint16_t* out, float* lse, uint32_t* status, cudaStream_t st, bool pdl = false) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
@@ -217,7 +218,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     if ((n1 > 0 && (kv_bstride < (int64_t)n1 * d || kv_bstride % 8)) ||
         (n2 > 0 && (kv2_bstride < (int64_t)n2 * d || kv2_bstride % 8)))
         return STI_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || (kv && !aligned(kv, 16)) || (kv2 && !aligned(kv2, 16))) return STI_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || (kv && !aligned(kv, 16)) || (kv2 && !aligned(kv2, 16)))
+        return STI_ERR_INVALID_ARG;
     if ((int64_t)b * seqlen * 8 > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
     const int nq = b * seqlen;
 
@@ -242,12 +244,13 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.d = d;
     p.k = k;
     p.d_pad = ((d + 127) / 128) * 128;
-    p.cluster = sti::attn_pick_cluster(nq, k);
+    p.cluster = sti::attn_pick_cluster(nq, k, d);
     p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
     p.rows1 = n1 > 0 ? kv_bstride / d : 0;
     p.rows2 = n2 > 0 ? kv2_bstride / d : 0;
     p.default_src = n1 > 0 ? 0 : 1;
+    p.pdl = pdl ? 1 : 0;
     p.use_tma = (n1 + n2 > 0) && (n1 == 0 || kv_bstride % d == 0) && (n2 == 0 || kv2_bstride % d == 0) &&
                 (int64_t)b * (p.rows1 > p.rows2 ? p.rows1 : p.rows2) < 0x7FFFFFFF;
     CUtensorMap tm_q, tm_kv1, tm_kv2;
@@ -342,7 +345,7 @@ sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t k
                                 int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                                 int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                                 uint16_t* out, float* lse, void* ws, size_t ws_bytes, sti_stream stream) {
-    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
+    if (!ws_ok(ws, ws_bytes, sti_sparse_attn_workspace_size(b, seqlen, h, d, k))) return STI_ERR_INVALID_ARG;
     return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
                      seqlen, h, d, k, out, lse, status_word(ws), static_cast<cudaStream_t>(stream));
 }
@@ -371,8 +374,14 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     const int W = a->window_size, K = a->index_topk, k_total = W + K;
     float* scores = reinterpret_cast<float*>(wsb + sti::kWsStatusBytes);
     uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + sti::kWsStatusBytes + decode_scores_bytes(a));
+    // timing events; inside a stream capture they become event-record nodes of the graph
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
     auto mark = [&](int i) -> cudaError_t {
-        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+        if (!events) return cudaSuccess;
+        return cap == cudaStreamCaptureStatusActive
+                   ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), st, cudaEventRecordExternal)
+                   : cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
     };
     cudaError_t e = mark(0);
     if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
@@ -383,13 +392,18 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
         if (s != STI_OK) return s;
     }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
-    // top-k of the compressed positions (+W) and the ring's window indices, one kernel
+    // top-k of the compressed positions (+W) and the ring's window indices, one kernel.  It and the
+    // attention are programmatic dependents: each is scheduled while its predecessor drains, does
+    // the work that needs nothing of the step (window indices; Q load, TMEM and barriers), then
+    // waits for the predecessor grid before reading its output.  The scores kernel launches
+    // normally, so everything the caller enqueued before this call is complete before either.
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
-                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W);
+                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
-                  a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, st);
+                  a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, st,
+                  /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
@@ -455,11 +469,11 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
         if (s != STI_OK) return s;
     }
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
-                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W);
+                  a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
-                     st);
+                     st, /*pdl=*/a->n_cols > 0);
 }
 
 sti_status sti_decode_noalloc_status(uint32_t* flags, sti_stream stream) {

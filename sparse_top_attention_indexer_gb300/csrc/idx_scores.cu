@@ -113,7 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const IdxScoresParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
+    // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    griddep_launch_dependents();   // the top-k may be scheduled now; it waits for this grid's end
     const int a_bytes = kTileKeys * p.Di * 2;
     const int b_bytes = p.n_pad * p.Di * 2;
     uint8_t* a_ring = smem;

@@ -150,12 +150,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
     const int row = blockIdx.x;
     const int b = row / p.s, t = row - b * p.s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();
     const int sp = __ldg(p.start_pos + b);
     if (p.win_out != nullptr) {
         int32_t* wrow = p.win_out + (int64_t)row * p.row_stride;
         for (int i = tid; i < p.win_width; i += kTopkThreads) wrow[i] = window_slot(p.s, t, sp, p.win_W, i);
         if (tid == 0 && p.s > 1 && sp != 0 && p.status) atomicOr(p.status, 4u /* STI_FLAG_CHUNKED */);
     }
+    griddep_wait();   // the scores (and histogram) are complete from here on
     int vis = (sp + t + 1) / p.ratio;
     vis = max(0, min(vis, p.n_cols));
     int32_t* out = p.idxs + (int64_t)row * p.row_stride;
@@ -262,6 +264,313 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
     // vis > k here, so exactly k entries were written; nothing to pad
 }
 
+// ---------------------------------------------------------------------------------------------
+// Cluster top-k for few long rows (decode): the CR CTAs of a cluster split one row into
+// contiguous chunks.  The first radix pass comes precomputed from the scores kernel, so every
+// CTA knows the threshold bin d1 without talking; rank 0 collects the bin's members (a few
+// hundred keys) from the cluster's shared memory and finishes the exact select (passes 2 and
+// 3); the CTAs then exchange their counts of selected keys and each writes its chunk's
+// positions at its offset, in ascending position order.
+
+constexpr int kClThreads = 256;
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClCandCap = 8192;   // threshold-bin members rank 0 can hold
+
+struct __align__(16) ClusterTopkSmem {
+    uint32_t hist[kBins];
+    int warp_tot[kClWarps];
+    int misc[8];
+    int n_cand;                 // this CTA's threshold-bin members
+    int pub_gt, pub_eq;         // this CTA's keys > tau and == tau
+    uint32_t pub_tau;           // (rank 0) the exact k-th key and how many keys == tau to take
+    int pub_need;
+    int pub_ok;                 // (rank 0) 1 if the candidates fitted and tau is valid
+};
+
+// 256-thread block scan (exclusive) with total.
+__device__ __forceinline__ int block_excl_scan256(int v, int* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += x;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    int wpre = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kClWarps; ++w) {
+        const int x = warp_tot[w];
+        wpre += w < warp ? x : 0;
+        tot += x;
+    }
+    __syncthreads();
+    total = tot;
+    return wpre + inc - v;
+}
+
+// Bin d* of `hist` (kBins bins, counts of matching keys) where the count from the top first
+// reaches `remaining`; *above = count in higher bins.  256 threads, 8 bins each.
+__device__ __forceinline__ int select_bin256(const uint32_t* hist, int remaining, int* warp_tot, int* misc,
+                                             int* above_out) {
+    const int tid = threadIdx.x;
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) local += (int)hist[8 * tid + i];
+    int total;
+    const int excl = block_excl_scan256(local, warp_tot, total);
+    int above = total - excl - local;
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+        const int bin = 8 * tid + i;
+        const int c = (int)hist[bin];
+        if (above < remaining && above + c >= remaining) {
+            misc[0] = bin;
+            misc[1] = above;
+        }
+        above += c;
+    }
+    __syncthreads();
+    const int d = misc[0];
+    *above_out = misc[1];
+    __syncthreads();
+    return d;
+}
+
+// Histogram over n keys from src (keys whose bits above hi_shift equal prefix), then select_bin256.
+template <typename Src>
+__device__ __forceinline__ int radix_pass256(Src src, int n, int hi_shift, int shift, int bits, uint32_t prefix,
+                                             int remaining, uint32_t* hist, int* warp_tot, int* misc,
+                                             int* above_out) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (int i = tid; i < kBins; i += kClThreads) hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kClThreads) {
+        const int j = base + tid;
+        bool m = false;
+        uint32_t dig = 0xFFFFFFFFu;
+        if (j < n) {
+            const uint32_t key = src(j);
+            m = (key >> hi_shift) == prefix;
+            if (m) dig = (key >> shift) & mask;
+        }
+        const unsigned peers = __match_any_sync(kFull, dig);
+        if (m && lane == __ffs(peers) - 1) atomicAdd(&hist[dig], (uint32_t)__popc(peers));
+    }
+    __syncthreads();
+    return select_bin256(hist, remaining, warp_tot, misc, above_out);
+}
+
+template <int CR>
+__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkParams p, int chunk_cap) {
+    extern __shared__ __align__(16) uint8_t cl_smem[];
+    ClusterTopkSmem* sm = reinterpret_cast<ClusterTopkSmem*>(cl_smem);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sm + 1);            // [chunk_cap] this CTA's chunk
+    uint32_t* cand = keys + chunk_cap;                               // [kClCandCap] (rank 0: all members)
+
+    const int row = blockIdx.x / CR, rank = blockIdx.x - (blockIdx.x / CR) * CR;
+    const int b = row / p.s, t = row - b * p.s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t* ghist = p.hist + (size_t)row * kBins;
+    griddep_launch_dependents();
+    // start_pos and the window indices depend on no earlier kernel of the step
+    const int sp = __ldg(p.start_pos + b);
+    if (p.win_out != nullptr && rank == 0) {
+        int32_t* wrow = p.win_out + (int64_t)row * p.row_stride;
+        for (int i = tid; i < p.win_width; i += kClThreads) wrow[i] = window_slot(p.s, t, sp, p.win_W, i);
+        if (tid == 0 && p.s > 1 && sp != 0 && p.status) atomicOr(p.status, 4u /* STI_FLAG_CHUNKED */);
+    }
+    griddep_wait();   // the scores and the histogram are complete from here on
+    uint32_t hreg[kBins / kClThreads];
+#pragma unroll
+    for (int i = 0; i < kBins / kClThreads; ++i) hreg[i] = __ldg(ghist + i * kClThreads + tid);
+    int vis = (sp + t + 1) / p.ratio;
+    vis = max(0, min(vis, p.n_cols));
+    int32_t* out = p.idxs + (int64_t)row * p.row_stride;
+
+    if (vis <= p.k) {   // every visible position is selected (row-uniform: the whole cluster returns)
+        if (rank == 0) {
+            for (int i = tid; i < p.k; i += kClThreads) out[i] = i < vis ? i + p.offset : -1;
+            for (int i = tid; i < kBins; i += kClThreads) ghist[i] = 0;
+        }
+        return;
+    }
+
+    // this CTA's chunk [lo, hi): whole warps of 32
+    const int chunk = (((vis + CR - 1) / CR) + 31) & ~31;
+    const int lo = min(vis, rank * chunk), hi = min(vis, lo + chunk);
+    const int n_mine = hi - lo;
+    const float* src = p.scores + (int64_t)row * p.n_cols;
+#pragma unroll
+    for (int i = 0; i < kBins / kClThreads; ++i) sm->hist[i * kClThreads + tid] = hreg[i];
+    // the chunk, eight loads in flight per thread
+    for (int base = 0; base < n_mine; base += 8 * kClThreads) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = base + u * kClThreads + tid;
+            v[u] = j < n_mine ? __ldg(src + lo + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = base + u * kClThreads + tid;
+            if (j < n_mine) keys[j] = float_key(v[u]);
+        }
+    }
+    if (tid == 0) sm->n_cand = 0;
+    __syncthreads();
+
+    // pass 1 from the precomputed histogram: the same d1 in every CTA
+    int above;
+    const int d1 = select_bin256(sm->hist, p.k, sm->warp_tot, sm->misc, &above);
+    const int remaining1 = p.k - above;
+    const int c1 = (int)sm->hist[d1];
+    // this CTA's members of bin d1
+    for (int base = 0; base < n_mine; base += kClThreads) {
+        const int j = base + tid;
+        const uint32_t key = j < n_mine ? keys[j] : 0u;
+        const bool m = j < n_mine && (key >> 21) == (uint32_t)d1;
+        const unsigned bal = __ballot_sync(kFull, m);
+        int wbase = 0;
+        if (lane == 0 && bal) wbase = atomicAdd(&sm->n_cand, __popc(bal));
+        wbase = __shfl_sync(kFull, wbase, 0);
+        const int at = wbase + __popc(bal & ((1u << lane) - 1u));
+        if (m && at < kClCandCap) cand[at] = key;
+    }
+    __syncthreads();
+    cluster_sync();   // #1: every CTA's members are in its shared memory; every CTA read the histogram
+
+    if (rank == 0) {
+        for (int i = tid; i < kBins; i += kClThreads) ghist[i] = 0;   // ready for the next call
+        // gather the members of the whole row (total c1) behind this CTA's own
+        // lane r of every warp reads rank r's count; warp w then copies rank w's members
+        const int my_cnt = lane < CR ? ld_dsmem_s32(dsmem_addr(&sm->n_cand, (uint32_t)lane)) : 0;
+        int incl = my_cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += x;
+        }
+        const int tot = __shfl_sync(kFull, incl, 31);
+        const bool fits = tot == c1 && tot <= kClCandCap;
+        if (fits && warp >= 1 && warp < CR) {
+            const int n_w = __shfl_sync(kFull, my_cnt, warp);
+            const int at = __shfl_sync(kFull, incl - my_cnt, warp);
+            for (int i0 = 0; i0 < n_w; i0 += 64) {   // two remote loads in flight per lane
+                const int i1 = i0 + lane, i2 = i0 + 32 + lane;
+                const uint32_t a1 = i1 < n_w ? ld_dsmem_u32(dsmem_addr(cand + i1, (uint32_t)warp)) : 0u;
+                const uint32_t a2 = i2 < n_w ? ld_dsmem_u32(dsmem_addr(cand + i2, (uint32_t)warp)) : 0u;
+                if (i1 < n_w) cand[at + i1] = a1;
+                if (i2 < n_w) cand[at + i2] = a2;
+            }
+        }
+        __syncthreads();
+        uint32_t prefix = (uint32_t)d1;
+        int remaining = remaining1;
+        if (fits) {
+            auto cand_at = [&](int j) -> uint32_t { return cand[j]; };
+            const int d2 = radix_pass256(cand_at, c1, 21, 10, 11, prefix, remaining, sm->hist, sm->warp_tot,
+                                         sm->misc, &above);
+            remaining -= above;
+            prefix = (prefix << 11) | (uint32_t)d2;
+            const int d3 = radix_pass256(cand_at, c1, 10, 0, 10, prefix, remaining, sm->hist, sm->warp_tot,
+                                         sm->misc, &above);
+            remaining -= above;
+            prefix = (prefix << 10) | (uint32_t)d3;
+        } else {
+            // too many members of one bin (heavy ties): passes 2 and 3 over the whole row
+            auto row_at = [&](int j) -> uint32_t { return float_key(__ldg(src + j)); };
+            const int d2 = radix_pass256(row_at, vis, 21, 10, 11, prefix, remaining, sm->hist, sm->warp_tot,
+                                         sm->misc, &above);
+            remaining -= above;
+            prefix = (prefix << 11) | (uint32_t)d2;
+            const int d3 = radix_pass256(row_at, vis, 10, 0, 10, prefix, remaining, sm->hist, sm->warp_tot,
+                                         sm->misc, &above);
+            remaining -= above;
+            prefix = (prefix << 10) | (uint32_t)d3;
+        }
+        if (tid == 0) {
+            sm->pub_tau = prefix;
+            sm->pub_need = remaining;
+        }
+    }
+    cluster_sync();   // #2: tau published
+    const uint32_t tau = ld_dsmem_u32(dsmem_addr(&sm->pub_tau, 0u));
+    const int need_eq = ld_dsmem_s32(dsmem_addr(&sm->pub_need, 0u));
+    static_assert(CR <= kClWarps && CR <= 32, "one warp per cluster rank");
+
+    // counts of this CTA's chunk, per warp segment (ordered compaction as in the one-CTA kernel)
+    const int seg = ((n_mine + kClWarps - 1) / kClWarps + 31) & ~31;
+    const int wlo = min(n_mine, warp * seg), whi = min(n_mine, wlo + seg);
+    int n_gt = 0, n_eq = 0;
+    for (int j0 = wlo; j0 < whi; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < whi ? keys[j] : 0u;
+        n_gt += __popc(__ballot_sync(kFull, j < whi && key > tau));
+        n_eq += __popc(__ballot_sync(kFull, j < whi && key == tau));
+    }
+    if (lane == 0) {
+        sm->warp_tot[warp] = n_gt;
+        sm->misc[warp] = n_eq;   // misc has 8 slots = kClWarps
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int g = 0, e = 0;
+        for (int w = 0; w < kClWarps; ++w) {
+            g += sm->warp_tot[w];
+            e += sm->misc[w];
+        }
+        sm->pub_gt = g;
+        sm->pub_eq = e;
+    }
+    __syncthreads();
+    cluster_sync();   // #3: every CTA's counts published
+    // offset of this CTA = keys selected by lower ranks; equal keys go to the lowest positions
+    // (lane r < rank reads rank r's counts; prefix over lanes gives the keys == tau before r)
+    int g_l = 0, e_l = 0;
+    if (lane < rank) {
+        g_l = ld_dsmem_s32(dsmem_addr(&sm->pub_gt, (uint32_t)lane));
+        e_l = ld_dsmem_s32(dsmem_addr(&sm->pub_eq, (uint32_t)lane));
+    }
+    int e_incl = e_l;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(kFull, e_incl, o);
+        if (lane >= o) e_incl += x;
+    }
+    int taken = g_l + max(0, min(e_l, need_eq - (e_incl - e_l)));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) taken += __shfl_xor_sync(kFull, taken, o);
+    const int base_out = taken;
+    const int eq_before = __shfl_sync(kFull, e_incl, 31);
+    // within the CTA: warp w's offset and equal-key budget
+    int w_gt_before = 0, w_eq_before = 0;
+    for (int w = 0; w < warp; ++w) {
+        w_gt_before += sm->warp_tot[w];
+        w_eq_before += sm->misc[w];
+    }
+    // keys == tau are taken in position order: lower ranks first, then lower warps
+    int pos = base_out + w_gt_before + max(0, min(w_eq_before, need_eq - eq_before));
+    int eq_seen = eq_before + w_eq_before;
+    for (int j0 = wlo; j0 < whi; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < whi ? keys[j] : 0u;
+        const bool gt = j < whi && key > tau;
+        const bool eq = j < whi && key == tau;
+        const unsigned eq_mask = __ballot_sync(kFull, eq);
+        const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
+        const bool take = gt || (eq && eq_rank < need_eq);
+        const unsigned take_mask = __ballot_sync(kFull, take);
+        const int at = pos + __popc(take_mask & ((1u << lane) - 1u));
+        if (take && at < p.k) out[at] = lo + j + p.offset;
+        pos += __popc(take_mask);
+        eq_seen += __popc(eq_mask);
+    }
+    cluster_sync();   // #4: no partner still reads this CTA's shared memory
+}
+
 }  // namespace
 
 cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, int width, int32_t* idxs,
@@ -277,13 +586,48 @@ cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, in
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
     const int rows = p.B * p.s;
     if (rows == 0) return cudaSuccess;
+    constexpr int CR = 8;
+    if (p.hist != nullptr && rows * CR <= 8 * device_num_sms() && p.n_cols <= CR * 8192) {
+        // few long rows with the first pass precomputed: one cluster of CR CTAs per row
+        const int chunk_cap = ((((p.n_cols + CR - 1) / CR) + 31) & ~31);
+        const size_t smem = sizeof(ClusterTopkSmem) + (size_t)(chunk_cap + kClCandCap) * 4;
+        cudaError_t err =
+            cudaFuncSetAttribute(topk_cluster_kernel<CR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(rows * CR));
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CR;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.pdl ? 2 : 1;
+        err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<CR>, p, chunk_cap);
+        return err != cudaSuccess ? err : cudaGetLastError();
+    }
     const int use_smem = p.n_cols <= kSmemKeyCap ? 1 : 0;
     const size_t smem = (size_t)(kBins + kWarps + 8 + kCandCap + (use_smem ? p.n_cols : 0)) * 4;
     auto kern = p.hist != nullptr ? topk_kernel<true> : topk_kernel<false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<rows, kTopkThreads, smem, stream>>>(p, use_smem);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    err = cudaLaunchKernelEx(&cfg, kern, p, use_smem);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace sti

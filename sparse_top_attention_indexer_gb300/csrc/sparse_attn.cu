@@ -38,7 +38,7 @@
 namespace sti {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: warps w and w+4 share TMEM lanes, split the 64 head columns
 constexpr int kRows = 128;        // KV rows per tile (MMA M)
 constexpr int kHp = 64;           // heads padded (MMA N)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -49,8 +49,9 @@ struct __align__(8) AttnSmemTail {
     uint64_t mma_bar;
     uint64_t q_bar;        // Q tile landed (TMA)
     uint64_t gather_bar;   // this tile's rows landed (TMA)
+    uint64_t recv_bar;     // cluster partners' O slices landed (bulk copies)
     uint32_t tmem_base;
-    uint32_t pad;
+    int rescale;           // some head's running max moved in this tile
     float m_run[kHp];     // running max, log2 domain
     float l_run[kHp];     // running sum of 2^(x - m)
     float alpha[kHp];     // rescale factor of this tile
@@ -67,14 +68,14 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
     return (uint32_t)(ch >> 3) * (uint32_t)rows * 128u + (uint32_t)r * 128u + (uint32_t)(((ch & 7) ^ (r & 7)) << 4);
 }
 
-// Reduce-scatter of 64 per-lane values over the 32 lanes of a warp: afterwards lane l holds the
-// reduction (over the warp's 32 rows) of heads 2l and 2l+1 in v[0], v[1].
+// Reduce-scatter of 32 per-lane values over the 32 lanes of a warp: afterwards lane l holds in
+// v[0] the reduction over the warp's 32 rows of value l.
 template <bool IS_MAX>
-__device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64]) {
+__device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int step = 0; step < 5; ++step) {
-        const int half = 32 >> step;          // values still held: 2*half
+        const int half = 16 >> step;          // values still held: 2*half
         const int off = 16 >> step;           // partner lane distance
         const bool upper = (lane & off) != 0;
 #pragma unroll
@@ -104,13 +105,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
                        const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
+    // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* q_s = smem;                                 // [64 heads] x d_pad, K-major SW128
     uint8_t* kv_s = q_s + (size_t)kHp * p.d_pad * 2;     // [128 rows] x d_pad, SW128
     uint8_t* p_s = kv_s + (size_t)kRows * p.d_pad * 2;   // [128 rows] x 64 heads bf16, SW128
     AttnSmemTail* tl = reinterpret_cast<AttnSmemTail*>(p_s + kRows * 128);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row = tid & (kRows - 1);       // TMEM lane / KV row this thread owns
+    const int hg = tid >> 7;                 // head group: columns [32*hg, 32*hg + 32)
     const int C = p.cluster;
     const int query = blockIdx.x / C, rank = blockIdx.x - (blockIdx.x / C) * C;   // rank in the cluster
     const int b = query / p.s;
@@ -130,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->mma_bar, 1);
         mbar_init(&tl->q_bar, 1);
         mbar_init(&tl->gather_bar, 1);
+        mbar_init(&tl->recv_bar, 1);
         fence_mbar_init();
     }
     if (tid < kHp) {
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tl->tmem_base;
     STI_TSTAMP(1);
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // this warp's TMEM lane quarter
     const uint32_t tm_s = tmem;              // S^T: columns [0, 64)
     const uint32_t tm_o = tmem + 64;         // O^T block m: columns [64 + 64m, 128 + 64m)
     const int nmb = p.d_pad / 128;           // d blocks of 128
@@ -183,10 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idesc_pv = idesc_bf16_f32(128, kHp, true, true);
     const int32_t* idx_row = p.idx + (size_t)query * p.idx_stride;
     const int n_rows = p.n1 + p.n2;
+    griddep_wait();   // the indices are complete from here on (Q, KV and the sink come from the caller)
 
     for (int tile = tile_begin; tile < tile_end; ++tile) {
-        // ---- gather: thread r resolves slot r of the tile
-        {
+        // ---- gather: thread r < 128 resolves slot r of the tile
+        if (tid == 0) tl->rescale = 0;
+        if (tid < kRows) {
             const int slot = slot_begin + tile * kRows + tid;
             int idx = slot < slot_end ? __ldg(idx_row + slot) : -1;
             if (idx < -1 || idx >= n_rows) {
@@ -200,6 +208,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tl->row_valid[tid] = idx >= 0;
             tl->row_coord[tid] = (int)coord;
             tl->row_srcid[tid] = srcid;
+            // the next tile's row goes to L2 now, so its gather does not wait on HBM
+            const int nslot = slot + kRows;
+            if (tile + 1 < tile_end && nslot < slot_end) {
+                const int nidx = __ldg(idx_row + nslot);
+                if (nidx >= 0 && nidx < n_rows) {
+                    const uint16_t* nsrc = nidx < p.n1 ? p.kv + (size_t)b * p.kv_bstride + (size_t)nidx * p.d
+                                                       : p.kv2 + (size_t)b * p.kv2_bstride + (size_t)(nidx - p.n1) * p.d;
+                    prefetch_l2_bulk(nsrc, (uint32_t)p.d * 2);
+                }
+            }
         }
         __syncthreads();
         const uint32_t kv_base = smem_u32(kv_s);
@@ -208,6 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // warp 0: lane g gathers rows 4g..4g+3, one 4-row TMA per 128-byte column block.  Masked
             // slots load a real row of the same source (their score is -inf, so P = 0); a group whose
             // rows come from both sources is copied with cp.async instead.
+            if (tid < kRows) {   // rows of 4-row groups with no valid slot get no copy: zero them here
+                const int g0 = tid & ~3;
+                const bool all_masked = tl->row_srcid[g0] < 0 && tl->row_srcid[g0 + 1] < 0 &&
+                                        tl->row_srcid[g0 + 2] < 0 && tl->row_srcid[g0 + 3] < 0;
+                if (all_masked)
+                    for (int cb = 0; cb < ncb_real; ++cb) {
+                        uint4* row = reinterpret_cast<uint4*>(kv_s + (size_t)cb * kRows * 128 + (size_t)tid * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                    }
+            }
             if (warp == 0) {
                 const int g = lane;
                 int sid[4], crd[4];
@@ -224,18 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool mixed = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) mixed = mixed || (sid[i] >= 0 && sid[i] != S);
-                if (S < 0) {
-                    S = p.default_src;
-                    fc = (int)(b * (S == 0 ? p.rows1 : p.rows2));
-                }
+                const bool empty = S < 0;   // zero-filled above
+
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (sid[i] != S) crd[i] = fc;
-                const unsigned tma_groups = __ballot_sync(kFull, !mixed);
+                const unsigned tma_groups = __ballot_sync(kFull, !mixed && !empty);
                 if (lane == 0 && !dead)
                     mbar_arrive_expect_tx(&tl->gather_bar, (uint32_t)(__popc(tma_groups) * ncb_real * 512));
                 __syncwarp();
-                if (!dead) {
+                if (!dead && !empty) {
                     if (!mixed) {
                         const void* map = S == 0 ? (const void*)&tm_kv1 : (const void*)&tm_kv2;
                         for (int cb = 0; cb < ncb_real; ++cb)
@@ -290,77 +317,71 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // ---- online softmax (thread = row, 64 heads in registers)
         if (tile < 2) STI_TSTAMP(3 + 4 * tile);
-        float x[kHp];
+        float x[32];   // this thread's row, heads [32*hg, 32*hg + 32)
         {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(tm_s + lane_base, r0);
-            tmem_ld32(tm_s + lane_base + 32, r1);
+            uint32_t r0[32];
+            tmem_ld32(tm_s + lane_base + (uint32_t)(32 * hg), r0);
             tmem_ld_wait();
-            const bool valid = tl->row_valid[tid] != 0;
+            const bool valid = tl->row_valid[row] != 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                x[i] = valid ? __uint_as_float(r0[i]) * p.scale_log2 : -INFINITY;
-                x[i + 32] = valid ? __uint_as_float(r1[i]) * p.scale_log2 : -INFINITY;
-            }
+            for (int i = 0; i < 32; ++i) x[i] = valid ? __uint_as_float(r0[i]) * p.scale_log2 : -INFINITY;
         }
         {
-            float v[kHp];
+            float v[32];
 #pragma unroll
-            for (int i = 0; i < kHp; ++i) v[i] = x[i];
-            warp_reduce_scatter64<true>(v);
-            tl->red[warp][2 * lane] = v[0];
-            tl->red[warp][2 * lane + 1] = v[1];
+            for (int i = 0; i < 32; ++i) v[i] = x[i];
+            warp_reduce_scatter32<true>(v);
+            tl->red[warp & 3][32 * hg + lane] = v[0];
         }
         __syncthreads();
         if (tid < kHp) {
             const float mt = fmaxf(fmaxf(tl->red[0][tid], tl->red[1][tid]), fmaxf(tl->red[2][tid], tl->red[3][tid]));
             const float m_old = tl->m_run[tid];
-            const float m_new = fmaxf(m_old, mt);
-            tl->alpha[tid] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+            // keep the running max unless this tile's max passes it by more than 8 (log2 units):
+            // every P stays <= 2^8, and O and l are rescaled only when some head's max moves
+            const float m_new = (m_old == -INFINITY || mt > m_old + 8.f) ? fmaxf(m_old, mt) : m_old;
+            const float a = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+            tl->alpha[tid] = a;
             tl->m_run[tid] = m_new;
+            if (a != 1.f) tl->rescale = 1;
         }
         __syncthreads();
         {
-            float v[kHp];
+            float v[32];
 #pragma unroll
-            for (int i = 0; i < kHp; ++i) {
-                const float m = tl->m_run[i];
+            for (int i = 0; i < 32; ++i) {
+                const float m = tl->m_run[32 * hg + i];
                 x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
                 v[i] = x[i];
             }
-            // P^T row (this thread's row): 64 heads as bf16, 8 chunks of 16 bytes, swizzled
-            uint8_t* prow = p_s + tid * 128;
+            // P^T row: heads [32*hg, 32*hg+32) as bf16 = 16-byte chunks 4*hg .. 4*hg+3, swizzled
+            uint8_t* prow = p_s + row * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint4 pk;
                 pk.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
                 pk.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
                 pk.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
                 pk.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = pk;
+                *reinterpret_cast<uint4*>(prow + (((4 * hg + c) ^ (row & 7)) << 4)) = pk;
             }
-            warp_reduce_scatter64<false>(v);
-            tl->red[warp][2 * lane] = v[0];   // every read of the maxima happened before the last barrier
-            tl->red[warp][2 * lane + 1] = v[1];
+            warp_reduce_scatter32<false>(v);
+            tl->red[warp & 3][32 * hg + lane] = v[0];   // every read of the maxima preceded the last barrier
         }
         __syncthreads();
         if (tid < kHp)
             tl->l_run[tid] = tl->l_run[tid] * tl->alpha[tid] + (tl->red[0][tid] + tl->red[1][tid]) +
                              (tl->red[2][tid] + tl->red[3][tid]);
-        // rescale the running O^T (lane = d within a block, column = head)
-        if (tile > tile_begin && !dead) {
+        // rescale the running O^T (lane = d within a block, column = head) when some max moved
+        if (tile > tile_begin && !dead && tl->rescale) {
             for (int m = 0; m < nmb; ++m) {
+                uint32_t r[32];
+                const uint32_t ta = tm_o + lane_base + (uint32_t)(64 * m + 32 * hg);
+                tmem_ld32(ta, r);
+                tmem_ld_wait();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t r[32];
-                    const uint32_t ta = tm_o + lane_base + (uint32_t)(64 * m + 32 * half);
-                    tmem_ld32(ta, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[32 * half + i]);
-                    tmem_st32(ta, r);
-                }
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[32 * hg + i]);
+                tmem_st32(ta, r);
             }
             tmem_st_wait();
         }
@@ -408,11 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.lse && tid < p.h) p.lse[(size_t)query * p.h + tid] = lse;
         }
         __syncthreads();
-        uint16_t* orow = p.out + (size_t)query * p.h * p.d;
+        // the query's [h][d] bf16 output, staged in the free Q buffer, leaves in one bulk store
+        uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
         for (int m = 0; m < nmb; ++m) {
-            const int dd = 128 * m + tid;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            const int dd = 128 * m + row;
+            {
+                const int half = hg;   // this thread's 32 head columns
                 uint32_t r[32];
                 if (has_tiles) {
                     tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), r);
@@ -425,22 +447,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int hh = 32 * half + i;
-                        if (hh < p.h) {
-                            const float v = __uint_as_float(r[i]) * tl->alpha[hh];
-                            orow[(size_t)hh * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-                        }
+                        if (hh < p.h)
+                            stage[(size_t)hh * p.d + dd] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[hh]));
                     }
                 }
             }
         }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(p.out + (size_t)query * p.h * p.d, stage, (uint32_t)(p.h * p.d * 2));
+            bulk_commit();
+            bulk_wait_all();
+        }
     } else {
-        // ---- cluster reduction through distributed shared memory
+        // ---- cluster reduction.  Rank r owns output columns [r*dper, (r+1)*dper) of every head.
+        // Each CTA scales its O^T by 2^(m_cta - M) / L, writes the slices the other ranks own into
+        // its shared memory ([64][dper] fp32, head-major) and pushes them into the owners' shared
+        // memory with bulk copies; each owner adds them to its own slice, read again from TMEM.
+        // Nothing but the output goes to global memory.
         if (!has_tiles && tid < kHp) tl->m_run[tid] = -INFINITY;   // nothing valid here
-        cluster_sync();                                            // every CTA's m, l are final
+        const int dper = p.d / C;                  // multiple of 32 (host choice)
+        const uint32_t slice_elems = (uint32_t)dper * kHp;
+        const uint32_t slice_bytes = slice_elems * 4u;
+        // freed shared memory: the KV tile, then Q; outgoing slices first, then receive slots
+        const size_t kv_slots = ((size_t)kRows * p.d_pad * 2) / slice_bytes;
+        auto region = [&](int i) -> uint8_t* {
+            return (size_t)i < kv_slots ? kv_s + (size_t)i * slice_bytes : q_s + ((size_t)i - kv_slots) * slice_bytes;
+        };
+        auto out_slot = [&](int j) { return reinterpret_cast<float*>(region(j)); };          // to j-th other rank
+        auto recv_slot = [&](int j) { return reinterpret_cast<float*>(region(C - 1 + j)); }; // from j-th other rank
+        if (tid == 0 && !dead) mbar_arrive_expect_tx(&tl->recv_bar, (uint32_t)(C - 1) * slice_bytes);
+        cluster_sync();                            // every CTA's m, l are final
         STI_TSTAMP(11);
         if (tid < kHp) {
-            // every partner's (m, l) in flight at once, then combined
-            float mr[8], lr[8];
+            float mr[8], lr[8];                    // every partner's (m, l) in flight at once
 #pragma unroll
             for (int r = 0; r < 8; ++r)
                 if (r < C) {
@@ -464,66 +506,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[(size_t)query * p.h + tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
         }
         __syncthreads();
-        // this CTA's normalised share of O^T -> own shared memory (the KV tile is free now):
-        // row dd holds 64 heads as 16 chunks of 4 floats, chunk c stored at c ^ (dd & 15)
-        float* dump = reinterpret_cast<float*>(kv_s);
         for (int m = 0; m < nmb; ++m) {
-            const int dd = 128 * m + tid;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
+            const int dd = 128 * m + row;          // TMEM block m holds columns [128m, 128m + 128)
+            const int owner = dd / dper;           // warp-uniform: dper is a multiple of 32
+            if (owner == rank) continue;
+            float* dst = out_slot(owner < rank ? owner : owner - 1) + (dd - owner * dper);
+            {
+                const int half = hg;   // this thread's 32 head columns
+                uint32_t v[32];
                 if (has_tiles) {
-                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), r);
+                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), v);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int hc = 8 * half + c;
-                    float4 v;
-                    v.x = __uint_as_float(r[4 * c + 0]) * tl->alpha[4 * hc + 0];
-                    v.y = __uint_as_float(r[4 * c + 1]) * tl->alpha[4 * hc + 1];
-                    v.z = __uint_as_float(r[4 * c + 2]) * tl->alpha[4 * hc + 2];
-                    v.w = __uint_as_float(r[4 * c + 3]) * tl->alpha[4 * hc + 3];
-                    *reinterpret_cast<float4*>(dump + (size_t)dd * kHp + ((hc ^ (dd & 15)) << 2)) = v;
+                for (int i = 0; i < 32; ++i) {
+                    const int hh = 32 * half + i;
+                    dst[(size_t)hh * dper] = __uint_as_float(v[i]) * tl->alpha[hh];
                 }
             }
         }
-        cluster_sync();   // every CTA's share is in its shared memory
+        fence_proxy_async_smem();                  // the bulk-copy engine reads these writes
+        cluster_sync();                            // slices written; every receiver armed and free
         STI_TSTAMP(12);
-        // CTA `rank` sums d in [rank*dper, (rank+1)*dper) over the cluster and writes the output
-        const int dper = (p.d + C - 1) / C;
-        const int d_lo = rank * dper, d_hi = min(p.d, d_lo + dper);
+        if (tid == 0 && !dead) {
+            for (int o = 0; o < C; ++o) {
+                if (o == rank) continue;
+                const int j = rank < o ? rank : rank - 1;   // this CTA's partner index in o's view
+                bulk_copy_to_peer(dsmem_addr(recv_slot(j), (uint32_t)o), out_slot(o < rank ? o : o - 1),
+                                  slice_bytes, dsmem_addr(&tl->recv_bar, (uint32_t)o));
+            }
+            bulk_commit();
+        }
+        if (!dead) dead = !mbar_wait(&tl->recv_bar, 0, p.status);
+        STI_TSTAMP(15);
+        if (tid == 0) bulk_wait_read_all();        // outgoing slices read: their space is free again
+        __syncthreads();
+        // own slice: O^T from TMEM, scaled, plus the received slices; staged as [h][dper] bf16 in the
+        // first outgoing slot and bulk-stored one head row (dper columns) at a time
         uint16_t* orow = p.out + (size_t)query * p.h * p.d;
-        const int n_hc = (p.h + 3) / 4;
-        for (int dd = d_lo + tid; dd < d_hi; dd += kThreads) {
-            for (int hc = 0; hc < n_hc; ++hc) {
-                const float* loc = dump + (size_t)dd * kHp + ((hc ^ (dd & 15)) << 2);
-                float4 v[8];   // all partners' shares in flight before any is added
+        uint16_t* ostage = reinterpret_cast<uint16_t*>(out_slot(0));
+        for (int m = 0; m < nmb; ++m) {
+            const int dd = 128 * m + row;
+            if (dd / dper != rank || dd >= p.d) continue;
+            const int dl = dd - rank * dper;
+            {
+                const int half = hg;   // this thread's 32 head columns
+                uint32_t v[32];
+                if (has_tiles) {
+                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), v);
+                    tmem_ld_wait();
+                } else {
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r < C) v[r] = ld_dsmem_f4(dsmem_addr(loc, (uint32_t)r));
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+                float a[32];
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r < C) {
-                        acc.x += v[r].x;
-                        acc.y += v[r].y;
-                        acc.z += v[r].z;
-                        acc.w += v[r].w;
+                for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * tl->alpha[32 * half + i];
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {      // at most 3 partners: every load issued before the adds
+                    if (j < C - 1) {
+                        const float* rb = recv_slot(j) + (size_t)(32 * half) * dper + dl;
+                        float r[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = rb[(size_t)i * dper];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] += r[i];
                     }
-                const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int hh = 4 * hc + j;
-                    if (hh < p.h) orow[(size_t)hh * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(a4[j]));
+                for (int i = 0; i < 32; ++i) {
+                    const int hh = 32 * half + i;
+                    if (hh < p.h) ostage[(size_t)hh * dper + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(a[i]));
                 }
             }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid < p.h) {
+            bulk_store(orow + (size_t)tid * p.d + (size_t)rank * dper, ostage + (size_t)tid * dper, (uint32_t)dper * 2u);
+            bulk_commit();
+            bulk_wait_all();
         }
         STI_TSTAMP(13);
-        cluster_sync();   // partners finished reading this CTA's shared memory
     }
 
     tc_fence_before();
@@ -541,17 +608,21 @@ size_t attn_smem_bytes(int d_pad) {
 
 }  // namespace
 
-static int attn_pick_cluster_uncached(int n_queries, int k) {
+static int attn_pick_cluster_uncached(int n_queries, int k, int d) {
     const int num_sms = device_num_sms();
     const int max_c = (k + 63) / 64;          // at least 64 slots per CTA
     int c = n_queries > 0 ? num_sms / n_queries : 1;
-    if (c > 8) c = 8;
     if (c > max_c) c = max_c;
+    // the reduction exchanges fp32 column slices through the freed Q and KV buffers: 2 or 4
+    // CTAs, d a multiple of 128 split into slices of a multiple of 32 columns
+    c = c >= 4 ? 4 : (c >= 2 ? 2 : 1);
+    if (d % 128 != 0) c = 1;
+    while (c > 1 && (d / c) % 32 != 0) c /= 2;
     if (c <= 1) return 1;
     // shrink the cluster until all queries' clusters are resident at once
     const size_t smem = attn_smem_bytes(512);
     cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    for (; c > 1; --c) {
+    for (; c > 1; c /= 2) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(n_queries * c));
         cfg.blockDim = dim3(kThreads);
@@ -573,9 +644,9 @@ static int attn_pick_cluster_uncached(int n_queries, int k) {
     return 1;
 }
 
-int attn_pick_cluster(int n_queries, int k) {
+int attn_pick_cluster(int n_queries, int k, int d) {
     struct Entry {
-        int dev, n_queries, k, c;
+        int dev, n_queries, k, d, c;
     };
     static std::mutex mu;
     static std::vector<Entry> cache;
@@ -584,11 +655,11 @@ int attn_pick_cluster(int n_queries, int k) {
     {
         std::lock_guard<std::mutex> g(mu);
         for (const Entry& e : cache)
-            if (e.dev == dev && e.n_queries == n_queries && e.k == k) return e.c;
+            if (e.dev == dev && e.n_queries == n_queries && e.k == k && e.d == d) return e.c;
     }
-    const int c = attn_pick_cluster_uncached(n_queries, k);
+    const int c = attn_pick_cluster_uncached(n_queries, k, d);
     std::lock_guard<std::mutex> g(mu);
-    if (cache.size() < 4096) cache.push_back({dev, n_queries, k, c});
+    if (cache.size() < 4096) cache.push_back({dev, n_queries, k, d, c});
     return c;
 }
 
@@ -600,22 +671,27 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv
     cudaError_t err =
         cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    if (p.cluster <= 1) {
-        sparse_attn_kernel<<<n_queries, kThreads, smem, stream>>>(tm_q, tm_kv1, tm_kv2, p);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_queries * p.cluster));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (p.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = (unsigned)na;
     err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, tm_kv1, tm_kv2, p);
     return err != cudaSuccess ? err : cudaGetLastError();
 }

@@ -51,6 +51,7 @@ struct TopkParams {
     int B, s, n_cols, ratio, k;
     int32_t offset;
     int win_W, win_width;
+    int pdl;                  // launch as a programmatic dependent of the previous kernel in the stream
 };
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream);
 
@@ -74,9 +75,10 @@ struct AttnParams {
     int use_tma;             // gather rows with TMA (tensor maps valid); else 16-byte cp.async
     int64_t rows1, rows2;    // rows per batch element of kv / kv2 (batch stride / d)
     int default_src;         // source whose row 0 stands in for masked slots (0: kv, 1: kv2)
+    int pdl;                 // launch as a programmatic dependent of the previous kernel in the stream
 };
-// CTAs per query for n_queries queries of k slots (1 = no cluster); cached per device.
-int attn_pick_cluster(int n_queries, int k);
+// CTAs per query for n_queries queries of k slots and head dim d (1 = no cluster); cached per device.
+int attn_pick_cluster(int n_queries, int k, int d);
 // tm_q: q as [B*s*h, d] (box 64 x h); tm_kv1 / tm_kv2: the sources as [B*rows, d] (box 64 x 1,
 // for 4-row gathers).  Ignored unless p.use_tma.
 cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,

@@ -74,6 +74,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic-proxy global accesses with later async-proxy (TMA/bulk) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n_threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
@@ -109,6 +114,19 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* map, uint64_t
         " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
         : "memory");
+}
+
+// Bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 without waiting.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ LSU async copies
@@ -218,6 +236,12 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------------------ thread-block clusters
 
+// Programmatic dependent launch.  wait: block until the grids this one depends on have completed
+// and their memory is visible (returns at once when the launch had no programmatic dependency).
+// launch_dependents: let the next grid in the stream be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // Hardware barrier across every thread of every CTA in the cluster; release/acquire order the
 // CTAs' shared-memory writes before it with their partners' reads after it.
 __device__ __forceinline__ void cluster_sync() {
@@ -237,6 +261,14 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) { return (int)ld_dsmem_u32(addr); }
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -244,6 +276,33 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to another CTA's shared
+// memory in the cluster; completion is signalled on the destination CTA's mbarrier.  Both
+// destination addresses come from dsmem_addr().
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+// 1-D bulk copy this CTA's shared memory -> global (16-byte aligned, size a multiple of 16);
+// completes as part of this thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Wait until every bulk copy this thread committed has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk copy this thread committed has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ misc

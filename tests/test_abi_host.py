@@ -96,6 +96,6 @@ def test_window_width_reported(libsti):
 def test_workspace_sizes(libsti):
     assert libsti.sti_idx_scores_workspace_size() >= 4
     assert libsti.sti_idx_topk_workspace_size() >= 4
-    # attention keeps only the status word there (split queries reduce in distributed shared memory)
+    # attention keeps only the status word there (split queries meet in distributed shared memory)
     assert libsti.sti_sparse_attn_workspace_size(2, 1, 64, 512, 640) == 256
     assert libsti.sti_sparse_attn_workspace_size(4096, 1, 64, 512, 640) == 256

@@ -209,3 +209,36 @@ def test_decode_fused_small(sti, orc):
     np.testing.assert_array_equal(got_idx[..., :W], ref_widx)
     check_topk_rows(got_idx[..., W:], ref_cidx, ref_scores, W, shp.topk)
     check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
+
+
+@pytest.mark.parametrize("probs,label", [((0.02, 0.49, 0.49), "tau bin fits: ~800 tied keys across every chunk"),
+                                         ((0.34, 0.33, 0.33), "tau bin too large: whole-row passes")])
+def test_decode_fused_topk_ties(sti, orc, probs, label):
+    """Index keys drawn from three distinct rows, so every score is one of three values and the
+    k-th largest is tied across the whole row: the selection must take the tied keys in position
+    order, across the chunks the row is split into."""
+    import torch
+
+    shp = workloads.custom("decode_ties", b=2, s=1, start_pos=[159999, 100000], seed=81, n_cols=40000, topk=512,
+                           h=64, d=512)
+    data = workloads.make(shp)
+    rng = rng_for(820, int(probs[0] * 100))
+    groups = to_bf16_bits(rng.standard_normal((3, shp.Di)))
+    pick = rng.choice(3, size=(shp.b, shp.n_cols), p=probs)
+    data["ik"] = np.ascontiguousarray(groups[pick])
+    sp = data["start_pos"]
+    ref_scores = orc.index_score(data["iq"], data["ik"], data["w"], shp.index_scale, sp, shp.n_cols, shp.ratio)
+    for bi in range(shp.b):   # the three values must be well apart for the order to be unambiguous
+        vals = np.unique(ref_scores[bi, 0][np.isfinite(ref_scores[bi, 0])])
+        assert len(vals) == 3 and np.min(np.diff(vals)) > 1e-3 * np.max(np.abs(vals)), label
+    ref_cidx = orc.topk(ref_scores, sp, shp.ratio, shp.topk, shp.window)
+    a, out, tk = sti.decode_args(to_dev(data["q"][0]), to_dev(data["win"][0]), to_dev(data["comp"]),
+                                 to_dev_any(data["sink"][0]), shp.softmax_scale, to_dev(data["iq"]),
+                                 to_dev(data["ik"]), to_dev(data["w"]), shp.index_scale, to_dev_any(sp), shp.ratio,
+                                 shp.n_cols, shp.topk)
+    ws = sti.workspace(sti.decode_workspace_size(a))
+    sti.decode_fused(a, ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got = tk.cpu().numpy().reshape(shp.b, 1, -1)[..., shp.window:]
+    np.testing.assert_array_equal(got, ref_cidx)
