@@ -146,12 +146,16 @@ sti_status sti_idx_topk(const float *scores, const int32_t *start_pos, int b, in
  *   lse: optional fp32 [b, seqlen, h] = ln(sum_i e^{s_i} + e^{sink}); -inf for a query with
  *        no valid slot; may be NULL.
  * Indices < -1 or >= n1+n2 are treated as masked and raise STI_FLAG_INDEX_RANGE.
- * With few queries (decode) a query's slots are split over a thread-block cluster of 2 or 4
- * CTAs; their partial outputs meet in distributed shared memory and each CTA of the cluster
- * finishes a slice of the head dimension.  The workspace holds only the status word.
+ * With few queries (decode) a query's slots are split over a thread-block cluster of 2, 4 or 8
+ * CTAs.  They exchange their softmax maxima and sums in distributed shared memory, add their
+ * rescaled partial outputs into an fp32 [b*seqlen, h, d] accumulator in the workspace (bulk
+ * reductions performed at L2), and each converts a slice of the head dimension to bf16 and
+ * zeroes it again.  sti_sparse_attn_workspace_size() includes that accumulator for batches of
+ * at most 256 queries (none beyond); a workspace of only 256 bytes is accepted too and then no
+ * query splits.
  * Supported: 1 <= h <= 64, d a multiple of 64 up to 512, k >= 1, kv_bstride/kv2_bstride
- * multiples of 8, q/kv/kv2/out 16-byte aligned.  ws: sti_sparse_attn_workspace_size(b, seqlen,
- * h, d, k) bytes.
+ * multiples of 8, q/kv/kv2/out 16-byte aligned.  ws: at least 256 bytes, up to
+ * sti_sparse_attn_workspace_size(b, seqlen, h, d, k).
  */
 size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k);
 sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,
@@ -198,7 +202,13 @@ typedef struct sti_decode_args {
     int32_t *topk_idxs;         /* int32 [b, W + index_topk] */
 } sti_decode_args;
 
-/* events: NULL, or 4 cudaEvent_t handles recorded on `stream` before step 1 and after steps
+/* Steps 2 and 3 launch as programmatic dependents of the step before them: each is scheduled
+ * while its predecessor drains and waits on the device before reading the predecessor's output
+ * (step 1 launches normally, so all work enqueued before the call is complete before any step).
+ * ws: sti_decode_workspace_size() bytes = status word, scores [b, n_cols] fp32, histograms
+ * [b, 2048] u32 and, for b <= 256, the attention accumulator [b, h, d] fp32; zero-filled once,
+ * left zeroed by every call that completes.
+ * events: NULL, or 4 cudaEvent_t handles recorded on `stream` before step 1 and after steps
  * 1, 2 and 3 (per-kernel timing). */
 size_t sti_decode_workspace_size(const sti_decode_args *a);
 sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream,
@@ -210,9 +220,11 @@ sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes,
  * sti_decode_fused, for callers that cannot hand the library a device workspace -- for example
  * a plugin inside a host runtime that owns every device allocation and offers no workspace
  * hook, or a serving loop that must never enter the CUDA allocator once it is running.  The
- * step's scratch (status word, scores, first-pass histograms) lives in one fixed array inside
- * this library instead: about 10 MiB of device memory that every GPU on which the library is
- * used holds until the process exits.  The call allocates and frees nothing.
+ * step's scratch (status word, scores, first-pass histograms, attention accumulator) lives in
+ * one fixed array inside this library instead: about 26 MiB of device memory that every GPU on
+ * which the library is used holds until the process exits.  The call allocates and frees
+ * nothing.  Batches of more than 128 queries (of 64 heads x 512) run the attention without
+ * splitting a query.
  *  - Limits: b <= STI_NOALLOC_MAX_BATCH and b * n_cols <= STI_NOALLOC_MAX_SCORES; larger calls
  *    return STI_ERR_TOO_LARGE before anything is enqueued.  Other checks as sti_decode_fused.
  *  - The first call on a device looks up the array's device address (once per device, with

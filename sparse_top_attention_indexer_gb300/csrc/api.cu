@@ -209,7 +209,8 @@ static sti_status topk_impl(const float* scores, const int32_t* start_pos, int b
 static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
                             int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
-                            uint16_t* out, float* lse, uint32_t* status, cudaStream_t st, bool pdl = false) {
+                            uint16_t* out, float* lse, uint32_t* status, float* acc, size_t acc_bytes,
+                            cudaStream_t st, bool pdl = false) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
@@ -244,7 +245,9 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.d = d;
     p.k = k;
     p.d_pad = ((d + 127) / 128) * 128;
-    p.cluster = sti::attn_pick_cluster(nq, k, d);
+    // a query splits over a cluster only when the caller's workspace holds its accumulator
+    p.acc = (acc != nullptr && acc_bytes >= (size_t)nq * h * d * sizeof(float)) ? acc : nullptr;
+    p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
     p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
     p.rows1 = n1 > 0 ? kv_bstride / d : 0;
@@ -267,6 +270,16 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     }
     cudaError_t e = sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
+}
+
+// Split queries add their partial outputs into a zeroed fp32 [queries, h, d] accumulator that
+// follows the status word in the workspace.  Only batches of at most 256 queries split (a split
+// needs at least two SMs per query), so larger batches need no accumulator.
+static constexpr int64_t kAttnSplitMaxQueries = 256;
+static size_t attn_acc_bytes(int b, int seqlen, int h, int d) {
+    const int64_t nq = (int64_t)b * seqlen;
+    if (nq <= 0 || nq > kAttnSplitMaxQueries || h < 1 || h > 64 || d < 1 || d > 512) return 0;
+    return sti::align_up((size_t)nq * (size_t)h * (size_t)d * sizeof(float), sti::kWsAlign);
 }
 
 extern "C" {
@@ -333,32 +346,34 @@ sti_status sti_idx_topk(const float* scores, const int32_t* start_pos, int b, in
 }
 
 size_t sti_sparse_attn_workspace_size(int b, int seqlen, int h, int d, int k) {
-    (void)b;
-    (void)seqlen;
-    (void)h;
-    (void)d;
     (void)k;
-    return sti::kWsStatusBytes;
+    return sti::kWsStatusBytes + attn_acc_bytes(b, seqlen, h, d);
 }
 
 sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
                                 int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                                 int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                                 uint16_t* out, float* lse, void* ws, size_t ws_bytes, sti_stream stream) {
-    if (!ws_ok(ws, ws_bytes, sti_sparse_attn_workspace_size(b, seqlen, h, d, k))) return STI_ERR_INVALID_ARG;
+    // the status word is required; the accumulator behind it is optional (without it no query splits)
+    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
+    float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sti::kWsStatusBytes);
     return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
-                     seqlen, h, d, k, out, lse, status_word(ws), static_cast<cudaStream_t>(stream));
+                     seqlen, h, d, k, out, lse, status_word(ws), acc, ws_bytes - sti::kWsStatusBytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
-// fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048]]
+// fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048] |
+//                          attention accumulator fp32 [b, h, d] (batches of at most 256)]
 static size_t decode_scores_bytes(const sti_decode_args* a) {
     return sti::align_up((size_t)a->b * (size_t)(a->n_cols > 0 ? a->n_cols : 1) * sizeof(float), sti::kWsAlign);
 }
 static size_t decode_hist_bytes(const sti_decode_args* a) { return (size_t)a->b * 2048 * sizeof(uint32_t); }
 
+static size_t decode_acc_bytes(const sti_decode_args* a) { return attn_acc_bytes(a->b, 1, a->h, a->d); }
+
 size_t sti_decode_workspace_size(const sti_decode_args* a) {
     if (!a || a->b <= 0) return sti::kWsStatusBytes;
-    return sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a);
+    return sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a) + decode_acc_bytes(a);
 }
 
 sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream,
@@ -374,6 +389,7 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     const int W = a->window_size, K = a->index_topk, k_total = W + K;
     float* scores = reinterpret_cast<float*>(wsb + sti::kWsStatusBytes);
     uint32_t* hist = reinterpret_cast<uint32_t*>(wsb + sti::kWsStatusBytes + decode_scores_bytes(a));
+    float* acc = reinterpret_cast<float*>(wsb + sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a));
     // timing events; inside a stream capture they become event-record nodes of the graph
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) cap = cudaStreamCaptureStatusNone;
@@ -402,8 +418,8 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     if (s != STI_OK) return s;
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
-                  a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, st,
-                  /*pdl=*/a->n_cols > 0);
+                  a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, acc,
+                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
@@ -418,7 +434,11 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
 
 static constexpr size_t kNoallocScoresOff = sti::kWsStatusBytes;
 static constexpr size_t kNoallocHistOff = kNoallocScoresOff + (size_t)STI_NOALLOC_MAX_SCORES * sizeof(float);
-static constexpr size_t kNoallocBytes = kNoallocHistOff + (size_t)STI_NOALLOC_MAX_BATCH * 2048 * sizeof(uint32_t);
+static constexpr size_t kNoallocAccOff = kNoallocHistOff + (size_t)STI_NOALLOC_MAX_BATCH * 2048 * sizeof(uint32_t);
+// attention accumulator for split queries: up to 128 queries of 64 heads x 512 (larger batches
+// run one CTA per query, which needs none)
+static constexpr size_t kNoallocAccBytes = (size_t)128 * 64 * 512 * sizeof(float);
+static constexpr size_t kNoallocBytes = kNoallocAccOff + kNoallocAccBytes;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
@@ -458,9 +478,13 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
     float* scores = reinterpret_cast<float*>(scratch + kNoallocScoresOff);
     uint32_t* hist = reinterpret_cast<uint32_t*>(scratch + kNoallocHistOff);
-    // the array still holds the previous call's data: zero the status word and the histograms
+    float* acc = reinterpret_cast<float*>(scratch + kNoallocAccOff);
+    const size_t acc_used = decode_acc_bytes(a) <= kNoallocAccBytes ? decode_acc_bytes(a) : 0;
+    // the array still holds the previous call's data: zero the status word, the histograms and
+    // the part of the accumulator this call may use
     cudaError_t e = cudaMemsetAsync(status, 0, sti::kWsStatusBytes, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(hist, 0, (size_t)a->b * 2048 * sizeof(uint32_t), st);
+    if (e == cudaSuccess && acc_used > 0) e = cudaMemsetAsync(acc, 0, acc_used, st);
     if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused_noalloc: cudaMemsetAsync");
     const int W = a->window_size, K = a->index_topk, k_total = W + K;
     if (a->n_cols > 0) {
@@ -473,7 +497,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     if (s != STI_OK) return s;
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
-                     st, /*pdl=*/a->n_cols > 0);
+                     acc, acc_used, st, /*pdl=*/a->n_cols > 0);
 }
 
 sti_status sti_decode_noalloc_status(uint32_t* flags, sti_stream stream) {

@@ -272,6 +272,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
 // 3); the CTAs then exchange their counts of selected keys and each writes its chunk's
 // positions at its offset, in ascending position order.
 
+#ifdef STI_TOPK_TIMING
+__device__ unsigned long long g_topk_t[2048][16];
+#define STI_KSTAMP(i)                                                                                  \
+    do {                                                                                               \
+        if (threadIdx.x == 0 && blockIdx.x < 2048) g_topk_t[blockIdx.x][i] = clock64();                \
+    } while (0)
+#define STI_KGSTAMP(i)                                                                                 \
+    do {                                                                                               \
+        if (threadIdx.x == 0 && blockIdx.x < 2048) g_topk_t[blockIdx.x][i] = global_timer_ns();        \
+    } while (0)
+#else
+#define STI_KSTAMP(i) \
+    do {              \
+    } while (0)
+#define STI_KGSTAMP(i) \
+    do {               \
+    } while (0)
+#endif
+
 constexpr int kClThreads = 256;
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClCandCap = 8192;   // threshold-bin members rank 0 can hold
@@ -374,6 +393,8 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
     const int b = row / p.s, t = row - b * p.s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t* ghist = p.hist + (size_t)row * kBins;
+    STI_KGSTAMP(14);
+    STI_KSTAMP(0);
     griddep_launch_dependents();
     // start_pos and the window indices depend on no earlier kernel of the step
     const int sp = __ldg(p.start_pos + b);
@@ -382,7 +403,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
         for (int i = tid; i < p.win_width; i += kClThreads) wrow[i] = window_slot(p.s, t, sp, p.win_W, i);
         if (tid == 0 && p.s > 1 && sp != 0 && p.status) atomicOr(p.status, 4u /* STI_FLAG_CHUNKED */);
     }
+    STI_KSTAMP(1);
     griddep_wait();   // the scores and the histogram are complete from here on
+    STI_KSTAMP(2);
     uint32_t hreg[kBins / kClThreads];
 #pragma unroll
     for (int i = 0; i < kBins / kClThreads; ++i) hreg[i] = __ldg(ghist + i * kClThreads + tid);
@@ -421,12 +444,14 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
     }
     if (tid == 0) sm->n_cand = 0;
     __syncthreads();
+    STI_KSTAMP(3);
 
     // pass 1 from the precomputed histogram: the same d1 in every CTA
     int above;
     const int d1 = select_bin256(sm->hist, p.k, sm->warp_tot, sm->misc, &above);
     const int remaining1 = p.k - above;
     const int c1 = (int)sm->hist[d1];
+    STI_KSTAMP(4);
     // this CTA's members of bin d1
     for (int base = 0; base < n_mine; base += kClThreads) {
         const int j = base + tid;
@@ -440,7 +465,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
         if (m && at < kClCandCap) cand[at] = key;
     }
     __syncthreads();
+    STI_KSTAMP(5);
     cluster_sync();   // #1: every CTA's members are in its shared memory; every CTA read the histogram
+    STI_KSTAMP(6);
 
     if (rank == 0) {
         for (int i = tid; i < kBins; i += kClThreads) ghist[i] = 0;   // ready for the next call
@@ -467,6 +494,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
             }
         }
         __syncthreads();
+        STI_KSTAMP(7);
         uint32_t prefix = (uint32_t)d1;
         int remaining = remaining1;
         if (fits) {
@@ -496,7 +524,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
             sm->pub_need = remaining;
         }
     }
+    STI_KSTAMP(8);
     cluster_sync();   // #2: tau published
+    STI_KSTAMP(9);
     const uint32_t tau = ld_dsmem_u32(dsmem_addr(&sm->pub_tau, 0u));
     const int need_eq = ld_dsmem_s32(dsmem_addr(&sm->pub_need, 0u));
     static_assert(CR <= kClWarps && CR <= 32, "one warp per cluster rank");
@@ -526,7 +556,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
         sm->pub_eq = e;
     }
     __syncthreads();
+    STI_KSTAMP(10);
     cluster_sync();   // #3: every CTA's counts published
+    STI_KSTAMP(11);
     // offset of this CTA = keys selected by lower ranks; equal keys go to the lowest positions
     // (lane r < rank reads rank r's counts; prefix over lanes gives the keys == tau before r)
     int g_l = 0, e_l = 0;
@@ -568,7 +600,10 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
         pos += __popc(take_mask);
         eq_seen += __popc(eq_mask);
     }
+    STI_KSTAMP(12);
     cluster_sync();   // #4: no partner still reads this CTA's shared memory
+    STI_KSTAMP(13);
+    STI_KGSTAMP(15);
 }
 
 }  // namespace
@@ -631,3 +666,10 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
 }
 
 }  // namespace sti
+
+#ifdef STI_TOPK_TIMING
+// profiling builds only: per-CTA clock64 stamps of the cluster top-k phases
+extern "C" int sti_dbg_topk_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_topk_t, sizeof(unsigned long long) * 16 * (size_t)n_blocks);
+}
+#endif

@@ -462,23 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_wait_all();
         }
     } else {
-        // ---- cluster reduction.  Rank r owns output columns [r*dper, (r+1)*dper) of every head.
-        // Each CTA scales its O^T by 2^(m_cta - M) / L, writes the slices the other ranks own into
-        // its shared memory ([64][dper] fp32, head-major) and pushes them into the owners' shared
-        // memory with bulk copies; each owner adds them to its own slice, read again from TMEM.
-        // Nothing but the output goes to global memory.
+        // ---- split query.  The CTAs of the cluster exchange their (m, l) in distributed shared
+        // memory; each scales its O^T by 2^(m_cta - M) / L and adds it into the query's fp32
+        // accumulator in global memory with bulk reductions (performed at L2).  After a cluster
+        // barrier rank r converts columns [r*dper, (r+1)*dper) of every head to bf16 and zeroes
+        // them again for the next call.
         if (!has_tiles && tid < kHp) tl->m_run[tid] = -INFINITY;   // nothing valid here
         const int dper = p.d / C;                  // multiple of 32 (host choice)
-        const uint32_t slice_elems = (uint32_t)dper * kHp;
-        const uint32_t slice_bytes = slice_elems * 4u;
-        // freed shared memory: the KV tile, then Q; outgoing slices first, then receive slots
-        const size_t kv_slots = ((size_t)kRows * p.d_pad * 2) / slice_bytes;
-        auto region = [&](int i) -> uint8_t* {
-            return (size_t)i < kv_slots ? kv_s + (size_t)i * slice_bytes : q_s + ((size_t)i - kv_slots) * slice_bytes;
-        };
-        auto out_slot = [&](int j) { return reinterpret_cast<float*>(region(j)); };          // to j-th other rank
-        auto recv_slot = [&](int j) { return reinterpret_cast<float*>(region(C - 1 + j)); }; // from j-th other rank
-        if (tid == 0 && !dead) mbar_arrive_expect_tx(&tl->recv_bar, (uint32_t)(C - 1) * slice_bytes);
         cluster_sync();                            // every CTA's m, l are final
         STI_TSTAMP(11);
         if (tid < kHp) {
@@ -506,89 +496,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.lse[(size_t)query * p.h + tid] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
         }
         __syncthreads();
-        for (int m = 0; m < nmb; ++m) {
-            const int dd = 128 * m + row;          // TMEM block m holds columns [128m, 128m + 128)
-            const int owner = dd / dper;           // warp-uniform: dper is a multiple of 32
-            if (owner == rank) continue;
-            float* dst = out_slot(owner < rank ? owner : owner - 1) + (dd - owner * dper);
-            {
-                const int half = hg;   // this thread's 32 head columns
+        float* acc_q = p.acc + (size_t)query * p.h * p.d;
+        if (has_tiles) {
+            // scaled O^T -> [h][d] fp32 in the freed KV tile (h*d*4 <= 64*d_pad*4 bytes), one
+            // bulk reduction per head row
+            float* stage = reinterpret_cast<float*>(kv_s);
+            for (int m = 0; m < nmb; ++m) {
+                const int dd = 128 * m + row;
                 uint32_t v[32];
-                if (has_tiles) {
-                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), v);
-                    tmem_ld_wait();
-                } else {
+                tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * hg), v);
+                tmem_ld_wait();
+                if (dd < p.d) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int hh = 32 * half + i;
-                    dst[(size_t)hh * dper] = __uint_as_float(v[i]) * tl->alpha[hh];
-                }
-            }
-        }
-        fence_proxy_async_smem();                  // the bulk-copy engine reads these writes
-        cluster_sync();                            // slices written; every receiver armed and free
-        STI_TSTAMP(12);
-        if (tid == 0 && !dead) {
-            for (int o = 0; o < C; ++o) {
-                if (o == rank) continue;
-                const int j = rank < o ? rank : rank - 1;   // this CTA's partner index in o's view
-                bulk_copy_to_peer(dsmem_addr(recv_slot(j), (uint32_t)o), out_slot(o < rank ? o : o - 1),
-                                  slice_bytes, dsmem_addr(&tl->recv_bar, (uint32_t)o));
-            }
-            bulk_commit();
-        }
-        if (!dead) dead = !mbar_wait(&tl->recv_bar, 0, p.status);
-        STI_TSTAMP(15);
-        if (tid == 0) bulk_wait_read_all();        // outgoing slices read: their space is free again
-        __syncthreads();
-        // own slice: O^T from TMEM, scaled, plus the received slices; staged as [h][dper] bf16 in the
-        // first outgoing slot and bulk-stored one head row (dper columns) at a time
-        uint16_t* orow = p.out + (size_t)query * p.h * p.d;
-        uint16_t* ostage = reinterpret_cast<uint16_t*>(out_slot(0));
-        for (int m = 0; m < nmb; ++m) {
-            const int dd = 128 * m + row;
-            if (dd / dper != rank || dd >= p.d) continue;
-            const int dl = dd - rank * dper;
-            {
-                const int half = hg;   // this thread's 32 head columns
-                uint32_t v[32];
-                if (has_tiles) {
-                    tmem_ld32(tm_o + lane_base + (uint32_t)(64 * m + 32 * half), v);
-                    tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-                float a[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = __uint_as_float(v[i]) * tl->alpha[32 * half + i];
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {      // at most 3 partners: every load issued before the adds
-                    if (j < C - 1) {
-                        const float* rb = recv_slot(j) + (size_t)(32 * half) * dper + dl;
-                        float r[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = rb[(size_t)i * dper];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) a[i] += r[i];
+                    for (int i = 0; i < 32; ++i) {
+                        const int hh = 32 * hg + i;
+                        if (hh < p.h) stage[(size_t)hh * p.d + dd] = __uint_as_float(v[i]) * tl->alpha[hh];
                     }
                 }
+            }
+            fence_proxy_async_smem();              // the bulk-copy engine reads these writes
+            __syncthreads();
+            if (tid < p.h) {
+                bulk_reduce_add_f32(acc_q + (size_t)tid * p.d, stage + (size_t)tid * p.d, (uint32_t)p.d * 4u);
+                bulk_commit();
+                bulk_wait_all();                   // the additions are performed
+            }
+            fence_proxy_async_global();
+        }
+        cluster_sync();                            // every partial is in the accumulator
+        STI_TSTAMP(12);
+        // this rank's columns: fp32 sums -> bf16 output, accumulator back to zero
+        const int q4 = dper / 4;                   // float4 per head row of this rank's slice
+        uint16_t* orow = p.out + (size_t)query * p.h * p.d + (size_t)rank * dper;
+        float* arow = acc_q + (size_t)rank * dper;
+        for (int e0 = 0; e0 < p.h * q4; e0 += 4 * kThreads) {
+            float4 v[4];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int hh = 32 * half + i;
-                    if (hh < p.h) ostage[(size_t)hh * dper + dl] = __bfloat16_as_ushort(__float2bfloat16_rn(a[i]));
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * kThreads + tid;
+                if (e < p.h * q4) {
+                    const int hh = e / q4, c4 = e - (e / q4) * q4;
+                    v[u] = __ldcg(reinterpret_cast<const float4*>(arow + (size_t)hh * p.d) + c4);
                 }
             }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid < p.h) {
-            bulk_store(orow + (size_t)tid * p.d + (size_t)rank * dper, ostage + (size_t)tid * dper, (uint32_t)dper * 2u);
-            bulk_commit();
-            bulk_wait_all();
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + u * kThreads + tid;
+                if (e < p.h * q4) {
+                    const int hh = e / q4, c4 = e - (e / q4) * q4;
+                    uint2 o;
+                    o.x = pack_bf16x2(v[u].x, v[u].y);
+                    o.y = pack_bf16x2(v[u].z, v[u].w);
+                    *reinterpret_cast<uint2*>(orow + (size_t)hh * p.d + 4 * c4) = o;
+                    __stcg(reinterpret_cast<float4*>(arow + (size_t)hh * p.d) + c4, make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+            }
         }
         STI_TSTAMP(13);
     }
@@ -613,9 +575,9 @@ static int attn_pick_cluster_uncached(int n_queries, int k, int d) {
     const int max_c = (k + 63) / 64;          // at least 64 slots per CTA
     int c = n_queries > 0 ? num_sms / n_queries : 1;
     if (c > max_c) c = max_c;
-    // the reduction exchanges fp32 column slices through the freed Q and KV buffers: 2 or 4
-    // CTAs, d a multiple of 128 split into slices of a multiple of 32 columns
-    c = c >= 4 ? 4 : (c >= 2 ? 2 : 1);
+    // 2, 4 or 8 CTAs (portable cluster sizes); after the reduction each converts a slice of
+    // d/c columns, d a multiple of 128 and the slice a multiple of 32
+    c = c >= 8 ? 8 : (c >= 4 ? 4 : (c >= 2 ? 2 : 1));
     if (d % 128 != 0) c = 1;
     while (c > 1 && (d / c) % 32 != 0) c /= 2;
     if (c <= 1) return 1;

@@ -76,6 +76,8 @@ struct AttnParams {
     int64_t rows1, rows2;    // rows per batch element of kv / kv2 (batch stride / d)
     int default_src;         // source whose row 0 stands in for masked slots (0: kv, 1: kv2)
     int pdl;                 // launch as a programmatic dependent of the previous kernel in the stream
+    float* acc;              // split queries: zeroed fp32 [B*s, h, d] the cluster adds its partials into
+                             // (left zeroed again); nullptr: no split
 };
 // CTAs per query for n_queries queries of k slots and head dim d (1 = no cluster); cached per device.
 int attn_pick_cluster(int n_queries, int k, int d);

@@ -296,6 +296,13 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                  "r"(bytes)
                  : "memory");
 }
+// dst[i] += src[i] for `bytes`/4 fp32 values: a bulk reduction from shared memory into global
+// memory, performed at L2 (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const float* src, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
 // Wait until every bulk copy this thread committed has completed (writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -96,6 +96,9 @@ def test_window_width_reported(libsti):
 def test_workspace_sizes(libsti):
     assert libsti.sti_idx_scores_workspace_size() >= 4
     assert libsti.sti_idx_topk_workspace_size() >= 4
-    # attention keeps only the status word there (split queries meet in distributed shared memory)
-    assert libsti.sti_sparse_attn_workspace_size(2, 1, 64, 512, 640) == 256
+    # attention: the status word, then (for batches that may split a query over a cluster) the
+    # fp32 [queries, h, d] accumulator the cluster adds its partial outputs into
+    assert libsti.sti_sparse_attn_workspace_size(2, 1, 64, 512, 640) == 256 + 2 * 64 * 512 * 4
+    assert libsti.sti_sparse_attn_workspace_size(256, 1, 64, 512, 640) == 256 + 256 * 64 * 512 * 4
     assert libsti.sti_sparse_attn_workspace_size(4096, 1, 64, 512, 640) == 256
+    assert libsti.sti_sparse_attn_workspace_size(1, 3, 4, 64, 32) == 256 + 3 * 4 * 64 * 4

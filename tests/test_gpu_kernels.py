@@ -158,6 +158,40 @@ def test_sparse_attn_whole_tiles_masked(sti, orc):
     assert np.all(got[3] == 0)
 
 
+@pytest.mark.parametrize("b,k", [(1, 640), (2, 640), (40, 640), (3, 129)])
+def test_sparse_attn_split_accumulator(sti, orc, b, k):
+    """Few decode queries split over a cluster (8, 4 or 2 CTAs) add into the workspace's fp32
+    accumulator: the result matches the oracle and the unsplit run (256-byte workspace), the
+    accumulator is zero again afterwards, and a second call on the same workspace agrees."""
+    import torch
+
+    rng = rng_for(730 + b, k)
+    h, d, n1, n2 = 64, 512, 128, 2000
+    q = to_bf16_bits(rng.standard_normal((b, 1, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = index_lists(rng, b, 1, k, n1 + n2, masked_frac=0.2)
+    ref, ref_lse = orc.sparse_attn(q, kv1, sink, idx, d ** -0.5, kv2=kv2)
+    args = (to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5)
+    ws = sti.workspace(sti.sparse_attn_workspace_size(b, 1, h, d, k))
+    assert ws.numel() == 256 + b * h * d * 4
+    outs = []
+    for _ in range(2):
+        lse = torch.empty(b, 1, h, dtype=torch.float32, device="cuda")
+        outs.append(sti.sparse_attn_sink(*args, kv2=to_dev(kv2), lse=lse, ws=ws))
+        torch.cuda.synchronize()
+        assert sti.read_device_status(ws) == 0
+        assert int(torch.count_nonzero(ws[256:])) == 0, "accumulator not left zeroed"
+        check_attn(bf16_out_to_f64(outs[-1]), ref)
+        np.testing.assert_allclose(lse.cpu().numpy().astype(np.float64), ref_lse, rtol=1e-4, atol=1e-4)
+    unsplit = sti.sparse_attn_sink(*args, kv2=to_dev(kv2), ws=sti.workspace(256))
+    check_attn(bf16_out_to_f64(unsplit), ref)
+    # the split and unsplit runs round the same fp32 values to bf16 except for summation order
+    diff = np.abs(bf16_out_to_f64(outs[0]) - bf16_out_to_f64(unsplit))
+    assert diff.max() <= 2e-2
+
+
 def test_sparse_attn_flags_out_of_range(sti, orc):
     rng = rng_for(710, 0)
     b, s, h, d, k, n1 = 1, 2, 8, 64, 20, 30
