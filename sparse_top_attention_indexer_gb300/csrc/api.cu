@@ -245,9 +245,11 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.d = d;
     p.k = k;
     p.d_pad = ((d + 127) / 128) * 128;
-    // a query splits over a cluster only when the caller's workspace holds its accumulator
+    // few queries of 32 or 64 heads: heads split over a cluster, tiles gathered once (multicast);
+    // otherwise a query's slots may split over a cluster when the workspace holds the accumulator
     p.acc = (acc != nullptr && acc_bytes >= (size_t)nq * h * d * sizeof(float)) ? acc : nullptr;
-    p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
+    const int c_hs = sti::attn_hs_pick(nq, h, d);
+    p.cluster = c_hs > 0 ? c_hs : (p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1);
     p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
     p.rows1 = n1 > 0 ? kv_bstride / d : 0;
@@ -260,15 +262,19 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     memset(&tm_q, 0, sizeof tm_q);
     memset(&tm_kv1, 0, sizeof tm_kv1);
     memset(&tm_kv2, 0, sizeof tm_kv2);
+    const bool head_split = c_hs > 0 && p.use_tma;
+    if (!head_split && c_hs > 0) p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
     if (p.use_tma) {
-        sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, (uint32_t)h);
+        const uint32_t q_rows = head_split ? (uint32_t)(h / c_hs) : (uint32_t)h;
+        sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, q_rows);
         if (s == STI_OK && n1 > 0) s = make_map_2d(&tm_kv1, kv, (uint64_t)d, (uint64_t)b * p.rows1, (uint64_t)d * 2, 64, 1);
         if (s == STI_OK && n2 > 0) s = make_map_2d(&tm_kv2, kv2, (uint64_t)d, (uint64_t)b * p.rows2, (uint64_t)d * 2, 64, 1);
         if (s != STI_OK) return s;
         if (n1 == 0) tm_kv1 = tm_kv2;
         if (n2 == 0) tm_kv2 = tm_kv1;
     }
-    cudaError_t e = sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
+    cudaError_t e = head_split ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, p, st)
+                               : sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
 

@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             bulk_store(p.out + (size_t)query * p.h * p.d, stage, (uint32_t)(p.h * p.d * 2));
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read_all();   // the stage may be released; the writes complete with the grid
         }
     } else {
         // ---- split query.  The CTAs of the cluster exchange their (m, l) in distributed shared

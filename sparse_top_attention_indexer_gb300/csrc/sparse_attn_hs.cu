@@ -1,0 +1,590 @@
+// sparse_attn_hs.cu -- sparse multi-head attention with an attention sink for few queries
+// (decode): a thread-block cluster per query splits the query's HEADS, and every KV tile is
+// gathered once into the shared memory of all CTAs of the cluster.
+//
+// DeepSeek V4.1, attention "attend/selected" page, sparse_attn_kernel / sparse_attn:
+//   for every query and head, over the slots i whose index is not -1:
+//     s_i = softmax_scale * q . kv[idx_i];  o = sum_i e^{s_i} kv[idx_i] / (sum_i e^{s_i} + e^{sink_h})
+//   the same row serving as key and value; a query with no valid slot gets 0.
+//
+// Why a head split: the heads of a query share every KV row, so a partial output over some rows
+// is as large as all heads' outputs (h x d fp32 = 128 KB for 64 x 512) -- splitting a query's
+// rows over CTAs makes them add up partials larger than the rows they read.  Splitting the heads
+// needs no reduction at all, provided each row is fetched once for the whole cluster:
+//   * cluster of C CTAs per query, CTA r owning heads [r*HC, (r+1)*HC) (HC = 16 or 32);
+//   * a tile = 128 KV rows = d/64 column blocks of 128 rows x 128 bytes (128-byte swizzle), held
+//     in a ring of S column-block slots.  CTA r gathers the tile's four-row groups g = r (mod C)
+//     with one TMA gather4 per column block, multicast to every CTA of the cluster, so each CTA
+//     receives the whole tile while issuing 1/C of it;
+//   * a slot is refilled only when all C CTAs have finished the PV product reading it: each CTA's
+//     MMA completion arrives on that slot's "empty" barrier in every CTA (multicast commit);
+//   * warp 0 resolves slots and issues the gathers, warp 1 allocates TMEM and issues the MMAs,
+//     warps 2-5 run the online softmax (thread = KV row) and the epilogue;
+//   * S^T = KV_tile . Q_r^T (tcgen05, M=128 rows x N=HC x K=d) accumulates column block by column
+//     block as the blocks land; O^T += V^T . P^T (M=128 d-block x N=HC x K=128 rows) reads the same
+//     tile as an MN-major operand, P^T being K-major bf16 [HC][128];
+//   * the output of the CTA's heads ([HC][d] bf16, contiguous) leaves in one bulk store.
+// Four-row groups with no valid slot are not fetched (their rows keep finite earlier contents,
+// the ring starting zeroed, and get probability 0); masked slots inside a group repeat one of
+// the group's valid rows; a group with rows of both sources fetches row by row.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+#include <vector>
+
+#include "sti_internal.h"
+#include "sti_ptx.cuh"
+
+namespace sti {
+namespace {
+
+#ifdef STI_ATTN_TIMING
+__device__ unsigned long long g_hs_t[2048][32];
+#define STI_HSTAMP(i)                                                                                  \
+    do {                                                                                               \
+        if (blockIdx.x < 2048) g_hs_t[blockIdx.x][i] = clock64();                                      \
+    } while (0)
+#else
+#define STI_HSTAMP(i) \
+    do {              \
+    } while (0)
+#endif
+
+constexpr int kHsThreads = 192;
+constexpr int kHsRows = 128;
+constexpr int kHsMaxSlots = 12;
+constexpr uint32_t kSlotBytes = kHsRows * 128;   // one column block of a tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+struct __align__(8) HsTail {
+    uint64_t full[kHsMaxSlots];    // slot filled (1 local arrival + the tile's bytes)
+    uint64_t empty[kHsMaxSlots];   // slot read by every CTA of the cluster (C arrivals)
+    uint64_t s_full[2];            // S^T of a tile in TMEM (double buffer)
+    uint64_t p_full;               // P^T written, O^T rescaled
+    uint64_t o_done;               // PV product of a tile complete
+    uint64_t q_bar;                // Q rows of this CTA's heads landed
+    uint32_t tmem_base;
+    int abort;                     // a wait of this CTA timed out: the others stop waiting
+    float m_run[32];               // running max per head, log2 domain
+    float l_run[32];               // running sum of 2^(x - m)
+    float alpha[32];               // rescale factor of this tile / final 1 / denominator
+    float red_max[4][32];          // per-warp partial maxima
+    float red_sum[4][32];          // per-warp partial sums
+};
+
+// Bounded wait that also gives up when another thread of the CTA already timed out.
+__device__ __forceinline__ bool hs_wait(uint64_t* bar, uint32_t parity, uint32_t* status, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
+            if (status) atomicOr(status, 2u /* STI_FLAG_TIMEOUT */);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Reduce N values per lane over the warp's 32 lanes, scattering the results: afterwards v[0] of
+// lane l is the reduction of value l >> (5 - log2 N) (each held by 32/N adjacent lanes).
+template <int N, bool IS_MAX>
+__device__ __forceinline__ void warp_reduce_scatter_n(float (&v)[N]) {
+    const int lane = threadIdx.x & 31;
+    int off = 16;
+#pragma unroll
+    for (int half = N / 2; half >= 1; half >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float lo = v[i], hi = v[i + half];
+            const float send = upper ? lo : hi;
+            const float keep = upper ? hi : lo;
+            const float recv = __shfl_xor_sync(kFull, send, off);
+            v[i] = IS_MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+#pragma unroll
+    for (; off >= 1; off >>= 1) {
+        const float recv = __shfl_xor_sync(kFull, v[0], off);
+        v[0] = IS_MAX ? fmaxf(v[0], recv) : v[0] + recv;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_ld16(taddr, r);
+    else tmem_ld32(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+    if constexpr (N == 16) tmem_st16(taddr, r);
+    else tmem_st32(taddr, r);
+}
+
+__host__ __device__ constexpr uint32_t hs_tmem_cols(int hc) { return hc == 16 ? 128u : 256u; }
+
+__host__ __device__ constexpr size_t hs_smem_bytes(int hc, int d, int slots) {
+    return 1024 + (size_t)slots * kSlotBytes + (size_t)hc * d * 2 + (size_t)hc * 256 + sizeof(HsTail);
+}
+
+template <int HC>
+__global__ void __launch_bounds__(kHsThreads, 1)
+    sparse_attn_hs_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
+                          const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p, int n_slots) {
+    static_assert(HC == 16 || HC == 32, "16 or 32 heads per CTA");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int S = n_slots;                                      // even, >= 2
+    uint8_t* ring = smem;                                       // S x [128 rows x 128 B], SW128
+    uint8_t* q_s = ring + (size_t)S * kSlotBytes;               // [d/64] x [HC x 128 B], SW128 K-major
+    uint8_t* p_s = q_s + (size_t)HC * p.d * 2;                  // P^T: [2] x [HC x 128 B], SW128 K-major
+    HsTail* tl = reinterpret_cast<HsTail*>(p_s + HC * 256);
+    volatile int* abort = &tl->abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int C = p.cluster;
+    const int query = blockIdx.x / C, rank = blockIdx.x - (blockIdx.x / C) * C;
+    const int b = query / p.s;
+    const int ncb = p.d / 64;                 // column blocks per tile
+    const int nmb = p.d / 128;                // d blocks of the PV product
+    const int n_tiles = (p.k + kHsRows - 1) / kHsRows;
+    const uint16_t cta_mask = (uint16_t)((1u << C) - 1u);
+    const int n_rows = p.n1 + p.n2;
+    const int32_t* idx_row = p.idx + (size_t)query * p.idx_stride;
+    if (tid == 0) STI_HSTAMP(0);
+
+    if (warp == 1) {
+        tmem_alloc(&tl->tmem_base, hs_tmem_cols(HC));
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&tl->full[i], 1);
+            mbar_init(&tl->empty[i], (uint32_t)C);
+        }
+        mbar_init(&tl->s_full[0], 1);
+        mbar_init(&tl->s_full[1], 1);
+        mbar_init(&tl->p_full, 1);
+        mbar_init(&tl->o_done, 1);
+        mbar_init(&tl->q_bar, 1);
+        tl->abort = 0;
+        fence_mbar_init();
+    }
+    if (tid < HC) {
+        tl->m_run[tid] = -INFINITY;
+        tl->l_run[tid] = 0.f;
+    }
+    {   // rows that no gather writes keep finite contents
+        uint4* r4 = reinterpret_cast<uint4*>(ring);
+        const int n16 = S * (int)kSlotBytes / 16;
+        for (int i = tid; i < n16; i += kHsThreads) r4[i] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    cluster_sync();   // every CTA's barriers initialised and ring zeroed before any multicast
+    tc_fence_after();
+    const uint32_t tmem = tl->tmem_base;
+    if (tid == 0) STI_HSTAMP(1);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_kv1);
+            tma_prefetch_desc(&tm_kv2);
+            mbar_arrive_expect_tx(&tl->q_bar, (uint32_t)(HC * p.d * 2));
+            for (int cb = 0; cb < ncb; ++cb)
+                tma_load_2d(q_s + (size_t)cb * HC * 128, &tm_q, &tl->q_bar, cb * 64, query * p.h + rank * HC);
+        }
+        griddep_wait();   // the indices are complete from here on
+        bool dead = false;
+        const bool mine = (lane % C) == rank;   // four-row group g = lane is this CTA's to fetch
+        for (int t = 0; t < n_tiles && !dead; ++t) {
+            int sid[4], crd[4];
+            int first_s = -1, first_c = 0, n_valid = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int slot = t * kHsRows + 4 * lane + i;
+                int idx = slot < p.k ? __ldg(idx_row + slot) : -1;
+                if (idx < -1 || idx >= n_rows) {
+                    if (rank == 0) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
+                    idx = -1;
+                }
+                sid[i] = idx < 0 ? -1 : (idx < p.n1 ? 0 : 1);
+                crd[i] = sid[i] < 0 ? 0 : (sid[i] == 0 ? b * (int)p.rows1 + idx : b * (int)p.rows2 + (idx - p.n1));
+                if (sid[i] >= 0) {
+                    ++n_valid;
+                    if (first_s < 0) {
+                        first_s = sid[i];
+                        first_c = crd[i];
+                    }
+                }
+            }
+            bool mixed = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mixed = mixed || (sid[i] >= 0 && sid[i] != first_s);
+            const bool empty = first_s < 0;
+            uint32_t tbytes = empty ? 0u : (mixed ? 128u * (uint32_t)n_valid : 512u);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) tbytes += __shfl_xor_sync(kFull, tbytes, o);
+            const void* map = first_s == 1 ? (const void*)&tm_kv2 : (const void*)&tm_kv1;
+            for (int j = 0; j < ncb; ++j) {
+                const int G = t * ncb + j, slot = G % S, use = G / S;
+                if (use > 0 && !dead) dead = !hs_wait(&tl->empty[slot], (uint32_t)((use - 1) & 1), p.status, abort);
+                dead = __any_sync(kFull, dead);
+                if (dead) break;
+                uint8_t* dst = ring + (size_t)slot * kSlotBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&tl->full[slot], tbytes);
+                if (mine && !empty) {
+                    if (!mixed) {
+                        // masked rows of the group repeat its first valid row
+                        tma_gather4_mc(dst + lane * 512, map, &tl->full[slot], j * 64, sid[0] >= 0 ? crd[0] : first_c,
+                                       sid[1] >= 0 ? crd[1] : first_c, sid[2] >= 0 ? crd[2] : first_c,
+                                       sid[3] >= 0 ? crd[3] : first_c, cta_mask);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (sid[i] >= 0)
+                                tma_load_2d_mc(dst + (4 * lane + i) * 128,
+                                               sid[i] == 1 ? (const void*)&tm_kv2 : (const void*)&tm_kv1,
+                                               &tl->full[slot], j * 64, crd[i], cta_mask);
+                    }
+                }
+            }
+            if (lane == 0 && t < 5) STI_HSTAMP(2 + t);
+        }
+        // every arrival the cluster makes on this CTA's barriers has landed before it may exit
+        const int total = n_tiles * ncb;
+        for (int s2 = 0; s2 < S && s2 < total && !dead; ++s2) {
+            const int uses = (total - s2 + S - 1) / S;
+            dead = !hs_wait(&tl->empty[s2], (uint32_t)((uses - 1) & 1), p.status, abort);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            bool dead = !hs_wait(&tl->q_bar, 0, p.status, abort);
+            const uint32_t idesc_qk = idesc_bf16_f32(kHsRows, HC, false, false);
+            const uint32_t idesc_pv = idesc_bf16_f32(128, HC, true, false);
+            const uint32_t q0 = smem_u32(q_s), p0 = smem_u32(p_s), r0 = smem_u32(ring);
+            // descriptors advance by their 16-byte address units: +2 per 32-byte K step
+            const uint64_t qd0 = sdesc(q0, 16, 1024, kLayoutSW128);
+            const uint64_t pd0 = sdesc(p0, 16, 1024, kLayoutSW128);
+            const uint64_t kd0 = sdesc(r0, 16, 1024, kLayoutSW128);               // K-major tile
+            const uint64_t vd0 = sdesc(r0, kSlotBytes, 1024, kLayoutSW128);       // MN-major tile
+            int qk_t = 0, qk_j = 0;   // next QK column block to issue
+            // QK for column block (qk_t, qk_j); `block`: wait for its data, else only if landed
+            auto issue_qk = [&](bool block) -> bool {
+                const int G = qk_t * ncb + qk_j, slot = G % S, use = G / S;
+                if (block) {
+                    if (!hs_wait(&tl->full[slot], (uint32_t)(use & 1), p.status, abort)) return false;
+                } else if (!mbar_try_wait(&tl->full[slot], (uint32_t)(use & 1))) {
+                    return false;
+                }
+                tc_fence_after();
+                const uint32_t ts = tmem + (uint32_t)((qk_t & 1) * HC);
+                const uint64_t a = kd0 + (uint64_t)((uint32_t)slot * (kSlotBytes >> 4));
+                const uint64_t bq = qd0 + (uint64_t)((uint32_t)(qk_j * HC * 128) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(ts, a + 2 * kk, bq + 2 * kk, idesc_qk, (qk_j > 0 || kk > 0) ? 1u : 0u);
+                if (++qk_j == ncb) {
+                    if (qk_t < 5) STI_HSTAMP(7 + qk_t);
+                    umma_commit(&tl->s_full[qk_t & 1]);
+                    qk_j = 0;
+                    ++qk_t;
+                }
+                return true;
+            };
+            for (int t = 0; t < n_tiles && !dead; ++t) {
+                while (qk_t == t && !dead) dead = !issue_qk(true);   // the rest of QK(t)
+                if (dead) break;
+                // while the softmax of tile t runs, QK of tile t+1 on column blocks already landed
+                // (it writes the other S^T buffer, whose softmax finished before PV(t-1))
+                {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(&tl->p_full, (uint32_t)(t & 1))) {
+                        if (qk_t == t + 1 && qk_t < n_tiles && issue_qk(false)) continue;
+                        if (*abort || global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
+                            if (!*abort) atomicOr(p.status, 2u /* STI_FLAG_TIMEOUT */);
+                            *abort = 1;
+                            dead = true;
+                            break;
+                        }
+                    }
+                }
+                if (dead) break;
+                tc_fence_after();
+                for (int m = 0; m < nmb; ++m) {
+                    const int slot = (t * ncb + 2 * m) % S;   // column blocks 2m, 2m+1: adjacent slots
+                    const uint64_t a = vd0 + (uint64_t)((uint32_t)slot * (kSlotBytes >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < kHsRows / 16; ++kk)
+                        umma_bf16(tmem + (uint32_t)(2 * HC + m * HC), a + (uint64_t)(kk * (2048 >> 4)),
+                                  pd0 + (uint64_t)(((kk >> 2) * HC * 128 + (kk & 3) * 32) >> 4), idesc_pv,
+                                  (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_mc(&tl->empty[slot], cta_mask);
+                    umma_commit_mc(&tl->empty[slot + 1], cta_mask);
+                }
+                umma_commit(&tl->o_done);
+                if (t < 5) STI_HSTAMP(25 + t);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int qd = warp & 3;                       // TMEM lane quarter of this warp
+        const int row = 32 * qd + lane;                // KV row of the tile / d row of an O^T block
+        const int st = tid - 64;                       // 0..127
+        const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+        constexpr int kSpread = 32 / HC;               // lanes holding one head after a reduce-scatter
+        griddep_wait();
+        bool dead = false;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int slot_i = t * kHsRows + row;
+            const int idx = slot_i < p.k ? __ldg(idx_row + slot_i) : -1;
+            const bool valid = idx >= 0 && idx < n_rows;
+            if (!dead) dead = !hs_wait(&tl->s_full[t & 1], (uint32_t)((t >> 1) & 1), p.status, abort);
+            if (st == 0 && t < 5) STI_HSTAMP(15 + t);
+            tc_fence_after();
+            float x[HC];
+            {
+                uint32_t r[HC];
+                tmem_ld_n<HC>(tmem + lane_base + (uint32_t)((t & 1) * HC), r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < HC; ++i) x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+            }
+            {
+                float v[HC];
+#pragma unroll
+                for (int i = 0; i < HC; ++i) v[i] = x[i];
+                warp_reduce_scatter_n<HC, true>(v);
+                if ((lane & (kSpread - 1)) == 0) tl->red_max[qd][lane / kSpread] = v[0];
+            }
+            named_bar_sync(1, 128);
+            if (st < HC) {
+                const float mt = fmaxf(fmaxf(tl->red_max[0][st], tl->red_max[1][st]),
+                                       fmaxf(tl->red_max[2][st], tl->red_max[3][st]));
+                const float m_old = tl->m_run[st];
+                // the running max moves only when a tile's max passes it by more than 8 (log2
+                // units): every P stays <= 2^8 and O, l are rescaled only when a max moves
+                const float m_new = (m_old == -INFINITY || mt > m_old + 8.f) ? fmaxf(m_old, mt) : m_old;
+                tl->alpha[st] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+                tl->m_run[st] = m_new;
+            }
+            named_bar_sync(1, 128);
+            // the previous tile's PV product has read P^T and O^T before they change
+            if (t > 0 && !dead) dead = !hs_wait(&tl->o_done, (uint32_t)((t - 1) & 1), p.status, abort);
+            tc_fence_after();
+            float v2[HC];
+#pragma unroll
+            for (int i = 0; i < HC; ++i) {
+                const float m = tl->m_run[i];
+                x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
+                v2[i] = x[i];
+            }
+            {   // P^T[i][row]: column block row/64, head row i, 16-byte chunk ((row%64)/8) ^ (i%8)
+                uint8_t* pb = p_s + (row >> 6) * HC * 128;
+                const int kr = row & 63;
+#pragma unroll
+                for (int i = 0; i < HC; ++i)
+                    *reinterpret_cast<__nv_bfloat16*>(pb + i * 128 + ((((kr >> 3) ^ (i & 7))) << 4) + (kr & 7) * 2) =
+                        __float2bfloat16_rn(x[i]);
+            }
+            warp_reduce_scatter_n<HC, false>(v2);
+            if ((lane & (kSpread - 1)) == 0) tl->red_sum[qd][lane / kSpread] = v2[0];
+            bool rescale = false;
+#pragma unroll
+            for (int i = 0; i < HC; ++i) rescale = rescale || tl->alpha[i] != 1.f;
+            if (t > 0 && rescale) {   // O^T rows (lane = d within a block) times the heads' factors
+                for (int m = 0; m < nmb; ++m) {
+                    const uint32_t ta = tmem + lane_base + (uint32_t)(2 * HC + m * HC);
+                    uint32_t r[HC];
+                    tmem_ld_n<HC>(ta, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < HC; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[i]);
+                    tmem_st_n<HC>(ta, r);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();   // P^T: generic writes read by the MMA
+            tc_fence_before();
+            named_bar_sync(1, 128);
+            if (st < HC)
+                tl->l_run[st] = tl->l_run[st] * tl->alpha[st] + (tl->red_sum[0][st] + tl->red_sum[1][st]) +
+                                (tl->red_sum[2][st] + tl->red_sum[3][st]);
+            if (st == 0) mbar_arrive(&tl->p_full);
+            if (st == 0 && t < 5) STI_HSTAMP(20 + t);
+        }
+        // ---- epilogue: o = O / (l + 2^(sink*log2e - m)); heads with no valid slot give 0
+        if (!dead) dead = !hs_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
+        if (st == 0) STI_HSTAMP(12);
+        tc_fence_after();
+        named_bar_sync(1, 128);   // the last l_run update is visible
+        if (st < HC) {
+            const int hh = rank * HC + st;
+            const float m = tl->m_run[st];
+            float inv = 0.f, lse = -INFINITY;
+            if (m != -INFINITY) {
+                const float den = tl->l_run[st] + exp2f(__ldg(p.sink + hh) * kLog2e - m);
+                inv = 1.f / den;
+                lse = (m + log2f(den)) * kLn2;
+            }
+            tl->alpha[st] = inv;
+            if (p.lse) p.lse[(size_t)query * p.h + hh] = lse;
+        }
+        named_bar_sync(1, 128);
+        // [HC][d] bf16 staged in the Q buffer (every QK product has completed) -> one bulk store
+        uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
+        for (int m = 0; m < nmb; ++m) {
+            uint32_t r[HC];
+            tmem_ld_n<HC>(tmem + lane_base + (uint32_t)(2 * HC + m * HC), r);
+            tmem_ld_wait();
+            const int dd = 128 * m + row;
+#pragma unroll
+            for (int i = 0; i < HC; ++i)
+                stage[(size_t)i * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[i]));
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (st == 0) {
+            bulk_store(p.out + ((size_t)query * p.h + (size_t)rank * HC) * p.d, stage, (uint32_t)(HC * p.d * 2));
+            bulk_commit();
+            bulk_wait_read_all();   // the stage may be released; the writes complete with the grid
+            STI_HSTAMP(13);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, hs_tmem_cols(HC));
+    }
+    cluster_sync();   // no CTA leaves while a partner may still signal or fill its shared memory
+    if (tid == 0) STI_HSTAMP(14);
+}
+
+constexpr int kSmemLimit = 232448;   // opt-in dynamic shared memory per CTA
+
+// Ring slots: even (a d-block's two column blocks sit in adjacent slots) and at least one tile's
+// column blocks (a tile's last block must not wait for a slot its own PV product frees).
+int hs_slots(int hc, int d) {
+    for (int s = kHsMaxSlots; s >= d / 64 && s >= 2; s -= 2)
+        if (hs_smem_bytes(hc, d, s) <= (size_t)kSmemLimit) return s;
+    return 0;
+}
+
+template <int HC>
+cudaError_t launch_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2, const AttnParams& p,
+                      cudaStream_t stream) {
+    const int slots = hs_slots(HC, p.d);
+    const size_t smem = hs_smem_bytes(HC, p.d, slots);
+    cudaError_t err =
+        cudaFuncSetAttribute(sparse_attn_hs_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.s * p.cluster));
+    cfg.blockDim = dim3(kHsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.pdl ? 2 : 1;
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_hs_kernel<HC>, tm_q, tm_kv1, tm_kv2, p, slots);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+template <int HC>
+bool hs_resident(int n_queries, int c, int d) {
+    const int slots = hs_slots(HC, d);
+    if (slots < 2) return false;
+    const size_t smem = hs_smem_bytes(HC, d, slots);
+    if (cudaFuncSetAttribute(sparse_attn_hs_kernel<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_queries * c));
+    cfg.blockDim = dim3(kHsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, sparse_attn_hs_kernel<HC>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return active >= n_queries;
+}
+
+int attn_hs_pick_uncached(int n_queries, int h, int d) {
+    // heads split over 4 or 2 CTAs (16 or 32 heads each); every cluster resident at once
+    const int cands[2][2] = {{16, 4}, {32, 2}};   // (heads per CTA, CTAs) for h = 64
+    if (h == 64) {
+        for (const auto& c : cands) {
+            const bool ok = c[0] == 16 ? hs_resident<16>(n_queries, c[1], d) : hs_resident<32>(n_queries, c[1], d);
+            if (ok) return c[1];
+        }
+        return 0;
+    }
+    if (h == 32) return hs_resident<16>(n_queries, 2, d) ? 2 : 0;
+    return 0;
+}
+
+}  // namespace
+
+int attn_hs_pick(int n_queries, int h, int d) {
+    if ((h != 64 && h != 32) || d % 128 != 0 || d > 512 || n_queries < 1) return 0;
+    struct Entry {
+        int dev, n_queries, h, d, c;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (const Entry& e : cache)
+            if (e.dev == dev && e.n_queries == n_queries && e.h == h && e.d == d) return e.c;
+    }
+    const int c = attn_hs_pick_uncached(n_queries, h, d);
+    std::lock_guard<std::mutex> g(mu);
+    if (cache.size() < 4096) cache.push_back({dev, n_queries, h, d, c});
+    return c;
+}
+
+cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                  const AttnParams& p, cudaStream_t stream) {
+    if (p.B * p.s == 0) return cudaSuccess;
+    const int hc = p.h / p.cluster;
+    if (hc == 16) return launch_hs<16>(tm_q, tm_kv1, tm_kv2, p, stream);
+    if (hc == 32) return launch_hs<32>(tm_q, tm_kv1, tm_kv2, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sti
+
+#ifdef STI_ATTN_TIMING
+// profiling builds only: per-CTA clock64 stamps of the head-split attention
+extern "C" int sti_dbg_hs_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_hs_t, sizeof(unsigned long long) * 32 * (size_t)n_blocks);
+}
+#endif

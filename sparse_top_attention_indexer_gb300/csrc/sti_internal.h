@@ -85,6 +85,11 @@ int attn_pick_cluster(int n_queries, int k, int d);
 // for 4-row gathers).  Ignored unless p.use_tma.
 cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                const AttnParams& p, cudaStream_t stream);
+// Few queries with 32 or 64 heads: CTAs per query of the head-split kernel (4 or 2; 0 = not
+// applicable or not resident), and its launch (tm_q's box is {64, h / cluster}).
+int attn_hs_pick(int n_queries, int h, int d);
+cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                  const AttnParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ device properties
 int device_num_sms();

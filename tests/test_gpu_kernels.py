@@ -158,15 +158,18 @@ def test_sparse_attn_whole_tiles_masked(sti, orc):
     assert np.all(got[3] == 0)
 
 
-@pytest.mark.parametrize("b,k", [(1, 640), (2, 640), (40, 640), (3, 129)])
-def test_sparse_attn_split_accumulator(sti, orc, b, k):
-    """Few decode queries split over a cluster (8, 4 or 2 CTAs) add into the workspace's fp32
-    accumulator: the result matches the oracle and the unsplit run (256-byte workspace), the
-    accumulator is zero again afterwards, and a second call on the same workspace agrees."""
+@pytest.mark.parametrize("b,k,h", [(1, 640, 64), (2, 640, 64), (40, 640, 64), (3, 129, 64), (2, 640, 32),
+                                   (2, 640, 48), (5, 300, 48)])
+def test_sparse_attn_split_queries(sti, orc, b, k, h):
+    """Few decode queries run split over a thread-block cluster: with 32 or 64 heads the heads
+    split (4 or 2 CTAs, tiles gathered once by multicast), otherwise the slots split (up to 8 CTAs
+    adding into the workspace's fp32 accumulator).  The result matches the oracle and the
+    unsplit run (256-byte workspace), the accumulator is zero again afterwards, and a second call
+    on the same workspace agrees."""
     import torch
 
-    rng = rng_for(730 + b, k)
-    h, d, n1, n2 = 64, 512, 128, 2000
+    rng = rng_for(730 + b, k + h)
+    d, n1, n2 = 512, 128, 2000
     q = to_bf16_bits(rng.standard_normal((b, 1, h, d)))
     kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
     kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
