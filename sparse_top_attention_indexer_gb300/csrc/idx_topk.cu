@@ -293,7 +293,7 @@ __device__ unsigned long long g_topk_t[2048][16];
 
 constexpr int kClThreads = 256;
 constexpr int kClWarps = kClThreads / 32;
-constexpr int kClCandCap = 8192;   // threshold-bin members rank 0 can hold
+constexpr int kClCandCap = 2048;   // threshold-bin members a CTA holds (rank 0: of the whole row)
 
 struct __align__(16) ClusterTopkSmem {
     uint32_t hist[kBins];
@@ -304,7 +304,13 @@ struct __align__(16) ClusterTopkSmem {
     uint32_t pub_tau;           // (rank 0) the exact k-th key and how many keys == tau to take
     int pub_need;
     int pub_ok;                 // (rank 0) 1 if the candidates fitted and tau is valid
+    int n_above;                // this CTA's keys whose first digit is above the threshold bin
+    int n_sel;                  // this CTA's threshold-bin members that are selected
+    int warp_above[kClWarps];   // per warp segment: keys above the bin
+    int warp_sel[kClWarps];     // per warp segment: selected members of the bin
 };
+
+constexpr int kRankCap = 1024;  // threshold-bin members every CTA ranks itself
 
 // 256-thread block scan (exclusive) with total.
 __device__ __forceinline__ int block_excl_scan256(int v, int* warp_tot, int& total) {
@@ -383,11 +389,16 @@ __device__ __forceinline__ int radix_pass256(Src src, int n, int hi_shift, int s
 }
 
 template <int CR>
-__global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkParams p, int chunk_cap) {
+__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(const TopkParams p, int chunk_cap) {
     extern __shared__ __align__(16) uint8_t cl_smem[];
     ClusterTopkSmem* sm = reinterpret_cast<ClusterTopkSmem*>(cl_smem);
     uint32_t* keys = reinterpret_cast<uint32_t*>(sm + 1);            // [chunk_cap] this CTA's chunk
     uint32_t* cand = keys + chunk_cap;                               // [kClCandCap] (rank 0: all members)
+    int* cand_pos = reinterpret_cast<int*>(cand + kClCandCap);       // [kClCandCap] their positions
+    // every rank's members as (key << 32 | ~position): a larger value ranks first
+    unsigned long long* all_comb = reinterpret_cast<unsigned long long*>(cand_pos + kClCandCap);   // [kRankCap]
+    int* rank_part = reinterpret_cast<int*>(all_comb + kRankCap);            // [kRankCap] own members' ranks
+    uint32_t* sel_bits = reinterpret_cast<uint32_t*>(rank_part + kRankCap);  // [chunk_cap / 32]
 
     const int row = blockIdx.x / CR, rank = blockIdx.x - (blockIdx.x / CR) * CR;
     const int b = row / p.s, t = row - b * p.s;
@@ -442,7 +453,14 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
             if (j < n_mine) keys[j] = float_key(v[u]);
         }
     }
-    if (tid == 0) sm->n_cand = 0;
+    for (int i = tid; i < chunk_cap / 32; i += kClThreads) sel_bits[i] = 0u;
+    for (int i = tid; i < kRankCap; i += kClThreads) rank_part[i] = 0;
+    if (tid == 0) {
+        sm->n_cand = 0;
+        sm->n_above = 0;
+        sm->n_sel = 0;
+    }
+    if (tid < kClWarps) sm->warp_sel[tid] = 0;
     __syncthreads();
     STI_KSTAMP(3);
 
@@ -452,21 +470,129 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
     const int remaining1 = p.k - above;
     const int c1 = (int)sm->hist[d1];
     STI_KSTAMP(4);
-    // this CTA's members of bin d1
-    for (int base = 0; base < n_mine; base += kClThreads) {
-        const int j = base + tid;
-        const uint32_t key = j < n_mine ? keys[j] : 0u;
-        const bool m = j < n_mine && (key >> 21) == (uint32_t)d1;
+    // this CTA's members of bin d1 (key and position) and, per warp segment, its keys above the
+    // bin; warp w owns chunk positions [w*seg, w*seg + seg), its lanes consecutive positions
+    const int seg = ((n_mine + kClWarps - 1) / kClWarps + 31) & ~31;
+    const int wlo = min(n_mine, warp * seg), whi = min(n_mine, wlo + seg);
+    int above_mine = 0;
+    for (int j0 = wlo; j0 < whi; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t key = j < whi ? keys[j] : 0u;
+        const bool m = j < whi && (key >> 21) == (uint32_t)d1;
+        above_mine += __popc(__ballot_sync(kFull, j < whi && (key >> 21) > (uint32_t)d1));
         const unsigned bal = __ballot_sync(kFull, m);
+        if (bal == 0u) continue;
         int wbase = 0;
-        if (lane == 0 && bal) wbase = atomicAdd(&sm->n_cand, __popc(bal));
+        if (lane == 0) wbase = atomicAdd(&sm->n_cand, __popc(bal));
         wbase = __shfl_sync(kFull, wbase, 0);
         const int at = wbase + __popc(bal & ((1u << lane) - 1u));
-        if (m && at < kClCandCap) cand[at] = key;
+        if (m && at < kClCandCap) {
+            cand[at] = key;
+            cand_pos[at] = lo + j;
+        }
+    }
+    if (lane == 0) {
+        sm->warp_above[warp] = above_mine;
+        atomicAdd(&sm->n_above, above_mine);
     }
     __syncthreads();
     STI_KSTAMP(5);
     cluster_sync();   // #1: every CTA's members are in its shared memory; every CTA read the histogram
+
+    // lane r of every warp reads rank r's member count; prefix over ranks and total
+    static_assert(CR <= kClWarps && CR <= 32, "one warp per cluster rank");
+    const int cnt_r = lane < CR ? ld_dsmem_s32(dsmem_addr(&sm->n_cand, (uint32_t)lane)) : 0;
+    int cnt_incl = cnt_r;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(kFull, cnt_incl, o);
+        if (lane >= o) cnt_incl += x;
+    }
+    const int tot = __shfl_sync(kFull, cnt_incl, 31);
+    STI_KSTAMP(6);
+    if (tot == c1 && tot <= kRankCap) {
+        // ---- every CTA ranks its own members among all of them: (score desc, position asc)
+        if (warp < CR) {   // warp w copies rank w's members
+            const int n_w = __shfl_sync(kFull, cnt_r, warp);
+            const int at = __shfl_sync(kFull, cnt_incl - cnt_r, warp);
+            for (int i0 = 0; i0 < n_w; i0 += 32) {
+                const int i = i0 + lane;
+                if (i < n_w) {
+                    const uint32_t k_ = ld_dsmem_u32(dsmem_addr(cand + i, (uint32_t)warp));
+                    const uint32_t p_ = ld_dsmem_u32(dsmem_addr(cand_pos + i, (uint32_t)warp));
+                    all_comb[at + i] = ((unsigned long long)k_ << 32) | (unsigned long long)(~p_);
+                }
+            }
+        }
+        // keys above the bin in lower ranks' chunks (lane r < rank reads rank r)
+        int ab = lane < rank ? ld_dsmem_s32(dsmem_addr(&sm->n_above, (uint32_t)lane)) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) ab += __shfl_xor_sync(kFull, ab, o);
+        __syncthreads();
+        STI_KSTAMP(7);
+        const int n_own = __shfl_sync(kFull, cnt_r, rank);
+        const int own_at = __shfl_sync(kFull, cnt_incl - cnt_r, rank);
+#ifdef STI_TOPK_TIMING
+        if (tid == 0 && blockIdx.x < 2048) g_topk_t[blockIdx.x][11] = (unsigned long long)tot | ((unsigned long long)n_own << 20) | ((unsigned long long)n_mine << 40);
+#endif
+        // rank of own member c = how many members rank before it; warp w counts over its eighth
+        // of all members, lane l over own members l, l+32, ... (the members read are broadcast)
+        {
+            const int f_lo = (int)((long long)warp * tot / kClWarps), f_hi = (int)((long long)(warp + 1) * tot / kClWarps);
+            for (int c0 = 0; c0 < n_own; c0 += 32) {
+                const int c = c0 + lane;
+                const unsigned long long me = c < n_own ? all_comb[own_at + c] : ~0ull;
+                int r = 0;
+#pragma unroll 4
+                for (int f = f_lo; f < f_hi; ++f) r += all_comb[f] > me ? 1 : 0;
+                if (c < n_own && r > 0) atomicAdd(&rank_part[c], r);
+            }
+        }
+        __syncthreads();
+        for (int c = tid; c < n_own; c += kClThreads) {
+            if (rank_part[c] < remaining1) {
+                const int pos = (int)(~(uint32_t)(all_comb[own_at + c] & 0xFFFFFFFFull));
+                atomicOr(&sel_bits[(pos - lo) >> 5], 1u << ((pos - lo) & 31));
+                atomicAdd(&sm->n_sel, 1);
+                atomicAdd(&sm->warp_sel[(pos - lo) / seg], 1);
+            }
+        }
+        __syncthreads();
+        STI_KSTAMP(8);
+        cluster_sync();   // #2: every rank's selected count is published
+        STI_KSTAMP(9);
+        int sl = lane < rank ? ld_dsmem_s32(dsmem_addr(&sm->n_sel, (uint32_t)lane)) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sl += __shfl_xor_sync(kFull, sl, o);
+        cluster_arrive();   // this CTA reads no partner's shared memory any more
+        const int base_sel = ab + sl;   // selected positions before this chunk
+        // ordered compaction: keys above the bin, and the bin's selected members
+        const uint32_t kb = smem_u32(keys), sb = smem_u32(sel_bits);
+        auto take_at = [kb, sb, whi, d1](int j) -> bool {
+            if (j >= whi) return false;
+            const uint32_t dig = lds_u32(kb + 4u * (uint32_t)j) >> 21;
+            return dig > (uint32_t)d1 || (dig == (uint32_t)d1 && ((lds_u32(sb + 4u * (uint32_t)(j >> 5)) >> (j & 31)) & 1u));
+        };
+        STI_KSTAMP(10);
+        int pos = base_sel;   // + the selected positions of lower warp segments
+        for (int w = 0; w < warp; ++w) pos += sm->warp_above[w] + sm->warp_sel[w];
+        for (int j0 = wlo; j0 < whi; j0 += 32) {
+            const int j = j0 + lane;
+            const bool take = take_at(j);
+            const unsigned tm = __ballot_sync(kFull, take);
+            const int at = pos + __popc(tm & ((1u << lane) - 1u));
+            if (take && at < p.k) out[at] = lo + j + p.offset;
+            pos += __popc(tm);
+        }
+        if (rank == 0)
+            for (int i = tid; i < kBins; i += kClThreads) ghist[i] = 0;   // ready for the next call
+        STI_KSTAMP(12);
+        cluster_wait();   // no partner still reads this CTA's shared memory
+        STI_KSTAMP(13);
+        STI_KGSTAMP(15);
+        return;
+    }
+    // ---- otherwise (too many members of one bin): rank 0 finishes the select alone
     STI_KSTAMP(6);
 
     if (rank == 0) {
@@ -529,11 +655,8 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_kernel(const TopkPara
     STI_KSTAMP(9);
     const uint32_t tau = ld_dsmem_u32(dsmem_addr(&sm->pub_tau, 0u));
     const int need_eq = ld_dsmem_s32(dsmem_addr(&sm->pub_need, 0u));
-    static_assert(CR <= kClWarps && CR <= 32, "one warp per cluster rank");
 
     // counts of this CTA's chunk, per warp segment (ordered compaction as in the one-CTA kernel)
-    const int seg = ((n_mine + kClWarps - 1) / kClWarps + 31) & ~31;
-    const int wlo = min(n_mine, warp * seg), whi = min(n_mine, wlo + seg);
     int n_gt = 0, n_eq = 0;
     for (int j0 = wlo; j0 < whi; j0 += 32) {
         const int j = j0 + lane;
@@ -625,7 +748,8 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
     if (p.hist != nullptr && rows * CR <= 8 * device_num_sms() && p.n_cols <= CR * 8192) {
         // few long rows with the first pass precomputed: one cluster of CR CTAs per row
         const int chunk_cap = ((((p.n_cols + CR - 1) / CR) + 31) & ~31);
-        const size_t smem = sizeof(ClusterTopkSmem) + (size_t)(chunk_cap + kClCandCap) * 4;
+        const size_t smem = sizeof(ClusterTopkSmem) +
+                            (size_t)(chunk_cap + 2 * kClCandCap + 3 * kRankCap + chunk_cap / 32) * 4;
         cudaError_t err =
             cudaFuncSetAttribute(topk_cluster_kernel<CR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
