@@ -364,6 +364,47 @@ def cpu_baseline(shape: workloads.Shape, data: dict, budget_s: float = 12.0) -> 
             "cores": oracle.default_threads(), "kind": "oracle", "sample": f"{sample} x{reps} ({el:.1f} s)"}
 
 
+def reference_arm(args, shape: workloads.Shape, cfg: dict) -> dict:
+    """The oracle as the reference arm: W untimed and K timed steps, each the path over a
+    bounded sample of the workload (the whole decode batch, or 16 query rows of a prefill)."""
+    import oracle
+
+    oracle.build()
+    data = workloads.make(shape)
+    rows = np.linspace(0, shape.s - 1, 16).astype(np.int64) if shape.prefill else None
+    sample = (f"16 query rows spread over the {shape.s}-query prefill per step" if shape.prefill else
+              f"the whole b={shape.b} decode batch (all {shape.n_layers} attention layer(s)) per step")
+    for _ in range(args.warmup):
+        oracle_step(shape, data, rows)
+    done, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        done += oracle_step(shape, data, rows)
+    el = time.perf_counter() - t0
+    value = round(done / el, 3)
+    unit = "queries/s" if shape.prefill else "tokens/s"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.default_threads(), "kind": "oracle",
+                             "sample": f"{sample}, {args.steps} steps ({el:.1f} s)"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def job_throughput(local_ms: float, units_per_step: int, steps: int, world: int, dist=None, device=None):
+    """Whole-job throughput: every rank ran `steps` steps of `units_per_step` units; the job
+    took as long as its slowest rank.  Returns (units / s over all ranks, that max time in ms)."""
+    total_ms = float(local_ms)
+    if dist is not None:
+        import torch
+
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return units_per_step * steps * world / (total_ms / 1e3), total_ms
+
+
 # ---------------------------------------------------------------------------------- main
 
 
@@ -371,7 +412,7 @@ def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -393,16 +434,9 @@ def main():
            "index_topk": shape.topk, "attention_layers": shape.n_layers, "l2": "256 MiB written then read before every step (outside the timed region)"}
 
     if args.impl == "reference":
-        if rank != 0:
+        if rank != 0:   # the CPU oracle runs once, on rank 0
             return
-        data = workloads.make(shape)
-        cb = cpu_baseline(shape, data)
-        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": cb["unit"], "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg, "cpu_baseline": cb,
-                "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-                "gpu_launches": 0}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(reference_arm(args, shape, cfg)), flush=True)
         return
 
     import torch
@@ -490,13 +524,7 @@ def main():
             step_ms.append(ev[0].elapsed_time(ev[-1]))
             for i, n in enumerate(path.names):
                 per_kernel[n].append(ev[i].elapsed_time(ev[i + 1]))
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    units = shape.b * shape.s
-    value = units * args.steps * world / (total_ms / 1e3)
+    value, total_ms = job_throughput(float(sum(step_ms)), shape.b * shape.s, args.steps, world, dist, device)
     avg_us = {n: round(1e3 * statistics.mean(v), 2) for n, v in per_kernel.items()}
 
     wk = work(shape, data)
