@@ -53,11 +53,16 @@ def peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources of the kernels whose ncu counters profiles/ records."""
+KERNEL_SOURCES = {"idx_scores": ["idx_scores.cu"], "idx_topk": ["idx_topk.cu"],
+                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu"], "window_idx": ["idx_topk.cu"]}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is compiled from (its file and the shared headers), for
+    matching the ncu counters profiles/ records against the kernel that runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_top_attention_indexer_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(KERNEL_SOURCES.get(kernel, [])) + ["sti_internal.h", "sti_ptx.cuh"]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -68,7 +73,7 @@ def recorded_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     with open(path) as f:
         for ln in f:
             m = re.match(r"\s*(\S+)\s+(\S+)\s+bytes_per_launch=(\d+)\s+sources=(\w+)", ln)

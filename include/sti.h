@@ -240,6 +240,17 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args *a, sti_stream stream)
 /* Synchronises `stream` and returns the STI_FLAG_* bits the last no-allocation call left. */
 sti_status sti_decode_noalloc_status(uint32_t *flags, sti_stream stream);
 
+/* ------------------------------------------------------------------ diagnostics */
+/*
+ * Not an operation of the paper: a check of the library's failure handling.  Every wait in the
+ * kernels above (on a TMA transfer, an MMA completion or a partner CTA) gives up after 1 s,
+ * sets STI_FLAG_TIMEOUT and lets the kernel return, so a stalled step reports an error instead
+ * of hanging the GPU.  This launches one small kernel whose wait nothing ever satisfies, with
+ * a limit of limit_us microseconds (1..100000): afterwards the workspace's status word holds
+ * STI_FLAG_TIMEOUT and the context is still usable.
+ */
+sti_status sti_selftest_wait_timeout(void *ws, size_t ws_bytes, uint32_t limit_us, sti_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,8 @@ FLAG_INDEX_RANGE, FLAG_TIMEOUT, FLAG_CHUNKED = 1, 2, 4
 EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_device_status", "sti_window_idxs",
            "sti_idx_scores_workspace_size", "sti_idx_scores", "sti_idx_topk_workspace_size", "sti_idx_topk",
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_decode_workspace_size",
-           "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status"]
+           "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
+           "sti_selftest_wait_timeout"]
 
 
 class StiError(RuntimeError):
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.sti_decode_workspace_size.restype = SZ
         L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
         L.sti_decode_fused.restype = I
+        L.sti_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint32, P]
+        L.sti_selftest_wait_timeout.restype = I
         L.sti_decode_fused_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), P]
         L.sti_decode_fused_noalloc.restype = I
         L.sti_decode_noalloc_status.argtypes = [P, P]
@@ -272,3 +275,9 @@ def decode_noalloc_status(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     lib().sti_decode_noalloc_status(ctypes.byref(flags), _stream(stream))
     return int(flags.value)
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 2000, stream=None) -> None:
+    """Launch the kernel whose wait nothing satisfies (see sti_selftest_wait_timeout)."""
+    _check(lib().sti_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)),
+           "sti_selftest_wait_timeout")

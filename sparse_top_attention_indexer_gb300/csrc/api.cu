@@ -10,6 +10,7 @@
 
 #include "sti.h"
 #include "sti_internal.h"
+#include "sti_ptx.cuh"
 
 namespace {
 
@@ -288,6 +289,18 @@ static size_t attn_acc_bytes(int b, int seqlen, int h, int d) {
     return sti::align_up((size_t)nq * (size_t)h * (size_t)d * sizeof(float), sti::kWsAlign);
 }
 
+// A wait on a barrier that nothing arrives at: it must give up after limit_ns, flag
+// STI_FLAG_TIMEOUT and return, leaving the context usable.
+static __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        sti::mbar_init(&bar, 1);
+        sti::fence_mbar_init();
+    }
+    __syncthreads();
+    sti::mbar_wait_ns(&bar, 0, threadIdx.x == 0 ? status : nullptr, limit_ns);
+}
+
 extern "C" {
 
 const char* sti_status_string(sti_status s) {
@@ -504,6 +517,14 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
                      acc, acc_used, st, /*pdl=*/a->n_cols > 0);
+}
+
+sti_status sti_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes) || limit_us == 0 || limit_us > 100000) return STI_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    selftest_wait_kernel<<<1, 32, 0, st>>>(status_word(ws), (uint64_t)limit_us * 1000u);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_selftest_wait_timeout");
 }
 
 sti_status sti_decode_noalloc_status(uint32_t* flags, sti_stream stream) {

@@ -55,17 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Returns false (and sets
-// STI_FLAG_TIMEOUT in *status when non-null) if it does not complete within the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// STI_FLAG_TIMEOUT in *status when non-null) if it does not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint32_t* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
             if (status) atomicOr(status, 2u /* STI_FLAG_TIMEOUT */);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+    return mbar_wait_ns(bar, parity, status, STI_WAIT_TIMEOUT_NS);
 }
 
 // ------------------------------------------------------------------ fences, named barriers

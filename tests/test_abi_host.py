@@ -83,6 +83,14 @@ def test_host_argument_checks(libsti):
     assert libsti.sti_window_idxs(None, 0, 1, 128, None, 128, None, None, None) == 0
 
 
+def test_selftest_argument_checks(libsti):
+    fake = 1 << 20
+    P = ctypes.c_void_p
+    assert libsti.sti_selftest_wait_timeout(None, 256, 1000, None) == 1
+    assert libsti.sti_selftest_wait_timeout(P(fake), 256, 0, None) == 1
+    assert libsti.sti_selftest_wait_timeout(P(fake), 256, 200000, None) == 1
+
+
 def test_window_width_reported(libsti):
     w = ctypes.c_int(0)
     assert libsti.sti_window_idxs(None, 0, 300, 128, None, 128, ctypes.byref(w), None, None) == 0

@@ -47,6 +47,18 @@ def test_window_idxs_flags_chunked_prefill(sti):
     assert np.all(got[1] == -1)
 
 
+def test_wait_timeout_reports_and_the_context_survives(sti):
+    """A kernel wait that nothing satisfies gives up, flags STI_FLAG_TIMEOUT and returns; the
+    next launches on the same context work."""
+    ws = sti.workspace(256)
+    sti.selftest_wait_timeout(ws, 2000)
+    assert sti.read_device_status(ws) & sti.FLAG_TIMEOUT
+    assert sti.read_device_status(ws) == 0   # cleared
+    got = sti.window_idxs(to_dev_any(np.array([7], np.int32)), 1, 4, ws=ws).cpu().numpy()
+    assert sorted(got[0, 0].tolist()) == [0, 1, 2, 3]   # position p sits in ring slot p % W
+    assert sti.read_device_status(ws) == 0
+
+
 # ----------------------------------------------------------------- index scores
 
 
