@@ -211,7 +211,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
                             int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                             uint16_t* out, float* lse, uint32_t* status, float* acc, size_t acc_bytes,
-                            cudaStream_t st, bool pdl = false) {
+                            cudaStream_t st, bool pdl = false, int win_ring = 0,
+                            const int32_t* start_pos = nullptr) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
@@ -249,7 +250,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     // few queries of 32 or 64 heads: heads split over a cluster, tiles gathered once (multicast);
     // otherwise a query's slots may split over a cluster when the workspace holds the accumulator
     p.acc = (acc != nullptr && acc_bytes >= (size_t)nq * h * d * sizeof(float)) ? acc : nullptr;
-    const int c_hs = sti::attn_hs_pick(nq, h, d);
+    int hs_rows = 1;
+    const int c_hs = sti::attn_hs_pick(nq, h, d, &hs_rows);
     p.cluster = c_hs > 0 ? c_hs : (p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1);
     p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
@@ -259,22 +261,30 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.pdl = pdl ? 1 : 0;
     p.use_tma = (n1 + n2 > 0) && (n1 == 0 || kv_bstride % d == 0) && (n2 == 0 || kv2_bstride % d == 0) &&
                 (int64_t)b * (p.rows1 > p.rows2 ? p.rows1 : p.rows2) < 0x7FFFFFFF;
-    CUtensorMap tm_q, tm_kv1, tm_kv2;
+    CUtensorMap tm_q, tm_kv1, tm_kv2, tm_win;
+    memset(&tm_win, 0, sizeof tm_win);
     memset(&tm_q, 0, sizeof tm_q);
     memset(&tm_kv1, 0, sizeof tm_kv1);
     memset(&tm_kv2, 0, sizeof tm_kv2);
     const bool head_split = c_hs > 0 && p.use_tma;
+    // the ring block load reads rows [b*rows1, b*rows1 + 128) of the first source
+    p.win_ring = (head_split && win_ring == 128 && start_pos != nullptr && seqlen == 1 && n1 == 128 &&
+                  p.rows1 >= 128) ? 128 : 0;
+    p.start_pos = start_pos;
+    p.hs_rows = head_split ? hs_rows : 1;
     if (!head_split && c_hs > 0) p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
     if (p.use_tma) {
-        const uint32_t q_rows = head_split ? (uint32_t)(h / c_hs) : (uint32_t)h;
+        const uint32_t q_rows = head_split ? (uint32_t)(h * hs_rows / c_hs) : (uint32_t)h;
         sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, q_rows);
         if (s == STI_OK && n1 > 0) s = make_map_2d(&tm_kv1, kv, (uint64_t)d, (uint64_t)b * p.rows1, (uint64_t)d * 2, 64, 1);
         if (s == STI_OK && n2 > 0) s = make_map_2d(&tm_kv2, kv2, (uint64_t)d, (uint64_t)b * p.rows2, (uint64_t)d * 2, 64, 1);
+        if (s == STI_OK && p.win_ring)
+            s = make_map_2d(&tm_win, kv, (uint64_t)d, (uint64_t)b * p.rows1, (uint64_t)d * 2, 64, 128);
         if (s != STI_OK) return s;
         if (n1 == 0) tm_kv1 = tm_kv2;
         if (n2 == 0) tm_kv2 = tm_kv1;
     }
-    cudaError_t e = head_split ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, p, st)
+    cudaError_t e = head_split ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, tm_win, p, st)
                                : sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
@@ -438,7 +448,7 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                   a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, acc,
-                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0);
+                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0, /*win_ring=*/W, a->start_pos);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
@@ -516,7 +526,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     if (s != STI_OK) return s;
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
-                     acc, acc_used, st, /*pdl=*/a->n_cols > 0);
+                     acc, acc_used, st, /*pdl=*/a->n_cols > 0, /*win_ring=*/W, a->start_pos);
 }
 
 sti_status sti_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, sti_stream stream) {

@@ -40,6 +40,18 @@ namespace sti {
 namespace {
 
 #ifdef STI_ATTN_TIMING
+__device__ unsigned long long g_hs_p[2048][40];   // producer: per tile and column block, empty wait done
+__device__ unsigned long long g_hs_e[2048][8];    // row-split merge phases
+#define STI_ESTAMP(i)                                                                                  \
+    do {                                                                                               \
+        if (blockIdx.x < 2048) g_hs_e[blockIdx.x][i] = clock64();                                      \
+    } while (0)
+#else
+#define STI_ESTAMP(i) \
+    do {              \
+    } while (0)
+#endif
+#ifdef STI_ATTN_TIMING
 __device__ unsigned long long g_hs_t[2048][32];
 #define STI_HSTAMP(i)                                                                                  \
     do {                                                                                               \
@@ -51,7 +63,8 @@ __device__ unsigned long long g_hs_t[2048][32];
     } while (0)
 #endif
 
-constexpr int kHsThreads = 192;
+constexpr int kHsThreads = 288;   // warps 0, 6, 7, 8 produce, 1 issues MMAs, 2-5 run the softmax
+constexpr int kProducers = 4;
 constexpr int kHsRows = 128;
 constexpr int kHsMaxSlots = 12;
 constexpr uint32_t kSlotBytes = kHsRows * 128;   // one column block of a tile
@@ -66,6 +79,9 @@ struct __align__(8) HsTail {
     uint64_t p_full;               // P^T written, O^T rescaled
     uint64_t o_done;               // PV product of a tile complete
     uint64_t q_bar;                // Q rows of this CTA's heads landed
+    uint64_t recv_bar;             // row-split merge: the partner's partial and (m, l) landed
+    uint64_t ready_bar;            // row-split merge: the partner's ring is free to receive
+    float peer_ml[32][2];          // row-split merge: the partner's (m, l) per head
     uint32_t tmem_base;
     int abort;                     // a wait of this CTA timed out: the others stop waiting
     float m_run[32];               // running max per head, log2 domain
@@ -135,7 +151,8 @@ __host__ __device__ constexpr size_t hs_smem_bytes(int hc, int d, int slots) {
 template <int HC>
 __global__ void __launch_bounds__(kHsThreads, 1)
     sparse_attn_hs_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
-                          const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p, int n_slots) {
+                          const __grid_constant__ CUtensorMap tm_kv2, const __grid_constant__ CUtensorMap tm_win,
+                          const AttnParams p, int n_slots) {
     static_assert(HC == 16 || HC == 32, "16 or 32 heads per CTA");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -147,15 +164,28 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     volatile int* abort = &tl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int C = p.cluster;
+    const int C = p.cluster;                  // CTAs per query = CH head groups x CR row groups
+    const int CR = p.hs_rows, CH = p.cluster / p.hs_rows;
     const int query = blockIdx.x / C, rank = blockIdx.x - (blockIdx.x / C) * C;
+    const int hg = rank % CH, rg = rank / CH;   // this CTA's heads [hg*HC, +HC) and row group
     const int b = query / p.s;
     const int ncb = p.d / 64;                 // column blocks per tile
     const int nmb = p.d / 128;                // d blocks of the PV product
-    const int n_tiles = (p.k + kHsRows - 1) / kHsRows;
-    const uint16_t cta_mask = (uint16_t)((1u << C) - 1u);
+    // the row group's slots [r0, r1) of the query's index row, in tiles of 128.  With a window
+    // ring the first group also takes the ring tile, which it runs before the indices exist, so
+    // the groups split the remaining slots evenly in whole tiles
+    const int pre = (p.win_ring == kHsRows && CR == 2 && p.k > kHsRows) ? kHsRows : 0;
+    const int rows_rg = pre + (((p.k - pre + CR - 1) / CR + kHsRows - 1) / kHsRows) * kHsRows;
+    const int r0 = rg == 0 ? 0 : min(p.k, rows_rg), r1 = rg == 0 ? min(p.k, rows_rg) : p.k;
+    const int n_tiles = (r1 - r0 + kHsRows - 1) / kHsRows;
+    // the CTAs that share this row group's tiles (multicast targets, slot releases)
+    const uint16_t cta_mask = (uint16_t)(((1u << CH) - 1u) << (rg * CH));
     const int n_rows = p.n1 + p.n2;
     const int32_t* idx_row = p.idx + (size_t)query * p.idx_stride;
+    // a full window ring is tile 0, loaded as one block in ring-row order (the attention does not
+    // depend on slot order); it needs no index, so it runs before the indices are complete
+    const bool ring_tile = p.win_ring == kHsRows && r0 == 0 && r1 - r0 >= kHsRows &&
+                           __ldg(p.start_pos + b) >= kHsRows - 1;
     if (tid == 0) STI_HSTAMP(0);
 
     if (warp == 1) {
@@ -165,13 +195,17 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&tl->full[i], 1);
-            mbar_init(&tl->empty[i], (uint32_t)C);
+            mbar_init(&tl->empty[i], (uint32_t)CH);
         }
         mbar_init(&tl->s_full[0], 1);
         mbar_init(&tl->s_full[1], 1);
         mbar_init(&tl->p_full, 1);
         mbar_init(&tl->o_done, 1);
         mbar_init(&tl->q_bar, 1);
+        mbar_init(&tl->recv_bar, 1);
+        mbar_init(&tl->ready_bar, 1);
+        // row-split merge: the partner's half of d for this CTA's heads, [d/2][HC] fp32, and (m, l)
+        if (CR == 2) mbar_arrive_expect_tx(&tl->recv_bar, (uint32_t)(p.d / 2 * HC * 4 + HC * 8));
         tl->abort = 0;
         fence_mbar_init();
     }
@@ -191,27 +225,43 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     const uint32_t tmem = tl->tmem_base;
     if (tid == 0) STI_HSTAMP(1);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp == 0 || warp >= 6) {
+        // ------------------------------------------------------------ producers
+        // producer pi owns the ring slots = pi (mod 4): it waits, arms and fills only those, so
+        // four issue streams of TMA gathers run side by side
+        const int pi = warp == 0 ? 0 : warp - 5;
+        if (warp == 0 && lane == 0) {
             tma_prefetch_desc(&tm_kv1);
             tma_prefetch_desc(&tm_kv2);
             mbar_arrive_expect_tx(&tl->q_bar, (uint32_t)(HC * p.d * 2));
             for (int cb = 0; cb < ncb; ++cb)
-                tma_load_2d(q_s + (size_t)cb * HC * 128, &tm_q, &tl->q_bar, cb * 64, query * p.h + rank * HC);
+                tma_load_2d(q_s + (size_t)cb * HC * 128, &tm_q, &tl->q_bar, cb * 64, query * p.h + hg * HC);
+        }
+        bool dead = false;
+        const bool mine = (lane % CH) == hg;   // four-row group g = lane is this CTA's to fetch
+        int t_first = 0;
+        if (ring_tile) {   // slots 0..ncb-1 are free on first use: no wait
+            if (lane == 0) {
+                for (int j = pi; j < ncb; j += kProducers) {   // tile 0: column block j in slot j
+                    mbar_arrive_expect_tx(&tl->full[j], kSlotBytes);
+                    if (hg == 0)
+                        tma_load_2d_mc(ring + (size_t)j * kSlotBytes, &tm_win, &tl->full[j], j * 64, b * (int)p.rows1,
+                                       cta_mask);
+                }
+            }
+            __syncwarp();
+            t_first = 1;
         }
         griddep_wait();   // the indices are complete from here on
-        bool dead = false;
-        const bool mine = (lane % C) == rank;   // four-row group g = lane is this CTA's to fetch
-        for (int t = 0; t < n_tiles && !dead; ++t) {
+        for (int t = t_first; t < n_tiles && !dead; ++t) {
             int sid[4], crd[4];
             int first_s = -1, first_c = 0, n_valid = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int slot = t * kHsRows + 4 * lane + i;
-                int idx = slot < p.k ? __ldg(idx_row + slot) : -1;
+                const int slot = r0 + t * kHsRows + 4 * lane + i;
+                int idx = slot < r1 ? __ldg(idx_row + slot) : -1;
                 if (idx < -1 || idx >= n_rows) {
-                    if (rank == 0) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
+                    if (rank == 0 && pi == 0) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);
                     idx = -1;
                 }
                 sid[i] = idx < 0 ? -1 : (idx < p.n1 ? 0 : 1);
@@ -232,9 +282,27 @@ __global__ void __launch_bounds__(kHsThreads, 1)
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) tbytes += __shfl_xor_sync(kFull, tbytes, o);
             const void* map = first_s == 1 ? (const void*)&tm_kv2 : (const void*)&tm_kv1;
+            // the next tile's rows go to L2 now (this CTA's groups, split over the producers), so its
+            // gathers -- issued when PV of this tile frees their slots -- do not wait on HBM
+            if (t + 1 < n_tiles && (lane % CH) == hg && ((lane / CH) % kProducers) == pi) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int slot = r0 + (t + 1) * kHsRows + 4 * lane + i;
+                    const int idx = slot < r1 ? __ldg(idx_row + slot) : -1;
+                    if (idx >= 0 && idx < n_rows) {
+                        const uint16_t* row_ptr = idx < p.n1 ? p.kv + (size_t)b * p.kv_bstride + (size_t)idx * p.d
+                                                             : p.kv2 + (size_t)b * p.kv2_bstride + (size_t)(idx - p.n1) * p.d;
+                        prefetch_l2_bulk(row_ptr, (uint32_t)p.d * 2u);
+                    }
+                }
+            }
             for (int j = 0; j < ncb; ++j) {
                 const int G = t * ncb + j, slot = G % S, use = G / S;
+                if (slot % kProducers != pi) continue;
                 if (use > 0 && !dead) dead = !hs_wait(&tl->empty[slot], (uint32_t)((use - 1) & 1), p.status, abort);
+#ifdef STI_ATTN_TIMING
+                (void)0;
+#endif
                 dead = __any_sync(kFull, dead);
                 if (dead) break;
                 uint8_t* dst = ring + (size_t)slot * kSlotBytes;
@@ -255,11 +323,11 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                     }
                 }
             }
-            if (lane == 0 && t < 5) STI_HSTAMP(2 + t);
+            if (pi == 0 && lane == 0 && t < 5) STI_HSTAMP(2 + t);
         }
         // every arrival the cluster makes on this CTA's barriers has landed before it may exit
         const int total = n_tiles * ncb;
-        for (int s2 = 0; s2 < S && s2 < total && !dead; ++s2) {
+        for (int s2 = pi; s2 < S && s2 < total && !dead; s2 += kProducers) {
             const int uses = (total - s2 + S - 1) / S;
             dead = !hs_wait(&tl->empty[s2], (uint32_t)((uses - 1) & 1), p.status, abort);
         }
@@ -318,6 +386,9 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 }
                 if (dead) break;
                 tc_fence_after();
+#ifdef STI_ATTN_TIMING
+                if (t < 5 && blockIdx.x < 2048) g_hs_p[blockIdx.x][t * 8 + 0] = clock64();
+#endif
                 for (int m = 0; m < nmb; ++m) {
                     const int slot = (t * ncb + 2 * m) % S;   // column blocks 2m, 2m+1: adjacent slots
                     const uint64_t a = vd0 + (uint64_t)((uint32_t)slot * (kSlotBytes >> 4));
@@ -326,8 +397,14 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                         umma_bf16(tmem + (uint32_t)(2 * HC + m * HC), a + (uint64_t)(kk * (2048 >> 4)),
                                   pd0 + (uint64_t)(((kk >> 2) * HC * 128 + (kk & 3) * 32) >> 4), idesc_pv,
                                   (t > 0 || kk > 0) ? 1u : 0u);
+#ifdef STI_ATTN_TIMING
+                    if (t < 5 && blockIdx.x < 2048) g_hs_p[blockIdx.x][t * 8 + 1 + 2 * m] = clock64();
+#endif
                     umma_commit_mc(&tl->empty[slot], cta_mask);
                     umma_commit_mc(&tl->empty[slot + 1], cta_mask);
+#ifdef STI_ATTN_TIMING
+                    if (t < 5 && blockIdx.x < 2048) g_hs_p[blockIdx.x][t * 8 + 2 + 2 * m] = clock64();
+#endif
                 }
                 umma_commit(&tl->o_done);
                 if (t < 5) STI_HSTAMP(25 + t);
@@ -341,12 +418,16 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         const int st = tid - 64;                       // 0..127
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
         constexpr int kSpread = 32 / HC;               // lanes holding one head after a reduce-scatter
-        griddep_wait();
+        if (!ring_tile) griddep_wait();
         bool dead = false;
         for (int t = 0; t < n_tiles; ++t) {
-            const int slot_i = t * kHsRows + row;
-            const int idx = slot_i < p.k ? __ldg(idx_row + slot_i) : -1;
-            const bool valid = idx >= 0 && idx < n_rows;
+            if (ring_tile && t == 1) griddep_wait();
+            bool valid = true;   // the full ring: every row valid
+            if (!(ring_tile && t == 0)) {
+                const int slot_i = r0 + t * kHsRows + row;
+                const int idx = slot_i < r1 ? __ldg(idx_row + slot_i) : -1;
+                valid = idx >= 0 && idx < n_rows;
+            }
             if (!dead) dead = !hs_wait(&tl->s_full[t & 1], (uint32_t)((t >> 1) & 1), p.status, abort);
             if (st == 0 && t < 5) STI_HSTAMP(15 + t);
             tc_fence_after();
@@ -421,13 +502,30 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             if (st == 0) mbar_arrive(&tl->p_full);
             if (st == 0 && t < 5) STI_HSTAMP(20 + t);
         }
-        // ---- epilogue: o = O / (l + 2^(sink*log2e - m)); heads with no valid slot give 0
-        if (!dead) dead = !hs_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
+        if (!dead && n_tiles > 0) dead = !hs_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
         if (st == 0) STI_HSTAMP(12);
-        tc_fence_after();
-        named_bar_sync(1, 128);   // the last l_run update is visible
-        if (st < HC) {
-            const int hh = rank * HC + st;
+    }
+
+    // ---- epilogue: o = O / (l + 2^(sink*log2e - m)); heads with no valid slot give 0
+    tc_fence_before();
+    __syncthreads();   // every MMA of this CTA has completed; m_run, l_run final
+    tc_fence_after();
+    const bool sm_warp = warp >= 2 && warp <= 5;
+    const int st = tid - 64;                                  // softmax threads: 0..127
+    const int row = 32 * (warp & 3) + lane;                   // their TMEM lane (d within a block)
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    auto o_block = [&](int m, uint32_t (&r)[HC]) {            // this thread's O^T row of d-block m
+        if (n_tiles > 0) {
+            tmem_ld_n<HC>(tmem + lane_base + (uint32_t)(2 * HC + m * HC), r);
+            tmem_ld_wait();
+        } else {
+#pragma unroll
+            for (int i = 0; i < HC; ++i) r[i] = 0u;
+        }
+    };
+    if (CR == 1) {
+        if (sm_warp && st < HC) {
+            const int hh = hg * HC + st;
             const float m = tl->m_run[st];
             float inv = 0.f, lse = -INFINITY;
             if (m != -INFINITY) {
@@ -438,26 +536,99 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             tl->alpha[st] = inv;
             if (p.lse) p.lse[(size_t)query * p.h + hh] = lse;
         }
-        named_bar_sync(1, 128);
+        __syncthreads();
         // [HC][d] bf16 staged in the Q buffer (every QK product has completed) -> one bulk store
         uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
-        for (int m = 0; m < nmb; ++m) {
-            uint32_t r[HC];
-            tmem_ld_n<HC>(tmem + lane_base + (uint32_t)(2 * HC + m * HC), r);
-            tmem_ld_wait();
-            const int dd = 128 * m + row;
+        if (sm_warp)
+            for (int m = 0; m < nmb; ++m) {
+                uint32_t r[HC];
+                o_block(m, r);
+                const int dd = 128 * m + row;
 #pragma unroll
-            for (int i = 0; i < HC; ++i)
-                stage[(size_t)i * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[i]));
-        }
+                for (int i = 0; i < HC; ++i)
+                    stage[(size_t)i * p.d + dd] =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[i]));
+            }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (st == 0) {
-            bulk_store(p.out + ((size_t)query * p.h + (size_t)rank * HC) * p.d, stage, (uint32_t)(HC * p.d * 2));
+        __syncthreads();
+        if (sm_warp && st == 0) {
+            bulk_store(p.out + ((size_t)query * p.h + (size_t)hg * HC) * p.d, stage, (uint32_t)(HC * p.d * 2));
             bulk_commit();
             bulk_wait_read_all();   // the stage may be released; the writes complete with the grid
             STI_HSTAMP(13);
         }
+    } else {
+        // two row groups: this CTA and its partner (same heads, the other half of the slots).
+        // Each sends the partner the partner's half of d of its unscaled O^T and its (m, l)
+        // (asynchronous stores counted on the partner's barrier) once the partner reports its
+        // ring free, then finishes its own half: o = (O_own 2^(m_own-M) + O_peer 2^(m_peer-M)) / L.
+        const int partner = (1 - rg) * CH + hg;
+        const int half = p.d / 2;
+        const int mb_own = rg * (nmb / 2), mb_peer = (1 - rg) * (nmb / 2);
+        constexpr int kChunks = HC / 4;                       // 16-byte chunks of a row of HC floats
+        float* recv = reinterpret_cast<float*>(ring);         // [half][HC], chunk c of row r at c ^ (r % kChunks)
+        if (tid == 0) mbar_arrive_remote(dsmem_addr(&tl->ready_bar, (uint32_t)partner));
+        if (tid == 64) STI_ESTAMP(0);
+        const bool ready = hs_wait(&tl->ready_bar, 0, p.status, abort);
+        if (tid == 64) STI_ESTAMP(1);
+        if (sm_warp && ready) {
+            const uint32_t rbar = dsmem_addr(&tl->recv_bar, (uint32_t)partner);
+            const uint32_t rbase = dsmem_addr(recv, (uint32_t)partner);
+            for (int m = mb_peer; m < mb_peer + nmb / 2; ++m) {
+                uint32_t r[HC];
+                o_block(m, r);
+                const int dl = (m - mb_peer) * 128 + row;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    st_async_v4(rbase + (uint32_t)(dl * HC + ((c ^ (dl % kChunks)) * 4)) * 4u, __uint_as_float(r[4 * c]),
+                                __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                                __uint_as_float(r[4 * c + 3]), rbar);
+            }
+            if (st < HC)
+                st_async_v2(dsmem_addr(&tl->peer_ml[st][0], (uint32_t)partner), tl->m_run[st], tl->l_run[st], rbar);
+        }
+        if (tid == 64) STI_ESTAMP(2);
+        const bool got = hs_wait(&tl->recv_bar, 0, p.status, abort);
+        if (tid == 64) STI_ESTAMP(3);
+        if (sm_warp && st < HC) {   // scale factors of the two partials; lse (first row group)
+            const int hh = hg * HC + st;
+            const float mo = tl->m_run[st], lo = tl->l_run[st];
+            const float mp = got ? tl->peer_ml[st][0] : -INFINITY, lp = got ? tl->peer_ml[st][1] : 0.f;
+            const float M = fmaxf(mo, mp);
+            float ao = 0.f, ap = 0.f, lse = -INFINITY;
+            if (M != -INFINITY) {
+                const float eo = mo == -INFINITY ? 0.f : exp2f(mo - M), ep = mp == -INFINITY ? 0.f : exp2f(mp - M);
+                const float L = lo * eo + lp * ep + exp2f(__ldg(p.sink + hh) * kLog2e - M);
+                ao = eo / L;
+                ap = ep / L;
+                lse = (M + log2f(L)) * kLn2;
+            }
+            tl->alpha[st] = ao;
+            tl->red_max[0][st] = ap;   // the peer's factor (the softmax scratch is free now)
+            if (rg == 0 && p.lse) p.lse[(size_t)query * p.h + hh] = lse;
+        }
+        __syncthreads();
+        if (sm_warp && got)   // own half of d: combine and write bf16 rows straight to global
+            for (int m = mb_own; m < mb_own + nmb / 2; ++m) {
+                uint32_t r[HC];
+                o_block(m, r);
+                const int dl = (m - mb_own) * 128 + row;
+                const float4* rv = reinterpret_cast<const float4*>(recv + (size_t)dl * HC);
+                uint16_t* orow = p.out + ((size_t)query * p.h + (size_t)hg * HC) * p.d + (size_t)rg * half + dl;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const float4 q4 = rv[c ^ (dl % kChunks)];
+                    const float pv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * c + e;
+                        orow[(size_t)i * p.d] = __bfloat16_as_ushort(__float2bfloat16_rn(
+                            __uint_as_float(r[i]) * tl->alpha[i] + pv[e] * tl->red_max[0][i]));
+                    }
+                }
+            }
+        if (tid == 64) STI_ESTAMP(4);
+        if (sm_warp && st == 0) STI_HSTAMP(13);
     }
 
     tc_fence_before();
@@ -481,8 +652,8 @@ int hs_slots(int hc, int d) {
 }
 
 template <int HC>
-cudaError_t launch_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2, const AttnParams& p,
-                      cudaStream_t stream) {
+cudaError_t launch_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                      const CUtensorMap& tm_win, const AttnParams& p, cudaStream_t stream) {
     const int slots = hs_slots(HC, p.d);
     const size_t smem = hs_smem_bytes(HC, p.d, slots);
     cudaError_t err =
@@ -502,7 +673,7 @@ cudaError_t launch_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.pdl ? 2 : 1;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_hs_kernel<HC>, tm_q, tm_kv1, tm_kv2, p, slots);
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_hs_kernel<HC>, tm_q, tm_kv1, tm_kv2, tm_win, p, slots);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -535,26 +706,37 @@ bool hs_resident(int n_queries, int c, int d) {
     return active >= n_queries;
 }
 
-int attn_hs_pick_uncached(int n_queries, int h, int d) {
-    // heads split over 4 or 2 CTAs (16 or 32 heads each); every cluster resident at once
-    const int cands[2][2] = {{16, 4}, {32, 2}};   // (heads per CTA, CTAs) for h = 64
-    if (h == 64) {
-        for (const auto& c : cands) {
-            const bool ok = c[0] == 16 ? hs_resident<16>(n_queries, c[1], d) : hs_resident<32>(n_queries, c[1], d);
-            if (ok) return c[1];
+// Candidates in order of preference: (heads per CTA, CTAs, row groups).  Two head groups x two
+// row groups halve both the MMAs and the slot gathers of a CTA against four head groups (a
+// tcgen05 MMA costs about the same for N = 16 or 32); they need d to split in two d-block halves.
+int attn_hs_pick_uncached(int n_queries, int h, int d, int* rows) {
+    struct Cand {
+        int hc, c, r;
+    };
+    const Cand c64[] = {{32, 4, 2}, {16, 4, 1}, {32, 2, 1}};
+    const Cand c32[] = {{32, 2, 2}, {16, 2, 1}};
+    const Cand* cands = h == 64 ? c64 : c32;
+    const int n = h == 64 ? 3 : 2;
+    for (int i = 0; i < n; ++i) {
+        const Cand& c = cands[i];
+        if (c.hc * c.c / c.r != h) continue;
+        if (c.r == 2 && d % 256 != 0) continue;
+        const bool ok = c.hc == 16 ? hs_resident<16>(n_queries, c.c, d) : hs_resident<32>(n_queries, c.c, d);
+        if (ok) {
+            *rows = c.r;
+            return c.c;
         }
-        return 0;
     }
-    if (h == 32) return hs_resident<16>(n_queries, 2, d) ? 2 : 0;
     return 0;
 }
 
 }  // namespace
 
-int attn_hs_pick(int n_queries, int h, int d) {
+int attn_hs_pick(int n_queries, int h, int d, int* rows) {
+    *rows = 1;
     if ((h != 64 && h != 32) || d % 128 != 0 || d > 512 || n_queries < 1) return 0;
     struct Entry {
-        int dev, n_queries, h, d, c;
+        int dev, n_queries, h, d, c, r;
     };
     static std::mutex mu;
     static std::vector<Entry> cache;
@@ -563,20 +745,25 @@ int attn_hs_pick(int n_queries, int h, int d) {
     {
         std::lock_guard<std::mutex> g(mu);
         for (const Entry& e : cache)
-            if (e.dev == dev && e.n_queries == n_queries && e.h == h && e.d == d) return e.c;
+            if (e.dev == dev && e.n_queries == n_queries && e.h == h && e.d == d) {
+                *rows = e.r;
+                return e.c;
+            }
     }
-    const int c = attn_hs_pick_uncached(n_queries, h, d);
+    int r = 1;
+    const int c = attn_hs_pick_uncached(n_queries, h, d, &r);
+    *rows = r;
     std::lock_guard<std::mutex> g(mu);
-    if (cache.size() < 4096) cache.push_back({dev, n_queries, h, d, c});
+    if (cache.size() < 4096) cache.push_back({dev, n_queries, h, d, c, r});
     return c;
 }
 
 cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
-                                  const AttnParams& p, cudaStream_t stream) {
+                                  const CUtensorMap& tm_win, const AttnParams& p, cudaStream_t stream) {
     if (p.B * p.s == 0) return cudaSuccess;
-    const int hc = p.h / p.cluster;
-    if (hc == 16) return launch_hs<16>(tm_q, tm_kv1, tm_kv2, p, stream);
-    if (hc == 32) return launch_hs<32>(tm_q, tm_kv1, tm_kv2, p, stream);
+    const int hc = p.h * p.hs_rows / p.cluster;
+    if (hc == 16) return launch_hs<16>(tm_q, tm_kv1, tm_kv2, tm_win, p, stream);
+    if (hc == 32) return launch_hs<32>(tm_q, tm_kv1, tm_kv2, tm_win, p, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -586,5 +773,11 @@ cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm
 // profiling builds only: per-CTA clock64 stamps of the head-split attention
 extern "C" int sti_dbg_hs_times(unsigned long long* host, int n_blocks) {
     return (int)cudaMemcpyFromSymbol(host, sti::g_hs_t, sizeof(unsigned long long) * 32 * (size_t)n_blocks);
+}
+extern "C" int sti_dbg_hs_merge(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_hs_e, sizeof(unsigned long long) * 8 * (size_t)n_blocks);
+}
+extern "C" int sti_dbg_hs_prod(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_hs_p, sizeof(unsigned long long) * 40 * (size_t)n_blocks);
 }
 #endif

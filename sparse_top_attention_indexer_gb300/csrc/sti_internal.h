@@ -78,6 +78,11 @@ struct AttnParams {
     int pdl;                 // launch as a programmatic dependent of the previous kernel in the stream
     float* acc;              // split queries: zeroed fp32 [B*s, h, d] the cluster adds its partials into
                              // (left zeroed again); nullptr: no split
+    int win_ring;            // decode: slots [0, 128) list the 128-row window ring of kv (any order), so a
+                             // full ring (start_pos >= 127) is loaded as one block; 0: indices only
+    const int32_t* start_pos;  // [B], with win_ring
+    int hs_rows;             // head-split kernel: row groups of a query's slots (1 or 2); the cluster
+                             // is (cluster / hs_rows) head groups x hs_rows row groups
 };
 // CTAs per query for n_queries queries of k slots and head dim d (1 = no cluster); cached per device.
 int attn_pick_cluster(int n_queries, int k, int d);
@@ -85,11 +90,12 @@ int attn_pick_cluster(int n_queries, int k, int d);
 // for 4-row gathers).  Ignored unless p.use_tma.
 cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                const AttnParams& p, cudaStream_t stream);
-// Few queries with 32 or 64 heads: CTAs per query of the head-split kernel (4 or 2; 0 = not
-// applicable or not resident), and its launch (tm_q's box is {64, h / cluster}).
-int attn_hs_pick(int n_queries, int h, int d);
+// Few queries with 32 or 64 heads: CTAs per query of the head-split kernel (0 = not applicable
+// or not resident) and, in *rows, how many row groups they form; its launch (tm_q's box is
+// {64, heads per CTA}).
+int attn_hs_pick(int n_queries, int h, int d, int* rows);
 cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
-                                  const AttnParams& p, cudaStream_t stream);
+                                  const CUtensorMap& tm_win, const AttnParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ device properties
 int device_num_sms();

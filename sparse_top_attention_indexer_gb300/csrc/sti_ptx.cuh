@@ -298,6 +298,27 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrive once on a barrier in another CTA of the cluster (address from dsmem_addr), releasing
+// this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// 16- and 8-byte stores into another CTA's shared memory that count their bytes on that CTA's
+// barrier (complete_tx), so the receiver waits on its own barrier for all of them.
+__device__ __forceinline__ void st_async_v4(uint32_t addr_cluster, float a, float b, float c, float d,
+                                            uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr_cluster),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar_cluster)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t addr_cluster, float a, float b, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                     addr_cluster),
+                 "f"(a), "f"(b), "r"(bar_cluster)
+                 : "memory");
+}
+
 // The two halves of cluster_sync, for work between "done with partners" and "partners done".
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
