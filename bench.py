@@ -3,14 +3,17 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2|3|4|5] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
-window indices, Indexer scores, top-k, sparse sink attention (and the split-KV combine),
-launched through the C ABI on one stream.  Default workload: single-layer decode, b=32,
-context 65536 (16384 compressed rows), 64 heads x 512, index heads 32 x 128, top-512.
+window indices, Indexer scores, top-k, sparse sink attention (every attention layer),
+launched through the C ABI on one stream (decode: a CUDA graph of the fused decode step).
+Default workload: single-layer decode, b=32, context 65536 (16384 compressed rows), 64 heads
+x 512, index heads 32 x 128, top-512.
 
-Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream with an event between every kernel; a 256 MiB buffer is written and then
-read before every step (outside the events), so no step finds the previous step's data in L2
-and no step pays for write-backs of the flush itself.
+Timing: W untimed warm-up steps, then K timed steps, each bracketed by CUDA events on the
+launching stream; a 256 MiB buffer is written and then read before every step (outside the
+events), so no step finds the previous step's data in L2 and no step pays for write-backs of
+the flush itself.  Then K more steps with an event between every kernel give the per-kernel
+durations (`kernel_us`, `roofline`); those events keep a kernel from starting its prologue
+under its predecessor's tail, so their sum (`ms_per_step_with_kernel_events`) exceeds the step.
 `value` is tokens/s (decode) or queries/s (prefill) over the timed region; `e2e` is the same
 metric through the fused public entry point with the step's inputs copied from pinned host
 memory and the output copied back every step (wall clock).  `roofline` reports the kernel
@@ -468,65 +471,68 @@ def main():
     use_graph = not shape.prefill and shape.n_layers == 1
     if use_graph:
         path.capture()
+    def plain_step():
+        # one step as a user runs it: the graph without events between its kernels (or direct calls)
+        path.pgraph.replay() if use_graph else path.step()
+
     for _ in range(args.warmup):
         path.flush_l2()
-        path.graph_step() if use_graph else path.step()
+        plain_step()
     torch.cuda.synchronize()
-    n_ev = len(path.names) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
-    graph_times = []
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    # timed region: K steps, each bracketed by CUDA events on this stream (the L2 flush before each
+    # step stays outside them)
+    se = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     for k in range(args.steps):
         path.flush_l2()
+        se[k][0].record()
+        plain_step()
+        se[k][1].record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in se]
+
+    # per-kernel durations: K more steps with events between the kernels (those events also stop
+    # one kernel's prologue from overlapping the previous one's tail, so these durations are
+    # upper bounds of what each kernel costs inside a step)
+    n_ev = len(path.names) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    graph_times = []
+    for k in range(args.steps):
+        path.flush_l2()
         if use_graph:
-            # the graph's own events time each replay; read them before the next replay
             path.graph_step()
-            torch.cuda.synchronize()
+            torch.cuda.synchronize()   # the graph's own events, read before the next replay
             graph_times.append(path.graph_times_ms())
         else:
             path.step(evs[k])
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
     clocks = None
     if sampler:
         # keep the GPU loaded until the clock sampler has seen the load
         t_end = time.perf_counter() + 0.6
         while time.perf_counter() < t_end:
             path.flush_l2()
-            path.graph_step() if use_graph else path.step()
+            plain_step()
         torch.cuda.synchronize()
         clocks = sampler.stop()
 
-    plain_ms = None
-    if use_graph:
-        # diagnostic: the same step replayed without events between its kernels
-        pe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        pl = []
-        for _ in range(min(args.steps, 50)):
-            path.flush_l2()
-            pe[0].record()
-            path.pgraph.replay()
-            pe[1].record()
-            torch.cuda.synchronize()
-            pl.append(pe[0].elapsed_time(pe[1]))
-        plain_ms = round(statistics.median(pl), 5)
-
     per_kernel = {n: [] for n in path.names}
-    step_ms = []
+    evented_ms = []
     if use_graph:
         for ks, st in graph_times:
-            step_ms.append(st)
+            evented_ms.append(st)
             for n, t in zip(path.names, ks):
                 per_kernel[n].append(t)
     else:
         for ev in evs:
-            step_ms.append(ev[0].elapsed_time(ev[-1]))
+            evented_ms.append(ev[0].elapsed_time(ev[-1]))
             for i, n in enumerate(path.names):
                 per_kernel[n].append(ev[i].elapsed_time(ev[i + 1]))
     value, total_ms = job_throughput(float(sum(step_ms)), shape.b * shape.s, args.steps, world, dist, device)
@@ -549,8 +555,7 @@ def main():
             "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
             "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks,
             "launch": "CUDA graph of sti_decode_fused, replayed per step" if use_graph else "direct C-ABI calls"}
-    if plain_ms is not None:
-        line["ms_per_step_without_kernel_events"] = plain_ms
+    line["ms_per_step_with_kernel_events"] = round(statistics.mean(evented_ms), 5)
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
