@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
                     }
             }
-            if (warp == 0) {
+            {   // warp w issues column block w (one issue stream per warp)
                 const int g = lane;
                 int sid[4], crd[4];
                 int S = -1, fc = 0;
@@ -259,16 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i)
                     if (sid[i] != S) crd[i] = fc;
                 const unsigned tma_groups = __ballot_sync(kFull, !mixed && !empty);
-                if (lane == 0 && !dead)
+                if (warp == 0 && lane == 0 && !dead)
                     mbar_arrive_expect_tx(&tl->gather_bar, (uint32_t)(__popc(tma_groups) * ncb_real * 512));
                 __syncwarp();
                 if (!dead && !empty) {
                     if (!mixed) {
                         const void* map = S == 0 ? (const void*)&tm_kv1 : (const void*)&tm_kv2;
-                        for (int cb = 0; cb < ncb_real; ++cb)
+                        for (int cb = warp; cb < ncb_real; cb += kThreads / 32)
                             tma_gather4(kv_s + (size_t)cb * kRows * 128 + (size_t)g * 512, map, &tl->gather_bar,
                                         cb * 64, crd[0], crd[1], crd[2], crd[3]);
-                    } else {
+                    } else if (warp == 0) {
                         for (int i = 0; i < 4; ++i) {
                             const int r = 4 * g + i;
                             const uint16_t* rs = tl->row_src[r];
