@@ -603,15 +603,17 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     ws = sti.workspace(sti.decode_workspace_size(a), path.dev)
     bi = h_q.numel() * 2 + h_iq.numel() * 2 + h_w.numel() * 2 + h_sp.numel() * 4
     bo = h_out.numel() * 2
+    main = torch.cuda.current_stream()
 
     def one():
-        d_q.copy_(h_q, non_blocking=True)
+        # the small inputs the first kernel needs go first; q (2 MB) is only read by the last
         d_iq.copy_(h_iq, non_blocking=True)
         d_w.copy_(h_w, non_blocking=True)
         d_sp.copy_(h_sp, non_blocking=True)
+        d_q.copy_(h_q, non_blocking=True)
         sti.decode_fused(a, ws)
         h_out.copy_(out.reshape(-1), non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        main.synchronize()
 
     for _ in range(warmup):
         path.flush_l2()

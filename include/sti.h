@@ -200,6 +200,10 @@ typedef struct sti_decode_args {
     /* outputs */
     uint16_t *out;              /* bf16 [b, h, d] */
     int32_t *topk_idxs;         /* int32 [b, W + index_topk] */
+    /* optional: a cudaEvent_t the attention step (step 3) waits for before it reads q, so that
+     * q's upload (on another stream) overlaps steps 1 and 2; NULL: q is ready when the call is
+     * enqueued */
+    void *q_ready;
 } sti_decode_args;
 
 /* Steps 2 and 3 launch as programmatic dependents of the step before them: each is scheduled

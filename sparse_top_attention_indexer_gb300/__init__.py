@@ -50,7 +50,7 @@ class DecodeArgs(ctypes.Structure):
         ("iq", ctypes.c_void_p), ("ik", ctypes.c_void_p), ("ik_bstride", ctypes.c_int64), ("w", ctypes.c_void_p),
         ("index_scale", ctypes.c_float), ("Hi", ctypes.c_int), ("Di", ctypes.c_int), ("index_topk", ctypes.c_int),
         ("ratio", ctypes.c_int), ("n_cols", ctypes.c_int), ("start_pos", ctypes.c_void_p), ("b", ctypes.c_int),
-        ("out", ctypes.c_void_p), ("topk_idxs", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("topk_idxs", ctypes.c_void_p), ("q_ready", ctypes.c_void_p),
     ]
 
 
@@ -219,9 +219,10 @@ def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
 
 
 def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, index_scale, start_pos, ratio, n_cols,
-                index_topk, out=None, topk_idxs=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
+                index_topk, out=None, topk_idxs=None, q_ready=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
     """Fill sti_decode_args from tensors.  q [b,h,d] (or [b,1,h,d]), window_kv [b,W,d],
     comp_kv [b,cap,d], iq [b,Hi,Di] (or [b,1,Hi,Di]), ik [b,cap,Di], w [b,Hi] (or [b,1,Hi]).
+    q_ready: optional torch.cuda.Event (already recorded once) the attention step waits for.
     The returned struct keeps references to every tensor it points to."""
     b = q.shape[0]
     h, d = q.shape[-2], q.shape[-1]
@@ -240,9 +241,10 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
         topk_idxs = torch.empty(b, W + index_topk, dtype=torch.int32, device=q.device)
     a = DecodeArgs(_ptr(q), _ptr(window_kv), window_kv.stride(0), _ptr(comp_kv), comp_kv.stride(0), _ptr(attn_sink),
                    float(softmax_scale), h, d, W, _ptr(iq), _ptr(ik), ik.stride(0), _ptr(w), float(index_scale), Hi,
-                   Di, index_topk, ratio, n_cols, _ptr(start_pos), b, _ptr(out), _ptr(topk_idxs))
+                   Di, index_topk, ratio, n_cols, _ptr(start_pos), b, _ptr(out), _ptr(topk_idxs),
+                   q_ready.cuda_event if q_ready is not None else None)
     # the struct holds raw device pointers: keep their tensors alive as long as it lives
-    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs)
+    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready)
     return a, out, topk_idxs
 
 

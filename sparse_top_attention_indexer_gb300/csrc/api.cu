@@ -446,9 +446,13 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
                   a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    // q may still be uploading on another stream: the attention waits for its event (and then
+    // launches as an ordinary dependent)
+    if (a->q_ready && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a->q_ready), 0)) != cudaSuccess)
+        return cuda_fail(e, "sti_decode_fused: cudaStreamWaitEvent");
     s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                   a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, acc,
-                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0, /*win_ring=*/W, a->start_pos);
+                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
@@ -524,9 +528,11 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
                   a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;
+    if (a->q_ready && (e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a->q_ready), 0)) != cudaSuccess)
+        return cuda_fail(e, "sti_decode_fused_noalloc: cudaStreamWaitEvent");
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
-                     acc, acc_used, st, /*pdl=*/a->n_cols > 0, /*win_ring=*/W, a->start_pos);
+                     acc, acc_used, st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos);
 }
 
 sti_status sti_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, sti_stream stream) {

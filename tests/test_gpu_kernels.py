@@ -291,3 +291,33 @@ def test_decode_fused_topk_ties(sti, orc, probs, label):
     assert sti.read_device_status(ws) == 0
     got = tk.cpu().numpy().reshape(shp.b, 1, -1)[..., shp.window:]
     np.testing.assert_array_equal(got, ref_cidx)
+
+
+def test_decode_fused_waits_for_q_ready(sti):
+    """q uploaded on another stream: the attention step waits for the q_ready event and the
+    result equals the call with q already in place."""
+    import torch
+
+    shp = workloads.custom("decode_qready", b=4, s=1, start_pos=[4095, 2047, 300, 9000], seed=78, n_cols=2300,
+                           topk=512, h=64, d=512)
+    data = workloads.make(shp)
+    common = (to_dev(data["win"][0]), to_dev(data["comp"]), to_dev_any(data["sink"][0]), shp.softmax_scale,
+              to_dev(data["iq"]), to_dev(data["ik"]), to_dev(data["w"]), shp.index_scale,
+              to_dev_any(data["start_pos"]), shp.ratio, shp.n_cols, shp.topk)
+    a0, out0, _ = sti.decode_args(to_dev(data["q"][0]), *common)
+    sti.decode_fused(a0, sti.workspace(sti.decode_workspace_size(a0)))
+    side = torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    h_q = torch.from_numpy(data["q"][0].view(np.int16)).view(torch.bfloat16).pin_memory()
+    d_q = torch.zeros(h_q.shape, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(2_000_000)   # the upload lands well after the call is enqueued
+        d_q.copy_(h_q, non_blocking=True)
+        ev.record(side)
+    a1, out1, _ = sti.decode_args(d_q, *common, q_ready=ev)
+    ws1 = sti.workspace(sti.decode_workspace_size(a1))
+    sti.decode_fused(a1, ws1)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws1) == 0
+    assert torch.equal(out0, out1)
