@@ -63,7 +63,7 @@ __device__ unsigned long long g_hs_t[2048][32];
     } while (0)
 #endif
 
-constexpr int kHsThreads = 288;   // warps 0, 6, 7, 8 produce, 1 issues MMAs, 2-5 run the softmax
+constexpr int kHsThreads = 416;   // warps 0, 6, 7, 8 produce, 1 issues MMAs, 2-5 and 9-12 run the softmax
 constexpr int kProducers = 4;
 constexpr int kHsRows = 128;
 constexpr int kHsMaxSlots = 12;
@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                           const __grid_constant__ CUtensorMap tm_kv2, const __grid_constant__ CUtensorMap tm_win,
                           const AttnParams p, int n_slots) {
     static_assert(HC == 16 || HC == 32, "16 or 32 heads per CTA");
+    constexpr int kSets = HC == 32 ? 2 : 1;   // softmax warp groups, each over NH heads of every row
+    constexpr int NH = HC / kSets;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int S = n_slots;                                      // even, >= 2
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         }
         mbar_init(&tl->s_full[0], 1);
         mbar_init(&tl->s_full[1], 1);
-        mbar_init(&tl->p_full, 1);
+        mbar_init(&tl->p_full, (uint32_t)kSets);
         mbar_init(&tl->o_done, 1);
         mbar_init(&tl->q_bar, 1);
         mbar_init(&tl->recv_bar, 1);
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     const uint32_t tmem = tl->tmem_base;
     if (tid == 0) STI_HSTAMP(1);
 
-    if (warp == 0 || warp >= 6) {
+    if (warp == 0 || (warp >= 6 && warp <= 8)) {
         // ------------------------------------------------------------ producers
         // producer pi owns the ring slots = pi (mod 4): it waits, arms and fills only those, so
         // four issue streams of TMA gathers run side by side
@@ -411,13 +413,17 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax + epilogue
+    } else if ((warp >= 2 && warp <= 5) || (kSets == 2 && warp >= 9)) {
+        // ------------------------------------------------------------ softmax
+        // kSets groups of four warps; set s owns heads [s*NH, s*NH + NH) of every row
+        const int set = warp >= 9 ? 1 : 0;
         const int qd = warp & 3;                       // TMEM lane quarter of this warp
-        const int row = 32 * qd + lane;                // KV row of the tile / d row of an O^T block
-        const int st = tid - 64;                       // 0..127
+        const int row = 32 * qd + lane;                // KV row of the tile
+        const int st = tid - (set == 0 ? 64 : 288);    // 0..127 within the set
+        const int hoff = set * NH;
+        const uint32_t bar_id = 1u + (uint32_t)set;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        constexpr int kSpread = 32 / HC;               // lanes holding one head after a reduce-scatter
+        constexpr int kSpread = 32 / NH;               // lanes holding one head after a reduce-scatter
         if (!ring_tile) griddep_wait();
         bool dead = false;
         for (int t = 0; t < n_tiles; ++t) {
@@ -429,42 +435,43 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 valid = idx >= 0 && idx < n_rows;
             }
             if (!dead) dead = !hs_wait(&tl->s_full[t & 1], (uint32_t)((t >> 1) & 1), p.status, abort);
-            if (st == 0 && t < 5) STI_HSTAMP(15 + t);
+            if (set == 0 && st == 0 && t < 5) STI_HSTAMP(15 + t);
             tc_fence_after();
-            float x[HC];
+            float x[NH];
             {
-                uint32_t r[HC];
-                tmem_ld_n<HC>(tmem + lane_base + (uint32_t)((t & 1) * HC), r);
+                uint32_t r[NH];
+                tmem_ld_n<NH>(tmem + lane_base + (uint32_t)((t & 1) * HC + hoff), r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < HC; ++i) x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                for (int i = 0; i < NH; ++i) x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
             }
             {
-                float v[HC];
+                float v[NH];
 #pragma unroll
-                for (int i = 0; i < HC; ++i) v[i] = x[i];
-                warp_reduce_scatter_n<HC, true>(v);
-                if ((lane & (kSpread - 1)) == 0) tl->red_max[qd][lane / kSpread] = v[0];
+                for (int i = 0; i < NH; ++i) v[i] = x[i];
+                warp_reduce_scatter_n<NH, true>(v);
+                if ((lane & (kSpread - 1)) == 0) tl->red_max[qd][hoff + lane / kSpread] = v[0];
             }
-            named_bar_sync(1, 128);
-            if (st < HC) {
-                const float mt = fmaxf(fmaxf(tl->red_max[0][st], tl->red_max[1][st]),
-                                       fmaxf(tl->red_max[2][st], tl->red_max[3][st]));
-                const float m_old = tl->m_run[st];
+            named_bar_sync(bar_id, 128);
+            if (st < NH) {
+                const int hh = hoff + st;
+                const float mt = fmaxf(fmaxf(tl->red_max[0][hh], tl->red_max[1][hh]),
+                                       fmaxf(tl->red_max[2][hh], tl->red_max[3][hh]));
+                const float m_old = tl->m_run[hh];
                 // the running max moves only when a tile's max passes it by more than 8 (log2
                 // units): every P stays <= 2^8 and O, l are rescaled only when a max moves
                 const float m_new = (m_old == -INFINITY || mt > m_old + 8.f) ? fmaxf(m_old, mt) : m_old;
-                tl->alpha[st] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
-                tl->m_run[st] = m_new;
+                tl->alpha[hh] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+                tl->m_run[hh] = m_new;
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(bar_id, 128);
             // the previous tile's PV product has read P^T and O^T before they change
             if (t > 0 && !dead) dead = !hs_wait(&tl->o_done, (uint32_t)((t - 1) & 1), p.status, abort);
             tc_fence_after();
-            float v2[HC];
+            float v2[NH];
 #pragma unroll
-            for (int i = 0; i < HC; ++i) {
-                const float m = tl->m_run[i];
+            for (int i = 0; i < NH; ++i) {
+                const float m = tl->m_run[hoff + i];
                 x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
                 v2[i] = x[i];
             }
@@ -472,38 +479,42 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 uint8_t* pb = p_s + (row >> 6) * HC * 128;
                 const int kr = row & 63;
 #pragma unroll
-                for (int i = 0; i < HC; ++i)
-                    *reinterpret_cast<__nv_bfloat16*>(pb + i * 128 + ((((kr >> 3) ^ (i & 7))) << 4) + (kr & 7) * 2) =
+                for (int i = 0; i < NH; ++i) {
+                    const int hi = hoff + i;
+                    *reinterpret_cast<__nv_bfloat16*>(pb + hi * 128 + ((((kr >> 3) ^ (hi & 7))) << 4) + (kr & 7) * 2) =
                         __float2bfloat16_rn(x[i]);
+                }
             }
-            warp_reduce_scatter_n<HC, false>(v2);
-            if ((lane & (kSpread - 1)) == 0) tl->red_sum[qd][lane / kSpread] = v2[0];
+            warp_reduce_scatter_n<NH, false>(v2);
+            if ((lane & (kSpread - 1)) == 0) tl->red_sum[qd][hoff + lane / kSpread] = v2[0];
             bool rescale = false;
 #pragma unroll
-            for (int i = 0; i < HC; ++i) rescale = rescale || tl->alpha[i] != 1.f;
+            for (int i = 0; i < NH; ++i) rescale = rescale || tl->alpha[hoff + i] != 1.f;
             if (t > 0 && rescale) {   // O^T rows (lane = d within a block) times the heads' factors
                 for (int m = 0; m < nmb; ++m) {
-                    const uint32_t ta = tmem + lane_base + (uint32_t)(2 * HC + m * HC);
-                    uint32_t r[HC];
-                    tmem_ld_n<HC>(ta, r);
+                    const uint32_t ta = tmem + lane_base + (uint32_t)(2 * HC + m * HC + hoff);
+                    uint32_t r[NH];
+                    tmem_ld_n<NH>(ta, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < HC; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[i]);
-                    tmem_st_n<HC>(ta, r);
+                    for (int i = 0; i < NH; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[hoff + i]);
+                    tmem_st_n<NH>(ta, r);
                 }
                 tmem_st_wait();
             }
             fence_proxy_async_smem();   // P^T: generic writes read by the MMA
             tc_fence_before();
-            named_bar_sync(1, 128);
-            if (st < HC)
-                tl->l_run[st] = tl->l_run[st] * tl->alpha[st] + (tl->red_sum[0][st] + tl->red_sum[1][st]) +
-                                (tl->red_sum[2][st] + tl->red_sum[3][st]);
-            if (st == 0) mbar_arrive(&tl->p_full);
-            if (st == 0 && t < 5) STI_HSTAMP(20 + t);
+            named_bar_sync(bar_id, 128);
+            if (st < NH) {
+                const int hh = hoff + st;
+                tl->l_run[hh] = tl->l_run[hh] * tl->alpha[hh] + (tl->red_sum[0][hh] + tl->red_sum[1][hh]) +
+                                (tl->red_sum[2][hh] + tl->red_sum[3][hh]);
+            }
+            if (st == 0) mbar_arrive(&tl->p_full);   // one arrival per set
+            if (set == 0 && st == 0 && t < 5) STI_HSTAMP(20 + t);
         }
         if (!dead && n_tiles > 0) dead = !hs_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
-        if (st == 0) STI_HSTAMP(12);
+        if (set == 0 && st == 0) STI_HSTAMP(12);
     }
 
     // ---- epilogue: o = O / (l + 2^(sink*log2e - m)); heads with no valid slot give 0
