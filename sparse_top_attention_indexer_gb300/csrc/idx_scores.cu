@@ -108,6 +108,10 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int Di, i
     return sdesc(addr, 16, 512, kLayoutSW64);
 }
 
+#ifdef STI_STEP_TIMING
+__device__ unsigned long long g_sc_t[2048][2];   // global timer at CTA start and end (profiling builds)
+#endif
+
 template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -116,6 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
     // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+#ifdef STI_STEP_TIMING
+    if (threadIdx.x == 0 && blockIdx.x < 2048) g_sc_t[blockIdx.x][0] = global_timer_ns();
+#endif
     griddep_launch_dependents();   // the top-k may be scheduled now; it waits for this grid's end
     const int a_bytes = kTileKeys * p.Di * 2;
     const int b_bytes = p.n_pad * p.Di * 2;
@@ -356,6 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
     }
+#ifdef STI_STEP_TIMING
+    if (threadIdx.x == 0 && blockIdx.x < 2048) g_sc_t[blockIdx.x][1] = global_timer_ns();
+#endif
 }
 
 }  // namespace
@@ -404,3 +414,10 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
 }
 
 }  // namespace sti
+
+#ifdef STI_STEP_TIMING
+// profiling builds only: global-timer stamps (ns) of the scores kernel's CTAs
+extern "C" int sti_dbg_scores_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_sc_t, sizeof(unsigned long long) * 2 * (size_t)n_blocks);
+}
+#endif

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
 // positions at its offset, in ascending position order.
 
 #ifdef STI_TOPK_TIMING
-__device__ unsigned long long g_topk_t[2048][16];
+__device__ unsigned long long g_topk_t[2048][17];
 #define STI_KSTAMP(i)                                                                                  \
     do {                                                                                               \
         if (threadIdx.x == 0 && blockIdx.x < 2048) g_topk_t[blockIdx.x][i] = clock64();                \
@@ -417,6 +417,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(const TopkP
     STI_KSTAMP(1);
     griddep_wait();   // the scores and the histogram are complete from here on
     STI_KSTAMP(2);
+    STI_KGSTAMP(16);
     uint32_t hreg[kBins / kClThreads];
 #pragma unroll
     for (int i = 0; i < kBins / kClThreads; ++i) hreg[i] = __ldg(ghist + i * kClThreads + tid);
@@ -794,6 +795,6 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
 #ifdef STI_TOPK_TIMING
 // profiling builds only: per-CTA clock64 stamps of the cluster top-k phases
 extern "C" int sti_dbg_topk_times(unsigned long long* host, int n_blocks) {
-    return (int)cudaMemcpyFromSymbol(host, sti::g_topk_t, sizeof(unsigned long long) * 16 * (size_t)n_blocks);
+    return (int)cudaMemcpyFromSymbol(host, sti::g_topk_t, sizeof(unsigned long long) * 17 * (size_t)n_blocks);
 }
 #endif

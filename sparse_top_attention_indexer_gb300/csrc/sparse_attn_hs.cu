@@ -81,14 +81,14 @@ struct __align__(8) HsTail {
     uint64_t q_bar;                // Q rows of this CTA's heads landed
     uint64_t recv_bar;             // row-split merge: the partner's partial and (m, l) landed
     uint64_t ready_bar;            // row-split merge: the partner's ring is free to receive
-    float peer_ml[32][2];          // row-split merge: the partner's (m, l) per head
+    float peer_ml[64][2];          // row-split merge: the partner's (m, l) per head
     uint32_t tmem_base;
     int abort;                     // a wait of this CTA timed out: the others stop waiting
-    float m_run[32];               // running max per head, log2 domain
-    float l_run[32];               // running sum of 2^(x - m)
-    float alpha[32];               // rescale factor of this tile / final 1 / denominator
-    float red_max[4][32];          // per-warp partial maxima
-    float red_sum[4][32];          // per-warp partial sums
+    float m_run[64];               // running max per head, log2 domain
+    float l_run[64];               // running sum of 2^(x - m)
+    float alpha[64];               // rescale factor of this tile / final 1 / denominator
+    float red_max[4][64];          // per-warp partial maxima
+    float red_sum[4][64];          // per-warp partial sums
 };
 
 // Bounded wait that also gives up when another thread of the CTA already timed out.
@@ -142,7 +142,8 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]
     else tmem_st32(taddr, r);
 }
 
-__host__ __device__ constexpr uint32_t hs_tmem_cols(int hc) { return hc == 16 ? 128u : 256u; }
+// S^T double buffer (2 x hc columns) and O^T (d/128 blocks of hc columns, d <= 512)
+__host__ __device__ constexpr uint32_t hs_tmem_cols(int hc) { return hc == 16 ? 128u : (hc == 32 ? 256u : 512u); }
 
 __host__ __device__ constexpr size_t hs_smem_bytes(int hc, int d, int slots) {
     return 1024 + (size_t)slots * kSlotBytes + (size_t)hc * d * 2 + (size_t)hc * 256 + sizeof(HsTail);
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     sparse_attn_hs_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
                           const __grid_constant__ CUtensorMap tm_kv2, const __grid_constant__ CUtensorMap tm_win,
                           const AttnParams p, int n_slots) {
-    static_assert(HC == 16 || HC == 32, "16 or 32 heads per CTA");
-    constexpr int kSets = HC == 32 ? 2 : 1;   // softmax warp groups, each over NH heads of every row
+    static_assert(HC == 16 || HC == 32 || HC == 64, "16, 32 or 64 heads per CTA");
+    constexpr int kSets = HC >= 32 ? 2 : 1;   // softmax warp groups, each over NH heads of every row
     constexpr int NH = HC / kSets;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -189,6 +190,9 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     const bool ring_tile = p.win_ring == kHsRows && r0 == 0 && r1 - r0 >= kHsRows &&
                            __ldg(p.start_pos + b) >= kHsRows - 1;
     if (tid == 0) STI_HSTAMP(0);
+#ifdef STI_ATTN_TIMING
+    if (tid == 0 && blockIdx.x < 2048) g_hs_t[blockIdx.x][30] = global_timer_ns();
+#endif
 
     if (warp == 1) {
         tmem_alloc(&tl->tmem_base, hs_tmem_cols(HC));
@@ -246,7 +250,9 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             if (lane == 0) {
                 for (int j = pi; j < ncb; j += kProducers) {   // tile 0: column block j in slot j
                     mbar_arrive_expect_tx(&tl->full[j], kSlotBytes);
-                    if (hg == 0)
+                    if (CH == 1)
+                        tma_load_2d(ring + (size_t)j * kSlotBytes, &tm_win, &tl->full[j], j * 64, b * (int)p.rows1);
+                    else if (hg == 0)
                         tma_load_2d_mc(ring + (size_t)j * kSlotBytes, &tm_win, &tl->full[j], j * 64, b * (int)p.rows1,
                                        cta_mask);
                 }
@@ -255,6 +261,9 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             t_first = 1;
         }
         griddep_wait();   // the indices are complete from here on
+#ifdef STI_ATTN_TIMING
+        if (pi == 0 && lane == 0 && blockIdx.x < 2048) g_hs_e[blockIdx.x][5] = global_timer_ns();
+#endif
         for (int t = t_first; t < n_tiles && !dead; ++t) {
             int sid[4], crd[4];
             int first_s = -1, first_c = 0, n_valid = 0;
@@ -312,16 +321,23 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 if (mine && !empty) {
                     if (!mixed) {
                         // masked rows of the group repeat its first valid row
-                        tma_gather4_mc(dst + lane * 512, map, &tl->full[slot], j * 64, sid[0] >= 0 ? crd[0] : first_c,
-                                       sid[1] >= 0 ? crd[1] : first_c, sid[2] >= 0 ? crd[2] : first_c,
-                                       sid[3] >= 0 ? crd[3] : first_c, cta_mask);
+                        const int y0 = sid[0] >= 0 ? crd[0] : first_c, y1 = sid[1] >= 0 ? crd[1] : first_c;
+                        const int y2 = sid[2] >= 0 ? crd[2] : first_c, y3 = sid[3] >= 0 ? crd[3] : first_c;
+                        if (CH == 1)
+                            tma_gather4(dst + lane * 512, map, &tl->full[slot], j * 64, y0, y1, y2, y3);
+                        else
+                            tma_gather4_mc(dst + lane * 512, map, &tl->full[slot], j * 64, y0, y1, y2, y3, cta_mask);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            if (sid[i] >= 0)
-                                tma_load_2d_mc(dst + (4 * lane + i) * 128,
-                                               sid[i] == 1 ? (const void*)&tm_kv2 : (const void*)&tm_kv1,
-                                               &tl->full[slot], j * 64, crd[i], cta_mask);
+                            if (sid[i] >= 0) {
+                                const void* m = sid[i] == 1 ? (const void*)&tm_kv2 : (const void*)&tm_kv1;
+                                if (CH == 1)
+                                    tma_load_2d(dst + (4 * lane + i) * 128, m, &tl->full[slot], j * 64, crd[i]);
+                                else
+                                    tma_load_2d_mc(dst + (4 * lane + i) * 128, m, &tl->full[slot], j * 64, crd[i],
+                                                   cta_mask);
+                            }
                     }
                 }
             }
@@ -402,8 +418,13 @@ __global__ void __launch_bounds__(kHsThreads, 1)
 #ifdef STI_ATTN_TIMING
                     if (t < 5 && blockIdx.x < 2048) g_hs_p[blockIdx.x][t * 8 + 1 + 2 * m] = clock64();
 #endif
-                    umma_commit_mc(&tl->empty[slot], cta_mask);
-                    umma_commit_mc(&tl->empty[slot + 1], cta_mask);
+                    if (CH == 1) {
+                        umma_commit(&tl->empty[slot]);
+                        umma_commit(&tl->empty[slot + 1]);
+                    } else {
+                        umma_commit_mc(&tl->empty[slot], cta_mask);
+                        umma_commit_mc(&tl->empty[slot + 1], cta_mask);
+                    }
 #ifdef STI_ATTN_TIMING
                     if (t < 5 && blockIdx.x < 2048) g_hs_p[blockIdx.x][t * 8 + 2 + 2 * m] = clock64();
 #endif
@@ -525,13 +546,16 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     const int st = tid - 64;                                  // softmax threads: 0..127
     const int row = 32 * (warp & 3) + lane;                   // their TMEM lane (d within a block)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    auto o_block = [&](int m, uint32_t (&r)[HC]) {            // this thread's O^T row of d-block m
+    // the epilogue runs on every softmax warp: set s takes heads [s*NH, s*NH + NH) of its O^T row
+    const bool ep_warp = sm_warp || (kSets == 2 && warp >= 9);
+    const int ehoff = warp >= 9 ? NH : 0;
+    auto o_part = [&](int m, uint32_t (&r)[NH]) {
         if (n_tiles > 0) {
-            tmem_ld_n<HC>(tmem + lane_base + (uint32_t)(2 * HC + m * HC), r);
+            tmem_ld_n<NH>(tmem + lane_base + (uint32_t)(2 * HC + m * HC + ehoff), r);
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int i = 0; i < HC; ++i) r[i] = 0u;
+            for (int i = 0; i < NH; ++i) r[i] = 0u;
         }
     };
     if (CR == 1) {
@@ -550,15 +574,15 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         __syncthreads();
         // [HC][d] bf16 staged in the Q buffer (every QK product has completed) -> one bulk store
         uint16_t* stage = reinterpret_cast<uint16_t*>(q_s);
-        if (sm_warp)
+        if (ep_warp)
             for (int m = 0; m < nmb; ++m) {
-                uint32_t r[HC];
-                o_block(m, r);
+                uint32_t r[NH];
+                o_part(m, r);
                 const int dd = 128 * m + row;
 #pragma unroll
-                for (int i = 0; i < HC; ++i)
-                    stage[(size_t)i * p.d + dd] =
-                        __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[i]));
+                for (int i = 0; i < NH; ++i)
+                    stage[(size_t)(ehoff + i) * p.d + dd] = __bfloat16_as_ushort(
+                        __float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[ehoff + i]));
             }
         fence_proxy_async_smem();
         __syncthreads();
@@ -582,20 +606,22 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         if (tid == 64) STI_ESTAMP(0);
         const bool ready = hs_wait(&tl->ready_bar, 0, p.status, abort);
         if (tid == 64) STI_ESTAMP(1);
-        if (sm_warp && ready) {
+        if (ep_warp && ready) {
             const uint32_t rbar = dsmem_addr(&tl->recv_bar, (uint32_t)partner);
             const uint32_t rbase = dsmem_addr(recv, (uint32_t)partner);
             for (int m = mb_peer; m < mb_peer + nmb / 2; ++m) {
-                uint32_t r[HC];
-                o_block(m, r);
+                uint32_t r[NH];
+                o_part(m, r);
                 const int dl = (m - mb_peer) * 128 + row;
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    st_async_v4(rbase + (uint32_t)(dl * HC + ((c ^ (dl % kChunks)) * 4)) * 4u, __uint_as_float(r[4 * c]),
+                for (int c = 0; c < NH / 4; ++c) {
+                    const int cc = ehoff / 4 + c;
+                    st_async_v4(rbase + (uint32_t)(dl * HC + ((cc ^ (dl % kChunks)) * 4)) * 4u, __uint_as_float(r[4 * c]),
                                 __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
                                 __uint_as_float(r[4 * c + 3]), rbar);
+                }
             }
-            if (st < HC)
+            if (sm_warp && st < HC)
                 st_async_v2(dsmem_addr(&tl->peer_ml[st][0], (uint32_t)partner), tl->m_run[st], tl->l_run[st], rbar);
         }
         if (tid == 64) STI_ESTAMP(2);
@@ -619,22 +645,23 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             if (rg == 0 && p.lse) p.lse[(size_t)query * p.h + hh] = lse;
         }
         __syncthreads();
-        if (sm_warp && got)   // own half of d: combine and write bf16 rows straight to global
+        if (ep_warp && got)   // own half of d: combine and write bf16 rows straight to global
             for (int m = mb_own; m < mb_own + nmb / 2; ++m) {
-                uint32_t r[HC];
-                o_block(m, r);
+                uint32_t r[NH];
+                o_part(m, r);
                 const int dl = (m - mb_own) * 128 + row;
                 const float4* rv = reinterpret_cast<const float4*>(recv + (size_t)dl * HC);
                 uint16_t* orow = p.out + ((size_t)query * p.h + (size_t)hg * HC) * p.d + (size_t)rg * half + dl;
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    const float4 q4 = rv[c ^ (dl % kChunks)];
+                for (int c = 0; c < NH / 4; ++c) {
+                    const int cc = ehoff / 4 + c;
+                    const float4 q4 = rv[cc ^ (dl % kChunks)];
                     const float pv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int i = 4 * c + e;
+                        const int i = 4 * cc + e;
                         orow[(size_t)i * p.d] = __bfloat16_as_ushort(__float2bfloat16_rn(
-                            __uint_as_float(r[i]) * tl->alpha[i] + pv[e] * tl->red_max[0][i]));
+                            __uint_as_float(r[4 * c + e]) * tl->alpha[i] + pv[e] * tl->red_max[0][i]));
                     }
                 }
             }
@@ -650,6 +677,9 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     }
     cluster_sync();   // no CTA leaves while a partner may still signal or fill its shared memory
     if (tid == 0) STI_HSTAMP(14);
+#ifdef STI_ATTN_TIMING
+    if (tid == 0 && blockIdx.x < 2048) g_hs_t[blockIdx.x][31] = global_timer_ns();
+#endif
 }
 
 constexpr int kSmemLimit = 232448;   // opt-in dynamic shared memory per CTA
@@ -775,6 +805,7 @@ cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm
     const int hc = p.h * p.hs_rows / p.cluster;
     if (hc == 16) return launch_hs<16>(tm_q, tm_kv1, tm_kv2, tm_win, p, stream);
     if (hc == 32) return launch_hs<32>(tm_q, tm_kv1, tm_kv2, tm_win, p, stream);
+    if (hc == 64) return launch_hs<64>(tm_q, tm_kv1, tm_kv2, tm_win, p, stream);
     return cudaErrorInvalidValue;
 }
 
