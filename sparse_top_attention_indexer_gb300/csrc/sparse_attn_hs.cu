@@ -35,6 +35,7 @@
 
 #include "sti_internal.h"
 #include "sti_ptx.cuh"
+#include "sti_attn_util.cuh"
 
 namespace sti {
 namespace {
@@ -90,57 +91,6 @@ struct __align__(8) HsTail {
     float red_max[4][64];          // per-warp partial maxima
     float red_sum[4][64];          // per-warp partial sums
 };
-
-// Bounded wait that also gives up when another thread of the CTA already timed out.
-__device__ __forceinline__ bool hs_wait(uint64_t* bar, uint32_t parity, uint32_t* status, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
-            if (status) atomicOr(status, 2u /* STI_FLAG_TIMEOUT */);
-            *abort = 1;
-            return false;
-        }
-    }
-}
-
-// Reduce N values per lane over the warp's 32 lanes, scattering the results: afterwards v[0] of
-// lane l is the reduction of value l >> (5 - log2 N) (each held by 32/N adjacent lanes).
-template <int N, bool IS_MAX>
-__device__ __forceinline__ void warp_reduce_scatter_n(float (&v)[N]) {
-    const int lane = threadIdx.x & 31;
-    int off = 16;
-#pragma unroll
-    for (int half = N / 2; half >= 1; half >>= 1, off >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float lo = v[i], hi = v[i + half];
-            const float send = upper ? lo : hi;
-            const float keep = upper ? hi : lo;
-            const float recv = __shfl_xor_sync(kFull, send, off);
-            v[i] = IS_MAX ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-#pragma unroll
-    for (; off >= 1; off >>= 1) {
-        const float recv = __shfl_xor_sync(kFull, v[0], off);
-        v[0] = IS_MAX ? fmaxf(v[0], recv) : v[0] + recv;
-    }
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
-    if constexpr (N == 16) tmem_ld16(taddr, r);
-    else tmem_ld32(taddr, r);
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 16) tmem_st16(taddr, r);
-    else tmem_st32(taddr, r);
-}
 
 // S^T double buffer (2 x hc columns) and O^T (d/128 blocks of hc columns, d <= 512)
 __host__ __device__ constexpr uint32_t hs_tmem_cols(int hc) { return hc == 16 ? 128u : (hc == 32 ? 256u : 512u); }
@@ -310,7 +260,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             for (int j = 0; j < ncb; ++j) {
                 const int G = t * ncb + j, slot = G % S, use = G / S;
                 if (slot % kProducers != pi) continue;
-                if (use > 0 && !dead) dead = !hs_wait(&tl->empty[slot], (uint32_t)((use - 1) & 1), p.status, abort);
+                if (use > 0 && !dead) dead = !attn_wait(&tl->empty[slot], (uint32_t)((use - 1) & 1), p.status, abort);
 #ifdef STI_ATTN_TIMING
                 (void)0;
 #endif
@@ -347,12 +297,12 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         const int total = n_tiles * ncb;
         for (int s2 = pi; s2 < S && s2 < total && !dead; s2 += kProducers) {
             const int uses = (total - s2 + S - 1) / S;
-            dead = !hs_wait(&tl->empty[s2], (uint32_t)((uses - 1) & 1), p.status, abort);
+            dead = !attn_wait(&tl->empty[s2], (uint32_t)((uses - 1) & 1), p.status, abort);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            bool dead = !hs_wait(&tl->q_bar, 0, p.status, abort);
+            bool dead = !attn_wait(&tl->q_bar, 0, p.status, abort);
             const uint32_t idesc_qk = idesc_bf16_f32(kHsRows, HC, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(128, HC, true, false);
             const uint32_t q0 = smem_u32(q_s), p0 = smem_u32(p_s), r0 = smem_u32(ring);
@@ -366,8 +316,8 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             auto issue_qk = [&](bool block) -> bool {
                 const int G = qk_t * ncb + qk_j, slot = G % S, use = G / S;
                 if (block) {
-                    if (!hs_wait(&tl->full[slot], (uint32_t)(use & 1), p.status, abort)) return false;
-                } else if (!mbar_try_wait(&tl->full[slot], (uint32_t)(use & 1))) {
+                    if (!attn_wait(&tl->full[slot], (uint32_t)(use & 1), p.status, abort)) return false;
+                } else if (!mbar_test_wait(&tl->full[slot], (uint32_t)(use & 1))) {
                     return false;
                 }
                 tc_fence_after();
@@ -392,7 +342,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 // (it writes the other S^T buffer, whose softmax finished before PV(t-1))
                 {
                     const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(&tl->p_full, (uint32_t)(t & 1))) {
+                    while (!mbar_test_wait(&tl->p_full, (uint32_t)(t & 1))) {
                         if (qk_t == t + 1 && qk_t < n_tiles && issue_qk(false)) continue;
                         if (*abort || global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
                             if (!*abort) atomicOr(p.status, 2u /* STI_FLAG_TIMEOUT */);
@@ -455,7 +405,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 const int idx = slot_i < r1 ? __ldg(idx_row + slot_i) : -1;
                 valid = idx >= 0 && idx < n_rows;
             }
-            if (!dead) dead = !hs_wait(&tl->s_full[t & 1], (uint32_t)((t >> 1) & 1), p.status, abort);
+            if (!dead) dead = !attn_wait(&tl->s_full[t & 1], (uint32_t)((t >> 1) & 1), p.status, abort);
             if (set == 0 && st == 0 && t < 5) STI_HSTAMP(15 + t);
             tc_fence_after();
             float x[NH];
@@ -487,7 +437,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             }
             named_bar_sync(bar_id, 128);
             // the previous tile's PV product has read P^T and O^T before they change
-            if (t > 0 && !dead) dead = !hs_wait(&tl->o_done, (uint32_t)((t - 1) & 1), p.status, abort);
+            if (t > 0 && !dead) dead = !attn_wait(&tl->o_done, (uint32_t)((t - 1) & 1), p.status, abort);
             tc_fence_after();
             float v2[NH];
 #pragma unroll
@@ -534,7 +484,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
             if (st == 0) mbar_arrive(&tl->p_full);   // one arrival per set
             if (set == 0 && st == 0 && t < 5) STI_HSTAMP(20 + t);
         }
-        if (!dead && n_tiles > 0) dead = !hs_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
+        if (!dead && n_tiles > 0) dead = !attn_wait(&tl->o_done, (uint32_t)((n_tiles - 1) & 1), p.status, abort);
         if (set == 0 && st == 0) STI_HSTAMP(12);
     }
 
@@ -604,7 +554,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         float* recv = reinterpret_cast<float*>(ring);         // [half][HC], chunk c of row r at c ^ (r % kChunks)
         if (tid == 0) mbar_arrive_remote(dsmem_addr(&tl->ready_bar, (uint32_t)partner));
         if (tid == 64) STI_ESTAMP(0);
-        const bool ready = hs_wait(&tl->ready_bar, 0, p.status, abort);
+        const bool ready = attn_wait(&tl->ready_bar, 0, p.status, abort);
         if (tid == 64) STI_ESTAMP(1);
         if (ep_warp && ready) {
             const uint32_t rbar = dsmem_addr(&tl->recv_bar, (uint32_t)partner);
@@ -625,7 +575,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 st_async_v2(dsmem_addr(&tl->peer_ml[st][0], (uint32_t)partner), tl->m_run[st], tl->l_run[st], rbar);
         }
         if (tid == 64) STI_ESTAMP(2);
-        const bool got = hs_wait(&tl->recv_bar, 0, p.status, abort);
+        const bool got = attn_wait(&tl->recv_bar, 0, p.status, abort);
         if (tid == 64) STI_ESTAMP(3);
         if (sm_warp && st < HC) {   // scale factors of the two partials; lse (first row group)
             const int hh = hg * HC + st;

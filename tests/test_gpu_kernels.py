@@ -149,6 +149,43 @@ def test_sparse_attn(sti, orc, b, s, h, d, k, n1, n2, empty):
     np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("b,s,d,k,n1,n2", [
+    (1, 300, 512, 200, 256, 256),    # k not a multiple of the 64-row tile
+    (2, 150, 256, 130, 100, 300),
+    (1, 260, 128, 640, 300, 700),
+])
+def test_sparse_attn_many_queries(sti, orc, b, s, d, k, n1, n2):
+    """More than 256 queries of 64 heads (one CTA per query, no split): random masked slots, rows
+    mixing both sources inside a four-row group, all -1 rows, and rows whose filled slots end
+    early (whole trailing tiles of -1)."""
+    import torch
+
+    rng = rng_for(760 + d, k)
+    h = 64
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = index_lists(rng, b, s, k, n1 + n2, masked_frac=0.15, empty_rows=2)
+    for t in range(0, s, 7):                    # filled slots end early
+        idx[0, t, rng.integers(0, k):] = -1
+    ref, ref_lse = orc.sparse_attn(q, kv1, sink, idx, d ** -0.5, kv2=kv2)
+    lse = torch.empty(b, s, h, dtype=torch.float32, device="cuda")
+    ws = sti.workspace(256)
+    out = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5,
+                               kv2=to_dev(kv2), lse=lse, ws=ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got = bf16_out_to_f64(out)
+    check_attn(got, ref)
+    empty = np.all(idx < 0, axis=-1)
+    assert np.all(got[empty] == 0)
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+
+
 def test_sparse_attn_whole_tiles_masked(sti, orc):
     """Decode-style rows where whole 128-slot tiles are -1 (short sequences), split over CTAs."""
     rng = rng_for(720, 0)
