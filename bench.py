@@ -1,6 +1,6 @@
 """Benchmark of the Indexer -> top-k -> sparse sink attention path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2|3|4|5] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..7] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
 window indices, Indexer scores, top-k, sparse sink attention (every attention layer),
@@ -428,7 +428,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -1,8 +1,9 @@
-"""GPU parity on the five named workloads at full size, in the launch configuration bench.py
-times (its GpuPath), against the CPU oracle on the same seeded inputs.
+"""GPU parity on the named workloads at full size, in the launch configuration bench.py times
+(its GpuPath), against the CPU oracle on the same seeded inputs.
 
-Decode workloads (b=32 ctx 65536; b=8 ctx 131072 with planted keys; b=64 ragged with three
-reuse layers) and the tiny prefill are compared element by element on every output.  The
+Decode workloads (b=32 ctx 65536 at compression ratios 4, 2 and 1; b=8 ctx 131072 with planted
+keys; b=64 ragged with three reuse layers) and the tiny prefill are compared element by element
+on every output.  The
 8192-query prefill is compared on a spread of sampled query rows (the oracle computes each
 one on its own), and on properties that hold for every row at full size."""
 import numpy as np
@@ -38,7 +39,7 @@ def _run(shape, data, device):
     return path
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 5])
+@pytest.mark.parametrize("n", [1, 2, 4, 5, 6, 7])
 def test_workload_full(gpu, orc, n):
     shape = workloads.config(n)
     data = workloads.make(shape)

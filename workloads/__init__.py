@@ -118,7 +118,8 @@ class Shape:
 
 
 def config(n: int) -> Shape:
-    """The five named workloads."""
+    """The named workloads: 1-5 as listed in the design notes, 6 and 7 the decode workload at
+    compression ratios 2 and 1 (32768 and 65536 index rows per sequence)."""
     seed = 1000 + n
     if n == 1:
         return Shape("tiny_prefill_s256_h4_d64", b=1, s=256, start_pos=np.zeros(1, np.int32), h=4, d=64, rd=16,
@@ -137,6 +138,10 @@ def config(n: int) -> Shape:
         n_cols = int(lengths.max() // 4)
         return Shape("mixed_serving_b64_ctx1k-64k", b=64, s=1, start_pos=sp, n_cols=n_cols, rms_keys=True,
                      n_layers=4, seed=seed)
+    if n in (6, 7):   # the model's own compression ratios (2 and 1) at context 65536
+        r = 2 if n == 6 else 1
+        return Shape(f"decode_b32_ctx65536_r{r}", b=32, s=1, start_pos=np.full(32, 65535, np.int32), ratio=r,
+                     n_cols=65536 // r, rms_keys=True, seed=seed)
     raise ValueError(f"no workload {n}")
 
 
