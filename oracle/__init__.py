@@ -15,6 +15,8 @@ Every function is pinned by the CPU tests in ``tests/test_oracle_*.py``:
   sparse_attn        textbook softmax (sink -> -inf), single-row closed form, empty rows,
                      duplicate-row sink shift, permutation invariance, mass + sink = 1
   dense_attn         independent of index lists; equal to sparse_attn when k >= visible
+  output_inverse_rope   identity at angle 0, the quarter-turn closed form, complex
+                     multiplication by e^{-i theta}, and undoing the generator's rotation
 """
 from __future__ import annotations
 
@@ -127,11 +129,33 @@ def topk(score, start_pos, ratio: int, k: int, offset: int, threads: int | None 
     return out
 
 
-def sparse_attn(q, kv1, sink, idx, scale: float, kv2=None, threads: int | None = None):
+def output_inverse_rope(out, rope_cs):
+    """The output's inverse rotary rotation, as Attention.forward applies it after sparse_attn
+    (DeepSeek V4.1, "attend/selected" page: apply_rotary_emb on o[..., -rd:] with the inverse
+    flag).  The rotation itself is not printed on the pages; its reading: the last rd dims form
+    rd/2 interleaved pairs (x, y) = (o[2i], o[2i+1]) of a complex number x + iy, multiplied by
+    conj(e^{i theta_i}) of the query's position.
+
+    out: [b, s, h, d] float64 (rotated in place and returned); rope_cs: [b, s, rd/2, 2] with
+    (cos theta_i, sin theta_i) per query and pair (any precision, widened to float64)."""
+    cs = np.asarray(rope_cs, dtype=np.float64)
+    b, s, h, d = out.shape
+    rd = 2 * cs.shape[2]
+    c = cs[..., 0][:, :, None, :]          # [b, s, 1, rd/2]
+    sn = cs[..., 1][:, :, None, :]
+    x = out[..., d - rd::2].copy()
+    y = out[..., d - rd + 1::2].copy()
+    out[..., d - rd::2] = x * c + y * sn
+    out[..., d - rd + 1::2] = y * c - x * sn
+    return out
+
+
+def sparse_attn(q, kv1, sink, idx, scale: float, kv2=None, threads: int | None = None, rope_cs=None):
     """Sparse attention with sink; returns (out [b,s,h,d] float64, lse [b,s,h] float64).
 
     q: [b, s, h, d] bf16 bits; kv1: [b, n1, d]; kv2: optional [b, n2, d] (row r >= n1 of the
-    concatenated KV is kv2[r - n1]); sink: [h] float32; idx: [b, s, k] int32."""
+    concatenated KV is kv2[r - n1]); sink: [h] float32; idx: [b, s, k] int32; rope_cs: optional
+    [b, s, rd/2, 2] (cos, sin) of the output's inverse rotation (output_inverse_rope)."""
     q = _c(q, np.uint16)
     kv1 = _c(kv1, np.uint16)
     kv2 = None if kv2 is None else _c(kv2, np.uint16)
@@ -147,6 +171,8 @@ def sparse_attn(q, kv1, sink, idx, scale: float, kv2=None, threads: int | None =
         _ptr(q), _ptr(kv1), n1 * d, _ptr(kv2), n2 * d, n1, n2, _ptr(sink), _ptr(idx), float(scale), b, s, h, d, k,
         _ptr(out), _ptr(lse), threads or default_threads(),
     )
+    if rope_cs is not None:
+        output_inverse_rope(out, rope_cs)
     return out, lse
 
 

@@ -11,6 +11,7 @@ import os
 import numpy as np
 import pytest
 
+import workloads
 from workloads import bf16_bits_to_f32, index_lists, rng_for, to_bf16_bits
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -381,3 +382,46 @@ def test_sparse_equals_dense_when_topk_covers(orc, mode):
     sparse, _ = orc.sparse_attn(q, win, sink, idx, d ** -0.5, kv2=comp)
     dense = orc.dense_attn(q, win, comp, sp, sink, d ** -0.5, W, r)
     np.testing.assert_allclose(sparse, dense, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ output inverse rotation
+
+
+def test_inverse_rope_identity_and_quarter_turn(orc):
+    rng = np.random.default_rng(5)
+    o = rng.standard_normal((2, 3, 4, 16))
+    cs0 = np.zeros((2, 3, 4, 2))
+    cs0[..., 0] = 1.0                                   # angle 0: nothing moves
+    np.testing.assert_array_equal(orc.output_inverse_rope(o.copy(), cs0), o)
+    cs90 = np.zeros((2, 3, 4, 2))
+    cs90[..., 1] = 1.0                                  # a quarter turn back: (x, y) -> (y, -x)
+    got = orc.output_inverse_rope(o.copy(), cs90)
+    np.testing.assert_array_equal(got[..., :8], o[..., :8])          # dims before the last rd
+    np.testing.assert_array_equal(got[..., 8::2], o[..., 9::2])
+    np.testing.assert_array_equal(got[..., 9::2], -o[..., 8::2])
+
+
+def test_inverse_rope_is_complex_multiplication_by_conjugate(orc):
+    rng = np.random.default_rng(6)
+    o = rng.standard_normal((1, 2, 3, 12))
+    theta = rng.uniform(-np.pi, np.pi, size=(1, 2, 4))
+    cs = np.stack([np.cos(theta), np.sin(theta)], axis=-1)
+    got = orc.output_inverse_rope(o.copy(), cs)
+    z = (o[..., 4::2] + 1j * o[..., 5::2]) * np.exp(-1j * theta)[:, :, None, :]
+    np.testing.assert_allclose(got[..., 4::2], z.real, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(got[..., 5::2], z.imag, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(got[..., :4], o[..., :4])
+
+
+def test_inverse_rope_undoes_the_generators_rotation(orc):
+    """The input generator rotates with its own code (position * theta^(-2i/rd), interleaved
+    pairs); the oracle's inverse with the same angles gives the vector back."""
+    rng = np.random.default_rng(7)
+    rd, th = 16, 10000.0
+    pos = np.array([0, 5, 1000])
+    x = rng.standard_normal((len(pos), 32))
+    rot = workloads._rope_interleaved(x.copy(), pos, rd, th)
+    ang = pos[:, None] * th ** (-np.arange(0, rd, 2) / rd)
+    cs = np.stack([np.cos(ang), np.sin(ang)], axis=-1)[None, :, None]          # [1, s, 1, rd/2, 2]
+    back = orc.output_inverse_rope(rot[None, :, None].copy(), cs[:, :, 0])
+    np.testing.assert_allclose(back[0, :, 0], x, rtol=0, atol=1e-12)
