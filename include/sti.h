@@ -163,6 +163,21 @@ sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t k
                                 int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                                 uint16_t *out, float *lse, void *ws, size_t ws_bytes, sti_stream stream);
 
+/* sti_sparse_attn_sink followed by the output's inverse rotary rotation, in the same kernel
+ * (Attention.forward, "attend/selected" page: apply_rotary_emb(o[..., -rd:], freqs_cis, True)
+ * right after sparse_attn).  rope_cs: fp32 [b, seqlen, rope_dims/2, 2], (cos, sin) of each
+ * interleaved pair's angle at the query's position -- the caller evaluates the frequencies, which
+ * the pages do not print.  Pair i = dims (d - rope_dims + 2i, +1) as x + iy is multiplied by
+ * cos - i sin: x' = x cos + y sin, y' = y cos - x sin, in fp32 before the bf16 rounding.
+ * rope_dims: even, 1 <= rope_dims <= d (STI_ERR_INVALID_ARG otherwise, or when rope_cs is NULL).
+ * lse is that of the attention (the rotation leaves it unchanged).  Everything else as
+ * sti_sparse_attn_sink. */
+sti_status sti_sparse_attn_sink_rope(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,
+                                     int64_t kv2_bstride, int n1, int n2, const float *attn_sink, const int32_t *idxs,
+                                     int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d,
+                                     int k, const float *rope_cs, int rope_dims, uint16_t *out, float *lse, void *ws,
+                                     size_t ws_bytes, sti_stream stream);
+
 /* ------------------------------------------------------------------ fused decode layer */
 /*
  * One decode step (seqlen == 1) of an index-source attention layer, as
@@ -204,6 +219,14 @@ typedef struct sti_decode_args {
      * q's upload (on another stream) overlaps steps 1 and 2; NULL: q is ready when the call is
      * enqueued */
     void *q_ready;
+    /* optional: the inverse rotary rotation Attention.forward applies to the output after
+     * sparse_attn ("attend/selected" page: apply_rotary_emb on o[..., -rd:] with the inverse
+     * flag), fused into the attention's epilogue.  rope_cs: fp32 [b, rope_dims/2, 2], the
+     * (cos, sin) of each interleaved pair's angle at the query's position (the caller evaluates
+     * its frequencies); pair i = dims (d - rope_dims + 2i, d - rope_dims + 2i + 1) as x + iy is
+     * multiplied by cos - i sin.  rope_dims: 0 (none) or even, <= d. */
+    const float *rope_cs;
+    int rope_dims;
 } sti_decode_args;
 
 /* Steps 2 and 3 launch as programmatic dependents of the step before them: each is scheduled

@@ -29,7 +29,8 @@ FLAG_INDEX_RANGE, FLAG_TIMEOUT, FLAG_CHUNKED = 1, 2, 4
 
 EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_device_status", "sti_window_idxs",
            "sti_idx_scores_workspace_size", "sti_idx_scores", "sti_idx_topk_workspace_size", "sti_idx_topk",
-           "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_decode_workspace_size",
+           "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_sparse_attn_sink_rope",
+           "sti_decode_workspace_size",
            "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
            "sti_selftest_wait_timeout"]
 
@@ -51,6 +52,7 @@ class DecodeArgs(ctypes.Structure):
         ("index_scale", ctypes.c_float), ("Hi", ctypes.c_int), ("Di", ctypes.c_int), ("index_topk", ctypes.c_int),
         ("ratio", ctypes.c_int), ("n_cols", ctypes.c_int), ("start_pos", ctypes.c_void_p), ("b", ctypes.c_int),
         ("out", ctypes.c_void_p), ("topk_idxs", ctypes.c_void_p), ("q_ready", ctypes.c_void_p),
+        ("rope_cs", ctypes.c_void_p), ("rope_dims", ctypes.c_int),
     ]
 
 
@@ -80,6 +82,9 @@ def lib() -> ctypes.CDLL:
         L.sti_sparse_attn_workspace_size.restype = SZ
         L.sti_sparse_attn_sink.argtypes = [P, P, I64, P, I64, I, I, P, P, I64, F, I, I, I, I, I, P, P, P, SZ, P]
         L.sti_sparse_attn_sink.restype = I
+        L.sti_sparse_attn_sink_rope.argtypes = [P, P, I64, P, I64, I, I, P, P, I64, F, I, I, I, I, I, P, I, P, P, P,
+                                                SZ, P]
+        L.sti_sparse_attn_sink_rope.restype = I
         L.sti_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.sti_decode_workspace_size.restype = SZ
         L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
@@ -193,9 +198,12 @@ def sparse_attn_workspace_size(b: int, s: int, h: int, d: int, k: int) -> int:
 
 def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor, topk_idxs: torch.Tensor,
                      softmax_scale: float, kv2: torch.Tensor | None = None, out: torch.Tensor | None = None,
-                     lse: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                     lse: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None,
+                     rope_cs: torch.Tensor | None = None) -> torch.Tensor:
     """sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale) with an optional second KV source:
-    row r < kv.shape[1] is kv[b, r], row r >= kv.shape[1] is kv2[b, r - kv.shape[1]]."""
+    row r < kv.shape[1] is kv[b, r], row r >= kv.shape[1] is kv2[b, r - kv.shape[1]].
+    rope_cs: optional fp32 [b, s, rd/2, 2] (cos, sin): the output's last rd dims are rotated
+    back by those angles in the same kernel (sti_sparse_attn_sink_rope)."""
     _need(q, torch.bfloat16, "q")
     _need(attn_sink, torch.float32, "attn_sink")
     _need(kv, torch.bfloat16, "kv", contiguous=False)
@@ -211,6 +219,16 @@ def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
     if out is None:
         out = torch.empty_like(q)
     ws = ws if ws is not None else workspace(sparse_attn_workspace_size(b, s, h, d, k), q.device)
+    if rope_cs is not None:
+        _need(rope_cs, torch.float32, "rope_cs")
+        if rope_cs.dim() != 4 or tuple(rope_cs.shape[:2]) != (b, s) or rope_cs.shape[3] != 2:
+            raise ValueError("rope_cs must be [b, s, rd/2, 2]")
+        _check(lib().sti_sparse_attn_sink_rope(
+            _ptr(q), _ptr(kv), kv.stride(0), _ptr(kv2), 0 if kv2 is None else kv2.stride(0), n1, n2, _ptr(attn_sink),
+            _ptr(topk_idxs), topk_idxs.stride(-2), float(softmax_scale), b, s, h, d, k, _ptr(rope_cs),
+            2 * rope_cs.shape[2], _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)),
+            "sti_sparse_attn_sink_rope")
+        return out
     _check(lib().sti_sparse_attn_sink(
         _ptr(q), _ptr(kv), kv.stride(0), _ptr(kv2), 0 if kv2 is None else kv2.stride(0), n1, n2, _ptr(attn_sink),
         _ptr(topk_idxs), topk_idxs.stride(-2), float(softmax_scale), b, s, h, d, k, _ptr(out), _ptr(lse), _ptr(ws),
@@ -219,10 +237,12 @@ def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
 
 
 def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, index_scale, start_pos, ratio, n_cols,
-                index_topk, out=None, topk_idxs=None, q_ready=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
+                index_topk, out=None, topk_idxs=None, q_ready=None,
+                rope_cs=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
     """Fill sti_decode_args from tensors.  q [b,h,d] (or [b,1,h,d]), window_kv [b,W,d],
     comp_kv [b,cap,d], iq [b,Hi,Di] (or [b,1,Hi,Di]), ik [b,cap,Di], w [b,Hi] (or [b,1,Hi]).
     q_ready: optional torch.cuda.Event (already recorded once) the attention step waits for.
+    rope_cs: optional fp32 [b, rd/2, 2] (cos, sin) of the output's inverse rotation.
     The returned struct keeps references to every tensor it points to."""
     b = q.shape[0]
     h, d = q.shape[-2], q.shape[-1]
@@ -243,8 +263,13 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
                    float(softmax_scale), h, d, W, _ptr(iq), _ptr(ik), ik.stride(0), _ptr(w), float(index_scale), Hi,
                    Di, index_topk, ratio, n_cols, _ptr(start_pos), b, _ptr(out), _ptr(topk_idxs),
                    q_ready.cuda_event if q_ready is not None else None)
+    if rope_cs is not None:
+        _need(rope_cs, torch.float32, "rope_cs")
+        if rope_cs.dim() != 3 or rope_cs.shape[0] != b or rope_cs.shape[2] != 2:
+            raise ValueError("rope_cs must be [b, rd/2, 2]")
+        a.rope_cs, a.rope_dims = _ptr(rope_cs), 2 * rope_cs.shape[1]
     # the struct holds raw device pointers: keep their tensors alive as long as it lives
-    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready)
+    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready, rope_cs)
     return a, out, topk_idxs
 
 

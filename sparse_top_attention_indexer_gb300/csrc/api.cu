@@ -212,8 +212,10 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                             uint16_t* out, float* lse, uint32_t* status, float* acc, size_t acc_bytes,
                             cudaStream_t st, bool pdl = false, int win_ring = 0,
-                            const int32_t* start_pos = nullptr) {
+                            const int32_t* start_pos = nullptr, const float* rope_cs = nullptr, int rope_dims = 0) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
+    if (rope_dims < 0 || rope_dims % 2 != 0 || rope_dims > d || (rope_dims > 0 && !rope_cs))
+        return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
     if (!q || !attn_sink || !idxs || !out || (n1 > 0 && !kv) || (n2 > 0 && !kv2)) return STI_ERR_INVALID_ARG;
@@ -272,6 +274,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
                   p.rows1 >= 128) ? 128 : 0;
     p.start_pos = start_pos;
     p.hs_rows = head_split ? hs_rows : 1;
+    p.rope_cs = rope_dims > 0 ? rope_cs : nullptr;
+    p.rope_dims = rope_dims;
     if (!head_split && c_hs > 0) p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
     if (p.use_tma) {
         const uint32_t q_rows = head_split ? (uint32_t)(h * hs_rows / c_hs) : (uint32_t)h;
@@ -391,6 +395,19 @@ sti_status sti_sparse_attn_sink(const uint16_t* q, const uint16_t* kv, int64_t k
                      static_cast<cudaStream_t>(stream));
 }
 
+sti_status sti_sparse_attn_sink_rope(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride, const uint16_t* kv2,
+                                     int64_t kv2_bstride, int n1, int n2, const float* attn_sink, const int32_t* idxs,
+                                     int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d,
+                                     int k, const float* rope_cs, int rope_dims, uint16_t* out, float* lse, void* ws,
+                                     size_t ws_bytes, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
+    if (rope_dims < 1) return STI_ERR_INVALID_ARG;
+    float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sti::kWsStatusBytes);
+    return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
+                     seqlen, h, d, k, out, lse, status_word(ws), acc, ws_bytes - sti::kWsStatusBytes,
+                     static_cast<cudaStream_t>(stream), false, 0, nullptr, rope_cs, rope_dims);
+}
+
 // fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048] |
 //                          attention accumulator fp32 [b, h, d] (batches of at most 256)]
 static size_t decode_scores_bytes(const sti_decode_args* a) {
@@ -405,10 +422,16 @@ size_t sti_decode_workspace_size(const sti_decode_args* a) {
     return sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a) + decode_acc_bytes(a);
 }
 
+// The optional output rotation's arguments (checked before any step is enqueued).
+static bool decode_rope_ok(const sti_decode_args* a) {
+    return a->rope_dims == 0 || (a->rope_dims > 0 && a->rope_dims % 2 == 0 && a->rope_dims <= a->d && a->rope_cs);
+}
+
 sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream,
                             void* const* events) {
     if (!a) return STI_ERR_INVALID_ARG;
     if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
+    if (!decode_rope_ok(a)) return STI_ERR_INVALID_ARG;
     if (a->b == 0) return STI_OK;
     if (!ws_ok(ws, ws_bytes, sti_decode_workspace_size(a))) return STI_ERR_INVALID_ARG;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
@@ -452,7 +475,8 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
         return cuda_fail(e, "sti_decode_fused: cudaStreamWaitEvent");
     s = attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                   a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status, acc,
-                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos);
+                  decode_acc_bytes(a), st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos,
+                  a->rope_cs, a->rope_dims);
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
@@ -500,6 +524,7 @@ static sti_status noalloc_scratch(uint8_t** out) {
 sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream) {
     if (!a) return STI_ERR_INVALID_ARG;
     if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
+    if (!decode_rope_ok(a)) return STI_ERR_INVALID_ARG;
     if (a->b == 0) return STI_OK;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
     if (a->b > STI_NOALLOC_MAX_BATCH || (int64_t)a->b * (a->n_cols > 0 ? a->n_cols : 1) > STI_NOALLOC_MAX_SCORES)
@@ -532,7 +557,8 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
         return cuda_fail(e, "sti_decode_fused_noalloc: cudaStreamWaitEvent");
     return attn_impl(a->q, a->window_kv, a->window_bstride, a->comp_kv, a->comp_bstride, W, a->n_cols, a->attn_sink,
                      a->topk_idxs, k_total, a->softmax_scale, a->b, 1, a->h, a->d, k_total, a->out, nullptr, status,
-                     acc, acc_used, st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos);
+                     acc, acc_used, st, /*pdl=*/a->n_cols > 0 && !a->q_ready, /*win_ring=*/W, a->start_pos,
+                     a->rope_cs, a->rope_dims);
 }
 
 sti_status sti_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, sti_stream stream) {

@@ -34,6 +34,7 @@
 
 #include "sti_internal.h"
 #include "sti_ptx.cuh"
+#include "sti_attn_util.cuh"
 
 namespace sti {
 namespace {
@@ -443,13 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = 0u;
                 }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * tl->alpha[32 * half + i];
+                if (p.rope_dims > 0 && 128 * m + 128 > p.d - p.rope_dims)   // the output's inverse rotation
+                    rope_inverse_pairs<32>(v, dd, p.d, p.rope_dims, p.rope_cs + (size_t)query * p.rope_dims);
                 if (dd < p.d) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int hh = 32 * half + i;
-                        if (hh < p.h)
-                            stage[(size_t)hh * p.d + dd] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[hh]));
+                        if (hh < p.h) stage[(size_t)hh * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
                     }
                 }
             }
@@ -537,6 +541,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (e < p.h * q4) {
                     const int hh = e / q4, c4 = e - (e / q4) * q4;
                     v[u] = __ldcg(reinterpret_cast<const float4*>(arow + (size_t)hh * p.d) + c4);
+                }
+            }
+            if (p.rope_dims > 0) {   // the output's inverse rotation: pairs (x, y), (z, w) of each float4
+                const float* cs = p.rope_cs + (size_t)query * p.rope_dims;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = e0 + u * kThreads + tid;
+                    if (e < p.h * q4) {
+                        const int c4 = e - (e / q4) * q4;
+                        const int dd = rank * dper + 4 * c4;
+                        float* f = reinterpret_cast<float*>(&v[u]);
+#pragma unroll
+                        for (int pr = 0; pr < 2; ++pr) {
+                            const int dp = dd + 2 * pr;
+                            if (dp >= p.d - p.rope_dims) {
+                                const int i = (dp - (p.d - p.rope_dims)) >> 1;
+                                const float c = __ldg(cs + 2 * i), sn = __ldg(cs + 2 * i + 1);
+                                const float x = f[2 * pr], y = f[2 * pr + 1];
+                                f[2 * pr] = x * c + y * sn;
+                                f[2 * pr + 1] = y * c - x * sn;
+                            }
+                        }
+                    }
                 }
             }
 #pragma unroll

@@ -529,10 +529,14 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 uint32_t r[NH];
                 o_part(m, r);
                 const int dd = 128 * m + row;
+                float v[NH];
+#pragma unroll
+                for (int i = 0; i < NH; ++i) v[i] = __uint_as_float(r[i]) * tl->alpha[ehoff + i];
+                if (p.rope_dims > 0 && 128 * m + 128 > p.d - p.rope_dims)   // the output's inverse rotation
+                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, p.rope_cs + (size_t)query * p.rope_dims);
 #pragma unroll
                 for (int i = 0; i < NH; ++i)
-                    stage[(size_t)(ehoff + i) * p.d + dd] = __bfloat16_as_ushort(
-                        __float2bfloat16_rn(__uint_as_float(r[i]) * tl->alpha[ehoff + i]));
+                    stage[(size_t)(ehoff + i) * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
             }
         fence_proxy_async_smem();
         __syncthreads();
@@ -602,6 +606,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 const int dl = (m - mb_own) * 128 + row;
                 const float4* rv = reinterpret_cast<const float4*>(recv + (size_t)dl * HC);
                 uint16_t* orow = p.out + ((size_t)query * p.h + (size_t)hg * HC) * p.d + (size_t)rg * half + dl;
+                float v[NH];
 #pragma unroll
                 for (int c = 0; c < NH / 4; ++c) {
                     const int cc = ehoff / 4 + c;
@@ -610,10 +615,15 @@ __global__ void __launch_bounds__(kHsThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = 4 * cc + e;
-                        orow[(size_t)i * p.d] = __bfloat16_as_ushort(__float2bfloat16_rn(
-                            __uint_as_float(r[4 * c + e]) * tl->alpha[i] + pv[e] * tl->red_max[0][i]));
+                        v[4 * c + e] = __uint_as_float(r[4 * c + e]) * tl->alpha[i] + pv[e] * tl->red_max[0][i];
                     }
                 }
+                const int dd = rg * half + dl;
+                if (p.rope_dims > 0 && rg * half + (m - mb_own) * 128 + 128 > p.d - p.rope_dims)
+                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, p.rope_cs + (size_t)query * p.rope_dims);
+#pragma unroll
+                for (int j = 0; j < NH; ++j)
+                    orow[(size_t)(ehoff + j) * p.d] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
             }
         if (tid == 64) STI_ESTAMP(4);
         if (sm_warp && st == 0) STI_HSTAMP(13);

@@ -58,4 +58,25 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]
     if constexpr (N == 16) tmem_st16(taddr, r);
     else tmem_st32(taddr, r);
 }
+// The output's inverse rotary rotation on values held as O^T rows: this lane holds dimension dd
+// of N heads' outputs and lane^1 holds dimension dd^1 of the same heads.  Dims [d - rd, d) form
+// rd/2 interleaved pairs (x, y) rotated back by their angle: x' = x c + y s, y' = y c - x s, with
+// (c, s) = cs[2i], cs[2i+1] for pair i.  Every lane of the warp must call it (shuffles).
+template <int N>
+__device__ __forceinline__ void rope_inverse_pairs(float (&v)[N], int dd, int d, int rd, const float* cs) {
+    const bool in = dd < d && dd >= d - rd;
+    float c = 1.f, s = 0.f;
+    if (in) {
+        const int i = (dd - (d - rd)) >> 1;
+        c = __ldg(cs + 2 * i);
+        s = __ldg(cs + 2 * i + 1);
+    }
+    const bool odd = (dd & 1) != 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const float pv = __shfl_xor_sync(kWarpFull, v[j], 1);
+        if (in) v[j] = odd ? v[j] * c - pv * s : v[j] * c + pv * s;
+    }
+}
+
 }  // namespace sti

@@ -83,6 +83,10 @@ struct AttnParams {
     const int32_t* start_pos;  // [B], with win_ring
     int hs_rows;             // head-split kernel: row groups of a query's slots (1 or 2); the cluster
                              // is (cluster / hs_rows) head groups x hs_rows row groups
+    // optional inverse rotary rotation of the output's last rope_dims dims: rope_cs[query] holds
+    // (cos, sin) of each of the rope_dims/2 interleaved pairs; rope_dims == 0: none
+    const float* rope_cs;
+    int rope_dims;
 };
 // CTAs per query for n_queries queries of k slots and head dim d (1 = no cluster); cached per device.
 int attn_pick_cluster(int n_queries, int k, int d);

@@ -83,6 +83,25 @@ def test_host_argument_checks(libsti):
     assert libsti.sti_window_idxs(None, 0, 1, 128, None, 128, None, None, None) == 0
 
 
+def test_output_rotation_argument_checks(libsti):
+    """rope_dims must be even, in [1, d] (attention entry point; 0 allowed in the decode
+    arguments), and come with a table; all of it is checked on the host."""
+    fake = 1 << 20
+    P = ctypes.c_void_p
+    head = (P(fake), P(fake), 100 * 512, None, 0, 100, 0, P(fake), P(fake), 640, 0.1, 1, 1, 64, 512, 640)
+    tail = (P(fake), None, P(fake), 1 << 30, None)
+    for cs, rd in ((P(fake), 0), (P(fake), 63), (P(fake), 514), (P(fake), -2), (None, 64)):
+        assert libsti.sti_sparse_attn_sink_rope(*head, cs, rd, *tail) == 1, (cs, rd)
+    import sparse_top_attention_indexer_gb300 as m
+
+    a = m.DecodeArgs()
+    a.b, a.window_size, a.index_topk, a.n_cols, a.d = 1, 128, 512, 1024, 512
+    for cs, rd in ((P(fake), 63), (P(fake), 514), (None, 64)):
+        a.rope_cs, a.rope_dims = cs, rd
+        assert libsti.sti_decode_fused(ctypes.byref(a), P(fake), 1 << 30, None, None) == 1, (cs, rd)
+        assert libsti.sti_decode_fused_noalloc(ctypes.byref(a), None) == 1, (cs, rd)
+
+
 def test_selftest_argument_checks(libsti):
     fake = 1 << 20
     P = ctypes.c_void_p

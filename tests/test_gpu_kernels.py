@@ -244,6 +244,77 @@ def test_sparse_attn_split_queries(sti, orc, b, k, h):
     assert diff.max() <= 2e-2
 
 
+def _rope_table(rng, lead, rd):
+    theta = rng.uniform(-np.pi, np.pi, size=(*lead, rd // 2))
+    return np.stack([np.cos(theta), np.sin(theta)], axis=-1).astype(np.float32)
+
+
+@pytest.mark.parametrize("b,s,h,d,k,rd,label", [
+    (2, 1, 64, 512, 640, 64, "head split, two row groups (merge epilogue)"),
+    (40, 1, 64, 512, 640, 64, "head split, one row group"),
+    (1, 300, 64, 512, 200, 64, "one CTA per query"),
+    (3, 1, 48, 512, 640, 64, "slots split over a cluster (fp32 accumulator)"),
+    (1, 40, 4, 64, 32, 16, "d = 64 (padded d block)"),
+    (2, 1, 64, 512, 640, 512, "every dim rotated"),
+])
+def test_sparse_attn_output_rotation(sti, orc, b, s, h, d, k, rd, label):
+    """The output's inverse rotary rotation fused into every attention epilogue equals the
+    oracle's attention followed by its rotation."""
+    import torch
+
+    rng = rng_for(780 + h + d, k + rd)
+    n1, n2 = 128, 900
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = index_lists(rng, b, s, k, n1 + n2, masked_frac=0.1, empty_rows=1)
+    cs = _rope_table(rng, (b, s), rd)
+    ref, ref_lse = orc.sparse_attn(q, kv1, sink, idx, d ** -0.5, kv2=kv2, rope_cs=cs)
+    lse = torch.empty(b, s, h, dtype=torch.float32, device="cuda")
+    ws = sti.workspace(sti.sparse_attn_workspace_size(b, s, h, d, k))
+    out = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5,
+                               kv2=to_dev(kv2), lse=lse, ws=ws, rope_cs=to_dev_any(cs))
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    check_attn(bf16_out_to_f64(out), ref)
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse.cpu().numpy().astype(np.float64)[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+    # the dims before the rotated ones are those of the plain call (bit for bit, except where the
+    # cluster's partial sums meet in L2 atomics, whose order varies between runs)
+    plain = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5,
+                                 kv2=to_dev(kv2), ws=ws)
+    if label.startswith("slots split"):
+        assert float((out[..., :d - rd].float() - plain[..., :d - rd].float()).abs().max()) <= 2e-2
+    else:
+        assert torch.equal(out[..., :d - rd], plain[..., :d - rd])
+
+
+def test_decode_fused_output_rotation(sti, orc):
+    import torch
+
+    shp = workloads.custom("decode_rope", b=3, s=1, start_pos=[4095, 700, 9000], seed=78, n_cols=2400, topk=512,
+                           h=64, d=512)
+    data = workloads.make(shp)
+    sp = data["start_pos"]
+    W = shp.window
+    ref_scores = orc.index_score(data["iq"], data["ik"], data["w"], shp.index_scale, sp, shp.n_cols, shp.ratio)
+    ref_idx = np.concatenate([np.concatenate([orc.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0),
+                              orc.topk(ref_scores, sp, shp.ratio, shp.topk, W)], axis=-1)
+    cs = _rope_table(rng_for(79, 0), (shp.b,), shp.rd)
+    ref_out, _ = orc.sparse_attn(data["q"][0], data["win"][0], data["sink"][0], ref_idx, shp.softmax_scale,
+                                 kv2=data["comp"], rope_cs=cs[:, None])
+    a, out, tk = sti.decode_args(to_dev(data["q"][0]), to_dev(data["win"][0]), to_dev(data["comp"]),
+                                 to_dev_any(data["sink"][0]), shp.softmax_scale, to_dev(data["iq"]),
+                                 to_dev(data["ik"]), to_dev(data["w"]), shp.index_scale, to_dev_any(sp), shp.ratio,
+                                 shp.n_cols, shp.topk, rope_cs=to_dev_any(cs))
+    ws = sti.workspace(sti.decode_workspace_size(a))
+    sti.decode_fused(a, ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
+
+
 def test_sparse_attn_flags_out_of_range(sti, orc):
     rng = rng_for(710, 0)
     b, s, h, d, k, n1 = 1, 2, 8, 64, 20, 30
