@@ -91,7 +91,7 @@ def recorded_traffic(kernel: str, workload: str):
 class GpuPath:
     """Device-resident inputs of one workload and the step that runs the path on them."""
 
-    def __init__(self, shape: workloads.Shape, data: dict, device):
+    def __init__(self, shape: workloads.Shape, data: dict, device, output_rope: bool = False):
         import torch
 
         import sparse_top_attention_indexer_gb300 as sti
@@ -120,6 +120,8 @@ class GpuPath:
         self.ws = sti.workspace(max(ws_attn, 256), device)
         self.splits = ws_attn > 256
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        # optional: the output's inverse rotary rotation, fused into the attention epilogue
+        self.rope_cs = to_dev_any(workloads.output_rope_table(shape), device) if output_rope else None
         if self.prefill:
             self.names = ["window_idx", "idx_scores", "idx_topk"] + [f"sparse_attn[{i}]" for i in range(self.L)]
         else:
@@ -131,7 +133,8 @@ class GpuPath:
                                               self.iq, self.ik, self.w, shape.index_scale, self.sp, shape.ratio,
                                               shape.n_cols, shape.topk,
                                               out=self.out[0].view(self.b, shape.h, shape.d),
-                                              topk_idxs=self.idx.view(self.b, self.k_total))
+                                              topk_idxs=self.idx.view(self.b, self.k_total),
+                                              rope_cs=None if self.rope_cs is None else self.rope_cs[:, 0])
             self.dws = sti.workspace(sti.decode_workspace_size(self.args), device)
 
     def capture(self):
@@ -186,7 +189,7 @@ class GpuPath:
             sti.decode_fused(self.args, self.dws, events=None if events is None else events[:4])
             for i in range(1, self.L):
                 sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale,
-                                     kv2=self.comp, out=self.out[i], ws=self.ws)
+                                     kv2=self.comp, out=self.out[i], ws=self.ws, rope_cs=self.rope_cs)
                 rec(3 + i)
             return
         rec(0)
@@ -201,7 +204,7 @@ class GpuPath:
         rec(3)
         for i in range(self.L):
             sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale, kv2=self.comp,
-                                 out=self.out[i], ws=self.ws)
+                                 out=self.out[i], ws=self.ws, rope_cs=self.rope_cs)
             rec(4 + i)
 
     l2_mode = "flush"
@@ -324,7 +327,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = None):
+def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = None, output_rope: bool = False):
     """The path on the CPU oracle (test infrastructure), for a subset of query rows of batch
     element 0 in prefill (rows given) or for the whole decode batch."""
     import oracle
@@ -341,21 +344,23 @@ def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = No
         widx = oracle.window_topk_idxs(W, 1, shape.s, 0)[0][t][:, None]
         idx = np.concatenate([widx, cidx], axis=-1).reshape(1, len(t), -1)
         q = data["q"][0][0][t][None]
+        cs = workloads.output_rope_table(shape)[:, t] if output_rope else None
         out, _ = oracle.sparse_attn(q, data["win"][0], data["sink"][0], idx, shape.softmax_scale,
-                                    kv2=data["comp"])
+                                    kv2=data["comp"], rope_cs=cs)
         return len(t)
     sp = data["start_pos"]
     score = oracle.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
     cidx = oracle.topk(score, sp, shape.ratio, shape.topk, W)
     widx = np.concatenate([oracle.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0)
     idx = np.concatenate([widx, cidx], axis=-1)
+    cs = workloads.output_rope_table(shape) if output_rope else None
     for i in range(shape.n_layers):
         oracle.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], idx, shape.softmax_scale,
-                           kv2=data["comp"])
+                           kv2=data["comp"], rope_cs=cs)
     return shape.b * shape.s
 
 
-def cpu_baseline(shape: workloads.Shape, data: dict, budget_s: float = 12.0) -> dict:
+def cpu_baseline(shape: workloads.Shape, data: dict, budget_s: float = 12.0, output_rope: bool = False) -> dict:
     """Oracle throughput on a bounded sample: decode runs whole batches, prefill a spread of
     query rows; repeated until about budget_s of CPU time."""
     import oracle
@@ -370,7 +375,7 @@ def cpu_baseline(shape: workloads.Shape, data: dict, budget_s: float = 12.0) -> 
     done, t0 = 0, time.perf_counter()
     reps = 0
     while True:
-        done += oracle_step(shape, data, rows)
+        done += oracle_step(shape, data, rows, output_rope)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= 50:
@@ -390,10 +395,10 @@ def reference_arm(args, shape: workloads.Shape, cfg: dict) -> dict:
     sample = (f"16 query rows spread over the {shape.s}-query prefill per step" if shape.prefill else
               f"the whole b={shape.b} decode batch (all {shape.n_layers} attention layer(s)) per step")
     for _ in range(args.warmup):
-        oracle_step(shape, data, rows)
+        oracle_step(shape, data, rows, args.output_rope)
     done, t0 = 0, time.perf_counter()
     for _ in range(args.steps):
-        done += oracle_step(shape, data, rows)
+        done += oracle_step(shape, data, rows, args.output_rope)
     el = time.perf_counter() - t0
     value = round(done / el, 3)
     unit = "queries/s" if shape.prefill else "tokens/s"
@@ -433,6 +438,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="skip nvidia-smi sampling (profiler runs)")
+    ap.add_argument("--output-rope", action="store_true",
+                    help="fuse the output's inverse rotary rotation (last rd dims) into the attention")
     ap.add_argument("--l2", default="flush", choices=["flush", "none"],
                     help="flush: write then read 256 MiB before every step; none: no flush (every step of "
                          "the decode workloads touches more bytes than L2 holds)")
@@ -453,6 +460,8 @@ def main():
            "l2": ("256 MiB written then read before every step (outside the timed region)" if args.l2 == "flush" else
                   "no flush: inputs larger than L2 (each decode step streams the index keys, "
                   f"{shape.b * shape.n_cols * shape.Di * 2 / 1e6:.0f} MB, through the 129 MB L2)")}
+    if args.output_rope:
+        cfg["output_inverse_rope_dims"] = shape.rd
 
     if args.impl == "reference":
         if rank != 0:   # the CPU oracle runs once, on rank 0
@@ -477,7 +486,7 @@ def main():
 
     __graft_entry__.build()
     data = workloads.make(shape)
-    path = GpuPath(shape, data, device)
+    path = GpuPath(shape, data, device, output_rope=args.output_rope)
     path.l2_mode = args.l2
     stream = torch.cuda.current_stream()
 
@@ -573,7 +582,7 @@ def main():
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(shape, data)
+        line["cpu_baseline"] = cpu_baseline(shape, data, output_rope=args.output_rope)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -597,11 +606,15 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     d_w = torch.empty_like(path.w).reshape(path.b, -1)
     d_sp = torch.empty_like(path.sp)
     shp = path.shape
+    # the output rotation's table is a per-step input too (its angles follow the positions)
+    h_cs = None if path.rope_cs is None else path.rope_cs[:, 0].cpu().pin_memory()
+    d_cs = None if h_cs is None else torch.empty_like(path.rope_cs[:, 0])
     a, out, tk = sti.decode_args(d_q.view_as(path.q[0]), path.win[0], path.comp, path.sink[0], shp.softmax_scale,
                                  d_iq.view_as(path.iq), path.ik, d_w.view_as(path.w), shp.index_scale, d_sp,
-                                 shp.ratio, shp.n_cols, shp.topk)
+                                 shp.ratio, shp.n_cols, shp.topk, rope_cs=d_cs)
     ws = sti.workspace(sti.decode_workspace_size(a), path.dev)
     bi = h_q.numel() * 2 + h_iq.numel() * 2 + h_w.numel() * 2 + h_sp.numel() * 4
+    bi += 0 if h_cs is None else h_cs.numel() * 4
     bo = h_out.numel() * 2
     main = torch.cuda.current_stream()
 
@@ -610,6 +623,8 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
         d_iq.copy_(h_iq, non_blocking=True)
         d_w.copy_(h_w, non_blocking=True)
         d_sp.copy_(h_sp, non_blocking=True)
+        if d_cs is not None:
+            d_cs.copy_(h_cs, non_blocking=True)
         d_q.copy_(h_q, non_blocking=True)
         sti.decode_fused(a, ws)
         h_out.copy_(out.reshape(-1), non_blocking=True)

@@ -169,7 +169,8 @@ sti_status sti_sparse_attn_sink(const uint16_t *q, const uint16_t *kv, int64_t k
  * interleaved pair's angle at the query's position -- the caller evaluates the frequencies, which
  * the pages do not print.  Pair i = dims (d - rope_dims + 2i, +1) as x + iy is multiplied by
  * cos - i sin: x' = x cos + y sin, y' = y cos - x sin, in fp32 before the bf16 rounding.
- * rope_dims: even, 1 <= rope_dims <= d (STI_ERR_INVALID_ARG otherwise, or when rope_cs is NULL).
+ * rope_dims: even, 1 <= rope_dims <= d; rope_cs 16-byte aligned (STI_ERR_INVALID_ARG otherwise, or
+ * when rope_cs is NULL).
  * lse is that of the attention (the rotation leaves it unchanged).  Everything else as
  * sti_sparse_attn_sink. */
 sti_status sti_sparse_attn_sink_rope(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride, const uint16_t *kv2,
@@ -224,7 +225,7 @@ typedef struct sti_decode_args {
      * flag), fused into the attention's epilogue.  rope_cs: fp32 [b, rope_dims/2, 2], the
      * (cos, sin) of each interleaved pair's angle at the query's position (the caller evaluates
      * its frequencies); pair i = dims (d - rope_dims + 2i, d - rope_dims + 2i + 1) as x + iy is
-     * multiplied by cos - i sin.  rope_dims: 0 (none) or even, <= d. */
+     * multiplied by cos - i sin.  rope_dims: 0 (none) or even, <= d; rope_cs 16-byte aligned. */
     const float *rope_cs;
     int rope_dims;
 } sti_decode_args;

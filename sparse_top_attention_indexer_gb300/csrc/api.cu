@@ -214,7 +214,7 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
                             cudaStream_t st, bool pdl = false, int win_ring = 0,
                             const int32_t* start_pos = nullptr, const float* rope_cs = nullptr, int rope_dims = 0) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
-    if (rope_dims < 0 || rope_dims % 2 != 0 || rope_dims > d || (rope_dims > 0 && !rope_cs))
+    if (rope_dims < 0 || rope_dims % 2 != 0 || rope_dims > d || (rope_dims > 0 && (!rope_cs || !aligned(rope_cs, 16))))
         return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
@@ -424,7 +424,8 @@ size_t sti_decode_workspace_size(const sti_decode_args* a) {
 
 // The optional output rotation's arguments (checked before any step is enqueued).
 static bool decode_rope_ok(const sti_decode_args* a) {
-    return a->rope_dims == 0 || (a->rope_dims > 0 && a->rope_dims % 2 == 0 && a->rope_dims <= a->d && a->rope_cs);
+    return a->rope_dims == 0 || (a->rope_dims > 0 && a->rope_dims % 2 == 0 && a->rope_dims <= a->d && a->rope_cs &&
+                                 aligned(a->rope_cs, 16));
 }
 
 sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream,

@@ -28,6 +28,7 @@
 // the ring starting zeroed, and get probability 0); masked slots inside a group repeat one of
 // the group's valid rows; a group with rows of both sources fetches row by row.
 #include <cuda_bf16.h>
+#include <cstddef>
 #include <math.h>
 
 #include <mutex>
@@ -73,7 +74,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-struct __align__(8) HsTail {
+struct __align__(16) HsTail {
     uint64_t full[kHsMaxSlots];    // slot filled (1 local arrival + the tile's bytes)
     uint64_t empty[kHsMaxSlots];   // slot read by every CTA of the cluster (C arrivals)
     uint64_t s_full[2];            // S^T of a tile in TMEM (double buffer)
@@ -82,6 +83,7 @@ struct __align__(8) HsTail {
     uint64_t q_bar;                // Q rows of this CTA's heads landed
     uint64_t recv_bar;             // row-split merge: the partner's partial and (m, l) landed
     uint64_t ready_bar;            // row-split merge: the partner's ring is free to receive
+    uint64_t rope_bar;             // the output-rotation table landed in rope_cs
     float peer_ml[64][2];          // row-split merge: the partner's (m, l) per head
     uint32_t tmem_base;
     int abort;                     // a wait of this CTA timed out: the others stop waiting
@@ -90,7 +92,10 @@ struct __align__(8) HsTail {
     float alpha[64];               // rescale factor of this tile / final 1 / denominator
     float red_max[4][64];          // per-warp partial maxima
     float red_sum[4][64];          // per-warp partial sums
+    alignas(16) float rope_cs[128];   // the query's output-rotation table (rope_dims <= 128): a bulk
+                                      // copy's destination, 16-byte aligned
 };
+static_assert(offsetof(HsTail, rope_cs) % 16 == 0, "bulk-copy destination must be 16-byte aligned");
 
 // S^T double buffer (2 x hc columns) and O^T (d/128 blocks of hc columns, d <= 512)
 __host__ __device__ constexpr uint32_t hs_tmem_cols(int hc) { return hc == 16 ? 128u : (hc == 32 ? 256u : 512u); }
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         mbar_init(&tl->q_bar, 1);
         mbar_init(&tl->recv_bar, 1);
         mbar_init(&tl->ready_bar, 1);
+        mbar_init(&tl->rope_bar, 1);
         // row-split merge: the partner's half of d for this CTA's heads, [d/2][HC] fp32, and (m, l)
         if (CR == 2) mbar_arrive_expect_tx(&tl->recv_bar, (uint32_t)(p.d / 2 * HC * 4 + HC * 8));
         tl->abort = 0;
@@ -169,6 +175,11 @@ __global__ void __launch_bounds__(kHsThreads, 1)
         tl->m_run[tid] = -INFINITY;
         tl->l_run[tid] = 0.f;
     }
+    // the output rotation's table is an input of the call (no earlier kernel writes it): one bulk
+    // copy into shared memory now, waited for in the epilogue, keeps its latency off the path
+    // (a row of 16-byte multiple, at most 128 values; otherwise the epilogue reads global memory)
+    const bool rope_smem = p.rope_dims > 0 && p.rope_dims <= 128 && p.rope_dims % 4 == 0;
+    const float* rope_tab = rope_smem ? tl->rope_cs : p.rope_cs + (size_t)query * p.rope_dims;
     {   // rows that no gather writes keep finite contents
         uint4* r4 = reinterpret_cast<uint4*>(ring);
         const int n16 = S * (int)kSlotBytes / 16;
@@ -180,6 +191,10 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tl->tmem_base;
     if (tid == 0) STI_HSTAMP(1);
+    if (rope_smem && tid == 0) {
+        mbar_arrive_expect_tx(&tl->rope_bar, (uint32_t)p.rope_dims * 4u);
+        bulk_load(tl->rope_cs, p.rope_cs + (size_t)query * p.rope_dims, (uint32_t)p.rope_dims * 4u, &tl->rope_bar);
+    }
 
     if (warp == 0 || (warp >= 6 && warp <= 8)) {
         // ------------------------------------------------------------ producers
@@ -492,6 +507,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
     tc_fence_before();
     __syncthreads();   // every MMA of this CTA has completed; m_run, l_run final
     tc_fence_after();
+    if (rope_smem) attn_wait(&tl->rope_bar, 0, p.status, abort);
     const bool sm_warp = warp >= 2 && warp <= 5;
     const int st = tid - 64;                                  // softmax threads: 0..127
     const int row = 32 * (warp & 3) + lane;                   // their TMEM lane (d within a block)
@@ -533,7 +549,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
 #pragma unroll
                 for (int i = 0; i < NH; ++i) v[i] = __uint_as_float(r[i]) * tl->alpha[ehoff + i];
                 if (p.rope_dims > 0 && 128 * m + 128 > p.d - p.rope_dims)   // the output's inverse rotation
-                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, p.rope_cs + (size_t)query * p.rope_dims);
+                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, rope_tab);
 #pragma unroll
                 for (int i = 0; i < NH; ++i)
                     stage[(size_t)(ehoff + i) * p.d + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
@@ -620,7 +636,7 @@ __global__ void __launch_bounds__(kHsThreads, 1)
                 }
                 const int dd = rg * half + dl;
                 if (p.rope_dims > 0 && rg * half + (m - mb_own) * 128 + 128 > p.d - p.rope_dims)
-                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, p.rope_cs + (size_t)query * p.rope_dims);
+                    rope_inverse_pairs<NH>(v, dd, p.d, p.rope_dims, rope_tab);
 #pragma unroll
                 for (int j = 0; j < NH; ++j)
                     orow[(size_t)(ehoff + j) * p.d] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));

@@ -68,8 +68,8 @@ __device__ __forceinline__ void rope_inverse_pairs(float (&v)[N], int dd, int d,
     float c = 1.f, s = 0.f;
     if (in) {
         const int i = (dd - (d - rd)) >> 1;
-        c = __ldg(cs + 2 * i);
-        s = __ldg(cs + 2 * i + 1);
+        c = cs[2 * i];       // (shared or global memory)
+        s = cs[2 * i + 1];
     }
     const bool odd = (dd & 1) != 0;
 #pragma unroll

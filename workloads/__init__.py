@@ -180,6 +180,17 @@ def planted_bias() -> float:
 # ------------------------------------------------------------------ generator
 
 
+def output_rope_table(shape: Shape, theta: float = 10000.0) -> np.ndarray:
+    """(cos, sin) of the angles the output's inverse rotary rotation undoes, per query and pair:
+    float32 [b, s, rd/2, 2] at positions start_pos + t, angle pos * theta^(-2i/rd) (the model's
+    own frequencies come from a table these pages do not print; any table is an input here)."""
+    theta = shape.rope_theta or theta
+    i = np.arange(shape.rd // 2, dtype=np.float64)
+    pos = shape.start_pos.astype(np.float64)[:, None] + np.arange(shape.s, dtype=np.float64)[None, :]
+    ang = pos[..., None] * theta ** (-2.0 * i / shape.rd)
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
+
+
 def make(shape: Shape, beta: float | None = None) -> dict:
     """Draw every input tensor of `shape`.
 
