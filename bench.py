@@ -57,7 +57,7 @@ def peaks():
 
 
 KERNEL_SOURCES = {"idx_scores": ["idx_scores.cu"], "idx_topk": ["idx_topk.cu"],
-                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu"], "window_idx": ["idx_topk.cu"]}
+                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu", "sti_attn_util.cuh"], "window_idx": ["idx_topk.cu"]}
 
 
 def kernel_source_hash(kernel: str) -> str:

@@ -158,7 +158,8 @@ def _rope_interleaved(x: np.ndarray, positions: np.ndarray, rd: int, theta: floa
     """Rotate the last rd dims of x (pairs (2i, 2i+1)) by angle pos * theta^(-2i/rd).
 
     x: float64 [..., n, dim] with positions [n] along axis -2.  Input preparation for
-    workload 1, whose recipe puts RoPE on the last rd dims; the path itself applies none."""
+    workload 1, whose recipe puts RoPE on the last rd dims; the path applies only the output's
+    inverse rotation, from a table its caller passes (output_rope_table)."""
     y = x.copy()
     i = np.arange(rd // 2, dtype=np.float64)
     inv = theta ** (-2.0 * i / rd)
