@@ -15,6 +15,8 @@ Every function is pinned by the CPU tests in ``tests/test_oracle_*.py``:
   sparse_attn        textbook softmax (sink -> -inf), single-row closed form, empty rows,
                      duplicate-row sink shift, permutation invariance, mass + sink = 1
   dense_attn         independent of index lists; equal to sparse_attn when k >= visible
+  window_topk_idxs_chunked   the prefill band of the pages when the chunk starts at 0 (rows
+                     shifted past the ring), brute-force positions of every referenced row
   output_inverse_rope   identity at angle 0, the quarter-turn closed form, complex
                      multiplication by e^{-i theta}, and undoing the generator's rotation
 """
@@ -89,6 +91,29 @@ def window_topk_idxs(window_size: int, bsz: int, seqlen: int, start_pos: int) ->
     out = np.empty((bsz, rows, width), dtype=np.int32)
     got = lib.oracle_window_topk_idxs(window_size, bsz, seqlen, start_pos, _ptr(out))
     assert got == width
+    return out
+
+
+def window_topk_idxs_chunked(window_size: int, seqlen: int, start_pos: int) -> np.ndarray:
+    """Window rows of a prefill chunk that continues a sequence (start_pos > 0): [seqlen, W].
+
+    The pages cover prefill from position 0 (get_window_topk_idxs' band) and decode (the
+    W-slot ring); a chunk starting later is not on them.  Reading: the chunk's window source is
+    the ring as it stood before the chunk (rows [0, W): slot i holds the newest position
+    p < start_pos with p % W == i) followed by the chunk's own raw rows (row W + i holds
+    position start_pos + i).  Query t at position P = start_pos + t sees, as the prefill band
+    does with t, the positions max(0, P - W + 1) + i for i < W, -1 past P; position p maps to
+    row W + (p - start_pos) when p >= start_pos, else to ring slot p % W."""
+    W = int(window_size)
+    out = np.full((seqlen, W), -1, dtype=np.int32)
+    for t in range(seqlen):
+        P = start_pos + t
+        first = max(0, P - W + 1)
+        for i in range(W):
+            p = first + i
+            if p > P:
+                continue
+            out[t, i] = W + (p - start_pos) if p >= start_pos else p % W
     return out
 
 

@@ -425,3 +425,31 @@ def test_inverse_rope_undoes_the_generators_rotation(orc):
     cs = np.stack([np.cos(ang), np.sin(ang)], axis=-1)[None, :, None]          # [1, s, 1, rd/2, 2]
     back = orc.output_inverse_rope(rot[None, :, None].copy(), cs[:, :, 0])
     np.testing.assert_allclose(back[0, :, 0], x, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ window rows of a later prefill chunk
+
+
+def test_chunked_window_from_position_zero_is_the_prefill_band(orc):
+    """A chunk starting at 0 (an empty ring) lists the pages' prefill band, every row shifted
+    past the W ring rows (golden rows of get_window_topk_idxs, W=4, s=6)."""
+    W, s = 4, 6
+    band = orc.window_topk_idxs(W, 1, s, 0)[0]                         # [s, min(s, W)]
+    got = orc.window_topk_idxs_chunked(W, s, 0)
+    np.testing.assert_array_equal(got[:, :band.shape[1]], np.where(band >= 0, band + W, -1))
+    assert np.all(got[:, band.shape[1]:] == -1)
+
+
+@pytest.mark.parametrize("W,s,sp", [(4, 6, 9), (8, 3, 5), (16, 40, 1000), (4, 1, 2)])
+def test_chunked_window_rows_hold_the_last_w_positions(orc, W, s, sp):
+    """Every referenced row of the [ring ; chunk] source holds one of the query's last W
+    positions, each exactly once (brute force over what each row holds)."""
+    got = orc.window_topk_idxs_chunked(W, s, sp)
+    # what each source row holds: ring slot r -> the newest p < sp with p % W == r; chunk row
+    held = {r: max([p for p in range(sp) if p % W == r], default=None) for r in range(W)}
+    held.update({W + i: sp + i for i in range(s)})
+    for t in range(s):
+        P = sp + t
+        want = set(range(max(0, P - W + 1), P + 1))
+        rows = [int(v) for v in got[t] if v >= 0]
+        assert sorted(held[r] for r in rows) == sorted(want)
