@@ -1,6 +1,6 @@
 """Benchmark of the Indexer -> top-k -> sparse sink attention path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..7] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..8] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
 window indices, Indexer scores, top-k, sparse sink attention (every attention layer),
@@ -193,7 +193,10 @@ class GpuPath:
                 rec(3 + i)
             return
         rec(0)
-        sti.window_idxs(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
+        if shp.chunked:
+            sti.window_idxs_chunked(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
+        else:
+            sti.window_idxs(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
         rec(1)
         sti.idx_scores(self.iq, self.ik, self.w, shp.index_scale, self.sp, shp.n_cols, shp.ratio, out=self.scores,
                        ws=self.ws)
@@ -233,7 +236,7 @@ def work(shape: workloads.Shape, data: dict) -> dict:
     n_keys = np.minimum((sp + s) // shape.ratio, shape.n_cols)                       # unique keys per sequence
     sel = np.minimum(vis, shape.topk)
     if shape.prefill:
-        win_valid = np.minimum(t + 1, shape.window)[None, :].repeat(b, 0)
+        win_valid = np.minimum(sp[:, None] + t[None, :] + 1, shape.window)
     else:
         win_valid = np.minimum(sp + 1, shape.window)[:, None]
     rows = (sel + win_valid).sum()                                                  # valid gathered rows
@@ -335,13 +338,14 @@ def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = No
     W = shape.window
     if shape.prefill:
         t = rows
-        sp = t.astype(np.int32)                 # query t of a start_pos=0 chunk sees (t+1)//ratio groups
+        sp = (int(shape.start_pos[0]) + t).astype(np.int32)   # query t sees (start_pos+t+1)//ratio groups
         iq = data["iq"][0][t][:, None]
         w = data["w"][0][t][:, None]
         ik = np.broadcast_to(data["ik"][0], (len(t),) + data["ik"].shape[1:])
         score = oracle.index_score(iq, ik, w, shape.index_scale, sp, shape.n_cols, shape.ratio)
         cidx = oracle.topk(score, sp, shape.ratio, shape.topk, shape.win_rows)
-        widx = oracle.window_topk_idxs(W, 1, shape.s, 0)[0][t][:, None]
+        widx = (oracle.window_topk_idxs_chunked(W, shape.s, int(shape.start_pos[0])) if shape.chunked else
+                oracle.window_topk_idxs(W, 1, shape.s, 0)[0])[t][:, None]
         idx = np.concatenate([widx, cidx], axis=-1).reshape(1, len(t), -1)
         q = data["q"][0][0][t][None]
         cs = workloads.output_rope_table(shape)[:, t] if output_rope else None
@@ -433,7 +437,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -78,7 +78,7 @@ sti_status sti_read_device_status(void *ws, uint32_t *flags, sti_stream stream);
  *   seqlen > 1 (prefill, start_pos[b] must be 0): row t holds max(0,t-W+1)+i for
  *       i < width = min(seqlen, W); entries > t are -1.  The window KV source is then the
  *       seqlen raw KV rows of the chunk.  (start_pos != 0 raises STI_FLAG_CHUNKED when ws
- *       is given and writes -1 rows.)
+ *       is given and writes -1 rows: such chunks take sti_window_idxs_chunked.)
  *   seqlen == 1 (decode): width = W; the ring slots oldest first,
  *       (start_pos%W)+1 .. W-1, 0 .. start_pos%W; a slot > start_pos is -1.  Position p
  *       lives in ring slot p % W.  (For start_pos == 0 this lists the same single slot as
@@ -89,6 +89,20 @@ sti_status sti_read_device_status(void *ws, uint32_t *flags, sti_stream stream);
  */
 sti_status sti_window_idxs(const int32_t *start_pos, int b, int seqlen, int window_size, int32_t *idxs,
                            int64_t row_stride, int *width_out, void *ws, sti_stream stream);
+
+/*
+ * Window rows of a prefill chunk that continues its sequence (start_pos[b] > 0, any seqlen):
+ * not on the pages, which cover prefill from position 0 (the band above) and decode (the ring).
+ * The chunk's window KV source is read as [the W-slot ring as it stood before the chunk
+ * (slot i: the newest position p < start_pos with p % W == i) ; the chunk's seqlen raw rows
+ * (row W + i: position start_pos + i)], W + seqlen rows; compressed indices then take offset
+ * W + seqlen.  Query t at P = start_pos + t sees the band of the prefill formula with t -> P:
+ * positions max(0, P-W+1) + i for i < W (-1 past P), position p at row W + (p - start_pos)
+ * when p >= start_pos, else ring slot p % W.  Row width W (row_stride >= W).  Also valid for
+ * start_pos == 0 (an empty ring: the prefill band shifted by W).  ws: optional, as above.
+ */
+sti_status sti_window_idxs_chunked(const int32_t *start_pos, int b, int seqlen, int window_size, int32_t *idxs,
+                                   int64_t row_stride, void *ws, sti_stream stream);
 
 /* ------------------------------------------------------------------ index scores */
 /*

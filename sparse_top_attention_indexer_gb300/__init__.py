@@ -32,7 +32,7 @@ EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_sparse_attn_sink_rope",
            "sti_decode_workspace_size",
            "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
-           "sti_selftest_wait_timeout"]
+           "sti_selftest_wait_timeout", "sti_window_idxs_chunked"]
 
 
 class StiError(RuntimeError):
@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.sti_version.argtypes, L.sti_version.restype = [], I
         L.sti_read_device_status.argtypes, L.sti_read_device_status.restype = [P, P, P], I
         L.sti_window_idxs.argtypes, L.sti_window_idxs.restype = [P, I, I, I, P, I64, P, P, P], I
+        L.sti_window_idxs_chunked.argtypes, L.sti_window_idxs_chunked.restype = [P, I, I, I, P, I64, P, P], I
         L.sti_idx_scores_workspace_size.argtypes, L.sti_idx_scores_workspace_size.restype = [], SZ
         L.sti_idx_scores.argtypes = [P, P, I64, P, F, P, I, I, I, I, I, I, P, P, SZ, P]
         L.sti_idx_scores.restype = I
@@ -153,6 +154,22 @@ def window_idxs(start_pos: torch.Tensor, seqlen: int, window_size: int, out: tor
     row_stride = out.stride(-2) if out.dim() >= 2 else width
     _check(lib().sti_window_idxs(_ptr(start_pos), b, seqlen, window_size, _ptr(out), row_stride, None, _ptr(ws),
                                  _stream(stream)), "sti_window_idxs")
+    return out
+
+
+def window_idxs_chunked(start_pos: torch.Tensor, seqlen: int, window_size: int, out: torch.Tensor | None = None,
+                        ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Window rows [b, seqlen, W] of a prefill chunk continuing its sequence, over the source
+    [ring before the chunk (W rows) ; the chunk's seqlen rows] (sti_window_idxs_chunked)."""
+    _need(start_pos, torch.int32, "start_pos")
+    b = start_pos.numel()
+    if out is None:
+        out = torch.empty(b, seqlen, window_size, dtype=torch.int32, device=start_pos.device)
+    if out.stride(-1) != 1:
+        raise ValueError("out rows must be contiguous")
+    row_stride = out.stride(-2) if out.dim() >= 2 else window_size
+    _check(lib().sti_window_idxs_chunked(_ptr(start_pos), b, seqlen, window_size, _ptr(out), row_stride, _ptr(ws),
+                                         _stream(stream)), "sti_window_idxs_chunked")
     return out
 
 

@@ -351,6 +351,18 @@ sti_status sti_read_device_status(void* ws, uint32_t* flags, sti_stream stream) 
     return STI_OK;
 }
 
+sti_status sti_window_idxs_chunked(const int32_t* start_pos, int b, int seqlen, int window_size, int32_t* idxs,
+                                   int64_t row_stride, void* ws, sti_stream stream) {
+    if (ws && !aligned(ws, sti::kWsAlign)) return STI_ERR_INVALID_ARG;
+    if (b < 0 || seqlen < 1 || window_size < 1) return STI_ERR_INVALID_ARG;
+    if (b == 0) return STI_OK;
+    if (!start_pos || !idxs || row_stride < window_size) return STI_ERR_INVALID_ARG;
+    cudaError_t e = sti::launch_window_idxs(start_pos, b, seqlen, window_size, window_size, idxs, row_stride,
+                                            ws ? status_word(ws) : nullptr, static_cast<cudaStream_t>(stream),
+                                            /*chunked=*/true);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_window_idxs_chunked");
+}
+
 sti_status sti_window_idxs(const int32_t* start_pos, int b, int seqlen, int window_size, int32_t* idxs,
                            int64_t row_stride, int* width_out, void* ws, sti_stream stream) {
     if (ws && !aligned(ws, sti::kWsAlign)) return STI_ERR_INVALID_ARG;

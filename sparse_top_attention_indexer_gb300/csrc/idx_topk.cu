@@ -26,7 +26,7 @@ constexpr int kCandCap = 4096;       // threshold-bin members kept for passes 2 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 __global__ void window_idx_kernel(const int32_t* __restrict__ start_pos, int B, int s, int W, int width,
-                                  int32_t* __restrict__ idxs, int64_t row_stride, uint32_t* status) {
+                                  int32_t* __restrict__ idxs, int64_t row_stride, uint32_t* status, int chunked) {
     const int64_t total = (int64_t)B * s * width;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
          e += (int64_t)gridDim.x * blockDim.x) {
@@ -35,7 +35,14 @@ __global__ void window_idx_kernel(const int32_t* __restrict__ start_pos, int B, 
         const int b = (int)(row / s), t = (int)(row - (int64_t)b * s);
         const int sp = __ldg(start_pos + b);
         int v;
-        if (s > 1) {
+        if (chunked) {
+            // a chunk continuing its sequence: the prefill band at position P = sp + t over the
+            // source [ring before the chunk (W rows) ; the chunk's rows]; position p lives in
+            // chunk row W + (p - sp) or, before the chunk, in ring slot p % W
+            const int P = sp + t;
+            const int p = max(0, P - W + 1) + i;
+            v = p > P ? -1 : (p >= sp ? W + (p - sp) : p % W);
+        } else if (s > 1) {
             // prefill band: starts at max(0, t-W+1); slots past t hold nothing
             if (sp != 0) {
                 if (i == 0 && status) atomicOr(status, 4u /* STI_FLAG_CHUNKED */);
@@ -733,12 +740,13 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_kernel(const TopkP
 }  // namespace
 
 cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, int width, int32_t* idxs,
-                               int64_t row_stride, uint32_t* status, cudaStream_t stream) {
+                               int64_t row_stride, uint32_t* status, cudaStream_t stream, bool chunked) {
     const int64_t total = (int64_t)B * s * width;
     if (total == 0) return cudaSuccess;
     int blocks = (int)((total + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    window_idx_kernel<<<blocks, 256, 0, stream>>>(start_pos, B, s, W, width, idxs, row_stride, status);
+    window_idx_kernel<<<blocks, 256, 0, stream>>>(start_pos, B, s, W, width, idxs, row_stride, status,
+                                                  chunked ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,8 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p);
 
 // ------------------------------------------------------------------ window indices, top-k
 cudaError_t launch_window_idxs(const int32_t* start_pos, int B, int s, int W, int width, int32_t* idxs,
-                               int64_t row_stride, uint32_t* status, cudaStream_t stream);
+                               int64_t row_stride, uint32_t* status, cudaStream_t stream,
+                               bool chunked = false);
 struct TopkParams {
     const float* scores;      // fp32 [B, s, n_cols]
     const int32_t* start_pos;

@@ -40,6 +40,16 @@ def test_window_idxs(sti, orc, W, s, sps):
         np.testing.assert_array_equal(got[bi], want)
 
 
+@pytest.mark.parametrize("W,s,sps", [(128, 300, [6144, 1, 5000]), (16, 40, [0, 3, 17]), (4, 1, [9])])
+def test_window_idxs_chunked(sti, orc, W, s, sps):
+    import torch
+
+    sp = torch.tensor(sps, dtype=torch.int32, device="cuda")
+    got = sti.window_idxs_chunked(sp, s, W).cpu().numpy()
+    for bi, v in enumerate(sps):
+        np.testing.assert_array_equal(got[bi], orc.window_topk_idxs_chunked(W, s, int(v)))
+
+
 def test_window_idxs_flags_chunked_prefill(sti):
     ws = sti.workspace(256)
     got = sti.window_idxs(to_dev_any(np.array([0, 5], np.int32)), 4, 8, ws=ws).cpu().numpy()

@@ -3,9 +3,9 @@
 
 Decode workloads (b=32 ctx 65536 at compression ratios 4, 2 and 1; b=8 ctx 131072 with planted
 keys; b=64 ragged with three reuse layers) and the tiny prefill are compared element by element
-on every output.  The
-8192-query prefill is compared on a spread of sampled query rows (the oracle computes each
-one on its own), and on properties that hold for every row at full size."""
+on every output.  The 8192-query prefill and the 2048-query chunk continuing a sequence at
+position 6144 are compared on a spread of sampled query rows (the oracle computes each one on
+its own), and on properties that hold for every row at full size."""
 import numpy as np
 import pytest
 
@@ -69,34 +69,38 @@ def test_workload_full(gpu, orc, n):
               f"mean {mn:.2e}")
 
 
-def test_workload_prefill_sampled(gpu, orc):
-    shape = workloads.config(3)
+@pytest.mark.parametrize("n", [3, 8])
+def test_workload_prefill_sampled(gpu, orc, n):
+    """The 8192-query prefill from position 0, and the 2048-query chunk continuing at 6144."""
+    shape = workloads.config(n)
     data = workloads.make(shape)
     path = _run(shape, data, gpu)
     s, W, K, r = shape.s, shape.window, shape.topk, shape.ratio
+    sp0 = int(shape.start_pos[0])
+    off = shape.win_rows                      # compressed rows follow the window source's rows
     got_s = path.scores_view()[0].cpu().numpy()
     got_i = path.idx[0].cpu().numpy()
     # properties of every row at full size
     t = np.arange(s)
-    vis = np.minimum((t + 1) // r, shape.n_cols)
+    vis = np.minimum((sp0 + t + 1) // r, shape.n_cols)
     assert np.array_equal(np.isfinite(got_s).sum(axis=1), vis)
     n_valid = (got_i[:, W:] >= 0).sum(axis=1)
     assert np.array_equal(n_valid, np.minimum(vis, K))
     comp = got_i[:, W:]
-    assert np.all((comp < 0) | ((comp >= s) & (comp < s + vis[:, None])))
-    # sampled rows against the oracle (row t of a start_pos=0 chunk sees (t+1)//ratio groups)
-    rows = np.unique(np.concatenate([np.arange(0, 8), np.linspace(8, s - 1, 40).astype(np.int64), [2047, 2048,
-                                                                                                     2051]]))
-    sp = rows.astype(np.int32)
+    assert np.all((comp < 0) | ((comp >= off) & (comp < off + vis[:, None])))
+    # sampled rows against the oracle (row t sees (start_pos + t + 1)//ratio groups)
+    rows = np.unique(np.concatenate([np.arange(0, 8), np.linspace(8, s - 1, 40).astype(np.int64),
+                                     [t for t in (2047, 2048, 2051) if t < s]]))
+    sp = (sp0 + rows).astype(np.int32)
     iq = data["iq"][0][rows][:, None]
     w = data["w"][0][rows][:, None]
     ik = np.broadcast_to(data["ik"][0], (len(rows),) + data["ik"].shape[1:])
     ref_s = orc.index_score(iq, ik, w, shape.index_scale, sp, shape.n_cols, r)
     check_scores(got_s[rows][:, None], ref_s)
-    ref_c = orc.topk(ref_s, sp, r, K, s)
-    ref_w = orc.window_topk_idxs(W, 1, s, 0)[0][rows]
+    ref_c = orc.topk(ref_s, sp, r, K, off)
+    ref_w = (orc.window_topk_idxs_chunked(W, s, sp0) if shape.chunked else orc.window_topk_idxs(W, 1, s, 0)[0])[rows]
     np.testing.assert_array_equal(got_i[rows, :W], ref_w)
-    check_topk_rows(got_i[rows, W:][:, None], ref_c, ref_s, s, K)
+    check_topk_rows(got_i[rows, W:][:, None], ref_c, ref_s, off, K)
     idx = np.concatenate([ref_w[:, None], ref_c], axis=-1).reshape(1, len(rows), -1)
     ref_o, _ = orc.sparse_attn(data["q"][0][0][rows][None], data["win"][0], data["sink"][0], idx,
                                shape.softmax_scale, kv2=data["comp"])

@@ -87,17 +87,26 @@ class Shape:
 
     @property
     def prefill(self) -> bool:
-        return bool(np.all(self.start_pos == 0)) and self.s > 1
+        """Several queries per sequence: a prefill from position 0, or a later chunk."""
+        return self.s > 1
+
+    @property
+    def chunked(self) -> bool:
+        """A prefill chunk that continues its sequence (start_pos > 0)."""
+        return self.s > 1 and bool(np.any(self.start_pos != 0))
 
     @property
     def win_rows(self) -> int:
-        """Rows of the window KV source: the s raw rows in prefill, the W-slot ring in decode."""
+        """Rows of the window KV source: the s raw rows in prefill from 0, the ring before the
+        chunk followed by its s rows in a later chunk, the W-slot ring in decode."""
+        if self.chunked:
+            return self.window + self.s
         return self.s if self.prefill else self.window
 
     @property
     def win_width(self) -> int:
-        """Window slots per query: min(s, W) in prefill, W in decode."""
-        return min(self.s, self.window) if self.prefill else self.window
+        """Window slots per query: min(s, W) in prefill from 0, W otherwise."""
+        return min(self.s, self.window) if (self.prefill and not self.chunked) else self.window
 
     @property
     def k_total(self) -> int:
@@ -119,7 +128,8 @@ class Shape:
 
 def config(n: int) -> Shape:
     """The named workloads: 1-5 as listed in the design notes, 6 and 7 the decode workload at
-    compression ratios 2 and 1 (32768 and 65536 index rows per sequence)."""
+    compression ratios 2 and 1 (32768 and 65536 index rows per sequence), 8 a prefill chunk
+    that continues its sequence."""
     seed = 1000 + n
     if n == 1:
         return Shape("tiny_prefill_s256_h4_d64", b=1, s=256, start_pos=np.zeros(1, np.int32), h=4, d=64, rd=16,
@@ -138,6 +148,9 @@ def config(n: int) -> Shape:
         n_cols = int(lengths.max() // 4)
         return Shape("mixed_serving_b64_ctx1k-64k", b=64, s=1, start_pos=sp, n_cols=n_cols, rms_keys=True,
                      n_layers=4, seed=seed)
+    if n == 8:   # a prefill chunk of 2048 queries continuing a sequence at position 6144
+        return Shape("chunked_prefill_s2048_at6144", b=1, s=2048, start_pos=np.full(1, 6144, np.int32), n_cols=2048,
+                     seed=seed)
     if n in (6, 7):   # the model's own compression ratios (2 and 1) at context 65536
         r = 2 if n == 6 else 1
         return Shape(f"decode_b32_ctx65536_r{r}", b=32, s=1, start_pos=np.full(32, 65535, np.int32), ratio=r,
@@ -230,6 +243,7 @@ def make(shape: Shape, beta: float | None = None) -> dict:
             q[:, bi] = np.moveaxis(_rope_interleaved(q64, qpos, rd, th), -2, 1)
             iq64 = np.moveaxis(iq[bi].astype(np.float64), 0, -2)            # [Hi, s, Di]
             iq[bi] = np.moveaxis(_rope_interleaved(iq64, qpos, rd, th), -2, 0)
+            assert not shape.chunked, "RoPE inputs are drawn for prefill from 0 and decode only"
             if shape.prefill:
                 wpos = np.arange(shape.win_rows)
             else:   # ring slot i holds the newest position p <= start_pos with p % W == i
