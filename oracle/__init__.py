@@ -15,6 +15,9 @@ Every function is pinned by the CPU tests in ``tests/test_oracle_*.py``:
   sparse_attn        textbook softmax (sink -> -inf), single-row closed form, empty rows,
                      duplicate-row sink shift, permutation invariance, mass + sink = 1
   dense_attn         independent of index lists; equal to sparse_attn when k >= visible
+  mxfp4_quantize / mxfp4_decode / index_score_mxfp4   the E2M1 code table from the format's
+                     definition, exact round trips of grid values, ties to even, saturation,
+                     the scale rule against frexp, zero blocks, the error bound
   window_topk_idxs_chunked   the prefill band of the pages when the chunk starts at 0 (rows
                      shifted past the ring), brute-force positions of every referenced row
   output_inverse_rope   identity at angle 0, the quarter-turn closed form, complex
@@ -115,6 +118,86 @@ def window_topk_idxs_chunked(window_size: int, seqlen: int, start_pos: int) -> n
                 continue
             out[t, i] = W + (p - start_pos) if p >= start_pos else p % W
     return out
+
+
+# ------------------------------------------------------------------ MXFP4 (fp4 index keys and queries)
+#
+# Indexer.forward ("attend/selected" page) passes its keys and queries through fp4_act_quant(x,
+# fp4_block_size, True) before the score einsum; the quantiser itself is not on the pages.
+# Reading: the OCP Microscaling (MX) MXFP4 format -- blocks of 32 consecutive elements along the
+# head dim share one E8M0 scale 2^X with X = floor(log2(max |x|)) - 2 (2 = the largest exponent of
+# E2M1), each element x / 2^X rounded to the nearest E2M1 value (ties to the even code) and
+# saturated at +-6.  The flag `True` is read as "in place": the einsum then runs on the
+# dequantised values.
+
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def mxfp4_decode(codes, scales, dim: int) -> np.ndarray:
+    """Packed E2M1 codes [..., dim/2] (element 2j in the low nibble of byte j, 2j+1 in the high
+    one; bit 3 of a nibble = sign) and E8M0 scales [..., dim/32] (byte e -> 2^(e-127)) ->
+    float64 [..., dim]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (dim,))
+    mag = np.asarray(E2M1_MAGNITUDES)[nib & 0x7]
+    val = np.where(nib & 0x8, -mag, mag)
+    sc = np.exp2(scales.astype(np.float64) - 127.0)
+    return val * np.repeat(sc, 32, axis=-1)
+
+
+def mxfp4_quantize(x):
+    """float [..., dim] (dim a multiple of 32) -> (codes uint8 [..., dim/2], scales uint8 [..., dim/32])."""
+    x = np.asarray(x, dtype=np.float64)
+    dim = x.shape[-1]
+    blk = x.reshape(x.shape[:-1] + (dim // 32, 32))
+    amax = np.abs(blk).max(axis=-1)
+    with np.errstate(divide="ignore"):
+        X = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0, -127.0)
+    X = np.clip(X, -127.0, 127.0)
+    p = blk / np.exp2(X)[..., None]
+    a = np.minimum(np.abs(p), 6.0)
+    grid = np.asarray(E2M1_MAGNITUDES)
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 7)       # first grid value >= a
+    lo = np.clip(hi - 1, 0, 7)
+    d_lo, d_hi = a - grid[lo], grid[hi] - a
+    # nearest; on a tie the even code (mantissa bit 0 clear)
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a == grid[hi], hi, code)
+    sign = ((p < 0) & (code > 0)).astype(np.uint8) << 3
+    nib = (code.astype(np.uint8) | sign).reshape(x.shape)
+    codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+    scales = (X + 127.0).astype(np.uint8)
+    return codes, scales
+
+
+def mxfp4_fake_quant(x) -> np.ndarray:
+    """The values the einsum sees: quantise, then decode (float64)."""
+    codes, scales = mxfp4_quantize(x)
+    return mxfp4_decode(codes, scales, np.asarray(x).shape[-1])
+
+
+def index_score_mxfp4(iq, ik_codes, ik_scales, w, c: float, start_pos, n_cols: int, ratio: int,
+                      threads: int | None = None) -> np.ndarray:
+    """Indexer scores with MXFP4 keys (stored quantised) and queries (quantised in the forward):
+    index_score over the decoded values.  iq: [b, s, H, D] bf16 bits; ik_codes: [b, >= n_cols,
+    D/2] uint8; ik_scales: [b, >= n_cols, D/32] uint8; w: [b, s, H] bf16 bits.  The decoded
+    values are exact in bf16, so they go to index_score as bf16 bit patterns."""
+    iq = _c(iq, np.uint16)
+    D = iq.shape[-1]
+    qf = (np.ascontiguousarray(iq).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    qd = mxfp4_fake_quant(qf)
+    kd = mxfp4_decode(ik_codes, ik_scales, D)
+    return index_score(_bf16_exact(qd), _bf16_exact(kd), w, c, start_pos, n_cols, ratio, threads)
+
+
+def _bf16_exact(x) -> np.ndarray:
+    """float64 values exactly representable in bf16 -> their bit patterns (checked)."""
+    f = np.asarray(x, dtype=np.float32)
+    assert np.array_equal(f.astype(np.float64), np.asarray(x, dtype=np.float64)), "not exact in fp32"
+    bits = (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << np.uint32(16)).view(np.float32), f), "not exact in bf16"
+    return bits
 
 
 def compress_len(start_pos: int, seqlen: int, ratio: int) -> int:

@@ -453,3 +453,82 @@ def test_chunked_window_rows_hold_the_last_w_positions(orc, W, s, sp):
         want = set(range(max(0, P - W + 1), P + 1))
         rows = [int(v) for v in got[t] if v >= 0]
         assert sorted(held[r] for r in rows) == sorted(want)
+
+
+# ------------------------------------------------------------------ MXFP4 quantiser (reading of fp4_act_quant)
+
+
+def test_mxfp4_code_table_from_the_format_definition(orc):
+    """E2M1: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0; exponent 0 is subnormal
+    (m * 0.5).  Every one of the 16 codes, under scale byte 127 (2^0) and 130 (2^3)."""
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        want = (m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1)) * (-1) ** s
+        packed = np.zeros(16, np.uint8)
+        packed[0] = code | (code << 4)
+        for sb, mul in ((127, 1.0), (130, 8.0)):
+            got = orc.mxfp4_decode(packed[None], np.array([[sb]], np.uint8), 32)[0]
+            assert got[0] == want * mul and got[1] == want * mul and np.all(got[2:] == 0)
+    # element 2j is the low nibble of byte j, 2j+1 the high one; scale j covers elements 32j..
+    packed = np.zeros((1, 32), np.uint8)
+    packed[0, 0], packed[0, 16] = 0x21, 0xE5                 # (0.5, 1.0) and (3.0, -4.0)
+    got = orc.mxfp4_decode(packed, np.array([[127, 126]], np.uint8), 64)[0]
+    assert (got[0], got[1], got[32], got[33]) == (0.5, 1.0, 1.5, -2.0) and np.count_nonzero(got) == 4
+
+
+def test_mxfp4_rounds_ties_to_even_and_saturates(orc):
+    x = np.zeros((1, 32))
+    x[0, :9] = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, -2.5]        # block max 7: X = 0
+    got = orc.mxfp4_fake_quant(x)[0, :9]
+    np.testing.assert_array_equal(got, [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, 6.0, -2.0])
+
+
+def test_mxfp4_scale_rule_and_exact_round_trip(orc):
+    rng = np.random.default_rng(11)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    for X in (-20, -3, 0, 5, 40):
+        vals = rng.choice(grid, size=(3, 64)) * rng.choice([-1, 1], size=(3, 64))
+        vals[:, 0] = 6.0                              # each 32-block's max is 6 * 2^X ...
+        vals[:, 32] = -4.0                            # ... or 4 * 2^X: X = floor(log2) - 2
+        x = vals * 2.0 ** X
+        codes, scales = orc.mxfp4_quantize(x)
+        assert np.all(scales == X + 127)
+        np.testing.assert_array_equal(orc.mxfp4_decode(codes, scales, 64), x)
+        amax = np.abs(x.reshape(3, 2, 32)).max(-1)
+        assert np.all(scales == np.array([[math.frexp(a)[1] - 1 - 2 + 127 for a in row] for row in amax]))
+
+
+def test_mxfp4_zero_block_and_error_bound(orc):
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((50, 128)) * np.exp2(rng.integers(-8, 8, size=(50, 1)))
+    x[3, 32:64] = 0.0
+    codes, scales = orc.mxfp4_quantize(x)
+    q = orc.mxfp4_decode(codes, scales, 128)
+    assert np.all(q[3, 32:64] == 0)
+    unit = np.repeat(np.exp2(scales.astype(np.float64) - 127), 32, axis=-1)
+    # inside the grid the gap is at most 2 units (between 4 and 6); past 6 units it saturates,
+    # and the block max is below 8 units
+    assert np.all(np.abs(q - x) <= unit * 2 + 1e-300)
+    inside = np.abs(x) <= 6 * unit
+    assert np.all(np.abs(q - x)[inside] <= unit[inside])
+
+
+def test_mxfp4_index_score_is_the_score_of_the_decoded_values(orc):
+    """index_score_mxfp4 = index_score of independently decoded keys and quantised queries,
+    checked against a plain numpy formula of the score."""
+    rng = np.random.default_rng(13)
+    b, s, H, D, n = 2, 1, 4, 64, 40
+    iq = to_bf16_bits(rng.standard_normal((b, s, H, D)))
+    codes = rng.integers(0, 256, size=(b, n, D // 2), dtype=np.uint8)
+    scales = rng.integers(120, 130, size=(b, n, D // 32), dtype=np.uint8)
+    w = to_bf16_bits(rng.standard_normal((b, s, H)))
+    sp = np.array([4 * n - 1, 4 * 20 - 1], np.int32)
+    got = orc.index_score_mxfp4(iq, codes, scales, w, 0.125, sp, n, 4)
+    qd = orc.mxfp4_fake_quant(bf16_bits_to_f32(iq).astype(np.float64))
+    kd = orc.mxfp4_decode(codes, scales, D)
+    want = 0.125 * np.einsum("bsh,bsht->bst", bf16_bits_to_f32(w).astype(np.float64),
+                             np.maximum(np.einsum("bshd,btd->bsht", qd, kd), 0.0))
+    vis = np.minimum((sp + 1) // 4, n)
+    for bi in range(b):
+        np.testing.assert_allclose(got[bi, 0, :vis[bi]], want[bi, 0, :vis[bi]], rtol=1e-12, atol=1e-12)
+        assert np.all(np.isneginf(got[bi, 0, vis[bi]:]))
