@@ -1,6 +1,6 @@
 """Benchmark of the Indexer -> top-k -> sparse sink attention path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..8] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..9] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
 window indices, Indexer scores, top-k, sparse sink attention (every attention layer),
@@ -110,7 +110,10 @@ class GpuPath:
         self.sink = [to_dev_any(data["sink"][i], device) for i in range(self.L)]
         self.comp = to_dev(data["comp"], device)
         self.iq = to_dev(data["iq"], device)
-        self.ik = to_dev(data["ik"], device)
+        self.ik = to_dev(data["ik"], device) if "ik" in data else None
+        # MXFP4 keys (workload 9): codes and scales instead of bf16 keys
+        self.ik_codes = to_dev_any(data["ik_codes"], device) if "ik_codes" in data else None
+        self.ik_scales = to_dev_any(data["ik_scales"], device) if "ik_scales" in data else None
         self.w = to_dev(data["w"], device)
         self.sp = to_dev_any(data["start_pos"], device)
         self.scores = torch.empty(self.b, self.s, shape.n_cols, dtype=torch.float32, device=device)
@@ -134,7 +137,8 @@ class GpuPath:
                                               shape.n_cols, shape.topk,
                                               out=self.out[0].view(self.b, shape.h, shape.d),
                                               topk_idxs=self.idx.view(self.b, self.k_total),
-                                              rope_cs=None if self.rope_cs is None else self.rope_cs[:, 0])
+                                              rope_cs=None if self.rope_cs is None else self.rope_cs[:, 0],
+                                              ik_codes=self.ik_codes, ik_scales=self.ik_scales)
             self.dws = sti.workspace(sti.decode_workspace_size(self.args), device)
 
     def capture(self):
@@ -198,8 +202,12 @@ class GpuPath:
         else:
             sti.window_idxs(self.sp, self.s, self.W, out=self.idx[..., :self.width], ws=self.ws)
         rec(1)
-        sti.idx_scores(self.iq, self.ik, self.w, shp.index_scale, self.sp, shp.n_cols, shp.ratio, out=self.scores,
-                       ws=self.ws)
+        if self.ik_codes is not None:
+            sti.idx_scores_mxfp4(self.iq, self.ik_codes, self.ik_scales, self.w, shp.index_scale, self.sp, shp.n_cols,
+                                 shp.ratio, out=self.scores, ws=self.ws)
+        else:
+            sti.idx_scores(self.iq, self.ik, self.w, shp.index_scale, self.sp, shp.n_cols, shp.ratio,
+                           out=self.scores, ws=self.ws)
         rec(2)
         # compressed rows follow the window source's rows: offset = s raw rows (prefill) or W slots (decode)
         sti.idx_topk(self.scores, self.sp, shp.ratio, shp.topk, shp.win_rows, out=self.idx[..., self.width:],
@@ -241,8 +249,9 @@ def work(shape: workloads.Shape, data: dict) -> dict:
         win_valid = np.minimum(sp + 1, shape.window)[:, None]
     rows = (sel + win_valid).sum()                                                  # valid gathered rows
     w = {}
+    key_bytes = (Di // 2 + Di // 32) if shape.fp4_keys else Di * 2                  # per key (MXFP4: codes + scales)
     w["idx_scores"] = {
-        "bytes": float(n_keys.sum() * Di * 2 + b * s * Hi * Di * 2 + b * s * Hi * 2 + b * s * shape.n_cols * 4),
+        "bytes": float(n_keys.sum() * key_bytes + b * s * Hi * Di * 2 + b * s * Hi * 2 + b * s * shape.n_cols * 4),
         "flops": float(2 * Hi * Di * vis.sum()),
     }
     w["idx_topk"] = {"bytes": float(vis.sum() * 4 + b * s * shape.topk * 4), "flops": 0.0}
@@ -353,7 +362,12 @@ def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = No
                                     kv2=data["comp"], rope_cs=cs)
         return len(t)
     sp = data["start_pos"]
-    score = oracle.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
+    if shape.fp4_keys:
+        score = oracle.index_score_mxfp4(data["iq"], data["ik_codes"], data["ik_scales"], data["w"], shape.index_scale,
+                                         sp, shape.n_cols, shape.ratio)
+    else:
+        score = oracle.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols,
+                                   shape.ratio)
     cidx = oracle.topk(score, sp, shape.ratio, shape.topk, W)
     widx = np.concatenate([oracle.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0)
     idx = np.concatenate([widx, cidx], axis=-1)
@@ -437,7 +451,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -615,7 +629,8 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     d_cs = None if h_cs is None else torch.empty_like(path.rope_cs[:, 0])
     a, out, tk = sti.decode_args(d_q.view_as(path.q[0]), path.win[0], path.comp, path.sink[0], shp.softmax_scale,
                                  d_iq.view_as(path.iq), path.ik, d_w.view_as(path.w), shp.index_scale, d_sp,
-                                 shp.ratio, shp.n_cols, shp.topk, rope_cs=d_cs)
+                                 shp.ratio, shp.n_cols, shp.topk, rope_cs=d_cs, ik_codes=path.ik_codes,
+                                 ik_scales=path.ik_scales)
     ws = sti.workspace(sti.decode_workspace_size(a), path.dev)
     bi = h_q.numel() * 2 + h_iq.numel() * 2 + h_w.numel() * 2 + h_sp.numel() * 4
     bi += 0 if h_cs is None else h_cs.numel() * 4

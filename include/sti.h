@@ -125,6 +125,28 @@ sti_status sti_idx_scores(const uint16_t *iq, const uint16_t *ik, int64_t ik_bst
                           const int32_t *start_pos, int b, int seqlen, int Hi, int Di, int n_cols, int ratio,
                           float *scores, void *ws, size_t ws_bytes, sti_stream stream);
 
+/*
+ * The same scores with the Indexer's fp4 keys and queries (Indexer.forward passes both through
+ * fp4_act_quant before the einsum; the quantiser is not on the pages).  Reading: OCP MXFP4 --
+ * blocks of 32 consecutive elements along Di share an E8M0 scale byte e (2^(e-127)); each
+ * element is an E2M1 nibble (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa;
+ * exponent 0: m * 0.5), i.e. one of +-{0, .5, 1, 1.5, 2, 3, 4, 6} times the scale.
+ *   ik_codes: uint8 [b, *, Di/2], batch b at + b*ik_codes_bstride bytes; byte j of a key holds
+ *       element 2j (low nibble) and 2j+1 (high nibble)
+ *   ik_scales: uint8 [b, *, Di/32], batch b at + b*ik_scales_bstride bytes
+ *   iq (bf16, as above) is quantised in the kernel: per 32-element block X = floor(log2 max|x|)
+ *       - 2 (clamped to [-127, 127]), x / 2^X to the nearest E2M1 value (ties to the even code,
+ *       saturating at 6), times 2^X.
+ * The score is the einsum/relu/weighted sum above over the decoded values (exact in bf16), with
+ * fp32 accumulation.  Keys move as 68 bytes per position at Di = 128 instead of 256.
+ * Supported: Di in {64, 128}; ik_codes, ik_scales 16-byte aligned; bstrides multiples of 16
+ * covering n_cols keys.  Everything else as sti_idx_scores.
+ */
+sti_status sti_idx_scores_mxfp4(const uint16_t *iq, const uint8_t *ik_codes, int64_t ik_codes_bstride,
+                                const uint8_t *ik_scales, int64_t ik_scales_bstride, const uint16_t *w, float c,
+                                const int32_t *start_pos, int b, int seqlen, int Hi, int Di, int n_cols, int ratio,
+                                float *scores, void *ws, size_t ws_bytes, sti_stream stream);
+
 /* ------------------------------------------------------------------ top-k */
 /*
  * Indexer.forward (attend/selected page), the selection block:
@@ -242,6 +264,12 @@ typedef struct sti_decode_args {
      * multiplied by cos - i sin.  rope_dims: 0 (none) or even, <= d; rope_cs 16-byte aligned. */
     const float *rope_cs;
     int rope_dims;
+    /* optional: MXFP4 index keys (as sti_idx_scores_mxfp4) instead of ik; the queries are then
+     * quantised to MXFP4 in the scores kernel.  NULL ik_codes: bf16 keys from ik. */
+    const uint8_t *ik_codes;
+    int64_t ik_codes_bstride;   /* bytes */
+    const uint8_t *ik_scales;
+    int64_t ik_scales_bstride;  /* bytes */
 } sti_decode_args;
 
 /* Steps 2 and 3 launch as programmatic dependents of the step before them: each is scheduled

@@ -32,7 +32,7 @@ EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_sparse_attn_sink_rope",
            "sti_decode_workspace_size",
            "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
-           "sti_selftest_wait_timeout", "sti_window_idxs_chunked"]
+           "sti_selftest_wait_timeout", "sti_window_idxs_chunked", "sti_idx_scores_mxfp4"]
 
 
 class StiError(RuntimeError):
@@ -53,6 +53,8 @@ class DecodeArgs(ctypes.Structure):
         ("ratio", ctypes.c_int), ("n_cols", ctypes.c_int), ("start_pos", ctypes.c_void_p), ("b", ctypes.c_int),
         ("out", ctypes.c_void_p), ("topk_idxs", ctypes.c_void_p), ("q_ready", ctypes.c_void_p),
         ("rope_cs", ctypes.c_void_p), ("rope_dims", ctypes.c_int),
+        ("ik_codes", ctypes.c_void_p), ("ik_codes_bstride", ctypes.c_int64), ("ik_scales", ctypes.c_void_p),
+        ("ik_scales_bstride", ctypes.c_int64),
     ]
 
 
@@ -75,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.sti_window_idxs_chunked.argtypes, L.sti_window_idxs_chunked.restype = [P, I, I, I, P, I64, P, P], I
         L.sti_idx_scores_workspace_size.argtypes, L.sti_idx_scores_workspace_size.restype = [], SZ
         L.sti_idx_scores.argtypes = [P, P, I64, P, F, P, I, I, I, I, I, I, P, P, SZ, P]
+        L.sti_idx_scores_mxfp4.argtypes = [P, P, I64, P, I64, P, F, P, I, I, I, I, I, I, P, P, SZ, P]
+        L.sti_idx_scores_mxfp4.restype = I
         L.sti_idx_scores.restype = I
         L.sti_idx_topk_workspace_size.argtypes, L.sti_idx_topk_workspace_size.restype = [], SZ
         L.sti_idx_topk.argtypes = [P, P, I, I, I, I, I, ctypes.c_int32, P, I64, P, SZ, P]
@@ -192,6 +196,28 @@ def idx_scores(iq: torch.Tensor, ik: torch.Tensor, w: torch.Tensor, c: float, st
     return out
 
 
+def idx_scores_mxfp4(iq: torch.Tensor, ik_codes: torch.Tensor, ik_scales: torch.Tensor, w: torch.Tensor, c: float,
+                     start_pos: torch.Tensor, n_cols: int, ratio: int, out: torch.Tensor | None = None,
+                     ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Indexer scores with MXFP4 keys: ik_codes uint8 [b, cap, Di/2], ik_scales uint8
+    [b, cap, Di/32] (cap >= n_cols); the queries are quantised to MXFP4 in the kernel."""
+    _need(iq, torch.bfloat16, "iq")
+    _need(w, torch.bfloat16, "w")
+    _need(start_pos, torch.int32, "start_pos")
+    b, s, Hi, Di = iq.shape
+    for name, t, inner in (("ik_codes", ik_codes, Di // 2), ("ik_scales", ik_scales, Di // 32)):
+        if t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != inner:
+            raise ValueError(f"{name} must be uint8 [b, rows, {inner}] with contiguous rows")
+    if out is None:
+        out = torch.empty(b, s, n_cols, dtype=torch.float32, device=iq.device)
+    ws = ws if ws is not None else workspace(lib().sti_idx_scores_workspace_size(), iq.device)
+    _check(lib().sti_idx_scores_mxfp4(_ptr(iq), _ptr(ik_codes), ik_codes.stride(0), _ptr(ik_scales),
+                                      ik_scales.stride(0), _ptr(w), float(c), _ptr(start_pos), b, s, Hi, Di, n_cols,
+                                      ratio, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+           "sti_idx_scores_mxfp4")
+    return out
+
+
 def idx_topk(scores: torch.Tensor, start_pos: torch.Tensor, ratio: int, k: int, offset: int,
              out: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Top-k visible positions per row, ascending, + offset, -1 padded: [b, s, k] int32.
@@ -254,12 +280,14 @@ def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
 
 
 def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, index_scale, start_pos, ratio, n_cols,
-                index_topk, out=None, topk_idxs=None, q_ready=None,
-                rope_cs=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
+                index_topk, out=None, topk_idxs=None, q_ready=None, rope_cs=None, ik_codes=None,
+                ik_scales=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
     """Fill sti_decode_args from tensors.  q [b,h,d] (or [b,1,h,d]), window_kv [b,W,d],
     comp_kv [b,cap,d], iq [b,Hi,Di] (or [b,1,Hi,Di]), ik [b,cap,Di], w [b,Hi] (or [b,1,Hi]).
     q_ready: optional torch.cuda.Event (already recorded once) the attention step waits for.
     rope_cs: optional fp32 [b, rd/2, 2] (cos, sin) of the output's inverse rotation.
+    ik_codes / ik_scales: optional MXFP4 index keys (uint8 [b, cap, Di/2] / [b, cap, Di/32]);
+    then `ik` is not read (it may be None).
     The returned struct keeps references to every tensor it points to."""
     b = q.shape[0]
     h, d = q.shape[-2], q.shape[-1]
@@ -269,6 +297,8 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
                         ("attn_sink", attn_sink, torch.float32), ("start_pos", start_pos, torch.int32)):
         _need(t, dt, name)
     for name, t, inner in (("window_kv", window_kv, d), ("comp_kv", comp_kv, d), ("ik", ik, Di)):
+        if t is None and name == "ik" and ik_codes is not None:
+            continue
         _need(t, torch.bfloat16, name, contiguous=False)
         if t.stride(2) != 1 or t.stride(1) != inner:
             raise ValueError(f"{name} must have contiguous rows")
@@ -277,7 +307,8 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
     if topk_idxs is None:
         topk_idxs = torch.empty(b, W + index_topk, dtype=torch.int32, device=q.device)
     a = DecodeArgs(_ptr(q), _ptr(window_kv), window_kv.stride(0), _ptr(comp_kv), comp_kv.stride(0), _ptr(attn_sink),
-                   float(softmax_scale), h, d, W, _ptr(iq), _ptr(ik), ik.stride(0), _ptr(w), float(index_scale), Hi,
+                   float(softmax_scale), h, d, W, _ptr(iq), _ptr(ik), 0 if ik is None else ik.stride(0), _ptr(w),
+                   float(index_scale), Hi,
                    Di, index_topk, ratio, n_cols, _ptr(start_pos), b, _ptr(out), _ptr(topk_idxs),
                    q_ready.cuda_event if q_ready is not None else None)
     if rope_cs is not None:
@@ -285,8 +316,15 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
         if rope_cs.dim() != 3 or rope_cs.shape[0] != b or rope_cs.shape[2] != 2:
             raise ValueError("rope_cs must be [b, rd/2, 2]")
         a.rope_cs, a.rope_dims = _ptr(rope_cs), 2 * rope_cs.shape[1]
+    if ik_codes is not None:
+        for name, t, inner in (("ik_codes", ik_codes, Di // 2), ("ik_scales", ik_scales, Di // 32)):
+            if t is None or t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != inner:
+                raise ValueError(f"{name} must be uint8 [b, rows, {inner}] with contiguous rows")
+        a.ik_codes, a.ik_codes_bstride = _ptr(ik_codes), ik_codes.stride(0)
+        a.ik_scales, a.ik_scales_bstride = _ptr(ik_scales), ik_scales.stride(0)
     # the struct holds raw device pointers: keep their tensors alive as long as it lives
-    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready, rope_cs)
+    a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready, rope_cs, ik_codes,
+                 ik_scales)
     return a, out, topk_idxs
 
 

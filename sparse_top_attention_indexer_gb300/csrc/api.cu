@@ -86,6 +86,29 @@ sti_status make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_
     return STI_OK;
 }
 
+// 3-D byte tensor map (no swizzle): dims {inner bytes, rows, batch}, strides in bytes.
+sti_status make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t batch,
+                          uint64_t row_stride_bytes, uint64_t batch_stride_bytes, uint32_t box_inner,
+                          uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled unavailable");
+        return STI_ERR_CUDA;
+    }
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {row_stride_bytes, batch_stride_bytes};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return STI_ERR_CUDA;
+    }
+    return STI_OK;
+}
+
 uint32_t* status_word(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
@@ -120,17 +143,39 @@ static sti_status window_impl(const int32_t* start_pos, int b, int seqlen, int w
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_window_idxs");
 }
 
+// MXFP4 index keys: E2M1 codes [b, *, Di/2] bytes and E8M0 scales [b, *, Di/32] bytes.
+struct Fp4Keys {
+    const uint8_t* codes = nullptr;
+    int64_t codes_bstride = 0;    // bytes
+    const uint8_t* scales = nullptr;
+    int64_t scales_bstride = 0;   // bytes
+};
+
+// Host checks of MXFP4 keys (done before anything is enqueued).
+static sti_status fp4_keys_check(const Fp4Keys& k, int Di, int n_cols) {
+    if (!(Di == 64 || Di == 128)) return STI_ERR_UNSUPPORTED;
+    if (!k.codes || !k.scales || !aligned(k.codes, 16) || !aligned(k.scales, 16)) return STI_ERR_INVALID_ARG;
+    if (k.codes_bstride < (int64_t)n_cols * Di / 2 || k.codes_bstride % 16 != 0) return STI_ERR_INVALID_ARG;
+    if (k.scales_bstride < ((int64_t)n_cols * Di / 32 + 15) / 16 * 16 || k.scales_bstride % 16 != 0)
+        return STI_ERR_INVALID_ARG;
+    return STI_OK;
+}
+
 static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_t ik_bstride, const uint16_t* w,
                                   float c, const int32_t* start_pos, int b, int seqlen, int Hi, int Di, int n_cols,
                                   int ratio, float* scores, uint32_t* status, cudaStream_t st,
-                                  uint32_t* hist = nullptr) {
+                                  uint32_t* hist = nullptr, const Fp4Keys* fp4 = nullptr) {
     if (b < 0 || seqlen < 1 || n_cols < 0 || ratio < 1) return STI_ERR_INVALID_ARG;
     if (!(Di == 32 || Di == 64 || Di == 128)) return STI_ERR_UNSUPPORTED;
     if (!(Hi == 4 || Hi == 8 || Hi == 16 || Hi == 32 || Hi == 64)) return STI_ERR_UNSUPPORTED;
+    if (fp4) {
+        const sti_status fs = fp4_keys_check(*fp4, Di, n_cols);
+        if (fs != STI_OK) return fs;
+    }
     if (b == 0 || n_cols == 0) return STI_OK;
-    if (!iq || !ik || !w || !start_pos || !scores) return STI_ERR_INVALID_ARG;
-    if (ik_bstride < (int64_t)n_cols * Di || (ik_bstride % 8) != 0) return STI_ERR_INVALID_ARG;
-    if (!aligned(iq, 16) || !aligned(ik, 16)) return STI_ERR_INVALID_ARG;
+    if (!iq || (!fp4 && !ik) || !w || !start_pos || !scores) return STI_ERR_INVALID_ARG;
+    if (!fp4 && (ik_bstride < (int64_t)n_cols * Di || (ik_bstride % 8) != 0)) return STI_ERR_INVALID_ARG;
+    if (!aligned(iq, 16) || (!fp4 && !aligned(ik, 16))) return STI_ERR_INVALID_ARG;
     if ((int64_t)seqlen * Hi > 0x7FFFFFFF || (int64_t)b * seqlen > 0x7FFFFFFF) return STI_ERR_UNSUPPORTED;
 
     sti::IdxScoresParams p{};
@@ -159,21 +204,36 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     // TMA producers); possible when both CTAs' accumulators fit the SM's 512 TMEM columns.
     p.ctas_per_sm = p.tmem_cols <= 256 ? 2 : 1;
     const size_t budget = p.ctas_per_sm == 2 ? 104 * 1024 : 200 * 1024;
-    int stages = (int)((budget - b_bytes) / a_bytes);
-    if (stages > 8) stages = 8;
+    p.fp4 = fp4 ? 1 : 0;
+    // MXFP4: four stages of packed tiles (a quarter of the bytes) feed two dequantised bf16 tiles
+    p.c_stages = fp4 ? 4 : 0;
+    const size_t c_total = fp4 ? (size_t)p.c_stages * ((size_t)128 * Di / 2 + (size_t)128 * Di / 32) : 0;
+    int stages = (int)((budget - b_bytes - c_total) / a_bytes);
+    if (stages > (fp4 ? 3 : 8)) stages = fp4 ? 3 : 8;
     if (stages < 2) stages = 2;
     p.stages = stages;
 
     const uint32_t box_inner = Di >= 64 ? 64u : (uint32_t)Di;
     const CUtensorMapSwizzle swz = Di >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tm_a, tm_b;
-    sti_status s = make_map_3d(&tm_a, ik, (uint64_t)Di, (uint64_t)n_cols, (uint64_t)b, (uint64_t)Di * 2,
-                               (uint64_t)ik_bstride * 2, box_inner, 128, swz);
+    CUtensorMap tm_a, tm_b, tm_s;
+    memset(&tm_s, 0, sizeof tm_s);
+    sti_status s;
+    if (fp4) {
+        // codes: rows of Di/2 bytes; scales: each batch's Di/32 bytes per key as rows of 16 bytes
+        s = make_map_3d_u8(&tm_a, fp4->codes, (uint64_t)Di / 2, (uint64_t)n_cols, (uint64_t)b, (uint64_t)Di / 2,
+                           (uint64_t)fp4->codes_bstride, (uint32_t)Di / 2, 128);
+        if (s == STI_OK)
+            s = make_map_3d_u8(&tm_s, fp4->scales, 16, ((uint64_t)n_cols * Di / 32 + 15) / 16, (uint64_t)b, 16,
+                               (uint64_t)fp4->scales_bstride, 16, (uint32_t)Di / 4);
+    } else {
+        s = make_map_3d(&tm_a, ik, (uint64_t)Di, (uint64_t)n_cols, (uint64_t)b, (uint64_t)Di * 2,
+                        (uint64_t)ik_bstride * 2, box_inner, 128, swz);
+    }
     if (s != STI_OK) return s;
     s = make_map_3d(&tm_b, iq, (uint64_t)Di, (uint64_t)seqlen * Hi, (uint64_t)b, (uint64_t)Di * 2,
                     (uint64_t)seqlen * Hi * Di * 2, box_inner, (uint32_t)p.n_pad, swz);
     if (s != STI_OK) return s;
-    cudaError_t e = sti::launch_idx_scores(tm_a, tm_b, p, sti::device_num_sms(), st);
+    cudaError_t e = sti::launch_idx_scores(tm_a, tm_b, tm_s, p, sti::device_num_sms(), st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_idx_scores");
 }
 
@@ -380,6 +440,20 @@ sti_status sti_idx_scores(const uint16_t* iq, const uint16_t* ik, int64_t ik_bst
                            status_word(ws), static_cast<cudaStream_t>(stream));
 }
 
+sti_status sti_idx_scores_mxfp4(const uint16_t* iq, const uint8_t* ik_codes, int64_t ik_codes_bstride,
+                                const uint8_t* ik_scales, int64_t ik_scales_bstride, const uint16_t* w, float c,
+                                const int32_t* start_pos, int b, int seqlen, int Hi, int Di, int n_cols, int ratio,
+                                float* scores, void* ws, size_t ws_bytes, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti_idx_scores_workspace_size())) return STI_ERR_INVALID_ARG;
+    Fp4Keys k;
+    k.codes = ik_codes;
+    k.codes_bstride = ik_codes_bstride;
+    k.scales = ik_scales;
+    k.scales_bstride = ik_scales_bstride;
+    return idx_scores_impl(iq, nullptr, 0, w, c, start_pos, b, seqlen, Hi, Di, n_cols, ratio, scores,
+                           status_word(ws), static_cast<cudaStream_t>(stream), nullptr, &k);
+}
+
 size_t sti_idx_topk_workspace_size(void) { return sti::kWsStatusBytes; }
 
 sti_status sti_idx_topk(const float* scores, const int32_t* start_pos, int b, int seqlen, int n_cols, int ratio,
@@ -434,6 +508,16 @@ size_t sti_decode_workspace_size(const sti_decode_args* a) {
     return sti::kWsStatusBytes + decode_scores_bytes(a) + decode_hist_bytes(a) + decode_acc_bytes(a);
 }
 
+// MXFP4 index keys of a decode step (NULL: bf16 keys).
+static const Fp4Keys* decode_fp4(const sti_decode_args* a, Fp4Keys* k) {
+    if (!a->ik_codes) return nullptr;
+    k->codes = a->ik_codes;
+    k->codes_bstride = a->ik_codes_bstride;
+    k->scales = a->ik_scales;
+    k->scales_bstride = a->ik_scales_bstride;
+    return k;
+}
+
 // The optional output rotation's arguments (checked before any step is enqueued).
 static bool decode_rope_ok(const sti_decode_args* a) {
     return a->rope_dims == 0 || (a->rope_dims > 0 && a->rope_dims % 2 == 0 && a->rope_dims <= a->d && a->rope_cs &&
@@ -445,6 +529,11 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     if (!a) return STI_ERR_INVALID_ARG;
     if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
     if (!decode_rope_ok(a)) return STI_ERR_INVALID_ARG;
+    Fp4Keys fk;
+    if (decode_fp4(a, &fk) && a->n_cols > 0) {
+        const sti_status fs = fp4_keys_check(fk, a->Di, a->n_cols);
+        if (fs != STI_OK) return fs;
+    }
     if (a->b == 0) return STI_OK;
     if (!ws_ok(ws, ws_bytes, sti_decode_workspace_size(a))) return STI_ERR_INVALID_ARG;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
@@ -469,7 +558,7 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     sti_status s = STI_OK;
     if (a->n_cols > 0) {
         s = idx_scores_impl(a->iq, a->ik, a->ik_bstride, a->w, a->index_scale, a->start_pos, a->b, 1, a->Hi, a->Di,
-                            a->n_cols, a->ratio, scores, status, st, hist);
+                            a->n_cols, a->ratio, scores, status, st, hist, decode_fp4(a, &fk));
         if (s != STI_OK) return s;
     }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
@@ -538,6 +627,11 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     if (!a) return STI_ERR_INVALID_ARG;
     if (a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return STI_ERR_INVALID_ARG;
     if (!decode_rope_ok(a)) return STI_ERR_INVALID_ARG;
+    Fp4Keys fk;
+    if (decode_fp4(a, &fk) && a->n_cols > 0) {
+        const sti_status fs = fp4_keys_check(fk, a->Di, a->n_cols);
+        if (fs != STI_OK) return fs;
+    }
     if (a->b == 0) return STI_OK;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
     if (a->b > STI_NOALLOC_MAX_BATCH || (int64_t)a->b * (a->n_cols > 0 ? a->n_cols : 1) > STI_NOALLOC_MAX_SCORES)
@@ -560,7 +654,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     const int W = a->window_size, K = a->index_topk, k_total = W + K;
     if (a->n_cols > 0) {
         s = idx_scores_impl(a->iq, a->ik, a->ik_bstride, a->w, a->index_scale, a->start_pos, a->b, 1, a->Hi, a->Di,
-                            a->n_cols, a->ratio, scores, status, st, hist);
+                            a->n_cols, a->ratio, scores, status, st, hist, decode_fp4(a, &fk));
         if (s != STI_OK) return s;
     }
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,

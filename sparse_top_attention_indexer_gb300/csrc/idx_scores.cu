@@ -26,13 +26,17 @@ namespace sti {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;      // bf16 keys: producer, MMA, 4 epilogue warps
+constexpr int kThreadsFp4 = 320;   // MXFP4 keys: + 4 warps that dequantise keys and quantise queries
 constexpr int kMaxStages = 8;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 struct __align__(8) Barriers {
     uint64_t full_a[kMaxStages];
     uint64_t empty_a[kMaxStages];
+    uint64_t full_c[kMaxStages];    // MXFP4: packed key tile (codes + scales) landed
+    uint64_t empty_c[kMaxStages];   // MXFP4: packed key tile dequantised (stage free)
+    uint64_t b_ready;               // MXFP4: the unit's queries quantised in place
     uint64_t full_b, empty_b;
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
@@ -112,10 +116,57 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int Di, i
 __device__ unsigned long long g_sc_t[2048][2];   // global timer at CTA start and end (profiling builds)
 #endif
 
-template <int HI>
-__global__ void __launch_bounds__(kThreads, 1)
+// E2M1 nibble (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa; exponent 0 is
+// subnormal: m * 0.5) as a float.
+__device__ __forceinline__ float e2m1_value(uint32_t nib) {
+    const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+    uint32_t bits = e ? ((126u + e) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(bits | ((nib & 8u) << 28));
+}
+
+// E8M0 scale byte -> 2^(e - 127) (255 is NaN).
+__device__ __forceinline__ float e8m0_value(uint32_t e) {
+    return e == 0u ? __uint_as_float(0x00400000u) : (e == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23));
+}
+
+// |x| / 2^X onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}: nearest, ties to the even code,
+// saturating at 6.
+__device__ __forceinline__ float e2m1_round(float a) {
+    return a <= 0.25f ? 0.f : a < 0.75f ? 0.5f : a <= 1.25f ? 1.f : a < 1.75f ? 1.5f
+         : a <= 2.5f ? 2.f : a < 3.5f ? 3.f : a <= 5.f ? 4.f : 6.f;
+}
+
+// One 32-element block of bf16 queries (four 16-byte chunks at c0..c3), quantised to MXFP4 and
+// decoded back in place (Indexer.forward's fp4_act_quant on q, read as OCP MXFP4: scale 2^X with
+// X = floor(log2 max|x|) - 2).  The decoded values are exact in bf16.
+__device__ __forceinline__ void mxfp4_fake_quant_block(uint4* c0, uint4* c1, uint4* c2, uint4* c3) {
+    uint4 v[4] = {*c0, *c1, *c2, *c3};
+    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    const int X = amax > 0.f ? max(-127, min(127, ilogbf(amax) - 2)) : -127;
+    const float sc = ldexpf(1.f, X), inv = ldexpf(1.f, -X);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+        const float ql = copysignf(e2m1_round(fabsf(lo) * inv), lo) * sc;
+        const float qh = copysignf(e2m1_round(fabsf(hi) * inv), hi) * sc;
+        w[i] = (__float_as_uint(ql) >> 16) | (__float_as_uint(qh) & 0xFFFF0000u);
+    }
+    *c0 = v[0];
+    *c1 = v[1];
+    *c2 = v[2];
+    *c3 = v[3];
+}
+
+template <int HI, bool FP4>
+__global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const IdxScoresParams p) {
+                      const __grid_constant__ CUtensorMap tm_s, const IdxScoresParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
     // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
@@ -128,7 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b_bytes = p.n_pad * p.Di * 2;
     uint8_t* a_ring = smem;
     uint8_t* b_buf = smem + (size_t)p.stages * a_bytes;
-    Barriers* bars = reinterpret_cast<Barriers*>(b_buf + b_bytes);
+    // MXFP4: packed key tiles, [128 keys x Di/2 code bytes | 128 keys x Di/32 scale bytes] per stage
+    const int c_code_bytes = kTileKeys * p.Di / 2;
+    const int c_bytes = FP4 ? c_code_bytes + kTileKeys * p.Di / 32 : 0;
+    uint8_t* c_ring = b_buf + b_bytes;
+    Barriers* bars = reinterpret_cast<Barriers*>(c_ring + (size_t)(FP4 ? p.c_stages : 0) * c_bytes);
     float* w_s = reinterpret_cast<float*>(bars + 1);   // [nq * HI], pre-multiplied by c
     int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq]
 
@@ -136,8 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&bars->full_a[i], 1);
+            mbar_init(&bars->full_a[i], FP4 ? 4 : 1);   // MXFP4: the four dequantising warps
             mbar_init(&bars->empty_a[i], 1);
+        }
+        if (FP4) {
+            for (int i = 0; i < p.c_stages; ++i) {
+                mbar_init(&bars->full_c[i], 1);
+                mbar_init(&bars->empty_c[i], 4);
+            }
+            mbar_init(&bars->b_ready, 1);
         }
         mbar_init(&bars->full_b, 1);
         mbar_init(&bars->empty_b, 1);
@@ -177,7 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_b);
+            if (FP4) tma_prefetch_desc(&tm_s);
         }
+        const int n_st = FP4 ? p.c_stages : p.stages;   // the ring this producer fills
         int stage = 0;
         uint32_t phase = 0, b_phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;  // per stage: armed at least once, parity of last arm
@@ -197,13 +261,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         b_issued = true;
                     }
                 }
-                ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
+                if (FP4) {
+                    // packed keys: 128 rows of Di/2 code bytes, then their Di/32 scale bytes per
+                    // key viewed as rows of 16 bytes (Di/4 rows per tile)
+                    ok = ok && mbar_wait(&bars->empty_c[stage], phase ^ 1u, p.status);
+                    if (ok) {
+                        uint8_t* dst = c_ring + (size_t)stage * c_bytes;
+                        mbar_arrive_expect_tx(&bars->full_c[stage], (uint32_t)c_bytes);
+                        tma_load_3d(dst, &tm_a, &bars->full_c[stage], 0, tile * kTileKeys, b);
+                        tma_load_3d(dst + c_code_bytes, &tm_s, &bars->full_c[stage], 0, tile * (p.Di / 4), b);
+                    }
+                } else {
+                    ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
+                    if (ok) {
+                        uint8_t* dst = a_ring + (size_t)stage * a_bytes;
+                        mbar_arrive_expect_tx(&bars->full_a[stage], (uint32_t)a_bytes);
+                        for (int cb = 0; cb < ncb; ++cb)
+                            tma_load_3d(dst + (size_t)cb * kTileKeys * box_inner * 2, &tm_a, &bars->full_a[stage],
+                                        cb * box_inner, tile * kTileKeys, b);
+                    }
+                }
                 if (ok) {
-                    uint8_t* dst = a_ring + (size_t)stage * a_bytes;
-                    mbar_arrive_expect_tx(&bars->full_a[stage], (uint32_t)a_bytes);
-                    for (int cb = 0; cb < ncb; ++cb)
-                        tma_load_3d(dst + (size_t)cb * kTileKeys * box_inner * 2, &tm_a, &bars->full_a[stage],
-                                    cb * box_inner, tile * kTileKeys, b);
                     issued_mask |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 } else {
@@ -212,15 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (u != cur_unit) b_phase ^= 1u;
             cur_unit = u;
-            if (++stage == p.stages) {
+            if (++stage == n_st) {
                 stage = 0;
                 phase ^= 1u;
             }
             advance(p, u, tile);
         }
         if (lane == 0) {
-            for (int st = 0; st < p.stages; ++st)
-                if (issued_mask & (1u << st)) mbar_wait(&bars->full_a[st], (issued_parity >> st) & 1u, p.status);
+            for (int st = 0; st < n_st; ++st)
+                if (issued_mask & (1u << st))
+                    mbar_wait(FP4 ? &bars->full_c[st] : &bars->full_a[st], (issued_parity >> st) & 1u, p.status);
             if (b_issued) mbar_wait(&bars->full_b, b_phase ^ 1u, p.status);
         }
     } else if (warp == 1) {
@@ -235,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 if (u != cur_unit) {
                     if (cur_unit >= 0) umma_commit(&bars->empty_b);
-                    ok = mbar_wait(&bars->full_b, b_phase, p.status);
+                    ok = mbar_wait(FP4 ? &bars->b_ready : &bars->full_b, b_phase, p.status);
                 }
                 ok = ok && mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, p.status);
                 ok = ok && mbar_wait(&bars->full_a[stage], phase, p.status);
@@ -268,6 +347,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
             umma_commit(&bars->mma_done);
             mbar_wait(&bars->mma_done, 0, p.status);
+        }
+    } else if (FP4 && warp >= 6) {
+        // ---------------------------------------------------------------- MXFP4 keys and queries
+        // Thread dq owns key row dq of every tile: its Di/2 code bytes and Di/32 scale bytes become
+        // Di bf16 values (exact: an E2M1 value times a power of two) in the 128-byte-swizzled tile
+        // the MMA reads.  At each new unit the four warps first quantise the unit's queries in
+        // place (32-element blocks of every query row), as the forward pass quantises q.
+        const int dq = threadIdx.x - 192;               // 0..127
+        const int nblk = p.Di / 32;
+        int astage = 0, cstage = 0;
+        uint32_t aphase = 0, cphase = 0, b_phase = 0;
+        int cur_unit = -1;
+        for (int g = g0; g < g1; ++g) {
+            bool ok = !aborted();
+            if (u != cur_unit) {
+                ok = ok && mbar_wait(&bars->full_b, b_phase, p.status);
+                if (ok) {
+                    for (int i = dq; i < p.n_pad * nblk; i += 128) {
+                        const int r = i / nblk, j = i - (i / nblk) * nblk;
+                        uint8_t* rowp = b_buf + (size_t)(j >> 1) * p.n_pad * 128 + (size_t)r * 128;
+                        const int c0 = (j & 1) * 4;
+                        mxfp4_fake_quant_block(reinterpret_cast<uint4*>(rowp + (((c0 + 0) ^ (r & 7)) << 4)),
+                                               reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)),
+                                               reinterpret_cast<uint4*>(rowp + (((c0 + 2) ^ (r & 7)) << 4)),
+                                               reinterpret_cast<uint4*>(rowp + (((c0 + 3) ^ (r & 7)) << 4)));
+                    }
+                }
+                fence_proxy_async_smem();   // generic stores, read by the tensor core
+                named_bar_sync(2, 128);
+                if (dq == 0 && ok) mbar_arrive(&bars->b_ready);
+                b_phase ^= 1u;
+                cur_unit = u;
+            }
+            ok = ok && mbar_wait(&bars->empty_a[astage], aphase ^ 1u, p.status);
+            ok = ok && mbar_wait(&bars->full_c[cstage], cphase, p.status);
+            if (ok) {
+                const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
+                const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
+                const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
+                uint8_t* arow = a_ring + (size_t)astage * a_bytes + (size_t)dq * 128;
+                for (int q4 = 0; q4 < p.Di / 32; ++q4) {
+                    // 16 code bytes = 32 elements = one scale block; rows start 64 bytes apart, so
+                    // lanes take the blocks in rotated order to spread the shared-memory banks
+                    const int qb = (q4 + dq) % (p.Di / 32);
+                    const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
+                    const float sc = e8m0_value(srow[qb]);
+                    const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {   // 8 elements -> one 16-byte chunk of the tile
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t byte = (cw[h] >> (8 * j)) & 0xFFu;
+                            const float lo = e2m1_value(byte & 0xFu) * sc, hi = e2m1_value(byte >> 4) * sc;
+                            pk[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                        }
+                        const int ch = qb * 4 + h;                 // chunk of 8 elements along Di
+                        *reinterpret_cast<uint4*>(arow + (size_t)(ch >> 3) * kTileKeys * 128 +
+                                                  (size_t)(((ch & 7) ^ (dq & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            } else {
+                atomicExch(&bars->abort, 1u);
+            }
+            fence_proxy_async_smem();   // generic stores, read by the tensor core
+            __syncwarp();
+            if (lane == 0 && ok) {
+                mbar_arrive(&bars->full_a[astage]);
+                mbar_arrive(&bars->empty_c[cstage]);
+            }
+            if (++astage == p.stages) {
+                astage = 0;
+                aphase ^= 1u;
+            }
+            if (++cstage == p.c_stages) {
+                cstage = 0;
+                cphase ^= 1u;
+            }
+            advance(p, u, tile);
         }
     } else {
         // ---------------------------------------------------------------- epilogue
@@ -381,11 +540,13 @@ int idx_scores_pick_nq(int Hi, int s) {
 size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
     const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t b_bytes = (size_t)p.n_pad * p.Di * 2;
-    return 1024 + p.stages * a_bytes + b_bytes + sizeof(Barriers) + 256 * 4 + 256 * 4;
+    const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
+    return 1024 + p.stages * a_bytes + b_bytes + (p.fp4 ? p.c_stages : 0) * c_bytes + sizeof(Barriers) + 256 * 4 +
+           256 * 4;
 }
 
-cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const IdxScoresParams& p,
-                              int num_sms, cudaStream_t stream) {
+cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_s,
+                              const IdxScoresParams& p, int num_sms, cudaStream_t stream) {
     size_t smem = idx_scores_smem_bytes(p);
     // p.ctas_per_sm CTAs share an SM (together they fit the SM's 512 TMEM columns); pad shared
     // memory so no more than that many become resident
@@ -395,10 +556,10 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
     cudaError_t err = cudaSuccess;
 #define STI_LAUNCH_HI(HV)                                                                              \
     case HV: {                                                                                         \
-        auto kern = idx_scores_kernel<HV>;                                                             \
+        auto kern = p.fp4 ? idx_scores_kernel<HV, true> : idx_scores_kernel<HV, false>;               \
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
         if (err != cudaSuccess) return err;                                                            \
-        kern<<<grid, kThreads, smem, stream>>>(tm_a, tm_b, p);                                         \
+        kern<<<grid, p.fp4 ? kThreadsFp4 : kThreads, smem, stream>>>(tm_a, tm_b, tm_s, p);            \
         return cudaGetLastError();                                                                     \
     }
     switch (p.Hi) {

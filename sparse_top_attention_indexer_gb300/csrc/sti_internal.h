@@ -30,10 +30,13 @@ struct IdxScoresParams {
     int stages;             // A pipeline depth
     int ctas_per_sm;        // 2 when two CTAs' TMEM fits one SM (decode), else 1
     int total_units;        // B * QT
+    int fp4;                // keys stored as MXFP4 (codes + E8M0 scales) and queries quantised to MXFP4
+    int c_stages;           // fp4: staging depth of the packed key tiles
 };
-// tm_a: index keys, tm_b: index queries.
-cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const IdxScoresParams& p,
-                              int num_sms, cudaStream_t stream);
+// tm_a: index keys (bf16; fp4: their E2M1 codes, uint8 [Di/2] per key), tm_b: index queries,
+// tm_s: fp4 only, the E8M0 scales viewed as rows of 16 bytes.
+cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_s,
+                              const IdxScoresParams& p, int num_sms, cudaStream_t stream);
 int idx_scores_pick_nq(int Hi, int s);
 size_t idx_scores_smem_bytes(const IdxScoresParams& p);
 

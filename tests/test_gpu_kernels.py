@@ -96,6 +96,33 @@ def test_idx_scores(sti, orc, b, s, Hi, Di, n_cols, sps, ratio):
 # ----------------------------------------------------------------- top-k (same fp32 input on both sides)
 
 
+@pytest.mark.parametrize("b,s,Hi,Di,n_cols,sps", [
+    (3, 1, 32, 128, 1500, [6000, 399, 5999]),     # decode: one query per unit, ragged visibility
+    (1, 40, 32, 128, 300, [0]),                   # prefill: 8 queries per unit
+    (2, 3, 8, 64, 700, [2799, 100]),
+    (1, 70, 4, 64, 200, [0]),                     # 64 queries per unit, several units
+])
+def test_idx_scores_mxfp4(sti, orc, b, s, Hi, Di, n_cols, sps):
+    """MXFP4 keys dequantised in shared memory and queries quantised in the kernel equal the
+    oracle's scores over the decoded values (OCP MXFP4 reading of fp4_act_quant)."""
+    import torch
+
+    rng = rng_for(790 + Di, n_cols)
+    sp = np.broadcast_to(np.asarray(sps, np.int32), (b,)).copy()
+    iq = to_bf16_bits(rng.standard_normal((b, s, Hi, Di)) * np.exp2(rng.integers(-3, 4, size=(b, s, Hi, 1))))
+    cap = (n_cols + 40 + 7) // 8 * 8      # scale rows per batch a multiple of 16 bytes
+    codes = rng.integers(0, 256, size=(b, cap, Di // 2), dtype=np.uint8)
+    scales = rng.integers(115, 135, size=(b, cap, Di // 32), dtype=np.uint8)
+    w = to_bf16_bits(rng.standard_normal((b, s, Hi)))
+    c = Di ** -0.5 * Hi ** -0.5
+    ref = orc.index_score_mxfp4(iq, codes, scales, w, c, sp, n_cols, 4)
+    ws = sti.workspace(256)
+    got = sti.idx_scores_mxfp4(to_dev(iq), to_dev_any(codes), to_dev_any(scales), to_dev(w), c, to_dev_any(sp),
+                               n_cols, 4, ws=ws).cpu().numpy()
+    assert sti.read_device_status(ws) == 0
+    check_scores(got, ref)
+
+
 @pytest.mark.parametrize("b,s,n_cols,k,sps,ratio", [
     (2, 1, 16384, 512, [65535, 40000], 4),
     (4, 1, 1000, 512, [3999, 2047, 2048, 7], 4),

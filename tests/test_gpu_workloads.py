@@ -1,8 +1,8 @@
 """GPU parity on the named workloads at full size, in the launch configuration bench.py times
 (its GpuPath), against the CPU oracle on the same seeded inputs.
 
-Decode workloads (b=32 ctx 65536 at compression ratios 4, 2 and 1; b=8 ctx 131072 with planted
-keys; b=64 ragged with three reuse layers) and the tiny prefill are compared element by element
+Decode workloads (b=32 ctx 65536 at compression ratios 4, 2 and 1, and with MXFP4 index keys;
+b=8 ctx 131072 with planted keys; b=64 ragged with three reuse layers) and the tiny prefill are compared element by element
 on every output.  The 8192-query prefill and the 2048-query chunk continuing a sequence at
 position 6144 are compared on a spread of sampled query rows (the oracle computes each one on
 its own), and on properties that hold for every row at full size."""
@@ -39,7 +39,7 @@ def _run(shape, data, device):
     return path
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 5, 6, 7])
+@pytest.mark.parametrize("n", [1, 2, 4, 5, 6, 7, 9])
 def test_workload_full(gpu, orc, n):
     shape = workloads.config(n)
     data = workloads.make(shape)
@@ -47,7 +47,11 @@ def test_workload_full(gpu, orc, n):
     sp = data["start_pos"]
     W, width = shape.window, shape.win_width
     # scores, every row and column
-    ref_s = orc.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
+    if shape.fp4_keys:
+        ref_s = orc.index_score_mxfp4(data["iq"], data["ik_codes"], data["ik_scales"], data["w"], shape.index_scale, sp,
+                                      shape.n_cols, shape.ratio)
+    else:
+        ref_s = orc.index_score(data["iq"], data["ik"], data["w"], shape.index_scale, sp, shape.n_cols, shape.ratio)
     got_s = path.scores_view().cpu().numpy()
     worst = check_scores(got_s, ref_s)
     # indices: window part exact, compressed part the same set outside the boundary band

@@ -83,6 +83,7 @@ class Shape:
     rms_keys: bool = False     # RMS-normalise index key rows
     planted: bool = False      # planted rank-one score bias on 1% of keys
     n_layers: int = 1          # attention layers sharing one index pass (reuse layers)
+    fp4_keys: bool = False     # index keys stored as MXFP4 (E2M1 codes + E8M0 scales)
     seed: int = 0
 
     @property
@@ -129,7 +130,7 @@ class Shape:
 def config(n: int) -> Shape:
     """The named workloads: 1-5 as listed in the design notes, 6 and 7 the decode workload at
     compression ratios 2 and 1 (32768 and 65536 index rows per sequence), 8 a prefill chunk
-    that continues its sequence."""
+    that continues its sequence, 9 workload 2 with MXFP4 index keys."""
     seed = 1000 + n
     if n == 1:
         return Shape("tiny_prefill_s256_h4_d64", b=1, s=256, start_pos=np.zeros(1, np.int32), h=4, d=64, rd=16,
@@ -148,6 +149,9 @@ def config(n: int) -> Shape:
         n_cols = int(lengths.max() // 4)
         return Shape("mixed_serving_b64_ctx1k-64k", b=64, s=1, start_pos=sp, n_cols=n_cols, rms_keys=True,
                      n_layers=4, seed=seed)
+    if n == 9:   # workload 2 with MXFP4 index keys
+        return Shape("decode_b32_ctx65536_mxfp4", b=32, s=1, start_pos=np.full(32, 65535, np.int32), n_cols=16384,
+                     fp4_keys=True, seed=seed)
     if n == 8:   # a prefill chunk of 2048 queries continuing a sequence at position 6144
         return Shape("chunked_prefill_s2048_at6144", b=1, s=2048, start_pos=np.full(1, 6144, np.int32), n_cols=2048,
                      seed=seed)
@@ -282,8 +286,27 @@ def make(shape: Shape, beta: float | None = None) -> dict:
         comp[bi, :n] = to_bf16_bits(c)
         ik[bi, :n] = to_bf16_bits(k)
     out["comp"] = comp
-    out["ik"] = ik
+    if shape.fp4_keys:
+        # MXFP4 keys are drawn directly as codes and scales: magnitude codes 0..7 with fixed
+        # frequencies shaped like a half-normal on the E2M1 grid, random signs, and scale
+        # bytes 125..127 (block scales 1/4 .. 1)
+        rc = rng_for(sd, 8)
+        mag = rc.choice(8, size=(b, shape.n_cols, shape.Di), p=FP4_CODE_FREQ).astype(np.uint8)
+        sgn = (rc.random(size=mag.shape) < 0.5).astype(np.uint8) << 3
+        nib = np.where(mag > 0, mag | sgn, 0).astype(np.uint8)
+        codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+        scales = rc.choice(np.array([125, 126, 127], np.uint8), size=(b, shape.n_cols, shape.Di // 32),
+                           p=[0.2, 0.7, 0.1])
+        for bi in range(b):   # rows past a sequence's visible count stay zero, as the bf16 keys do
+            codes[bi, int(vis[bi]):] = 0
+            scales[bi, int(vis[bi]):] = 0
+        out["ik_codes"], out["ik_scales"] = codes, scales
+    else:
+        out["ik"] = ik
     return out
+
+
+FP4_CODE_FREQ = [0.10, 0.18, 0.17, 0.15, 0.13, 0.14, 0.09, 0.04]   # E2M1 magnitude codes 0..7
 
 
 def index_lists(rng: np.random.Generator, b: int, s: int, k: int, n_rows: int, masked_frac: float = 0.1,
