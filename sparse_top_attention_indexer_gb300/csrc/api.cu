@@ -205,10 +205,20 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     p.ctas_per_sm = p.tmem_cols <= 256 ? 2 : 1;
     const size_t budget = p.ctas_per_sm == 2 ? 104 * 1024 : 200 * 1024;
     p.fp4 = fp4 ? 1 : 0;
-    // MXFP4: four stages of packed tiles (a quarter of the bytes) feed two dequantised bf16 tiles
-    p.c_stages = fp4 ? 4 : 0;
+    if (fp4) {
+        p.k_codes = fp4->codes;
+        p.k_codes_bstride = fp4->codes_bstride;
+        p.k_scales = fp4->scales;
+        p.k_scales_bstride = fp4->scales_bstride;
+    }
+    // MXFP4: three stages of packed tiles (a quarter of the bytes) feed two decoded tiles (E5M2, or
+    // bf16 when a block's scale is out of E5M2's exact range); with Di == 128 the queries are held
+    // a second time as E5M2
+    p.c_stages = fp4 ? 3 : 0;
+    p.f8 = (fp4 && Di == 128) ? 1 : 0;
     const size_t c_total = fp4 ? (size_t)p.c_stages * ((size_t)128 * Di / 2 + (size_t)128 * Di / 32) : 0;
-    int stages = (int)((budget - b_bytes - c_total) / a_bytes);
+    const size_t b8_bytes = p.f8 ? (size_t)p.n_pad * 128 : 0;
+    int stages = (int)((budget - b_bytes - b8_bytes - c_total) / a_bytes);
     if (stages > (fp4 ? 3 : 8)) stages = fp4 ? 3 : 8;
     if (stages < 2) stages = 2;
     p.stages = stages;

@@ -27,7 +27,8 @@ namespace {
 
 constexpr int kTileKeys = 128;
 constexpr int kThreads = 192;      // bf16 keys: producer, MMA, 4 epilogue warps
-constexpr int kThreadsFp4 = 320;   // MXFP4 keys: + 4 warps that dequantise keys and quantise queries
+constexpr int kThreadsFp4 = 448;   // MXFP4 keys: + 8 warps that dequantise keys and quantise queries
+constexpr int kDqWarps = 8;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
@@ -40,16 +41,21 @@ struct __align__(8) Barriers {
     uint64_t full_b, empty_b;
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
+    uint32_t fmt[kMaxStages];       // MXFP4: 1 when the stage holds E5M2 keys, 0 for bf16
     uint32_t tmem_base;
     uint32_t abort;
 };
 
-__device__ __forceinline__ int unit_tiles(const IdxScoresParams& p, int u) {
+// Keys visible to the last (so to any) query of unit u.
+__device__ __forceinline__ int unit_vis(const IdxScoresParams& p, int u) {
     const int b = u / p.QT, qt = u - b * p.QT;
     const int t_last = min(p.s, (qt + 1) * p.nq) - 1;
-    int vis = (__ldg(p.start_pos + b) + t_last + 1) / p.ratio;
-    vis = max(0, min(vis, p.n_cols));
-    return (vis + kTileKeys - 1) / kTileKeys;
+    const int vis = (__ldg(p.start_pos + b) + t_last + 1) / p.ratio;
+    return max(0, min(vis, p.n_cols));
+}
+
+__device__ __forceinline__ int unit_tiles(const IdxScoresParams& p, int u) {
+    return (unit_vis(p, u) + kTileKeys - 1) / kTileKeys;
 }
 
 // Warp-cooperative: total number of compute tiles over all units.
@@ -93,12 +99,52 @@ __device__ void locate(const IdxScoresParams& p, int g, int& u_out, int& tile_ou
     tile_out = 0;
 }
 
-__device__ __forceinline__ void advance(const IdxScoresParams& p, int& u, int& tile) {
-    ++tile;
-    while (u < p.total_units && tile >= unit_tiles(p, u)) {
-        ++u;
-        tile = 0;
+// Warp-cooperative: this CTA's contiguous range [g0, g1) of the flattened tile list and the
+// (unit, tile) of g0.  Up to 32 units (a decode batch) take one round of start_pos reads.
+__device__ void cta_range(const IdxScoresParams& p, int& g0, int& g1, int& u_out, int& tile_out) {
+    if (p.total_units <= 32) {
+        const int lane = threadIdx.x & 31;
+        const int n = lane < p.total_units ? unit_tiles(p, lane) : 0;
+        int inc = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int T = __shfl_sync(kFull, inc, 31);
+        g0 = (int)(((int64_t)T * blockIdx.x) / gridDim.x);
+        g1 = (int)(((int64_t)T * (blockIdx.x + 1)) / gridDim.x);
+        const unsigned m = __ballot_sync(kFull, inc > g0);
+        const int l = m ? __ffs(m) - 1 : 31;
+        const int excl = __shfl_sync(kFull, inc - n, l);
+        u_out = m ? l : p.total_units;
+        tile_out = m ? g0 - excl : 0;
+        return;
     }
+    const int T = total_tiles(p);
+    g0 = (int)(((int64_t)T * blockIdx.x) / gridDim.x);
+    g1 = (int)(((int64_t)T * (blockIdx.x + 1)) / gridDim.x);
+    locate(p, g0, u_out, tile_out);
+}
+
+__device__ __forceinline__ int unit_tiles_at(const IdxScoresParams& p, int u) {
+    return u < p.total_units ? unit_tiles(p, u) : 0;
+}
+
+// Next (unit, tile) of the flattened list.  n caches the current unit's tile count and n_next the
+// following unit's, read one unit ahead: a step touches global memory only when it enters a new
+// unit, and then never waits for that read (a per-tile read of start_pos sat on the MMA issuer's
+// critical path, about 0.4 us a tile).
+__device__ __forceinline__ void advance(const IdxScoresParams& p, int& u, int& tile, int& n, int& n_next) {
+    if (++tile < n) return;
+    tile = 0;
+    ++u;
+    n = n_next;
+    while (u < p.total_units && n == 0) {
+        ++u;
+        n = unit_tiles_at(p, u);
+    }
+    n_next = unit_tiles_at(p, u + 1);
 }
 
 // K-major operand descriptor of K-step kk (16 bf16) for a tile of `rows` rows stored as column
@@ -124,43 +170,108 @@ __device__ __forceinline__ float e2m1_value(uint32_t nib) {
     return __uint_as_float(bits | ((nib & 8u) << 28));
 }
 
+// Eight E2M1 nibbles (one 32-bit word: byte j holds elements 2j (low nibble) and 2j+1) -> four
+// bf16x2 words of the values times 2^X, for scale bytes e8 in [2, 252] (X = e8 - 127): byte
+// permutes look up each magnitude's bf16 bytes (a table of the eight E2M1 magnitudes), the sign
+// bits move into place, and X is added to the exponent field of every non-zero half.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t cw, uint32_t expadd, uint32_t (&o)[4]) {
+    const uint32_t lo = cw & 0x07070707u, hi = (cw >> 4) & 0x07070707u;   // magnitude codes per byte
+    const uint32_t yl = lo | (lo >> 4), yh = hi | (hi >> 4);
+    const uint32_t sel_l = (yl & 0xFFu) | ((yl >> 8) & 0xFF00u);            // 4 selector nibbles
+    const uint32_t sel_h = (yh & 0xFFu) | ((yh >> 8) & 0xFF00u);
+    // bf16 of 0, .5, 1, 1.5 | 2, 3, 4, 6: high bytes 00 3F 3F 3F | 40 40 40 40, low bytes 00 00 80 C0 | 00 40 80 C0
+    uint32_t hl = __byte_perm(0x3F3F3F00u, 0x40404040u, sel_l);
+    const uint32_t ll = __byte_perm(0xC0800000u, 0xC0804000u, sel_l);
+    uint32_t hh = __byte_perm(0x3F3F3F00u, 0x40404040u, sel_h);
+    const uint32_t lh = __byte_perm(0xC0800000u, 0xC0804000u, sel_h);
+    hl |= (cw << 4) & 0x80808080u;   // sign of the low nibble -> top bit of its high byte
+    hh |= cw & 0x80808080u;          // sign of the high nibble
+    const uint32_t t0 = __byte_perm(ll, hl, 0x5140u);   // elements 0 | 2 << 16
+    const uint32_t t1 = __byte_perm(lh, hh, 0x5140u);   // elements 1 | 3 << 16
+    const uint32_t t2 = __byte_perm(ll, hl, 0x7362u);   // elements 4 | 6 << 16
+    const uint32_t t3 = __byte_perm(lh, hh, 0x7362u);   // elements 5 | 7 << 16
+    o[0] = __byte_perm(t0, t1, 0x5410u);
+    o[1] = __byte_perm(t0, t1, 0x7632u);
+    o[2] = __byte_perm(t2, t3, 0x5410u);
+    o[3] = __byte_perm(t2, t3, 0x7632u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = __vadd2(o[k], expadd & __vcmpne2(o[k] & 0x7FFF7FFFu, 0u));
+}
+
 // E8M0 scale byte -> 2^(e - 127) (255 is NaN).
 __device__ __forceinline__ float e8m0_value(uint32_t e) {
     return e == 0u ? __uint_as_float(0x00400000u) : (e == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23));
 }
 
-// |x| / 2^X onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}: nearest, ties to the even code,
-// saturating at 6.
-__device__ __forceinline__ float e2m1_round(float a) {
-    return a <= 0.25f ? 0.f : a < 0.75f ? 0.5f : a <= 1.25f ? 1.f : a < 1.75f ? 1.5f
-         : a <= 2.5f ? 2.f : a < 3.5f ? 3.f : a <= 5.f ? 4.f : 6.f;
+// 2^e for e in [-149, 127], exactly.
+__device__ __forceinline__ float exp2i(int e) {
+    return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
-// One 32-element block of bf16 queries (four 16-byte chunks at c0..c3), quantised to MXFP4 and
-// decoded back in place (Indexer.forward's fp4_act_quant on q, read as OCP MXFP4: scale 2^X with
-// X = floor(log2 max|x|) - 2).  The decoded values are exact in bf16.
-__device__ __forceinline__ void mxfp4_fake_quant_block(uint4* c0, uint4* c1, uint4* c2, uint4* c3) {
-    uint4 v[4] = {*c0, *c1, *c2, *c3};
-    uint32_t* w = reinterpret_cast<uint32_t*>(v);
+// a = |x| / 2^X onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}: the index 0..7 of the
+// nearest one, ties to the even code, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1_index(float a) {
+    return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
+           (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.f);
+}
+
+// E5M2 bytes of the eight E2M1 magnitudes times 2^X as a byte-permute table (t0: 0, .5, 1, 1.5;
+// t1: 2, 3, 4, 6).  For X in [-13, 13] every such product is a normal E5M2 number (exponent field
+// 1..30), so X only adds 4X to each non-zero byte, without carries between bytes.
+__device__ __forceinline__ void e5m2_table(int X, uint32_t& t0, uint32_t& t1) {
+    t0 = 0x3E3C3800u + (uint32_t)X * 0x04040400u;
+    t1 = 0x46444240u + (uint32_t)X * 0x04040404u;
+}
+
+// Eight E2M1 codes (nibble i of cw = element i) -> their E5M2 bytes (element i in byte i of the
+// pair) through the table of e5m2_table.  The sign comes from a second permute that takes each
+// whole nibble as its selector: a set sign bit replicates the top bit of 0x7F (0x00), a clear one
+// copies 0x7F; adding 1 per byte gives 0x01 or 0x80, and its complement's top bit is the sign.
+__device__ __forceinline__ uint2 e2m1x8_to_e5m2(uint32_t cw, uint32_t t0, uint32_t t1) {
+    const uint32_t hi = cw >> 16;
+    const uint32_t m0 = prmt(t0, t1, cw & 0x7777u), m1 = prmt(t0, t1, hi & 0x7777u);
+    const uint32_t n0 = prmt(0x7F7F7F7Fu, 0x7F7F7F7Fu, cw) + 0x01010101u;
+    const uint32_t n1 = prmt(0x7F7F7F7Fu, 0x7F7F7F7Fu, hi) + 0x01010101u;
+    return make_uint2(m0 | (~n0 & 0x80808080u), m1 | (~n1 & 0x80808080u));
+}
+
+// One 16-byte chunk (8 bf16 queries) of a 32-element block whose four chunks sit in lanes 4k..4k+3
+// of the warp: the block is quantised to MXFP4 and decoded back in place (Indexer.forward's
+// fp4_act_quant on q, read as OCP MXFP4: scale 2^X with X = floor(log2 max|x|) - 2); the decoded
+// values are exact in bf16.  e5 (if not null) receives the same eight values as E5M2 bytes.
+// Returns whether they are exact in E5M2: X in [-13, 13], or an all-zero block.
+__device__ __forceinline__ bool mxfp4_fake_quant_chunk(uint4* chunk, uint2* e5) {
+    const uint4 v = *chunk;
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4; ++i) {
         amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
         amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
     }
-    const int X = amax > 0.f ? max(-127, min(127, ilogbf(amax) - 2)) : -127;
-    const float sc = ldexpf(1.f, X), inv = ldexpf(1.f, -X);
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    // floor(log2 amax) is the exponent field of a normal amax; zero and subnormals are rare
+    const int eb = (int)(__float_as_uint(amax) >> 23);
+    const int X = eb > 0 ? max(-127, min(127, eb - 129)) : (amax > 0.f ? max(-127, ilogbf(amax) - 2) : -127);
+    const float sc = exp2i(X), inv = exp2i(-X);
+    uint32_t t0, t1;
+    e5m2_table(max(-13, min(13, X)), t0, t1);
+    uint32_t e[2] = {0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
-        const float ql = copysignf(e2m1_round(fabsf(lo) * inv), lo) * sc;
-        const float qh = copysignf(e2m1_round(fabsf(hi) * inv), hi) * sc;
+        const uint32_t il = e2m1_index(fabsf(lo) * inv), ih = e2m1_index(fabsf(hi) * inv);
+        const float ql = copysignf(e2m1_value(il), lo) * sc;
+        const float qh = copysignf(e2m1_value(ih), hi) * sc;
         w[i] = (__float_as_uint(ql) >> 16) | (__float_as_uint(qh) & 0xFFFF0000u);
+        const uint32_t bl = prmt(t0, t1, il) | ((__float_as_uint(lo) >> 24) & 0x80u);
+        const uint32_t bh = prmt(t0, t1, ih) | ((__float_as_uint(hi) >> 24) & 0x80u);
+        e[i >> 1] |= (bl | (bh << 8)) << (16 * (i & 1));
     }
-    *c0 = v[0];
-    *c1 = v[1];
-    *c2 = v[2];
-    *c3 = v[3];
+    *chunk = make_uint4(w[0], w[1], w[2], w[3]);
+    if (e5 != nullptr) *e5 = make_uint2(e[0], e[1]);
+    return amax == 0.f || (X >= -13 && X <= 13);
 }
 
 template <int HI, bool FP4>
@@ -182,7 +293,10 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     // MXFP4: packed key tiles, [128 keys x Di/2 code bytes | 128 keys x Di/32 scale bytes] per stage
     const int c_code_bytes = kTileKeys * p.Di / 2;
     const int c_bytes = FP4 ? c_code_bytes + kTileKeys * p.Di / 32 : 0;
-    uint8_t* c_ring = b_buf + b_bytes;
+    // MXFP4 with Di == 128: the quantised queries again as E5M2, rows of 128 bytes (128-byte swizzle)
+    uint8_t* b8 = b_buf + b_bytes;
+    const int b8_bytes = (FP4 && p.f8) ? p.n_pad * 128 : 0;
+    uint8_t* c_ring = b8 + b8_bytes;
     Barriers* bars = reinterpret_cast<Barriers*>(c_ring + (size_t)(FP4 ? p.c_stages : 0) * c_bytes);
     float* w_s = reinterpret_cast<float*>(bars + 1);   // [nq * HI], pre-multiplied by c
     int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq]
@@ -191,13 +305,13 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&bars->full_a[i], FP4 ? 4 : 1);   // MXFP4: the four dequantising warps
+            mbar_init(&bars->full_a[i], FP4 ? kDqWarps : 1);   // MXFP4: the dequantising warps
             mbar_init(&bars->empty_a[i], 1);
         }
         if (FP4) {
             for (int i = 0; i < p.c_stages; ++i) {
                 mbar_init(&bars->full_c[i], 1);
-                mbar_init(&bars->empty_c[i], 4);
+                mbar_init(&bars->empty_c[i], kDqWarps);
             }
             mbar_init(&bars->b_ready, 1);
         }
@@ -215,17 +329,20 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         tmem_alloc(&bars->tmem_base, (uint32_t)p.tmem_cols);
         tmem_relinquish();
     }
+    if (FP4) {   // rows a partial last tile does not fill keep zeros (never scored, but finite)
+        uint4* c4 = reinterpret_cast<uint4*>(c_ring);
+        for (int i = threadIdx.x; i < p.c_stages * c_bytes / 16; i += kThreadsFp4) c4[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
     // this CTA's contiguous range of the flattened (unit, tile) list
-    const int T = total_tiles(p);
-    const int g0 = (int)(((int64_t)T * blockIdx.x) / gridDim.x);
-    const int g1 = (int)(((int64_t)T * (blockIdx.x + 1)) / gridDim.x);
-    int u, tile;
-    locate(p, g0, u, tile);
+    int g0, g1, u, tile;
+    cta_range(p, g0, g1, u, tile);
+    int un = unit_tiles_at(p, u), un_next = unit_tiles_at(p, u + 1);
     const int ncb = p.Di >= 64 ? p.Di / 64 : 1;  // column blocks per row
     const int box_inner = p.Di >= 64 ? 64 : p.Di;
 
@@ -266,10 +383,18 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                     // key viewed as rows of 16 bytes (Di/4 rows per tile)
                     ok = ok && mbar_wait(&bars->empty_c[stage], phase ^ 1u, p.status);
                     if (ok) {
+                        // a tile's packed keys are contiguous: two bulk copies, the keys past n_cols
+                        // left out (their rows keep finite earlier contents and are never scored)
                         uint8_t* dst = c_ring + (size_t)stage * c_bytes;
-                        mbar_arrive_expect_tx(&bars->full_c[stage], (uint32_t)c_bytes);
-                        tma_load_3d(dst, &tm_a, &bars->full_c[stage], 0, tile * kTileKeys, b);
-                        tma_load_3d(dst + c_code_bytes, &tm_s, &bars->full_c[stage], 0, tile * (p.Di / 4), b);
+                        const int nk = min(kTileKeys, p.n_cols - tile * kTileKeys);
+                        const uint32_t cb_bytes = (uint32_t)(nk * (p.Di / 2));
+                        const uint32_t sb_bytes = (uint32_t)((nk * (p.Di / 32) + 15) & ~15);
+                        mbar_arrive_expect_tx(&bars->full_c[stage], cb_bytes + sb_bytes);
+                        bulk_load(dst, p.k_codes + (size_t)b * p.k_codes_bstride + (size_t)tile * kTileKeys * (p.Di / 2),
+                                  cb_bytes, &bars->full_c[stage]);
+                        bulk_load(dst + c_code_bytes,
+                                  p.k_scales + (size_t)b * p.k_scales_bstride + (size_t)tile * kTileKeys * (p.Di / 32),
+                                  sb_bytes, &bars->full_c[stage]);
                     }
                 } else {
                     ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
@@ -294,7 +419,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 stage = 0;
                 phase ^= 1u;
             }
-            advance(p, u, tile);
+            advance(p, u, tile, un, un_next);
         }
         if (lane == 0) {
             for (int st = 0; st < n_st; ++st)
@@ -305,6 +430,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idesc = idesc_bf16_f32(128, p.n_pad, false, false);
+        const uint32_t idesc8 = idesc_e5m2_f32(128, p.n_pad);
         const int ksteps = p.Di / 16;
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0, b_phase = 0;
@@ -323,9 +449,18 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                     const uint32_t a_base = smem_u32(a_ring + (size_t)stage * a_bytes);
                     const uint32_t b_base = smem_u32(b_buf);
                     const uint32_t d_tmem = tmem + (uint32_t)(acc * p.n_alloc);
-                    for (int kk = 0; kk < ksteps; ++kk)
-                        umma_bf16(d_tmem, kmajor_desc(a_base, kk, p.Di, kTileKeys),
-                                  kmajor_desc(b_base, kk, p.Di, p.n_pad), idesc, kk > 0 ? 1u : 0u);
+                    if (FP4 && *(volatile uint32_t*)&bars->fmt[stage] != 0u) {
+                        // E5M2 keys and queries: rows of 128 bytes, K = 32 per instruction, so the
+                        // descriptors step like a 64-wide bf16 tile
+                        const uint32_t b8_base = smem_u32(b8);
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f8f6f4(d_tmem, kmajor_desc(a_base, kk, 64, kTileKeys),
+                                        kmajor_desc(b8_base, kk, 64, p.n_pad), idesc8, kk > 0 ? 1u : 0u);
+                    } else {
+                        for (int kk = 0; kk < ksteps; ++kk)
+                            umma_bf16(d_tmem, kmajor_desc(a_base, kk, p.Di, kTileKeys),
+                                      kmajor_desc(b_base, kk, p.Di, p.n_pad), idesc, kk > 0 ? 1u : 0u);
+                    }
                     umma_commit(&bars->empty_a[stage]);
                     umma_commit(&bars->acc_full[acc]);
                 } else {
@@ -342,7 +477,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            advance(p, u, tile);
+            advance(p, u, tile, un, un_next);
         }
         if (lane == 0) {  // every MMA this thread issued has finished before TMEM is freed
             umma_commit(&bars->mma_done);
@@ -350,58 +485,107 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         }
     } else if (FP4 && warp >= 6) {
         // ---------------------------------------------------------------- MXFP4 keys and queries
-        // Thread dq owns key row dq of every tile: its Di/2 code bytes and Di/32 scale bytes become
-        // Di bf16 values (exact: an E2M1 value times a power of two) in the 128-byte-swizzled tile
-        // the MMA reads.  At each new unit the four warps first quantise the unit's queries in
-        // place (32-element blocks of every query row), as the forward pass quantises q.
-        const int dq = threadIdx.x - 192;               // 0..127
+        // At each new unit the eight warps first quantise the unit's queries in place (32-element
+        // blocks of every query row, four lanes to a block), as the forward pass quantises q, and
+        // with Di == 128 also write them as E5M2.  Then threads dq and dq + 128 own key row dq of
+        // every tile, half of its scale blocks each.  When the unit's queries and every scale block
+        // of the tile's visible keys have X in [-13, 13], each E2M1 code times 2^X is an exact
+        // E5M2 number: the row becomes 128 E5M2 bytes (kind::f8f6f4, half the bytes and MMAs of
+        // bf16).  Otherwise the Di/2 code bytes and Di/32 scale bytes become Di bf16 values (also
+        // exact).  Either way the tile lands 128-byte-swizzled where the MMA reads it, and the
+        // stage's fmt word tells the MMA which it is.
+        const int dq_t = threadIdx.x - 192;             // 0..255
+        const int dq = dq_t & 127;                      // key row of a tile
+        const int half = dq_t >> 7;                     // this thread's half of the row's scale blocks
         const int nblk = p.Di / 32;
         int astage = 0, cstage = 0;
         uint32_t aphase = 0, cphase = 0, b_phase = 0;
-        int cur_unit = -1;
+        int cur_unit = -1, vis_unit = 0;
+        bool q_f8 = false;
         for (int g = g0; g < g1; ++g) {
             bool ok = !aborted();
             if (u != cur_unit) {
+                vis_unit = unit_vis(p, u);
                 ok = ok && mbar_wait(&bars->full_b, b_phase, p.status);
+                ok = __all_sync(kFull, ok);   // warp-uniform: the quantiser shuffles within the warp
+                bool q_in = true;
                 if (ok) {
-                    for (int i = dq; i < p.n_pad * nblk; i += 128) {
-                        const int r = i / nblk, j = i - (i / nblk) * nblk;
+                    // n_pad * nblk * 4 is a multiple of 32: a warp's lanes run the same trips
+                    for (int i = dq_t; i < p.n_pad * nblk * 4; i += 32 * kDqWarps) {
+                        const int blk = i >> 2, t4 = i & 3;
+                        const int r = blk / nblk, j = blk - (blk / nblk) * nblk;
                         uint8_t* rowp = b_buf + (size_t)(j >> 1) * p.n_pad * 128 + (size_t)r * 128;
-                        const int c0 = (j & 1) * 4;
-                        mxfp4_fake_quant_block(reinterpret_cast<uint4*>(rowp + (((c0 + 0) ^ (r & 7)) << 4)),
-                                               reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4)),
-                                               reinterpret_cast<uint4*>(rowp + (((c0 + 2) ^ (r & 7)) << 4)),
-                                               reinterpret_cast<uint4*>(rowp + (((c0 + 3) ^ (r & 7)) << 4)));
+                        const int c = (j & 1) * 4 + t4;
+                        uint2* e5 = p.f8 ? reinterpret_cast<uint2*>(b8 + (size_t)r * 128 +
+                                                                    ((((2 * j + (t4 >> 1)) ^ (r & 7))) << 4) +
+                                                                    (t4 & 1) * 8)
+                                         : nullptr;
+                        q_in = mxfp4_fake_quant_chunk(reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)), e5) && q_in;
                     }
                 }
                 fence_proxy_async_smem();   // generic stores, read by the tensor core
-                named_bar_sync(2, 128);
-                if (dq == 0 && ok) mbar_arrive(&bars->b_ready);
+                q_f8 = named_bar_and(2, 32 * kDqWarps, q_in) && p.f8;
+                if (dq_t == 0 && ok) mbar_arrive(&bars->b_ready);
                 b_phase ^= 1u;
                 cur_unit = u;
             }
             ok = ok && mbar_wait(&bars->empty_a[astage], aphase ^ 1u, p.status);
             ok = ok && mbar_wait(&bars->full_c[cstage], cphase, p.status);
-            if (ok) {
-                const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
-                const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
-                const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
-                uint8_t* arow = a_ring + (size_t)astage * a_bytes + (size_t)dq * 128;
-                for (int q4 = 0; q4 < p.Di / 32; ++q4) {
+            const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
+            const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
+            const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
+            uint8_t* arow = a_ring + (size_t)astage * a_bytes + (size_t)dq * 128;
+            // Every warp checks all 512 scale bytes of the tile (16 a lane: keys 4*lane .. 4*lane+3),
+            // so all eight reach the same decision without a barrier.  Keys no query of the unit
+            // sees may hold anything.  ok is warp-uniform here (the vote below needs every lane).
+            ok = __all_sync(kFull, ok);
+            bool f8 = false;
+            if (ok && q_f8) {
+                const uint4 sc4 = *reinterpret_cast<const uint4*>(cst + c_code_bytes + lane * 16);
+                const uint32_t sw[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+                bool in = true;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t r = __vcmpgeu4(sw[k], 0x72727272u) & __vcmpleu4(sw[k], 0x8C8C8C8Cu);  // 114..140
+                    in = in && (r == 0xFFFFFFFFu || tile * kTileKeys + lane * 4 + k >= vis_unit);
+                }
+                f8 = __all_sync(kFull, in);
+            }
+            if (ok && f8) {
+                for (int q4 = half; q4 < nblk; q4 += 2) {
+                    const int qb = (q4 + dq) & 3;   // rotated, as below; Di == 128 here
+                    const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
+                    uint32_t t0, t1;
+                    e5m2_table(max(-13, min(13, (int)srow[qb] - 127)), t0, t1);
+                    const uint2 o0 = e2m1x8_to_e5m2(cw4.x, t0, t1), o1 = e2m1x8_to_e5m2(cw4.y, t0, t1);
+                    const uint2 o2 = e2m1x8_to_e5m2(cw4.z, t0, t1), o3 = e2m1x8_to_e5m2(cw4.w, t0, t1);
+                    *reinterpret_cast<uint4*>(arow + (((2 * qb) ^ (dq & 7)) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+                    *reinterpret_cast<uint4*>(arow + (((2 * qb + 1) ^ (dq & 7)) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+                }
+            } else if (ok) {
+                for (int q4 = half; q4 < p.Di / 32; q4 += 2) {
                     // 16 code bytes = 32 elements = one scale block; rows start 64 bytes apart, so
                     // lanes take the blocks in rotated order to spread the shared-memory banks
                     const int qb = (q4 + dq) % (p.Di / 32);
                     const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
-                    const float sc = e8m0_value(srow[qb]);
+                    const uint32_t e8 = srow[qb];
+                    const bool fast = e8 >= 2u && e8 <= 252u;   // the exponent stays in the normal range
+                    const float sc = e8m0_value(e8);
+                    const uint32_t k16 = ((e8 - 127u) << 7) & 0xFFFFu;
+                    const uint32_t expadd = k16 | (k16 << 16);
                     const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {   // 8 elements -> one 16-byte chunk of the tile
                         uint32_t pk[4];
+                        if (fast) {
+                            e2m1x8_to_bf16(cw[h], expadd, pk);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t byte = (cw[h] >> (8 * j)) & 0xFFu;
-                            const float lo = e2m1_value(byte & 0xFu) * sc, hi = e2m1_value(byte >> 4) * sc;
-                            pk[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t byte = (cw[h] >> (8 * j)) & 0xFFu;
+                                const float lo = e2m1_value(byte & 0xFu) * sc, hi = e2m1_value(byte >> 4) * sc;
+                                pk[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                            }
                         }
                         const int ch = qb * 4 + h;                 // chunk of 8 elements along Di
                         *reinterpret_cast<uint4*>(arow + (size_t)(ch >> 3) * kTileKeys * 128 +
@@ -412,6 +596,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             } else {
                 atomicExch(&bars->abort, 1u);
             }
+            if (dq_t == 0) bars->fmt[astage] = f8 ? 1u : 0u;
             fence_proxy_async_smem();   // generic stores, read by the tensor core
             __syncwarp();
             if (lane == 0 && ok) {
@@ -426,7 +611,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 cstage = 0;
                 cphase ^= 1u;
             }
-            advance(p, u, tile);
+            advance(p, u, tile, un, un_next);
         }
     } else {
         // ---------------------------------------------------------------- epilogue
@@ -501,7 +686,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            advance(p, u, tile);
+            advance(p, u, tile, un, un_next);
         }
         // -inf for key tiles no query of a unit can see (units strided over CTAs)
         for (int uu = blockIdx.x; uu < p.total_units; uu += gridDim.x) {
@@ -541,8 +726,9 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
     const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t b_bytes = (size_t)p.n_pad * p.Di * 2;
     const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
-    return 1024 + p.stages * a_bytes + b_bytes + (p.fp4 ? p.c_stages : 0) * c_bytes + sizeof(Barriers) + 256 * 4 +
-           256 * 4;
+    const size_t b8_bytes = (p.fp4 && p.f8) ? (size_t)p.n_pad * 128 : 0;
+    return 1024 + p.stages * a_bytes + b_bytes + b8_bytes + (p.fp4 ? p.c_stages : 0) * c_bytes + sizeof(Barriers) +
+           256 * 4 + 256 * 4;
 }
 
 cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_s,

@@ -32,6 +32,11 @@ struct IdxScoresParams {
     int total_units;        // B * QT
     int fp4;                // keys stored as MXFP4 (codes + E8M0 scales) and queries quantised to MXFP4
     int c_stages;           // fp4: staging depth of the packed key tiles
+    int f8;                 // fp4 with Di == 128: tiles whose scales allow it run as E5M2 (kind::f8f6f4)
+    const uint8_t* k_codes;   // fp4: E2M1 codes [B, *, Di/2], batch stride in bytes
+    int64_t k_codes_bstride;
+    const uint8_t* k_scales;  // fp4: E8M0 scales [B, *, Di/32], batch stride in bytes
+    int64_t k_scales_bstride;
 };
 // tm_a: index keys (bf16; fp4: their E2M1 codes, uint8 [Di/2] per key), tm_b: index queries,
 // tm_s: fp4 only, the E8M0 scales viewed as rows of 16 bytes.

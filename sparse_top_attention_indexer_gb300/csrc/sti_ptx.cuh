@@ -100,6 +100,28 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n_threads) 
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n_threads) : "memory");
 }
 
+// Named barrier over n_threads that also returns the AND of every participant's predicate.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n_threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(n_threads)
+        : "memory");
+    return r != 0u;
+}
+
+// prmt.b32 in its default mode: byte i of the result is byte (c >> 4i) & 7 of {b, a}; when bit 3
+// of that selector nibble is set, the selected byte's top bit is replicated over the whole byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 // ------------------------------------------------------------------ TMA (tensor maps)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
@@ -233,6 +255,23 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E5M2 A/B and an fp32 accumulator: the
+// same fields as kind::f16's, where format 1 of A (bits 7-9) and B (bits 10-12) means E5M2.
+__host__ __device__ constexpr uint32_t idesc_e5m2_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] x B[smem], 8-bit operands (K = 32 per instruction); issued by one thread.
+__device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }

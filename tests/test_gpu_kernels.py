@@ -103,8 +103,9 @@ def test_idx_scores(sti, orc, b, s, Hi, Di, n_cols, sps, ratio):
     (1, 70, 4, 64, 200, [0]),                     # 64 queries per unit, several units
 ])
 def test_idx_scores_mxfp4(sti, orc, b, s, Hi, Di, n_cols, sps):
-    """MXFP4 keys dequantised in shared memory and queries quantised in the kernel equal the
-    oracle's scores over the decoded values (OCP MXFP4 reading of fp4_act_quant)."""
+    """MXFP4 keys decoded in shared memory (E5M2 with Di == 128, else bf16) and queries quantised
+    in the kernel equal the oracle's scores over the decoded values (OCP MXFP4 reading of
+    fp4_act_quant)."""
     import torch
 
     rng = rng_for(790 + Di, n_cols)
@@ -114,6 +115,43 @@ def test_idx_scores_mxfp4(sti, orc, b, s, Hi, Di, n_cols, sps):
     codes = rng.integers(0, 256, size=(b, cap, Di // 2), dtype=np.uint8)
     scales = rng.integers(115, 135, size=(b, cap, Di // 32), dtype=np.uint8)
     w = to_bf16_bits(rng.standard_normal((b, s, Hi)))
+    c = Di ** -0.5 * Hi ** -0.5
+    ref = orc.index_score_mxfp4(iq, codes, scales, w, c, sp, n_cols, 4)
+    ws = sti.workspace(256)
+    got = sti.idx_scores_mxfp4(to_dev(iq), to_dev_any(codes), to_dev_any(scales), to_dev(w), c, to_dev_any(sp),
+                               n_cols, 4, ws=ws).cpu().numpy()
+    assert sti.read_device_status(ws) == 0
+    check_scores(got, ref)
+
+
+@pytest.mark.parametrize("case", ["key_outliers", "query_outliers", "zero_blocks"])
+def test_idx_scores_mxfp4_scale_ranges(sti, orc, case):
+    """With Di == 128 a key tile runs as E5M2 only when every scale block of its visible keys, and
+    of the unit's queries, has X in [-13, 13]; other tiles (here: tiles with far-out key scales, or
+    a unit whose query block is 2^20 or 2^-30 times larger or smaller) are decoded to bf16.  Both
+    give the oracle's scores, in the same launch."""
+    b, Hi, Di, n_cols = 4, 32, 128, 1500
+    sps = [5999, 3000, 5999, 1200]
+    rng = rng_for(795, len(case))
+    sp = np.asarray(sps, np.int32)
+    q = rng.standard_normal((b, 1, Hi, Di))
+    cap = (n_cols + 7) // 8 * 8
+    codes = rng.integers(0, 256, size=(b, cap, Di // 2), dtype=np.uint8)
+    scales = rng.integers(118, 132, size=(b, cap, Di // 32), dtype=np.uint8)
+    if case == "key_outliers":
+        scales[0, 130, 1] = 100            # X = -27: tile 1 of sequence 0
+        scales[2, 700, 3] = 150            # X = 23: tile 5 of sequence 2
+        scales[3, 299, 0] = 0              # tile 2 of sequence 3, the last one it sees
+        scales[1, 900, 2] = 200            # past what sequence 1 sees (750 keys): no effect
+    elif case == "query_outliers":
+        q[1, 0, 3, 32:64] *= 2.0 ** 20
+        q[2, 0, 17, 96:] *= 2.0 ** -30
+    else:
+        codes[0, 256:384] = 0              # whole tiles of zero keys with out-of-range scales
+        scales[0, 256:384] = 0
+        q[3, 0, 5, :32] = 0.0              # an all-zero query block
+    iq = to_bf16_bits(q)
+    w = to_bf16_bits(rng.standard_normal((b, 1, Hi)))
     c = Di ** -0.5 * Hi ** -0.5
     ref = orc.index_score_mxfp4(iq, codes, scales, w, c, sp, n_cols, 4)
     ws = sti.workspace(256)
