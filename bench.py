@@ -480,6 +480,9 @@ def main():
                   f"{shape.b * shape.n_cols * shape.Di * 2 / 1e6:.0f} MB, through the 129 MB L2)")}
     if args.output_rope:
         cfg["output_inverse_rope_dims"] = shape.rd
+    if shape.fp4_keys:
+        cfg["index_keys"] = ("MXFP4 (E2M1 codes, an E8M0 scale per 32); queries quantised to MXFP4 in the scores "
+                             "kernel; scores on E5M2 tensor cores (kind::f8f6f4) where the scales allow, else bf16")
 
     if args.impl == "reference":
         if rank != 0:   # the CPU oracle runs once, on rank 0
@@ -592,8 +595,8 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
-            "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e5m2+bf16" if shape.fp4_keys else "bf16",
+            "data": "synthetic", "config": cfg, "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
             "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks,
             "launch": "CUDA graph of sti_decode_fused, replayed per step" if use_graph else "direct C-ABI calls"}
     line["ms_per_step_with_kernel_events"] = round(statistics.mean(evented_ms), 5)
