@@ -211,9 +211,9 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
         p.k_scales = fp4->scales;
         p.k_scales_bstride = fp4->scales_bstride;
     }
-    // MXFP4: three stages of packed tiles (a quarter of the bytes) feed two decoded tiles (E5M2, or
-    // bf16 when a block's scale is out of E5M2's exact range); with Di == 128 the queries are held
-    // a second time as E5M2
+    // MXFP4: three or four stages of packed tiles (a quarter of the bytes) feed two decoded tiles
+    // (E5M2, or bf16 when a block's scale is out of E5M2's exact range); with Di == 128 the
+    // queries are held a second time as E5M2
     p.c_stages = fp4 ? 3 : 0;
     p.f8 = (fp4 && Di == 128) ? 1 : 0;
     const size_t c_total = fp4 ? (size_t)p.c_stages * ((size_t)128 * Di / 2 + (size_t)128 * Di / 32) : 0;
@@ -222,6 +222,11 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     if (stages > (fp4 ? 3 : 8)) stages = fp4 ? 3 : 8;
     if (stages < 2) stages = 2;
     p.stages = stages;
+    // a fourth packed-tile stage when two CTAs still fit an SM's 228 KB (1 KB reserved per CTA)
+    if (fp4) {
+        p.c_stages = 4;
+        if (p.ctas_per_sm == 2 && sti::idx_scores_smem_bytes(p) > (size_t)(228 * 1024 / 2 - 1024)) p.c_stages = 3;
+    }
 
     const uint32_t box_inner = Di >= 64 ? 64u : (uint32_t)Di;
     const CUtensorMapSwizzle swz = Di >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;

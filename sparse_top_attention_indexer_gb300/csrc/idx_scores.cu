@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     uint8_t* c_ring = b8 + b8_bytes;
     Barriers* bars = reinterpret_cast<Barriers*>(c_ring + (size_t)(FP4 ? p.c_stages : 0) * c_bytes);
     float* w_s = reinterpret_cast<float*>(bars + 1);   // [nq * HI], pre-multiplied by c
-    int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq]
+    int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq], nq <= 64
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -728,7 +728,7 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
     const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
     const size_t b8_bytes = (p.fp4 && p.f8) ? (size_t)p.n_pad * 128 : 0;
     return 1024 + p.stages * a_bytes + b_bytes + b8_bytes + (p.fp4 ? p.c_stages : 0) * c_bytes + sizeof(Barriers) +
-           256 * 4 + 256 * 4;
+           256 * 4 + 64 * 4;
 }
 
 cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_s,
