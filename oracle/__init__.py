@@ -18,6 +18,10 @@ Every function is pinned by the CPU tests in ``tests/test_oracle_*.py``:
   mxfp4_quantize / mxfp4_decode / index_score_mxfp4   the E2M1 code table from the format's
                      definition, exact round trips of grid values, ties to even, saturation,
                      the scale rule against frexp, zero blocks, the error bound
+  e4m3_value / e4m3_round / kvfp4_quantize / kvfp4_decode / sparse_attn_fp4kv   the E4M3 table
+                     from the format's definition (bias, subnormals, NaN, 448), ties to even and
+                     saturation, the scale rule, exact round trips, zero and tiny blocks, the
+                     error bound, attention over the decoded rows equal to the plain attention
   window_topk_idxs_chunked   the prefill band of the pages when the chunk starts at 0 (rows
                      shifted past the ring), brute-force positions of every referenced row
   output_inverse_rope   identity at angle 0, the quarter-turn closed form, complex
@@ -155,20 +159,29 @@ def mxfp4_quantize(x):
     with np.errstate(divide="ignore"):
         X = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0, -127.0)
     X = np.clip(X, -127.0, 127.0)
-    p = blk / np.exp2(X)[..., None]
-    a = np.minimum(np.abs(p), 6.0)
-    grid = np.asarray(E2M1_MAGNITUDES)
-    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, 7)       # first grid value >= a
-    lo = np.clip(hi - 1, 0, 7)
-    d_lo, d_hi = a - grid[lo], grid[hi] - a
-    # nearest; on a tie the even code (mantissa bit 0 clear)
-    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
-    code = np.where(a == grid[hi], hi, code)
-    sign = ((p < 0) & (code > 0)).astype(np.uint8) << 3
-    nib = (code.astype(np.uint8) | sign).reshape(x.shape)
+    nib = _e2m1_nibbles(blk / np.exp2(X)[..., None]).reshape(x.shape)
     codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
     scales = (X + 127.0).astype(np.uint8)
     return codes, scales
+
+
+def _nearest_on_grid(grid, a):
+    """Index of the value of the ascending grid nearest to a (a within [grid[0], grid[-1]]); on a
+    tie the even index (for E2M1 and E4M3 codes: the one whose mantissa's last bit is clear)."""
+    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, len(grid) - 1)   # first grid value >= a
+    lo = np.clip(hi - 1, 0, len(grid) - 1)
+    d_lo, d_hi = a - grid[lo], grid[hi] - a
+    idx = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return np.where(a == grid[hi], hi, idx)
+
+
+def _e2m1_nibbles(p) -> np.ndarray:
+    """Values already divided by their block scale -> E2M1 nibbles (bit 3 sign, bits 0-2 the
+    magnitude code), nearest with ties to the even code, saturating at +-6; zero has no sign."""
+    p = np.asarray(p, dtype=np.float64)
+    code = _nearest_on_grid(np.asarray(E2M1_MAGNITUDES), np.minimum(np.abs(p), 6.0))
+    sign = ((p < 0) & (code > 0)).astype(np.uint8) << 3
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
 
 
 def mxfp4_fake_quant(x) -> np.ndarray:
@@ -189,6 +202,72 @@ def index_score_mxfp4(iq, ik_codes, ik_scales, w, c: float, start_pos, n_cols: i
     qd = mxfp4_fake_quant(qf)
     kd = mxfp4_decode(ik_codes, ik_scales, D)
     return index_score(_bf16_exact(qd), _bf16_exact(kd), w, c, start_pos, n_cols, ratio, threads)
+
+
+# ------------------------------------------------------------------ fp4 compressed KV (E4M3 scales, groups of 16)
+#
+# Attention._compress_kv ("read-weights" page) applies the rotary embedding to the latent's last
+# rope dims, then fp4_act_quant(latent, 16, True, scale_dtype=float8_e4m3fn) -- in place -- and
+# writes the result to the compressed-KV cache; the page's comment there: the compressed KV uses
+# groups of 16 with E4M3 scales.  The quantiser's body is not on the pages.  Reading (the
+# NVFP4-style block format without a second, per-tensor scale): blocks of 16 consecutive
+# elements along the row share one E4M3 scale s, the E4M3 value nearest to max|x| / 6 (ties to
+# the even code, saturating at 448), and each element x / s is rounded to the nearest E2M1
+# value as for MXFP4 (a block whose s is 0 is all zeros).  The cache (the attention's second KV
+# source) holds the decoded values; the window rows stay bf16.
+
+def e4m3_value(byte) -> np.ndarray:
+    """E4M3 (the float8_e4m3fn format: sign, 4-bit exponent with bias 7, 3-bit mantissa,
+    subnormals at exponent 0, no infinities, S.1111.111 = NaN) byte(s) -> float64."""
+    b = np.asarray(byte, dtype=np.uint8).astype(np.int64)
+    sgn = np.where(b & 0x80, -1.0, 1.0)
+    e, m = (b >> 3) & 0xF, b & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sgn * mag
+
+
+_E4M3_POSITIVE = e4m3_value(np.arange(0x7F, dtype=np.uint8))   # codes 0x00 .. 0x7E, ascending
+
+
+def e4m3_round(a) -> np.ndarray:
+    """Non-negative float(s) -> the byte of the nearest E4M3 value (ties to the even code),
+    saturating at 448."""
+    a = np.minimum(np.asarray(a, dtype=np.float64), 448.0)
+    return _nearest_on_grid(_E4M3_POSITIVE, a).astype(np.uint8)
+
+
+def kvfp4_quantize(x):
+    """float [..., d] (d a multiple of 16) -> (codes uint8 [..., d/2], E4M3 scale bytes [..., d/16]);
+    codes packed as for MXFP4 (element 2j in the low nibble of byte j)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    blk = x.reshape(x.shape[:-1] + (d // 16, 16))
+    sbyte = e4m3_round(np.abs(blk).max(axis=-1) / 6.0)
+    s = e4m3_value(sbyte)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        p = np.where(s > 0, blk / np.where(s > 0, s, 1.0), 0.0)
+    nib = _e2m1_nibbles(p).reshape(x.shape)
+    return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8), sbyte
+
+
+def kvfp4_decode(codes, scales, d: int) -> np.ndarray:
+    """Packed E2M1 codes [..., d/2] and E4M3 scale bytes [..., d/16] -> float64 [..., d]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(codes.shape[:-1] + (d,))
+    mag = np.asarray(E2M1_MAGNITUDES)[nib & 0x7]
+    val = np.where(nib & 0x8, -mag, mag)
+    return val * np.repeat(e4m3_value(scales), 16, axis=-1)
+
+
+def sparse_attn_fp4kv(q, kv1, kv2_codes, kv2_scales, sink, idx, scale: float, threads: int | None = None,
+                      rope_cs=None):
+    """sparse_attn with the second (compressed) KV source stored as fp4 rows: kv2_codes [b, n2,
+    d/2], kv2_scales [b, n2, d/16]; the attention runs over the decoded rows (exact in bf16: an
+    E2M1 value times an E4M3 scale has at most 5 significant bits)."""
+    d = np.asarray(q).shape[-1]
+    kv2 = _bf16_exact(kvfp4_decode(kv2_codes, kv2_scales, d))
+    return sparse_attn(q, kv1, sink, idx, scale, kv2=kv2, threads=threads, rope_cs=rope_cs)
 
 
 def _bf16_exact(x) -> np.ndarray:

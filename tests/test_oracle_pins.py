@@ -532,3 +532,89 @@ def test_mxfp4_index_score_is_the_score_of_the_decoded_values(orc):
     for bi in range(b):
         np.testing.assert_allclose(got[bi, 0, :vis[bi]], want[bi, 0, :vis[bi]], rtol=1e-12, atol=1e-12)
         assert np.all(np.isneginf(got[bi, 0, vis[bi]:]))
+
+
+# ----------------------------------------------------------------- fp4 compressed KV (E4M3 scales, 16)
+
+
+def test_e4m3_table_equals_the_library_float8_e4m3fn(orc):
+    """Every E4M3 byte decodes as torch's float8_e4m3fn does (an independent implementation of the
+    format); the format's landmarks: 1.0 = 0x38, 448 the largest finite, 2^-9 the smallest
+    subnormal, 2^-6 the smallest normal, 0x7F and 0xFF NaN."""
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    ours = orc.e4m3_value(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    assert np.array_equal(lib[~np.isnan(lib)], ours[~np.isnan(ours)])
+    assert ours[0x38] == 1.0 and ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+    assert np.isnan(ours[0x7F]) and np.isnan(ours[0xFF]) and np.nanmax(ours) == 448.0
+
+
+def test_e4m3_round_equals_the_library_cast_in_range_and_saturates(orc):
+    """Round to nearest E4M3, ties to even: equal to torch's cast on [0, 448], including every
+    midpoint between neighbouring codes; above 448 the reading saturates (a plain cast gives NaN
+    past 464)."""
+    torch = pytest.importorskip("torch")
+    grid = orc.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    a = np.concatenate([np.random.default_rng(21).uniform(0, 448, 20000), (grid[1:] + grid[:-1]) / 2, grid])
+    lib = torch.tensor(a, dtype=torch.float64).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(orc.e4m3_round(a), lib)
+    assert orc.e4m3_round(np.array([1.0625]))[0] == 0x38      # 1 and 1.125 tie -> 1 (even code)
+    assert orc.e4m3_round(np.array([1.1875]))[0] == 0x3A      # 1.125 and 1.25 tie -> 1.25
+    np.testing.assert_array_equal(orc.e4m3_round(np.array([448.0, 464.0, 1e6])), [0x7E, 0x7E, 0x7E])
+
+
+def test_kvfp4_scale_rule_and_exact_round_trip(orc):
+    """Rows built as E2M1 values times an E4M3 scale s, each block holding +-6 s, quantise to
+    exactly that scale byte and those codes, and decode back exactly."""
+    rng = np.random.default_rng(22)
+    d = 64
+    mags = np.asarray(orc.E2M1_MAGNITUDES)
+    sbytes = rng.integers(0x10, 0x70, size=(5, d // 16)).astype(np.uint8)
+    s = orc.e4m3_value(sbytes)
+    m = mags[rng.integers(0, 8, size=(5, d // 16, 16))]
+    m[..., 3] = 6.0
+    x = (np.where(rng.random(m.shape) < 0.5, -m, m) * s[..., None]).reshape(5, d)
+    codes, scales = orc.kvfp4_quantize(x)
+    np.testing.assert_array_equal(scales, sbytes)
+    np.testing.assert_array_equal(orc.kvfp4_decode(codes, scales, d), x)
+
+
+def test_kvfp4_zero_tiny_blocks_and_error_bound(orc):
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((40, 512)) * np.exp2(rng.integers(-6, 6, size=(40, 1)))
+    x[1, 16:32] = 0.0
+    x[2, 32:48] = rng.standard_normal(16) * 2.0 ** -16     # max/6 below half of E4M3's 2^-9
+    codes, scales = orc.kvfp4_quantize(x)
+    q = orc.kvfp4_decode(codes, scales, 512)
+    assert scales[1, 1] == 0 and scales[2, 2] == 0 and np.all(q[1, 16:32] == 0) and np.all(q[2, 32:48] == 0)
+    s = np.repeat(orc.e4m3_value(scales), 16, axis=-1)
+    # the E2M1 grid's gaps are at most 2 (between 4 and 6): rounding costs at most 1 s; past 6 s
+    # (s rounded down from max/6) the value saturates at 6 s
+    assert np.all(np.abs(q - x) <= np.maximum(s, np.abs(x) - 6 * s) * (1 + 1e-12))
+    assert np.all(np.abs(q) <= 6 * s)
+
+
+def test_sparse_attn_fp4kv_is_the_sink_softmax_over_decoded_rows(orc):
+    """Brute force in numpy on a tiny case: o = sum_i e^{s_i} v_i / (sum_i e^{s_i} + e^{sink})
+    over the decoded compressed rows (selected by index r - n1) and the bf16 window rows."""
+    rng = np.random.default_rng(24)
+    b, s_, h, d, n1, n2, k = 1, 2, 2, 32, 3, 5, 6
+    q = to_bf16_bits(rng.standard_normal((b, s_, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    codes = rng.integers(0, 256, size=(b, n2, d // 2), dtype=np.uint8)
+    scales = rng.integers(0x28, 0x40, size=(b, n2, d // 16), dtype=np.uint8)
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = np.array([[[0, 4, -1, 7, 2, 3], [5, -1, -1, 6, 1, 0]]], np.int32)
+    scale = d ** -0.5
+    out, _ = orc.sparse_attn_fp4kv(q, kv1, codes, scales, sink, idx, scale)
+    qf = bf16_bits_to_f32(q).astype(np.float64)
+    rows = np.concatenate([bf16_bits_to_f32(kv1).astype(np.float64), orc.kvfp4_decode(codes, scales, d)], axis=1)
+    for t in range(s_):
+        sel = [r for r in idx[0, t] if r >= 0]
+        v = rows[0, sel]
+        for hh in range(h):
+            sc = scale * (v @ qf[0, t, hh])
+            e = np.exp(sc)
+            want = (e @ v) / (e.sum() + math.exp(float(sink[hh])))
+            np.testing.assert_allclose(out[0, t, hh], want, rtol=1e-10, atol=1e-12)
