@@ -1,6 +1,6 @@
 """Benchmark of the Indexer -> top-k -> sparse sink attention path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..9] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..10] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic inputs resident in HBM:
 window indices, Indexer scores, top-k, sparse sink attention (every attention layer),
@@ -57,7 +57,7 @@ def peaks():
 
 
 KERNEL_SOURCES = {"idx_scores": ["idx_scores.cu"], "idx_topk": ["idx_topk.cu"],
-                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu", "sti_attn_util.cuh"], "window_idx": ["idx_topk.cu"]}
+                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu", "sti_attn_util.cuh", "sti_kvfp4.h"], "window_idx": ["idx_topk.cu"]}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -108,7 +108,10 @@ class GpuPath:
         self.q = [to_dev(data["q"][i], device) for i in range(self.L)]
         self.win = [to_dev(data["win"][i], device) for i in range(self.L)]
         self.sink = [to_dev_any(data["sink"][i], device) for i in range(self.L)]
-        self.comp = to_dev(data["comp"], device)
+        self.comp = to_dev(data["comp"], device) if "comp" in data else None
+        # fp4 compressed KV (workload 10): packed codes and E4M3 scales instead of bf16 rows
+        self.comp_codes = to_dev_any(data["comp_codes"], device) if "comp_codes" in data else None
+        self.comp_scales = to_dev_any(data["comp_scales"], device) if "comp_scales" in data else None
         self.iq = to_dev(data["iq"], device)
         self.ik = to_dev(data["ik"], device) if "ik" in data else None
         # MXFP4 keys (workload 9): codes and scales instead of bf16 keys
@@ -214,8 +217,12 @@ class GpuPath:
                      ws=self.ws)
         rec(3)
         for i in range(self.L):
-            sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale, kv2=self.comp,
-                                 out=self.out[i], ws=self.ws, rope_cs=self.rope_cs)
+            if self.comp_codes is not None:
+                sti.sparse_attn_sink_fp4kv(self.q[i], self.win[i], self.comp_codes, self.comp_scales, self.sink[i],
+                                           self.idx, shp.softmax_scale, out=self.out[i], ws=self.ws)
+            else:
+                sti.sparse_attn_sink(self.q[i], self.win[i], self.sink[i], self.idx, shp.softmax_scale,
+                                     kv2=self.comp, out=self.out[i], ws=self.ws, rope_cs=self.rope_cs)
             rec(4 + i)
 
     l2_mode = "flush"
@@ -258,8 +265,9 @@ def work(shape: workloads.Shape, data: dict) -> dict:
     w["window_idx"] = {"bytes": float(b * s * shape.win_width * 4), "flops": 0.0}
     if not shape.prefill:   # the decode top-k kernel also writes the window indices
         w["idx_topk"]["bytes"] += w.pop("window_idx")["bytes"]
+    comp_row = (d // 2 + d // 16) if shape.fp4_kv else d * 2                        # per compressed row (fp4: codes + scales)
     if shape.prefill:
-        kv_bytes = (shape.win_rows + n_keys.sum()) * d * 2                          # unique rows (L2 serves reuse)
+        kv_bytes = shape.win_rows * d * 2 + n_keys.sum() * comp_row                # unique rows (L2 serves reuse)
     else:
         kv_bytes = rows * d * 2                                                     # every gathered row from HBM
     attn = {"bytes": float(kv_bytes + 2 * b * s * h * d * 2 + b * s * shape.k_total * 4),
@@ -358,8 +366,12 @@ def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = No
         idx = np.concatenate([widx, cidx], axis=-1).reshape(1, len(t), -1)
         q = data["q"][0][0][t][None]
         cs = workloads.output_rope_table(shape)[:, t] if output_rope else None
-        out, _ = oracle.sparse_attn(q, data["win"][0], data["sink"][0], idx, shape.softmax_scale,
-                                    kv2=data["comp"], rope_cs=cs)
+        if shape.fp4_kv:
+            oracle.sparse_attn_fp4kv(q, data["win"][0], data["comp_codes"], data["comp_scales"], data["sink"][0], idx,
+                                     shape.softmax_scale)
+        else:
+            oracle.sparse_attn(q, data["win"][0], data["sink"][0], idx, shape.softmax_scale, kv2=data["comp"],
+                               rope_cs=cs)
         return len(t)
     sp = data["start_pos"]
     if shape.fp4_keys:
@@ -451,7 +463,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -479,7 +491,12 @@ def main():
                   "no flush: inputs larger than L2 (each decode step streams the index keys, "
                   f"{shape.b * shape.n_cols * shape.Di * 2 / 1e6:.0f} MB, through the 129 MB L2)")}
     if args.output_rope:
+        if shape.fp4_kv:
+            raise SystemExit("--output-rope is not available with fp4 compressed KV")
         cfg["output_inverse_rope_dims"] = shape.rd
+    if shape.fp4_kv:
+        cfg["compressed_kv"] = ("fp4 rows (E2M1 codes, an E4M3 scale per 16 elements), gathered and decoded to "
+                                "bf16 in the attention kernel")
     if shape.fp4_keys:
         cfg["index_keys"] = ("MXFP4 (E2M1 codes, an E8M0 scale per 32); queries quantised to MXFP4 in the scores "
                              "kernel; scores on E5M2 tensor cores (kind::f8f6f4) where the scales allow, else bf16")
@@ -595,7 +612,7 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e5m2+bf16" if shape.fp4_keys else "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e5m2+bf16" if shape.fp4_keys else "fp4kv+bf16" if shape.fp4_kv else "bf16",
             "data": "synthetic", "config": cfg, "roofline": roof, "kernel_us": avg_us, "kernel_roofline_frac": others,
             "gpu_launches": path.launches_per_step() * args.steps, "clocks": clocks,
             "launch": "CUDA graph of sti_decode_fused, replayed per step" if use_graph else "direct C-ABI calls"}

@@ -215,6 +215,29 @@ sti_status sti_sparse_attn_sink_rope(const uint16_t *q, const uint16_t *kv, int6
                                      int k, const float *rope_cs, int rope_dims, uint16_t *out, float *lse, void *ws,
                                      size_t ws_bytes, sti_stream stream);
 
+/* sti_sparse_attn_sink with the second (compressed) KV source stored as fp4 rows, the form
+ * Attention._compress_kv ("read-weights" page) gives the compressed latent before writing its
+ * cache: fp4_act_quant(latent, 16, True, scale_dtype=float8_e4m3fn) -- groups of 16 elements
+ * along the row share one E4M3 scale (float8_e4m3fn: sign, exponent bias 7, 3 mantissa bits),
+ * each element an E2M1 code (as in sti_idx_scores_mxfp4).  The quantiser is not on the pages;
+ * any codes and scales are accepted and decoded as value = code * scale.
+ *   kv2_codes:  uint8 [b, *, d/2], batch b at + b*kv2_codes_bstride bytes; row r of batch b holds
+ *               compressed row r (index n1 + r); byte j = elements 2j (low nibble), 2j+1
+ *   kv2_scales: uint8 [b, *, d/16], batch b at + b*kv2_scales_bstride bytes; byte g = the E4M3
+ *               scale of elements 16g .. 16g+15
+ * The window rows (indices < n1) stay bf16 in kv.  A packed 512-wide row is 288 bytes instead of
+ * 1 KB.  The decoded values are exact in bf16, so the result is sti_sparse_attn_sink's over
+ * those rows.  The rows are gathered with plain loads and decoded in shared memory by the
+ * one-CTA-per-query kernel (never the head-split one).
+ * Supported: as sti_sparse_attn_sink; kv2_codes and kv2_scales 16-byte aligned, their batch
+ * strides multiples of 16 covering n2 rows (STI_ERR_INVALID_ARG otherwise). */
+sti_status sti_sparse_attn_sink_fp4kv(const uint16_t *q, const uint16_t *kv, int64_t kv_bstride,
+                                      const uint8_t *kv2_codes, int64_t kv2_codes_bstride, const uint8_t *kv2_scales,
+                                      int64_t kv2_scales_bstride, int n1, int n2, const float *attn_sink,
+                                      const int32_t *idxs, int64_t idx_row_stride, float softmax_scale, int b,
+                                      int seqlen, int h, int d, int k, uint16_t *out, float *lse, void *ws,
+                                      size_t ws_bytes, sti_stream stream);
+
 /* ------------------------------------------------------------------ fused decode layer */
 /*
  * One decode step (seqlen == 1) of an index-source attention layer, as

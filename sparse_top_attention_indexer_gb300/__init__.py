@@ -30,6 +30,7 @@ FLAG_INDEX_RANGE, FLAG_TIMEOUT, FLAG_CHUNKED = 1, 2, 4
 EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_device_status", "sti_window_idxs",
            "sti_idx_scores_workspace_size", "sti_idx_scores", "sti_idx_topk_workspace_size", "sti_idx_topk",
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_sparse_attn_sink_rope",
+           "sti_sparse_attn_sink_fp4kv",
            "sti_decode_workspace_size",
            "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
            "sti_selftest_wait_timeout", "sti_window_idxs_chunked", "sti_idx_scores_mxfp4"]
@@ -90,6 +91,9 @@ def lib() -> ctypes.CDLL:
         L.sti_sparse_attn_sink_rope.argtypes = [P, P, I64, P, I64, I, I, P, P, I64, F, I, I, I, I, I, P, I, P, P, P,
                                                 SZ, P]
         L.sti_sparse_attn_sink_rope.restype = I
+        L.sti_sparse_attn_sink_fp4kv.argtypes = [P, P, I64, P, I64, P, I64, I, I, P, P, I64, F, I, I, I, I, I, P, P,
+                                                 P, SZ, P]
+        L.sti_sparse_attn_sink_fp4kv.restype = I
         L.sti_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.sti_decode_workspace_size.restype = SZ
         L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
@@ -276,6 +280,38 @@ def sparse_attn_sink(q: torch.Tensor, kv: torch.Tensor, attn_sink: torch.Tensor,
         _ptr(q), _ptr(kv), kv.stride(0), _ptr(kv2), 0 if kv2 is None else kv2.stride(0), n1, n2, _ptr(attn_sink),
         _ptr(topk_idxs), topk_idxs.stride(-2), float(softmax_scale), b, s, h, d, k, _ptr(out), _ptr(lse), _ptr(ws),
         ws.numel(), _stream(stream)), "sti_sparse_attn_sink")
+    return out
+
+
+def sparse_attn_sink_fp4kv(q: torch.Tensor, kv: torch.Tensor, kv2_codes: torch.Tensor, kv2_scales: torch.Tensor,
+                           attn_sink: torch.Tensor, topk_idxs: torch.Tensor, softmax_scale: float,
+                           out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                           ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """sparse_attn_sink with the second (compressed) source as fp4 rows: kv2_codes uint8
+    [b, rows, d/2] and kv2_scales uint8 [b, rows, d/16] (E4M3 scale per 16 elements), rows
+    contiguous; row r >= kv.shape[1] of the index space is compressed row r - kv.shape[1]."""
+    _need(q, torch.bfloat16, "q")
+    _need(attn_sink, torch.float32, "attn_sink")
+    _need(kv, torch.bfloat16, "kv", contiguous=False)
+    if topk_idxs.dtype != torch.int32 or topk_idxs.stride(-1) != 1:
+        raise ValueError("topk_idxs must be int32 with contiguous rows")
+    b, s, h, d = q.shape
+    k = topk_idxs.shape[-1]
+    n1, n2 = kv.shape[1], kv2_codes.shape[1]
+    if kv.stride(2) != 1 or kv.stride(1) != d:
+        raise ValueError("kv must be [b, rows, d] with contiguous rows")
+    for name, t, inner in (("kv2_codes", kv2_codes, d // 2), ("kv2_scales", kv2_scales, d // 16)):
+        if t.dtype != torch.uint8 or t.dim() != 3 or t.shape[2] != inner or t.stride(2) != 1 or t.stride(1) != inner:
+            raise ValueError(f"{name} must be uint8 [b, rows, {inner}] with contiguous rows")
+    if kv2_scales.shape[1] < n2:
+        raise ValueError("kv2_scales must hold as many rows as kv2_codes")
+    if out is None:
+        out = torch.empty_like(q)
+    ws = ws if ws is not None else workspace(sparse_attn_workspace_size(b, s, h, d, k), q.device)
+    _check(lib().sti_sparse_attn_sink_fp4kv(
+        _ptr(q), _ptr(kv), kv.stride(0), _ptr(kv2_codes), kv2_codes.stride(0), _ptr(kv2_scales), kv2_scales.stride(0),
+        n1, n2, _ptr(attn_sink), _ptr(topk_idxs), topk_idxs.stride(-2), float(softmax_scale), b, s, h, d, k,
+        _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "sti_sparse_attn_sink_fp4kv")
     return out
 
 

@@ -10,6 +10,7 @@
 
 #include "sti.h"
 #include "sti_internal.h"
+#include "sti_kvfp4.h"
 #include "sti_ptx.cuh"
 
 namespace {
@@ -287,16 +288,22 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
                             int64_t idx_row_stride, float softmax_scale, int b, int seqlen, int h, int d, int k,
                             uint16_t* out, float* lse, uint32_t* status, float* acc, size_t acc_bytes,
                             cudaStream_t st, bool pdl = false, int win_ring = 0,
-                            const int32_t* start_pos = nullptr, const float* rope_cs = nullptr, int rope_dims = 0) {
+                            const int32_t* start_pos = nullptr, const float* rope_cs = nullptr, int rope_dims = 0,
+                            const sti::KvFp4* fp4 = nullptr) {
     if (b < 0 || seqlen < 1 || h < 1 || d < 1 || k < 1 || n1 < 0 || n2 < 0) return STI_ERR_INVALID_ARG;
     if (rope_dims < 0 || rope_dims % 2 != 0 || rope_dims > d || (rope_dims > 0 && (!rope_cs || !aligned(rope_cs, 16))))
         return STI_ERR_INVALID_ARG;
     if (h > 64 || (d % 64) != 0 || d > 512) return STI_ERR_UNSUPPORTED;
     if (b == 0) return STI_OK;
-    if (!q || !attn_sink || !idxs || !out || (n1 > 0 && !kv) || (n2 > 0 && !kv2)) return STI_ERR_INVALID_ARG;
+    if (!q || !attn_sink || !idxs || !out || (n1 > 0 && !kv) || (n2 > 0 && !kv2 && !fp4)) return STI_ERR_INVALID_ARG;
     if (idx_row_stride < k) return STI_ERR_INVALID_ARG;
     if ((n1 > 0 && (kv_bstride < (int64_t)n1 * d || kv_bstride % 8)) ||
-        (n2 > 0 && (kv2_bstride < (int64_t)n2 * d || kv2_bstride % 8)))
+        (n2 > 0 && !fp4 && (kv2_bstride < (int64_t)n2 * d || kv2_bstride % 8)))
+        return STI_ERR_INVALID_ARG;
+    if (fp4 && n2 > 0 &&
+        (!fp4->codes || !fp4->scales || !aligned(fp4->codes, 16) || !aligned(fp4->scales, 16) ||
+         fp4->codes_bstride < (int64_t)n2 * (d / 2) || fp4->codes_bstride % 16 ||
+         fp4->scales_bstride < (int64_t)n2 * (d / 16) || fp4->scales_bstride % 16))
         return STI_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || (kv && !aligned(kv, 16)) || (kv2 && !aligned(kv2, 16)))
         return STI_ERR_INVALID_ARG;
@@ -330,7 +337,6 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     int hs_rows = 1;
     const int c_hs = sti::attn_hs_pick(nq, h, d, &hs_rows);
     p.cluster = c_hs > 0 ? c_hs : (p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1);
-    p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     // TMA gathers need each source to be whole d-element rows: batch stride a multiple of d
     p.rows1 = n1 > 0 ? kv_bstride / d : 0;
     p.rows2 = n2 > 0 ? kv2_bstride / d : 0;
@@ -338,6 +344,12 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.pdl = pdl ? 1 : 0;
     p.use_tma = (n1 + n2 > 0) && (n1 == 0 || kv_bstride % d == 0) && (n2 == 0 || kv2_bstride % d == 0) &&
                 (int64_t)b * (p.rows1 > p.rows2 ? p.rows1 : p.rows2) < 0x7FFFFFFF;
+    // fp4 compressed rows are gathered with plain loads and decoded into the tile by the
+    // one-CTA-per-query kernel (no TMA, no head split)
+    if (fp4) {
+        p.rows2 = 0;
+        p.use_tma = 0;
+    }
     CUtensorMap tm_q, tm_kv1, tm_kv2, tm_win;
     memset(&tm_win, 0, sizeof tm_win);
     memset(&tm_q, 0, sizeof tm_q);
@@ -352,6 +364,8 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
     p.rope_cs = rope_dims > 0 ? rope_cs : nullptr;
     p.rope_dims = rope_dims;
     if (!head_split && c_hs > 0) p.cluster = p.acc != nullptr ? sti::attn_pick_cluster(nq, k, d) : 1;
+    // after the cluster is final: a query's slots split evenly over its CTAs
+    p.rows_per_cta = (k + p.cluster - 1) / p.cluster;
     if (p.use_tma) {
         const uint32_t q_rows = head_split ? (uint32_t)(h * hs_rows / c_hs) : (uint32_t)h;
         sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, q_rows);
@@ -364,6 +378,7 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
         if (n2 == 0) tm_kv2 = tm_kv1;
     }
     cudaError_t e = head_split ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, tm_win, p, st)
+                     : fp4     ? sti::launch_sparse_attn_kvfp4(tm_q, tm_kv1, tm_kv2, p, *fp4, st)
                                : sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
@@ -507,6 +522,26 @@ sti_status sti_sparse_attn_sink_rope(const uint16_t* q, const uint16_t* kv, int6
     return attn_impl(q, kv, kv_bstride, kv2, kv2_bstride, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b,
                      seqlen, h, d, k, out, lse, status_word(ws), acc, ws_bytes - sti::kWsStatusBytes,
                      static_cast<cudaStream_t>(stream), false, 0, nullptr, rope_cs, rope_dims);
+}
+
+sti_status sti_sparse_attn_sink_fp4kv(const uint16_t* q, const uint16_t* kv, int64_t kv_bstride,
+                                      const uint8_t* kv2_codes, int64_t kv2_codes_bstride, const uint8_t* kv2_scales,
+                                      int64_t kv2_scales_bstride, int n1, int n2, const float* attn_sink,
+                                      const int32_t* idxs, int64_t idx_row_stride, float softmax_scale, int b,
+                                      int seqlen, int h, int d, int k, uint16_t* out, float* lse, void* ws,
+                                      size_t ws_bytes, sti_stream stream) {
+    if (!ws_ok(ws, ws_bytes, sti::kWsStatusBytes)) return STI_ERR_INVALID_ARG;
+    if (d % 16 != 0) return STI_ERR_INVALID_ARG;
+    sti::KvFp4 f{};
+    f.codes = kv2_codes;
+    f.scales = kv2_scales;
+    f.codes_bstride = kv2_codes_bstride;
+    f.scales_bstride = kv2_scales_bstride;
+    f.on = 1;
+    float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sti::kWsStatusBytes);
+    return attn_impl(q, kv, kv_bstride, nullptr, 0, n1, n2, attn_sink, idxs, idx_row_stride, softmax_scale, b, seqlen,
+                     h, d, k, out, lse, status_word(ws), acc, ws_bytes - sti::kWsStatusBytes,
+                     static_cast<cudaStream_t>(stream), false, 0, nullptr, nullptr, 0, &f);
 }
 
 // fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048] |

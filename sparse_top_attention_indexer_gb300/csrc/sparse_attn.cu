@@ -33,6 +33,7 @@
 #include <vector>
 
 #include "sti_internal.h"
+#include "sti_kvfp4.h"
 #include "sti_ptx.cuh"
 #include "sti_attn_util.cuh"
 
@@ -62,6 +63,37 @@ struct __align__(8) AttnSmemTail {
     int row_coord[kRows];  // row in its source viewed as [B*rows, d]
     int row_srcid[kRows];  // 0: kv, 1: kv2, -1: masked
 };
+
+// E4M3 byte (sign, 4-bit exponent with bias 7, 3-bit mantissa; exponent 0 subnormal: m * 2^-9;
+// S.1111.111 NaN) -> float.
+__device__ __forceinline__ float e4m3_to_float(uint32_t v) {
+    const uint32_t e = (v >> 3) & 15u, m = v & 7u, sg = (v & 0x80u) << 24;
+    if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
+    return e == 0u ? __uint_as_float(sg | __float_as_uint((float)m * 0.001953125f))
+                   : __uint_as_float(sg | ((e + 120u) << 23) | (m << 20));
+}
+
+// E2M1 nibble (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa; exponent 0 is
+// subnormal: m * 0.5) -> float.
+__device__ __forceinline__ float e2m1_to_float(uint32_t nib) {
+    const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
+    const uint32_t bits = e ? ((126u + e) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
+    return __uint_as_float(bits | ((nib & 8u) << 28));
+}
+
+// Eight fp4 elements (nibble i of cw = element i) times their E4M3 scale s as eight bf16 (one
+// 16-byte chunk of the tile).  A product of an E2M1 value and an E4M3 value has at most five
+// significant bits, so dropping the low half of its fp32 pattern is exact.
+__device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = e2m1_to_float((cw >> (8 * j)) & 15u) * s;
+        const float hi = e2m1_to_float((cw >> (8 * j + 4)) & 15u) * s;
+        o[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // Swizzled byte offset of 16-byte chunk `ch` (of 8 bf16) of row `r` in a tile of `rows` rows
 // stored as column blocks of rows x 128 bytes (128-byte swizzle: chunk ^= row % 8).
@@ -104,7 +136,7 @@ __device__ unsigned long long g_attn_t[2048][16];
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
-                       const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p) {
+                       const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p, const KvFp4 f) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
     // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
@@ -203,8 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 idx = -1;
             }
             const int srcid = idx < 0 ? -1 : (idx < p.n1 ? 0 : 1);
-            const int64_t coord = srcid < 0 ? 0 : (srcid == 0 ? b * p.rows1 + idx : b * p.rows2 + (idx - p.n1));
-            const uint16_t* src = srcid < 0 ? nullptr : (srcid == 0 ? p.kv : p.kv2) + coord * p.d;
+            // fp4 rows of the second source: coord is the row within its batch element, decoded below
+            const bool fp4_row = srcid == 1 && f.on;
+            const int64_t coord = srcid < 0 ? 0
+                                  : (srcid == 0 ? b * p.rows1 + idx : (fp4_row ? idx - p.n1 : b * p.rows2 + (idx - p.n1)));
+            const uint16_t* src = (srcid < 0 || fp4_row) ? nullptr : (srcid == 0 ? p.kv : p.kv2) + coord * p.d;
             tl->row_src[tid] = src;
             tl->row_valid[tid] = idx >= 0;
             tl->row_coord[tid] = (int)coord;
@@ -213,7 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nslot = slot + kRows;
             if (tile + 1 < tile_end && nslot < slot_end) {
                 const int nidx = __ldg(idx_row + nslot);
-                if (nidx >= 0 && nidx < n_rows) {
+                if (nidx >= 0 && nidx < n_rows && nidx >= p.n1 && f.on) {
+                    const size_t r2 = (size_t)(nidx - p.n1);
+                    prefetch_l2_bulk(f.codes + (size_t)b * f.codes_bstride + r2 * (p.d / 2), (uint32_t)p.d / 2);
+                    if ((p.d / 16) % 16 == 0)
+                        prefetch_l2_bulk(f.scales + (size_t)b * f.scales_bstride + r2 * (p.d / 16), (uint32_t)p.d / 16);
+                } else if (nidx >= 0 && nidx < n_rows) {
                     const uint16_t* nsrc = nidx < p.n1 ? p.kv + (size_t)b * p.kv_bstride + (size_t)nidx * p.d
                                                        : p.kv2 + (size_t)b * p.kv2_bstride + (size_t)(nidx - p.n1) * p.d;
                     prefetch_l2_bulk(nsrc, (uint32_t)p.d * 2);
@@ -290,6 +330,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             for (int c = tid; c < kRows * chunks_per_row; c += kThreads) {
                 const int r = c / chunks_per_row, ch = c - r * chunks_per_row;
+                if (f.on && tl->row_srcid[r] == 1) {
+                    // fp4 row: 4 code bytes and the E4M3 scale of their 16-element group -> 8 bf16
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (ch * 8 < p.d) {
+                        const size_t r2 = (size_t)tl->row_coord[r];
+                        const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(
+                                                      f.codes + (size_t)b * f.codes_bstride + r2 * (p.d / 2)) + ch);
+                        const uint32_t sb = __ldg(f.scales + (size_t)b * f.scales_bstride + r2 * (p.d / 16) + (ch >> 1));
+                        v = kvfp4_decode8(cw, e4m3_to_float(sb));
+                    }
+                    *reinterpret_cast<uint4*>(kv_s + sw128_offset(r, ch, kRows)) = v;
+                    continue;
+                }
                 const uint16_t* rs = tl->row_src[r];
                 const bool ok = rs != nullptr && ch * 8 < p.d;
                 cp_async_16(kv_base + sw128_offset(r, ch, kRows), ok ? rs + ch * 8 : p.q, ok ? 16u : 0u);
@@ -654,6 +707,13 @@ int attn_pick_cluster(int n_queries, int k, int d) {
 
 cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                const AttnParams& p, cudaStream_t stream) {
+    KvFp4 none{};
+    return launch_sparse_attn_kvfp4(tm_q, tm_kv1, tm_kv2, p, none, stream);
+}
+
+cudaError_t launch_sparse_attn_kvfp4(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                     const AttnParams& p, const KvFp4& f, cudaStream_t stream) {
+    if (f.on && p.use_tma) return cudaErrorInvalidValue;
     const int n_queries = p.B * p.s;
     if (n_queries == 0) return cudaSuccess;
     const size_t smem = attn_smem_bytes(p.d_pad);
@@ -681,7 +741,7 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, tm_kv1, tm_kv2, p);
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, tm_kv1, tm_kv2, p, f);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -102,6 +102,24 @@ def test_output_rotation_argument_checks(libsti):
         assert libsti.sti_decode_fused_noalloc(ctypes.byref(a), None) == 1, (cs, rd)
 
 
+def test_fp4kv_argument_checks(libsti):
+    """The fp4 compressed rows' pointers and batch strides are checked on the host."""
+    fake = 1 << 20
+    P = ctypes.c_void_p
+    n2, d = 100, 512
+
+    def call(codes=P(fake), cb=n2 * d // 2, scales=P(fake), sb=n2 * d // 16):
+        return libsti.sti_sparse_attn_sink_fp4kv(P(fake), P(fake), 128 * d, codes, cb, scales, sb, 128, n2, P(fake),
+                                                 P(fake), 640, 0.1, 1, 1, 64, d, 640, P(fake), None, P(fake),
+                                                 1 << 30, None)
+
+    assert call(codes=P(fake + 8)) == 1          # codes not 16-byte aligned
+    assert call(codes=None) == 1
+    assert call(scales=None) == 1
+    assert call(cb=n2 * d // 2 - 16) == 1        # codes batch stride short of n2 rows
+    assert call(sb=n2 * d // 16 + 8) == 1        # scales batch stride not a multiple of 16
+
+
 def test_selftest_argument_checks(libsti):
     fake = 1 << 20
     P = ctypes.c_void_p

@@ -224,6 +224,46 @@ def test_sparse_attn(sti, orc, b, s, h, d, k, n1, n2, empty):
     np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
 
 
+@pytest.mark.parametrize("b,s,h,d,k,n1,n2,ws_full", [
+    (2, 1, 64, 512, 640, 128, 300, True),     # decode shape: window + compressed rows, split over a cluster
+    (3, 1, 64, 512, 640, 128, 2000, False),   # decode shape, one CTA per query
+    (1, 70, 64, 512, 256, 200, 100, False),   # several queries
+    (2, 5, 16, 64, 300, 10, 700, True),       # small rows (d = 64: 4 scale bytes per row)
+])
+def test_sparse_attn_fp4kv(sti, orc, b, s, h, d, k, n1, n2, ws_full):
+    """The compressed source as fp4 rows (E2M1 codes, an E4M3 scale per 16 elements; the form
+    Attention._compress_kv gives the latent) decoded in the gather: the oracle's attention over
+    the decoded rows.  Random masked slots, all -1 rows, both sources within a tile."""
+    import torch
+
+    rng = rng_for(800 + d, k + n2)
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    codes = rng.integers(0, 256, size=(b, n2, d // 2), dtype=np.uint8)
+    # E4M3 1/4 .. 7/16 (rows of magnitude like N(0,1), which the absolute output tolerance assumes),
+    # a few rows at 1/64 .. 1/32, and three zero rows
+    scales = rng.integers(0x28, 0x2F, size=(b, n2, d // 16), dtype=np.uint8)
+    scales[0, 3:9] = rng.integers(0x18, 0x1F, size=(6, d // 16))
+    scales[0, :3] = 0
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = index_lists(rng, b, s, k, n1 + n2, masked_frac=0.15, empty_rows=1)
+    ref, ref_lse = orc.sparse_attn_fp4kv(q, kv1, codes, scales, sink, idx, d ** -0.5)
+    lse = torch.empty(b, s, h, dtype=torch.float32, device="cuda")
+    ws = sti.workspace(sti.sparse_attn_workspace_size(b, s, h, d, k) if ws_full else 256)
+    out = sti.sparse_attn_sink_fp4kv(to_dev(q), to_dev(kv1), to_dev_any(codes), to_dev_any(scales),
+                                     to_dev_any(sink), to_dev_any(idx), d ** -0.5, lse=lse, ws=ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got = bf16_out_to_f64(out)
+    check_attn(got, ref)
+    empty = np.all(idx < 0, axis=-1)
+    assert np.all(got[empty] == 0)
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+
+
 @pytest.mark.parametrize("b,s,d,k,n1,n2", [
     (1, 300, 512, 200, 256, 256),    # k not a multiple of the 64-row tile
     (2, 150, 256, 130, 100, 300),

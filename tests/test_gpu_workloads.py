@@ -73,9 +73,10 @@ def test_workload_full(gpu, orc, n):
               f"mean {mn:.2e}")
 
 
-@pytest.mark.parametrize("n", [3, 8])
+@pytest.mark.parametrize("n", [3, 8, 10])
 def test_workload_prefill_sampled(gpu, orc, n):
-    """The 8192-query prefill from position 0, and the 2048-query chunk continuing at 6144."""
+    """The 8192-query prefill from position 0 (with bf16 and with fp4 compressed KV), and the
+    2048-query chunk continuing at 6144."""
     shape = workloads.config(n)
     data = workloads.make(shape)
     path = _run(shape, data, gpu)
@@ -106,7 +107,11 @@ def test_workload_prefill_sampled(gpu, orc, n):
     np.testing.assert_array_equal(got_i[rows, :W], ref_w)
     check_topk_rows(got_i[rows, W:][:, None], ref_c, ref_s, off, K)
     idx = np.concatenate([ref_w[:, None], ref_c], axis=-1).reshape(1, len(rows), -1)
-    ref_o, _ = orc.sparse_attn(data["q"][0][0][rows][None], data["win"][0], data["sink"][0], idx,
-                               shape.softmax_scale, kv2=data["comp"])
+    if shape.fp4_kv:
+        ref_o, _ = orc.sparse_attn_fp4kv(data["q"][0][0][rows][None], data["win"][0], data["comp_codes"],
+                                         data["comp_scales"], data["sink"][0], idx, shape.softmax_scale)
+    else:
+        ref_o, _ = orc.sparse_attn(data["q"][0][0][rows][None], data["win"][0], data["sink"][0], idx,
+                                   shape.softmax_scale, kv2=data["comp"])
     got_o = bf16_out_to_f64(path.out[0][0][rows])
     check_attn(got_o, ref_o[0])

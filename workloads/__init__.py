@@ -84,6 +84,7 @@ class Shape:
     planted: bool = False      # planted rank-one score bias on 1% of keys
     n_layers: int = 1          # attention layers sharing one index pass (reuse layers)
     fp4_keys: bool = False     # index keys stored as MXFP4 (E2M1 codes + E8M0 scales)
+    fp4_kv: bool = False       # compressed KV rows stored as fp4 (E2M1 codes + an E4M3 scale per 16)
     seed: int = 0
 
     @property
@@ -130,7 +131,8 @@ class Shape:
 def config(n: int) -> Shape:
     """The named workloads: 1-5 as listed in the design notes, 6 and 7 the decode workload at
     compression ratios 2 and 1 (32768 and 65536 index rows per sequence), 8 a prefill chunk
-    that continues its sequence, 9 workload 2 with MXFP4 index keys."""
+    that continues its sequence, 9 workload 2 with MXFP4 index keys, 10 workload 3 with the
+    compressed KV rows stored as fp4."""
     seed = 1000 + n
     if n == 1:
         return Shape("tiny_prefill_s256_h4_d64", b=1, s=256, start_pos=np.zeros(1, np.int32), h=4, d=64, rd=16,
@@ -152,6 +154,9 @@ def config(n: int) -> Shape:
     if n == 9:   # workload 2 with MXFP4 index keys
         return Shape("decode_b32_ctx65536_mxfp4", b=32, s=1, start_pos=np.full(32, 65535, np.int32), n_cols=16384,
                      fp4_keys=True, seed=seed)
+    if n == 10:  # workload 3 with fp4 compressed-KV rows
+        return Shape("prefill_s8192_kvfp4", b=1, s=8192, start_pos=np.zeros(1, np.int32), n_cols=2048, fp4_kv=True,
+                     seed=seed)
     if n == 8:   # a prefill chunk of 2048 queries continuing a sequence at position 6144
         return Shape("chunked_prefill_s2048_at6144", b=1, s=2048, start_pos=np.full(1, 6144, np.int32), n_cols=2048,
                      seed=seed)
@@ -303,6 +308,23 @@ def make(shape: Shape, beta: float | None = None) -> dict:
         out["ik_codes"], out["ik_scales"] = codes, scales
     else:
         out["ik"] = ik
+    if shape.fp4_kv:
+        # fp4 compressed KV drawn directly as codes and E4M3 scales: the magnitude frequencies of
+        # the MXFP4 keys, random signs, and scale bytes 0x28 .. 0x2E (1/4 .. 7/16: max|x| / 6 of a
+        # 16-element block of N(0,1) values); rows past the sequence's compressed count are zero
+        rc = rng_for(sd, 10)
+        d2 = shape.d
+        mag = rc.choice(8, size=(b, shape.n_cols, d2), p=FP4_CODE_FREQ).astype(np.uint8)
+        sgn = (rc.random(size=mag.shape) < 0.5).astype(np.uint8) << 3
+        nib = np.where(mag > 0, mag | sgn, 0).astype(np.uint8)
+        kc = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+        ksc = rc.integers(0x28, 0x2F, size=(b, shape.n_cols, d2 // 16), dtype=np.uint8)
+        n_comp = np.minimum((shape.start_pos.astype(np.int64) + shape.s) // shape.ratio, shape.n_cols)
+        for bi in range(b):
+            kc[bi, int(n_comp[bi]):] = 0
+            ksc[bi, int(n_comp[bi]):] = 0
+        out["comp_codes"], out["comp_scales"] = kc, ksc
+        del out["comp"]
     return out
 
 
