@@ -9,10 +9,15 @@
 // epilogue, with no cross-lane traffic.  Keys stream from HBM by TMA (128-byte swizzle) through
 // a multi-stage shared-memory ring; the index queries of a unit (<= 256 rows) stay resident.
 //
-// Persistent kernel, one CTA per SM, warp-specialised:
+// Persistent kernel, one or two CTAs per SM (two when both accumulators fit the SM's TMEM),
+// warp-specialised:
 //   warp 0      TMA producer (index-key tiles, and the unit's query tile)
 //   warp 1      TMEM allocator + single-thread MMA issuer
 //   warps 2..5  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced)
+// With MXFP4 keys (Indexer.forward's fp4 keys and queries) warp 0 stages packed tiles (E2M1
+// codes + E8M0 scales) by bulk copy and warps 6..13 decode them in shared memory -- to E5M2 for
+// kind::f8f6f4 MMAs where every block's scale allows an exact E5M2 value, else to bf16 -- after
+// quantising each unit's queries in place.
 // Work = the flattened list of (unit, key tile) pairs over all units (unit = one sequence and
 // nq consecutive queries), cut into equal contiguous ranges, one per CTA.  Key tiles past the
 // last visible position of a unit are not computed; the epilogue writes -inf there.
