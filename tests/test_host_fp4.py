@@ -11,13 +11,21 @@ import pytest
 import workloads
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_DATA = {}
+
+
+def _make(n: int):
+    """workloads.make(config(n)), built once per test session."""
+    if n not in _DATA:
+        shape = workloads.config(n)
+        _DATA[n] = (shape, workloads.make(shape))
+    return _DATA[n]
 
 
 def test_mxfp4_key_inputs():
     """Workload 9: packed keys and E8M0 scales in their documented ranges, zero past the visible
     keys, no bf16 keys."""
-    shape = workloads.config(9)
-    data = workloads.make(shape)
+    shape, data = _make(9)
     assert "ik" not in data
     codes, scales = data["ik_codes"], data["ik_scales"]
     assert codes.shape == (shape.b, shape.n_cols, shape.Di // 2) and codes.dtype == np.uint8
@@ -34,8 +42,7 @@ def test_mxfp4_key_inputs():
 
 def test_fp4_compressed_kv_inputs():
     """Workload 10: the compressed rows as fp4 codes and E4M3 scale bytes 0x28..0x2E."""
-    shape = workloads.config(10)
-    data = workloads.make(shape)
+    shape, data = _make(10)
     assert "comp" not in data and shape.prefill and shape.fp4_kv
     codes, scales = data["comp_codes"], data["comp_scales"]
     assert codes.shape == (1, shape.n_cols, shape.d // 2) and scales.shape == (1, shape.n_cols, shape.d // 16)
@@ -47,13 +54,13 @@ def test_bench_bytes_of_the_fp4_workloads():
     per fp4 compressed row (256 + 32) in the prefill attention."""
     import bench
 
-    s9 = workloads.config(9)
-    w9 = bench.work(s9, workloads.make(s9))
+    s9, d9 = _make(9)
+    w9 = bench.work(s9, d9)
     keys = s9.b * s9.n_cols
     extra = s9.b * s9.Hi * s9.Di * 2 + s9.b * s9.Hi * 2 + s9.b * s9.n_cols * 4
     assert w9["idx_scores"]["bytes"] == keys * 68 + extra
-    s3, s10 = workloads.config(3), workloads.config(10)
-    w3, w10 = bench.work(s3, workloads.make(s3)), bench.work(s10, workloads.make(s10))
+    (s3, d3), (s10, d10) = _make(3), _make(10)
+    w3, w10 = bench.work(s3, d3), bench.work(s10, d10)
     diff = w3["sparse_attn[0]"]["bytes"] - w10["sparse_attn[0]"]["bytes"]
     assert diff == s3.n_cols * (s3.d * 2 - (s3.d // 2 + s3.d // 16))
     assert w3["sparse_attn[0]"]["flops"] == w10["sparse_attn[0]"]["flops"]
