@@ -63,3 +63,67 @@ def test_query_bytes_from_magnitude_index():
         t1 = (0x46444240 + X * 0x04040404) & 0xFFFFFFFF
         for idx in range(8):
             assert e5m2_value(prmt(t0, t1, idx) & 0xFF) == mags[idx] * 2.0 ** X
+
+
+def _bf16_value(h: int) -> float:
+    return float(np.array([h << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def e2m1x8_to_bf16(cw: int, e8: int) -> list[int]:
+    """The kernel's bf16 decode: magnitude high/low bytes by byte permutes, the sign moved into
+    place, and X = e8 - 127 added to the exponent field of every non-zero half (vadd2 under a
+    vcmpne2 mask)."""
+    lo, hi = cw & 0x07070707, (cw >> 4) & 0x07070707
+    yl, yh = lo | (lo >> 4), hi | (hi >> 4)
+    sel_l = (yl & 0xFF) | ((yl >> 8) & 0xFF00)
+    sel_h = (yh & 0xFF) | ((yh >> 8) & 0xFF00)
+    hl = prmt(0x3F3F3F00, 0x40404040, sel_l) | ((cw << 4) & 0x80808080)
+    ll = prmt(0xC0800000, 0xC0804000, sel_l)
+    hh = prmt(0x3F3F3F00, 0x40404040, sel_h) | (cw & 0x80808080)
+    lh = prmt(0xC0800000, 0xC0804000, sel_h)
+    t0, t1 = prmt(ll, hl, 0x5140), prmt(lh, hh, 0x5140)
+    t2, t3 = prmt(ll, hl, 0x7362), prmt(lh, hh, 0x7362)
+    o = [prmt(t0, t1, 0x5410), prmt(t0, t1, 0x7632), prmt(t2, t3, 0x5410), prmt(t2, t3, 0x7632)]
+    k16 = ((e8 - 127) << 7) & 0xFFFF
+    out = []
+    for w in o:
+        for half in (w & 0xFFFF, w >> 16):
+            out.append(((half + k16) & 0xFFFF) if (half & 0x7FFF) != 0 else half)
+    return out   # elements 0, 1, ..., 7 as bf16 bit patterns
+
+
+def test_e2m1_to_bf16_every_nibble_and_scale():
+    mags = oracle.E2M1_MAGNITUDES
+    rng = np.random.default_rng(6)
+    words = [sum(((n + k) % 16) << (4 * k) for k in range(8)) for n in range(16)]
+    words += [int(v) for v in rng.integers(0, 2 ** 32, 100, dtype=np.uint64)]
+    for e8 in list(range(2, 253, 7)) + [2, 127, 252]:
+        for cw in words:
+            out = e2m1x8_to_bf16(cw, e8)
+            for i in range(8):
+                nib = (cw >> (4 * i)) & 0xF
+                want = (-1.0 if nib & 8 else 1.0) * mags[nib & 7] * 2.0 ** (e8 - 127)
+                assert _bf16_value(out[i]) == want, (e8, hex(cw), i)
+
+
+def test_fp4_kv_decode_values():
+    """The attention's fp4 row decode: E4M3 byte -> fp32 from its bit fields, times the E2M1
+    value, truncated to bf16 -- equal to the oracle's decode for every code and finite scale."""
+    def e4m3_to_f32(v: int) -> float:
+        e, m, sg = (v >> 3) & 15, v & 7, (v & 0x80) << 24
+        if e == 0:
+            bits = sg | int(np.array([m * 0.001953125], dtype=np.float32).view(np.uint32)[0])
+        else:
+            bits = sg | ((e + 120) << 23) | (m << 20)
+        return float(np.array([bits], dtype=np.uint32).view(np.float32)[0])
+
+    mags = oracle.E2M1_MAGNITUDES
+    for sb in range(256):
+        if sb & 0x7F == 0x7F:
+            continue
+        s = e4m3_to_f32(sb)
+        assert s == oracle.e4m3_value(np.array([sb], np.uint8))[0], hex(sb)
+        for nib in range(16):
+            v = np.float32((-1.0 if nib & 8 else 1.0) * mags[nib & 7]) * np.float32(s)
+            bits = int(np.array([v], dtype=np.float32).view(np.uint32)[0]) >> 16
+            assert _bf16_value(bits) == float(v), (hex(sb), nib)   # exact in bf16
