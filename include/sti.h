@@ -306,6 +306,14 @@ typedef struct sti_decode_args {
 size_t sti_decode_workspace_size(const sti_decode_args *a);
 sti_status sti_decode_fused(const sti_decode_args *a, void *ws, size_t ws_bytes, sti_stream stream,
                             void *const *events);
+/* How many kernels sti_decode_fused enqueues for these arguments (the device must be current):
+ * 3 (scores; top-k + window indices; attention); 2 when steps 2 and 3 run as one kernel -- the
+ * pages' decode shape (h = 64, d = 512, window 128, index_topk 512, n_cols <= 65536, both KV
+ * sources in whole rows): a 4-CTA cluster per query selects the top-k and attends over its own
+ * quarter of the index row, then merges; events 2 and 3 are then both recorded after it -- or
+ * when n_cols == 0 (no scores kernel); 0 for b == 0; -1 if the arguments would be rejected.
+ * Enqueues nothing. */
+int sti_decode_kernel_count(const sti_decode_args *a);
 
 /* ------------------------------------------------------------------ fused decode, no allocation */
 /*

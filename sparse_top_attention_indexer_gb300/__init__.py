@@ -20,7 +20,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 # STI_LIB selects another build of the same library (for example one compiled with other
 # tuning macros); by default the in-tree libsti.so
-LIB_PATH = os.environ.get("STI_LIB") or os.path.join(_HERE, "libsti.so")
+DEFAULT_LIB_PATH = os.path.join(_HERE, "libsti.so")
+LIB_PATH = os.environ.get("STI_LIB") or DEFAULT_LIB_PATH
 
 STATUS_NAMES = {0: "STI_OK", 1: "STI_ERR_INVALID_ARG", 2: "STI_ERR_UNSUPPORTED", 3: "STI_ERR_CUDA",
                 4: "STI_ERR_INDEX_RANGE", 5: "STI_ERR_DEVICE_TIMEOUT", 6: "STI_ERR_DEVICE_UNSUPPORTED",
@@ -32,7 +33,7 @@ EXPORTS = ["sti_status_string", "sti_last_cuda_error", "sti_version", "sti_read_
            "sti_sparse_attn_workspace_size", "sti_sparse_attn_sink", "sti_sparse_attn_sink_rope",
            "sti_sparse_attn_sink_fp4kv",
            "sti_decode_workspace_size",
-           "sti_decode_fused", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
+           "sti_decode_fused", "sti_decode_kernel_count", "sti_decode_fused_noalloc", "sti_decode_noalloc_status",
            "sti_selftest_wait_timeout", "sti_window_idxs_chunked", "sti_idx_scores_mxfp4"]
 
 
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.sti_sparse_attn_sink_fp4kv.restype = I
         L.sti_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
         L.sti_decode_workspace_size.restype = SZ
+        L.sti_decode_kernel_count.argtypes = [ctypes.POINTER(DecodeArgs)]
+        L.sti_decode_kernel_count.restype = I
         L.sti_decode_fused.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
         L.sti_decode_fused.restype = I
         L.sti_selftest_wait_timeout.argtypes = [P, SZ, ctypes.c_uint32, P]
@@ -131,6 +134,20 @@ def _need(t: torch.Tensor, dtype, name: str, contiguous: bool = True):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def upload_bf16(bits, device="cuda") -> torch.Tensor:
+    """A numpy array of bf16 bit patterns (uint16) as a torch.bfloat16 tensor on `device`."""
+    import numpy as np
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def upload(a, device="cuda") -> torch.Tensor:
+    """A numpy array (any dtype torch knows) as a tensor on `device`."""
+    import numpy as np
+
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
@@ -366,6 +383,14 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
 
 def decode_workspace_size(a: DecodeArgs) -> int:
     return int(lib().sti_decode_workspace_size(ctypes.byref(a)))
+
+
+def decode_kernel_count(a: DecodeArgs) -> int:
+    """Kernels one decode_fused call enqueues for these arguments (see sti_decode_kernel_count)."""
+    n = int(lib().sti_decode_kernel_count(ctypes.byref(a)))
+    if n < 0:
+        raise StiError(1, "sti_decode_kernel_count")
+    return n
 
 
 def decode_fused(a: DecodeArgs, ws: torch.Tensor, stream=None, events=None):

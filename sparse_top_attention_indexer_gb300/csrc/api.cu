@@ -544,14 +544,45 @@ sti_status sti_sparse_attn_sink_fp4kv(const uint16_t* q, const uint16_t* kv, int
                      static_cast<cudaStream_t>(stream), false, 0, nullptr, nullptr, 0, &f);
 }
 
+// The decode step's top-k and attention run as one kernel (decode_attn.cu) for the pages' decode
+// shape: 64 heads x 512, window 128, index_topk 512, at most 65536 compressed positions, both KV
+// sources in whole rows (TMA).  decode_fusable also needs the device to launch its 4-CTA clusters.
+static bool decode_shape_fusable(const sti_decode_args* a) {
+    constexpr int64_t kD = 512;
+    if (a->b <= 0 || a->n_cols <= 0 || a->n_cols > 65536 || a->h != 64 || a->d != kD || a->window_size != 128 ||
+        a->index_topk != 512)
+        return false;
+    if (!a->q || !a->window_kv || !a->comp_kv || !a->attn_sink || !a->out || !a->topk_idxs) return false;
+    if (a->window_bstride % kD != 0 || a->comp_bstride % kD != 0 || a->window_bstride < 128 * kD ||
+        a->comp_bstride < (int64_t)a->n_cols * kD)
+        return false;
+    if (!aligned(a->q, 16) || !aligned(a->window_kv, 16) || !aligned(a->comp_kv, 16) || !aligned(a->out, 16))
+        return false;
+    if ((int64_t)a->b * (a->window_bstride / kD) >= 0x7FFFFFFF || (int64_t)a->b * 64 >= 0x7FFFFFFF) return false;
+    return true;
+}
+static bool decode_fusable(const sti_decode_args* a) {
+    return decode_shape_fusable(a) && sti::decode_topk_attn_available();
+}
+
 // fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048] |
-//                          attention accumulator fp32 [b, h, d] (batches of at most 256)]
+//   attention accumulator fp32 [b, h, d] (batches of at most 256), or, when the top-k and attention
+//   run as one kernel, its merge scratch (partial outputs and per-head max and sum)]
 static size_t decode_scores_bytes(const sti_decode_args* a) {
     return sti::align_up((size_t)a->b * (size_t)(a->n_cols > 0 ? a->n_cols : 1) * sizeof(float), sti::kWsAlign);
 }
 static size_t decode_hist_bytes(const sti_decode_args* a) { return (size_t)a->b * 2048 * sizeof(uint32_t); }
 
-static size_t decode_acc_bytes(const sti_decode_args* a) { return attn_acc_bytes(a->b, 1, a->h, a->d); }
+static size_t decode_fused_scratch_bytes(int b) {
+    return sti::align_up(sti::decode_topk_attn_xchg_bytes(b), sti::kWsAlign) +
+           sti::align_up(sti::decode_topk_attn_xml_bytes(b), sti::kWsAlign);
+}
+static size_t decode_acc_bytes(const sti_decode_args* a) {
+    const size_t acc = attn_acc_bytes(a->b, 1, a->h, a->d);
+    if (!decode_shape_fusable(a)) return acc;
+    const size_t x = decode_fused_scratch_bytes(a->b);
+    return x > acc ? x : acc;
+}
 
 size_t sti_decode_workspace_size(const sti_decode_args* a) {
     if (!a || a->b <= 0) return sti::kWsStatusBytes;
@@ -572,6 +603,44 @@ static const Fp4Keys* decode_fp4(const sti_decode_args* a, Fp4Keys* k) {
 static bool decode_rope_ok(const sti_decode_args* a) {
     return a->rope_dims == 0 || (a->rope_dims > 0 && a->rope_dims % 2 == 0 && a->rope_dims <= a->d && a->rope_cs &&
                                  aligned(a->rope_cs, 16));
+}
+
+// Steps 2 and 3 of a decode step as the fused kernel (after the scores kernel filled `scores` and
+// `hist`); a programmatic dependent of the scores kernel unless it must wait for q_ready.
+static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* scores, uint32_t* hist,
+                                        uint32_t* status, uint8_t* scratch, cudaStream_t st) {
+    constexpr int kD = 512;
+    if (a->q_ready) {
+        const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a->q_ready), 0);
+        if (e != cudaSuccess) return cuda_fail(e, "sti_decode_fused: cudaStreamWaitEvent");
+    }
+    sti::DecodeAttnParams p{};
+    p.scores = scores;
+    p.hist = hist;
+    p.start_pos = a->start_pos;
+    p.idx_out = a->topk_idxs;
+    p.sink = a->attn_sink;
+    p.out = a->out;
+    p.rope_cs = a->rope_dims > 0 ? a->rope_cs : nullptr;
+    p.rope_dims = a->rope_dims;
+    p.status = status;
+    p.scale_log2 = (float)((double)a->softmax_scale * 1.4426950408889634);
+    p.B = a->b;
+    p.n_cols = a->n_cols;
+    p.ratio = a->ratio;
+    p.rows1 = a->window_bstride / kD;
+    p.comp_kv = a->comp_kv;
+    p.comp_bstride = a->comp_bstride;
+    p.xchg = reinterpret_cast<float*>(scratch);
+    p.xml = reinterpret_cast<float*>(scratch +
+                                     sti::align_up(sti::decode_topk_attn_xchg_bytes(a->b), sti::kWsAlign));
+    CUtensorMap tm_q, tm_ring, tm_ring_rows;
+    sti_status s = make_map_2d(&tm_q, a->q, kD, (uint64_t)a->b * 64, kD * 2, 64, 64);
+    if (s == STI_OK) s = make_map_2d(&tm_ring, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 32);
+    if (s == STI_OK) s = make_map_2d(&tm_ring_rows, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 1);
+    if (s != STI_OK) return s;
+    const cudaError_t e = sti::launch_decode_topk_attn(tm_q, tm_ring, tm_ring_rows, p, /*pdl=*/!a->q_ready, st);
+    return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_decode_fused: top-k + attention");
 }
 
 sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes, sti_stream stream,
@@ -612,6 +681,12 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
         if (s != STI_OK) return s;
     }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+    if (decode_fusable(a)) {
+        s = decode_topk_attn_impl(a, scores, hist, status, reinterpret_cast<uint8_t*>(acc), st);
+        if (s != STI_OK) return s;
+        if ((e = mark(2)) != cudaSuccess || (e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
+        return STI_OK;
+    }
     // top-k of the compressed positions (+W) and the ring's window indices, one kernel.  It and the
     // attention are programmatic dependents: each is scheduled while its predecessor drains, does
     // the work that needs nothing of the step (window indices; Q load, TMEM and barriers), then
@@ -632,6 +707,13 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     if (s != STI_OK) return s;
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     return STI_OK;
+}
+
+int sti_decode_kernel_count(const sti_decode_args* a) {
+    if (!a || a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return -1;
+    if (a->b == 0) return 0;
+    if (decode_fusable(a)) return 2;
+    return a->n_cols > 0 ? 3 : 2;
 }
 
 // ---------------------------------------------------------------------- fused decode, no allocation
@@ -694,7 +776,11 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     float* scores = reinterpret_cast<float*>(scratch + kNoallocScoresOff);
     uint32_t* hist = reinterpret_cast<uint32_t*>(scratch + kNoallocHistOff);
     float* acc = reinterpret_cast<float*>(scratch + kNoallocAccOff);
-    const size_t acc_used = decode_acc_bytes(a) <= kNoallocAccBytes ? decode_acc_bytes(a) : 0;
+    // the fused top-k + attention kernel's merge scratch shares the accumulator's place (it needs
+    // no zeroing); otherwise the split attention's accumulator, when it fits
+    const bool fused = decode_fusable(a) && decode_fused_scratch_bytes(a->b) <= kNoallocAccBytes;
+    const size_t acc_need = attn_acc_bytes(a->b, 1, a->h, a->d);
+    const size_t acc_used = fused ? 0 : (acc_need <= kNoallocAccBytes ? acc_need : 0);
     // the array still holds the previous call's data: zero the status word, the histograms and
     // the part of the accumulator this call may use
     cudaError_t e = cudaMemsetAsync(status, 0, sti::kWsStatusBytes, st);
@@ -707,6 +793,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
                             a->n_cols, a->ratio, scores, status, st, hist, decode_fp4(a, &fk));
         if (s != STI_OK) return s;
     }
+    if (fused) return decode_topk_attn_impl(a, scores, hist, status, reinterpret_cast<uint8_t*>(acc), st);
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
                   a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;

@@ -23,6 +23,23 @@ __device__ __forceinline__ bool attn_wait(uint64_t* bar, uint32_t parity, uint32
     }
 }
 
+// The same, acquiring at cluster scope (for barriers that other CTAs of the cluster arrive on
+// after writing shared memory this thread then reads).
+__device__ __forceinline__ bool attn_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                  volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > STI_WAIT_TIMEOUT_NS) {
+            if (status) atomicOr(status, 2u /* STI_FLAG_TIMEOUT */);
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 // Reduce N values per lane over the warp's 32 lanes, scattering the results: afterwards v[0] of
 // lane l is the reduction of value l >> (5 - log2 N) (each held by 32/N adjacent lanes).
 template <int N, bool IS_MAX>

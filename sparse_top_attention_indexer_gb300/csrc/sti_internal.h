@@ -110,6 +110,38 @@ int attn_hs_pick(int n_queries, int h, int d, int* rows);
 cudaError_t launch_sparse_attn_hs(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                   const CUtensorMap& tm_win, const AttnParams& p, cudaStream_t stream);
 
+// ------------------------------------------------------------------ fused decode top-k + attention
+// One kernel for the decode step's top-k (with the ring's window indices) and its attention, for
+// 64 heads x 512, window 128, index_topk 512: a 4-CTA cluster per query (decode_attn.cu).
+struct DecodeAttnParams {
+    const float* scores;       // fp32 [B, n_cols] (one query per sequence)
+    uint32_t* hist;            // [B, 2048] the scores kernel's first-pass histograms (re-zeroed)
+    const int32_t* start_pos;  // [B]
+    int32_t* idx_out;          // [B, 128 + 512]: window slots, then compressed positions + 128
+    const uint16_t* comp_kv;   // bf16 compressed KV, batch b at + b*comp_bstride, rows of 512
+    int64_t comp_bstride;      // elements
+    const float* sink;         // [64]
+    uint16_t* out;             // bf16 [B, 64, 512]
+    const float* rope_cs;      // optional [B, rope_dims/2, 2]: the output's inverse rotation
+    int rope_dims;
+    uint32_t* status;
+    float* xchg;               // merge scratch: [B][4 d-blocks][3 other CTAs][128 d][64 heads] fp32
+    float* xml;                // merge scratch: [B][4 CTAs][2][64] fp32 (running max, sum)
+    float scale_log2;          // softmax_scale * log2(e)
+    int B, n_cols, ratio;
+    int64_t rows1;             // rows per batch element of the ring (batch stride / 512)
+};
+// Bytes of the merge scratch for b queries (16-byte aligned parts: xchg then xml).
+inline size_t decode_topk_attn_xchg_bytes(int b) { return (size_t)b * 4 * 3 * 128 * 64 * 4; }
+inline size_t decode_topk_attn_xml_bytes(int b) { return (size_t)b * 4 * 2 * 64 * 4; }
+bool decode_topk_attn_available();
+size_t decode_topk_attn_smem_bytes();
+// tm_q: q as [B*64, 512] (box 64 x 64); tm_ring: the ring as [B*rows1, 512] (box 64 x 32, a full
+// ring's slice per CTA); tm_ring_rows: the same with box 64 x 1, for four-row gathers (whose box is
+// one row high).
+cudaError_t launch_decode_topk_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_ring, const CUtensorMap& tm_ring_rows,
+                                    const DecodeAttnParams& p, bool pdl, cudaStream_t stream);
+
 // ------------------------------------------------------------------ device properties
 int device_num_sms();
 

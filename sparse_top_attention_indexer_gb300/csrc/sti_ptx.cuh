@@ -68,6 +68,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with acquire semantics at cluster scope: once it reports the phase complete, writes
+// that other CTAs of the cluster released before arriving (mbar_arrive_remote) are visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false (and sets
 // STI_FLAG_TIMEOUT in *status when non-null) if it does not complete within limit_ns.
 __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint32_t* status, uint64_t limit_ns) {
@@ -369,6 +383,13 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr_cluster, float a, floa
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
                      addr_cluster),
                  "f"(a), "f"(b), "r"(bar_cluster)
+                 : "memory");
+}
+
+// 4-byte store into another CTA's shared memory counted (complete_tx) on that CTA's barrier.
+__device__ __forceinline__ void st_async_b32(uint32_t addr_cluster, uint32_t v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr_cluster),
+                 "r"(v), "r"(bar_cluster)
                  : "memory");
 }
 

@@ -17,15 +17,15 @@ TOPK_BAND = 1e-6
 
 
 def to_dev(bits: np.ndarray, device="cuda"):
-    import torch
+    from sparse_top_attention_indexer_gb300 import upload_bf16
 
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+    return upload_bf16(bits, device)
 
 
 def to_dev_any(a: np.ndarray, device="cuda"):
-    import torch
+    from sparse_top_attention_indexer_gb300 import upload
 
-    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return upload(a, device)
 
 
 def bf16_out_to_f64(t) -> np.ndarray:
@@ -57,6 +57,35 @@ def check_scores(gpu: np.ndarray, ref: np.ndarray):
         worst = max(worst, float(err.max()))
     assert worst <= SCORE_RTOL, f"score relative error {worst:.3e} > {SCORE_RTOL}"
     return worst
+
+
+def score_error_stats(gpu: np.ndarray, ref: np.ndarray) -> dict:
+    """The score error three ways, for reporting beside check_scores: the floored relative error
+    it asserts; the plain relative error |g-r|/|r| over the entries with |r| >= 1e-2 * rms(row)
+    (where the floor does not act); and, below that, the absolute error in units of the row's
+    rms (the entries where heads cancel to about zero)."""
+    rows = ref.reshape(-1, ref.shape[-1])
+    g = gpu.reshape(-1, ref.shape[-1]).astype(np.float64)
+    floored = above = below = 0.0
+    n_below = 0
+    for i in range(rows.shape[0]):
+        f = np.isfinite(rows[i])
+        if not f.any():
+            continue
+        r, gi = rows[i][f], g[i][f]
+        rms = float(np.sqrt(np.mean(r * r)))
+        if rms == 0.0:
+            continue
+        err = np.abs(gi - r)
+        big = np.abs(r) >= SCORE_FLOOR * rms
+        floored = max(floored, float((err / np.maximum(np.abs(r), SCORE_FLOOR * rms)).max()))
+        if big.any():
+            above = max(above, float((err[big] / np.abs(r[big])).max()))
+        if (~big).any():
+            below = max(below, float(err[~big].max()) / rms)
+            n_below += int((~big).sum())
+    return {"floored_rel": floored, "rel_where_abs_ge_1e-2_rms": above, "abs_over_rms_below": below,
+            "entries_below_floor": n_below}
 
 
 def check_topk_rows(gpu_rows: np.ndarray, ref_rows: np.ndarray, ref_scores: np.ndarray | None, offset: int,

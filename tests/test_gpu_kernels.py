@@ -483,6 +483,42 @@ def test_decode_fused_small(sti, orc):
     check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
 
 
+@pytest.mark.parametrize("n_cols,sps,label", [
+    (2101, [127, 126, 95, 31, 1, 2047, 2051, 8399],
+     "ring full / one slot short / whole ring slices empty; vis = K, K+1; score rows not 16-byte aligned"),
+    (20000, [79999, 65535, 17000, 130], "score rows past 16384 positions (quarters read twice from L2)"),
+])
+def test_decode_fused_boundaries(sti, orc, n_cols, sps, label):
+    """The decode step's fused top-k + attention kernel: each CTA of a query's cluster owns 32
+    ring slots and a quarter of the score row; these start positions put the ring's filling edge
+    and the visible count at every boundary of that split."""
+    import torch
+
+    shp = workloads.custom("decode_bounds", b=len(sps), s=1, start_pos=sps, seed=83, n_cols=n_cols, topk=512, h=64,
+                           d=512)
+    data = workloads.make(shp)
+    sp = data["start_pos"]
+    W = shp.window
+    ref_scores = orc.index_score(data["iq"], data["ik"], data["w"], shp.index_scale, sp, shp.n_cols, shp.ratio)
+    ref_cidx = orc.topk(ref_scores, sp, shp.ratio, shp.topk, W)
+    ref_widx = np.concatenate([orc.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0)
+    ref_out, _ = orc.sparse_attn(data["q"][0], data["win"][0], data["sink"][0],
+                                 np.concatenate([ref_widx, ref_cidx], axis=-1), shp.softmax_scale, kv2=data["comp"])
+    a, out, tk = sti.decode_args(to_dev(data["q"][0]), to_dev(data["win"][0]), to_dev(data["comp"]),
+                                 to_dev_any(data["sink"][0]), shp.softmax_scale, to_dev(data["iq"]),
+                                 to_dev(data["ik"]), to_dev(data["w"]), shp.index_scale, to_dev_any(sp), shp.ratio,
+                                 shp.n_cols, shp.topk)
+    assert sti.decode_kernel_count(a) == 2, "the fused kernel takes this shape"
+    ws = sti.workspace(sti.decode_workspace_size(a))
+    sti.decode_fused(a, ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got_idx = tk.cpu().numpy().reshape(shp.b, 1, -1)
+    np.testing.assert_array_equal(got_idx[..., :W], ref_widx)
+    check_topk_rows(got_idx[..., W:], ref_cidx, ref_scores, W, shp.topk)
+    check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
+
+
 @pytest.mark.parametrize("probs,label", [((0.02, 0.49, 0.49), "tau bin fits: ~800 tied keys across every chunk"),
                                          ((0.34, 0.33, 0.33), "tau bin too large: whole-row passes")])
 def test_decode_fused_topk_ties(sti, orc, probs, label):

@@ -35,8 +35,20 @@ def test_noalloc_rejects_sizes_beyond_the_fixed_scratch():
     assert L.sti_status_string(7) == b"STI_ERR_TOO_LARGE"
 
 
+# Batches that take each of the scratch's uses: the head-split attention (64 heads, few queries);
+# the row-split attention whose clusters add partial outputs into the scratch's accumulator (16
+# heads: not head-split), which the call must clear; and more than 128 queries, where the
+# accumulator is not used and no query splits.
+NOALLOC_CASES = {
+    "head_split": dict(b=6, start_pos=[8191, 4095, 1500, 300, 40, 2], n_cols=2048, h=64),
+    "row_split_acc": dict(b=20, start_pos=[8191 - 397 * i for i in range(20)], n_cols=2048, h=16),
+    "many_queries": dict(b=140, start_pos=[4095 - 29 * i for i in range(140)], n_cols=1024, h=64),
+}
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_twice():
+@pytest.mark.parametrize("case", list(NOALLOC_CASES))
+def test_noalloc_matches_workspace_entry_twice(case):
     import torch
 
     if not torch.cuda.is_available():
@@ -44,9 +56,10 @@ def test_noalloc_matches_workspace_entry_twice():
     import sparse_top_attention_indexer_gb300 as sti
 
     sti.lib()
+    kw = NOALLOC_CASES[case]
     # ragged decode batch: sequences longer and shorter than index_topk, one with a filling ring
-    shape = workloads.custom("noalloc_decode", b=6, s=1, start_pos=[8191, 4095, 1500, 300, 40, 2],
-                             seed=9090, n_cols=2048, topk=512, h=64, d=512)
+    shape = workloads.custom(f"noalloc_decode_{case}", b=kw["b"], s=1, start_pos=kw["start_pos"], seed=9090,
+                             n_cols=kw["n_cols"], topk=512, h=kw["h"], d=512)
     data = workloads.make(shape)
     args = dict(q=to_dev(data["q"][0]), window_kv=to_dev(data["win"][0]), comp_kv=to_dev(data["comp"]),
                 attn_sink=to_dev_any(data["sink"][0]), softmax_scale=shape.softmax_scale, iq=to_dev(data["iq"]),
