@@ -632,8 +632,8 @@ static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* s
     p.comp_kv = a->comp_kv;
     p.comp_bstride = a->comp_bstride;
     p.xchg = reinterpret_cast<float*>(scratch);
-    p.xml = reinterpret_cast<float*>(scratch +
-                                     sti::align_up(sti::decode_topk_attn_xchg_bytes(a->b), sti::kWsAlign));
+    const size_t xchg_bytes = sti::align_up(sti::decode_topk_attn_xchg_bytes(a->b), sti::kWsAlign);
+    p.xml = reinterpret_cast<float*>(scratch + xchg_bytes);
     CUtensorMap tm_q, tm_ring, tm_ring_rows;
     sti_status s = make_map_2d(&tm_q, a->q, kD, (uint64_t)a->b * 64, kD * 2, 64, 64);
     if (s == STI_OK) s = make_map_2d(&tm_ring, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 32);

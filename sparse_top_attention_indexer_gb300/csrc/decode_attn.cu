@@ -55,7 +55,7 @@ namespace {
 
 #ifdef STI_DA_TIMING
 // global-timer stamps per CTA (profiling builds): [0, 16) math-thread phases, [16, 24) MMA issuer
-__device__ unsigned long long g_da_t[1024][32];
+__device__ unsigned long long g_da_t[1024][64];
 #define STI_DSTAMP(i)                                                                                  \
     do {                                                                                               \
         if (blockIdx.x < 1024) g_da_t[blockIdx.x][i] = global_timer_ns();                              \
@@ -83,7 +83,7 @@ constexpr int kRows = 128;                // tile rows
 constexpr int kRingRows = kW / kCtas;     // ring slots per CTA
 constexpr int kRingRow0 = kRows - kRingRows;   // tile row of the first ring slot
 constexpr int kBins = 2048;
-constexpr int kMemCap = 1024;             // threshold-bin members resolved from a list (more: row passes)
+constexpr int kSegCap = 64;               // threshold-bin members one warp lists (more: row passes)
 constexpr uint32_t kBlkBytes = kRows * 128;    // one column block of the tile (128 rows x 128 B)
 constexpr uint32_t kQBlkBytes = kH * 128;      // one column block of Q (64 heads x 128 B)
 constexpr uint32_t kTileBytes = 8 * kBlkBytes;
@@ -99,14 +99,16 @@ struct __align__(16) DaTail {
     uint64_t ring_bar;         // the ring slice landed (4 loader arrivals + bytes)
     uint64_t s_full[2];        // S^T of the ring slice / of the compressed tile in TMEM
     uint64_t p_full;           // P^T written (one arrival per softmax set), phase 0 ring, 1 tile
-    uint64_t o_done;           // PV complete, phase 0 ring, 1 tile
+    uint64_t o_done;           // the ring slice's PV complete (O^T initialised)
     uint64_t ring_free;        // the ring slice's PV complete: rows 96..127 may be overwritten
+    uint64_t pv_bar[4];        // the compressed tile's PV complete for d-block m
     uint64_t pub_bar;          // merge: every CTA's partial outputs written (4 CTAs)
+    uint64_t tk_bar;           // top-k: the other CTAs' words, members and counts landed (24 arrivals + bytes)
+    uint64_t recv_bar;         // merge: the three other CTAs' partials of this CTA's d-block landed
     uint32_t tmem_base;
     int abort;
-    int n_mem;                 // threshold-bin members listed
+    int seg_cnt[8 * kCtas];    // top-k: members each warp of the cluster found in the threshold bin
     int warp_tot[8], warp_tot2[8];
-    int misc[4];
     float m_run[kH], l_run[kH], alpha[kH];
     float red_max[4][kH], red_sum[4][kH];
     float wgt[kCtas][kH];
@@ -161,47 +163,50 @@ __device__ __forceinline__ void scan2_m(int a, int b, DaTail* tl, int mt, int& a
     b_tot = tb;
 }
 
-// The bin d* (of 2048, eight per math thread in h8) where the count from the top first reaches
-// `remaining`; *above = matching keys in higher bins, *cnt = keys in d*.  256 math threads.
-__device__ int select_bin_m(const uint32_t (&h8)[8], int remaining, DaTail* tl, int mt, int* above_out,
-                            int* cnt_out) {
-    const int lane = mt & 31, w = mt >> 5;
+// The bin d (of 32 * per bins, per = 32 or 64, in shared memory) where the count from the top
+// first reaches `remaining`: (d, keys in higher bins, keys in d); (-1, total, 0) when the histogram
+// holds fewer keys.  One warp, no block barrier: every warp that needs the bin computes it.  Lane l
+// sums bins [per l, per l + per) (its 16-byte reads rotated by l, so the eight lanes of a phase hit
+// distinct banks), a suffix scan over the lanes finds the lane of d, then that lane's bins are
+// split over the warp and scanned the same way.
+__device__ __forceinline__ int3 select_bin_w(const uint32_t* h, int per, int remaining, int lane) {
+    const int nv = per / 4;
+    const uint4* h4 = reinterpret_cast<const uint4*>(h + per * lane);
     int local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) local += (int)h8[i];
-    int inc = local;
+#pragma unroll 4
+    for (int i = 0; i < nv; ++i) {
+        const uint4 v = h4[(i + lane) & (nv - 1)];
+        local += (int)(v.x + v.y + v.z + v.w);
+    }
+    int suf = local;   // keys in the bins of lanes >= lane
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += x;
+        const int x = __shfl_down_sync(kFull, suf, o);
+        if (lane + o < 32) suf += x;
     }
-    if (lane == 31) tl->warp_tot[w] = inc;
-    if (mt == 0) tl->misc[0] = -1;
-    named_bar_sync(kBarMath, 256);
-    int wpre = 0, tot = 0;
+    const unsigned hit = __ballot_sync(kFull, suf - local < remaining && suf >= remaining);
+    if (hit == 0u) return make_int3(-1, __shfl_sync(kFull, suf, 0), 0);
+    const int L = __ffs(hit) - 1;
+    const int above_l = __shfl_sync(kFull, suf - local, L);
+    const int sub = per / 32;   // bins of lane L per lane: 1 or 2
+    const int b0 = per * L + sub * lane;
+    const int c_hi = (int)h[b0 + sub - 1];
+    const int c_lo = sub == 2 ? (int)h[b0] : 0;
+    const int loc2 = c_hi + c_lo;
+    int suf2 = loc2;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int x = tl->warp_tot[i];
-        wpre += i < w ? x : 0;
-        tot += x;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_down_sync(kFull, suf2, o);
+        if (lane + o < 32) suf2 += x;
     }
-    int above = tot - (wpre + inc);   // keys in the bins of higher threads
-#pragma unroll
-    for (int i = 7; i >= 0; --i) {
-        const int c = (int)h8[i];
-        if (above < remaining && above + c >= remaining) {
-            tl->misc[0] = 8 * mt + i;
-            tl->misc[1] = above;
-            tl->misc[2] = c;
-        }
-        above += c;
-    }
-    named_bar_sync(kBarMath, 256);
-    const int d = tl->misc[0];
-    *above_out = tl->misc[1];
-    *cnt_out = tl->misc[2];
-    named_bar_sync(kBarMath, 256);   // misc and warp_tot are rewritten by the next call
-    return d;
+    const int above_j = above_l + suf2 - loc2;   // keys above this lane's bins
+    const unsigned hit2 = __ballot_sync(kFull, above_j < remaining && above_j + loc2 >= remaining);
+    const int J = hit2 ? __ffs(hit2) - 1 : 0;
+    const bool top = above_j + c_hi >= remaining;   // d is this lane's higher bin
+    const int d = __shfl_sync(kFull, top ? b0 + sub - 1 : b0, J);
+    const int ab = __shfl_sync(kFull, top ? above_j : above_j + c_hi, J);
+    const int c = __shfl_sync(kFull, top ? c_hi : c_lo, J);
+    return make_int3(d, ab, c);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -240,9 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->p_full, 2);
         mbar_init(&tl->o_done, 1);
         mbar_init(&tl->ring_free, 1);
+        for (int m = 0; m < 4; ++m) mbar_init(&tl->pv_bar[m], 1);
         mbar_init(&tl->pub_bar, kCtas);
+        mbar_init(&tl->tk_bar, (kCtas - 1) * 8);
+        mbar_init(&tl->recv_bar, 1);
         tl->abort = 0;
-        tl->n_mem = 0;
         fence_mbar_init();
     }
     if (tid < kH) {
@@ -319,6 +326,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                             cb * 64, ys[0] >= 0 ? ys[0] : first, ys[1] >= 0 ? ys[1] : first, ys[2] >= 0 ? ys[2] : first,
                             ys[3] >= 0 ? ys[3] : first);
         }
+        if (warp == 11) {
+            // ---- the ring slice's softmax, by the one warp whose TMEM lane quarter holds tile rows
+            // 96..127 (lane = ring slot 32*rank + lane), while the math warps run the top-k: the
+            // first tile, so the running max is its own max and the running sum its own sum
+            bool ok = attn_wait(&tl->s_full[0], 0, p.status, abort);
+            ok = __all_sync(kFull, ok);
+            tc_fence_after();
+            const bool valid = ok && ring_valid(lane);
+            float x[64];
+            {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)kRingRow0 << 16), r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                tmem_ld32(tmem + ((uint32_t)kRingRow0 << 16) + 32u, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[32 + i] = valid ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+            }
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {   // per-head maxima over the 32 rows: lane l gets head 32 hb + l
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = x[32 * hb + i];
+                warp_reduce_scatter_n<32, true>(v);
+                tl->m_run[32 * hb + lane] = v[0];
+            }
+            __syncwarp();
+            uint8_t* pb = p_s + kQBlkBytes;   // P^T row block 1 (rows 64..127); this lane's row 96 + lane
+            const int kr = kRingRow0 - 64 + lane;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const float m = tl->m_run[i];
+                x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
+                *reinterpret_cast<__nv_bfloat16*>(pb + i * 128 + (((kr >> 3) ^ (i & 7)) << 4) + (kr & 7) * 2) =
+                    __float2bfloat16_rn(x[i]);
+            }
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = x[32 * hb + i];
+                warp_reduce_scatter_n<32, false>(v);
+                tl->l_run[32 * hb + lane] = v[0];
+            }
+            fence_proxy_async_smem();   // P^T: generic writes read by the MMA
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {   // both arrivals of phase 0 (the math warps' two sets make phase 1's)
+                mbar_arrive(&tl->p_full);
+                mbar_arrive(&tl->p_full);
+            }
+            if (lane == 0) STI_DSTAMP(27);
+        }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
@@ -373,11 +435,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&tl->s_full[1]);
             ok = ok && attn_wait(&tl->p_full, 1, p.status, abort);
             STI_DSTAMP(20);
-            if (ok) {
-                tc_fence_after();
-                pv(0, false);
+            if (ok) tc_fence_after();
+            for (int m = 0; m < 4; ++m) {   // d-block by d-block, so the merge starts on the first
+                const int mm = (m + rank + 1) & 3;   // this CTA's own d-block last: it is merged last
+                if (ok) {
+                    const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * mm) * (kBlkBytes >> 4));
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16(tmem + kTmemO + (uint32_t)(mm * kH), a + (uint64_t)(kk * (2048 >> 4)),
+                                  pd0 + (uint64_t)(((kk >> 2) * kQBlkBytes + (kk & 3) * 32) >> 4), idesc_pv, 1u);
+                }
+                umma_commit(&tl->pv_bar[mm]);
             }
-            umma_commit(&tl->o_done);
         }
         __syncwarp();
     } else {
@@ -398,25 +466,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             dead = __any_sync(kFull, dead);
         };
 
-        // online softmax over one tile's S^T (t = 0: the ring slice, 1: the compressed tile)
+        // online softmax over one tile's S^T (t = 0: the ring slice, 1: the compressed tile).  The
+        // set's 32 heads go 8 at a time through rolled loops (S re-read from TMEM in the second
+        // pass): each CTA runs this code only twice, so its size, not its issue count, decides
+        // how long the first run waits on instruction fetch.
         auto softmax_tile = [&](int t, bool valid) {
             mwait(&tl->s_full[t], 0);
             if (t == 1 && mt == 0) STI_DSTAMP(11);
             tc_fence_after();
-            float x[32];
-            {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + (uint32_t)(t * kH + hoff), r);
+            const uint32_t s_col = tmem + lane_base + (uint32_t)(t * kH + hoff);
+            auto load8 = [&](int c, float (&x)[8]) {   // this row's S of heads hoff + 8c .. + 8, log2 units
+                uint32_t r[8];
+                tmem_ld8(s_col + (uint32_t)(8 * c), r);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = (valid && !dead) ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
-            }
-            {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = x[i];
-                warp_reduce_scatter_n<32, true>(v);
-                tl->red_max[qd][hoff + lane] = v[0];
+                for (int i = 0; i < 8; ++i) x[i] = (valid && !dead) ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+            };
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {   // per-head maxima over this warp's 32 rows
+                float x[8];
+                load8(c, x);
+                warp_reduce_scatter_n<8, true>(x);   // lanes 4j..4j+3 hold head 8c + j
+                if ((lane & 3) == 0) tl->red_max[qd][hoff + 8 * c + (lane >> 2)] = x[0];
             }
             if (t == 1 && mt == 0) STI_DSTAMP(21);
             named_bar_sync(bar_set, 128);
@@ -435,32 +506,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the ring slice's PV has read P^T and written O^T before the tile's P^T and rescale
             if (t == 1) mwait(&tl->o_done, 0);
             tc_fence_after();
-            float v2[32];
+            uint8_t* pb = p_s + (row >> 6) * kQBlkBytes;   // P^T[h][row]: row block row/64, head h,
+            const int kr = row & 63;                       // 16-byte chunk ((row%64)/8) ^ (h%8)
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {   // probabilities (bf16 P^T) and per-head sums
+                float x[8];
+                load8(c, x);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float m = tl->m_run[hoff + i];
-                x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
-                v2[i] = x[i];
-            }
-            {   // P^T[h][row]: row block row/64, head h, 16-byte chunk ((row%64)/8) ^ (h%8)
-                uint8_t* pb = p_s + (row >> 6) * kQBlkBytes;
-                const int kr = row & 63;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int hi = hoff + i;
+                for (int i = 0; i < 8; ++i) {
+                    const int hi = hoff + 8 * c + i;
+                    const float m = tl->m_run[hi];
+                    x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
                     *reinterpret_cast<__nv_bfloat16*>(pb + hi * 128 + (((kr >> 3) ^ (hi & 7)) << 4) + (kr & 7) * 2) =
                         __float2bfloat16_rn(x[i]);
                 }
+                warp_reduce_scatter_n<8, false>(x);
+                if ((lane & 3) == 0) tl->red_sum[qd][hoff + 8 * c + (lane >> 2)] = x[0];
             }
             if (t == 1 && mt == 0) STI_DSTAMP(23);
-            warp_reduce_scatter_n<32, false>(v2);
-            tl->red_sum[qd][hoff + lane] = v2[0];
-            if (t == 1 && mt == 0) STI_DSTAMP(24);
             if (t == 1) {
                 bool rescale = false;
-#pragma unroll
                 for (int i = 0; i < 32; ++i) rescale = rescale || tl->alpha[hoff + i] != 1.f;
                 if (rescale && !dead) {   // O^T rows (lane = d within a block) times the heads' factors
+#pragma unroll 1
                     for (int m = 0; m < 4; ++m) {
                         const uint32_t ta = tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff);
                         uint32_t r[32];
@@ -474,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
             }
+            if (t == 1 && mt == 0) STI_DSTAMP(24);
             fence_proxy_async_smem();   // P^T: generic writes read by the MMA
             tc_fence_before();
             named_bar_sync(bar_set, 128);
@@ -485,106 +554,196 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st == 0) mbar_arrive(&tl->p_full);
         };
 
-        // ---- the ring slice (needs nothing of the step)
-        softmax_tile(0, row >= kRingRow0 && ring_valid(row - kRingRow0));
-        if (mt == 0) STI_DSTAMP(1);
+        // ---- top-k scratch in tile rows 0..95 (free until the gather; the ring slice's QK reads them
+        // only into masked rows of S): rows 64..95 of column blocks 0-1 and 2-3 hold the position
+        // bitmaps (keys above tau, keys equal to tau), of block 6 the pass-3 histogram; rows 0..63 of
+        // blocks 4-5 the threshold bin's members as every warp of the cluster found them (segment
+        // 8 * CTA + warp: up to kSegCap (key, position) pairs), and rows 0..63 of every block the
+        // staged scores of the row passes (only when the members overflow their segments); P^T rows
+        // 0..63 (the ring slice's probabilities use rows 96..127 only) the pass-2 histogram
+        auto bm = [&](int blk0, int w) {   // bitmap word w (blk0 = 0: keys > tau, 2: keys == tau)
+            return reinterpret_cast<uint32_t*>(tile + (size_t)(blk0 + (w >> 10)) * kBlkBytes + 8192) + (w & 1023);
+        };
+        auto seg = [&](int sg, int j) {   // member j of segment sg
+            const int i = sg * kSegCap + j;
+            return reinterpret_cast<uint2*>(tile + (size_t)(4 + (i >> 10)) * kBlkBytes) + (i & 1023);
+        };
+        uint32_t* h2 = reinterpret_cast<uint32_t*>(p_s);                           // [2048]
+        uint32_t* h3 = reinterpret_cast<uint32_t*>(tile + 6 * kBlkBytes + 8192);   // [1024]
 
-        // ---- top-k of the compressed positions (the scores and histogram are complete from here)
-        griddep_wait();
-        if (mt == 0) STI_DSTAMP(2);
-        const int vis = max(0, min((sp + 1) / p.ratio, n2));
-        const int my0 = kRows * rank;   // this CTA's output slots [my0, my0 + 128)
-        if (vis <= kK) {
-            // every visible position is selected: output slot o holds position o
-            if (mt < kRows) {
-                const int o = my0 + mt;
-                tl->tile_idx[mt] = o < vis ? o : -1;
-                idx_row[kW + o] = o < vis ? o + kW : -1;
+        // ---- the Indexer's top-k of one row, exact (ties to the lower position).  Each CTA scans a
+        // quarter of the row against the threshold bin of the scores kernel's histogram and sends
+        // what it finds to the whole cluster; every CTA then resolves the bin (passes 2 and 3 over
+        // its members) and keeps output slots [128 rank, 128 rank + 128): its tile's index list and
+        // its quarter of the published row.
+        auto topk_row = [&](int vis_) {
+            const int my0 = kRows * rank;
+            if (vis_ <= kK) {   // every visible position is selected: slot o holds position o
+                if (mt < kRows) {
+                    const int o = my0 + mt;
+                    tl->tile_idx[mt] = o < vis_ ? o : -1;
+                    idx_row[kW + o] = o < vis_ ? o + kW : -1;
+                }
+                if (rank == 0) {   // nobody reads the histogram: ready for the next call
+                    uint4* gh = reinterpret_cast<uint4*>(p.hist + (size_t)b * kBins);
+                    gh[2 * mt] = make_uint4(0, 0, 0, 0);
+                    gh[2 * mt + 1] = make_uint4(0, 0, 0, 0);
+                }
+                return;
             }
-        } else {
             const uint32_t* ghist = p.hist + (size_t)b * kBins;
             const float* src = p.scores + (size_t)b * n2;
-            // scratch in tile rows 0..95 (the first 12 KB of column blocks 0..3), free until the gather
-            uint32_t* bm_gt = reinterpret_cast<uint32_t*>(tile);                   // [2048] key > tau
-            uint32_t* bm_eq = reinterpret_cast<uint32_t*>(tile + kBlkBytes);       // [2048] key == tau
-            uint32_t* mem_key = reinterpret_cast<uint32_t*>(tile + 2 * kBlkBytes); // [1024] bin-d1 members
-            int* mem_pos = reinterpret_cast<int*>(tile + 2 * kBlkBytes + 4096);     // [1024]
-            uint32_t* h2 = reinterpret_cast<uint32_t*>(tile + 3 * kBlkBytes);      // [2048]
-            uint32_t* h3 = h2 + 2048;                                               // [1024]
-            // thread mt owns positions [mt*P, mt*P + P) (P a multiple of 32: whole bitmap words)
-            const int P = ((vis + 255) / 256 + 31) & ~31;
-            const int p0 = min(vis, mt * P), p1 = min(vis, p0 + P);
-            const int w0 = mt * (P / 32), nw = P / 32;
-            uint32_t h8[8];
-            {
-                const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(ghist) + 2 * mt);
-                const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(ghist) + 2 * mt + 1);
-                h8[0] = a0.x; h8[1] = a0.y; h8[2] = a0.z; h8[3] = a0.w;
-                h8[4] = a1.x; h8[5] = a1.y; h8[6] = a1.z; h8[7] = a1.w;
-            }
-            // every key of this thread's segment in 64-key batches: f(valid, position, key); a fixed
-            // trip count over the warp (the per-batch ballots need every lane).  Rows start 16-byte
-            // aligned only when n_cols is a multiple of 4: otherwise scalar loads
+            const int nwords = (vis_ + 31) / 32;
             const bool vec4 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0u;
-            auto for_keys = [&](auto&& f) {
-                for (int c0 = 0; c0 < P; c0 += 64) {
-                    float v[64];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int pos = mt * P + c0 + 4 * i;
-                        float4 f4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                        if (vec4 && pos + 3 < p1) {
-                            f4 = __ldg(reinterpret_cast<const float4*>(src + pos));
+            constexpr int kStage = 16384;
+            auto stage_ptr = [&](int i) {   // staged score i of the current round
+                return reinterpret_cast<const uint32_t*>(tile + (size_t)(i >> 11) * kBlkBytes) + (i & 2047);
+            };
+            // all words of the row in rounds: f(word, valid, position, key), warp mw taking four words
+            // per iteration (four independent load-compare-ballot chains), lane = bit
+            auto row_pass = [&](auto&& f) {
+                for (int r0 = 0; r0 < vis_; r0 += kStage) {
+                    const int rn = min(kStage, vis_ - r0);
+                    const bool v4 = vec4 && (r0 & 3) == 0;
+                    for (int c = mt; c < rn / 4; c += 256) {
+                        const int i = 4 * c;
+                        const uint32_t dst = smem_u32(stage_ptr(i));
+                        if (v4) {
+                            cp_async_16(dst, src + r0 + i, 16u);
                         } else {
-                            if (pos + 3 < p1) f4.w = __ldg(src + pos + 3);
-                            if (pos < p1) f4.x = __ldg(src + pos);
-                            if (pos + 1 < p1) f4.y = __ldg(src + pos + 1);
-                            if (pos + 2 < p1) f4.z = __ldg(src + pos + 2);
+                            for (int e = 0; e < 4; ++e) cp_async_4(dst + 4u * e, src + r0 + i + e);
                         }
-                        v[4 * i] = f4.x; v[4 * i + 1] = f4.y; v[4 * i + 2] = f4.z; v[4 * i + 3] = f4.w;
                     }
+                    for (int i = (rn & ~3) + mt; i < rn; i += 256) cp_async_4(smem_u32(stage_ptr(i)), src + r0 + i);
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    named_bar_sync(kBarMath, 256);
+                    const int w_lo = r0 / 32, w_hi = (r0 + rn + 31) / 32;
+                    for (int w4 = w_lo + 4 * mw; w4 < w_hi; w4 += 32) {
+                        uint32_t key[4];
+                        bool v[4];
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const int pos = mt * P + c0 + i;
-                        f(pos < p1, pos, float_key(v[i]));
+                        for (int q = 0; q < 4; ++q) {
+                            const int pos = 32 * (w4 + q) + lane;
+                            v[q] = w4 + q < w_hi && pos < vis_;
+                            key[q] = v[q] ? float_key(__uint_as_float(*stage_ptr(pos - r0))) : 0u;
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (w4 + q < w_hi) f(w4 + q, v[q], 32 * (w4 + q) + lane, key[q]);
                     }
+                    named_bar_sync(kBarMath, 256);   // before the next round overwrites the staged scores
                 }
             };
-            // pass 1 from the scores kernel's histogram: the threshold bin d1
-            int above1, c1;
-            const int d1 = select_bin_m(h8, kK, tl, mt, &above1, &c1);
-            const int remaining1 = kK - above1;   // keys of bin d1 to take (>= 1)
-            if (mt == 0) STI_DSTAMP(3);
-            // one pass: bitmap of keys above the bin; list of the bin's members
-            for (int w = 0; w < nw; ++w) bm_eq[w0 + w] = 0u;
+            // this CTA's quarter of the row; warp mw stages 16 words (32 scores each) at a time in
+            // rows 0..63 of column blocks 0-1, lane = bit (each lane reads back only its own copies)
+            const int wq = (nwords + kCtas - 1) / kCtas;
+            const int wa = min(nwords, rank * wq), wb = min(nwords, wa + wq);
+            float* stg = reinterpret_cast<float*>(tile + (size_t)(mw >> 2) * kBlkBytes + (size_t)(mw & 3) * 2048);
+            auto stage16 = [&](int g) {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int pos = 32 * (g + q) + lane;
+                    if (g + q < wb && pos < vis_) cp_async_4(smem_u32(stg + 32 * q + lane), src + pos);
+                }
+                cp_async_commit();
+            };
+            if (wa + 16 * mw < wb) stage16(wa + 16 * mw);   // in flight during the bin selection
+            // pass 1 from the scores kernel's histogram, copied to rows 0..63 of block 2: the threshold bin
+            uint32_t* h1 = reinterpret_cast<uint32_t*>(tile + 2 * kBlkBytes);
             {
-                uint32_t word = 0u;
-                for_keys([&](bool v, int pos, uint32_t key) {
-                    const uint32_t dig = key >> 21;
-                    if (v && dig > (uint32_t)d1) word |= 1u << (pos & 31);
-                    const bool m = v && dig == (uint32_t)d1;
-                    const unsigned bal = __ballot_sync(kFull, m);
-                    if (bal) {
-                        int base = 0;
-                        if (lane == 0) base = atomicAdd(&tl->n_mem, __popc(bal));
-                        base = __shfl_sync(kFull, base, 0);
-                        const int at = base + __popc(bal & ((1u << lane) - 1u));
-                        if (m && at < kMemCap) {
-                            mem_key[at] = key;
-                            mem_pos[at] = pos;
-                        }
-                    }
-                    if ((pos & 31) == 31) {
-                        if ((pos >> 5) < w0 + nw) bm_gt[pos >> 5] = word;
-                        word = 0u;
-                    }
-                });
+                const uint4* gh = reinterpret_cast<const uint4*>(ghist);
+                uint4* h14 = reinterpret_cast<uint4*>(h1);
+                const uint4 a0 = __ldcg(gh + 2 * mt), a1 = __ldcg(gh + 2 * mt + 1);
+                h14[2 * mt] = a0;
+                h14[2 * mt + 1] = a1;
             }
             named_bar_sync(kBarMath, 256);
+            const int3 s1 = select_bin_w(h1, 64, kK, lane);
+            const int d1 = s1.x, above1 = s1.y, c1 = s1.z;
+            const int remaining1 = kK - above1;   // keys of bin d1 to take (>= 1)
+            if (mt == 0) STI_DSTAMP(3);
+            // this CTA's quarter of the row, 16 words per warp at a time: each word of keys above the
+            // bin and each of the warp's members of the bin is stored here and, by st.async, in the
+            // other three CTAs, counted there on tk_bar; then the warp's member count, and one arrive
+            // per other CTA that announces the bytes sent to it
+            {
+                const int sg_own = 8 * rank + mw;
+                int cnt = 0, nw = 0;
+                for (int g = wa + 16 * mw; g < wb; g += 128) {
+                    cp_async_wait<0>();
+                    uint32_t my_above = 0u;
+#pragma unroll 4
+                    for (int q = 0; q < 16; ++q) {
+                        const int pos = 32 * (g + q) + lane;
+                        const bool v = g + q < wb && pos < vis_;
+                        const uint32_t key = float_key(stg[32 * q + lane]);
+                        const uint32_t dig = key >> 21;
+                        const unsigned above = __ballot_sync(kFull, v && dig > (uint32_t)d1);
+                        const bool m = v && dig == (uint32_t)d1;
+                        const unsigned mem = __ballot_sync(kFull, m);
+                        if (lane == q) my_above = above;
+                        const int at = cnt + __popc(mem & ((1u << lane) - 1u));
+                        if (m && at < kSegCap) {
+                            uint2* dst = seg(sg_own, at);
+                            *dst = make_uint2(key, (uint32_t)pos);
+#pragma unroll
+                            for (int c = 1; c < kCtas; ++c) {
+                                const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
+                                st_async_u2(dsmem_addr(dst, peer), key, (uint32_t)pos, dsmem_addr(&tl->tk_bar, peer));
+                            }
+                        }
+                        cnt += __popc(mem);
+                    }
+                    if (g + 128 < wb) stage16(g + 128);
+                    const int nq = min(16, wb - g);
+                    if (lane < nq) {
+                        uint32_t* dst = bm(0, g + lane);
+                        *dst = my_above;
+#pragma unroll
+                        for (int c = 1; c < kCtas; ++c) {
+                            const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
+                            st_async_b32(dsmem_addr(dst, peer), my_above, dsmem_addr(&tl->tk_bar, peer));
+                        }
+                    }
+                    nw += nq;
+                }
+                if (lane == 0) {
+                    tl->seg_cnt[sg_own] = cnt;
+                    const uint32_t bytes = 4u * (uint32_t)nw + 8u * (uint32_t)min(cnt, kSegCap) + 4u;
+#pragma unroll
+                    for (int c = 1; c < kCtas; ++c) {
+                        const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
+                        const uint32_t pbar = dsmem_addr(&tl->tk_bar, peer);
+                        st_async_b32(dsmem_addr(&tl->seg_cnt[sg_own], peer), (uint32_t)cnt, pbar);
+                        mbar_arrive_expect_tx_remote(pbar, bytes);
+                    }
+                }
+            }
+            named_bar_sync(kBarMath, 256);   // this CTA's words, members and counts
+            if (mt == 0) STI_DSTAMP(28);
+            if (!dead) dead = !attn_wait_cluster(&tl->tk_bar, 0, p.status, abort);   // the other CTAs'
+            dead = __any_sync(kFull, dead);
             if (mt == 0) STI_DSTAMP(4);
-            const int n_mem = tl->n_mem;
-            const bool listed = n_mem <= kMemCap && n_mem == c1;
-            // passes 2 and 3: the next 11 and 10 bits, over the listed members (or the whole row)
+            if (rank == 0) {   // every CTA of the cluster has read the histogram: ready for the next call
+                uint4* gh = reinterpret_cast<uint4*>(p.hist + (size_t)b * kBins);
+                gh[2 * mt] = make_uint4(0, 0, 0, 0);
+                gh[2 * mt + 1] = make_uint4(0, 0, 0, 0);
+            }
+            int n_mem = 0;
+            bool fits = true;
+#pragma unroll
+            for (int i = 0; i < 8 * kCtas; ++i) {
+                const int c = tl->seg_cnt[i];
+                n_mem += c;
+                fits = fits && c <= kSegCap;
+            }
+            // the members resolve the bin when none overflowed its segment (else: row passes)
+            const bool listed = !dead && fits && n_mem == c1;
+            const int sgm = mt >> 3, jm = mt & 7;   // thread mt: every eighth member of segment mt / 8
+            const int nseg = listed ? tl->seg_cnt[sgm] : 0;
+            if (mt == 0) STI_DSTAMP(37);
+            // passes 2 and 3: the next 11 and 10 bits (histograms zeroed before the scores were ready)
             uint32_t prefix = (uint32_t)d1;
             int remaining = remaining1;
             for (int pass = 0; pass < 2; ++pass) {
@@ -592,78 +751,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = pass == 0 ? 2048 : 1024;
                 const int hi_shift = pass == 0 ? 21 : 10, shift = pass == 0 ? 10 : 0;
                 const uint32_t mask = pass == 0 ? 0x7FFu : 0x3FFu;
-                for (int i = mt; i < nb; i += 256) hh[i] = 0u;
-                named_bar_sync(kBarMath, 256);
                 if (listed) {
-                    for (int i = mt; i < n_mem; i += 256) {
-                        const uint32_t key = mem_key[i];
+                    for (int j = jm; j < nseg; j += 8) {
+                        const uint32_t key = seg(sgm, j)->x;
                         if ((key >> hi_shift) == prefix) atomicAdd(&hh[(key >> shift) & mask], 1u);
                     }
+                    named_bar_sync(kBarMath, 256);
+                    if (mt == 0) STI_DSTAMP(40 + 3 * pass);
                 } else {
-                    for_keys([&](bool v, int, uint32_t key) {
+                    row_pass([&](int, bool v, int, uint32_t key) {
                         const bool m = v && (key >> hi_shift) == prefix;
                         const uint32_t dig = m ? (key >> shift) & mask : 0xFFFFFFFFu;
                         const unsigned peers = __match_any_sync(kFull, dig);
                         if (m && lane == __ffs(peers) - 1) atomicAdd(&hh[dig], (uint32_t)__popc(peers));
                     });
                 }
-                named_bar_sync(kBarMath, 256);
-                uint32_t hs[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hs[i] = 8 * mt + i < nb ? hh[8 * mt + i] : 0u;
-                int above_p, cnt_p;
-                const int dp = select_bin_m(hs, remaining, tl, mt, &above_p, &cnt_p);
-                remaining -= above_p;
+                const int3 sp_ = select_bin_w(hh, nb / 32, remaining, lane);
+                const int dp = sp_.x;
+                remaining -= sp_.y;
                 prefix = (prefix << (pass == 0 ? 11 : 10)) | (uint32_t)max(dp, 0);
+                if (mt == 0) STI_DSTAMP(41 + 3 * pass);
             }
-            if (mt == 0) STI_DSTAMP(5);
             const uint32_t tau = prefix;    // the exact k-th key
             const int need_eq = remaining;  // keys == tau taken, lowest positions first (>= 1)
-            // the bin's keys above tau join the bitmap; keys equal to tau get their own
+            if (mt == 0) STI_DSTAMP(5);
+            // the bin's keys above tau join the first bitmap; keys equal to tau get the second
             if (listed) {
-                for (int i = mt; i < n_mem; i += 256) {
-                    const uint32_t key = mem_key[i];
-                    const int pos = mem_pos[i];
-                    if (key > tau) atomicOr(&bm_gt[pos >> 5], 1u << (pos & 31));
-                    else if (key == tau) atomicOr(&bm_eq[pos >> 5], 1u << (pos & 31));
+                for (int j = jm; j < nseg; j += 8) {
+                    const uint2 kp = *seg(sgm, j);
+                    if (kp.x > tau) atomicOr(bm(0, (int)(kp.y >> 5)), 1u << (kp.y & 31));
+                    else if (kp.x == tau) atomicOr(bm(2, (int)(kp.y >> 5)), 1u << (kp.y & 31));
                 }
+                named_bar_sync(kBarMath, 256);
             } else {
-                for_keys([&](bool v, int pos, uint32_t key) {
-                    if (v && (key >> 21) == (uint32_t)d1) {
-                        if (key > tau) bm_gt[pos >> 5] |= 1u << (pos & 31);
-                        else if (key == tau) bm_eq[pos >> 5] |= 1u << (pos & 31);
+                row_pass([&](int w, bool v, int, uint32_t key) {
+                    const bool in_bin = v && (key >> 21) == (uint32_t)d1;
+                    const unsigned g = __ballot_sync(kFull, in_bin && key > tau);
+                    const unsigned e = __ballot_sync(kFull, in_bin && key == tau);
+                    if (lane == 0) {
+                        *bm(0, w) |= g;
+                        *bm(2, w) = e;
                     }
                 });
             }
-            named_bar_sync(kBarMath, 256);
-            // output slots in ascending position order: keys above tau, and the first need_eq keys
-            // equal to tau
-            int gt = 0, eq = 0;
-            for (int w = 0; w < nw; ++w) {
-                gt += __popc(bm_gt[w0 + w]);
-                eq += __popc(bm_eq[w0 + w]);
-            }
             if (mt == 0) STI_DSTAMP(6);
+            // output slots in ascending position order: keys above tau, and the first need_eq keys
+            // equal to tau; thread mt owns words [mt*nwt, mt*nwt + nwt)
+            const int nwt = (nwords + 255) / 256;
+            const int ws0 = min(nwords, mt * nwt), ws1 = min(nwords, ws0 + nwt);
+            int gt = 0, eq = 0;
+            for (int w = ws0; w < ws1; ++w) {
+                gt += __popc(*bm(0, w));
+                eq += __popc(*bm(2, w));
+            }
             int gt_before, eq_before, gt_tot, eq_tot;
             scan2_m(gt, eq, tl, mt, gt_before, eq_before, gt_tot, eq_tot);
             if (mt == 0) STI_DSTAMP(7);
             int o = gt_before + min(eq_before, need_eq);
             int eq_left = max(0, need_eq - eq_before);
-            for (int w = 0; w < nw && o < my0 + kRows; ++w) {
-                uint32_t e = bm_eq[w0 + w];
-                uint32_t take_e = 0u;
+            for (int w = ws0; w < ws1 && o < my0 + kRows; ++w) {
+                uint32_t e = *bm(2, w), take_e = 0u;
                 while (e && eq_left > 0) {   // the lowest positions first
                     const uint32_t lo_bit = e & (0u - e);
                     take_e |= lo_bit;
                     e ^= lo_bit;
                     --eq_left;
                 }
-                uint32_t sel = bm_gt[w0 + w] | take_e;
+                uint32_t sel = *bm(0, w) | take_e;
+                if (o + __popc(sel) <= my0) {   // the whole word falls before this CTA's slots
+                    o += __popc(sel);
+                    continue;
+                }
                 while (sel) {
                     const int bit = __ffs(sel) - 1;
                     sel &= sel - 1u;
                     if (o >= my0 && o < my0 + kRows) {
-                        const int pos = 32 * (w0 + w) + bit;
+                        const int pos = 32 * w + bit;
                         tl->tile_idx[o - my0] = pos;
                         idx_row[kW + o] = pos + kW;
                     }
@@ -671,78 +834,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (mt == 0) STI_DSTAMP(8);
-        }
-        // every index is in tile_idx; the scratch rows are free for the gather
-        named_bar_sync(kBarMath, 256);
-        if (mt == 0) STI_DSTAMP(9);
+        };
+
         // ---- gather the compressed tile: math warp mw copies column block mw (16-byte cp.async
-        // into the 128-byte-swizzled layout; masked rows zero-filled); rows 96..127 once the ring
-        // slice's PV has read them
-        {
-            const uint16_t* comp = p.comp_kv + (size_t)b * p.comp_bstride + (size_t)mw * 64;
+        // into the 128-byte-swizzled layout; masked rows zero-filled); rows 0..95 at once, rows
+        // 96..127 once the ring slice's PV has read them
+        const uint16_t* comp_blk = p.comp_kv + (size_t)b * p.comp_bstride + (size_t)mw * 64;
+        auto copy_rows = [&](int i0, int i1) {   // groups of four rows i0..i1-1 of column block mw
             const uint32_t blk = smem_u32(tile) + (uint32_t)mw * kBlkBytes;
             const int ch = lane & 7;
-            auto copy_rows = [&](int i0, int i1) {
-                for (int i = i0; i < i1; ++i) {
-                    const int r = 4 * i + (lane >> 3);
-                    const int raw = tl->tile_idx[r];
-                    const bool ok = raw >= 0 && raw < n2 && !dead;
-                    if (raw < -1 || raw >= n2) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);   // masked
-                    const uint16_t* s = ok ? comp + (size_t)raw * kD + ch * 8 : comp;
-                    cp_async_16(blk + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)), s, ok ? 16u : 0u);
-                }
-            };
-            copy_rows(0, 24);
+            for (int i = i0; i < i1; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const int raw = tl->tile_idx[r];
+                const bool ok = raw >= 0 && raw < n2 && !dead;
+                if (raw < -1 || raw >= n2) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);   // masked
+                const uint16_t* src = ok ? comp_blk + (size_t)raw * kD + ch * 8 : comp_blk;
+                cp_async_16(blk + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)), src, ok ? 16u : 0u);
+            }
+            cp_async_commit();
+        };
+        auto finish_gather = [&]() {
             mwait(&tl->ring_free, 0);
             copy_rows(24, 32);
-            cp_async_commit();
             cp_async_wait<0>();
             fence_proxy_async_smem();   // generic-proxy copies, read by the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(&tl->full[mw]);
-            if (mt == 0) STI_DSTAMP(10);
-        }
-        // ---- the compressed tile
-        softmax_tile(1, !dead && tl->tile_idx[row] >= 0 && tl->tile_idx[row] < n2);
-        if (mt == 0) STI_DSTAMP(12);
-        mwait(&tl->o_done, 1);
-        tc_fence_after();
+        };
 
-        // ---- merge through L2: the three d-blocks others own, [128 d][64 heads] fp32 each, and
-        // (m, l); then this CTA's d-block from the three others
+        // compressed row of tile row i once the indices are here: -1 when masked or out of range
+        auto tile_row = [&](int i) {
+            const int v = tl->tile_idx[i];
+            return (v >= 0 && v < n2) ? v : -1;
+        };
+        // the top-k (the step's critical path; warp 11 runs the ring slice's softmax meanwhile),
+        // the compressed tile's gather, then its softmax
+        // the histograms of passes 2 and 3 and the bitmap of keys equal to tau start at zero
+        for (int i = mt; i < 2048; i += 256) {
+            h2[i] = 0u;
+            *bm(2, i) = 0u;
+        }
+        for (int i = mt; i < 1024; i += 256) h3[i] = 0u;
+        griddep_wait();   // the scores and histogram are complete from here on
+        if (mt == 0) STI_DSTAMP(2);
+        topk_row(max(0, min((sp + 1) / p.ratio, n2)));
+        named_bar_sync(kBarMath, 256);   // every index is in tile_idx; the scratch rows are free
+        if (mt == 0) STI_DSTAMP(9);
+        copy_rows(0, 24);
+        if (mt == 0) STI_DSTAMP(1);
+        finish_gather();   // rows 96..127 once the ring slice's PV has read them
+        if (mt == 0) STI_DSTAMP(10);
+        mwait(&tl->p_full, 0);   // the ring slice's running max and sum (warp 11) are visible
+        softmax_tile(1, !dead && tile_row(row) >= 0);
+        if (mt == 0) STI_DSTAMP(12);
+
+        // ---- merge through L2, by bulk copies: each CTA stages the three d-blocks of its O^T that
+        // the others own as [64 heads][128 d] fp32 in its tile buffer (each as soon as its PV is
+        // done) and bulk-stores them (32 KB each), writes its (max, sum) per head, and signals the
+        // cluster; then it bulk-loads the three others' partials of its own d-block and combines
+        // them with its own
         const int d_loc = row;   // TMEM lane = d within a block
+        float* stage = reinterpret_cast<float*>(tile);   // slot m: [64][128] fp32 at m * 32 KB
+        constexpr uint32_t kPartBytes = kRows * kH * 4;
         auto xblk = [&](int owner, int src) -> float* {   // block `owner` written by CTA `src` != owner
             const int slot = src < owner ? src : src - 1;
             return p.xchg + ((size_t)(b * kCtas + owner) * 3 + slot) * (kRows * kH);
         };
-        if (!dead) {
-            for (int m = 0; m < kCtas; ++m) {
-                if (m == rank) continue;
+#pragma unroll 1
+        for (int j = 1; j < kCtas; ++j) {   // the others' d-blocks, in the order their PV ran
+            const int m = (j + rank) & 3;
+            mwait(&tl->pv_bar[m], 0);
+            tc_fence_after();
+            if (!dead) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
                 tmem_ld_wait();
-                float4* dst = reinterpret_cast<float4*>(xblk(m, rank) + (size_t)d_loc * kH + hoff);
+                float* dst = stage + (size_t)m * (kRows * kH) + (size_t)hoff * kRows + d_loc;
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    dst[c] = make_float4(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1]),
-                                         __uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3]));
+                for (int i = 0; i < 32; ++i) dst[(size_t)i * kRows] = __uint_as_float(r[i]);
+            }
+            fence_proxy_async_smem();   // generic writes, read by the bulk-copy engine
+            named_bar_sync(kBarMath, 256);
+            if (mt == 0 && !dead) {
+                bulk_store(xblk(m, rank), stage + (size_t)m * (kRows * kH), kPartBytes);
+                bulk_commit();
             }
         }
-        if (mt == 0) STI_DSTAMP(25);
         float* xml = p.xml + (size_t)(b * kCtas + rank) * 2 * kH;   // this CTA's (m, l) per head
         if (mt < kH) {
             xml[mt] = tl->m_run[mt];
             xml[kH + mt] = tl->l_run[mt];
+        }
+        if (mt == 0) {
+            bulk_wait_all();   // the writes are performed before the cluster is told
+            fence_proxy_async_global();
         }
         if (mt == 0) STI_DSTAMP(13);
         publish_to_cluster(&tl->pub_bar, mt);
         if (!dead) dead = !attn_wait_cluster(&tl->pub_bar, 0, p.status, abort);
         dead = __any_sync(kFull, dead);
         if (mt == 0) STI_DSTAMP(14);
-        if (rank == 0) {   // every CTA has read the histogram: ready for the next call
-            uint4* gh = reinterpret_cast<uint4*>(p.hist + (size_t)b * kBins);
-            gh[2 * mt] = make_uint4(0, 0, 0, 0);
-            gh[2 * mt + 1] = make_uint4(0, 0, 0, 0);
+        // the three others' partials of this CTA's d-block into staging slots 0..2 (their bulk
+        // stores have read them)
+        if (mt == 0 && !dead) {
+            fence_proxy_async_global();   // the acquired writes, then the bulk-copy engine's reads
+            mbar_arrive_expect_tx(&tl->recv_bar, 3 * kPartBytes);
+            for (int k = 0; k < kCtas - 1; ++k) {
+                const int c = k + (k >= rank ? 1 : 0);
+                bulk_load(stage + (size_t)k * (kRows * kH), xblk(rank, c), kPartBytes, &tl->recv_bar);
+            }
         }
         if (mt < kH) {   // the four partials' weights for head mt
             float mc[kCtas], lc[kCtas];
@@ -765,50 +965,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < kCtas; ++c) tl->wgt[c][mt] = M == -INFINITY ? 0.f : e[c] / L;
         }
-        named_bar_sync(kBarMath, 256);
-        if (mt == 0) STI_DSTAMP(26);
+        mwait(&tl->pv_bar[rank], 0);   // this CTA's own d-block (its PV ran last)
+        tc_fence_after();
+        float v[32];
         {
-            float v[32];
-            {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(rank * kH + hoff), r);
-                tmem_ld_wait();
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(rank * kH + hoff), r);
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * tl->wgt[rank][hoff + i];
-            }
-            // the three others' partials of this CTA's d-block (peer k is CTA k + (k >= rank)):
-            // two peers' loads in flight, then the third (128 registers a thread at 416 threads)
-            auto add_peers = [&](auto k0_c, auto n_c) {
-                constexpr int k0 = decltype(k0_c)::value, n = decltype(n_c)::value;
-                float4 q4[n][8];
-#pragma unroll
-                for (int k = 0; k < n; ++k) {
-                    const int c = (k0 + k) + (k0 + k >= rank ? 1 : 0);
-                    const float4* src4 = reinterpret_cast<const float4*>(xblk(rank, c) + (size_t)d_loc * kH + hoff);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) q4[k][j] = dead ? make_float4(0.f, 0.f, 0.f, 0.f) : __ldcg(src4 + j);
-                }
-#pragma unroll
-                for (int k = 0; k < n; ++k) {
-                    const int c = (k0 + k) + (k0 + k >= rank ? 1 : 0);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        v[4 * j] += q4[k][j].x * tl->wgt[c][hoff + 4 * j];
-                        v[4 * j + 1] += q4[k][j].y * tl->wgt[c][hoff + 4 * j + 1];
-                        v[4 * j + 2] += q4[k][j].z * tl->wgt[c][hoff + 4 * j + 2];
-                        v[4 * j + 3] += q4[k][j].w * tl->wgt[c][hoff + 4 * j + 3];
-                    }
-                }
-            };
-            add_peers(std::integral_constant<int, 0>(), std::integral_constant<int, 2>());
-            add_peers(std::integral_constant<int, 2>(), std::integral_constant<int, 1>());
-            const int dd = kRows * rank + d_loc;
-            if (p.rope_dims > 0 && kRows * rank + kRows > kD - p.rope_dims)   // the output's inverse rotation
-                rope_inverse_pairs<32>(v, dd, kD, p.rope_dims, p.rope_cs + (size_t)b * p.rope_dims);
-            uint16_t* orow = p.out + ((size_t)b * kH + hoff) * kD + dd;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) orow[(size_t)i * kD] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
         }
+        named_bar_sync(kBarMath, 256);   // the weights
+        if (mt == 0) STI_DSTAMP(26);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= tl->wgt[rank][hoff + i];
+        mwait(&tl->recv_bar, 0);
+#pragma unroll
+        for (int k = 0; k < kCtas - 1; ++k) {
+            const int c = k + (k >= rank ? 1 : 0);
+            const float* part = stage + (size_t)k * (kRows * kH) + (size_t)hoff * kRows + d_loc;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += (dead ? 0.f : part[(size_t)i * kRows]) * tl->wgt[c][hoff + i];
+        }
+        const int dd = kRows * rank + d_loc;
+        if (p.rope_dims > 0 && kRows * rank + kRows > kD - p.rope_dims)   // the output's inverse rotation
+            rope_inverse_pairs<32>(v, dd, kD, p.rope_dims, p.rope_cs + (size_t)b * p.rope_dims);
+        uint16_t* orow = p.out + ((size_t)b * kH + hoff) * kD + dd;   // lanes: consecutive d of a head
+#pragma unroll
+        for (int i = 0; i < 32; ++i) orow[(size_t)i * kD] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
         if (mt == 0) {
             STI_DSTAMP(15);
             STI_DCLOCK(31);
@@ -889,6 +1073,6 @@ cudaError_t launch_decode_topk_attn(const CUtensorMap& tm_q, const CUtensorMap& 
 #ifdef STI_DA_TIMING
 // profiling builds only: global-timer stamps of the fused decode kernel's CTAs
 extern "C" int sti_dbg_da_times(unsigned long long* host, int n_blocks) {
-    return (int)cudaMemcpyFromSymbol(host, sti::g_da_t, sizeof(unsigned long long) * 32 * (size_t)n_blocks);
+    return (int)cudaMemcpyFromSymbol(host, sti::g_da_t, sizeof(unsigned long long) * 64 * (size_t)n_blocks);
 }
 #endif

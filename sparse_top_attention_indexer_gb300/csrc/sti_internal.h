@@ -125,7 +125,7 @@ struct DecodeAttnParams {
     const float* rope_cs;      // optional [B, rope_dims/2, 2]: the output's inverse rotation
     int rope_dims;
     uint32_t* status;
-    float* xchg;               // merge scratch: [B][4 d-blocks][3 other CTAs][128 d][64 heads] fp32
+    float* xchg;               // merge scratch: [B][4 d-blocks][3 other CTAs][64 heads][128 d] fp32
     float* xml;                // merge scratch: [B][4 CTAs][2][64] fp32 (running max, sum)
     float scale_log2;          // softmax_scale * log2(e)
     int B, n_cols, ratio;

@@ -209,6 +209,10 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, 
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// 4-byte global->shared copy (L1-allocating form; the 16-byte form above bypasses L1).
+__device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst_smem), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -307,6 +311,13 @@ __device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask)
         : "memory");
 }
 
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -386,10 +397,25 @@ __device__ __forceinline__ void st_async_v2(uint32_t addr_cluster, float a, floa
                  : "memory");
 }
 
+__device__ __forceinline__ void st_async_u2(uint32_t addr_cluster, uint32_t a, uint32_t b, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+                     addr_cluster),
+                 "r"(a), "r"(b), "r"(bar_cluster)
+                 : "memory");
+}
+
 // 4-byte store into another CTA's shared memory counted (complete_tx) on that CTA's barrier.
 __device__ __forceinline__ void st_async_b32(uint32_t addr_cluster, uint32_t v, uint32_t bar_cluster) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr_cluster),
                  "r"(v), "r"(bar_cluster)
+                 : "memory");
+}
+
+// Arrive once on a barrier in another CTA of the cluster and add `bytes` to the transfer count it
+// waits for (the bytes this thread's st.async stores deliver there, before or after the arrive).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
+                 "r"(bytes)
                  : "memory");
 }
 
