@@ -566,23 +566,14 @@ static bool decode_fusable(const sti_decode_args* a) {
 }
 
 // fused decode workspace: [status | scores fp32 [b, n_cols] | first-pass histograms u32 [b, 2048] |
-//   attention accumulator fp32 [b, h, d] (batches of at most 256), or, when the top-k and attention
-//   run as one kernel, its merge scratch (partial outputs and per-head max and sum)]
+//   attention accumulator fp32 [b, h, d] (batches of at most 256; unused when the top-k and
+//   attention run as one kernel, which merges its partial outputs in shared memory)]
 static size_t decode_scores_bytes(const sti_decode_args* a) {
     return sti::align_up((size_t)a->b * (size_t)(a->n_cols > 0 ? a->n_cols : 1) * sizeof(float), sti::kWsAlign);
 }
 static size_t decode_hist_bytes(const sti_decode_args* a) { return (size_t)a->b * 2048 * sizeof(uint32_t); }
 
-static size_t decode_fused_scratch_bytes(int b) {
-    return sti::align_up(sti::decode_topk_attn_xchg_bytes(b), sti::kWsAlign) +
-           sti::align_up(sti::decode_topk_attn_xml_bytes(b), sti::kWsAlign);
-}
-static size_t decode_acc_bytes(const sti_decode_args* a) {
-    const size_t acc = attn_acc_bytes(a->b, 1, a->h, a->d);
-    if (!decode_shape_fusable(a)) return acc;
-    const size_t x = decode_fused_scratch_bytes(a->b);
-    return x > acc ? x : acc;
-}
+static size_t decode_acc_bytes(const sti_decode_args* a) { return attn_acc_bytes(a->b, 1, a->h, a->d); }
 
 size_t sti_decode_workspace_size(const sti_decode_args* a) {
     if (!a || a->b <= 0) return sti::kWsStatusBytes;
@@ -608,7 +599,7 @@ static bool decode_rope_ok(const sti_decode_args* a) {
 // Steps 2 and 3 of a decode step as the fused kernel (after the scores kernel filled `scores` and
 // `hist`); a programmatic dependent of the scores kernel unless it must wait for q_ready.
 static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* scores, uint32_t* hist,
-                                        uint32_t* status, uint8_t* scratch, cudaStream_t st) {
+                                        uint32_t* status, cudaStream_t st) {
     constexpr int kD = 512;
     if (a->q_ready) {
         const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a->q_ready), 0);
@@ -631,9 +622,6 @@ static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* s
     p.rows1 = a->window_bstride / kD;
     p.comp_kv = a->comp_kv;
     p.comp_bstride = a->comp_bstride;
-    p.xchg = reinterpret_cast<float*>(scratch);
-    const size_t xchg_bytes = sti::align_up(sti::decode_topk_attn_xchg_bytes(a->b), sti::kWsAlign);
-    p.xml = reinterpret_cast<float*>(scratch + xchg_bytes);
     CUtensorMap tm_q, tm_ring, tm_ring_rows;
     sti_status s = make_map_2d(&tm_q, a->q, kD, (uint64_t)a->b * 64, kD * 2, 64, 64);
     if (s == STI_OK) s = make_map_2d(&tm_ring, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 32);
@@ -682,7 +670,7 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
     if (decode_fusable(a)) {
-        s = decode_topk_attn_impl(a, scores, hist, status, reinterpret_cast<uint8_t*>(acc), st);
+        s = decode_topk_attn_impl(a, scores, hist, status, st);
         if (s != STI_OK) return s;
         if ((e = mark(2)) != cudaSuccess || (e = mark(3)) != cudaSuccess) return cuda_fail(e, "sti_decode_fused");
         return STI_OK;
@@ -776,9 +764,9 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     float* scores = reinterpret_cast<float*>(scratch + kNoallocScoresOff);
     uint32_t* hist = reinterpret_cast<uint32_t*>(scratch + kNoallocHistOff);
     float* acc = reinterpret_cast<float*>(scratch + kNoallocAccOff);
-    // the fused top-k + attention kernel's merge scratch shares the accumulator's place (it needs
-    // no zeroing); otherwise the split attention's accumulator, when it fits
-    const bool fused = decode_fusable(a) && decode_fused_scratch_bytes(a->b) <= kNoallocAccBytes;
+    // the fused top-k + attention kernel needs no accumulator; otherwise the split attention's,
+    // when it fits
+    const bool fused = decode_fusable(a);
     const size_t acc_need = attn_acc_bytes(a->b, 1, a->h, a->d);
     const size_t acc_used = fused ? 0 : (acc_need <= kNoallocAccBytes ? acc_need : 0);
     // the array still holds the previous call's data: zero the status word, the histograms and
@@ -793,7 +781,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
                             a->n_cols, a->ratio, scores, status, st, hist, decode_fp4(a, &fk));
         if (s != STI_OK) return s;
     }
-    if (fused) return decode_topk_attn_impl(a, scores, hist, status, reinterpret_cast<uint8_t*>(acc), st);
+    if (fused) return decode_topk_attn_impl(a, scores, hist, status, st);
     s = topk_impl(scores, a->start_pos, a->b, 1, a->n_cols, a->ratio, K, W, a->topk_idxs + W, k_total, status, st,
                   a->n_cols > 0 ? hist : nullptr, a->topk_idxs, W, W, /*pdl=*/a->n_cols > 0);
     if (s != STI_OK) return s;

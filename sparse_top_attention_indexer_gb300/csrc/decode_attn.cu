@@ -102,32 +102,23 @@ struct __align__(16) DaTail {
     uint64_t o_done;           // the ring slice's PV complete (O^T initialised)
     uint64_t ring_free;        // the ring slice's PV complete: rows 96..127 may be overwritten
     uint64_t pv_bar[4];        // the compressed tile's PV complete for d-block m
-    uint64_t pub_bar;          // merge: every CTA's partial outputs written (4 CTAs)
+    uint64_t free_bar;         // merge: every CTA's PV complete, its tile free to receive partials (4 CTAs)
+    uint64_t ml_bar;           // merge: the other CTAs' (max, sum) per head landed (bytes)
     uint64_t tk_bar;           // top-k: the other CTAs' words, members and counts landed (24 arrivals + bytes)
-    uint64_t recv_bar;         // merge: the three other CTAs' partials of this CTA's d-block landed
+    uint64_t recv_bar;         // merge: the three other CTAs' partials of this CTA's d-block landed (bytes)
     uint32_t tmem_base;
     int abort;
     int seg_cnt[8 * kCtas];    // top-k: members each warp of the cluster found in the threshold bin
     int warp_tot[8], warp_tot2[8];
     float m_run[kH], l_run[kH], alpha[kH];
     float red_max[4][kH], red_sum[4][kH];
-    float wgt[kCtas][kH];
+    float wgt[kCtas][kH];      // merge weights per head: [0, 3) the senders in slot order, 3 this CTA
+    float2 xml[kCtas - 1][kH]; // the other CTAs' (running max, sum) per head, in slot order
     int tile_idx[kRows];
 };
 
 constexpr size_t kSmemBytes = 1024 + kTileBytes + kQBytes + kPBytes + sizeof(DaTail);
 static_assert(kSmemBytes <= 232448, "shared memory of the fused decode kernel");
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// Publish this CTA's writes made before the call (by all 256 math threads; shared or global
-// memory) to the cluster: one release arrive on `bar` in each of the four CTAs.
-__device__ __forceinline__ void publish_to_cluster(uint64_t* bar, int mt) {
-    fence_acq_rel_cluster();
-    named_bar_sync(kBarMath, 256);
-    if (mt == 0)
-        for (int c = 0; c < kCtas; ++c) mbar_arrive_remote(dsmem_addr(bar, (uint32_t)c));
-}
 
 // Exclusive scan of two counts over the 256 math threads; returns the two totals too.
 __device__ __forceinline__ void scan2_m(int a, int b, DaTail* tl, int mt, int& a_before, int& b_before, int& a_tot,
@@ -246,9 +237,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->o_done, 1);
         mbar_init(&tl->ring_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&tl->pv_bar[m], 1);
-        mbar_init(&tl->pub_bar, kCtas);
+        mbar_init(&tl->free_bar, kCtas);
+        mbar_init(&tl->ml_bar, 1);
         mbar_init(&tl->tk_bar, (kCtas - 1) * 8);
         mbar_init(&tl->recv_bar, 1);
+        // the merge's incoming bytes, fixed: three (max, sum) vectors and three partial d-blocks
+        mbar_arrive_expect_tx(&tl->ml_bar, (kCtas - 1) * kH * 8);
+        mbar_arrive_expect_tx(&tl->recv_bar, (kCtas - 1) * kRows * kH * 4);
         tl->abort = 0;
         fence_mbar_init();
     }
@@ -463,6 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bounded waits of the math warps; `dead` stays warp-uniform (it guards warp collectives)
         auto mwait = [&](uint64_t* bar, uint32_t parity) {
             if (!dead) dead = !attn_wait(bar, parity, p.status, abort);
+            dead = __any_sync(kFull, dead);
+        };
+        auto mwait_c = [&](uint64_t* bar) {   // phase 0 of a barrier the cluster's st.async stores complete
+            if (!dead) dead = !attn_wait_cluster(bar, 0, p.status, abort);
             dead = __any_sync(kFull, dead);
         };
 
@@ -888,85 +887,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_tile(1, !dead && tile_row(row) >= 0);
         if (mt == 0) STI_DSTAMP(12);
 
-        // ---- merge through L2, by bulk copies: each CTA stages the three d-blocks of its O^T that
-        // the others own as [64 heads][128 d] fp32 in its tile buffer (each as soon as its PV is
-        // done) and bulk-stores them (32 KB each), writes its (max, sum) per head, and signals the
-        // cluster; then it bulk-loads the three others' partials of its own d-block and combines
-        // them with its own
+        // ---- merge in shared memory.  Each CTA sends its (max, sum) per head to the other three as
+        // soon as its softmax is done.  Once its PV is complete (tile, Q and P^T no longer read) it
+        // stages the three d-blocks of its O^T that the others own as [128 d][64 heads] fp32, the
+        // sixteen 16-byte chunks of a d row XOR-swizzled by d (tile bytes [96K, 128K), then Q), and
+        // when every CTA's PV is complete copies each to its owner's tile (bulk shared-to-shared
+        // copies counted on the owner's recv_bar; slot k at the owner, bytes [32K k, 32K k + 32K),
+        // comes from CTA k + (k >= owner)).  Then it combines its own block with the three received.
         const int d_loc = row;   // TMEM lane = d within a block
-        float* stage = reinterpret_cast<float*>(tile);   // slot m: [64][128] fp32 at m * 32 KB
+        if (st < 32 && !dead) {
+            const int hh = hoff + st;
+            const float2 ml = make_float2(tl->m_run[hh], tl->l_run[hh]);
+#pragma unroll
+            for (int c = 1; c < kCtas; ++c) {
+                const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
+                const int slot = rank < (int)peer ? rank : rank - 1;
+                st_async_u2(dsmem_addr(&tl->xml[slot][hh], peer), __float_as_uint(ml.x), __float_as_uint(ml.y),
+                            dsmem_addr(&tl->ml_bar, peer));
+            }
+        }
         constexpr uint32_t kPartBytes = kRows * kH * 4;
-        auto xblk = [&](int owner, int src) -> float* {   // block `owner` written by CTA `src` != owner
-            const int slot = src < owner ? src : src - 1;
-            return p.xchg + ((size_t)(b * kCtas + owner) * 3 + slot) * (kRows * kH);
+        auto out_stage = [&](int j) -> uint8_t* {   // staging of the block for CTA (rank + j) % 4
+            return j == 1 ? tile + 3 * kPartBytes : q_s + (size_t)(j - 2) * kPartBytes;
         };
 #pragma unroll 1
-        for (int j = 1; j < kCtas; ++j) {   // the others' d-blocks, in the order their PV ran
-            const int m = (j + rank) & 3;
-            mwait(&tl->pv_bar[m], 0);
-            tc_fence_after();
-            if (!dead) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
-                tmem_ld_wait();
-                float* dst = stage + (size_t)m * (kRows * kH) + (size_t)hoff * kRows + d_loc;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) dst[(size_t)i * kRows] = __uint_as_float(r[i]);
-            }
-            fence_proxy_async_smem();   // generic writes, read by the bulk-copy engine
-            named_bar_sync(kBarMath, 256);
-            if (mt == 0 && !dead) {
-                bulk_store(xblk(m, rank), stage + (size_t)m * (kRows * kH), kPartBytes);
-                bulk_commit();
-            }
-        }
-        float* xml = p.xml + (size_t)(b * kCtas + rank) * 2 * kH;   // this CTA's (m, l) per head
-        if (mt < kH) {
-            xml[mt] = tl->m_run[mt];
-            xml[kH + mt] = tl->l_run[mt];
-        }
-        if (mt == 0) {
-            bulk_wait_all();   // the writes are performed before the cluster is told
-            fence_proxy_async_global();
-        }
+        for (int j = 1; j <= kCtas; ++j) mwait(&tl->pv_bar[(j + rank) & 3], 0);   // this CTA's PV, all four blocks
+        tc_fence_after();
+        if (mt == 0 && !dead)
+            for (int c = 0; c < kCtas; ++c) mbar_arrive_remote(dsmem_addr(&tl->free_bar, (uint32_t)c));
         if (mt == 0) STI_DSTAMP(13);
-        publish_to_cluster(&tl->pub_bar, mt);
-        if (!dead) dead = !attn_wait_cluster(&tl->pub_bar, 0, p.status, abort);
+        const uint32_t swz = (uint32_t)(d_loc & 7);
+#pragma unroll 1
+        for (int j = 1; j < kCtas && !dead; ++j) {   // the others' d-blocks, staged
+            const int m = (j + rank) & 3;
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
+            tmem_ld_wait();
+            uint8_t* dst = out_stage(j) + (size_t)d_loc * 256;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(dst + ((((uint32_t)(8 * set + c)) ^ swz) << 4)) =
+                    make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        }
+        fence_proxy_async_smem();   // generic writes, read by the bulk copies
+        named_bar_sync(kBarMath, 256);
+        if (!dead) dead = !attn_wait_cluster(&tl->free_bar, 0, p.status, abort);
         dead = __any_sync(kFull, dead);
         if (mt == 0) STI_DSTAMP(14);
-        // the three others' partials of this CTA's d-block into staging slots 0..2 (their bulk
-        // stores have read them)
-        if (mt == 0 && !dead) {
-            fence_proxy_async_global();   // the acquired writes, then the bulk-copy engine's reads
-            mbar_arrive_expect_tx(&tl->recv_bar, 3 * kPartBytes);
-            for (int k = 0; k < kCtas - 1; ++k) {
-                const int c = k + (k >= rank ? 1 : 0);
-                bulk_load(stage + (size_t)k * (kRows * kH), xblk(rank, c), kPartBytes, &tl->recv_bar);
-            }
+        if (mt < kCtas - 1 && !dead) {   // thread j - 1 copies the block of CTA (rank + j) % 4
+            const int j = mt + 1;
+            const int m = (j + rank) & 3;
+            const int slot = rank < m ? rank : rank - 1;
+            bulk_copy_to_peer(dsmem_addr(tile, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
+                              dsmem_addr(&tl->recv_bar, (uint32_t)m));
         }
-        if (mt < kH) {   // the four partials' weights for head mt
+        if (mt == 0) STI_DSTAMP(25);
+        mwait_c(&tl->ml_bar);
+        if (st < 32) {   // the four partials' weights for head hoff + st (whose max and sum this thread wrote)
+            const int hh = hoff + st;
             float mc[kCtas], lc[kCtas];
             float M = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kCtas; ++c) {
-                const float* xc = p.xml + (size_t)(b * kCtas + c) * 2 * kH;
-                mc[c] = dead ? -INFINITY : (c == rank ? tl->m_run[mt] : __ldcg(xc + mt));
-                lc[c] = dead ? 0.f : (c == rank ? tl->l_run[mt] : __ldcg(xc + kH + mt));
-                M = fmaxf(M, mc[c]);
+            for (int k = 0; k < kCtas; ++k) {
+                const float2 ml = k < kCtas - 1 ? tl->xml[k][hh] : make_float2(tl->m_run[hh], tl->l_run[hh]);
+                mc[k] = dead ? -INFINITY : ml.x;
+                lc[k] = dead ? 0.f : ml.y;
+                M = fmaxf(M, mc[k]);
             }
             float L = 0.f;
             float e[kCtas];
 #pragma unroll
-            for (int c = 0; c < kCtas; ++c) {
-                e[c] = (M == -INFINITY || mc[c] == -INFINITY) ? 0.f : exp2f(mc[c] - M);
-                L += lc[c] * e[c];
+            for (int k = 0; k < kCtas; ++k) {
+                e[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : exp2f(mc[k] - M);
+                L += lc[k] * e[k];
             }
-            if (M != -INFINITY) L += exp2f(__ldg(p.sink + mt) * kLog2e - M);
+            if (M != -INFINITY) L += exp2f(__ldg(p.sink + hh) * kLog2e - M);
 #pragma unroll
-            for (int c = 0; c < kCtas; ++c) tl->wgt[c][mt] = M == -INFINITY ? 0.f : e[c] / L;
+            for (int k = 0; k < kCtas; ++k) tl->wgt[k][hh] = M == -INFINITY ? 0.f : e[k] / L;
         }
-        mwait(&tl->pv_bar[rank], 0);   // this CTA's own d-block (its PV ran last)
-        tc_fence_after();
         float v[32];
         {
             uint32_t r[32];
@@ -978,14 +976,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarMath, 256);   // the weights
         if (mt == 0) STI_DSTAMP(26);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= tl->wgt[rank][hoff + i];
-        mwait(&tl->recv_bar, 0);
-#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= tl->wgt[kCtas - 1][hoff + i];
+        mwait_c(&tl->recv_bar);
+#pragma unroll 1
         for (int k = 0; k < kCtas - 1; ++k) {
-            const int c = k + (k >= rank ? 1 : 0);
-            const float* part = stage + (size_t)k * (kRows * kH) + (size_t)hoff * kRows + d_loc;
+            const uint8_t* part = tile + (size_t)k * kPartBytes + (size_t)d_loc * 256;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += (dead ? 0.f : part[(size_t)i * kRows]) * tl->wgt[c][hoff + i];
+            for (int c = 0; c < 8; ++c) {
+                const float4 x = dead ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : *reinterpret_cast<const float4*>(part + (((uint32_t)(8 * set + c) ^ swz) << 4));
+                v[4 * c] += x.x * tl->wgt[k][hoff + 4 * c];
+                v[4 * c + 1] += x.y * tl->wgt[k][hoff + 4 * c + 1];
+                v[4 * c + 2] += x.z * tl->wgt[k][hoff + 4 * c + 2];
+                v[4 * c + 3] += x.w * tl->wgt[k][hoff + 4 * c + 3];
+            }
         }
         const int dd = kRows * rank + d_loc;
         if (p.rope_dims > 0 && kRows * rank + kRows > kD - p.rope_dims)   // the output's inverse rotation

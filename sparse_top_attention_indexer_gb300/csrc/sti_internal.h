@@ -125,15 +125,10 @@ struct DecodeAttnParams {
     const float* rope_cs;      // optional [B, rope_dims/2, 2]: the output's inverse rotation
     int rope_dims;
     uint32_t* status;
-    float* xchg;               // merge scratch: [B][4 d-blocks][3 other CTAs][64 heads][128 d] fp32
-    float* xml;                // merge scratch: [B][4 CTAs][2][64] fp32 (running max, sum)
     float scale_log2;          // softmax_scale * log2(e)
     int B, n_cols, ratio;
     int64_t rows1;             // rows per batch element of the ring (batch stride / 512)
 };
-// Bytes of the merge scratch for b queries (16-byte aligned parts: xchg then xml).
-inline size_t decode_topk_attn_xchg_bytes(int b) { return (size_t)b * 4 * 3 * 128 * 64 * 4; }
-inline size_t decode_topk_attn_xml_bytes(int b) { return (size_t)b * 4 * 2 * 64 * 4; }
 bool decode_topk_attn_available();
 size_t decode_topk_attn_smem_bytes();
 // tm_q: q as [B*64, 512] (box 64 x 64); tm_ring: the ring as [B*rows1, 512] (box 64 x 32, a full
