@@ -559,6 +559,7 @@ static bool decode_shape_fusable(const sti_decode_args* a) {
     if (!aligned(a->q, 16) || !aligned(a->window_kv, 16) || !aligned(a->comp_kv, 16) || !aligned(a->out, 16))
         return false;
     if ((int64_t)a->b * (a->window_bstride / kD) >= 0x7FFFFFFF || (int64_t)a->b * 64 >= 0x7FFFFFFF) return false;
+    if ((int64_t)a->b * (a->comp_bstride / kD) >= 0x7FFFFFFF) return false;
     return true;
 }
 static bool decode_fusable(const sti_decode_args* a) {
@@ -622,12 +623,15 @@ static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* s
     p.rows1 = a->window_bstride / kD;
     p.comp_kv = a->comp_kv;
     p.comp_bstride = a->comp_bstride;
-    CUtensorMap tm_q, tm_ring, tm_ring_rows;
+    p.rows_c = a->comp_bstride / kD;
+    CUtensorMap tm_q, tm_ring, tm_ring_rows, tm_comp_rows;
     sti_status s = make_map_2d(&tm_q, a->q, kD, (uint64_t)a->b * 64, kD * 2, 64, 64);
     if (s == STI_OK) s = make_map_2d(&tm_ring, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 32);
     if (s == STI_OK) s = make_map_2d(&tm_ring_rows, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 1);
+    if (s == STI_OK) s = make_map_2d(&tm_comp_rows, a->comp_kv, kD, (uint64_t)a->b * p.rows_c, kD * 2, 64, 1);
     if (s != STI_OK) return s;
-    const cudaError_t e = sti::launch_decode_topk_attn(tm_q, tm_ring, tm_ring_rows, p, /*pdl=*/!a->q_ready, st);
+    const cudaError_t e =
+        sti::launch_decode_topk_attn(tm_q, tm_ring, tm_ring_rows, tm_comp_rows, p, /*pdl=*/!a->q_ready, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_decode_fused: top-k + attention");
 }
 

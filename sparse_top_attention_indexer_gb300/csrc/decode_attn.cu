@@ -94,7 +94,7 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr uint32_t kBarMath = 1, kBarSet0 = 2;   // named barriers: the 256 math threads; each set of 128
 
 struct __align__(16) DaTail {
-    uint64_t full[8];          // compressed tile, column block j landed (its math warp's copies)
+    uint64_t full[8];          // compressed tile, column block j landed (8 math-warp arrivals + bytes)
     uint64_t q_bar;            // Q landed
     uint64_t ring_bar;         // the ring slice landed (4 loader arrivals + bytes)
     uint64_t s_full[2];        // S^T of the ring slice / of the compressed tile in TMEM
@@ -202,7 +202,8 @@ __device__ __forceinline__ int3 select_bin_w(const uint32_t* h, int per, int rem
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_topk_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ring,
-                            const __grid_constant__ CUtensorMap tm_ring_rows, const DecodeAttnParams p) {
+                            const __grid_constant__ CUtensorMap tm_ring_rows,
+                            const __grid_constant__ CUtensorMap tm_comp_rows, const DecodeAttnParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* tile = smem;                          // 8 column blocks x [128 rows x 128 B], SW128
@@ -228,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int j = 0; j < 8; ++j) mbar_init(&tl->full[j], 1);
+        for (int j = 0; j < 8; ++j) mbar_init(&tl->full[j], 8);
         mbar_init(&tl->q_bar, 1);
         mbar_init(&tl->ring_bar, 4);
         mbar_init(&tl->s_full[0], 1);
@@ -263,6 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tl->tmem_base;
     // TMEM columns: S^T of the ring slice [0, 64), of the compressed tile [64, 128), O^T [128, 384)
     constexpr uint32_t kTmemO = 128;
+    // [384, 448): the compressed tile's second partial S^T (its QK alternates two accumulators so
+    // consecutive MMAs do not wait on each other; the softmax adds the two)
+    constexpr uint32_t kTmemS2 = 384;
 
     // ring slot 32*rank + i (tile row 96 + i) holds a position <= start_pos: every slot of a full
     // ring, slot s itself (position s) while the ring is filling
@@ -275,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 tma_prefetch_desc(&tm_ring);
                 tma_prefetch_desc(&tm_ring_rows);
+                tma_prefetch_desc(&tm_comp_rows);
                 mbar_arrive_expect_tx(&tl->q_bar, kQBytes);
                 for (int cb = 0; cb < 8; ++cb)
                     tma_load_2d(q_s + (size_t)cb * kQBlkBytes, &tm_q, &tl->q_bar, cb * 64, b * kH);
@@ -418,29 +423,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(&tl->o_done);
             umma_commit(&tl->ring_free);
-            for (int j = 0; j < 8; ++j) {   // QK of the compressed tile, column block by column block
-                ok = ok && attn_wait(&tl->full[j], 0, p.status, abort);
-                if (j == 0) STI_DSTAMP(18);
+            for (int j = 0; j < 8; ++j) {   // QK of the compressed tile, column block by column block, its
+                ok = ok && attn_wait(&tl->full[j], 0, p.status, abort);   // K steps alternating between
+                if (j == 0) STI_DSTAMP(18);                                // two accumulators
                 if (j == 7) STI_DSTAMP(19);
                 if (ok) {
                     tc_fence_after();
-                    qk_block(64, j);
+                    const uint64_t a = kd0 + (uint64_t)((uint32_t)j * (kBlkBytes >> 4));
+                    const uint64_t bq = qd0 + (uint64_t)((uint32_t)j * (kQBlkBytes >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16(tmem + ((kk & 1) ? kTmemS2 : (uint32_t)kH), a + 2 * kk, bq + 2 * kk, idesc_qk,
+                                  (j > 0 || kk > 1) ? 1u : 0u);
                 }
             }
             umma_commit(&tl->s_full[1]);
             ok = ok && attn_wait(&tl->p_full, 1, p.status, abort);
             STI_DSTAMP(20);
-            if (ok) tc_fence_after();
-            for (int m = 0; m < 4; ++m) {   // d-block by d-block, so the merge starts on the first
-                const int mm = (m + rank + 1) & 3;   // this CTA's own d-block last: it is merged last
-                if (ok) {
-                    const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * mm) * (kBlkBytes >> 4));
-                    for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16(tmem + kTmemO + (uint32_t)(mm * kH), a + (uint64_t)(kk * (2048 >> 4)),
+            if (ok) {   // K step by K step over the four d-blocks' independent accumulators
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * m) * (kBlkBytes >> 4));
+                        umma_bf16(tmem + kTmemO + (uint32_t)(m * kH), a + (uint64_t)(kk * (2048 >> 4)),
                                   pd0 + (uint64_t)(((kk >> 2) * kQBlkBytes + (kk & 3) * 32) >> 4), idesc_pv, 1u);
-                }
-                umma_commit(&tl->pv_bar[mm]);
+                    }
             }
+            for (int m = 0; m < 4; ++m) umma_commit(&tl->pv_bar[m]);
         }
         __syncwarp();
     } else {
@@ -475,11 +485,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t s_col = tmem + lane_base + (uint32_t)(t * kH + hoff);
             auto load8 = [&](int c, float (&x)[8]) {   // this row's S of heads hoff + 8c .. + 8, log2 units
-                uint32_t r[8];
+                uint32_t r[8], r2[8];
                 tmem_ld8(s_col + (uint32_t)(8 * c), r);
+                tmem_ld8(s_col + (kTmemS2 - (uint32_t)kH) + (uint32_t)(8 * c), r2);   // the second partial
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = (valid && !dead) ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                for (int i = 0; i < 8; ++i)
+                    x[i] = (valid && !dead) ? (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * p.scale_log2
+                                            : -INFINITY;
             };
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {   // per-head maxima over this warp's 32 rows
@@ -835,30 +848,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mt == 0) STI_DSTAMP(8);
         };
 
-        // ---- gather the compressed tile: math warp mw copies column block mw (16-byte cp.async
-        // into the 128-byte-swizzled layout; masked rows zero-filled); rows 0..95 at once, rows
-        // 96..127 once the ring slice's PV has read them
-        const uint16_t* comp_blk = p.comp_kv + (size_t)b * p.comp_bstride + (size_t)mw * 64;
-        auto copy_rows = [&](int i0, int i1) {   // groups of four rows i0..i1-1 of column block mw
-            const uint32_t blk = smem_u32(tile) + (uint32_t)mw * kBlkBytes;
-            const int ch = lane & 7;
-            for (int i = i0; i < i1; ++i) {
-                const int r = 4 * i + (lane >> 3);
-                const int raw = tl->tile_idx[r];
+        // ---- gather the compressed tile: math warp mw loads rows 16mw..16mw+15, lane l the four rows
+        // of group 4mw + l/8 in column block l%8 by one four-row TMA gather (so the eight pieces of a
+        // row leave together; in the tile's 128-byte swizzle; masked rows of a group repeat its first
+        // valid row, whose probability is zero; groups with none are zeroed).  Rows 96..127 load once
+        // the ring slice's PV has read them.  Column block j is complete when its bytes and one
+        // arrive of every math warp reached full[j].
+        auto gather_comp = [&]() {
+            const int grp = 4 * mw + (lane >> 3), cb = lane & 7;
+            int ys[4], first = -1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int raw = tl->tile_idx[4 * grp + i];
                 const bool ok = raw >= 0 && raw < n2 && !dead;
-                if (raw < -1 || raw >= n2) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);   // masked
-                const uint16_t* src = ok ? comp_blk + (size_t)raw * kD + ch * 8 : comp_blk;
-                cp_async_16(blk + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)), src, ok ? 16u : 0u);
+                if (cb == 0 && (raw < -1 || raw >= n2)) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);   // masked
+                ys[i] = ok ? b * (int)p.rows_c + raw : -1;
+                if (ok && first < 0) first = ys[i];
             }
-            cp_async_commit();
-        };
-        auto finish_gather = [&]() {
-            mwait(&tl->ring_free, 0);
-            copy_rows(24, 32);
-            cp_async_wait<0>();
-            fence_proxy_async_smem();   // generic-proxy copies, read by the tensor core
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ys[i] = ys[i] >= 0 ? ys[i] : first;
+            const bool issue = first >= 0;
+            const unsigned im = __ballot_sync(kFull, issue);   // the same for the eight lanes of a group
+            if (lane < 8) mbar_expect_tx(&tl->full[lane], (uint32_t)__popc(im) * 64u);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tl->full[mw]);
+            uint8_t* dst = tile + (size_t)cb * kBlkBytes + (size_t)grp * 512;
+            if (mw >= 6) mwait(&tl->ring_free, 0);   // rows 96..127
+            if (issue) {
+                tma_gather4(dst, &tm_comp_rows, &tl->full[cb], cb * 64, ys[0], ys[1], ys[2], ys[3]);
+            } else {
+#pragma unroll 4
+                for (int i = 0; i < 32; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();   // zeroed rows: generic writes, read by the tensor core
+            }
+            __syncwarp();
+            if (lane < 8) mbar_arrive(&tl->full[lane]);
         };
 
         // compressed row of tile row i once the indices are here: -1 when masked or out of range
@@ -879,9 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         topk_row(max(0, min((sp + 1) / p.ratio, n2)));
         named_bar_sync(kBarMath, 256);   // every index is in tile_idx; the scratch rows are free
         if (mt == 0) STI_DSTAMP(9);
-        copy_rows(0, 24);
-        if (mt == 0) STI_DSTAMP(1);
-        finish_gather();   // rows 96..127 once the ring slice's PV has read them
+        gather_comp();
         if (mt == 0) STI_DSTAMP(10);
         mwait(&tl->p_full, 0);   // the ring slice's running max and sum (warp 11) are visible
         softmax_tile(1, !dead && tile_row(row) >= 0);
@@ -1049,7 +1070,8 @@ bool decode_topk_attn_available() {
 }
 
 cudaError_t launch_decode_topk_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_ring, const CUtensorMap& tm_ring_rows,
-                                    const DecodeAttnParams& p, bool pdl, cudaStream_t stream) {
+                                    const CUtensorMap& tm_comp_rows, const DecodeAttnParams& p, bool pdl,
+                                    cudaStream_t stream) {
     if (p.B == 0) return cudaSuccess;
     cudaError_t err =
         cudaFuncSetAttribute(decode_topk_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -1068,7 +1090,7 @@ cudaError_t launch_decode_topk_attn(const CUtensorMap& tm_q, const CUtensorMap& 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    err = cudaLaunchKernelEx(&cfg, decode_topk_attn_kernel, tm_q, tm_ring, tm_ring_rows, p);
+    err = cudaLaunchKernelEx(&cfg, decode_topk_attn_kernel, tm_q, tm_ring, tm_ring_rows, tm_comp_rows, p);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -128,14 +128,16 @@ struct DecodeAttnParams {
     float scale_log2;          // softmax_scale * log2(e)
     int B, n_cols, ratio;
     int64_t rows1;             // rows per batch element of the ring (batch stride / 512)
+    int64_t rows_c;            // rows per batch element of the compressed KV (comp_bstride / 512)
 };
 bool decode_topk_attn_available();
 size_t decode_topk_attn_smem_bytes();
 // tm_q: q as [B*64, 512] (box 64 x 64); tm_ring: the ring as [B*rows1, 512] (box 64 x 32, a full
 // ring's slice per CTA); tm_ring_rows: the same with box 64 x 1, for four-row gathers (whose box is
-// one row high).
+// one row high); tm_comp_rows: the compressed KV as [B*rows_c, 512], box 64 x 1.
 cudaError_t launch_decode_topk_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_ring, const CUtensorMap& tm_ring_rows,
-                                    const DecodeAttnParams& p, bool pdl, cudaStream_t stream);
+                                    const CUtensorMap& tm_comp_rows, const DecodeAttnParams& p, bool pdl,
+                                    cudaStream_t stream);
 
 // ------------------------------------------------------------------ device properties
 int device_num_sms();
