@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const float m = tl->m_run[i];
-                x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
+                x[i] = (m == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
                 *reinterpret_cast<__nv_bfloat16*>(pb + i * 128 + (((kr >> 3) ^ (i & 7)) << 4) + (kr & 7) * 2) =
                     __float2bfloat16_rn(x[i]);
             }
@@ -438,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             umma_commit(&tl->s_full[1]);
+            STI_DSTAMP(50);
             ok = ok && attn_wait(&tl->p_full, 1, p.status, abort);
             STI_DSTAMP(20);
             if (ok) {   // K step by K step over the four d-blocks' independent accumulators
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
             }
             for (int m = 0; m < 4; ++m) umma_commit(&tl->pv_bar[m]);
+            STI_DSTAMP(45);
         }
         __syncwarp();
     } else {
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_old = tl->m_run[hh];
                 // the running max moves only when a tile's max passes it by more than 8 (log2 units)
                 const float m_new = (m_old == -INFINITY || mx > m_old + 8.f) ? fmaxf(m_old, mx) : m_old;
-                tl->alpha[hh] = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+                tl->alpha[hh] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_old - m_new);
                 tl->m_run[hh] = m_new;
             }
             named_bar_sync(bar_set, 128);
@@ -528,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 8; ++i) {
                     const int hi = hoff + 8 * c + i;
                     const float m = tl->m_run[hi];
-                    x[i] = (m == -INFINITY) ? 0.f : exp2f(x[i] - m);
+                    x[i] = (m == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
                     *reinterpret_cast<__nv_bfloat16*>(pb + hi * 128 + (((kr >> 3) ^ (hi & 7)) << 4) + (kr & 7) * 2) =
                         __float2bfloat16_rn(x[i]);
                 }
@@ -756,9 +758,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nseg = listed ? tl->seg_cnt[sgm] : 0;
             if (mt == 0) STI_DSTAMP(37);
             // passes 2 and 3: the next 11 and 10 bits (histograms zeroed before the scores were ready)
+            // a bin taken whole ends the passes: every key from its prefix up is selected
             uint32_t prefix = (uint32_t)d1;
             int remaining = remaining1;
-            for (int pass = 0; pass < 2; ++pass) {
+            bool whole = c1 == remaining1;
+            int bits_left = 21;   // key bits below the prefix
+            for (int pass = 0; pass < 2 && !whole; ++pass) {
                 uint32_t* hh = pass == 0 ? h2 : h3;
                 const int nb = pass == 0 ? 2048 : 1024;
                 const int hi_shift = pass == 0 ? 21 : 10, shift = pass == 0 ? 10 : 0;
@@ -779,13 +784,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     });
                 }
                 const int3 sp_ = select_bin_w(hh, nb / 32, remaining, lane);
-                const int dp = sp_.x;
                 remaining -= sp_.y;
-                prefix = (prefix << (pass == 0 ? 11 : 10)) | (uint32_t)max(dp, 0);
+                prefix = (prefix << (pass == 0 ? 11 : 10)) | (uint32_t)max(sp_.x, 0);
+                bits_left = pass == 0 ? 10 : 0;
+                whole = sp_.z == remaining;
                 if (mt == 0) STI_DSTAMP(41 + 3 * pass);
             }
-            const uint32_t tau = prefix;    // the exact k-th key
-            const int need_eq = remaining;  // keys == tau taken, lowest positions first (>= 1)
+            // keys > tau are taken, and the first need_eq keys == tau (lowest positions first): tau is
+            // the exact k-th key after pass 3, else the smallest key of the bin taken whole (all of
+            // whose keys are taken)
+            const uint32_t tau = prefix << bits_left;
+            const int need_eq = whole ? (1 << 30) : remaining;
             if (mt == 0) STI_DSTAMP(5);
             // the bin's keys above tau join the first bitmap; keys equal to tau get the second
             if (listed) {
@@ -932,10 +941,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             return j == 1 ? tile + 3 * kPartBytes : q_s + (size_t)(j - 2) * kPartBytes;
         };
 #pragma unroll 1
-        for (int j = 1; j <= kCtas; ++j) mwait(&tl->pv_bar[(j + rank) & 3], 0);   // this CTA's PV, all four blocks
+        for (int j = 1; j <= kCtas; ++j) {   // this CTA's PV, all four blocks
+            mwait(&tl->pv_bar[(j + rank) & 3], 0);
+            if (mt == 0) STI_DSTAMP(45 + j);
+        }
         tc_fence_after();
         if (mt == 0 && !dead)
-            for (int c = 0; c < kCtas; ++c) mbar_arrive_remote(dsmem_addr(&tl->free_bar, (uint32_t)c));
+            for (int c = 0; c < kCtas; ++c) mbar_arrive_remote_relaxed(dsmem_addr(&tl->free_bar, (uint32_t)c));
         if (mt == 0) STI_DSTAMP(13);
         const uint32_t swz = (uint32_t)(d_loc & 7);
 #pragma unroll 1
@@ -979,10 +991,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float e[kCtas];
 #pragma unroll
             for (int k = 0; k < kCtas; ++k) {
-                e[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : exp2f(mc[k] - M);
+                e[k] = (M == -INFINITY || mc[k] == -INFINITY) ? 0.f : fast_exp2(mc[k] - M);
                 L += lc[k] * e[k];
             }
-            if (M != -INFINITY) L += exp2f(__ldg(p.sink + hh) * kLog2e - M);
+            if (M != -INFINITY) L += fast_exp2(__ldg(p.sink + hh) * kLog2e - M);
 #pragma unroll
             for (int k = 0; k < kCtas; ++k) tl->wgt[k][hh] = M == -INFINITY ? 0.f : e[k] / L;
         }

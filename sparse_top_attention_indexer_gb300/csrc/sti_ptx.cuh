@@ -381,6 +381,18 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrive once on a barrier in another CTA of the cluster, ordering nothing (a pure signal).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// 2^x by the SFU's approximate base-2 exponential (PTX ex2.approx.ftz.f32: relative error of a
+// few ulp, subnormal results flushed to zero, 2^-inf = 0); for softmax weights that are rounded
+// to bf16 or summed in fp32.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // Arrive once on a barrier in another CTA of the cluster (address from dsmem_addr), releasing
 // this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
