@@ -23,7 +23,9 @@ predecessor's tail, so their sum (`ms_per_step_with_kernel_events`) exceeds the 
 against the measured peaks.  `dominant_kernel_roofline` is the same for the kernel with the
 largest share of the step, over its own event-timed duration; `kernel_roofline_frac` lists
 every kernel's.  `e2e` is the same metric through the fused public entry point with the step's
-inputs copied from one pinned host buffer and the output copied back every step (wall clock).
+inputs copied from one pinned host buffer and the output copied back every step (wall clock):
+`value` overlaps each step's copies with its neighbours' kernels (double-buffered, as a serving
+loop would), `serial_value` runs copy, call, copy back and synchronise one step at a time.
 `cpu_baseline` times the CPU oracle on a bounded sample of the same workload.
 
 The library runs on one GPU.  Asked for more (--gpus > 1, or WORLD_SIZE > 1 under torchrun),
@@ -726,8 +728,9 @@ def main(argv=None):
 def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     """Decode steps through sti_decode_fused with the step's inputs (q, index q, weights,
     start_pos, and the rotation table if any) packed in one pinned host buffer, uploaded with one
-    copy into one device buffer the decode arguments point into, and the attention output copied
-    back; synchronised every step."""
+    copy into a device buffer the decode arguments point into, and the attention output copied
+    back to pinned host memory: once one step at a time, synchronised (serial_value), and once as
+    a double-buffered serving loop whose copies overlap the neighbouring steps' kernels (value)."""
     import torch
 
     sti = path.sti
@@ -764,7 +767,7 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     bo = h_out.numel() * 2
     main = torch.cuda.current_stream()
 
-    def one():
+    def serial():
         d_buf.copy_(h_buf, non_blocking=True)
         sti.decode_fused(a, ws)
         h_out.copy_(out.view(-1), non_blocking=True)
@@ -772,18 +775,73 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
 
     for _ in range(warmup):
         path.flush_l2()
-        one()
+        serial()
     el = 0.0
     for _ in range(steps):
         path.flush_l2()
         main.synchronize()
         t0 = time.perf_counter()
-        one()
+        serial()
         el += time.perf_counter() - t0
-    return {"value": round(path.b * steps / el, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(bi),
-            "d2h_bytes_per_step": int(bo),
-            "how": "sti_decode_fused; inputs in one pinned buffer, one host-to-device copy, output copied back; "
-                   "wall clock, synchronised every step"}
+    serial_value = round(path.b * steps / el, 1)
+
+    # A serving loop: two device input buffers and two outputs.  Step i's upload (one copy stream)
+    # overlaps step i-1's kernels, its download (a second copy stream) overlaps step i+1's, and
+    # the host waits for step i-1's result on the host before issuing step i+1.  Every step still
+    # moves its own inputs and output; no L2 flush fits between overlapped steps (the index keys a
+    # step streams, 134 MB at the decode shape, exceed L2).
+    d_bufs = [d_buf, torch.empty_like(d_buf)]
+    views1 = {}
+    for name, like, dt in (("q", path.q[0], torch.bfloat16), ("iq", path.iq, torch.bfloat16),
+                           ("w", path.w, torch.bfloat16), ("start_pos", path.sp, torch.int32)):
+        n = like.numel() * like.element_size()
+        views1[name] = d_bufs[1][offs[name]:offs[name] + n].view(dt).view(like.shape)
+    d_cs1 = None
+    if path.rope_cs is not None:
+        n = path.rope_cs[:, 0].numel() * 4
+        d_cs1 = d_bufs[1][offs["rope_cs"]:offs["rope_cs"] + n].view(torch.float32).view(path.rope_cs[:, 0].shape)
+    a1, out1, _ = sti.decode_args(views1["q"], path.win[0], path.comp, path.sink[0], shp.softmax_scale, views1["iq"],
+                                  path.ik, views1["w"], shp.index_scale, views1["start_pos"], shp.ratio, shp.n_cols,
+                                  shp.topk, rope_cs=d_cs1, ik_codes=path.ik_codes, ik_scales=path.ik_scales)
+    argv, outs = [a, a1], [out, out1]
+    h_outs = [h_out, torch.empty(out.numel(), dtype=torch.bfloat16).pin_memory()]
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(n):
+        main.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n):
+            k = i & 1
+            with torch.cuda.stream(s_up):
+                if i >= 2:
+                    s_up.wait_event(ev_comp[k])   # step i-2's kernels have read d_bufs[k]
+                d_bufs[k].copy_(h_buf, non_blocking=True)
+                ev_up[k].record(s_up)
+            main.wait_event(ev_up[k])
+            sti.decode_fused(argv[k], ws)
+            ev_comp[k].record(main)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_comp[k])
+                h_outs[k].copy_(outs[k].view(-1), non_blocking=True)
+                ev_down[k].record(s_down)
+            if i >= 1:
+                ev_down[(i - 1) & 1].synchronize()   # step i-1's output is on the host
+        ev_down[(n - 1) & 1].synchronize()
+        return time.perf_counter() - t0
+
+    pipelined(max(warmup, 2))
+    value = round(path.b * steps / pipelined(steps), 1)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "serial_value": serial_value,
+            "how": "sti_decode_fused with the step's inputs in one pinned host buffer (one host-to-device copy "
+                   "into the device buffer the arguments point into) and the attention output copied back to "
+                   "pinned host memory, every step; value: a serving loop that overlaps step i's upload and "
+                   "step i-1's download with the kernels (double-buffered inputs and outputs, the host waiting "
+                   "for each step's output); serial_value: copy, call, copy back and synchronise, one step at "
+                   "a time with the L2 flushed between steps; wall clock"}
 
 
 if __name__ == "__main__":

@@ -1011,6 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= tl->wgt[kCtas - 1][hoff + i];
         mwait_c(&tl->recv_bar);
+        if (mt == 0) STI_DSTAMP(51);
 #pragma unroll 1
         for (int k = 0; k < kCtas - 1; ++k) {
             const uint8_t* part = tile + (size_t)k * kPartBytes + (size_t)d_loc * 256;
