@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->recv_bar, 1);
         // the merge's incoming bytes, fixed: three (max, sum) vectors and three partial d-blocks
         mbar_arrive_expect_tx(&tl->ml_bar, (kCtas - 1) * kH * 8);
-        mbar_arrive_expect_tx(&tl->recv_bar, (kCtas - 1) * kRows * kH * 4);
+        mbar_arrive_expect_tx(&tl->recv_bar, (kCtas - 1) * kRows * kH * 2);
         tl->abort = 0;
         fence_mbar_init();
     }
@@ -918,12 +918,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt == 0) STI_DSTAMP(12);
 
         // ---- merge in shared memory.  Each CTA sends its (max, sum) per head to the other three as
-        // soon as its softmax is done.  Once its PV is complete (tile, Q and P^T no longer read) it
-        // stages the three d-blocks of its O^T that the others own as [128 d][64 heads] fp32, the
-        // sixteen 16-byte chunks of a d row XOR-swizzled by d (tile bytes [96K, 128K), then Q), and
-        // when every CTA's PV is complete copies each to its owner's tile (bulk shared-to-shared
-        // copies counted on the owner's recv_bar; slot k at the owner, bytes [32K k, 32K k + 32K),
-        // comes from CTA k + (k >= owner)).  Then it combines its own block with the three received.
+        // soon as its softmax is done.  Once its PV is complete (its tile no longer read) it computes
+        // every CTA's weight per head, 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)), and
+        // stages the three d-blocks of its O^T that the others own times its own weight -- its share
+        // of the output -- as [128 d][64 heads] bf16, the eight 16-byte chunks of a d row
+        // XOR-swizzled by d (tile bytes [48K, 96K)).  When every CTA's PV is complete it copies each
+        // to its owner's tile (bulk shared-to-shared copies counted on the owner's recv_bar; slot k
+        // at the owner, bytes [16K k, 16K k + 16K), comes from CTA k + (k >= owner)), and adds the
+        // three shares it receives to its own block times its own weight.
         const int d_loc = row;   // TMEM lane = d within a block
         if (st < 32 && !dead) {
             const int hh = hoff + st;
@@ -936,9 +938,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dsmem_addr(&tl->ml_bar, peer));
             }
         }
-        constexpr uint32_t kPartBytes = kRows * kH * 4;
+        constexpr uint32_t kPartBytes = kRows * kH * 2;   // one d-block's share: [128 d][64 heads] bf16
         auto out_stage = [&](int j) -> uint8_t* {   // staging of the block for CTA (rank + j) % 4
-            return j == 1 ? tile + 3 * kPartBytes : q_s + (size_t)(j - 2) * kPartBytes;
+            return tile + (size_t)(2 + j) * kPartBytes;
         };
 #pragma unroll 1
         for (int j = 1; j <= kCtas; ++j) {   // this CTA's PV, all four blocks
@@ -949,34 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt == 0 && !dead)
             for (int c = 0; c < kCtas; ++c) mbar_arrive_remote_relaxed(dsmem_addr(&tl->free_bar, (uint32_t)c));
         if (mt == 0) STI_DSTAMP(13);
-        const uint32_t swz = (uint32_t)(d_loc & 7);
-#pragma unroll 1
-        for (int j = 1; j < kCtas && !dead; ++j) {   // the others' d-blocks, staged
-            const int m = (j + rank) & 3;
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
-            tmem_ld_wait();
-            uint8_t* dst = out_stage(j) + (size_t)d_loc * 256;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(dst + ((((uint32_t)(8 * set + c)) ^ swz) << 4)) =
-                    make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-        }
-        fence_proxy_async_smem();   // generic writes, read by the bulk copies
-        named_bar_sync(kBarMath, 256);
-        if (!dead) dead = !attn_wait_cluster(&tl->free_bar, 0, p.status, abort);
-        dead = __any_sync(kFull, dead);
-        if (mt == 0) STI_DSTAMP(14);
-        if (mt < kCtas - 1 && !dead) {   // thread j - 1 copies the block of CTA (rank + j) % 4
-            const int j = mt + 1;
-            const int m = (j + rank) & 3;
-            const int slot = rank < m ? rank : rank - 1;
-            bulk_copy_to_peer(dsmem_addr(tile, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
-                              dsmem_addr(&tl->recv_bar, (uint32_t)m));
-        }
-        if (mt == 0) STI_DSTAMP(25);
         mwait_c(&tl->ml_bar);
-        if (st < 32) {   // the four partials' weights for head hoff + st (whose max and sum this thread wrote)
+        if (st < 32) {   // the four CTAs' weights for head hoff + st (whose max and sum this thread wrote)
             const int hh = hoff + st;
             float mc[kCtas], lc[kCtas];
             float M = -INFINITY;
@@ -998,31 +974,70 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kCtas; ++k) tl->wgt[k][hh] = M == -INFINITY ? 0.f : e[k] / L;
         }
+        named_bar_sync(kBarMath, 256);   // the weights
+        if (mt == 0) STI_DSTAMP(26);
+        // the others' d-blocks times this CTA's weight (so each is this CTA's share of the output,
+        // no larger than the largest |v|), staged as bf16
+        const uint32_t swz = (uint32_t)(d_loc & 7);
+        const float* w_own = tl->wgt[kCtas - 1] + hoff;
+#pragma unroll 1
+        for (int j = 1; j < kCtas && !dead; ++j) {
+            const int m = (j + rank) & 3;
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
+            tmem_ld_wait();
+            uint8_t* dst = out_stage(j) + (size_t)d_loc * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int h0 = 8 * c + 2 * i;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[h0]) * w_own[h0],
+                                                                    __uint_as_float(r[h0 + 1]) * w_own[h0 + 1]);
+                    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+                }
+                *reinterpret_cast<uint4*>(dst + ((((uint32_t)(4 * set + c)) ^ swz) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+        fence_proxy_async_smem();   // generic writes, read by the bulk copies
+        named_bar_sync(kBarMath, 256);
+        if (!dead) dead = !attn_wait_cluster(&tl->free_bar, 0, p.status, abort);
+        dead = __any_sync(kFull, dead);
+        if (mt == 0) STI_DSTAMP(14);
+        if (mt < kCtas - 1 && !dead) {   // thread j - 1 copies the block of CTA (rank + j) % 4
+            const int j = mt + 1;
+            const int m = (j + rank) & 3;
+            const int slot = rank < m ? rank : rank - 1;
+            bulk_copy_to_peer(dsmem_addr(tile, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
+                              dsmem_addr(&tl->recv_bar, (uint32_t)m));
+        }
+        if (mt == 0) STI_DSTAMP(25);
         float v[32];
         {
             uint32_t r[32];
             tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(rank * kH + hoff), r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * w_own[i];
         }
-        named_bar_sync(kBarMath, 256);   // the weights
-        if (mt == 0) STI_DSTAMP(26);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= tl->wgt[kCtas - 1][hoff + i];
         mwait_c(&tl->recv_bar);
         if (mt == 0) STI_DSTAMP(51);
 #pragma unroll 1
-        for (int k = 0; k < kCtas - 1; ++k) {
-            const uint8_t* part = tile + (size_t)k * kPartBytes + (size_t)d_loc * 256;
+        for (int k = 0; k < kCtas - 1; ++k) {   // the three others' shares of this CTA's d-block
+            const uint8_t* part = tile + (size_t)k * kPartBytes + (size_t)d_loc * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 x = dead ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                      : *reinterpret_cast<const float4*>(part + (((uint32_t)(8 * set + c) ^ swz) << 4));
-                v[4 * c] += x.x * tl->wgt[k][hoff + 4 * c];
-                v[4 * c + 1] += x.y * tl->wgt[k][hoff + 4 * c + 1];
-                v[4 * c + 2] += x.z * tl->wgt[k][hoff + 4 * c + 2];
-                v[4 * c + 3] += x.w * tl->wgt[k][hoff + 4 * c + 3];
+            for (int c = 0; c < 4; ++c) {
+                const uint4 x = dead ? make_uint4(0, 0, 0, 0)
+                                     : *reinterpret_cast<const uint4*>(part + (((uint32_t)(4 * set + c) ^ swz) << 4));
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[i]));
+                    v[8 * c + 2 * i] += f.x;
+                    v[8 * c + 2 * i + 1] += f.y;
+                }
             }
         }
         const int dd = kRows * rank + d_loc;
