@@ -102,7 +102,7 @@ struct __align__(16) DaTail {
     uint64_t o_done;           // the ring slice's PV complete (O^T initialised)
     uint64_t ring_free;        // the ring slice's PV complete: rows 96..127 may be overwritten
     uint64_t pv_bar[4];        // the compressed tile's PV complete for d-block m
-    uint64_t free_bar;         // merge: every CTA's PV complete, its tile free to receive partials (4 CTAs)
+    uint64_t qfree_bar;        // merge: every CTA's compressed QK complete, its Q buffer free to receive (4 CTAs)
     uint64_t ml_bar;           // merge: the other CTAs' (max, sum) per head landed (bytes)
     uint64_t tk_bar;           // top-k: the other CTAs' words, members and counts landed (24 arrivals + bytes)
     uint64_t recv_bar;         // merge: the three other CTAs' partials of this CTA's d-block landed (bytes)
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->o_done, 1);
         mbar_init(&tl->ring_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&tl->pv_bar[m], 1);
-        mbar_init(&tl->free_bar, kCtas);
+        mbar_init(&tl->qfree_bar, kCtas);
         mbar_init(&tl->ml_bar, 1);
         mbar_init(&tl->tk_bar, (kCtas - 1) * 8);
         mbar_init(&tl->recv_bar, 1);
@@ -485,6 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mwait(&tl->s_full[t], 0);
             if (t == 1 && mt == 0) STI_DSTAMP(11);
             tc_fence_after();
+            if (t == 1 && mt == 0 && !dead)   // the QK has read Q: its buffer may receive the merge shares
+                for (int c = 0; c < kCtas; ++c) mbar_arrive_remote_relaxed(dsmem_addr(&tl->qfree_bar, (uint32_t)c));
             const uint32_t s_col = tmem + lane_base + (uint32_t)(t * kH + hoff);
             auto load8 = [&](int c, float (&x)[8]) {   // this row's S of heads hoff + 8c .. + 8, log2 units
                 uint32_t r[8], r2[8];
@@ -651,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // this CTA's quarter of the row; warp mw stages 16 words (32 scores each) at a time in
             // rows 0..63 of column blocks 0-1, lane = bit (each lane reads back only its own copies)
-            const int wq = (nwords + kCtas - 1) / kCtas;
+            const int wq = ((nwords + kCtas - 1) / kCtas + 15) & ~15;   // whole 16-word groups
             const int wa = min(nwords, rank * wq), wb = min(nwords, wa + wq);
             float* stg = reinterpret_cast<float*>(tile + (size_t)(mw >> 2) * kBlkBytes + (size_t)(mw & 3) * 2048);
             auto stage16 = [&](int g) {
@@ -677,15 +679,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int d1 = s1.x, above1 = s1.y, c1 = s1.z;
             const int remaining1 = kK - above1;   // keys of bin d1 to take (>= 1)
             if (mt == 0) STI_DSTAMP(3);
-            // this CTA's quarter of the row, 16 words per warp at a time: each word of keys above the
-            // bin and each of the warp's members of the bin is stored here and, by st.async, in the
-            // other three CTAs, counted there on tk_bar; then the warp's member count, and one arrive
-            // per other CTA that announces the bytes sent to it
+            // this CTA's quarter of the row, 16 words per warp at a time: the words of keys above the
+            // bin and the warp's members of the bin (its segment) are written here, then bulk-copied
+            // into the other three CTAs (shared to shared, counted on their tk_bar) with the member
+            // count and one arrive per CTA that announces the bytes sent to it
             {
                 const int sg_own = 8 * rank + mw;
-                int cnt = 0, nw = 0;
-                for (int g = wa + 16 * mw; g < wb; g += 128) {
+                int cnt = 0, groups = 0;
+                for (int g = wa + 16 * mw; g < wb; g += 128, ++groups) {
                     cp_async_wait<0>();
+                    if (mt == 0) STI_DSTAMP(52);
                     uint32_t my_above = 0u;
 #pragma unroll 4
                     for (int q = 0; q < 16; ++q) {
@@ -698,41 +701,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const unsigned mem = __ballot_sync(kFull, m);
                         if (lane == q) my_above = above;
                         const int at = cnt + __popc(mem & ((1u << lane) - 1u));
-                        if (m && at < kSegCap) {
-                            uint2* dst = seg(sg_own, at);
-                            *dst = make_uint2(key, (uint32_t)pos);
-#pragma unroll
-                            for (int c = 1; c < kCtas; ++c) {
-                                const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
-                                st_async_u2(dsmem_addr(dst, peer), key, (uint32_t)pos, dsmem_addr(&tl->tk_bar, peer));
-                            }
-                        }
+                        if (m && at < kSegCap) *seg(sg_own, at) = make_uint2(key, (uint32_t)pos);
                         cnt += __popc(mem);
                     }
+                    if (mt == 0) STI_DSTAMP(53);
                     if (g + 128 < wb) stage16(g + 128);
-                    const int nq = min(16, wb - g);
-                    if (lane < nq) {
-                        uint32_t* dst = bm(0, g + lane);
-                        *dst = my_above;
-#pragma unroll
-                        for (int c = 1; c < kCtas; ++c) {
-                            const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
-                            st_async_b32(dsmem_addr(dst, peer), my_above, dsmem_addr(&tl->tk_bar, peer));
-                        }
+                    if (lane < 16) *bm(0, g + lane) = g + lane < wb ? my_above : 0u;
+                    fence_proxy_async_smem();   // generic writes, read by the bulk copies
+                    __syncwarp();
+                    if (lane < kCtas - 1) {   // the group's 16 words (64 B) to CTA (rank + 1 + lane) % 4
+                        const uint32_t peer = (uint32_t)((rank + 1 + lane) & (kCtas - 1));
+                        bulk_copy_to_peer(dsmem_addr(bm(0, g), peer), bm(0, g), 64u, dsmem_addr(&tl->tk_bar, peer));
                     }
-                    nw += nq;
+                    if (mt == 0) STI_DSTAMP(54);
                 }
-                if (lane == 0) {
-                    tl->seg_cnt[sg_own] = cnt;
-                    const uint32_t bytes = 4u * (uint32_t)nw + 8u * (uint32_t)min(cnt, kSegCap) + 4u;
-#pragma unroll
-                    for (int c = 1; c < kCtas; ++c) {
-                        const uint32_t peer = (uint32_t)((rank + c) & (kCtas - 1));
-                        const uint32_t pbar = dsmem_addr(&tl->tk_bar, peer);
-                        st_async_b32(dsmem_addr(&tl->seg_cnt[sg_own], peer), (uint32_t)cnt, pbar);
-                        mbar_arrive_expect_tx_remote(pbar, bytes);
-                    }
+                const uint32_t mem_bytes = (uint32_t)((min(cnt, kSegCap) * 8 + 15) & ~15);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane < kCtas - 1) {   // the members and their count to CTA (rank + 1 + lane) % 4
+                    const uint32_t peer = (uint32_t)((rank + 1 + lane) & (kCtas - 1));
+                    const uint32_t pbar = dsmem_addr(&tl->tk_bar, peer);
+                    if (mem_bytes) bulk_copy_to_peer(dsmem_addr(seg(sg_own, 0), peer), seg(sg_own, 0), mem_bytes, pbar);
+                    st_async_b32(dsmem_addr(&tl->seg_cnt[sg_own], peer), (uint32_t)cnt, pbar);
+                    mbar_arrive_expect_tx_remote(pbar, 64u * (uint32_t)groups + mem_bytes + 4u);
                 }
+                if (lane == 0) tl->seg_cnt[sg_own] = cnt;
             }
             named_bar_sync(kBarMath, 256);   // this CTA's words, members and counts
             if (mt == 0) STI_DSTAMP(28);
@@ -918,14 +911,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt == 0) STI_DSTAMP(12);
 
         // ---- merge in shared memory.  Each CTA sends its (max, sum) per head to the other three as
-        // soon as its softmax is done.  Once its PV is complete (its tile no longer read) it computes
-        // every CTA's weight per head, 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)), and
-        // stages the three d-blocks of its O^T that the others own times its own weight -- its share
-        // of the output -- as [128 d][64 heads] bf16, the eight 16-byte chunks of a d row
-        // XOR-swizzled by d (tile bytes [48K, 96K)).  When every CTA's PV is complete it copies each
-        // to its owner's tile (bulk shared-to-shared copies counted on the owner's recv_bar; slot k
-        // at the owner, bytes [16K k, 16K k + 16K), comes from CTA k + (k >= owner)), and adds the
-        // three shares it receives to its own block times its own weight.
+        // soon as its softmax is done and, while its PV runs, computes every CTA's weight per head,
+        // 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)).  Once its PV is complete it stages
+        // the three d-blocks of its O^T that the others own times its own weight -- its share of the
+        // output -- as [128 d][64 heads] bf16 in its tile, the eight 16-byte chunks of a d row
+        // XOR-swizzled by d, and copies each into its owner's Q buffer, free since the owner's QK
+        // (bulk shared-to-shared copies counted on the owner's recv_bar; slot k, bytes
+        // [16K k, 16K k + 16K), comes from CTA k + (k >= owner)).  The owner adds the three shares to
+        // its own block times its own weight.
         const int d_loc = row;   // TMEM lane = d within a block
         if (st < 32 && !dead) {
             const int hh = hoff + st;
@@ -940,17 +933,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         constexpr uint32_t kPartBytes = kRows * kH * 2;   // one d-block's share: [128 d][64 heads] bf16
         auto out_stage = [&](int j) -> uint8_t* {   // staging of the block for CTA (rank + j) % 4
-            return tile + (size_t)(2 + j) * kPartBytes;
+            return tile + (size_t)(j - 1) * kPartBytes;
         };
-#pragma unroll 1
-        for (int j = 1; j <= kCtas; ++j) {   // this CTA's PV, all four blocks
-            mwait(&tl->pv_bar[(j + rank) & 3], 0);
-            if (mt == 0) STI_DSTAMP(45 + j);
-        }
-        tc_fence_after();
-        if (mt == 0 && !dead)
-            for (int c = 0; c < kCtas; ++c) mbar_arrive_remote_relaxed(dsmem_addr(&tl->free_bar, (uint32_t)c));
-        if (mt == 0) STI_DSTAMP(13);
+        // the weights, while the PV runs
         mwait_c(&tl->ml_bar);
         if (st < 32) {   // the four CTAs' weights for head hoff + st (whose max and sum this thread wrote)
             const int hh = hoff + st;
@@ -976,8 +961,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(kBarMath, 256);   // the weights
         if (mt == 0) STI_DSTAMP(26);
+#pragma unroll 1
+        for (int j = 1; j <= kCtas; ++j) {   // this CTA's PV, all four blocks
+            mwait(&tl->pv_bar[(j + rank) & 3], 0);
+            if (mt == 0) STI_DSTAMP(45 + j);
+        }
+        tc_fence_after();
+        if (mt == 0) STI_DSTAMP(13);
         // the others' d-blocks times this CTA's weight (so each is this CTA's share of the output,
-        // no larger than the largest |v|), staged as bf16
+        // no larger than the largest |v|), staged as bf16 in the tile the PV has finished reading
         const uint32_t swz = (uint32_t)(d_loc & 7);
         const float* w_own = tl->wgt[kCtas - 1] + hoff;
 #pragma unroll 1
@@ -1003,14 +995,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();   // generic writes, read by the bulk copies
         named_bar_sync(kBarMath, 256);
-        if (!dead) dead = !attn_wait_cluster(&tl->free_bar, 0, p.status, abort);
+        if (!dead) dead = !attn_wait_cluster(&tl->qfree_bar, 0, p.status, abort);   // every Q buffer free
         dead = __any_sync(kFull, dead);
         if (mt == 0) STI_DSTAMP(14);
         if (mt < kCtas - 1 && !dead) {   // thread j - 1 copies the block of CTA (rank + j) % 4
             const int j = mt + 1;
             const int m = (j + rank) & 3;
             const int slot = rank < m ? rank : rank - 1;
-            bulk_copy_to_peer(dsmem_addr(tile, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
+            bulk_copy_to_peer(dsmem_addr(q_s, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
                               dsmem_addr(&tl->recv_bar, (uint32_t)m));
         }
         if (mt == 0) STI_DSTAMP(25);
@@ -1026,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt == 0) STI_DSTAMP(51);
 #pragma unroll 1
         for (int k = 0; k < kCtas - 1; ++k) {   // the three others' shares of this CTA's d-block
-            const uint8_t* part = tile + (size_t)k * kPartBytes + (size_t)d_loc * 128;
+            const uint8_t* part = q_s + (size_t)k * kPartBytes + (size_t)d_loc * 128;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint4 x = dead ? make_uint4(0, 0, 0, 0)
