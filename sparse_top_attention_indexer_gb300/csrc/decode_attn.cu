@@ -11,33 +11,36 @@
 //
 // Shape: 64 heads x 512, window 128, index_topk 512: 640 rows per query, the ring's 128 and 512
 // compressed.  CTA r of a query's cluster owns
-//   * ring slots [32r, 32r+32): rows 96..127 of its tile, run through QK, softmax and PV before the
-//     indices exist (while the scores kernel drains);
+//   * ring slots [32r, 32r+32): rows 96..127 of its tile, run through QK and softmax before the
+//     scores are complete (the kernel is a programmatic dependent of the scores kernel);
 //   * the compressed rows of output slots [128r, 128r+128) of the index row: one 128-row tile;
 //   * d-block r (dims [128r, 128r+128)) of the output in the merge.
-// Top-k (exact; ties go to the lower position), computed whole by every CTA of the cluster -- its
-// inputs are a few tens of KB from L2, and no CTA waits on another: the scores kernel's first
-// radix pass (top 11 key bits) gives the threshold bin d1; one pass over the row marks the keys
-// above the bin in a position bitmap and lists the bin's members; two radix passes over the
-// members (shared-memory histograms of the next 11 and 10 bits) give the exact k-th key tau and
-// how many keys equal to it are taken; a second bitmap marks the keys equal to tau; one block scan
-// over both bitmaps gives every selected position its output slot, in ascending position order.
-// A bin with more than 1024 members (heavy ties) takes the two passes over the whole row instead.
-// Each CTA keeps the slots it owns: its tile's index list and its quarter of the published row.
+// Top-k (exact; ties go to the lower position): the scores kernel's first radix pass (top 11 key
+// bits) gives the threshold bin d1, found by every warp from a shared-memory copy of the
+// histogram.  Each CTA scans a quarter of the row: a bitmap of the keys above the bin and, per
+// warp, a segment of the bin's members, which it bulk-copies into the other three CTAs (shared to
+// shared, counted on their barrier).  Every CTA then holds the whole row's bitmap and members:
+// two radix passes over the members (shared-memory histograms of the next 11 and 10 bits, a bin
+// taken whole ending them) give the k-th key tau and how many keys equal to it are taken; the
+// members above tau join the bitmap, those equal to tau mark a second one; one block scan over
+// both gives every selected position its output slot, in ascending position order.  A warp with
+// more than 64 members (heavy ties) sends the passes over the whole row instead.  Each CTA keeps
+// the slots it owns: its tile's index list and its quarter of the published row.
 // Attention, per tile: S^T = KV.Q^T (tcgen05, M = 128 rows, N = 64 heads, K = 512) into TMEM; an
 // online softmax with thread = row in two warp groups of 32 heads; O^T += V^T.P^T (M = 128 d-rows
 // per d-block, N = 64, K = rows) reading the same tile as an MN-major operand.  The compressed
-// rows arrive by 16-byte cp.async from the eight math warps (one column block each; masked rows
-// zero-filled).
-// Merge, through L2: each CTA writes the three d-blocks of its unnormalised O^T that the others
-// own, and its (max, sum) per head, to the workspace and signals the cluster (one remote barrier
-// arrive per CTA); each then reads its d-block from the three others:
-//   o = sum_c O_c 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)).
+// rows arrive by four-row TMA gathers issued by the eight math warps (masked rows repeat a valid
+// row of their group, whose probability is zero; groups with none are zeroed).
+// Merge, in shared memory: each CTA sends its (max, sum) per head to the other three, computes
+// every CTA's weight
+//   w_c = 2^(m_c - M) / (sum_c' l_c' 2^(m_c' - M) + 2^(sink - M)),
+// and bulk-copies the three d-blocks of its O^T that the others own, times its own weight, as bf16
+// into their Q buffers; each owner adds the three to its own weighted block:  o = sum_c w_c O_c.
 //
-// Roles (13 warps): warp 0 and warps 10-12 load Q and the ring slice; warp 1 allocates TMEM and
-// issues the MMAs; warps 2-9 (256 "math" threads) run the top-k, gather the compressed tile
-// (warp 2 + j: column block j), the softmax (warps 2-5: heads 0-31, warps 6-9: heads 32-63) and
-// the merge.
+// Roles (13 warps): warp 0 and warps 10-12 load Q and the ring slice, warp 11 then runs the ring
+// slice's softmax; warp 1 allocates TMEM and issues the MMAs; warps 2-9 (256 "math" threads) run
+// the top-k, gather the compressed tile, the softmax (warps 2-5: heads 0-31, warps 6-9: heads
+// 32-63) and the merge.
 #include <cuda_bf16.h>
 #include <cstddef>
 #include <math.h>
@@ -477,10 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             dead = __any_sync(kFull, dead);
         };
 
-        // online softmax over one tile's S^T (t = 0: the ring slice, 1: the compressed tile).  The
-        // set's 32 heads go 8 at a time through rolled loops (S re-read from TMEM in the second
-        // pass): each CTA runs this code only twice, so its size, not its issue count, decides
-        // how long the first run waits on instruction fetch.
+        // online softmax over the compressed tile's S^T (t = 1; the sum of its two partial
+        // accumulators), continuing the ring slice's running max and sum.  The set's 32 heads go 8
+        // at a time through rolled loops (S re-read from TMEM in the second pass): each CTA runs
+        // this code once, so its size, not its issue count, decides how long it waits on
+        // instruction fetch.
         auto softmax_tile = [&](int t, bool valid) {
             mwait(&tl->s_full[t], 0);
             if (t == 1 && mt == 0) STI_DSTAMP(11);
