@@ -155,7 +155,8 @@ class GpuPath:
                                           out=self.out[0].view(self.b, shape.h, shape.d),
                                           topk_idxs=self.idx.view(self.b, self.k_total),
                                           rope_cs=None if self.rope_cs is None else self.rope_cs[:, 0],
-                                          ik_codes=self.ik_codes, ik_scales=self.ik_scales)
+                                          ik_codes=self.ik_codes, ik_scales=self.ik_scales,
+                                          comp_codes=self.comp_codes, comp_scales=self.comp_scales)
         self.dws = sti.workspace(sti.decode_workspace_size(self.args), device)
         self.fused_kernels = sti.decode_kernel_count(self.args)
         first = (["idx_scores", "topk_sparse_attn[0]"] if self.fused_kernels == 2 else
@@ -286,8 +287,8 @@ def work(shape: workloads.Shape, data: dict) -> dict:
     comp_row = (d // 2 + d // 16) if shape.fp4_kv else d * 2                        # per compressed row (fp4: codes + scales)
     if shape.prefill:
         kv_bytes = shape.win_rows * d * 2 + n_keys.sum() * comp_row                # unique rows (L2 serves reuse)
-    else:
-        kv_bytes = rows * d * 2                                                     # every gathered row from HBM
+    else:   # every gathered row from HBM
+        kv_bytes = win_valid.sum() * d * 2 + sel.sum() * comp_row
     attn = {"bytes": float(kv_bytes + 2 * b * s * h * d * 2 + b * s * shape.k_total * 4),
             "flops": float(4 * h * d * rows)}
     for i in range(shape.n_layers):
@@ -451,8 +452,12 @@ def oracle_step(shape: workloads.Shape, data: dict, rows: np.ndarray | None = No
     idx = np.concatenate([widx, cidx], axis=-1)
     cs = workloads.output_rope_table(shape) if output_rope else None
     for i in range(shape.n_layers):
-        oracle.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], idx, shape.softmax_scale,
-                           kv2=data["comp"], rope_cs=cs, threads=threads)
+        if shape.fp4_kv:
+            oracle.sparse_attn_fp4kv(data["q"][i], data["win"][i], data["comp_codes"], data["comp_scales"],
+                                     data["sink"][i], idx, shape.softmax_scale, threads)
+        else:
+            oracle.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], idx, shape.softmax_scale,
+                               kv2=data["comp"], rope_cs=cs, threads=threads)
     return shape.b * shape.s
 
 
@@ -537,7 +542,7 @@ def parse(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -760,7 +765,8 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
     d_cs = None if path.rope_cs is None else view("rope_cs", path.rope_cs[:, 0].contiguous(), torch.float32)
     a, out, tk = sti.decode_args(d_q, path.win[0], path.comp, path.sink[0], shp.softmax_scale, d_iq, path.ik, d_w,
                                  shp.index_scale, d_sp, shp.ratio, shp.n_cols, shp.topk, rope_cs=d_cs,
-                                 ik_codes=path.ik_codes, ik_scales=path.ik_scales)
+                                 ik_codes=path.ik_codes, ik_scales=path.ik_scales,
+                                 comp_codes=path.comp_codes, comp_scales=path.comp_scales)
     ws = sti.workspace(sti.decode_workspace_size(a), path.dev)
     h_out = torch.empty(out.numel(), dtype=torch.bfloat16).pin_memory()
     bi = sum(arr.size for _, arr in parts)
@@ -802,7 +808,8 @@ def measure_e2e(path: GpuPath, data: dict, steps: int, warmup: int) -> dict:
         d_cs1 = d_bufs[1][offs["rope_cs"]:offs["rope_cs"] + n].view(torch.float32).view(path.rope_cs[:, 0].shape)
     a1, out1, _ = sti.decode_args(views1["q"], path.win[0], path.comp, path.sink[0], shp.softmax_scale, views1["iq"],
                                   path.ik, views1["w"], shp.index_scale, views1["start_pos"], shp.ratio, shp.n_cols,
-                                  shp.topk, rope_cs=d_cs1, ik_codes=path.ik_codes, ik_scales=path.ik_scales)
+                                  shp.topk, rope_cs=d_cs1, ik_codes=path.ik_codes, ik_scales=path.ik_scales,
+                                 comp_codes=path.comp_codes, comp_scales=path.comp_scales)
     argv, outs = [a, a1], [out, out1]
     h_outs = [h_out, torch.empty(out.numel(), dtype=torch.bfloat16).pin_memory()]
     s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()

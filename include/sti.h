@@ -293,6 +293,20 @@ typedef struct sti_decode_args {
     int64_t ik_codes_bstride;   /* bytes */
     const uint8_t *ik_scales;
     int64_t ik_scales_bstride;  /* bytes */
+    /* optional: the compressed KV as fp4 rows (as sti_sparse_attn_sink_fp4kv: Attention._compress_kv
+     * on the "read-weights" page quantises the compressed latent with fp4_act_quant(latent, 16, ...)
+     * before the cache write) instead of comp_kv, which is then unused (it may be NULL):
+     *   comp_codes:  uint8 [b, *, d/2], batch b at + b*comp_codes_bstride bytes; byte j of a row holds
+     *                element 2j (low nibble) and 2j+1 (high nibble) as E2M1 codes;
+     *   comp_scales: uint8 [b, *, d/16], batch b at + b*comp_scales_bstride bytes; byte g is the E4M3
+     *                scale of elements 16g .. 16g+15; an element's value is code * scale.
+     * Supported only where steps 2 and 3 run as one kernel (sti_decode_kernel_count() == 2 with
+     * these arguments): both arrays 16-byte aligned, bstrides multiples of 16 holding n_cols rows;
+     * other shapes return STI_ERR_UNSUPPORTED.  NULL comp_codes: bf16 rows from comp_kv. */
+    const uint8_t *comp_codes;
+    int64_t comp_codes_bstride;  /* bytes */
+    const uint8_t *comp_scales;
+    int64_t comp_scales_bstride; /* bytes */
 } sti_decode_args;
 
 /* Steps 2 and 3 launch as programmatic dependents of the step before them: each is scheduled

@@ -57,6 +57,8 @@ class DecodeArgs(ctypes.Structure):
         ("rope_cs", ctypes.c_void_p), ("rope_dims", ctypes.c_int),
         ("ik_codes", ctypes.c_void_p), ("ik_codes_bstride", ctypes.c_int64), ("ik_scales", ctypes.c_void_p),
         ("ik_scales_bstride", ctypes.c_int64),
+        ("comp_codes", ctypes.c_void_p), ("comp_codes_bstride", ctypes.c_int64), ("comp_scales", ctypes.c_void_p),
+        ("comp_scales_bstride", ctypes.c_int64),
     ]
 
 
@@ -334,13 +336,15 @@ def sparse_attn_sink_fp4kv(q: torch.Tensor, kv: torch.Tensor, kv2_codes: torch.T
 
 def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, index_scale, start_pos, ratio, n_cols,
                 index_topk, out=None, topk_idxs=None, q_ready=None, rope_cs=None, ik_codes=None,
-                ik_scales=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
+                ik_scales=None, comp_codes=None, comp_scales=None) -> tuple[DecodeArgs, torch.Tensor, torch.Tensor]:
     """Fill sti_decode_args from tensors.  q [b,h,d] (or [b,1,h,d]), window_kv [b,W,d],
     comp_kv [b,cap,d], iq [b,Hi,Di] (or [b,1,Hi,Di]), ik [b,cap,Di], w [b,Hi] (or [b,1,Hi]).
     q_ready: optional torch.cuda.Event (already recorded once) the attention step waits for.
     rope_cs: optional fp32 [b, rd/2, 2] (cos, sin) of the output's inverse rotation.
     ik_codes / ik_scales: optional MXFP4 index keys (uint8 [b, cap, Di/2] / [b, cap, Di/32]);
     then `ik` is not read (it may be None).
+    comp_codes / comp_scales: optional fp4 compressed KV rows (uint8 [b, cap, d/2] / [b, cap, d/16]);
+    then `comp_kv` is not read (it may be None).
     The returned struct keeps references to every tensor it points to."""
     b = q.shape[0]
     h, d = q.shape[-2], q.shape[-1]
@@ -350,7 +354,7 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
                         ("attn_sink", attn_sink, torch.float32), ("start_pos", start_pos, torch.int32)):
         _need(t, dt, name)
     for name, t, inner in (("window_kv", window_kv, d), ("comp_kv", comp_kv, d), ("ik", ik, Di)):
-        if t is None and name == "ik" and ik_codes is not None:
+        if t is None and ((name == "ik" and ik_codes is not None) or (name == "comp_kv" and comp_codes is not None)):
             continue
         _need(t, torch.bfloat16, name, contiguous=False)
         if t.stride(2) != 1 or t.stride(1) != inner:
@@ -359,7 +363,8 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
         out = torch.empty(b, h, d, dtype=torch.bfloat16, device=q.device)
     if topk_idxs is None:
         topk_idxs = torch.empty(b, W + index_topk, dtype=torch.int32, device=q.device)
-    a = DecodeArgs(_ptr(q), _ptr(window_kv), window_kv.stride(0), _ptr(comp_kv), comp_kv.stride(0), _ptr(attn_sink),
+    a = DecodeArgs(_ptr(q), _ptr(window_kv), window_kv.stride(0), _ptr(comp_kv),
+                   0 if comp_kv is None else comp_kv.stride(0), _ptr(attn_sink),
                    float(softmax_scale), h, d, W, _ptr(iq), _ptr(ik), 0 if ik is None else ik.stride(0), _ptr(w),
                    float(index_scale), Hi,
                    Di, index_topk, ratio, n_cols, _ptr(start_pos), b, _ptr(out), _ptr(topk_idxs),
@@ -375,9 +380,15 @@ def decode_args(q, window_kv, comp_kv, attn_sink, softmax_scale, iq, ik, w, inde
                 raise ValueError(f"{name} must be uint8 [b, rows, {inner}] with contiguous rows")
         a.ik_codes, a.ik_codes_bstride = _ptr(ik_codes), ik_codes.stride(0)
         a.ik_scales, a.ik_scales_bstride = _ptr(ik_scales), ik_scales.stride(0)
+    if comp_codes is not None:
+        for name, t, inner in (("comp_codes", comp_codes, d // 2), ("comp_scales", comp_scales, d // 16)):
+            if t is None or t.dtype != torch.uint8 or t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != inner:
+                raise ValueError(f"{name} must be uint8 [b, rows, {inner}] with contiguous rows")
+        a.comp_codes, a.comp_codes_bstride = _ptr(comp_codes), comp_codes.stride(0)
+        a.comp_scales, a.comp_scales_bstride = _ptr(comp_scales), comp_scales.stride(0)
     # the struct holds raw device pointers: keep their tensors alive as long as it lives
     a.tensors = (q, window_kv, comp_kv, attn_sink, iq, ik, w, start_pos, out, topk_idxs, q_ready, rope_cs, ik_codes,
-                 ik_scales)
+                 ik_scales, comp_codes, comp_scales)
     return a, out, topk_idxs
 
 

@@ -552,13 +552,19 @@ static bool decode_shape_fusable(const sti_decode_args* a) {
     if (a->b <= 0 || a->n_cols <= 0 || a->n_cols > 65536 || a->h != 64 || a->d != kD || a->window_size != 128 ||
         a->index_topk != 512)
         return false;
-    if (!a->q || !a->window_kv || !a->comp_kv || !a->attn_sink || !a->out || !a->topk_idxs) return false;
-    if (a->window_bstride % kD != 0 || a->comp_bstride % kD != 0 || a->window_bstride < 128 * kD ||
-        a->comp_bstride < (int64_t)a->n_cols * kD)
-        return false;
-    if (!aligned(a->q, 16) || !aligned(a->window_kv, 16) || !aligned(a->comp_kv, 16) || !aligned(a->out, 16))
-        return false;
+    if (!a->q || !a->window_kv || !a->attn_sink || !a->out || !a->topk_idxs) return false;
+    if (a->window_bstride % kD != 0 || a->window_bstride < 128 * kD) return false;
+    if (!aligned(a->q, 16) || !aligned(a->window_kv, 16) || !aligned(a->out, 16)) return false;
     if ((int64_t)a->b * (a->window_bstride / kD) >= 0x7FFFFFFF || (int64_t)a->b * 64 >= 0x7FFFFFFF) return false;
+    if (a->comp_codes) {   // fp4 rows: 256 code bytes and 32 scale bytes per row, 16-byte aligned
+        if (!a->comp_scales || !aligned(a->comp_codes, 16) || !aligned(a->comp_scales, 16)) return false;
+        if (a->comp_codes_bstride % 16 != 0 || a->comp_scales_bstride % 16 != 0 ||
+            a->comp_codes_bstride < (int64_t)a->n_cols * (kD / 2) || a->comp_scales_bstride < (int64_t)a->n_cols * (kD / 16))
+            return false;
+        return true;
+    }
+    if (!a->comp_kv || a->comp_bstride % kD != 0 || a->comp_bstride < (int64_t)a->n_cols * kD) return false;
+    if (!aligned(a->comp_kv, 16)) return false;
     if ((int64_t)a->b * (a->comp_bstride / kD) >= 0x7FFFFFFF) return false;
     return true;
 }
@@ -623,12 +629,19 @@ static sti_status decode_topk_attn_impl(const sti_decode_args* a, const float* s
     p.rows1 = a->window_bstride / kD;
     p.comp_kv = a->comp_kv;
     p.comp_bstride = a->comp_bstride;
-    p.rows_c = a->comp_bstride / kD;
+    p.rows_c = a->comp_codes ? 0 : a->comp_bstride / kD;
+    p.kvfp4 = a->comp_codes ? 1 : 0;
+    p.comp_codes = a->comp_codes;
+    p.comp_scales = a->comp_scales;
+    p.codes_bstride = a->comp_codes_bstride;
+    p.scales_bstride = a->comp_scales_bstride;
     CUtensorMap tm_q, tm_ring, tm_ring_rows, tm_comp_rows;
+    memset(&tm_comp_rows, 0, sizeof tm_comp_rows);
     sti_status s = make_map_2d(&tm_q, a->q, kD, (uint64_t)a->b * 64, kD * 2, 64, 64);
     if (s == STI_OK) s = make_map_2d(&tm_ring, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 32);
     if (s == STI_OK) s = make_map_2d(&tm_ring_rows, a->window_kv, kD, (uint64_t)a->b * p.rows1, kD * 2, 64, 1);
-    if (s == STI_OK) s = make_map_2d(&tm_comp_rows, a->comp_kv, kD, (uint64_t)a->b * p.rows_c, kD * 2, 64, 1);
+    if (s == STI_OK && !p.kvfp4)   // fp4 rows are gathered by cp.async (no map)
+        s = make_map_2d(&tm_comp_rows, a->comp_kv, kD, (uint64_t)a->b * p.rows_c, kD * 2, 64, 1);
     if (s != STI_OK) return s;
     const cudaError_t e =
         sti::launch_decode_topk_attn(tm_q, tm_ring, tm_ring_rows, tm_comp_rows, p, /*pdl=*/!a->q_ready, st);
@@ -648,6 +661,7 @@ sti_status sti_decode_fused(const sti_decode_args* a, void* ws, size_t ws_bytes,
     if (a->b == 0) return STI_OK;
     if (!ws_ok(ws, ws_bytes, sti_decode_workspace_size(a))) return STI_ERR_INVALID_ARG;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
+    if (a->comp_codes && !decode_fusable(a)) return STI_ERR_UNSUPPORTED;   // fp4 rows: the fused kernel only
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     uint32_t* status = status_word(ws);
@@ -705,6 +719,7 @@ int sti_decode_kernel_count(const sti_decode_args* a) {
     if (!a || a->b < 0 || a->window_size < 1 || a->index_topk < 1 || a->n_cols < 0) return -1;
     if (a->b == 0) return 0;
     if (decode_fusable(a)) return 2;
+    if (a->comp_codes) return -1;   // fp4 compressed rows need the fused kernel
     return a->n_cols > 0 ? 3 : 2;
 }
 
@@ -758,6 +773,7 @@ sti_status sti_decode_fused_noalloc(const sti_decode_args* a, sti_stream stream)
     }
     if (a->b == 0) return STI_OK;
     if (!a->topk_idxs || !a->start_pos) return STI_ERR_INVALID_ARG;
+    if (a->comp_codes && !decode_fusable(a)) return STI_ERR_UNSUPPORTED;   // fp4 rows: the fused kernel only
     if (a->b > STI_NOALLOC_MAX_BATCH || (int64_t)a->b * (a->n_cols > 0 ? a->n_cols : 1) > STI_NOALLOC_MAX_SCORES)
         return STI_ERR_TOO_LARGE;
     uint8_t* scratch = nullptr;

@@ -50,6 +50,7 @@
 #include <vector>
 
 #include "sti_internal.h"
+#include "sti_kvfp4.h"
 #include "sti_ptx.cuh"
 #include "sti_attn_util.cuh"
 
@@ -109,6 +110,7 @@ struct __align__(16) DaTail {
     uint64_t ml_bar;           // merge: the other CTAs' (max, sum) per head landed (bytes)
     uint64_t tk_bar;           // top-k: the other CTAs' words, members and counts landed (24 arrivals + bytes)
     uint64_t recv_bar;         // merge: the three other CTAs' partials of this CTA's d-block landed (bytes)
+    uint64_t f4_bar;           // fp4 compressed rows: the tile's packed rows staged (bytes)
     uint32_t tmem_base;
     int abort;
     int seg_cnt[8 * kCtas];    // top-k: members each warp of the cluster found in the threshold bin
@@ -245,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&tl->ml_bar, 1);
         mbar_init(&tl->tk_bar, (kCtas - 1) * 8);
         mbar_init(&tl->recv_bar, 1);
+        mbar_init(&tl->f4_bar, 1);
         // the merge's incoming bytes, fixed: three (max, sum) vectors and three partial d-blocks
         mbar_arrive_expect_tx(&tl->ml_bar, (kCtas - 1) * kH * 8);
         mbar_arrive_expect_tx(&tl->recv_bar, (kCtas - 1) * kRows * kH * 2);
@@ -890,6 +893,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < 8) mbar_arrive(&tl->full[lane]);
         };
 
+        // ---- the same tile from fp4 rows (256 code bytes + 32 E4M3 scale bytes per row): the packed
+        // rows are staged by bulk copies -- tile rows 0..95 into the ring slice's rows of column
+        // blocks 0..6, rows 96..127 into P^T (both free once the ring slice's PV has read them) --
+        // then all 256 threads decode 16-byte chunks of 8 elements (4 code bytes and their group's
+        // scale) into the tile's swizzled bf16 layout: rows 0..95 first, then, once those stagings
+        // are consumed, rows 96..127 over them.  Masked rows are zero.  One arrive per warp
+        // completes full[j].
+        auto stage_fp4 = [&](int r) -> uint8_t* {   // staged packed row of tile row r (288 bytes)
+            return r < 96 ? tile + (size_t)(r / 14) * kBlkBytes + (size_t)kRingRow0 * 128 + (size_t)(r % 14) * 288
+                          : p_s + (size_t)(r - 96) * 288;
+        };
+        auto gather_comp_fp4 = [&]() {
+            mwait(&tl->ring_free, 0);
+            // one bulk copy of the 256 code bytes and one of the 32 scale bytes per visible row,
+            // lane l of warp mw taking row 16 mw + l, all counted on f4_bar
+            if (lane < 16) {
+                const int r = 16 * mw + lane;
+                const int raw = tl->tile_idx[r];
+                if (raw < -1 || raw >= n2) atomicOr(p.status, 1u /* STI_FLAG_INDEX_RANGE */);   // masked
+                if (raw >= 0 && raw < n2 && !dead) {
+                    uint8_t* dst = stage_fp4(r);
+                    bulk_load(dst, p.comp_codes + (size_t)b * p.codes_bstride + (size_t)raw * (kD / 2), kD / 2,
+                              &tl->f4_bar);
+                    bulk_load(dst + kD / 2, p.comp_scales + (size_t)b * p.scales_bstride + (size_t)raw * (kD / 16),
+                              kD / 16, &tl->f4_bar);
+                }
+            }
+            if (mw == 0) {   // the bytes of every visible row of the tile
+                int nv = 0;
+#pragma unroll
+                for (int r = lane; r < kRows; r += 32) nv += (tl->tile_idx[r] >= 0 && tl->tile_idx[r] < n2) ? 1 : 0;
+                nv = __reduce_add_sync(kFull, nv);
+                if (lane == 0) mbar_arrive_expect_tx(&tl->f4_bar, dead ? 0u : (uint32_t)nv * (kD / 2 + kD / 16));
+            }
+            if (mt == 0) STI_DSTAMP(55);
+            mwait(&tl->f4_bar, 0);
+            if (mt == 0) STI_DSTAMP(56);
+            auto decode = [&](int r0, int r1) {   // four chunks per thread at a time (rows come in
+                for (int i0 = mt; i0 < (r1 - r0) * 64; i0 += 1024) {   // multiples of 16): all four
+                    uint32_t cw[4], sb[4];                               // loaded before any store, so
+                    int rr[4];                                           // the loads need not wait on them
+                    bool ok[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + 256 * u;
+                        rr[u] = r0 + (i >> 6);
+                        const int raw = tl->tile_idx[rr[u]];
+                        ok[u] = raw >= 0 && raw < n2 && !dead;
+                        const uint8_t* st8 = stage_fp4(rr[u]);
+                        const int c = i & 63;
+                        cw[u] = ok[u] ? *reinterpret_cast<const uint32_t*>(st8 + 4 * c) : 0u;
+                        sb[u] = ok[u] ? st8[256 + (c >> 1)] : 0u;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = (i0 + 256 * u) & 63, r = rr[u];
+                        const uint4 v = ok[u] ? kvfp4_decode8(cw[u], e4m3_to_float(sb[u])) : make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(tile + (size_t)(c >> 3) * kBlkBytes + (size_t)r * 128 +
+                                                  ((((uint32_t)(c & 7)) ^ (uint32_t)(r & 7)) << 4)) = v;
+                    }
+                }
+            };
+            decode(0, 96);
+            if (mt == 0) STI_DSTAMP(57);
+            named_bar_sync(kBarMath, 256);   // rows 0..95's stagings are consumed
+            decode(96, 128);
+            if (mt == 0) STI_DSTAMP(58);
+            fence_proxy_async_smem();   // generic writes, read by the tensor core
+            __syncwarp();
+            if (lane < 8) mbar_arrive(&tl->full[lane]);
+        };
+
         // compressed row of tile row i once the indices are here: -1 when masked or out of range
         auto tile_row = [&](int i) {
             const int v = tl->tile_idx[i];
@@ -906,9 +981,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         griddep_wait();   // the scores and histogram are complete from here on
         if (mt == 0) STI_DSTAMP(2);
         topk_row(max(0, min((sp + 1) / p.ratio, n2)));
+        fence_proxy_async_smem();   // the scratch's generic writes, before the gather's async copies over it
         named_bar_sync(kBarMath, 256);   // every index is in tile_idx; the scratch rows are free
         if (mt == 0) STI_DSTAMP(9);
-        gather_comp();
+        if (p.kvfp4) gather_comp_fp4();
+        else gather_comp();
         if (mt == 0) STI_DSTAMP(10);
         mwait(&tl->p_full, 0);   // the ring slice's running max and sum (warp 11) are visible
         softmax_tile(1, !dead && tile_row(row) >= 0);

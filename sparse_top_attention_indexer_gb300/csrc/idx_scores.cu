@@ -175,33 +175,6 @@ __device__ __forceinline__ float e2m1_value(uint32_t nib) {
     return __uint_as_float(bits | ((nib & 8u) << 28));
 }
 
-// Eight E2M1 nibbles (one 32-bit word: byte j holds elements 2j (low nibble) and 2j+1) -> four
-// bf16x2 words of the values times 2^X, for scale bytes e8 in [2, 252] (X = e8 - 127): byte
-// permutes look up each magnitude's bf16 bytes (a table of the eight E2M1 magnitudes), the sign
-// bits move into place, and X is added to the exponent field of every non-zero half.
-__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t cw, uint32_t expadd, uint32_t (&o)[4]) {
-    const uint32_t lo = cw & 0x07070707u, hi = (cw >> 4) & 0x07070707u;   // magnitude codes per byte
-    const uint32_t yl = lo | (lo >> 4), yh = hi | (hi >> 4);
-    const uint32_t sel_l = (yl & 0xFFu) | ((yl >> 8) & 0xFF00u);            // 4 selector nibbles
-    const uint32_t sel_h = (yh & 0xFFu) | ((yh >> 8) & 0xFF00u);
-    // bf16 of 0, .5, 1, 1.5 | 2, 3, 4, 6: high bytes 00 3F 3F 3F | 40 40 40 40, low bytes 00 00 80 C0 | 00 40 80 C0
-    uint32_t hl = __byte_perm(0x3F3F3F00u, 0x40404040u, sel_l);
-    const uint32_t ll = __byte_perm(0xC0800000u, 0xC0804000u, sel_l);
-    uint32_t hh = __byte_perm(0x3F3F3F00u, 0x40404040u, sel_h);
-    const uint32_t lh = __byte_perm(0xC0800000u, 0xC0804000u, sel_h);
-    hl |= (cw << 4) & 0x80808080u;   // sign of the low nibble -> top bit of its high byte
-    hh |= cw & 0x80808080u;          // sign of the high nibble
-    const uint32_t t0 = __byte_perm(ll, hl, 0x5140u);   // elements 0 | 2 << 16
-    const uint32_t t1 = __byte_perm(lh, hh, 0x5140u);   // elements 1 | 3 << 16
-    const uint32_t t2 = __byte_perm(ll, hl, 0x7362u);   // elements 4 | 6 << 16
-    const uint32_t t3 = __byte_perm(lh, hh, 0x7362u);   // elements 5 | 7 << 16
-    o[0] = __byte_perm(t0, t1, 0x5410u);
-    o[1] = __byte_perm(t0, t1, 0x7632u);
-    o[2] = __byte_perm(t2, t3, 0x5410u);
-    o[3] = __byte_perm(t2, t3, 0x7632u);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = __vadd2(o[k], expadd & __vcmpne2(o[k] & 0x7FFF7FFFu, 0u));
-}
 
 // E8M0 scale byte -> 2^(e - 127) (255 is NaN).
 __device__ __forceinline__ float e8m0_value(uint32_t e) {

@@ -64,37 +64,6 @@ struct __align__(8) AttnSmemTail {
     int row_srcid[kRows];  // 0: kv, 1: kv2, -1: masked
 };
 
-// E4M3 byte (sign, 4-bit exponent with bias 7, 3-bit mantissa; exponent 0 subnormal: m * 2^-9;
-// S.1111.111 NaN) -> float.
-__device__ __forceinline__ float e4m3_to_float(uint32_t v) {
-    const uint32_t e = (v >> 3) & 15u, m = v & 7u, sg = (v & 0x80u) << 24;
-    if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
-    return e == 0u ? __uint_as_float(sg | __float_as_uint((float)m * 0.001953125f))
-                   : __uint_as_float(sg | ((e + 120u) << 23) | (m << 20));
-}
-
-// E2M1 nibble (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa; exponent 0 is
-// subnormal: m * 0.5) -> float.
-__device__ __forceinline__ float e2m1_to_float(uint32_t nib) {
-    const uint32_t e = (nib >> 1) & 3u, m = nib & 1u;
-    const uint32_t bits = e ? ((126u + e) << 23) | (m << 22) : (m ? 0x3F000000u : 0u);
-    return __uint_as_float(bits | ((nib & 8u) << 28));
-}
-
-// Eight fp4 elements (nibble i of cw = element i) times their E4M3 scale s as eight bf16 (one
-// 16-byte chunk of the tile).  A product of an E2M1 value and an E4M3 value has at most five
-// significant bits, so dropping the low half of its fp32 pattern is exact.
-__device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float lo = e2m1_to_float((cw >> (8 * j)) & 15u) * s;
-        const float hi = e2m1_to_float((cw >> (8 * j + 4)) & 15u) * s;
-        o[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 // Swizzled byte offset of 16-byte chunk `ch` (of 8 bf16) of row `r` in a tile of `rows` rows
 // stored as column blocks of rows x 128 bytes (128-byte swizzle: chunk ^= row % 8).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {

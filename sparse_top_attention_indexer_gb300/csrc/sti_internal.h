@@ -129,6 +129,11 @@ struct DecodeAttnParams {
     int B, n_cols, ratio;
     int64_t rows1;             // rows per batch element of the ring (batch stride / 512)
     int64_t rows_c;            // rows per batch element of the compressed KV (comp_bstride / 512)
+    // optional fp4 compressed KV (comp_kv unused): codes [B][*][256] and E4M3 scales [B][*][32]
+    const uint8_t* comp_codes;
+    const uint8_t* comp_scales;
+    int64_t codes_bstride, scales_bstride;   // bytes
+    int kvfp4;
 };
 bool decode_topk_attn_available();
 size_t decode_topk_attn_smem_bytes();

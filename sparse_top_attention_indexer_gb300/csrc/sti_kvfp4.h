@@ -8,6 +8,10 @@
 #pragma once
 
 #include "sti_internal.h"
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#include "sti_ptx.cuh"
+#endif
 
 namespace sti {
 
@@ -18,6 +22,34 @@ struct KvFp4 {
     int64_t scales_bstride;
     int on;                   // 0: the second source is bf16 (AttnParams::kv2)
 };
+
+#ifdef __CUDACC__
+// E4M3 byte (sign, 4-bit exponent with bias 7, 3-bit mantissa; exponent 0 subnormal: m * 2^-9;
+// S.1111.111 NaN) -> float.
+__device__ __forceinline__ float e4m3_to_float(uint32_t v) {
+    const uint32_t e = (v >> 3) & 15u, m = v & 7u, sg = (v & 0x80u) << 24;
+    if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
+    return e == 0u ? __uint_as_float(sg | __float_as_uint((float)m * 0.001953125f))
+                   : __uint_as_float(sg | ((e + 120u) << 23) | (m << 20));
+}
+
+// Eight fp4 elements (nibble i of cw = element i) times their E4M3 scale s as eight bf16 (one
+// 16-byte chunk of the tile): the E2M1 values by byte-permute lookup (e2m1x8_to_bf16), then four
+// bf16x2 products with the scale.  Every factor is exact in bf16 and a product of an E2M1 value
+// and an E4M3 value has at most six significant bits, so each product is exact.
+__device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
+    uint32_t o[4];
+    e2m1x8_to_bf16(cw, 0u, o);
+    const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&o[j]), s2);
+        o[j] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+#endif
 
 // launch_sparse_attn with the second source given as fp4 rows (f.on != 0; p.kv2 unused); the rows
 // are gathered with plain loads and decoded into the tile, so p.use_tma must be 0.

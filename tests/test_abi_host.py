@@ -120,6 +120,29 @@ def test_fp4kv_argument_checks(libsti):
     assert call(sb=n2 * d // 16 + 8) == 1        # scales batch stride not a multiple of 16
 
 
+def test_decode_fp4kv_rows_need_the_fused_shape(libsti):
+    """fp4 compressed rows in the decode arguments: a shape the fused kernel does not take (32
+    heads) is refused on the host, before anything is enqueued, and the kernel count says so."""
+    fake = 1 << 20
+    P = ctypes.c_void_p
+    import sparse_top_attention_indexer_gb300 as m
+
+    a = m.DecodeArgs()
+    a.q, a.window_kv, a.window_bstride, a.attn_sink = P(fake), P(fake), 128 * 512, P(fake)
+    a.h, a.d, a.window_size, a.softmax_scale = 32, 512, 128, 0.04
+    a.iq, a.ik, a.ik_bstride, a.w, a.index_scale = P(fake), P(fake), 1024 * 128, P(fake), 0.01
+    a.Hi, a.Di, a.index_topk, a.ratio, a.n_cols = 32, 128, 512, 4, 1024
+    a.start_pos, a.b, a.out, a.topk_idxs = P(fake), 2, P(fake), P(fake)
+    a.comp_codes, a.comp_codes_bstride = P(fake), 1024 * 256
+    a.comp_scales, a.comp_scales_bstride = P(fake), 1024 * 32
+    assert libsti.sti_decode_kernel_count(ctypes.byref(a)) == -1
+    assert libsti.sti_decode_fused(ctypes.byref(a), P(fake), 1 << 30, None, None) == 2
+    assert libsti.sti_decode_fused_noalloc(ctypes.byref(a), None) == 2
+    a.comp_codes = None   # the same shape with bf16 rows (none given here): three kernels
+    a.comp_kv, a.comp_bstride = P(fake), 1024 * 512
+    assert libsti.sti_decode_kernel_count(ctypes.byref(a)) == 3
+
+
 def test_selftest_argument_checks(libsti):
     fake = 1 << 20
     P = ctypes.c_void_p

@@ -107,8 +107,9 @@ def test_e2m1_to_bf16_every_nibble_and_scale():
 
 
 def test_fp4_kv_decode_values():
-    """The attention's fp4 row decode: E4M3 byte -> fp32 from its bit fields, times the E2M1
-    value, truncated to bf16 -- equal to the oracle's decode for every code and finite scale."""
+    """The attention's fp4 row decode: the E4M3 scale byte -> fp32 from its bit fields (exact in
+    bf16), times the E2M1 value (looked up by the byte-permute decoder checked above) -- every
+    product exact in bf16 and equal to the oracle's decode for every code and finite scale."""
     def e4m3_to_f32(v: int) -> float:
         e, m, sg = (v >> 3) & 15, v & 7, (v & 0x80) << 24
         if e == 0:

@@ -483,6 +483,50 @@ def test_decode_fused_small(sti, orc):
     check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
 
 
+def test_decode_fused_fp4kv(sti, orc):
+    """The decode step with the compressed KV as fp4 rows (codes + E4M3 scales, the form
+    Attention._compress_kv writes): the fused kernel stages and decodes the packed rows; ragged
+    batch with rows short of index_topk (masked slots), a filling ring, and one sequence with no
+    compressed rows yet.  A shape the fused kernel does not take is refused on the host."""
+    import torch
+
+    shp = workloads.custom("decode_fp4kv", b=5, s=1, start_pos=[8191, 700, 5, 3000, 2], seed=91, n_cols=2048,
+                           topk=512, h=64, d=512, fp4_kv=True)
+    data = workloads.make(shp)
+    sp = data["start_pos"]
+    W = shp.window
+    ref_scores = orc.index_score(data["iq"], data["ik"], data["w"], shp.index_scale, sp, shp.n_cols, shp.ratio)
+    ref_cidx = orc.topk(ref_scores, sp, shp.ratio, shp.topk, W)
+    ref_widx = np.concatenate([orc.window_topk_idxs(W, 1, 1, int(v)) for v in sp], axis=0)
+    ref_idx = np.concatenate([ref_widx, ref_cidx], axis=-1)
+    ref_out, _ = orc.sparse_attn_fp4kv(data["q"][0], data["win"][0], data["comp_codes"], data["comp_scales"],
+                                       data["sink"][0], ref_idx, shp.softmax_scale)
+    codes, scales = to_dev_any(data["comp_codes"]), to_dev_any(data["comp_scales"])
+    a, out, tk = sti.decode_args(to_dev(data["q"][0]), to_dev(data["win"][0]), None, to_dev_any(data["sink"][0]),
+                                 shp.softmax_scale, to_dev(data["iq"]), to_dev(data["ik"]), to_dev(data["w"]),
+                                 shp.index_scale, to_dev_any(sp), shp.ratio, shp.n_cols, shp.topk,
+                                 comp_codes=codes, comp_scales=scales)
+    assert sti.decode_kernel_count(a) == 2
+    ws = sti.workspace(sti.decode_workspace_size(a))
+    for _ in range(2):
+        sti.decode_fused(a, ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got_idx = tk.cpu().numpy().reshape(shp.b, 1, -1)
+    np.testing.assert_array_equal(got_idx[..., :W], ref_widx)
+    check_topk_rows(got_idx[..., W:], ref_cidx, ref_scores, W, shp.topk)
+    check_attn(bf16_out_to_f64(out).reshape(ref_out.shape), ref_out)
+    # 32 heads: not the fused shape, so fp4 rows are refused before anything is enqueued
+    a32, _, _ = sti.decode_args(to_dev(data["q"][0][:, :, :32]), to_dev(data["win"][0]), None,
+                                to_dev_any(data["sink"][0][:32]), shp.softmax_scale, to_dev(data["iq"]),
+                                to_dev(data["ik"]), to_dev(data["w"]), shp.index_scale, to_dev_any(sp), shp.ratio,
+                                shp.n_cols, shp.topk, comp_codes=codes, comp_scales=scales)
+    with pytest.raises(RuntimeError):   # sti_decode_kernel_count returns -1
+        sti.decode_kernel_count(a32)
+    with pytest.raises(RuntimeError):   # STI_ERR_UNSUPPORTED
+        sti.decode_fused(a32, sti.workspace(sti.decode_workspace_size(a32)))
+
+
 @pytest.mark.parametrize("n_cols,sps,label", [
     (2101, [127, 126, 95, 31, 1, 2047, 2051, 8399],
      "ring full / one slot short / whole ring slices empty; vis = K, K+1; score rows not 16-byte aligned"),

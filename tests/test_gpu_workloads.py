@@ -39,7 +39,7 @@ def _run(shape, data, device):
     return path
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 5, 6, 7, 9])
+@pytest.mark.parametrize("n", [1, 2, 4, 5, 6, 7, 9, 11])
 def test_workload_full(gpu, orc, n):
     shape = workloads.config(n)
     data = workloads.make(shape)
@@ -67,8 +67,12 @@ def test_workload_full(gpu, orc, n):
     # attention of every layer (the oracle on its own indices)
     ref_idx = np.concatenate([ref_w, ref_c], axis=-1)
     for i in range(shape.n_layers):
-        ref_o, _ = orc.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], ref_idx, shape.softmax_scale,
-                                   kv2=data["comp"])
+        if shape.fp4_kv:
+            ref_o, _ = orc.sparse_attn_fp4kv(data["q"][i], data["win"][i], data["comp_codes"], data["comp_scales"],
+                                             data["sink"][i], ref_idx, shape.softmax_scale)
+        else:
+            ref_o, _ = orc.sparse_attn(data["q"][i], data["win"][i], data["sink"][i], ref_idx, shape.softmax_scale,
+                                       kv2=data["comp"])
         mx, mn = check_attn(bf16_out_to_f64(path.out[i]), ref_o)
         print(f"workload {n} layer {i}: score rel err {worst:.2e}, banded rows {banded}, attn max {mx:.2e} "
               f"mean {mn:.2e}")

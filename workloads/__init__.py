@@ -131,8 +131,8 @@ class Shape:
 def config(n: int) -> Shape:
     """The named workloads: 1-5 as listed in the design notes, 6 and 7 the decode workload at
     compression ratios 2 and 1 (32768 and 65536 index rows per sequence), 8 a prefill chunk
-    that continues its sequence, 9 workload 2 with MXFP4 index keys, 10 workload 3 with the
-    compressed KV rows stored as fp4."""
+    that continues its sequence, 9 workload 2 with MXFP4 index keys, 10 workload 3 and 11
+    workload 2 with the compressed KV rows stored as fp4."""
     seed = 1000 + n
     if n == 1:
         return Shape("tiny_prefill_s256_h4_d64", b=1, s=256, start_pos=np.zeros(1, np.int32), h=4, d=64, rd=16,
@@ -154,6 +154,9 @@ def config(n: int) -> Shape:
     if n == 9:   # workload 2 with MXFP4 index keys
         return Shape("decode_b32_ctx65536_mxfp4", b=32, s=1, start_pos=np.full(32, 65535, np.int32), n_cols=16384,
                      fp4_keys=True, seed=seed)
+    if n == 11:  # workload 2 with fp4 compressed-KV rows
+        return Shape("decode_b32_ctx65536_kvfp4", b=32, s=1, start_pos=np.full(32, 65535, np.int32), n_cols=16384,
+                     rms_keys=True, fp4_kv=True, seed=seed)
     if n == 10:  # workload 3 with fp4 compressed-KV rows
         return Shape("prefill_s8192_kvfp4", b=1, s=8192, start_pos=np.zeros(1, np.int32), n_cols=2048, fp4_kv=True,
                      seed=seed)
