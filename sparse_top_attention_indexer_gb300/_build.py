@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsti.so")
-SOURCES = ["api.cu", "idx_scores.cu", "idx_topk.cu", "sparse_attn.cu", "sparse_attn_hs.cu", "decode_attn.cu"]
+SOURCES = ["api.cu", "idx_scores.cu", "idx_topk.cu", "sparse_attn.cu", "sparse_attn_stream.cu", "sparse_attn_hs.cu",
+           "decode_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

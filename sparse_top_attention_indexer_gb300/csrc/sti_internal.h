@@ -103,6 +103,11 @@ int attn_pick_cluster(int n_queries, int k, int d);
 // for 4-row gathers).  Ignored unless p.use_tma.
 cudaError_t launch_sparse_attn(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                const AttnParams& p, cudaStream_t stream);
+// Many queries (prefill): persistent CTAs with the tile streamed by column block (64 heads at
+// most, d = 512, TMA gathers, no cluster); same maps as launch_sparse_attn.
+bool sparse_attn_stream_fits(const AttnParams& p);
+cudaError_t launch_sparse_attn_stream(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                      const AttnParams& p, cudaStream_t stream);
 // Few queries with 32 or 64 heads: CTAs per query of the head-split kernel (0 = not applicable
 // or not resident) and, in *rows, how many row groups they form; its launch (tm_q's box is
 // {64, heads per CTA}).

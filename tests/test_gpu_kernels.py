@@ -301,6 +301,61 @@ def test_sparse_attn_many_queries(sti, orc, b, s, d, k, n1, n2):
     np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
 
 
+def test_sparse_attn_streamed_prefill(sti, orc):
+    """Many queries of up to 64 heads x 512 run on persistent CTAs that stream each tile by column
+    block (several queries per CTA at 500 queries).  Index rows like the pages' prefill rows
+    ([window | compressed], -1 where nothing is visible) plus what the stream must survive: rows
+    whose middle or leading tiles are all -1, rows with no valid slot between live ones, four-row
+    groups mixing both sources, an out-of-range index (flagged and masked), 48 heads, the output
+    rotation and the lse."""
+    import torch
+
+    rng = rng_for(790, 0)
+    b, s, h, d, k, n1, n2, rd = 2, 250, 48, 512, 640, 300, 900, 64
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = np.full((b, s, k), -1, np.int32)
+    for bi in range(b):
+        for t in range(s):
+            w = min(128, t + 1)                                   # window slots, -1 before the start
+            idx[bi, t, 128 - w:128] = np.arange(t + 1 - w, t + 1) % n1
+            nc = int(rng.integers(0, 513))                        # compressed slots, ascending, -1 padded
+            idx[bi, t, 128:128 + nc] = n1 + np.sort(rng.choice(n2, nc, replace=False))
+    idx[0, 3] = -1                                                # no valid slot
+    idx[1, 100] = -1
+    idx[0, 10, :256] = -1                                         # leading tiles dead
+    idx[0, 11, 128:512] = -1                                      # middle tiles dead, last tile live
+    idx[0, 11, 600:620] = n1 + np.arange(20)
+    idx[1, 7, 128:132] = [5, n1 + 9, -1, 6]                       # groups mixing both sources
+    idx[1, 7, 40:44] = [n1 + 1, 3, n1 + 2, -1]
+    bad = idx.copy()
+    bad[1, 20, 130] = n1 + n2 + 5                                 # out of range: flagged, masked
+    idx[1, 20, 130] = -1
+    cs = _rope_table(rng, (b, s), rd)
+    ref, ref_lse = orc.sparse_attn(q, kv1, sink, idx, d ** -0.5, kv2=kv2, rope_cs=cs)
+    lse = torch.empty(b, s, h, dtype=torch.float32, device="cuda")
+    ws = sti.workspace(256)
+    out = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(bad), d ** -0.5,
+                               kv2=to_dev(kv2), lse=lse, ws=ws, rope_cs=to_dev_any(cs))
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == sti.FLAG_INDEX_RANGE
+    got = bf16_out_to_f64(out)
+    check_attn(got, ref)
+    assert np.all(got[np.all(idx < 0, axis=-1)] == 0)
+    lg = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+    # a second call on the same buffers gives the same bits
+    out2 = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5,
+                                kv2=to_dev(kv2), ws=ws, rope_cs=to_dev_any(cs))
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    assert torch.equal(out, out2)
+
+
 def test_sparse_attn_whole_tiles_masked(sti, orc):
     """Decode-style rows where whole 128-slot tiles are -1 (short sequences), split over CTAs."""
     rng = rng_for(720, 0)
