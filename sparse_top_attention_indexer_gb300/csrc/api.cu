@@ -378,10 +378,16 @@ static sti_status attn_impl(const uint16_t* q, const uint16_t* kv, int64_t kv_bs
         if (n2 == 0) tm_kv2 = tm_kv1;
     }
     const bool stream = !head_split && !fp4 && sti::sparse_attn_stream_fits(p);
-    cudaError_t e = head_split ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, tm_win, p, st)
-                     : fp4     ? sti::launch_sparse_attn_kvfp4(tm_q, tm_kv1, tm_kv2, p, *fp4, st)
-                     : stream  ? sti::launch_sparse_attn_stream(tm_q, tm_kv1, tm_kv2, p, st)
-                               : sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
+    const bool stream_fp4 = fp4 && sti::sparse_attn_stream_fits_fp4(p);
+    if (stream_fp4) {   // Q by TMA; the rows by LSU copies and fp4 decoding
+        sti_status s = make_map_2d(&tm_q, q, (uint64_t)d, (uint64_t)nq * h, (uint64_t)d * 2, 64, (uint32_t)h);
+        if (s != STI_OK) return s;
+    }
+    cudaError_t e = head_split   ? sti::launch_sparse_attn_hs(tm_q, tm_kv1, tm_kv2, tm_win, p, st)
+                     : stream_fp4 ? sti::launch_sparse_attn_stream_fp4(tm_q, p, *fp4, st)
+                     : fp4        ? sti::launch_sparse_attn_kvfp4(tm_q, tm_kv1, tm_kv2, p, *fp4, st)
+                     : stream     ? sti::launch_sparse_attn_stream(tm_q, tm_kv1, tm_kv2, p, st)
+                                  : sti::launch_sparse_attn(tm_q, tm_kv1, tm_kv2, p, st);
     return e == cudaSuccess ? STI_OK : cuda_fail(e, "sti_sparse_attn_sink");
 }
 

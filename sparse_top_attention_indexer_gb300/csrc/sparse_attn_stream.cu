@@ -39,6 +39,7 @@
 
 #include "sti_attn_util.cuh"
 #include "sti_internal.h"
+#include "sti_kvfp4.h"
 #include "sti_ptx.cuh"
 
 namespace sti {
@@ -53,9 +54,11 @@ constexpr uint32_t kQBlkB = kSH * 128;         // one Q column block: 8 KB
 constexpr uint32_t kTBlkB = kSRows * 128;      // one tile column block: 16 KB
 constexpr uint32_t kTmS0 = 0, kTmS1 = 64;      // TMEM columns of the two S^T partials
 constexpr uint32_t kTmO = 128;                 // O^T d-block m at columns [128 + 64 m, 192 + 64 m)
-// a tile column block is filled by 16 four-row TMA gathers (rows 0..63) and by 128 threads' LSU
-// copies (rows 64..127, 64 bytes each): the TMA unit and the LSU pipes run side by side
+// bf16 rows: a tile column block is filled by 16 four-row TMA gathers (rows 0..63) and by 128
+// threads' LSU copies (rows 64..127, 64 bytes each), so the TMA unit and the LSU run side by
+// side; fp4 compressed rows: by 128 threads, one row each, decoded from registers
 constexpr uint32_t kFullArrivals = 16 + 128;
+constexpr uint32_t kFullArrivalsFp4 = 128;
 constexpr uint32_t kBarMath = 3;               // named barrier of the 256 math threads (1, 2: head groups)
 constexpr float kLog2eS = 1.4426950408889634f;
 constexpr float kLn2S = 0.69314718055994531f;
@@ -66,7 +69,7 @@ struct __align__(16) StreamTail {
     float red[2][2][4][32];   // [tile parity][head group][warp quarter][head]: per-warp maxima
     float lsum[2][4][32];     // [head group][warp quarter][head]: per-warp sums at a query's end
     float sink_log2[kSH];     // the heads' sinks times log2(e)
-    uint64_t full[kSCb];   // column block j of the tile landed: kFullArrivals arrivals (+ the TMA bytes)
+    uint64_t full[kSCb];   // column block j of the tile landed (see kFullArrivals; + the TMA bytes)
     uint64_t pv[4];        // the tile's PV of d-block m done (column blocks 2m, 2m+1 free)
     uint64_t s_full;       // the tile's QK done
     uint64_t p_full;       // the tile's P^T written: one arrival per math warp
@@ -119,9 +122,12 @@ __device__ unsigned long long g_stream_t[160][16][24];
     } while (0)
 #endif
 
+// FP4: the second source holds fp4 rows (f); every row of a tile is then copied by one thread:
+// bf16 rows by LSU copies, fp4 rows loaded into registers before their block is free and decoded.
+template <bool FP4>
 __global__ void __launch_bounds__(kSThreads, 1)
     sparse_attn_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv1,
-                              const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p) {
+                              const __grid_constant__ CUtensorMap tm_kv2, const AttnParams p, const KvFp4 f) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned start (the swizzle atoms), offset from the __shared__ array itself
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tmem_relinquish();
     }
     if (tid == 32) {
-        for (int j = 0; j < kSCb; ++j) mbar_init(&tl->full[j], kFullArrivals);
+        for (int j = 0; j < kSCb; ++j) mbar_init(&tl->full[j], FP4 ? kFullArrivalsFp4 : kFullArrivals);
         for (int m = 0; m < 4; ++m) mbar_init(&tl->pv[m], 1);
         mbar_init(&tl->s_full, 1);
         mbar_init(&tl->p_full, 8);
@@ -166,8 +172,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // ------------------------------------------------------------------ Q loads
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_kv1);
-            tma_prefetch_desc(&tm_kv2);
+            if (!FP4) {
+                tma_prefetch_desc(&tm_kv1);
+                tma_prefetch_desc(&tm_kv2);
+            }
         }
         uint32_t qn = 0;
         for (int qi = blockIdx.x; qi < nq; qi += stride) {
@@ -256,6 +264,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int lr = 64 + ((mt >> 1) & 63);
         const int lb = mt >> 7;
         const int lc0 = 4 * (mt & 1);
+        // fp4 compressed rows (FP4): this thread copies row fr of column block 2m + fh of every pair
+        const int fr = mt & 127;
+        const int fh = mt >> 7;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
         const uint32_t bar_set = 1u + (uint32_t)set;
         uint32_t n = 0;                           // tiles this CTA has processed
@@ -280,9 +291,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int sl = s0 + 4 * tg + i;
-                ti.g[i] = (tma_lane && sl < p.k) ? __ldg(idx_row + sl) : -1;
+                ti.g[i] = (!FP4 && tma_lane && sl < p.k) ? __ldg(idx_row + sl) : -1;
             }
-            ti.l = s0 + lr < p.k ? __ldg(idx_row + s0 + lr) : -1;
+            const int gr = FP4 ? fr : lr;
+            ti.l = s0 + gr < p.k ? __ldg(idx_row + s0 + gr) : -1;
             ti.r = s0 + row < p.k ? __ldg(idx_row + s0 + row) : -1;
         };
         // a slot's row: source (-1 masked) and coordinate in the [B * rows, d] view of its source
@@ -290,6 +302,53 @@ __global__ void __launch_bounds__(kSThreads, 1)
             if (v < -1 || v >= n_rows) v = -1;
             sid = v < 0 ? -1 : (v < p.n1 ? 0 : 1);
             crd = sid < 0 ? 0 : sid == 0 ? (int)((int64_t)b * p.rows1 + v) : (int)((int64_t)b * p.rows2 + (v - p.n1));
+        };
+
+        auto gather_fp4 = [&](const TileIdx& ti, int b) {
+            int sid, crd;
+            resolve(ti.l, b, sid, crd);   // fp4 rows: crd is the row within its batch element
+            uint4 cw[4][2];
+            uint32_t sw[4];
+            if (sid == 1) {   // the packed bytes do not wait for the block: load them now
+                const uint8_t* cr = f.codes + (size_t)b * f.codes_bstride + (size_t)crd * (kSD / 2);
+                const uint8_t* sr = f.scales + (size_t)b * f.scales_bstride + (size_t)crd * (kSD / 16);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int j = 2 * m + fh;
+                    cw[m][0] = __ldg(reinterpret_cast<const uint4*>(cr + j * 32));
+                    cw[m][1] = __ldg(reinterpret_cast<const uint4*>(cr + j * 32 + 16));
+                    sw[m] = __ldg(reinterpret_cast<const uint32_t*>(sr + j * 4));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (n > 0) mwait(&tl->pv[m], (n - 1) & 1u);   // column blocks 2m, 2m+1 are free
+                if (mw == 0 && lane == 0 && n > 0) STI_STAMP(n - 1, 7 + m);
+                if (dead) continue;
+                const int j = 2 * m + fh;
+                uint8_t* dst = t_s + (size_t)j * kTBlkB + (size_t)fr * 128;
+                if (sid == 0) {   // a bf16 row of the first source
+                    const uint16_t* src = p.kv + (size_t)crd * kSD + j * 64;
+                    const uint32_t d0 = smem_u32(dst);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) cp_async_16(d0 + (uint32_t)((c ^ (fr & 7)) << 4), src + c * 8, 16u);
+                    cp_async_mbar_arrive_noinc(&tl->full[j]);
+                    continue;
+                }
+                if (sid == 1) {   // 64 elements: eight words of eight codes, an E4M3 scale per two words
+                    const uint32_t w[8] = {cw[m][0].x, cw[m][0].y, cw[m][0].z, cw[m][0].w,
+                                           cw[m][1].x, cw[m][1].y, cw[m][1].z, cw[m][1].w};
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(dst + ((c ^ (fr & 7)) << 4)) =
+                            kvfp4_decode8(w[c], e4m3_to_float((sw[m] >> (8 * (c >> 1))) & 0xFFu));
+                } else {          // masked: zeros (finite, and P = 0 for them)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + (c << 4)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&tl->full[j]);
+            }
         };
 
         auto gather = [&](const TileIdx& ti, int b) {
@@ -563,7 +622,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
             while (rem) {
                 rem &= rem - 1u;
                 if (mw == 0 && lane == 0) STI_STAMP(n, 0);
-                gather(cur, b);
+                if constexpr (FP4) gather_fp4(cur, b);
+                else gather(cur, b);
                 if (mw == 0 && lane == 0) STI_STAMP(n, 1);
                 // the next tile's index slots load while this tile's rows land
                 if (!rem) qn = next_live(qi, live_n);
@@ -614,14 +674,20 @@ bool sparse_attn_stream_fits(const AttnParams& p) {
            p.k <= 32 * kSRows && p.rope_dims <= kSD;
 }
 
-cudaError_t launch_sparse_attn_stream(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
-                                      const AttnParams& p, cudaStream_t stream) {
-    if (!sparse_attn_stream_fits(p)) return cudaErrorInvalidValue;
+bool sparse_attn_stream_fits_fp4(const AttnParams& p) {
+    // the first source's rows are addressed as kv + (b * rows1 + idx) * d: whole rows per batch element
+    return p.cluster == 1 && p.d == kSD && p.d_pad == kSD && p.h >= 1 && p.h <= kSH && p.k >= 1 &&
+           p.k <= 32 * kSRows && p.rope_dims <= kSD && (p.n1 == 0 || p.kv_bstride == p.rows1 * kSD);
+}
+
+template <bool FP4>
+static cudaError_t launch_stream(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                 const AttnParams& p, const KvFp4& f, cudaStream_t stream) {
     const int nq = p.B * p.s;
     if (nq == 0) return cudaSuccess;
     const size_t smem = stream_smem_bytes();
     cudaError_t err =
-        cudaFuncSetAttribute(sparse_attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(sparse_attn_stream_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const int sms = device_num_sms();
     cudaLaunchConfig_t cfg = {};
@@ -638,8 +704,21 @@ cudaError_t launch_sparse_attn_stream(const CUtensorMap& tm_q, const CUtensorMap
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_stream_kernel, tm_q, tm_kv1, tm_kv2, p);
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_stream_kernel<FP4>, tm_q, tm_kv1, tm_kv2, p, f);
     return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+cudaError_t launch_sparse_attn_stream(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
+                                      const AttnParams& p, cudaStream_t stream) {
+    if (!sparse_attn_stream_fits(p)) return cudaErrorInvalidValue;
+    KvFp4 none{};
+    return launch_stream<false>(tm_q, tm_kv1, tm_kv2, p, none, stream);
+}
+
+cudaError_t launch_sparse_attn_stream_fp4(const CUtensorMap& tm_q, const AttnParams& p, const KvFp4& f,
+                                          cudaStream_t stream) {
+    if (!sparse_attn_stream_fits_fp4(p) || !f.on) return cudaErrorInvalidValue;
+    return launch_stream<true>(tm_q, tm_q, tm_q, p, f, stream);
 }
 
 }  // namespace sti

@@ -55,5 +55,11 @@ __device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
 // are gathered with plain loads and decoded into the tile, so p.use_tma must be 0.
 cudaError_t launch_sparse_attn_kvfp4(const CUtensorMap& tm_q, const CUtensorMap& tm_kv1, const CUtensorMap& tm_kv2,
                                      const AttnParams& p, const KvFp4& f, cudaStream_t stream);
+// The streamed many-query kernel with fp4 rows in the second source (64 heads at most, d = 512, no
+// cluster): the first source's rows come by LSU copies, the fp4 rows are loaded into registers
+// and decoded into the tile.  tm_q: q as [B*s*h, d] (box 64 x h).
+bool sparse_attn_stream_fits_fp4(const AttnParams& p);
+cudaError_t launch_sparse_attn_stream_fp4(const CUtensorMap& tm_q, const AttnParams& p, const KvFp4& f,
+                                          cudaStream_t stream);
 
 }  // namespace sti

@@ -228,6 +228,7 @@ def test_sparse_attn(sti, orc, b, s, h, d, k, n1, n2, empty):
     (2, 1, 64, 512, 640, 128, 300, True),     # decode shape: window + compressed rows, split over a cluster
     (3, 1, 64, 512, 640, 128, 2000, False),   # decode shape, one CTA per query
     (1, 70, 64, 512, 256, 200, 100, False),   # several queries
+    (1, 400, 48, 512, 640, 128, 900, False),  # more queries than SMs: the streamed kernel, 48 heads
     (2, 5, 16, 64, 300, 10, 700, True),       # small rows (d = 64: 4 scale bytes per row)
 ])
 def test_sparse_attn_fp4kv(sti, orc, b, s, h, d, k, n1, n2, ws_full):
