@@ -69,9 +69,10 @@ def peaks():
 
 
 KERNEL_SOURCES = {"idx_scores": ["idx_scores.cu"], "idx_topk": ["idx_topk.cu"],
-                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_hs.cu", "sti_attn_util.cuh", "sti_kvfp4.h"],
+                  "sparse_attn": ["sparse_attn.cu", "sparse_attn_stream.cu", "sparse_attn_hs.cu", "sti_attn_util.cuh",
+                                  "sti_kvfp4.h"],
                   "window_idx": ["idx_topk.cu"],
-                  "topk_sparse_attn": ["decode_attn.cu", "sti_attn_util.cuh"]}
+                  "topk_sparse_attn": ["decode_attn.cu", "sti_attn_util.cuh", "sti_kvfp4.h"]}
 
 
 def kernel_source_hash(kernel: str) -> str:
