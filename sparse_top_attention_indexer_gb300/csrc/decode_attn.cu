@@ -92,7 +92,7 @@ constexpr uint32_t kBlkBytes = kRows * 128;    // one column block of the tile (
 constexpr uint32_t kQBlkBytes = kH * 128;      // one column block of Q (64 heads x 128 B)
 constexpr uint32_t kTileBytes = 8 * kBlkBytes;
 constexpr uint32_t kQBytes = 8 * kQBlkBytes;
-constexpr uint32_t kPBytes = 2 * kQBlkBytes;   // P^T: 2 row blocks x 64 heads x 128 B
+constexpr uint32_t kPBytes = 2 * kQBlkBytes;   // P^T: 128 rows x 64 heads bf16 (128 B per row)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr uint32_t kBarMath = 1, kBarSet0 = 2;   // named barriers: the 256 math threads; each set of 128
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* tile = smem;                          // 8 column blocks x [128 rows x 128 B], SW128
     uint8_t* q_s = tile + kTileBytes;              // 8 column blocks x [64 heads x 128 B], SW128
-    uint8_t* p_s = q_s + kQBytes;                  // P^T: 2 row blocks x [64 heads x 128 B], SW128
+    uint8_t* p_s = q_s + kQBytes;                  // P^T: [128 rows][64 heads] bf16, SW128 (MN-major B)
     DaTail* tl = reinterpret_cast<DaTail*>(p_s + kPBytes);
     volatile int* abort = &tl->abort;
 
@@ -361,14 +361,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tl->m_run[32 * hb + lane] = v[0];
             }
             __syncwarp();
-            uint8_t* pb = p_s + kQBlkBytes;   // P^T row block 1 (rows 64..127); this lane's row 96 + lane
-            const int kr = kRingRow0 - 64 + lane;
+            const int rr = kRingRow0 + lane;   // this lane's tile row; P^T[rr][h], 16-byte chunk h/8 ^ rr % 8
+            uint8_t* prow = p_s + rr * 128;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float m = tl->m_run[i];
-                x[i] = (m == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
-                *reinterpret_cast<__nv_bfloat16*>(pb + i * 128 + (((kr >> 3) ^ (i & 7)) << 4) + (kr & 7) * 2) =
-                    __float2bfloat16_rn(x[i]);
+            for (int c = 0; c < 8; ++c) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float m = tl->m_run[8 * c + j];
+                    x[8 * c + j] = (m == -INFINITY) ? 0.f : fast_exp2(x[8 * c + j] - m);
+                }
+                uint4 pk;
+                pk.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
+                pk.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+                pk.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+                pk.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+                *reinterpret_cast<uint4*>(prow + ((c ^ (rr & 7)) << 4)) = pk;
             }
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
@@ -391,11 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_bf16_f32(kRows, kH, false, false);
-            const uint32_t idesc_pv = idesc_bf16_f32(128, kH, true, false);
+            const uint32_t idesc_pv = idesc_bf16_f32(128, kH, true, true);
             const uint64_t kd0 = sdesc(smem_u32(tile), 16, 1024, kLayoutSW128);          // K-major tile
             const uint64_t vd0 = sdesc(smem_u32(tile), kBlkBytes, 1024, kLayoutSW128);   // MN-major tile
             const uint64_t qd0 = sdesc(smem_u32(q_s), 16, 1024, kLayoutSW128);
-            const uint64_t pd0 = sdesc(smem_u32(p_s), 16, 1024, kLayoutSW128);
+            const uint64_t pd0 = sdesc(smem_u32(p_s), kPBytes, 1024, kLayoutSW128);   // MN-major P^T [row][head]
             // descriptors advance in 16-byte units: +2 per 32-byte K step of a K-major operand
             auto qk_block = [&](uint32_t s_col, int j) {
                 const uint64_t a = kd0 + (uint64_t)((uint32_t)j * (kBlkBytes >> 4));
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * m) * (kBlkBytes >> 4));
                     for (int kk = kk0; kk < 8; ++kk)
                         umma_bf16(tmem + kTmemO + (uint32_t)(m * kH), a + (uint64_t)(kk * (2048 >> 4)),
-                                  pd0 + (uint64_t)(((kk >> 2) * kQBlkBytes + (kk & 3) * 32) >> 4), idesc_pv,
+                                  pd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                                   (!first || kk > kk0) ? 1u : 0u);
                 }
             };
@@ -454,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int m = 0; m < 4; ++m) {
                         const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * m) * (kBlkBytes >> 4));
                         umma_bf16(tmem + kTmemO + (uint32_t)(m * kH), a + (uint64_t)(kk * (2048 >> 4)),
-                                  pd0 + (uint64_t)(((kk >> 2) * kQBlkBytes + (kk & 3) * 32) >> 4), idesc_pv, 1u);
+                                  pd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
                     }
             }
             for (int m = 0; m < 4; ++m) umma_commit(&tl->pv_bar[m]);
@@ -484,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         // online softmax over the compressed tile's S^T (t = 1; the sum of its two partial
-        // accumulators), continuing the ring slice's running max and sum.  The set's 32 heads go 8
-        // at a time through rolled loops (S re-read from TMEM in the second pass): each CTA runs
-        // this code once, so its size, not its issue count, decides how long it waits on
-        // instruction fetch.
+        // accumulators), continuing the ring slice's running max and sum.  Thread = row, the set's
+        // 32 heads in registers (one TMEM pass); lane l of every warp of the set resolves head
+        // hoff + l's new max and rescale factor itself (one barrier), P^T rows leave as 16-byte
+        // stores.
         auto softmax_tile = [&](int t, bool valid) {
             mwait(&tl->s_full[t], 0);
             if (t == 1 && mt == 0) STI_DSTAMP(11);
@@ -495,84 +502,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t == 1 && mt == 0 && !dead)   // the QK has read Q: its buffer may receive the merge shares
                 for (int c = 0; c < kCtas; ++c) mbar_arrive_remote_relaxed(dsmem_addr(&tl->qfree_bar, (uint32_t)c));
             const uint32_t s_col = tmem + lane_base + (uint32_t)(t * kH + hoff);
-            auto load8 = [&](int c, float (&x)[8]) {   // this row's S of heads hoff + 8c .. + 8, log2 units
-                uint32_t r[8], r2[8];
-                tmem_ld8(s_col + (uint32_t)(8 * c), r);
-                tmem_ld8(s_col + (kTmemS2 - (uint32_t)kH) + (uint32_t)(8 * c), r2);   // the second partial
+            float x[32];   // this row's S of heads hoff .. hoff + 31, log2 units
+            {
+                uint32_t r[32], r2[32];
+                tmem_ld32(s_col, r);
+                tmem_ld32(s_col + (kTmemS2 - (uint32_t)kH), r2);   // the second partial
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 32; ++i)
                     x[i] = (valid && !dead) ? (__uint_as_float(r[i]) + __uint_as_float(r2[i])) * p.scale_log2
                                             : -INFINITY;
-            };
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {   // per-head maxima over this warp's 32 rows
-                float x[8];
-                load8(c, x);
-                warp_reduce_scatter_n<8, true>(x);   // lanes 4j..4j+3 hold head 8c + j
-                if ((lane & 3) == 0) tl->red_max[qd][hoff + 8 * c + (lane >> 2)] = x[0];
+            }
+            {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = x[i];
+                warp_reduce_scatter_n<32, true>(v);   // lane l: head hoff + l over this warp's 32 rows
+                tl->red_max[qd][hoff + lane] = v[0];
             }
             if (t == 1 && mt == 0) STI_DSTAMP(21);
             named_bar_sync(bar_set, 128);
             if (t == 1 && mt == 0) STI_DSTAMP(22);
-            if (st < 32) {
-                const int hh = hoff + st;
-                const float mx = fmaxf(fmaxf(tl->red_max[0][hh], tl->red_max[1][hh]),
-                                       fmaxf(tl->red_max[2][hh], tl->red_max[3][hh]));
-                const float m_old = tl->m_run[hh];
-                // the running max moves only when a tile's max passes it by more than 8 (log2 units)
-                const float m_new = (m_old == -INFINITY || mx > m_old + 8.f) ? fmaxf(m_old, mx) : m_old;
-                tl->alpha[hh] = (m_new == -INFINITY) ? 1.f : fast_exp2(m_old - m_new);
-                tl->m_run[hh] = m_new;
-            }
-            named_bar_sync(bar_set, 128);
+            const int hl = hoff + lane;
+            const float mx = fmaxf(fmaxf(tl->red_max[0][hl], tl->red_max[1][hl]), fmaxf(tl->red_max[2][hl], tl->red_max[3][hl]));
+            const float m_old = tl->m_run[hl];
+            // the running max moves only when a tile's max passes it by more than 8 (log2 units)
+            const float m_new = (m_old == -INFINITY || mx > m_old + 8.f) ? fmaxf(m_old, mx) : m_old;
+            const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_old - m_new);
             // the ring slice's PV has read P^T and written O^T before the tile's P^T and rescale
             if (t == 1) mwait(&tl->o_done, 0);
             tc_fence_after();
-            uint8_t* pb = p_s + (row >> 6) * kQBlkBytes;   // P^T[h][row]: row block row/64, head h,
-            const int kr = row & 63;                       // 16-byte chunk ((row%64)/8) ^ (h%8)
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {   // probabilities (bf16 P^T) and per-head sums
-                float x[8];
-                load8(c, x);
+            uint8_t* prow = p_s + row * 128;   // P^T[row][h]: 16-byte chunk h/8, swizzled by row % 8
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int hi = hoff + 8 * c + i;
-                    const float m = tl->m_run[hi];
-                    x[i] = (m == -INFINITY) ? 0.f : fast_exp2(x[i] - m);
-                    *reinterpret_cast<__nv_bfloat16*>(pb + hi * 128 + (((kr >> 3) ^ (hi & 7)) << 4) + (kr & 7) * 2) =
-                        __float2bfloat16_rn(x[i]);
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float mh = __shfl_sync(kFull, m_new, 8 * c + j);
+                    x[8 * c + j] = (mh == -INFINITY) ? 0.f : fast_exp2(x[8 * c + j] - mh);
                 }
-                warp_reduce_scatter_n<8, false>(x);
-                if ((lane & 3) == 0) tl->red_sum[qd][hoff + 8 * c + (lane >> 2)] = x[0];
+                uint4 pk;
+                pk.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
+                pk.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+                pk.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
+                pk.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+                *reinterpret_cast<uint4*>(prow + (((4 * set + c) ^ (row & 7)) << 4)) = pk;
             }
+            warp_reduce_scatter_n<32, false>(x);   // lane l: the sum of head hoff + l over this warp's rows
+            tl->red_sum[qd][hl] = x[0];
             if (t == 1 && mt == 0) STI_DSTAMP(23);
-            if (t == 1) {
-                bool rescale = false;
-                for (int i = 0; i < 32; ++i) rescale = rescale || tl->alpha[hoff + i] != 1.f;
-                if (rescale && !dead) {   // O^T rows (lane = d within a block) times the heads' factors
+            if (t == 1 && !dead && __any_sync(kFull, alpha != 1.f)) {
+                // O^T rows (lane = d within a block) times the heads' factors
 #pragma unroll 1
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t ta = tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff);
-                        uint32_t r[32];
-                        tmem_ld32(ta, r);
-                        tmem_ld_wait();
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t ta = tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff);
+                    uint32_t r[32];
+                    tmem_ld32(ta, r);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * tl->alpha[hoff + i]);
-                        tmem_st32(ta, r);
-                    }
-                    tmem_st_wait();
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * __shfl_sync(kFull, alpha, i));
+                    tmem_st32(ta, r);
                 }
+                tmem_st_wait();
             }
             if (t == 1 && mt == 0) STI_DSTAMP(24);
             fence_proxy_async_smem();   // P^T: generic writes read by the MMA
             tc_fence_before();
             named_bar_sync(bar_set, 128);
-            if (st < 32) {
-                const int hh = hoff + st;
-                tl->l_run[hh] = tl->l_run[hh] * tl->alpha[hh] + (tl->red_sum[0][hh] + tl->red_sum[1][hh]) +
-                                (tl->red_sum[2][hh] + tl->red_sum[3][hh]);
+            if (st < 32) {   // warps 2 and 6: lane st holds head hoff + st
+                tl->m_run[hl] = m_new;
+                tl->alpha[hl] = alpha;
+                tl->l_run[hl] = tl->l_run[hl] * alpha + (tl->red_sum[0][hl] + tl->red_sum[1][hl]) +
+                                (tl->red_sum[2][hl] + tl->red_sum[3][hl]);
             }
             if (st == 0) mbar_arrive(&tl->p_full);
         };
