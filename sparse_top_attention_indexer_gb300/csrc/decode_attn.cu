@@ -454,17 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             STI_DSTAMP(50);
             ok = ok && attn_wait(&tl->p_full, 1, p.status, abort);
             STI_DSTAMP(20);
-            if (ok) {   // K step by K step over the four d-blocks' independent accumulators
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk)
+            if (ok) tc_fence_after();
+            // d-block by d-block, the blocks the other CTAs own first (their shares leave as soon as
+            // each is done), this CTA's own block last
+            for (int j = 1; j <= kCtas; ++j) {
+                const int m = (rank + j) & 3;
+                if (ok) {
+                    const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * m) * (kBlkBytes >> 4));
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint64_t a = vd0 + (uint64_t)((uint32_t)(2 * m) * (kBlkBytes >> 4));
+                    for (int kk = 0; kk < 8; ++kk)
                         umma_bf16(tmem + kTmemO + (uint32_t)(m * kH), a + (uint64_t)(kk * (2048 >> 4)),
                                   pd0 + (uint64_t)(kk * (2048 >> 4)), idesc_pv, 1u);
-                    }
+                }
+                umma_commit(&tl->pv_bar[m]);
             }
-            for (int m = 0; m < 4; ++m) umma_commit(&tl->pv_bar[m]);
             STI_DSTAMP(45);
         }
         __syncwarp();
@@ -993,14 +996,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (mt == 0) STI_DSTAMP(12);
 
         // ---- merge in shared memory.  Each CTA sends its (max, sum) per head to the other three as
-        // soon as its softmax is done and, while its PV runs, computes every CTA's weight per head,
-        // 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)).  Once its PV is complete it stages
-        // the three d-blocks of its O^T that the others own times its own weight -- its share of the
-        // output -- as [128 d][64 heads] bf16 in its tile, the eight 16-byte chunks of a d row
-        // XOR-swizzled by d, and copies each into its owner's Q buffer, free since the owner's QK
-        // (bulk shared-to-shared copies counted on the owner's recv_bar; slot k, bytes
-        // [16K k, 16K k + 16K), comes from CTA k + (k >= owner)).  The owner adds the three shares to
-        // its own block times its own weight.
+        // soon as its softmax is done.  Its PV runs d-block by d-block, the three blocks the others own
+        // first: as each completes, the block of its O^T is staged as [128 d][64 heads] bf16 (the
+        // eight 16-byte chunks of a d row XOR-swizzled by d) and copied into its owner's Q buffer,
+        // free since the owner's QK (bulk shared-to-shared copies counted on the owner's recv_bar;
+        // slot k, bytes [16K k, 16K k + 16K), comes from CTA k + (k >= owner)).  Meanwhile each CTA
+        // computes every CTA's weight per head, 2^(m_c - M) / (sum_c l_c 2^(m_c - M) + 2^(sink - M)),
+        // and the owner adds the three shares times their senders' weights to its own block times
+        // its own.
         const int d_loc = row;   // TMEM lane = d within a block
         if (st < 32 && !dead) {
             const int hh = hoff + st;
@@ -1014,10 +1017,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         constexpr uint32_t kPartBytes = kRows * kH * 2;   // one d-block's share: [128 d][64 heads] bf16
-        auto out_stage = [&](int j) -> uint8_t* {   // staging of the block for CTA (rank + j) % 4
-            return tile + (size_t)(j - 1) * kPartBytes;
-        };
-        // the weights, while the PV runs
+        // the share of d-block m is staged over the first of its own two column blocks of the tile: the
+        // PV of block m has read them, and the later PVs read only their own blocks
+        auto out_stage = [&](int m) -> uint8_t* { return tile + (size_t)(2 * m) * kBlkBytes; };
+        // every Q buffer is free (each CTA's compressed QK has read its Q)
+        if (!dead) dead = !attn_wait_cluster(&tl->qfree_bar, 0, p.status, abort);
+        dead = __any_sync(kFull, dead);
+        if (mt == 0) STI_DSTAMP(14);
+        // the others' d-blocks, each as soon as its PV is done: staged as bf16 (unweighted; the owner
+        // applies this CTA's weight) in the tile the PV has finished reading, and copied to the owner
+        const uint32_t swz = (uint32_t)(d_loc & 7);
+#pragma unroll 1
+        for (int j = 1; j < kCtas; ++j) {
+            const int m = (j + rank) & 3;
+            mwait(&tl->pv_bar[m], 0);
+            if (mt == 0) STI_DSTAMP(45 + j);
+            tc_fence_after();
+            if (!dead) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
+                tmem_ld_wait();
+                uint8_t* dst = out_stage(m) + (size_t)d_loc * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(__uint_as_float(r[8 * c + 0]), __uint_as_float(r[8 * c + 1]));
+                    pk.y = pack_bf16x2(__uint_as_float(r[8 * c + 2]), __uint_as_float(r[8 * c + 3]));
+                    pk.z = pack_bf16x2(__uint_as_float(r[8 * c + 4]), __uint_as_float(r[8 * c + 5]));
+                    pk.w = pack_bf16x2(__uint_as_float(r[8 * c + 6]), __uint_as_float(r[8 * c + 7]));
+                    *reinterpret_cast<uint4*>(dst + ((((uint32_t)(4 * set + c)) ^ swz) << 4)) = pk;
+                }
+            }
+            fence_proxy_async_smem();   // generic writes, read by the bulk copy
+            named_bar_sync(kBarMath, 256);
+            if (mt == 0 && !dead) {
+                const int slot = rank < m ? rank : rank - 1;
+                bulk_copy_to_peer(dsmem_addr(q_s, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(m),
+                                  kPartBytes, dsmem_addr(&tl->recv_bar, (uint32_t)m));
+            }
+        }
+        if (mt == 0) STI_DSTAMP(25);
+        // the weights, while the own block's PV runs
         mwait_c(&tl->ml_bar);
         if (st < 32) {   // the four CTAs' weights for head hoff + st (whose max and sum this thread wrote)
             const int hh = hoff + st;
@@ -1043,53 +1083,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(kBarMath, 256);   // the weights
         if (mt == 0) STI_DSTAMP(26);
-#pragma unroll 1
-        for (int j = 1; j <= kCtas; ++j) {   // this CTA's PV, all four blocks
-            mwait(&tl->pv_bar[(j + rank) & 3], 0);
-            if (mt == 0) STI_DSTAMP(45 + j);
-        }
+        mwait(&tl->pv_bar[rank], 0);   // this CTA's own block
+        if (mt == 0) STI_DSTAMP(49);
         tc_fence_after();
         if (mt == 0) STI_DSTAMP(13);
-        // the others' d-blocks times this CTA's weight (so each is this CTA's share of the output,
-        // no larger than the largest |v|), staged as bf16 in the tile the PV has finished reading
-        const uint32_t swz = (uint32_t)(d_loc & 7);
-        const float* w_own = tl->wgt[kCtas - 1] + hoff;
-#pragma unroll 1
-        for (int j = 1; j < kCtas && !dead; ++j) {
-            const int m = (j + rank) & 3;
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(m * kH + hoff), r);
-            tmem_ld_wait();
-            uint8_t* dst = out_stage(j) + (size_t)d_loc * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int h0 = 8 * c + 2 * i;
-                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[h0]) * w_own[h0],
-                                                                    __uint_as_float(r[h0 + 1]) * w_own[h0 + 1]);
-                    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
-                }
-                *reinterpret_cast<uint4*>(dst + ((((uint32_t)(4 * set + c)) ^ swz) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-        }
-        fence_proxy_async_smem();   // generic writes, read by the bulk copies
-        named_bar_sync(kBarMath, 256);
-        if (!dead) dead = !attn_wait_cluster(&tl->qfree_bar, 0, p.status, abort);   // every Q buffer free
-        dead = __any_sync(kFull, dead);
-        if (mt == 0) STI_DSTAMP(14);
-        if (mt < kCtas - 1 && !dead) {   // thread j - 1 copies the block of CTA (rank + j) % 4
-            const int j = mt + 1;
-            const int m = (j + rank) & 3;
-            const int slot = rank < m ? rank : rank - 1;
-            bulk_copy_to_peer(dsmem_addr(q_s, (uint32_t)m) + (uint32_t)slot * kPartBytes, out_stage(j), kPartBytes,
-                              dsmem_addr(&tl->recv_bar, (uint32_t)m));
-        }
-        if (mt == 0) STI_DSTAMP(25);
         float v[32];
         {
+            const float* w_own = tl->wgt[kCtas - 1] + hoff;
             uint32_t r[32];
             tmem_ld32(tmem + lane_base + kTmemO + (uint32_t)(rank * kH + hoff), r);
             tmem_ld_wait();
@@ -1099,8 +1099,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mwait_c(&tl->recv_bar);
         if (mt == 0) STI_DSTAMP(51);
 #pragma unroll 1
-        for (int k = 0; k < kCtas - 1; ++k) {   // the three others' shares of this CTA's d-block
+        for (int k = 0; k < kCtas - 1; ++k) {   // the three others' shares of this CTA's d-block, weighted
             const uint8_t* part = q_s + (size_t)k * kPartBytes + (size_t)d_loc * 128;
+            const float* wk = tl->wgt[k] + hoff;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint4 x = dead ? make_uint4(0, 0, 0, 0)
@@ -1109,17 +1110,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[i]));
-                    v[8 * c + 2 * i] += f.x;
-                    v[8 * c + 2 * i + 1] += f.y;
+                    v[8 * c + 2 * i] += f.x * wk[8 * c + 2 * i];
+                    v[8 * c + 2 * i + 1] += f.y * wk[8 * c + 2 * i + 1];
                 }
             }
         }
         const int dd = kRows * rank + d_loc;
         if (p.rope_dims > 0 && kRows * rank + kRows > kD - p.rope_dims)   // the output's inverse rotation
             rope_inverse_pairs<32>(v, dd, kD, p.rope_dims, p.rope_cs + (size_t)b * p.rope_dims);
-        uint16_t* orow = p.out + ((size_t)b * kH + hoff) * kD + dd;   // lanes: consecutive d of a head
+        {   // the block's [64 heads][128 d] bf16: each warp turns its 32 d x 32 heads around in 2 KB of the
+            // free quarter of the Q buffer and stores 16-byte pieces (a head's 32 d: 64 contiguous bytes)
+            uint16_t* stg = reinterpret_cast<uint16_t*>(q_s + 3 * kPartBytes) + mw * 32 * 32;
+            const bool odd = (lane & 1) != 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) orow[(size_t)i * kD] = __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+            for (int i = 0; i < 32; i += 2) {   // lane pairs: the even lane head i, the odd lane head i + 1
+                const float send = odd ? v[i] : v[i + 1];
+                const float recv = __shfl_xor_sync(kFull, send, 1);
+                const uint32_t pr = odd ? pack_bf16x2(recv, v[i + 1]) : pack_bf16x2(v[i], recv);
+                *reinterpret_cast<uint32_t*>(stg + (i + (odd ? 1 : 0)) * 32 + (lane & ~1)) = pr;
+            }
+            __syncwarp();
+            uint16_t* obase = p.out + (size_t)b * kH * kD + kRows * rank + 32 * qd;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {   // piece c: head hoff + c / 4, d 8 (c % 4) .. + 8 of this warp's 32
+                const int c = lane + 32 * k;
+                const uint4 val = *reinterpret_cast<const uint4*>(stg + c * 8);
+                *reinterpret_cast<uint4*>(obase + (size_t)(hoff + (c >> 2)) * kD + 8 * (c & 3)) = val;
+            }
+        }
         if (mt == 0) {
             STI_DSTAMP(15);
             STI_DCLOCK(31);
