@@ -338,10 +338,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 if (sid == 1) {   // 64 elements: eight words of eight codes, an E4M3 scale per two words
                     const uint32_t w[8] = {cw[m][0].x, cw[m][0].y, cw[m][0].z, cw[m][0].w,
                                            cw[m][1].x, cw[m][1].y, cw[m][1].z, cw[m][1].w};
+                    const float2 s01 = e4m3x2_to_float2(sw[m] & 0xFFFFu), s23 = e4m3x2_to_float2(sw[m] >> 16);
+                    const __nv_bfloat162 sc[4] = {__float2bfloat162_rn(s01.x), __float2bfloat162_rn(s01.y),
+                                                  __float2bfloat162_rn(s23.x), __float2bfloat162_rn(s23.y)};
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(dst + ((c ^ (fr & 7)) << 4)) =
-                            kvfp4_decode8(w[c], e4m3_to_float((sw[m] >> (8 * (c >> 1))) & 0xFFu));
+                        *reinterpret_cast<uint4*>(dst + ((c ^ (fr & 7)) << 4)) = kvfp4_decode8_s2(w[c], sc[c >> 1]);
                 } else {          // masked: zeros (finite, and P = 0 for them)
 #pragma unroll
                     for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(dst + (c << 4)) = make_uint4(0, 0, 0, 0);

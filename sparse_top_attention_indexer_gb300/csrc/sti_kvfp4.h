@@ -24,29 +24,41 @@ struct KvFp4 {
 };
 
 #ifdef __CUDACC__
-// E4M3 byte (sign, 4-bit exponent with bias 7, 3-bit mantissa; exponent 0 subnormal: m * 2^-9;
-// S.1111.111 NaN) -> float.
-__device__ __forceinline__ float e4m3_to_float(uint32_t v) {
-    const uint32_t e = (v >> 3) & 15u, m = v & 7u, sg = (v & 0x80u) << 24;
-    if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
-    return e == 0u ? __uint_as_float(sg | __float_as_uint((float)m * 0.001953125f))
-                   : __uint_as_float(sg | ((e + 120u) << 23) | (m << 20));
+// Two E4M3 bytes (bits 0-7 and 8-15 of `two`; sign, 4-bit exponent with bias 7, 3-bit mantissa;
+// exponent 0 subnormal: m * 2^-9; S.1111.111 NaN) -> two floats, by the hardware's E4M3 -> f16
+// conversion and f16 -> f32: every E4M3 value, subnormals and NaN included, is an f16 value, so
+// both steps are exact.  No branches.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 t, a, b;\n\t.reg .b32 h;\n\t"
+        "cvt.u16.u32 t, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, t;\n\t"
+        "mov.b32 {a, b}, h;\n\t"
+        "cvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(two));
+    return make_float2(lo, hi);
 }
+// One E4M3 byte (bits 0-7 of v) -> float.
+__device__ __forceinline__ float e4m3_to_float(uint32_t v) { return e4m3x2_to_float2(v & 0xFFu).x; }
 
 // Eight fp4 elements (nibble i of cw = element i) times their E4M3 scale s as eight bf16 (one
 // 16-byte chunk of the tile): the E2M1 values by byte-permute lookup (e2m1x8_to_bf16), then four
 // bf16x2 products with the scale.  Every factor is exact in bf16 and a product of an E2M1 value
 // and an E4M3 value has at most six significant bits, so each product is exact.
-__device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
+__device__ __forceinline__ uint4 kvfp4_decode8_s2(uint32_t cw, __nv_bfloat162 s2) {   // s2 = (s, s)
     uint32_t o[4];
     e2m1x8_to_bf16(cw, 0u, o);
-    const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&o[j]), s2);
         o[j] = *reinterpret_cast<const uint32_t*>(&v);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ uint4 kvfp4_decode8(uint32_t cw, float s) {
+    return kvfp4_decode8_s2(cw, __float2bfloat162_rn(s));
 }
 
 #endif
