@@ -357,6 +357,38 @@ def test_sparse_attn_streamed_prefill(sti, orc):
     assert torch.equal(out, out2)
 
 
+@pytest.mark.parametrize("b,s,h,k,n1,n2", [
+    (1, 300, 1, 4096, 100, 6000),   # one head, the longest index row (32 tiles)
+    (2, 170, 64, 129, 60, 300),     # a last tile of one slot
+])
+def test_sparse_attn_streamed_limits(sti, orc, b, s, h, k, n1, n2):
+    """The streamed kernel at the ends of its range: 1 head (Q boxes one row high, 63 padded
+    heads) with 32 tiles per query, and a last tile holding a single slot."""
+    import torch
+
+    rng = rng_for(795 + h, k)
+    d = 512
+    q = to_bf16_bits(rng.standard_normal((b, s, h, d)))
+    kv1 = to_bf16_bits(rng.standard_normal((b, n1, d)))
+    kv2 = to_bf16_bits(rng.standard_normal((b, n2, d)))
+    sink = rng.standard_normal(h).astype(np.float32)
+    idx = index_lists(rng, b, s, k, n1 + n2, masked_frac=0.2, empty_rows=1)
+    ref, ref_lse = orc.sparse_attn(q, kv1, sink, idx, d ** -0.5, kv2=kv2)
+    lse = torch.empty(b, s, h, dtype=torch.float32, device="cuda")
+    ws = sti.workspace(256)
+    out = sti.sparse_attn_sink(to_dev(q), to_dev(kv1), to_dev_any(sink), to_dev_any(idx), d ** -0.5,
+                               kv2=to_dev(kv2), lse=lse, ws=ws)
+    torch.cuda.synchronize()
+    assert sti.read_device_status(ws) == 0
+    got = bf16_out_to_f64(out)
+    check_attn(got, ref)
+    assert np.all(got[np.all(idx < 0, axis=-1)] == 0)
+    fin = np.isfinite(ref_lse)
+    lg = lse.cpu().numpy().astype(np.float64)
+    assert np.array_equal(np.isfinite(lg), fin)
+    np.testing.assert_allclose(lg[fin], ref_lse[fin], rtol=1e-4, atol=1e-4)
+
+
 def test_sparse_attn_whole_tiles_masked(sti, orc):
     """Decode-style rows where whole 128-slot tiles are -1 (short sequences), split over CTAs."""
     rng = rng_for(720, 0)
