@@ -7,19 +7,20 @@
 //     s_i = softmax_scale * q . kv[idx_i];  o = sum_i e^{s_i} kv[idx_i] / (sum_i e^{s_i} + e^{sink_h})
 //   one latent row serving as key and value; a query with no valid slot gets 0.
 //
-// Shape: up to 64 heads x 512 dims, rows from one or two bf16 sources.  One CTA per SM, 320
-// threads:
+// Shape: up to 64 heads x 512 dims, rows from one or two bf16 sources, or (FP4) the second source
+// as fp4 rows (E2M1 codes, an E4M3 scale per 16).  One CTA per SM, 320 threads:
 //   * warp 0 loads each query's Q (eight TMA boxes of h heads x 64 dims) as soon as the previous
 //     query's last QK has read the buffer;
 //   * warp 1 issues the MMAs;
 //   * warps 2..9 gather the tiles, run the online softmax and write the outputs.
-// A query's index slots form tiles of 128 rows; tiles with no valid slot are skipped.  Each lane
-// of the math warps copies one four-row group of one column block (64 dims) of a tile with a
-// four-row TMA gather; every warp holds four row groups of every column block, so when the
-// previous tile's PV releases a pair of blocks (one d-block) all eight warps re-fill it at once.
-// The QK consumes column block j as soon as it has landed, so a tile's gather overlaps the
-// previous tile's PV and its own QK.  The index slots of the next tile are loaded while the
-// current tile's rows land.
+// A query's index slots form tiles of 128 rows; tiles with no valid slot are skipped.  A tile is
+// refilled one pair of column blocks (one d-block, 128 dims) at a time, as soon as the previous
+// tile's PV of that d-block has released it: bf16 rows 0..63 by four-row TMA gathers (four lanes
+// of every math warp), rows 64..127 by 16-byte LSU copies of every math thread, so the TMA unit
+// and the LSU work side by side; fp4 rows are loaded into registers as soon as their index is
+// known and decoded into the tile once their block is free.  The QK consumes column block j as
+// soon as it has landed, so a tile's gather overlaps the previous tile's PV and its own QK.  The
+// index slots of the next tile are loaded while the current tile's rows land.
 //   * S^T = KV . Q^T: M = 128 rows, N = 64 heads, K = 512, the K steps alternating between two
 //     TMEM accumulators so that consecutive MMAs do not wait on each other (the softmax adds
 //     the two).
