@@ -272,6 +272,125 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
 }
 
 // ---------------------------------------------------------------------------------------------
+// Warp top-k for rows of at most 2048 columns (prefill): one warp per row, its 64 keys a lane in
+// registers (lane l holds positions 32 i + l), four radix passes of 8 bits over a 256-bin
+// histogram in the warp's own shared memory, then the ordered compaction by ballots -- no block
+// barrier anywhere, so the many short rows of a prefill are not bound by block-wide
+// synchronisation.
+
+constexpr int kWarpRowCap = 2048;             // visible positions a warp holds (64 a lane)
+constexpr int kWtThreads = 512;               // 16 rows per CTA
+constexpr int kWtRows = kWtThreads / 32;
+
+// The digit d of a 256-bin histogram where the count of keys from the top first reaches
+// `remaining` (1 <= remaining <= total), and in *above the keys in higher bins.  Lane l holds
+// bins [8 l, 8 l + 8); the same d and *above come back in every lane.
+__device__ __forceinline__ int warp_select256(const uint32_t* hist, int remaining, int lane, int* above_out) {
+    uint32_t c[8];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        c[i] = hist[8 * lane + i];
+        local += (int)c[i];
+    }
+    int inc = local;   // suffix sum: this lane's bins and every higher lane's
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_down_sync(kFull, inc, o);
+        if (lane + o < 32) inc += x;
+    }
+    int above = inc - local, d = -1, ab = 0;
+#pragma unroll
+    for (int i = 7; i >= 0; --i) {
+        if (above < remaining && above + (int)c[i] >= remaining) {
+            d = 8 * lane + i;
+            ab = above;
+        }
+        above += (int)c[i];
+    }
+    const unsigned m = __ballot_sync(kFull, d >= 0);
+    const int from = m ? __ffs(m) - 1 : 0;
+    *above_out = __shfl_sync(kFull, ab, from);
+    return __shfl_sync(kFull, d, from);
+}
+
+template <bool HAS_WIN>
+__global__ void __launch_bounds__(kWtThreads) topk_warp_kernel(const TopkParams p) {
+    __shared__ uint32_t hist_s[kWtRows][256];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int row = blockIdx.x * kWtRows + wib;
+    griddep_launch_dependents();
+    if (row >= p.B * p.s) return;
+    const int b = row / p.s, t = row - b * p.s;
+    const int sp = __ldg(p.start_pos + b);
+    if (HAS_WIN) {
+        int32_t* wrow = p.win_out + (int64_t)row * p.row_stride;
+        for (int i = lane; i < p.win_width; i += 32) wrow[i] = window_slot(p.s, t, sp, p.win_W, i);
+        if (lane == 0 && p.s > 1 && sp != 0 && p.status) atomicOr(p.status, 4u /* STI_FLAG_CHUNKED */);
+    }
+    griddep_wait();   // the scores are complete from here on
+    int vis = (sp + t + 1) / p.ratio;
+    vis = max(0, min(vis, p.n_cols));
+    int32_t* out = p.idxs + (int64_t)row * p.row_stride;
+    if (vis <= p.k) {   // every visible position is selected
+        for (int i = lane; i < p.k; i += 32) out[i] = i < vis ? i + p.offset : -1;
+        return;
+    }
+    const float* src = p.scores + (int64_t)row * p.n_cols;
+    uint32_t key[kWarpRowCap / 32];
+#pragma unroll
+    for (int i = 0; i < kWarpRowCap / 32; ++i) {
+        const int j = 32 * i + lane;
+        key[i] = j < vis ? float_key(__ldg(src + j)) : 0u;
+    }
+    // four passes of 8 bits: the exact key tau of the k-th largest visible score
+    uint32_t* h = hist_s[wib];
+    uint32_t prefix = 0u;
+    int remaining = p.k;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[8 * lane + i] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kWarpRowCap / 32; ++i) {
+            const int j = 32 * i + lane;
+            const bool m = j < vis && (pass == 0 || (key[i] >> (shift + 8)) == prefix);
+            if (__ballot_sync(kFull, m) == 0u) continue;   // no key of this slot matches the prefix
+            const uint32_t dig = m ? (key[i] >> shift) & 255u : 0xFFFFFFFFu;
+            const unsigned peers = __match_any_sync(kFull, dig);
+            if (m && lane == __ffs(peers) - 1) atomicAdd(&h[dig], (uint32_t)__popc(peers));
+        }
+        __syncwarp();
+        int above;
+        const int d = warp_select256(h, remaining, lane, &above);
+        remaining -= above;
+        prefix = (prefix << 8) | (uint32_t)d;
+        __syncwarp();   // every lane has read the histogram before the next pass clears it
+    }
+    const uint32_t tau = prefix;
+    const int need_eq = remaining;   // >= 1 keys equal to tau are taken, lowest positions first
+    // ordered compaction: keys above tau, and the first need_eq keys equal to tau, by position
+    const unsigned below = (1u << lane) - 1u;
+    int pos = 0, eq_seen = 0;
+#pragma unroll
+    for (int i = 0; i < kWarpRowCap / 32; ++i) {
+        const int j = 32 * i + lane;
+        const bool v = j < vis;
+        const bool gt = v && key[i] > tau, eq = v && key[i] == tau;
+        const unsigned em = __ballot_sync(kFull, eq);
+        const bool take = gt || (eq && eq_seen + __popc(em & below) < need_eq);
+        const unsigned tm = __ballot_sync(kFull, take);
+        const int at = pos + __popc(tm & below);
+        if (take && at < p.k) out[at] = j + p.offset;
+        pos += __popc(tm);
+        eq_seen += __popc(em);
+    }
+    // vis > k here, so exactly k entries were written
+}
+
+// ---------------------------------------------------------------------------------------------
 // Cluster top-k for few long rows (decode): the CR CTAs of a cluster split one row into
 // contiguous chunks.  The first radix pass comes precomputed from the scores kernel, so every
 // CTA knows the threshold bin d1 without talking; rank 0 collects the bin's members (a few
@@ -777,6 +896,21 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = p.pdl ? 2 : 1;
         err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<CR>, p, chunk_cap);
+        return err != cudaSuccess ? err : cudaGetLastError();
+    }
+    if (p.hist == nullptr && p.n_cols <= kWarpRowCap) {
+        // short rows without a precomputed first pass (prefill): one warp per row
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((rows + kWtRows - 1) / kWtRows));
+        cfg.blockDim = dim3(kWtThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.pdl ? 1 : 0;
+        const cudaError_t err = p.win_out != nullptr ? cudaLaunchKernelEx(&cfg, topk_warp_kernel<true>, p)
+                                                     : cudaLaunchKernelEx(&cfg, topk_warp_kernel<false>, p);
         return err != cudaSuccess ? err : cudaGetLastError();
     }
     const int use_smem = p.n_cols <= kSmemKeyCap ? 1 : 0;

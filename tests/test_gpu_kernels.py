@@ -180,6 +180,20 @@ def test_topk_exact(sti, orc, b, s, n_cols, k, sps, ratio):
     np.testing.assert_array_equal(got, ref)
 
 
+@pytest.mark.parametrize("levels", [3, 40])
+def test_topk_many_ties(sti, orc, levels):
+    """Prefill rows (one warp a row) whose scores take only a few values: the k-th largest key is
+    shared by many positions, so the lower-position rule decides most of the set."""
+    rng = rng_for(602, levels)
+    b, s, n_cols, k = 2, 96, 2048, 512
+    scores = rng.integers(0, levels, size=(b, s, n_cols)).astype(np.float32) * 0.25 - 1.0
+    scores[0, 5, :] = 0.5                              # one row all equal
+    sp = np.array([0, 0], np.int32)
+    ref = orc.topk(scores.astype(np.float64), sp, 1, k, 7)
+    got = sti.idx_topk(to_dev_any(scores), to_dev_any(sp), 1, k, 7).cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
 def test_topk_writes_into_wider_rows(sti, orc):
     import torch
 
