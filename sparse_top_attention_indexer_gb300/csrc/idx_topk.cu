@@ -273,26 +273,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const TopkParams p, 
 
 // ---------------------------------------------------------------------------------------------
 // Warp top-k for rows of at most 2048 columns (prefill): one warp per row, its 64 keys a lane in
-// registers (lane l holds positions 32 i + l), four radix passes of 8 bits over a 256-bin
-// histogram in the warp's own shared memory, then the ordered compaction by ballots -- no block
-// barrier anywhere, so the many short rows of a prefill are not bound by block-wide
-// synchronisation.
+// registers (lane l holds positions 32 i + l), a first radix pass over the top 11 bits into the
+// warp's own 2048-bin histogram, the threshold bin's keys listed and three passes of 7 bits over
+// them, then the ordered compaction by ballots -- no block barrier anywhere, so the many short
+// rows of a prefill are not bound by block-wide synchronisation.
 
 constexpr int kWarpRowCap = 2048;             // visible positions a warp holds (64 a lane)
 constexpr int kWtThreads = 512;               // 16 rows per CTA
 constexpr int kWtRows = kWtThreads / 32;
+constexpr int kWtCandCap = 512;               // keys of the first pass's threshold bin listed per row
 
-// The digit d of a 256-bin histogram where the count of keys from the top first reaches
+// The digit d of a 128-bin histogram where the count of keys from the top first reaches
 // `remaining` (1 <= remaining <= total), and in *above the keys in higher bins.  Lane l holds
-// bins [8 l, 8 l + 8); the same d and *above come back in every lane.
-__device__ __forceinline__ int warp_select256(const uint32_t* hist, int remaining, int lane, int* above_out) {
-    uint32_t c[8];
-    int local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        c[i] = hist[8 * lane + i];
-        local += (int)c[i];
-    }
+// bins [4 l, 4 l + 4); the same d and *above come back in every lane.
+__device__ __forceinline__ int warp_select128(const uint32_t* hist, int remaining, int lane, int* above_out) {
+    const uint4 c4 = reinterpret_cast<const uint4*>(hist)[lane];
+    const int c[4] = {(int)c4.x, (int)c4.y, (int)c4.z, (int)c4.w};
+    const int local = c[0] + c[1] + c[2] + c[3];
     int inc = local;   // suffix sum: this lane's bins and every higher lane's
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -301,12 +298,12 @@ __device__ __forceinline__ int warp_select256(const uint32_t* hist, int remainin
     }
     int above = inc - local, d = -1, ab = 0;
 #pragma unroll
-    for (int i = 7; i >= 0; --i) {
-        if (above < remaining && above + (int)c[i] >= remaining) {
-            d = 8 * lane + i;
+    for (int i = 3; i >= 0; --i) {
+        if (above < remaining && above + c[i] >= remaining) {
+            d = 4 * lane + i;
             ab = above;
         }
-        above += (int)c[i];
+        above += c[i];
     }
     const unsigned m = __ballot_sync(kFull, d >= 0);
     const int from = m ? __ffs(m) - 1 : 0;
@@ -316,7 +313,9 @@ __device__ __forceinline__ int warp_select256(const uint32_t* hist, int remainin
 
 template <bool HAS_WIN>
 __global__ void __launch_bounds__(kWtThreads) topk_warp_kernel(const TopkParams p) {
-    __shared__ uint32_t hist_s[kWtRows][256];
+    extern __shared__ __align__(16) uint32_t wt_smem[];
+    uint32_t (*hist_s)[kBins] = reinterpret_cast<uint32_t (*)[kBins]>(wt_smem);                  // per warp
+    uint32_t (*cand_s)[kWtCandCap] = reinterpret_cast<uint32_t (*)[kWtCandCap]>(wt_smem + kWtRows * kBins);
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int row = blockIdx.x * kWtRows + wib;
     griddep_launch_dependents();
@@ -343,31 +342,119 @@ __global__ void __launch_bounds__(kWtThreads) topk_warp_kernel(const TopkParams 
         const int j = 32 * i + lane;
         key[i] = j < vis ? float_key(__ldg(src + j)) : 0u;
     }
-    // four passes of 8 bits: the exact key tau of the k-th largest visible score
+    // pass 1 over the top 11 bits (a float key's sign, exponent and two mantissa bits) into the
+    // warp's 2048-bin histogram, lane l owning bins [64 l, 64 l + 64) for the selection
     uint32_t* h = hist_s[wib];
+    uint32_t* cand = cand_s[wib];
     uint32_t prefix = 0u;
     int remaining = p.k;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
+    {
+        uint4* h4 = reinterpret_cast<uint4*>(h);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h[8 * lane + i] = 0u;
+        for (int i = 0; i < 16; ++i) h4[32 * i + lane] = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kWarpRowCap / 32; ++i)
+            if (32 * i + lane < vis) atomicAdd(&h[key[i] >> 21], 1u);
+        __syncwarp();
+        // the threshold bin: suffix sums of the lanes' 64-bin totals, then a walk down one lane's bins
+        int local = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint4 c = h4[16 * lane + i];
+            local += (int)(c.x + c.y + c.z + c.w);
+        }
+        int inc = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_down_sync(kFull, inc, o);
+            if (lane + o < 32) inc += x;
+        }
+        int above = inc - local, d = -1, ab = 0;
+        if (above < remaining && inc >= remaining) {
+            for (int bin = 64 * lane + 63; bin >= 64 * lane; --bin) {
+                const int c = (int)h[bin];
+                if (above + c >= remaining) {
+                    d = bin;
+                    ab = above;
+                    break;
+                }
+                above += c;
+            }
+        }
+        const unsigned m = __ballot_sync(kFull, d >= 0);
+        const int from = m ? __ffs(m) - 1 : 0;
+        d = __shfl_sync(kFull, d, from);
+        ab = __shfl_sync(kFull, ab, from);
+        remaining -= ab;
+        prefix = (uint32_t)d;
+    }
+    // the bin's keys, listed (ascending position; up to kWtCandCap of them)
+    const int c1 = (int)h[prefix];
+    if (c1 <= kWtCandCap) {
+        int n = 0;
 #pragma unroll
         for (int i = 0; i < kWarpRowCap / 32; ++i) {
-            const int j = 32 * i + lane;
-            const bool m = j < vis && (pass == 0 || (key[i] >> (shift + 8)) == prefix);
-            if (__ballot_sync(kFull, m) == 0u) continue;   // no key of this slot matches the prefix
-            const uint32_t dig = m ? (key[i] >> shift) & 255u : 0xFFFFFFFFu;
-            const unsigned peers = __match_any_sync(kFull, dig);
-            if (m && lane == __ffs(peers) - 1) atomicAdd(&h[dig], (uint32_t)__popc(peers));
+            const bool mm = 32 * i + lane < vis && (key[i] >> 21) == prefix;
+            const unsigned bal = __ballot_sync(kFull, mm);
+            if (mm) cand[n + __popc(bal & ((1u << lane) - 1u))] = key[i];
+            n += __popc(bal);
         }
         __syncwarp();
-        int above;
-        const int d = warp_select256(h, remaining, lane, &above);
-        remaining -= above;
-        prefix = (prefix << 8) | (uint32_t)d;
-        __syncwarp();   // every lane has read the histogram before the next pass clears it
+        // passes 2..4 over the listed keys: 7 bits each into a 128-bin histogram (four bins a lane)
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = 14 - 7 * pass;
+            reinterpret_cast<uint4*>(h)[lane] = make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+            for (int j = lane; j < c1; j += 32) {
+                const uint32_t kj = cand[j];
+                if ((kj >> (shift + 7)) == prefix) atomicAdd(&h[(kj >> shift) & 127u], 1u);
+            }
+            __syncwarp();
+            const uint4 c = reinterpret_cast<const uint4*>(h)[lane];
+            const int cs[4] = {(int)c.x, (int)c.y, (int)c.z, (int)c.w};
+            const int local = cs[0] + cs[1] + cs[2] + cs[3];
+            int inc = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_down_sync(kFull, inc, o);
+                if (lane + o < 32) inc += x;
+            }
+            int above = inc - local, d = -1, ab = 0;
+#pragma unroll
+            for (int i = 3; i >= 0; --i) {
+                if (above < remaining && above + cs[i] >= remaining) {
+                    d = 4 * lane + i;
+                    ab = above;
+                }
+                above += cs[i];
+            }
+            const unsigned m = __ballot_sync(kFull, d >= 0);
+            const int from = m ? __ffs(m) - 1 : 0;
+            remaining -= __shfl_sync(kFull, ab, from);
+            prefix = (prefix << 7) | (uint32_t)__shfl_sync(kFull, d, from);
+            __syncwarp();   // every lane has read the histogram before the next pass clears it
+        }
+    } else {
+        // a threshold bin too large to list (rows of many equal scores): passes of 7 bits over the
+        // keys in registers
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = 14 - 7 * pass;
+            reinterpret_cast<uint4*>(h)[lane] = make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < kWarpRowCap / 32; ++i)
+                if (32 * i + lane < vis && (key[i] >> (shift + 7)) == prefix)
+                    atomicAdd(&h[(key[i] >> shift) & 127u], 1u);
+            __syncwarp();
+            int above;
+            const int d = warp_select128(h, remaining, lane, &above);
+            remaining -= above;
+            prefix = (prefix << 7) | (uint32_t)d;
+            __syncwarp();
+        }
     }
     const uint32_t tau = prefix;
     const int need_eq = remaining;   // >= 1 keys equal to tau are taken, lowest positions first
@@ -900,9 +987,15 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
     }
     if (p.hist == nullptr && p.n_cols <= kWarpRowCap) {
         // short rows without a precomputed first pass (prefill): one warp per row
+        const size_t wsmem = (size_t)kWtRows * (kBins + kWtCandCap) * 4;
+        cudaError_t e0 = cudaFuncSetAttribute(topk_warp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
+        if (e0 == cudaSuccess)
+            e0 = cudaFuncSetAttribute(topk_warp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
+        if (e0 != cudaSuccess) return e0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)((rows + kWtRows - 1) / kWtRows));
         cfg.blockDim = dim3(kWtThreads);
+        cfg.dynamicSmemBytes = wsmem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
