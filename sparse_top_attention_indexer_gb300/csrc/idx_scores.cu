@@ -13,7 +13,9 @@
 // warp-specialised:
 //   warp 0      TMA producer (index-key tiles, and the unit's query tile)
 //   warp 1      TMEM allocator + single-thread MMA issuer
-//   warps 2..5  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced)
+//   warps 2..9  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced); two
+//               warps per TMEM lane quarter, taking alternate query chunks of a unit (one query per
+//               unit, as in decode, and MXFP4: warps 2..5, one per quarter)
 // With MXFP4 keys (Indexer.forward's fp4 keys and queries) warp 0 stages packed tiles (E2M1
 // codes + E8M0 scales) by bulk copy and warps 6..13 decode them in shared memory -- to E5M2 for
 // kind::f8f6f4 MMAs where every block's scale allows an exact E5M2 value, else to bf16 -- after
@@ -31,7 +33,8 @@ namespace sti {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 192;      // bf16 keys: producer, MMA, 4 epilogue warps
+constexpr int kThreads = 320;      // bf16 keys: producer, MMA, 8 epilogue warps (two per TMEM lane quarter)
+constexpr int kThreadsOneQ = 192;  // bf16 keys, one query per unit (decode): 4 epilogue warps
 constexpr int kThreadsFp4 = 448;   // MXFP4 keys: + 8 warps that dequantise keys and quantise queries
 constexpr int kDqWarps = 8;
 constexpr int kMaxStages = 8;
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         mbar_init(&bars->empty_b, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->acc_full[i], 1);
-            mbar_init(&bars->acc_empty[i], 4);
+            mbar_init(&bars->acc_empty[i], FP4 ? 4u : (blockDim.x - 64u) / 32u);   // one arrival per epilogue warp
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
@@ -593,7 +596,12 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         }
     } else {
         // ---------------------------------------------------------------- epilogue
-        const int ep_tid = threadIdx.x - 64;           // 0..127
+        // bf16 keys with several queries per unit: two warps per TMEM lane quarter, each taking every
+        // other query chunk of a unit
+        const int EPI = FP4 ? 4 : ((int)blockDim.x - 64) / 32;   // epilogue warps (4 or 8)
+        const int NG = EPI / 4;                                  // warps per lane quarter
+        const int ep_tid = threadIdx.x - 64;           // 0 .. 32 EPI - 1
+        const int eg = (warp - 2) >> 2;                // this warp's group: query chunks eg, eg + NG, ...
         const int quarter = warp & 3;                  // TMEM lane quarter this warp may access
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         constexpr int QPC = HI >= 32 ? 1 : 32 / HI;    // queries per 32-column load
@@ -606,14 +614,14 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             const int t0 = qt * p.nq;
             const int nq_here = min(p.nq, p.s - t0);
             if (u != cur_unit) {
-                named_bar_sync(1, 128);
-                for (int i = ep_tid; i < nq_here * HI; i += 128) {
+                named_bar_sync(1, 32 * EPI);
+                for (int i = ep_tid; i < nq_here * HI; i += 32 * EPI) {
                     const uint16_t wb = p.w[((size_t)b * p.s + t0) * HI + i];
                     w_s[i] = __uint_as_float((uint32_t)wb << 16) * p.c;
                 }
-                for (int i = ep_tid; i < nq_here; i += 128)
+                for (int i = ep_tid; i < nq_here; i += 32 * EPI)
                     vis_s[i] = max(0, min(p.n_cols, (__ldg(p.start_pos + b) + t0 + i + 1) / p.ratio));
-                named_bar_sync(1, 128);
+                named_bar_sync(1, 32 * EPI);
                 cur_unit = u;
             }
             bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
@@ -623,7 +631,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             const int key = tile * kTileKeys + quarter * 32 + lane;
             const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * p.n_alloc);
             if (ok) {
-                for (int q0 = 0; q0 < nq_here; q0 += QPC) {
+                for (int q0 = eg * QPC; q0 < nq_here; q0 += QPC * NG) {
                     float sacc[QPC];
 #pragma unroll
                     for (int i = 0; i < QPC; ++i) sacc[i] = 0.f;
@@ -674,7 +682,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             const int first = unit_tiles(p, uu) * kTileKeys;
             for (int q = 0; q < nq_here; ++q) {
                 float* row = p.scores + ((size_t)b * p.s + t0 + q) * p.n_cols;
-                for (int j = first + ep_tid; j < p.n_cols; j += 128) row[j] = -INFINITY;
+                for (int j = first + ep_tid; j < p.n_cols; j += 32 * EPI) row[j] = -INFINITY;
             }
         }
     }
@@ -723,7 +731,7 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
         auto kern = p.fp4 ? idx_scores_kernel<HV, true> : idx_scores_kernel<HV, false>;               \
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
         if (err != cudaSuccess) return err;                                                            \
-        kern<<<grid, p.fp4 ? kThreadsFp4 : kThreads, smem, stream>>>(tm_a, tm_b, tm_s, p);            \
+        kern<<<grid, p.fp4 ? kThreadsFp4 : (p.nq > 1 ? kThreads : kThreadsOneQ), smem, stream>>>(tm_a, tm_b, tm_s, p); \
         return cudaGetLastError();                                                                     \
     }
     switch (p.Hi) {

@@ -282,6 +282,7 @@ constexpr int kWarpRowCap = 2048;             // visible positions a warp holds 
 constexpr int kWtThreads = 512;               // 16 rows per CTA
 constexpr int kWtRows = kWtThreads / 32;
 constexpr int kWtCandCap = 512;               // keys of the first pass's threshold bin listed per row
+constexpr int kWarpRowsMin = 4096;            // fewer rows take the CTA-per-row kernel
 
 // The digit d of a 128-bin histogram where the count of keys from the top first reaches
 // `remaining` (1 <= remaining <= total), and in *above the keys in higher bins.  Lane l holds
@@ -985,8 +986,10 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t stream) {
         err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<CR>, p, chunk_cap);
         return err != cudaSuccess ? err : cudaGetLastError();
     }
-    if (p.hist == nullptr && p.n_cols <= kWarpRowCap) {
-        // short rows without a precomputed first pass (prefill): one warp per row
+    if (p.hist == nullptr && p.n_cols <= kWarpRowCap && rows >= kWarpRowsMin) {
+        // many short rows without a precomputed first pass (prefill): one warp per row.  A warp
+        // takes longer over a row than a 512-thread CTA but holds 16 rows per SM at once, so it
+        // wins only when there are rows enough to fill the GPU several times over
         const size_t wsmem = (size_t)kWtRows * (kBins + kWtCandCap) * 4;
         cudaError_t e0 = cudaFuncSetAttribute(topk_warp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsmem);
         if (e0 == cudaSuccess)

@@ -165,6 +165,7 @@ def test_idx_scores_mxfp4_scale_ranges(sti, orc, case):
     (2, 1, 16384, 512, [65535, 40000], 4),
     (4, 1, 1000, 512, [3999, 2047, 2048, 7], 4),
     (1, 64, 2048, 512, [0], 1),
+    (1, 4200, 2048, 512, [0], 1),                 # many short rows: one warp per row
     (1, 300, 75, 16, [0], 4),
     (1, 1, 32768, 512, [131071], 4),
     (2, 1, 40000, 100, [159999, 100000], 4),     # beyond the shared-memory staging size
@@ -185,9 +186,9 @@ def test_topk_many_ties(sti, orc, levels):
     """Prefill rows (one warp a row) whose scores take only a few values: the k-th largest key is
     shared by many positions, so the lower-position rule decides most of the set."""
     rng = rng_for(602, levels)
-    b, s, n_cols, k = 2, 96, 2048, 512
+    b, s, n_cols, k = 2, 2100, 2048, 512   # 4200 rows: the warp-per-row kernel
     scores = rng.integers(0, levels, size=(b, s, n_cols)).astype(np.float32) * 0.25 - 1.0
-    scores[0, 5, :] = 0.5                              # one row all equal
+    scores[0, 2050, :] = 0.5                           # one row all equal (its bin too large to list)
     sp = np.array([0, 0], np.int32)
     ref = orc.topk(scores.astype(np.float64), sp, 1, k, 7)
     got = sti.idx_topk(to_dev_any(scores), to_dev_any(sp), 1, k, 7).cpu().numpy()
