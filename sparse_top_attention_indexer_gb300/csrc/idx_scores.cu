@@ -169,6 +169,22 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, int Di, i
 #ifdef STI_STEP_TIMING
 __device__ unsigned long long g_sc_t[2048][2];   // global timer at CTA start and end (profiling builds)
 #endif
+#ifdef STI_SC_TILE_TIMING
+__device__ unsigned long long g_sc_pro[2048][4];  // prologue: after the barrier, after the range, first copy issued
+#endif
+#ifdef STI_SC_TILE_TIMING
+// profiling builds only: global-timer stamps of the first 16 tiles of every CTA (e: 0 packed tile
+// landed, 1 tile decoded, 2 MMAs issued, 3 epilogue done, 4 copy issued)
+__device__ unsigned long long g_sc_tile[2048][16][5];
+#define STI_SCSTAMP(li, e)                                                                              \
+    do {                                                                                                \
+        if (blockIdx.x < 2048 && (li) >= 0 && (li) < 16) g_sc_tile[blockIdx.x][(li)][(e)] = global_timer_ns(); \
+    } while (0)
+#else
+#define STI_SCSTAMP(li, e) \
+    do {                   \
+    } while (0)
+#endif
 
 // E2M1 nibble (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa; exponent 0 is
 // subnormal: m * 0.5) as a float.
@@ -319,11 +335,17 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+#ifdef STI_SC_TILE_TIMING
+    if (threadIdx.x == 0 && blockIdx.x < 2048) g_sc_pro[blockIdx.x][0] = global_timer_ns();
+#endif
 
     // this CTA's contiguous range of the flattened (unit, tile) list
     int g0, g1, u, tile;
     cta_range(p, g0, g1, u, tile);
     int un = unit_tiles_at(p, u), un_next = unit_tiles_at(p, u + 1);
+#ifdef STI_SC_TILE_TIMING
+    if (threadIdx.x == 0 && blockIdx.x < 2048) g_sc_pro[blockIdx.x][1] = global_timer_ns();
+#endif
     const int ncb = p.Di >= 64 ? p.Di / 64 : 1;  // column blocks per row
     const int box_inner = p.Di >= 64 ? 64 : p.Di;
 
@@ -376,6 +398,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                         bulk_load(dst + c_code_bytes,
                                   p.k_scales + (size_t)b * p.k_scales_bstride + (size_t)tile * kTileKeys * (p.Di / 32),
                                   sb_bytes, &bars->full_c[stage]);
+                        STI_SCSTAMP(g - g0, 4);
                     }
                 } else {
                     ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
@@ -385,6 +408,9 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                         for (int cb = 0; cb < ncb; ++cb)
                             tma_load_3d(dst + (size_t)cb * kTileKeys * box_inner * 2, &tm_a, &bars->full_a[stage],
                                         cb * box_inner, tile * kTileKeys, b);
+#ifdef STI_SC_TILE_TIMING
+                        if (g == g0 && blockIdx.x < 2048) g_sc_pro[blockIdx.x][2] = global_timer_ns();
+#endif
                     }
                 }
                 if (ok) {
@@ -444,6 +470,10 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                     }
                     umma_commit(&bars->empty_a[stage]);
                     umma_commit(&bars->acc_full[acc]);
+                    STI_SCSTAMP(g - g0, 2);
+#ifdef STI_SC_TILE_TIMING
+                    if (g == g0 && blockIdx.x < 2048) g_sc_pro[blockIdx.x][3] = global_timer_ns();
+#endif
                 } else {
                     atomicExch(&bars->abort, 1u);
                 }
@@ -512,6 +542,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             }
             ok = ok && mbar_wait(&bars->empty_a[astage], aphase ^ 1u, p.status);
             ok = ok && mbar_wait(&bars->full_c[cstage], cphase, p.status);
+            if (dq_t == 0) STI_SCSTAMP(g - g0, 0);
             const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
             const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
             const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
@@ -577,7 +608,10 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             } else {
                 atomicExch(&bars->abort, 1u);
             }
-            if (dq_t == 0) bars->fmt[astage] = f8 ? 1u : 0u;
+            if (dq_t == 0) {
+                bars->fmt[astage] = f8 ? 1u : 0u;
+                STI_SCSTAMP(g - g0, 1);
+            }
             fence_proxy_async_smem();   // generic stores, read by the tensor core
             __syncwarp();
             if (lane == 0 && ok) {
@@ -668,6 +702,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+            if (ep_tid == 0) STI_SCSTAMP(g - g0, 3);
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -748,6 +783,15 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
 
 }  // namespace sti
 
+#ifdef STI_SC_TILE_TIMING
+// profiling builds only: per-tile global-timer stamps of the scores kernel's first 16 tiles per CTA
+extern "C" int sti_dbg_scores_tile_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_sc_tile, sizeof(unsigned long long) * 16 * 5 * (size_t)n_blocks);
+}
+extern "C" int sti_dbg_scores_prologue_times(unsigned long long* host, int n_blocks) {
+    return (int)cudaMemcpyFromSymbol(host, sti::g_sc_pro, sizeof(unsigned long long) * 4 * (size_t)n_blocks);
+}
+#endif
 #ifdef STI_STEP_TIMING
 // profiling builds only: global-timer stamps (ns) of the scores kernel's CTAs
 extern "C" int sti_dbg_scores_times(unsigned long long* host, int n_blocks) {
