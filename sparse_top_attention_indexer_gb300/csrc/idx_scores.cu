@@ -302,13 +302,13 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(&bars->full_a[i], FP4 ? kDqWarps : 1);   // MXFP4: the dequantising warps
+            mbar_init(&bars->full_a[i], FP4 ? kDqWarps / 2 : 1);   // MXFP4: the decoding group's warps
             mbar_init(&bars->empty_a[i], 1);
         }
         if (FP4) {
             for (int i = 0; i < p.c_stages; ++i) {
                 mbar_init(&bars->full_c[i], 1);
-                mbar_init(&bars->empty_c[i], kDqWarps);
+                mbar_init(&bars->empty_c[i], kDqWarps / 2);
             }
             mbar_init(&bars->b_ready, 1);
         }
@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         // ---------------------------------------------------------------- MXFP4 keys and queries
         // At each new unit the eight warps first quantise the unit's queries in place (32-element
         // blocks of every query row, four lanes to a block), as the forward pass quantises q, and
-        // with Di == 128 also write them as E5M2.  Then threads dq and dq + 128 own key row dq of
-        // every tile, half of its scale blocks each.  When the unit's queries and every scale block
+        // with Di == 128 also write them as E5M2.  Then the warps form two groups of four that take
+        // the CTA's tiles in turn, thread dq of a group owning key row dq of its tiles.  When the unit's queries and every scale block
         // of the tile's visible keys have X in [-13, 13], each E2M1 code times 2^X is an exact
         // E5M2 number: the row becomes 128 E5M2 bytes (kind::f8f6f4, half the bytes and MMAs of
         // bf16).  Otherwise the Di/2 code bytes and Di/32 scale bytes become Di bf16 values (also
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         // stage's fmt word tells the MMA which it is.
         const int dq_t = threadIdx.x - 192;             // 0..255
         const int dq = dq_t & 127;                      // key row of a tile
-        const int half = dq_t >> 7;                     // this thread's half of the row's scale blocks
+        const int dg = dq_t >> 7;                       // decode group: the CTA's tiles alternate between the two
         const int nblk = p.Di / 32;
         int astage = 0, cstage = 0;
         uint32_t aphase = 0, cphase = 0, b_phase = 0;
@@ -540,83 +540,87 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 b_phase ^= 1u;
                 cur_unit = u;
             }
-            ok = ok && mbar_wait(&bars->empty_a[astage], aphase ^ 1u, p.status);
-            ok = ok && mbar_wait(&bars->full_c[cstage], cphase, p.status);
-            if (dq_t == 0) STI_SCSTAMP(g - g0, 0);
-            const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
-            const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
-            const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
-            uint8_t* arow = a_ring + (size_t)astage * a_bytes + (size_t)dq * 128;
-            // Every warp checks all 512 scale bytes of the tile (16 a lane: keys 4*lane .. 4*lane+3),
-            // so all eight reach the same decision without a barrier.  Keys no query of the unit
-            // sees may hold anything.  ok is warp-uniform here (the vote below needs every lane).
-            ok = __all_sync(kFull, ok);
-            bool f8 = false;
-            if (ok && q_f8) {
-                const uint4 sc4 = *reinterpret_cast<const uint4*>(cst + c_code_bytes + lane * 16);
-                const uint32_t sw[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
-                bool in = true;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t r = __vcmpgeu4(sw[k], 0x72727272u) & __vcmpleu4(sw[k], 0x8C8C8C8Cu);  // 114..140
-                    in = in && (r == 0xFFFFFFFFu || tile * kTileKeys + lane * 4 + k >= vis_unit);
-                }
-                f8 = __all_sync(kFull, in);
-            }
-            if (ok && f8) {
-                for (int q4 = half; q4 < nblk; q4 += 2) {
-                    const int qb = (q4 + dq) & 3;   // rotated, as below; Di == 128 here
-                    const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
-                    uint32_t t0, t1;
-                    e5m2_table(max(-13, min(13, (int)srow[qb] - 127)), t0, t1);
-                    const uint2 o0 = e2m1x8_to_e5m2(cw4.x, t0, t1), o1 = e2m1x8_to_e5m2(cw4.y, t0, t1);
-                    const uint2 o2 = e2m1x8_to_e5m2(cw4.z, t0, t1), o3 = e2m1x8_to_e5m2(cw4.w, t0, t1);
-                    *reinterpret_cast<uint4*>(arow + (((2 * qb) ^ (dq & 7)) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-                    *reinterpret_cast<uint4*>(arow + (((2 * qb + 1) ^ (dq & 7)) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
-                }
-            } else if (ok) {
-                for (int q4 = half; q4 < p.Di / 32; q4 += 2) {
-                    // 16 code bytes = 32 elements = one scale block; rows start 64 bytes apart, so
-                    // lanes take the blocks in rotated order to spread the shared-memory banks
-                    const int qb = (q4 + dq) % (p.Di / 32);
-                    const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
-                    const uint32_t e8 = srow[qb];
-                    const bool fast = e8 >= 2u && e8 <= 252u;   // the exponent stays in the normal range
-                    const float sc = e8m0_value(e8);
-                    const uint32_t k16 = ((e8 - 127u) << 7) & 0xFFFFu;
-                    const uint32_t expadd = k16 | (k16 << 16);
-                    const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {   // 8 elements -> one 16-byte chunk of the tile
-                        uint32_t pk[4];
-                        if (fast) {
-                            e2m1x8_to_bf16(cw[h], expadd, pk);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint32_t byte = (cw[h] >> (8 * j)) & 0xFFu;
-                                const float lo = e2m1_value(byte & 0xFu) * sc, hi = e2m1_value(byte >> 4) * sc;
-                                pk[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
-                            }
-                        }
-                        const int ch = qb * 4 + h;                 // chunk of 8 elements along Di
-                        *reinterpret_cast<uint4*>(arow + (size_t)(ch >> 3) * kTileKeys * 128 +
-                                                  (size_t)(((ch & 7) ^ (dq & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            // every warp walks every tile (units change in step); a group decodes every other one, so
+            // two tiles are in decoding at once
+            if (((g - g0) & 1) == dg) {
+                ok = ok && mbar_wait(&bars->empty_a[astage], aphase ^ 1u, p.status);
+                ok = ok && mbar_wait(&bars->full_c[cstage], cphase, p.status);
+                if (dq == 0) STI_SCSTAMP(g - g0, 0);
+                const uint8_t* cst = c_ring + (size_t)cstage * c_bytes;
+                const uint8_t* crow = cst + (size_t)dq * (p.Di / 2);
+                const uint8_t* srow = cst + c_code_bytes + (size_t)dq * nblk;
+                uint8_t* arow = a_ring + (size_t)astage * a_bytes + (size_t)dq * 128;
+                // Every warp checks all 512 scale bytes of the tile (16 a lane: keys 4*lane .. 4*lane+3),
+                // so the group's four reach the same decision without a barrier.  Keys no query of the unit
+                // sees may hold anything.  ok is warp-uniform here (the vote below needs every lane).
+                ok = __all_sync(kFull, ok);
+                bool f8 = false;
+                if (ok && q_f8) {
+                    const uint4 sc4 = *reinterpret_cast<const uint4*>(cst + c_code_bytes + lane * 16);
+                    const uint32_t sw[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+                    bool in = true;
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t r = __vcmpgeu4(sw[k], 0x72727272u) & __vcmpleu4(sw[k], 0x8C8C8C8Cu);  // 114..140
+                        in = in && (r == 0xFFFFFFFFu || tile * kTileKeys + lane * 4 + k >= vis_unit);
                     }
+                    f8 = __all_sync(kFull, in);
                 }
-            } else {
-                atomicExch(&bars->abort, 1u);
-            }
-            if (dq_t == 0) {
-                bars->fmt[astage] = f8 ? 1u : 0u;
-                STI_SCSTAMP(g - g0, 1);
-            }
-            fence_proxy_async_smem();   // generic stores, read by the tensor core
-            __syncwarp();
-            if (lane == 0 && ok) {
-                mbar_arrive(&bars->full_a[astage]);
-                mbar_arrive(&bars->empty_c[cstage]);
+                if (ok && f8) {
+                    for (int q4 = 0; q4 < nblk; ++q4) {
+                        const int qb = (q4 + dq) & 3;   // rotated, as below; Di == 128 here
+                        const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
+                        uint32_t t0, t1;
+                        e5m2_table(max(-13, min(13, (int)srow[qb] - 127)), t0, t1);
+                        const uint2 o0 = e2m1x8_to_e5m2(cw4.x, t0, t1), o1 = e2m1x8_to_e5m2(cw4.y, t0, t1);
+                        const uint2 o2 = e2m1x8_to_e5m2(cw4.z, t0, t1), o3 = e2m1x8_to_e5m2(cw4.w, t0, t1);
+                        *reinterpret_cast<uint4*>(arow + (((2 * qb) ^ (dq & 7)) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+                        *reinterpret_cast<uint4*>(arow + (((2 * qb + 1) ^ (dq & 7)) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+                    }
+                } else if (ok) {
+                    for (int q4 = 0; q4 < p.Di / 32; ++q4) {
+                        // 16 code bytes = 32 elements = one scale block; rows start 64 bytes apart, so
+                        // lanes take the blocks in rotated order to spread the shared-memory banks
+                        const int qb = (q4 + dq) % (p.Di / 32);
+                        const uint4 cw4 = *reinterpret_cast<const uint4*>(crow + qb * 16);
+                        const uint32_t e8 = srow[qb];
+                        const bool fast = e8 >= 2u && e8 <= 252u;   // the exponent stays in the normal range
+                        const float sc = e8m0_value(e8);
+                        const uint32_t k16 = ((e8 - 127u) << 7) & 0xFFFFu;
+                        const uint32_t expadd = k16 | (k16 << 16);
+                        const uint32_t cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+    #pragma unroll
+                        for (int h = 0; h < 4; ++h) {   // 8 elements -> one 16-byte chunk of the tile
+                            uint32_t pk[4];
+                            if (fast) {
+                                e2m1x8_to_bf16(cw[h], expadd, pk);
+                            } else {
+    #pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t byte = (cw[h] >> (8 * j)) & 0xFFu;
+                                    const float lo = e2m1_value(byte & 0xFu) * sc, hi = e2m1_value(byte >> 4) * sc;
+                                    pk[j] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+                                }
+                            }
+                            const int ch = qb * 4 + h;                 // chunk of 8 elements along Di
+                            *reinterpret_cast<uint4*>(arow + (size_t)(ch >> 3) * kTileKeys * 128 +
+                                                      (size_t)(((ch & 7) ^ (dq & 7)) << 4)) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
+                    }
+                } else {
+                    atomicExch(&bars->abort, 1u);
+                }
+                if (dq == 0) {
+                    bars->fmt[astage] = f8 ? 1u : 0u;
+                    STI_SCSTAMP(g - g0, 1);
+                }
+                fence_proxy_async_smem();   // generic stores, read by the tensor core
+                __syncwarp();
+                if (lane == 0 && ok) {
+                    mbar_arrive(&bars->full_a[astage]);
+                    mbar_arrive(&bars->empty_c[cstage]);
+                }
             }
             if (++astage == p.stages) {
                 astage = 0;
