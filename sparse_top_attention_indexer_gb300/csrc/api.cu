@@ -110,6 +110,23 @@ sti_status make_map_3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint
     return STI_OK;
 }
 
+// 3-D tensor map of MXFP4 codes for E2M1 MMA operands: dims {128 codes, rows, batch}, strides in
+// bytes (row 64 B); a box of 128 codes x 128 rows lands as 128-byte rows of 16-byte chunks, each
+// holding 16 codes in its first 8 bytes, 128-byte swizzled.  False when the driver declines the map
+// (the caller then decodes the codes in shared memory instead); no error is recorded.
+static bool make_map_3d_e2m1(CUtensorMap* m, const void* base, uint64_t rows, uint64_t batch,
+                             uint64_t batch_stride_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, rows, batch};
+    cuuint64_t strides[2] = {64, batch_stride_bytes};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uint32_t* status_word(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 
 bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
@@ -233,8 +250,22 @@ static sti_status idx_scores_impl(const uint16_t* iq, const uint16_t* ik, int64_
     const CUtensorMapSwizzle swz = Di >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap tm_a, tm_b, tm_s;
     memset(&tm_s, 0, sizeof tm_s);
-    sti_status s;
-    if (fp4) {
+    sti_status s = STI_OK;
+    // One query per unit (decode) with Di == 128: the codes go to the tensor core as E2M1 operands,
+    // one accumulator per 32-code scale block (4 x n_alloc TMEM columns per buffer), the scales
+    // applied in the epilogue; no decode in shared memory.
+    const bool e2 = fp4 && Di == 128 && p.nq == 1 && p.n_pad <= 32 && aligned(fp4->codes, 32) &&
+                    fp4->codes_bstride % 32 == 0 &&
+                    make_map_3d_e2m1(&tm_a, fp4->codes, (uint64_t)n_cols, (uint64_t)b, (uint64_t)fp4->codes_bstride);
+    if (e2) {
+        p.fp4 = 2;
+        p.f8 = 0;
+        p.c_stages = 0;
+        p.tmem_cols = 256;   // 2 buffers x 4 blocks x 32 columns
+        p.ctas_per_sm = 2;
+        for (p.stages = 8; p.stages > 2 && sti::idx_scores_smem_bytes(p) > (size_t)(228 * 1024 / 2 - 1024); --p.stages) {
+        }
+    } else if (fp4) {
         // codes: rows of Di/2 bytes; scales: each batch's Di/32 bytes per key as rows of 16 bytes
         s = make_map_3d_u8(&tm_a, fp4->codes, (uint64_t)Di / 2, (uint64_t)n_cols, (uint64_t)b, (uint64_t)Di / 2,
                            (uint64_t)fp4->codes_bstride, (uint32_t)Di / 2, 128);

@@ -174,7 +174,8 @@ __device__ unsigned long long g_sc_pro[2048][4];  // prologue: after the barrier
 #endif
 #ifdef STI_SC_TILE_TIMING
 // profiling builds only: global-timer stamps of the first 16 tiles of every CTA (e: 0 packed tile
-// landed, 1 tile decoded, 2 MMAs issued, 3 epilogue done, 4 copy issued)
+// landed, 1 tile decoded, 2 MMAs issued, 3 epilogue done, 4 copy issued; with E2M1 operands 0 is the
+// MMA issuer seeing the tile landed and 1 the epilogue seeing the accumulators ready)
 __device__ unsigned long long g_sc_tile[2048][16][5];
 #define STI_SCSTAMP(li, e)                                                                              \
     do {                                                                                                \
@@ -232,6 +233,14 @@ __device__ __forceinline__ uint2 e2m1x8_to_e5m2(uint32_t cw, uint32_t t0, uint32
     return make_uint2(m0 | (~n0 & 0x80808080u), m1 | (~n1 & 0x80808080u));
 }
 
+// The block scale exponent X = floor(log2 max|x|) - 2 of an MXFP4 block, clamped to E8M0's range
+// (-127 for an all-zero block).  floor(log2 amax) is the exponent field of a normal amax; zero and
+// subnormals are rare.
+__device__ __forceinline__ int mxfp4_block_exp(float amax) {
+    const int eb = (int)(__float_as_uint(amax) >> 23);
+    return eb > 0 ? max(-127, min(127, eb - 129)) : (amax > 0.f ? max(-127, ilogbf(amax) - 2) : -127);
+}
+
 // One 16-byte chunk (8 bf16 queries) of a 32-element block whose four chunks sit in lanes 4k..4k+3
 // of the warp: the block is quantised to MXFP4 and decoded back in place (Indexer.forward's
 // fp4_act_quant on q, read as OCP MXFP4: scale 2^X with X = floor(log2 max|x|) - 2); the decoded
@@ -248,9 +257,7 @@ __device__ __forceinline__ bool mxfp4_fake_quant_chunk(uint4* chunk, uint2* e5) 
     }
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-    // floor(log2 amax) is the exponent field of a normal amax; zero and subnormals are rare
-    const int eb = (int)(__float_as_uint(amax) >> 23);
-    const int X = eb > 0 ? max(-127, min(127, eb - 129)) : (amax > 0.f ? max(-127, ilogbf(amax) - 2) : -127);
+    const int X = mxfp4_block_exp(amax);
     const float sc = exp2i(X), inv = exp2i(-X);
     uint32_t t0, t1;
     e5m2_table(max(-13, min(13, X)), t0, t1);
@@ -271,10 +278,38 @@ __device__ __forceinline__ bool mxfp4_fake_quant_chunk(uint4* chunk, uint2* e5) 
     return amax == 0.f || (X >= -13 && X <= 13);
 }
 
-template <int HI, bool FP4>
-__global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
+// KM: 0 bf16 keys, 1 MXFP4 keys decoded in shared memory, 2 MXFP4 keys as E2M1 MMA operands.
+// The same quantisation of a chunk, returned as its eight E2M1 codes (element i in nibble i: sign in
+// bit 3, magnitude index in bits 0-2) with the block's X.
+__device__ __forceinline__ uint32_t mxfp4_quant_e2m1(const uint4 v, int& X) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    X = mxfp4_block_exp(amax);
+    const float inv = exp2i(-X);
+    uint32_t nib = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = w[i] << 16, hi = w[i] & 0xFFFF0000u;
+        const uint32_t cl = e2m1_index(fabsf(__uint_as_float(lo)) * inv) | ((lo >> 28) & 8u);
+        const uint32_t ch = e2m1_index(fabsf(__uint_as_float(hi)) * inv) | ((hi >> 28) & 8u);
+        nib |= (cl | (ch << 4)) << (8 * i);
+    }
+    return nib;
+}
+
+template <int HI, int KM>
+__global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOneQ : kThreads), KM == 0 ? 1 : 2)
     idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_s, const IdxScoresParams p) {
+    constexpr bool FP4 = KM == 1;
+    constexpr bool E2 = KM == 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned start, offset from the __shared__ array itself so every derived pointer
     // stays a known shared-memory pointer (ld/st.shared, not generic accesses)
@@ -283,28 +318,36 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
     if (threadIdx.x == 0 && blockIdx.x < 2048) g_sc_t[blockIdx.x][0] = global_timer_ns();
 #endif
     griddep_launch_dependents();   // the top-k may be scheduled now; it waits for this grid's end
-    const int a_bytes = kTileKeys * p.Di * 2;
+    // E2M1 operands (Di == 128): a key tile is 128 rows of 128 bytes, each 16-byte chunk holding 16
+    // codes in its first 8 bytes (the layout TMA's 16 x U4 / 16-byte-aligned load writes)
+    const int a_bytes = E2 ? kTileKeys * 128 : kTileKeys * p.Di * 2;
     const int b_bytes = p.n_pad * p.Di * 2;
     uint8_t* a_ring = smem;
     uint8_t* b_buf = smem + (size_t)p.stages * a_bytes;
-    // MXFP4: packed key tiles, [128 keys x Di/2 code bytes | 128 keys x Di/32 scale bytes] per stage
+    // MXFP4: packed key tiles, [128 keys x Di/2 code bytes | 128 keys x Di/32 scale bytes] per stage;
+    // E2M1 operands: only the scale bytes, one ring slot per key stage
     const int c_code_bytes = kTileKeys * p.Di / 2;
-    const int c_bytes = FP4 ? c_code_bytes + kTileKeys * p.Di / 32 : 0;
-    // MXFP4 with Di == 128: the quantised queries again as E5M2, rows of 128 bytes (128-byte swizzle)
+    const int c_bytes = FP4 ? c_code_bytes + kTileKeys * p.Di / 32 : (E2 ? kTileKeys * 4 : 0);
+    // MXFP4 with Di == 128: the quantised queries again as E5M2, or (E2M1 operands) as E2M1 codes in
+    // the key tile's layout; rows of 128 bytes, 128-byte swizzle
     uint8_t* b8 = b_buf + b_bytes;
-    const int b8_bytes = (FP4 && p.f8) ? p.n_pad * 128 : 0;
+    const int b8_bytes = ((FP4 && p.f8) || E2) ? p.n_pad * 128 : 0;
     uint8_t* c_ring = b8 + b8_bytes;
-    Barriers* bars = reinterpret_cast<Barriers*>(c_ring + (size_t)(FP4 ? p.c_stages : 0) * c_bytes);
+    Barriers* bars = reinterpret_cast<Barriers*>(c_ring + (size_t)(FP4 ? p.c_stages : (E2 ? p.stages : 0)) * c_bytes);
     float* w_s = reinterpret_cast<float*>(bars + 1);   // [nq * HI], pre-multiplied by c
     int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq], nq <= 64
+    float* sq_s = reinterpret_cast<float*>(vis_s + 64); // E2M1 operands: 2^X of query block j, head h at [32 j + h]
+    uint32_t* hs = reinterpret_cast<uint32_t*>(sq_s + 128);   // E2M1 operands: the unit's first-pass histogram
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&bars->full_a[i], FP4 ? kDqWarps / 2 : 1);   // MXFP4: the decoding group's warps
-            mbar_init(&bars->empty_a[i], 1);
+            // E2M1 operands: the MMAs' commit and the four epilogue warps, which read the stage's scales
+            mbar_init(&bars->empty_a[i], E2 ? 5 : 1);
         }
+        if (E2) mbar_init(&bars->b_ready, 1);
         if (FP4) {
             for (int i = 0; i < p.c_stages; ++i) {
                 mbar_init(&bars->full_c[i], 1);
@@ -402,7 +445,20 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                     }
                 } else {
                     ok = ok && mbar_wait(&bars->empty_a[stage], phase ^ 1u, p.status);
-                    if (ok) {
+                    if (ok && E2) {
+                        // codes by one TMA box (128 codes x 128 keys: 8 KB of codes spread over 16 KB,
+                        // the box's transfer count; keys past n_cols read as zero codes), scale bytes
+                        // by a bulk copy of the tile's keys
+                        uint8_t* dst = a_ring + (size_t)stage * a_bytes;
+                        const int nk = min(kTileKeys, p.n_cols - tile * kTileKeys);
+                        const uint32_t sb_bytes = (uint32_t)((nk * 4 + 15) & ~15);
+                        mbar_arrive_expect_tx(&bars->full_a[stage], (uint32_t)a_bytes / 2 + sb_bytes);
+                        tma_load_3d(dst, &tm_a, &bars->full_a[stage], 0, tile * kTileKeys, b);
+                        bulk_load(c_ring + (size_t)stage * c_bytes,
+                                  p.k_scales + (size_t)b * p.k_scales_bstride + (size_t)tile * kTileKeys * 4, sb_bytes,
+                                  &bars->full_a[stage]);
+                        STI_SCSTAMP(g - g0, 4);
+                    } else if (ok) {
                         uint8_t* dst = a_ring + (size_t)stage * a_bytes;
                         mbar_arrive_expect_tx(&bars->full_a[stage], (uint32_t)a_bytes);
                         for (int cb = 0; cb < ncb; ++cb)
@@ -438,6 +494,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         // ---------------------------------------------------------------- MMA issuer
         const uint32_t idesc = idesc_bf16_f32(128, p.n_pad, false, false);
         const uint32_t idesc8 = idesc_e5m2_f32(128, p.n_pad);
+        const uint32_t idesc4 = idesc_e2m1_f32(128, p.n_pad);
         const int ksteps = p.Di / 16;
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0, b_phase = 0;
@@ -447,16 +504,24 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                 bool ok = true;
                 if (u != cur_unit) {
                     if (cur_unit >= 0) umma_commit(&bars->empty_b);
-                    ok = mbar_wait(FP4 ? &bars->b_ready : &bars->full_b, b_phase, p.status);
+                    ok = mbar_wait((FP4 || E2) ? &bars->b_ready : &bars->full_b, b_phase, p.status);
                 }
                 ok = ok && mbar_wait(&bars->acc_empty[acc], acc_phase ^ 1u, p.status);
                 ok = ok && mbar_wait(&bars->full_a[stage], phase, p.status);
                 if (ok) {
+                    if (E2) STI_SCSTAMP(g - g0, 0);
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(a_ring + (size_t)stage * a_bytes);
                     const uint32_t b_base = smem_u32(b_buf);
-                    const uint32_t d_tmem = tmem + (uint32_t)(acc * p.n_alloc);
-                    if (FP4 && *(volatile uint32_t*)&bars->fmt[stage] != 0u) {
+                    const uint32_t d_tmem = tmem + (uint32_t)(acc * (E2 ? 4 : 1) * p.n_alloc);
+                    if (E2) {
+                        // one K = 32 step per scale block, each into its own accumulator (the block's
+                        // two E8M0 scales are applied in the epilogue)
+                        const uint32_t b8_base = smem_u32(b8);
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f8f6f4(d_tmem + (uint32_t)(kk * p.n_alloc), kmajor_desc(a_base, kk, 64, kTileKeys),
+                                        kmajor_desc(b8_base, kk, 64, p.n_pad), idesc4, 0u);
+                    } else if (FP4 && *(volatile uint32_t*)&bars->fmt[stage] != 0u) {
                         // E5M2 keys and queries: rows of 128 bytes, K = 32 per instruction, so the
                         // descriptors step like a 64-wide bf16 tile
                         const uint32_t b8_base = smem_u32(b8);
@@ -636,7 +701,7 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         // ---------------------------------------------------------------- epilogue
         // bf16 keys with several queries per unit: two warps per TMEM lane quarter, each taking every
         // other query chunk of a unit
-        const int EPI = FP4 ? 4 : ((int)blockDim.x - 64) / 32;   // epilogue warps (4 or 8)
+        const int EPI = (FP4 || E2) ? 4 : ((int)blockDim.x - 64) / 32;   // epilogue warps (4 or 8)
         const int NG = EPI / 4;                                  // warps per lane quarter
         const int ep_tid = threadIdx.x - 64;           // 0 .. 32 EPI - 1
         const int eg = (warp - 2) >> 2;                // this warp's group: query chunks eg, eg + NG, ...
@@ -647,32 +712,117 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         int cur_unit = -1;
+        int st_e = 0;                  // E2M1 operands: the key stage of this tile (its scale bytes)
+        uint32_t st_phase = 0, qb_phase = 0;
+        // E2M1 operands: the first-pass histogram of the top-k gathers in shared memory (one shared
+        // atomic per visible key) and goes to the unit's row in global memory when the CTA leaves the
+        // unit (one atomic per non-empty bin); called after a barrier of the epilogue warps
+        auto flush_hist = [&](int uu) {
+            const int fb = uu / p.QT, ft0 = (uu - fb * p.QT) * p.nq;
+            uint32_t* row = p.hist + ((size_t)fb * p.s + ft0) * 2048;
+            for (int i = ep_tid; i < 2048; i += 32 * EPI) {
+                const uint32_t v = hs[i];
+                if (v != 0u) {
+                    atomicAdd(row + i, v);
+                    hs[i] = 0u;
+                }
+            }
+        };
+        if (E2 && p.hist != nullptr)
+            for (int i = ep_tid; i < 2048; i += 32 * EPI) hs[i] = 0u;   // ordered by the first unit's barrier
         for (int g = g0; g < g1; ++g) {
             const int b = u / p.QT, qt = u - (u / p.QT) * p.QT;
             const int t0 = qt * p.nq;
             const int nq_here = min(p.nq, p.s - t0);
             if (u != cur_unit) {
                 named_bar_sync(1, 32 * EPI);
+                if (E2 && p.hist != nullptr && cur_unit >= 0) flush_hist(cur_unit);
                 for (int i = ep_tid; i < nq_here * HI; i += 32 * EPI) {
                     const uint16_t wb = p.w[((size_t)b * p.s + t0) * HI + i];
                     w_s[i] = __uint_as_float((uint32_t)wb << 16) * p.c;
                 }
                 for (int i = ep_tid; i < nq_here; i += 32 * EPI)
                     vis_s[i] = max(0, min(p.n_cols, (__ldg(p.start_pos + b) + t0 + i + 1) / p.ratio));
+                if (E2) {
+                    // the unit's queries (one per unit, n_pad <= 32 rows) quantised to MXFP4 into the
+                    // E2M1 operand (codes of a 32-element block in two 16-code chunks) and the block
+                    // scales 2^X; every tile of the previous unit has been scored, so its MMAs are done
+                    bool okb = !aborted() && mbar_wait(&bars->full_b, qb_phase, p.status);
+                    okb = __all_sync(kFull, okb);   // warp-uniform: the quantiser shuffles within the warp
+                    if (okb) {
+                        // n_pad * 16 is a multiple of 128: a warp's lanes run the same trips
+                        for (int i = ep_tid; i < p.n_pad * 16; i += 32 * EPI) {
+                            const int r = i >> 4, j = (i >> 2) & 3, t4 = i & 3;
+                            const uint8_t* rowp = b_buf + (size_t)(j >> 1) * p.n_pad * 128 + (size_t)r * 128;
+                            const int c = (j & 1) * 4 + t4;
+                            int X;
+                            const uint32_t nib = mxfp4_quant_e2m1(*reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4)), X);
+                            const int grp = 2 * j + (t4 >> 1);
+                            uint8_t* dst = b8 + (size_t)r * 128 + ((grp ^ (r & 7)) << 4) + (t4 & 1) * 4;
+                            // the chunk's second half is never read as codes; it gets the same bytes
+                            *reinterpret_cast<uint32_t*>(dst) = nib;
+                            *reinterpret_cast<uint32_t*>(dst + 8) = nib;
+                            if (t4 == 0) sq_s[j * 32 + r] = exp2i(X);
+                        }
+                    } else {
+                        atomicExch(&bars->abort, 1u);
+                    }
+                    fence_proxy_async_smem();   // generic stores, read by the tensor core
+                    qb_phase ^= 1u;
+                }
                 named_bar_sync(1, 32 * EPI);
+                if (E2 && ep_tid == 0 && !aborted()) mbar_arrive(&bars->b_ready);
                 cur_unit = u;
             }
             bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
+            // E2M1 operands: the stage's scale bytes landed with its codes (already complete)
+            if (E2) ok = ok && mbar_wait(&bars->full_a[st_e], st_phase, p.status);
             ok = __all_sync(kFull, ok);   // warp-uniform: the loop below holds warp collectives
             if (!ok) atomicExch(&bars->abort, 1u);
+            if (E2 && ep_tid == 0) STI_SCSTAMP(g - g0, 1);
             tc_fence_after();
             const int key = tile * kTileKeys + quarter * 32 + lane;
-            const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * p.n_alloc);
+            const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * (E2 ? 4 : 1) * p.n_alloc);
             if (ok) {
                 for (int q0 = eg * QPC; q0 < nq_here; q0 += QPC * NG) {
                     float sacc[QPC];
 #pragma unroll
                     for (int i = 0; i < QPC; ++i) sacc[i] = 0.f;
+                    if constexpr (E2) {
+                        // one query: y_h = sum over the four 32-code blocks of acc_hj * 2^(Xq_hj + Xk_j)
+                        // (products of E2M1 values are exact, so is each block's fp32 sum), then
+                        // sum_h w_h relu(y_h)
+                        constexpr int HE = HI <= 32 ? HI : 32;
+                        const uint32_t skw = *reinterpret_cast<const uint32_t*>(
+                            c_ring + (size_t)st_e * c_bytes + (size_t)(quarter * 32 + lane) * 4);
+                        // (pairs of heads in packed fp32x2 multiplies and FMAs)
+                        float2 y[HE / 2];
+#pragma unroll
+                        for (int h = 0; h < HE / 2; ++h) y[h] = make_float2(0.f, 0.f);
+                        {   // the four blocks' loads in flight together, one wait
+                            uint32_t r[4][32];
+#pragma unroll
+                            for (int kb = 0; kb < 4; ++kb) tmem_ld32(col_base + (uint32_t)(kb * p.n_alloc), r[kb]);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int kb = 0; kb < 4; ++kb) {
+                                const float sk = e8m0_value((skw >> (8 * kb)) & 0xFFu);
+                                const float2 sk2 = make_float2(sk, sk);
+#pragma unroll
+                                for (int h = 0; h < HE / 2; ++h) {
+                                    const float2 f = __fmul2_rn(*reinterpret_cast<const float2*>(sq_s + kb * 32 + 2 * h), sk2);
+                                    y[h] = __ffma2_rn(make_float2(__uint_as_float(r[kb][2 * h]), __uint_as_float(r[kb][2 * h + 1])),
+                                                      f, y[h]);
+                                }
+                            }
+                        }
+                        float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int h = 0; h < HE / 2; ++h)
+                            s2 = __ffma2_rn(*reinterpret_cast<const float2*>(w_s + 2 * h),
+                                            make_float2(fmaxf(y[h].x, 0.f), fmaxf(y[h].y, 0.f)), s2);
+                        sacc[0] = s2.x + s2.y;
+                    } else {
 #pragma unroll
                     for (int cq = 0; cq < CPQ; ++cq) {
                         uint32_t r[32];
@@ -686,13 +836,16 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
                             sacc[qq] = fmaf(w_s[(q0 + qq) * HI + hh], v, sacc[qq]);
                         }
                     }
+                    }
 #pragma unroll
                     for (int qq = 0; qq < QPC; ++qq) {
                         const int q = q0 + qq;
                         const bool in_row = q < nq_here && key < p.n_cols;
                         const bool visible = in_row && key < vis_s[q];
                         if (in_row) p.scores[((size_t)b * p.s + t0 + q) * p.n_cols + key] = visible ? sacc[qq] : -INFINITY;
-                        if (p.hist != nullptr) {
+                        if (E2 && p.hist != nullptr) {
+                            if (visible) atomicAdd(&hs[float_key(sacc[qq]) >> 21], 1u);
+                        } else if (p.hist != nullptr) {
                             // first radix pass of the top-k: top 11 bits of the order-preserving key,
                             // one aggregated shared-L2 atomic per distinct bin in the warp
                             const uint32_t dig = visible ? (float_key(sacc[qq]) >> 21) : 0xFFFFFFFFu;
@@ -706,12 +859,23 @@ __global__ void __launch_bounds__(FP4 ? kThreadsFp4 : kThreads, FP4 ? 2 : 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+            if (E2) {
+                if (lane == 0) mbar_arrive(&bars->empty_a[st_e]);
+                if (++st_e == p.stages) {
+                    st_e = 0;
+                    st_phase ^= 1u;
+                }
+            }
             if (ep_tid == 0) STI_SCSTAMP(g - g0, 3);
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
             advance(p, u, tile, un, un_next);
+        }
+        if (E2 && p.hist != nullptr && cur_unit >= 0) {
+            named_bar_sync(1, 32 * EPI);
+            flush_hist(cur_unit);
         }
         // -inf for key tiles no query of a unit can see (units strided over CTAs)
         for (int uu = blockIdx.x; uu < p.total_units; uu += gridDim.x) {
@@ -748,8 +912,13 @@ int idx_scores_pick_nq(int Hi, int s) {
 }
 
 size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
-    const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t b_bytes = (size_t)p.n_pad * p.Di * 2;
+    if (p.fp4 == 2) {   // E2M1 operands: padded code tiles + scale bytes per stage, E2M1 queries, 2^X table,
+                        // histogram
+        return 1024 + (size_t)p.stages * (kTileKeys * 128 + kTileKeys * 4) + b_bytes + (size_t)p.n_pad * 128 +
+               sizeof(Barriers) + 256 * 4 + 64 * 4 + 128 * 4 + 2048 * 4;
+    }
+    const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
     const size_t b8_bytes = (p.fp4 && p.f8) ? (size_t)p.n_pad * 128 : 0;
     return 1024 + p.stages * a_bytes + b_bytes + b8_bytes + (p.fp4 ? p.c_stages : 0) * c_bytes + sizeof(Barriers) +
@@ -767,10 +936,13 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
     cudaError_t err = cudaSuccess;
 #define STI_LAUNCH_HI(HV)                                                                              \
     case HV: {                                                                                         \
-        auto kern = p.fp4 ? idx_scores_kernel<HV, true> : idx_scores_kernel<HV, false>;               \
+        auto kern = p.fp4 == 2 ? idx_scores_kernel<HV, 2>                                              \
+                               : (p.fp4 ? idx_scores_kernel<HV, 1> : idx_scores_kernel<HV, 0>);        \
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
         if (err != cudaSuccess) return err;                                                            \
-        kern<<<grid, p.fp4 ? kThreadsFp4 : (p.nq > 1 ? kThreads : kThreadsOneQ), smem, stream>>>(tm_a, tm_b, tm_s, p); \
+        const int threads = p.fp4 == 2 ? kThreadsOneQ                                                 \
+                                       : (p.fp4 ? kThreadsFp4 : (p.nq > 1 ? kThreads : kThreadsOneQ)); \
+        kern<<<grid, threads, smem, stream>>>(tm_a, tm_b, tm_s, p);                                    \
         return cudaGetLastError();                                                                     \
     }
     switch (p.Hi) {

@@ -293,6 +293,13 @@ __host__ __device__ constexpr uint32_t idesc_e5m2_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with E2M1 A and B (format 5).  Both operands then sit in shared memory as 16-byte chunks
+// whose first 8 bytes hold 16 packed codes, K = 32 codes per instruction, so their descriptors are
+// those of an 8-bit operand.
+__host__ __device__ constexpr uint32_t idesc_e2m1_f32(int M, int N) {
+    return (1u << 4) | (5u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] x B[smem], 8-bit operands (K = 32 per instruction); issued by one thread.
 __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {

@@ -98,14 +98,17 @@ def test_idx_scores(sti, orc, b, s, Hi, Di, n_cols, sps, ratio):
 
 @pytest.mark.parametrize("b,s,Hi,Di,n_cols,sps", [
     (3, 1, 32, 128, 1500, [6000, 399, 5999]),     # decode: one query per unit, ragged visibility
+    (2, 1, 16, 128, 900, [3599, 1000]),           # decode, N = 16: E2M1 operands
+    (1, 1, 4, 128, 130, [519]),                   # 4 heads padded to N = 16; a 2-key last tile
     (1, 40, 32, 128, 300, [0]),                   # prefill: 8 queries per unit
     (2, 3, 8, 64, 700, [2799, 100]),
     (1, 70, 4, 64, 200, [0]),                     # 64 queries per unit, several units
 ])
 def test_idx_scores_mxfp4(sti, orc, b, s, Hi, Di, n_cols, sps):
-    """MXFP4 keys decoded in shared memory (E5M2 with Di == 128, else bf16) and queries quantised
-    in the kernel equal the oracle's scores over the decoded values (OCP MXFP4 reading of
-    fp4_act_quant)."""
+    """MXFP4 keys and queries quantised in the kernel give the oracle's scores over the decoded
+    values (OCP MXFP4 reading of fp4_act_quant): one query per unit with Di == 128 runs the codes as
+    E2M1 MMA operands with the scales applied per block; otherwise the keys are decoded in shared
+    memory (E5M2 with Di == 128, else bf16)."""
     import torch
 
     rng = rng_for(790 + Di, n_cols)
@@ -124,17 +127,19 @@ def test_idx_scores_mxfp4(sti, orc, b, s, Hi, Di, n_cols, sps):
     check_scores(got, ref)
 
 
+@pytest.mark.parametrize("s", [1, 3])
 @pytest.mark.parametrize("case", ["key_outliers", "query_outliers", "zero_blocks"])
-def test_idx_scores_mxfp4_scale_ranges(sti, orc, case):
-    """With Di == 128 a key tile runs as E5M2 only when every scale block of its visible keys, and
-    of the unit's queries, has X in [-13, 13]; other tiles (here: tiles with far-out key scales, or
-    a unit whose query block is 2^20 or 2^-30 times larger or smaller) are decoded to bf16.  Both
-    give the oracle's scores, in the same launch."""
+def test_idx_scores_mxfp4_scale_ranges(sti, orc, case, s):
+    """Far-out block scales.  One query per unit (s = 1): the E2M1 operands take any scale, applied
+    per block in fp32.  Several queries per unit (s = 3): a key tile runs as E5M2 only when every
+    scale block of its visible keys, and of the unit's queries, has X in [-13, 13]; other tiles
+    (here: tiles with far-out key scales, or a unit whose query block is 2^20 or 2^-30 times larger
+    or smaller) are decoded to bf16, in the same launch.  All give the oracle's scores."""
     b, Hi, Di, n_cols = 4, 32, 128, 1500
     sps = [5999, 3000, 5999, 1200]
     rng = rng_for(795, len(case))
-    sp = np.asarray(sps, np.int32)
-    q = rng.standard_normal((b, 1, Hi, Di))
+    sp = np.asarray(sps, np.int32) - (s - 1)
+    q = rng.standard_normal((b, s, Hi, Di))
     cap = (n_cols + 7) // 8 * 8
     codes = rng.integers(0, 256, size=(b, cap, Di // 2), dtype=np.uint8)
     scales = rng.integers(118, 132, size=(b, cap, Di // 32), dtype=np.uint8)
@@ -151,7 +156,7 @@ def test_idx_scores_mxfp4_scale_ranges(sti, orc, case):
         scales[0, 256:384] = 0
         q[3, 0, 5, :32] = 0.0              # an all-zero query block
     iq = to_bf16_bits(q)
-    w = to_bf16_bits(rng.standard_normal((b, 1, Hi)))
+    w = to_bf16_bits(rng.standard_normal((b, s, Hi)))
     c = Di ** -0.5 * Hi ** -0.5
     ref = orc.index_score_mxfp4(iq, codes, scales, w, c, sp, n_cols, 4)
     ws = sti.workspace(256)
