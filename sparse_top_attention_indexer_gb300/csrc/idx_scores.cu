@@ -15,11 +15,16 @@
 //   warp 1      TMEM allocator + single-thread MMA issuer
 //   warps 2..9  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced); two
 //               warps per TMEM lane quarter, taking alternate query chunks of a unit (one query per
-//               unit, as in decode, and MXFP4: warps 2..5, one per quarter)
-// With MXFP4 keys (Indexer.forward's fp4 keys and queries) warp 0 stages packed tiles (E2M1
-// codes + E8M0 scales) by bulk copy and warps 6..13 decode them in shared memory -- to E5M2 for
-// kind::f8f6f4 MMAs where every block's scale allows an exact E5M2 value, else to bf16 -- after
-// quantising each unit's queries in place.
+//               unit, as in decode, and MXFP4 decoded in shared memory: warps 2..5, one per quarter;
+//               MXFP4 as E2M1 operands: the two warps of a quarter take half of the heads each)
+// With MXFP4 keys (Indexer.forward's fp4 keys and queries) and one query per unit (decode, Di ==
+// 128), warp 0 loads each tile's codes by TMA straight into the layout kind::f8f6f4 reads as E2M1
+// operands (16 codes in the first 8 bytes of each 16-byte chunk) plus its scale bytes; the epilogue
+// warps quantise the unit's queries into the same layout, every 32-code scale block has its own
+// accumulator and the epilogue applies both blocks' 2^X.  Otherwise warp 0 stages packed tiles
+// (E2M1 codes + E8M0 scales) by bulk copy and warps 6..13 decode them in shared memory -- to E5M2
+// for kind::f8f6f4 MMAs where every block's scale allows an exact E5M2 value, else to bf16 --
+// after quantising each unit's queries in place.
 // Work = the flattened list of (unit, key tile) pairs over all units (unit = one sequence and
 // nq consecutive queries), cut into equal contiguous ranges, one per CTA.  Key tiles past the
 // last visible position of a unit are not computed; the epilogue writes -inf there.
@@ -48,6 +53,7 @@ struct __align__(8) Barriers {
     uint64_t b_ready;               // MXFP4: the unit's queries quantised in place
     uint64_t full_b, empty_b;
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t part_full[2];          // E2M1 operands: the second warp of each lane quarter's partial scores
     uint64_t mma_done;
     uint32_t fmt[kMaxStages];       // MXFP4: 1 when the stage holds E5M2 keys, 0 for bf16
     uint32_t tmem_base;
@@ -305,7 +311,7 @@ __device__ __forceinline__ uint32_t mxfp4_quant_e2m1(const uint4 v, int& X) {
 }
 
 template <int HI, int KM>
-__global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOneQ : kThreads), KM == 0 ? 1 : 2)
+__global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : kThreads, KM == 0 ? 1 : 2)
     idx_scores_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_s, const IdxScoresParams p) {
     constexpr bool FP4 = KM == 1;
@@ -338,16 +344,20 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOne
     int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq], nq <= 64
     float* sq_s = reinterpret_cast<float*>(vis_s + 64); // E2M1 operands: 2^X of query block j, head h at [32 j + h]
     uint32_t* hs = reinterpret_cast<uint32_t*>(sq_s + 128);   // E2M1 operands: the unit's first-pass histogram
+    float* pbuf = reinterpret_cast<float*>(hs + 2048);          // E2M1 operands: [2][128] partial scores
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&bars->full_a[i], FP4 ? kDqWarps / 2 : 1);   // MXFP4: the decoding group's warps
-            // E2M1 operands: the MMAs' commit and the four epilogue warps, which read the stage's scales
-            mbar_init(&bars->empty_a[i], E2 ? 5 : 1);
+            // E2M1 operands: the MMAs' commit and the eight epilogue warps, which read the stage's scales
+            mbar_init(&bars->empty_a[i], E2 ? 9 : 1);
         }
-        if (E2) mbar_init(&bars->b_ready, 1);
+        if (E2) {
+            mbar_init(&bars->b_ready, 1);
+            for (int i = 0; i < 2; ++i) mbar_init(&bars->part_full[i], 4);
+        }
         if (FP4) {
             for (int i = 0; i < p.c_stages; ++i) {
                 mbar_init(&bars->full_c[i], 1);
@@ -701,7 +711,7 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOne
         // ---------------------------------------------------------------- epilogue
         // bf16 keys with several queries per unit: two warps per TMEM lane quarter, each taking every
         // other query chunk of a unit
-        const int EPI = (FP4 || E2) ? 4 : ((int)blockDim.x - 64) / 32;   // epilogue warps (4 or 8)
+        const int EPI = FP4 ? 4 : ((int)blockDim.x - 64) / 32;   // epilogue warps (4 or 8)
         const int NG = EPI / 4;                                  // warps per lane quarter
         const int ep_tid = threadIdx.x - 64;           // 0 .. 32 EPI - 1
         const int eg = (warp - 2) >> 2;                // this warp's group: query chunks eg, eg + NG, ...
@@ -734,44 +744,53 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOne
             const int b = u / p.QT, qt = u - (u / p.QT) * p.QT;
             const int t0 = qt * p.nq;
             const int nq_here = min(p.nq, p.s - t0);
-            if (u != cur_unit) {
+            if (u != cur_unit && E2) {
+                // one query per unit.  First the unit's queries, quantised to MXFP4 into the E2M1 operand
+                // (codes of a 32-element block in two 16-code chunks) and the block scales 2^X, so the
+                // MMAs of the unit can start; then the previous unit's histogram and this unit's weights.
+                // Every tile of the previous unit has been scored, so its MMAs are done.
                 named_bar_sync(1, 32 * EPI);
-                if (E2 && p.hist != nullptr && cur_unit >= 0) flush_hist(cur_unit);
+                const bool has_w = ep_tid < HI;   // the unit's weights and start position, read early
+                const uint16_t wb = has_w ? p.w[((size_t)b * p.s + t0) * HI + ep_tid] : (uint16_t)0;
+                const int spv = ep_tid == 0 ? __ldg(p.start_pos + b) : 0;
+                bool okb = !aborted() && mbar_wait(&bars->full_b, qb_phase, p.status);
+                okb = __all_sync(kFull, okb);   // warp-uniform: the quantiser shuffles within the warp
+                if (okb) {
+                    // n_pad * 16 is a multiple of 32 * EPI: a warp's lanes run the same trips
+                    for (int i = ep_tid; i < p.n_pad * 16; i += 32 * EPI) {
+                        const int r = i >> 4, j = (i >> 2) & 3, t4 = i & 3;
+                        const uint8_t* rowp = b_buf + (size_t)(j >> 1) * p.n_pad * 128 + (size_t)r * 128;
+                        const int c = (j & 1) * 4 + t4;
+                        int X;
+                        const uint32_t nib = mxfp4_quant_e2m1(*reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4)), X);
+                        const int grp = 2 * j + (t4 >> 1);
+                        uint8_t* dst = b8 + (size_t)r * 128 + ((grp ^ (r & 7)) << 4) + (t4 & 1) * 4;
+                        // the chunk's second half is never read as codes; it gets the same bytes
+                        *reinterpret_cast<uint32_t*>(dst) = nib;
+                        *reinterpret_cast<uint32_t*>(dst + 8) = nib;
+                        if (t4 == 0) sq_s[j * 32 + r] = exp2i(X);
+                    }
+                } else {
+                    atomicExch(&bars->abort, 1u);
+                }
+                fence_proxy_async_smem();   // generic stores, read by the tensor core
+                qb_phase ^= 1u;
+                named_bar_sync(1, 32 * EPI);
+                if (ep_tid == 0 && !aborted()) mbar_arrive(&bars->b_ready);
+                if (p.hist != nullptr && cur_unit >= 0) flush_hist(cur_unit);
+                if (has_w) w_s[ep_tid] = __uint_as_float((uint32_t)wb << 16) * p.c;
+                if (ep_tid == 0) vis_s[0] = max(0, min(p.n_cols, (spv + t0 + 1) / p.ratio));
+                named_bar_sync(1, 32 * EPI);
+                cur_unit = u;
+            } else if (u != cur_unit) {
+                named_bar_sync(1, 32 * EPI);
                 for (int i = ep_tid; i < nq_here * HI; i += 32 * EPI) {
                     const uint16_t wb = p.w[((size_t)b * p.s + t0) * HI + i];
                     w_s[i] = __uint_as_float((uint32_t)wb << 16) * p.c;
                 }
                 for (int i = ep_tid; i < nq_here; i += 32 * EPI)
                     vis_s[i] = max(0, min(p.n_cols, (__ldg(p.start_pos + b) + t0 + i + 1) / p.ratio));
-                if (E2) {
-                    // the unit's queries (one per unit, n_pad <= 32 rows) quantised to MXFP4 into the
-                    // E2M1 operand (codes of a 32-element block in two 16-code chunks) and the block
-                    // scales 2^X; every tile of the previous unit has been scored, so its MMAs are done
-                    bool okb = !aborted() && mbar_wait(&bars->full_b, qb_phase, p.status);
-                    okb = __all_sync(kFull, okb);   // warp-uniform: the quantiser shuffles within the warp
-                    if (okb) {
-                        // n_pad * 16 is a multiple of 128: a warp's lanes run the same trips
-                        for (int i = ep_tid; i < p.n_pad * 16; i += 32 * EPI) {
-                            const int r = i >> 4, j = (i >> 2) & 3, t4 = i & 3;
-                            const uint8_t* rowp = b_buf + (size_t)(j >> 1) * p.n_pad * 128 + (size_t)r * 128;
-                            const int c = (j & 1) * 4 + t4;
-                            int X;
-                            const uint32_t nib = mxfp4_quant_e2m1(*reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4)), X);
-                            const int grp = 2 * j + (t4 >> 1);
-                            uint8_t* dst = b8 + (size_t)r * 128 + ((grp ^ (r & 7)) << 4) + (t4 & 1) * 4;
-                            // the chunk's second half is never read as codes; it gets the same bytes
-                            *reinterpret_cast<uint32_t*>(dst) = nib;
-                            *reinterpret_cast<uint32_t*>(dst + 8) = nib;
-                            if (t4 == 0) sq_s[j * 32 + r] = exp2i(X);
-                        }
-                    } else {
-                        atomicExch(&bars->abort, 1u);
-                    }
-                    fence_proxy_async_smem();   // generic stores, read by the tensor core
-                    qb_phase ^= 1u;
-                }
                 named_bar_sync(1, 32 * EPI);
-                if (E2 && ep_tid == 0 && !aborted()) mbar_arrive(&bars->b_ready);
                 cur_unit = u;
             }
             bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
@@ -783,46 +802,62 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOne
             tc_fence_after();
             const int key = tile * kTileKeys + quarter * 32 + lane;
             const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * (E2 ? 4 : 1) * p.n_alloc);
-            if (ok) {
+            if (E2) {
+                // one query: y_h = sum over the four 32-code blocks of acc_hj * 2^(Xq_hj + Xk_j) (products
+                // of E2M1 values are exact, so is each block's fp32 sum), score = sum_h w_h relu(y_h).  The
+                // two warps of a lane quarter take half of the heads each (pairs in packed fp32x2 math);
+                // the second hands its partial sum to the first through shared memory.
+                constexpr int HH = (HI <= 32 ? HI : 32) / 2;   // heads per warp
+                float part = 0.f;
+                if (ok) {
+                    const int h0 = eg * HH;
+                    const uint32_t skw = *reinterpret_cast<const uint32_t*>(
+                        c_ring + (size_t)st_e * c_bytes + (size_t)(quarter * 32 + lane) * 4);
+                    float2 y[HH / 2];
+#pragma unroll
+                    for (int h = 0; h < HH / 2; ++h) y[h] = make_float2(0.f, 0.f);
+                    uint32_t r[4][16];   // the four blocks' loads in flight together, one wait
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) tmem_ld16(col_base + (uint32_t)(kb * p.n_alloc + h0), r[kb]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+                        const float sk = e8m0_value((skw >> (8 * kb)) & 0xFFu);
+                        const float2 sk2 = make_float2(sk, sk);
+#pragma unroll
+                        for (int h = 0; h < HH / 2; ++h) {
+                            const float2 f = __fmul2_rn(*reinterpret_cast<const float2*>(sq_s + kb * 32 + h0 + 2 * h), sk2);
+                            y[h] = __ffma2_rn(make_float2(__uint_as_float(r[kb][2 * h]), __uint_as_float(r[kb][2 * h + 1])),
+                                              f, y[h]);
+                        }
+                    }
+                    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int h = 0; h < HH / 2; ++h)
+                        s2 = __ffma2_rn(*reinterpret_cast<const float2*>(w_s + h0 + 2 * h),
+                                        make_float2(fmaxf(y[h].x, 0.f), fmaxf(y[h].y, 0.f)), s2);
+                    part = s2.x + s2.y;
+                }
+                float* pb = pbuf + acc * kTileKeys + quarter * 32 + lane;
+                if (eg == 1) {
+                    *pb = part;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->part_full[acc]);
+                } else if (ok) {
+                    bool okp = mbar_wait(&bars->part_full[acc], acc_phase, p.status);
+                    okp = __all_sync(kFull, okp);
+                    if (!okp) atomicExch(&bars->abort, 1u);
+                    const float sc = part + *pb;
+                    const bool in_row = key < p.n_cols;
+                    const bool visible = in_row && key < vis_s[0];
+                    if (in_row) p.scores[((size_t)b * p.s + t0) * p.n_cols + key] = visible ? sc : -INFINITY;
+                    if (p.hist != nullptr && visible) atomicAdd(&hs[float_key(sc) >> 21], 1u);
+                }
+            } else if (ok) {
                 for (int q0 = eg * QPC; q0 < nq_here; q0 += QPC * NG) {
                     float sacc[QPC];
 #pragma unroll
                     for (int i = 0; i < QPC; ++i) sacc[i] = 0.f;
-                    if constexpr (E2) {
-                        // one query: y_h = sum over the four 32-code blocks of acc_hj * 2^(Xq_hj + Xk_j)
-                        // (products of E2M1 values are exact, so is each block's fp32 sum), then
-                        // sum_h w_h relu(y_h)
-                        constexpr int HE = HI <= 32 ? HI : 32;
-                        const uint32_t skw = *reinterpret_cast<const uint32_t*>(
-                            c_ring + (size_t)st_e * c_bytes + (size_t)(quarter * 32 + lane) * 4);
-                        // (pairs of heads in packed fp32x2 multiplies and FMAs)
-                        float2 y[HE / 2];
-#pragma unroll
-                        for (int h = 0; h < HE / 2; ++h) y[h] = make_float2(0.f, 0.f);
-                        {   // the four blocks' loads in flight together, one wait
-                            uint32_t r[4][32];
-#pragma unroll
-                            for (int kb = 0; kb < 4; ++kb) tmem_ld32(col_base + (uint32_t)(kb * p.n_alloc), r[kb]);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int kb = 0; kb < 4; ++kb) {
-                                const float sk = e8m0_value((skw >> (8 * kb)) & 0xFFu);
-                                const float2 sk2 = make_float2(sk, sk);
-#pragma unroll
-                                for (int h = 0; h < HE / 2; ++h) {
-                                    const float2 f = __fmul2_rn(*reinterpret_cast<const float2*>(sq_s + kb * 32 + 2 * h), sk2);
-                                    y[h] = __ffma2_rn(make_float2(__uint_as_float(r[kb][2 * h]), __uint_as_float(r[kb][2 * h + 1])),
-                                                      f, y[h]);
-                                }
-                            }
-                        }
-                        float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int h = 0; h < HE / 2; ++h)
-                            s2 = __ffma2_rn(*reinterpret_cast<const float2*>(w_s + 2 * h),
-                                            make_float2(fmaxf(y[h].x, 0.f), fmaxf(y[h].y, 0.f)), s2);
-                        sacc[0] = s2.x + s2.y;
-                    } else {
 #pragma unroll
                     for (int cq = 0; cq < CPQ; ++cq) {
                         uint32_t r[32];
@@ -836,16 +871,13 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : (KM == 2 ? kThreadsOne
                             sacc[qq] = fmaf(w_s[(q0 + qq) * HI + hh], v, sacc[qq]);
                         }
                     }
-                    }
 #pragma unroll
                     for (int qq = 0; qq < QPC; ++qq) {
                         const int q = q0 + qq;
                         const bool in_row = q < nq_here && key < p.n_cols;
                         const bool visible = in_row && key < vis_s[q];
                         if (in_row) p.scores[((size_t)b * p.s + t0 + q) * p.n_cols + key] = visible ? sacc[qq] : -INFINITY;
-                        if (E2 && p.hist != nullptr) {
-                            if (visible) atomicAdd(&hs[float_key(sacc[qq]) >> 21], 1u);
-                        } else if (p.hist != nullptr) {
+                        if (p.hist != nullptr) {
                             // first radix pass of the top-k: top 11 bits of the order-preserving key,
                             // one aggregated shared-L2 atomic per distinct bin in the warp
                             const uint32_t dig = visible ? (float_key(sacc[qq]) >> 21) : 0xFFFFFFFFu;
@@ -916,7 +948,7 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
     if (p.fp4 == 2) {   // E2M1 operands: padded code tiles + scale bytes per stage, E2M1 queries, 2^X table,
                         // histogram
         return 1024 + (size_t)p.stages * (kTileKeys * 128 + kTileKeys * 4) + b_bytes + (size_t)p.n_pad * 128 +
-               sizeof(Barriers) + 256 * 4 + 64 * 4 + 128 * 4 + 2048 * 4;
+               sizeof(Barriers) + 256 * 4 + 64 * 4 + 128 * 4 + 2048 * 4 + 256 * 4;
     }
     const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
@@ -940,7 +972,7 @@ cudaError_t launch_idx_scores(const CUtensorMap& tm_a, const CUtensorMap& tm_b, 
                                : (p.fp4 ? idx_scores_kernel<HV, 1> : idx_scores_kernel<HV, 0>);        \
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);      \
         if (err != cudaSuccess) return err;                                                            \
-        const int threads = p.fp4 == 2 ? kThreadsOneQ                                                 \
+        const int threads = p.fp4 == 2 ? kThreads                                                     \
                                        : (p.fp4 ? kThreadsFp4 : (p.nq > 1 ? kThreads : kThreadsOneQ)); \
         kern<<<grid, threads, smem, stream>>>(tm_a, tm_b, tm_s, p);                                    \
         return cudaGetLastError();                                                                     \
