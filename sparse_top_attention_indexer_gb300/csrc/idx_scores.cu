@@ -38,7 +38,8 @@ namespace sti {
 namespace {
 
 constexpr int kTileKeys = 128;
-constexpr int kThreads = 320;      // bf16 keys: producer, MMA, 8 epilogue warps (two per TMEM lane quarter)
+constexpr int kThreads = 320;      // producer, MMA, 8 epilogue warps (two per TMEM lane quarter): bf16 keys with
+                                   // several queries per unit, and MXFP4 keys as E2M1 operands
 constexpr int kThreadsOneQ = 192;  // bf16 keys, one query per unit (decode): 4 epilogue warps
 constexpr int kThreadsFp4 = 448;   // MXFP4 keys: + 8 warps that dequantise keys and quantise queries
 constexpr int kDqWarps = 8;
