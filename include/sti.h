@@ -139,6 +139,10 @@ sti_status sti_idx_scores(const uint16_t *iq, const uint16_t *ik, int64_t ik_bst
  *       saturating at 6), times 2^X.
  * The score is the einsum/relu/weighted sum above over the decoded values (exact in bf16), with
  * fp32 accumulation.  Keys move as 68 bytes per position at Di = 128 instead of 256.
+ * With seqlen == 1, Di == 128, Hi <= 32, ik_codes 32-byte aligned and ik_codes_bstride a multiple
+ * of 32, the codes go to the tensor core as they are (E2M1 operands, the scales applied per
+ * 32-element block in fp32); other calls decode them in shared memory first.  Both give the
+ * scores above up to fp32 rounding order.
  * Supported: Di in {64, 128}; ik_codes, ik_scales 16-byte aligned; bstrides multiples of 16
  * covering n_cols keys.  Everything else as sti_idx_scores.
  */
