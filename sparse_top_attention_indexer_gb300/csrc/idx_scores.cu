@@ -16,7 +16,7 @@
 //   warps 2..9  epilogue: TMEM -> registers -> sum_h w*relu(acc) -> fp32 scores (coalesced); two
 //               warps per TMEM lane quarter, taking alternate query chunks of a unit (one query per
 //               unit, as in decode, and MXFP4 decoded in shared memory: warps 2..5, one per quarter;
-//               MXFP4 as E2M1 operands: the two warps of a quarter take half of the heads each)
+//               MXFP4 as E2M1 operands: two groups of four take the CTA's tiles in turn)
 // With MXFP4 keys (Indexer.forward's fp4 keys and queries) and one query per unit (decode, Di ==
 // 128), warp 0 loads each tile's codes by TMA straight into the layout kind::f8f6f4 reads as E2M1
 // operands (16 codes in the first 8 bytes of each 16-byte chunk) plus its scale bytes; the epilogue
@@ -54,7 +54,6 @@ struct __align__(8) Barriers {
     uint64_t b_ready;               // MXFP4: the unit's queries quantised in place
     uint64_t full_b, empty_b;
     uint64_t acc_full[2], acc_empty[2];
-    uint64_t part_full[2];          // E2M1 operands: the second warp of each lane quarter's partial scores
     uint64_t mma_done;
     uint32_t fmt[kMaxStages];       // MXFP4: 1 when the stage holds E5M2 keys, 0 for bf16
     uint32_t tmem_base;
@@ -345,20 +344,17 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : kThreads, KM == 0 ? 1 
     int* vis_s = reinterpret_cast<int*>(w_s + 256);     // [nq], nq <= 64
     float* sq_s = reinterpret_cast<float*>(vis_s + 64); // E2M1 operands: 2^X of query block j, head h at [32 j + h]
     uint32_t* hs = reinterpret_cast<uint32_t*>(sq_s + 128);   // E2M1 operands: the unit's first-pass histogram
-    float* pbuf = reinterpret_cast<float*>(hs + 2048);          // E2M1 operands: [2][128] partial scores
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(&bars->full_a[i], FP4 ? kDqWarps / 2 : 1);   // MXFP4: the decoding group's warps
-            // E2M1 operands: the MMAs' commit and the eight epilogue warps, which read the stage's scales
-            mbar_init(&bars->empty_a[i], E2 ? 9 : 1);
+            // E2M1 operands: the MMAs' commit and the four epilogue warps of the tile's group, which
+            // read the stage's scales
+            mbar_init(&bars->empty_a[i], E2 ? 5 : 1);
         }
-        if (E2) {
-            mbar_init(&bars->b_ready, 1);
-            for (int i = 0; i < 2; ++i) mbar_init(&bars->part_full[i], 4);
-        }
+        if (E2) mbar_init(&bars->b_ready, 1);
         if (FP4) {
             for (int i = 0; i < p.c_stages; ++i) {
                 mbar_init(&bars->full_c[i], 1);
@@ -370,7 +366,8 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : kThreads, KM == 0 ? 1 
         mbar_init(&bars->empty_b, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->acc_full[i], 1);
-            mbar_init(&bars->acc_empty[i], FP4 ? 4u : (blockDim.x - 64u) / 32u);   // one arrival per epilogue warp
+            // one arrival per epilogue warp (E2M1 operands: per warp of the group that owns the buffer)
+            mbar_init(&bars->acc_empty[i], (FP4 || E2) ? 4u : (blockDim.x - 64u) / 32u);
         }
         mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
@@ -794,67 +791,65 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : kThreads, KM == 0 ? 1 
                 named_bar_sync(1, 32 * EPI);
                 cur_unit = u;
             }
-            bool ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
-            // E2M1 operands: the stage's scale bytes landed with its codes (already complete)
-            if (E2) ok = ok && mbar_wait(&bars->full_a[st_e], st_phase, p.status);
-            ok = __all_sync(kFull, ok);   // warp-uniform: the loop below holds warp collectives
-            if (!ok) atomicExch(&bars->abort, 1u);
-            if (E2 && ep_tid == 0) STI_SCSTAMP(g - g0, 1);
-            tc_fence_after();
+            // E2M1 operands: the two warp groups take the CTA's tiles in turn, group eg the tiles of
+            // accumulator buffer eg; every warp walks every tile so unit changes stay in step
+            const bool mine = !E2 || ((g - g0) & 1) == eg;
+            bool ok = true;
+            if (mine) {
+                ok = !aborted() && mbar_wait(&bars->acc_full[acc], acc_phase, p.status);
+                // E2M1 operands: the stage's scale bytes landed with its codes (already complete)
+                if (E2) ok = ok && mbar_wait(&bars->full_a[st_e], st_phase, p.status);
+                ok = __all_sync(kFull, ok);   // warp-uniform: the loop below holds warp collectives
+                if (!ok) atomicExch(&bars->abort, 1u);
+                if (E2 && ep_tid == 0) STI_SCSTAMP(g - g0, 1);
+                tc_fence_after();
+            }
             const int key = tile * kTileKeys + quarter * 32 + lane;
             const uint32_t col_base = tmem + lane_base + (uint32_t)(acc * (E2 ? 4 : 1) * p.n_alloc);
-            if (E2) {
+            if (E2 && mine && ok) {
                 // one query: y_h = sum over the four 32-code blocks of acc_hj * 2^(Xq_hj + Xk_j) (products
-                // of E2M1 values are exact, so is each block's fp32 sum), score = sum_h w_h relu(y_h).  The
-                // two warps of a lane quarter take half of the heads each (pairs in packed fp32x2 math);
-                // the second hands its partial sum to the first through shared memory.
-                constexpr int HH = (HI <= 32 ? HI : 32) / 2;   // heads per warp
-                float part = 0.f;
-                if (ok) {
-                    const int h0 = eg * HH;
-                    const uint32_t skw = *reinterpret_cast<const uint32_t*>(
-                        c_ring + (size_t)st_e * c_bytes + (size_t)(quarter * 32 + lane) * 4);
-                    float2 y[HH / 2];
+                // of E2M1 values are exact, so is each block's fp32 sum), score = sum_h w_h relu(y_h);
+                // heads in pairs (packed fp32x2 math), 16 columns of two blocks per TMEM wait
+                constexpr int HE = HI <= 32 ? HI : 32;
+                const uint32_t skw = *reinterpret_cast<const uint32_t*>(
+                    c_ring + (size_t)st_e * c_bytes + (size_t)(quarter * 32 + lane) * 4);
+                float2 y[HE / 2];
 #pragma unroll
-                    for (int h = 0; h < HH / 2; ++h) y[h] = make_float2(0.f, 0.f);
-                    uint32_t r[4][16];   // the four blocks' loads in flight together, one wait
+                for (int h = 0; h < HE / 2; ++h) y[h] = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) tmem_ld16(col_base + (uint32_t)(kb * p.n_alloc + h0), r[kb]);
-                    tmem_ld_wait();
+                for (int hg = 0; hg < (HE + 15) / 16; ++hg) {
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
-                        const float sk = e8m0_value((skw >> (8 * kb)) & 0xFFu);
-                        const float2 sk2 = make_float2(sk, sk);
+                    for (int k2 = 0; k2 < 4; k2 += 2) {
+                        uint32_t r[2][16];
+                        tmem_ld16(col_base + (uint32_t)(k2 * p.n_alloc + hg * 16), r[0]);
+                        tmem_ld16(col_base + (uint32_t)((k2 + 1) * p.n_alloc + hg * 16), r[1]);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int h = 0; h < HH / 2; ++h) {
-                            const float2 f = __fmul2_rn(*reinterpret_cast<const float2*>(sq_s + kb * 32 + h0 + 2 * h), sk2);
-                            y[h] = __ffma2_rn(make_float2(__uint_as_float(r[kb][2 * h]), __uint_as_float(r[kb][2 * h + 1])),
-                                              f, y[h]);
+                        for (int i2 = 0; i2 < 2; ++i2) {
+                            const int kb = k2 + i2;
+                            const float sk = e8m0_value((skw >> (8 * kb)) & 0xFFu);
+                            const float2 sk2 = make_float2(sk, sk);
+#pragma unroll
+                            for (int h = 0; h < (HE < 16 ? HE : 16) / 2; ++h) {
+                                const int hh = hg * 8 + h;   // head pair
+                                const float2 f = __fmul2_rn(*reinterpret_cast<const float2*>(sq_s + kb * 32 + 2 * hh), sk2);
+                                y[hh] = __ffma2_rn(make_float2(__uint_as_float(r[i2][2 * h]), __uint_as_float(r[i2][2 * h + 1])),
+                                                   f, y[hh]);
+                            }
                         }
                     }
-                    float2 s2 = make_float2(0.f, 0.f);
+                }
+                float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int h = 0; h < HH / 2; ++h)
-                        s2 = __ffma2_rn(*reinterpret_cast<const float2*>(w_s + h0 + 2 * h),
-                                        make_float2(fmaxf(y[h].x, 0.f), fmaxf(y[h].y, 0.f)), s2);
-                    part = s2.x + s2.y;
-                }
-                float* pb = pbuf + acc * kTileKeys + quarter * 32 + lane;
-                if (eg == 1) {
-                    *pb = part;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->part_full[acc]);
-                } else if (ok) {
-                    bool okp = mbar_wait(&bars->part_full[acc], acc_phase, p.status);
-                    okp = __all_sync(kFull, okp);
-                    if (!okp) atomicExch(&bars->abort, 1u);
-                    const float sc = part + *pb;
-                    const bool in_row = key < p.n_cols;
-                    const bool visible = in_row && key < vis_s[0];
-                    if (in_row) p.scores[((size_t)b * p.s + t0) * p.n_cols + key] = visible ? sc : -INFINITY;
-                    if (p.hist != nullptr && visible) atomicAdd(&hs[float_key(sc) >> 21], 1u);
-                }
-            } else if (ok) {
+                for (int h = 0; h < HE / 2; ++h)
+                    s2 = __ffma2_rn(*reinterpret_cast<const float2*>(w_s + 2 * h),
+                                    make_float2(fmaxf(y[h].x, 0.f), fmaxf(y[h].y, 0.f)), s2);
+                const float sc = s2.x + s2.y;
+                const bool in_row = key < p.n_cols;
+                const bool visible = in_row && key < vis_s[0];
+                if (in_row) p.scores[((size_t)b * p.s + t0) * p.n_cols + key] = visible ? sc : -INFINITY;
+                if (p.hist != nullptr && visible) atomicAdd(&hs[float_key(sc) >> 21], 1u);
+            } else if (!E2 && ok) {
                 for (int q0 = eg * QPC; q0 < nq_here; q0 += QPC * NG) {
                     float sacc[QPC];
 #pragma unroll
@@ -889,11 +884,13 @@ __global__ void __launch_bounds__(KM == 1 ? kThreadsFp4 : kThreads, KM == 0 ? 1 
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+            if (mine) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+                if (E2 && lane == 0) mbar_arrive(&bars->empty_a[st_e]);
+            }
             if (E2) {
-                if (lane == 0) mbar_arrive(&bars->empty_a[st_e]);
                 if (++st_e == p.stages) {
                     st_e = 0;
                     st_phase ^= 1u;
@@ -949,7 +946,7 @@ size_t idx_scores_smem_bytes(const IdxScoresParams& p) {
     if (p.fp4 == 2) {   // E2M1 operands: padded code tiles + scale bytes per stage, E2M1 queries, 2^X table,
                         // histogram
         return 1024 + (size_t)p.stages * (kTileKeys * 128 + kTileKeys * 4) + b_bytes + (size_t)p.n_pad * 128 +
-               sizeof(Barriers) + 256 * 4 + 64 * 4 + 128 * 4 + 2048 * 4 + 256 * 4;
+               sizeof(Barriers) + 256 * 4 + 64 * 4 + 128 * 4 + 2048 * 4;
     }
     const size_t a_bytes = (size_t)kTileKeys * p.Di * 2;
     const size_t c_bytes = p.fp4 ? (size_t)kTileKeys * p.Di / 2 + (size_t)kTileKeys * p.Di / 32 : 0;
