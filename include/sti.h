@@ -142,7 +142,8 @@ sti_status sti_idx_scores(const uint16_t *iq, const uint16_t *ik, int64_t ik_bst
  * With seqlen == 1, Di == 128, Hi <= 32, ik_codes 32-byte aligned and ik_codes_bstride a multiple
  * of 32, the codes go to the tensor core as they are (E2M1 operands, the scales applied per
  * 32-element block in fp32); other calls decode them in shared memory first.  Both give the
- * scores above up to fp32 rounding order.
+ * scores above up to fp32 rounding order, for scales whose values fit fp32 (a block whose
+ * products exceed fp32's range gives a non-finite score).
  * Supported: Di in {64, 128}; ik_codes, ik_scales 16-byte aligned; bstrides multiples of 16
  * covering n_cols keys.  Everything else as sti_idx_scores.
  */

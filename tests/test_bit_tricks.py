@@ -128,3 +128,53 @@ def test_fp4_kv_decode_values():
             v = np.float32((-1.0 if nib & 8 else 1.0) * mags[nib & 7]) * np.float32(s)
             bits = int(np.array([v], dtype=np.float32).view(np.uint32)[0]) >> 16
             assert _bf16_value(bits) == float(v), (hex(sb), nib)   # exact in bf16
+
+
+def test_e2m1_block_sums_are_exact_in_fp32():
+    """The E2M1-operand scores kernel keeps one fp32 accumulator per 32-code scale block: every
+    product of two E2M1 values is a multiple of 1/4 below 36 in magnitude, so a block's sum
+    (at most 1152) is exact in fp32 whatever order the tensor core adds in."""
+    mags = np.asarray(oracle.E2M1_MAGNITUDES)
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([-mags[::-1], mags])          # every E2M1 value, both zeros
+    worst = np.full(32, 6.0)                            # the extreme block: 32 x 6 x 6
+    for trial in range(2000):
+        a = rng.choice(vals, 32) if trial else worst
+        b = rng.choice(vals, 32) if trial else worst
+        exact = float(np.dot(a.astype(np.float64), b.astype(np.float64)))
+        p = (a * b).astype(np.float32)
+        for order in (np.arange(32), np.arange(32)[::-1], rng.permutation(32)):
+            acc = np.float32(0.0)
+            for i in order:
+                acc = np.float32(acc + p[i])
+            assert float(acc) == exact
+        pair = p.copy()                                  # pairwise tree
+        while len(pair) > 1:
+            pair = (pair[0::2] + pair[1::2]).astype(np.float32)
+        assert float(pair[0]) == exact
+
+
+def test_e2m1_block_scaling_matches_the_decoded_dot_product():
+    """The epilogue forms y = sum_j acc_j * (2^Xq_j * 2^Xk_j) over the four blocks with fp32
+    multiplies and FMAs; against the fp64 dot product of the decoded values it stays within a few
+    fp32 ulps of the terms, far inside the scores' 2e-3 relative tolerance, for scale exponents
+    whose scaled products fit fp32 (e = 0 is 2^-127, a subnormal in fp32; scale products below
+    2^-149 flush to zero, which costs at most 1152 * 2^-149 absolute)."""
+    mags = np.asarray(oracle.E2M1_MAGNITUDES)
+    vals = np.concatenate([-mags[::-1], mags])
+    rng = np.random.default_rng(12)
+    for trial in range(3000):
+        a = rng.choice(vals, 128)
+        b = rng.choice(vals, 128)
+        ek = rng.integers(0, 201, 4) if trial % 3 == 0 else rng.integers(110, 145, 4)
+        xq = rng.integers(-40, 27, 4)                                 # Xq + Xk <= 99
+        sk = np.array([2.0 ** -127 if e == 0 else 2.0 ** (int(e) - 127) for e in ek])
+        sq = 2.0 ** xq.astype(np.float64)
+        acc = np.array([np.dot(a[32 * j:32 * j + 32], b[32 * j:32 * j + 32]) for j in range(4)], np.float32)
+        y = np.float32(0.0)
+        for j in range(4):
+            f = np.float32(np.float32(sq[j]) * np.float32(sk[j]))      # exact: a power of two
+            y = np.float32(float(acc[j]) * float(f) + float(y))        # one rounding, as an FMA
+        ref = float(sum(float(acc[j]) * sq[j] * sk[j] for j in range(4)))
+        mag = float(sum(abs(float(acc[j])) * sq[j] * sk[j] for j in range(4)))
+        assert abs(float(y) - ref) <= 4 * 2.0 ** -24 * mag + 2.0 ** -137, (trial, float(y), ref)
