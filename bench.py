@@ -573,7 +573,8 @@ def workload_config(shape: workloads.Shape, args) -> dict:
                                 "bf16 in the attention kernel")
     if shape.fp4_keys:
         cfg["index_keys"] = ("MXFP4 (E2M1 codes, an E8M0 scale per 32); queries quantised to MXFP4 in the scores "
-                             "kernel; scores on E5M2 tensor cores (kind::f8f6f4) where the scales allow, else bf16")
+                             "kernel; decode units run the codes as E2M1 tensor-core operands (kind::f8f6f4, one "
+                             "fp32 accumulator per scale block, scales applied in the epilogue)")
     if shape.n_layers > 1:
         cfg["sequence_lengths"] = f"{int(shape.start_pos.min()) + 1}..{int(shape.start_pos.max()) + 1} (ragged)"
     return cfg
@@ -674,7 +675,7 @@ def bench_workload(n: int, args, device, primary: bool) -> dict:
            "launch": "CUDA graph of the decode step, replayed per step" if use_graph else "direct C-ABI calls",
            "device_status_flags": status}
     if primary:
-        rec["dtype"] = "e5m2+bf16" if shape.fp4_keys else "fp4kv+bf16" if shape.fp4_kv else "bf16"
+        rec["dtype"] = "e2m1+bf16" if shape.fp4_keys else "fp4kv+bf16" if shape.fp4_kv else "bf16"
         rec["config"] = workload_config(shape, args)
         if not args.no_e2e and shape.n_layers == 1 and not shape.prefill:
             rec["e2e"] = measure_e2e(path, data, args.steps, args.warmup)
